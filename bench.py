@@ -1,0 +1,484 @@
+"""Benchmark: one decode layer of an 8B-shaped model over a host/HBM tiered placement.
+
+Step = the whole direct-access hot path once: the four decode linears of an 8B-shaped
+layer (QKV 6144x4096, O 4096x4096, gate+up 28672x4096, down 4096x14336; bf16 weights)
+at batch N through dak_gemm, and decode GQA attention (32 requests, 32/8 heads, head dim
+128, context 8192, bf16 KV) through dak_attn, with a fraction x of every weight matrix's
+tile rows and of the requests' KV in pinned host memory (default x = 0.25, N = 32).
+
+Metric: effective bandwidth (bytes of weights + KV per step / step time) and decode
+tokens/s, against the tier-aggregate roofline R(x) = C / max(x C / B_host, (1-x) C / B_hbm)
+with B_host and B_hbm measured in the same run by read-stream kernels over each tier.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--x 0.25] [--batch 32]
+  python bench.py --impl reference ...   (the CPU oracle on a bounded sample of the step)
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "effective GB/s & decode tok/s vs tier-aggregate roofline, per offload ratio x"
+LAYERS_8B = 32
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="dak", choices=["dak", "reference"])
+    ap.add_argument("--x", type=float, default=0.25)
+    ap.add_argument("--batch", type=int, default=32)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------------------ workload
+
+def workload_bytes(batch):
+    import synth
+    w = sum(M * K * 2 for M, K in synth.LINEARS_8B.values())
+    c = synth.ATTN_DECODE
+    kv = 2 * c["batch"] * c["h_kv"] * c["context"] * c["head_dim"] * 2
+    return w, kv
+
+
+def gen_inputs(batch, seed=0):
+    import synth
+    lin = {}
+    for i, (name, (M, K)) in enumerate(synth.LINEARS_8B.items()):
+        lin[name] = synth.gemm_inputs(M, K, batch, seed=seed, tensor_index=i)
+    c = synth.ATTN_DECODE
+    attn = synth.attn_inputs(c["batch"], c["h_q"], c["h_kv"], c["head_dim"], c["context"], seed=seed,
+                             tensor_index=len(lin))
+    return lin, attn
+
+
+class Step:
+    """The placed workload at one offload ratio plus device buffers for one step."""
+
+    def __init__(self, dak, lin, attn, x, dev):
+        import torch
+        self.dak = dak
+        self.x = x
+        self.pl, self.B, self.C = {}, {}, {}
+        for name, (A, B) in lin.items():
+            M = A.shape[0]
+            self.pl[name] = dak.dak_place_matrix(A, dak.host_tiles_for_ratio(x, M))
+            self.B[name] = torch.from_numpy(B.view("int16")).view(torch.bfloat16).to(dev)
+            self.C[name] = torch.empty((B.shape[0], M), dtype=torch.bfloat16, device=dev)
+        q, k, v = attn
+        self.kv = dak.dak_place_kv(k, v, dak.host_requests_for_ratio(x, k.shape[0]))
+        self.Q = torch.from_numpy(q.view("int16")).view(torch.bfloat16).to(dev)
+        self.O = torch.empty_like(self.Q)
+        self.n_split = dak.dak_attn_default_split(self.kv)
+        ws = dak.dak_attn_workspace_bytes(q.shape[0], q.shape[1], q.shape[2], self.n_split)
+        self.ws = torch.empty(max(1, ws // 4), dtype=torch.float32, device=dev)
+        self.tun = dict(n_split=self.n_split)
+        self.host_bytes = sum(p.host_bytes for p in self.pl.values()) + self.kv.host_bytes
+        self.total_bytes = sum(p.host_bytes + p.hbm_bytes for p in self.pl.values()) + \
+            self.kv.host_bytes + self.kv.hbm_bytes
+        self.launches = len(self.pl) + (2 if self.n_split > 1 else 1)
+
+    def run(self, ev=None):
+        d = self.dak
+        for name, p in self.pl.items():
+            d.dak_gemm(p, self.B[name], self.C[name])
+        if ev is not None:
+            ev[0].record()
+        d.dak_attn(self.Q, self.kv, O=self.O, workspace=self.ws, tuning=self.tun)
+        if ev is not None:
+            ev[1].record()
+
+    # prefetch baseline: copy every host-resident part into HBM staging, then the all-HBM kernels
+    def alloc_staging(self, dev):
+        import torch
+        self.stage = {n: torch.empty(max(16, p.host_bytes), dtype=torch.uint8, device=dev) for n, p in self.pl.items()}
+        self.stage_kv = torch.empty(max(16, self.kv.host_bytes), dtype=torch.uint8, device=dev)
+
+    def run_prefetch_serial(self):
+        d = self.dak
+        for name, p in self.pl.items():
+            d.dak_prefetch(p, self.stage[name])
+        d.dak_prefetch(self.kv, self.stage_kv)
+        for name, p in self.pl.items():
+            d.dak_gemm_staged(p, self.stage[name], self.B[name], self.C[name])
+        d.dak_attn_staged(self.Q, self.kv, self.stage_kv, O=self.O, workspace=self.ws, tuning=self.tun)
+
+    def run_prefetch_overlap(self, copy_stream, events):
+        """FlexGen-style: copies of the host parts run on a side stream in op order and each
+        op waits only for its own copy (best case: staging for every op)."""
+        import torch
+        d = self.dak
+        cur = torch.cuda.current_stream()
+        copy_stream.wait_stream(cur)
+        names = list(self.pl)
+        with torch.cuda.stream(copy_stream):
+            for i, name in enumerate(names):
+                d.dak_prefetch(self.pl[name], self.stage[name], stream=copy_stream)
+                events[i].record(copy_stream)
+            d.dak_prefetch(self.kv, self.stage_kv, stream=copy_stream)
+            events[len(names)].record(copy_stream)
+        for i, name in enumerate(names):
+            cur.wait_event(events[i])
+            d.dak_gemm_staged(self.pl[name], self.stage[name], self.B[name], self.C[name])
+        cur.wait_event(events[len(names)])
+        d.dak_attn_staged(self.Q, self.kv, self.stage_kv, O=self.O, workspace=self.ws, tuning=self.tun)
+
+    def free(self):
+        for p in self.pl.values():
+            p.free()
+        self.kv.free()
+
+
+# ------------------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [s.strip() for s in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [r for t, r in self.rows if t0 <= t <= t1]
+        where = "timed region"
+        if not inside:
+            inside = [r for t, r in self.rows]
+            where = "around the timed region (region shorter than the sampling period)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm = [float(r[1]) for r in inside if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in inside if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in inside for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside), "sampled": where,
+                "power_w_max": max((float(r[3]) for r in inside if r[3].replace(".", "").isdigit()), default=None)}
+
+
+# ------------------------------------------------------------------------------ measurement
+
+def measure_tiers(dak):
+    """B_host and B_hbm: best read-stream bandwidth of each tier (GB/s), plus the
+    concurrent split at the kernels' default host CTA count."""
+    G = 1 << 30
+    best_h, best_g = 0.0, 0.0
+    for m, c, w in ((0, 16, 4), (0, 32, 4), (2, 16, 4)):
+        try:
+            g, ok = dak.dak_probe_read_bw(0, G, m, c, w, 32768, 3)
+            if ok:
+                best_h = max(best_h, g)
+        except dak.DakError:
+            pass
+    for c in (dak.dak_sm_count(), 100):
+        g, ok = dak.dak_probe_read_bw(1, 4 * G, 0, c, 4, 32768, 3)
+        if ok:
+            best_g = max(best_g, g)
+    hc = 16
+    ch, cg = dak.dak_probe_concurrent(G, 4 * G, hc, 4, dak.dak_sm_count() - hc, 4, 32768, 3)
+    return best_h * 1e9, best_g * 1e9, {"host_ctas": hc, "host_gbps": ch, "hbm_gbps": cg}
+
+
+def time_steps(fn, steps, warmup, sync_all=None):
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    if sync_all:
+        sync_all()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    if sync_all:
+        sync_all()
+    return e0.elapsed_time(e1) / 1e3 / steps
+
+
+def tier_roofline(C, x, bh, bg):
+    t = max(x * C / bh, (1 - x) * C / bg)
+    return C / t
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+# ------------------------------------------------------------------------------ CPU oracle
+
+def cpu_oracle_sample(lin, attn, frac_rows=1 / 32):
+    """Time the CPU oracle (as it stands) on a bounded sample of one step: every 32nd tile
+    row of each linear and one request in 32 of the attention. Returns (GB/s, sample, s)."""
+    import numpy as np
+    from oracle import attention as oa
+    from oracle import gemm as og
+    t0 = time.perf_counter()
+    nbytes = 0
+    for A, B in lin.values():
+        rows = np.concatenate([np.arange(t * 64, t * 64 + 64) for t in range(0, A.shape[0] // 64, int(1 / frac_rows))])
+        og.gemm_ref(A[rows], B)
+        nbytes += rows.size * A.shape[1] * 2
+    q, k, v = attn
+    nreq = max(1, int(q.shape[0] * frac_rows))
+    oa.decode_attention_ref(q[:nreq], k[:nreq], v[:nreq])
+    nbytes += 2 * k[:nreq].size * 2
+    dt = time.perf_counter() - t0
+    return nbytes / dt / 1e9, f"1/{int(1 / frac_rows)} of the step: every {int(1 / frac_rows)}th 64-row tile of each " \
+                              f"linear and {nreq} of {q.shape[0]} attention requests ({nbytes / 1e6:.0f} MB)", dt
+
+
+def cpu_threads():
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        if info:
+            return max(i.get("num_threads", 1) for i in info)
+    except Exception:
+        pass
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------------------ main
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w_bytes, kv_bytes = workload_bytes(args.batch)
+    lin, attn = gen_inputs(args.batch)
+    for _ in range(args.warmup):
+        cpu_oracle_sample(lin, attn)
+    vals, dts = [], []
+    for _ in range(args.steps):
+        gbps, sample, dt = cpu_oracle_sample(lin, attn)
+        vals.append(gbps)
+        dts.append(dt)
+    v = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(dts),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"8B-shaped decode layer, batch {args.batch}: QKV/O/gate+up/down linears + GQA "
+                               f"attention 32x(32/8 heads, D 128, ctx 8192); bounded sample per step",
+                   "x": args.x, "l2": "inputs larger than L2"},
+        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cpu_threads(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = _args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "dak" else "gloo")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        if dist:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
+    import torch
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import direct_host_memory_gb300 as dak
+
+    def sync_all():
+        if dist:
+            dist.barrier()
+
+    b_host, b_hbm, conc = measure_tiers(dak)
+    lin, attn = gen_inputs(args.batch)
+    w_bytes, kv_bytes = workload_bytes(args.batch)
+
+    st = Step(dak, lin, attn, args.x, dev)
+    C = st.total_bytes
+    # the attention launch is the step's dominant kernel: time it with events on its stream
+    att_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    for _ in range(args.warmup):
+        st.run()
+    torch.cuda.synchronize()
+    status = dak.dak_last_error()
+    sync_all()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    e0.record()
+    for i in range(args.steps):
+        st.run(att_ev[i])
+    e1.record()
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    sync_all()
+    t_step = e0.elapsed_time(e1) / 1e3 / args.steps
+    if dist:
+        tt = torch.tensor([t_step], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_step = float(tt.item())
+    att_ms = statistics.mean(a.elapsed_time(b) for a, b in att_ev)
+    time.sleep(0.3)
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+    status2 = dak.dak_last_error()
+
+    # end to end through the public API with host buffers: hidden states / queries copied in
+    # from pinned memory and outputs copied back every step
+    hostB = {n: b.cpu().pin_memory() for n, b in st.B.items()}
+    hostQ = st.Q.cpu().pin_memory()
+    hostC = {n: torch.empty(c.shape, dtype=c.dtype).pin_memory() for n, c in st.C.items()}
+    hostO = torch.empty(st.O.shape, dtype=st.O.dtype).pin_memory()
+    h2d = sum(b.numel() * 2 for b in hostB.values()) + hostQ.numel() * 2
+    d2h = sum(c.numel() * 2 for c in hostC.values()) + hostO.numel() * 2
+
+    def e2e_step():
+        for n in st.B:
+            st.B[n].copy_(hostB[n], non_blocking=True)
+        st.Q.copy_(hostQ, non_blocking=True)
+        st.run()
+        for n in st.C:
+            hostC[n].copy_(st.C[n], non_blocking=True)
+        hostO.copy_(st.O, non_blocking=True)
+
+    t_e2e = time_steps(e2e_step, max(10, args.steps // 3), 3, sync_all)
+
+    # per-x sweep with the prefetch baselines
+    per_x = []
+    if not args.no_sweep:
+        cs = torch.cuda.Stream()
+        evs = [torch.cuda.Event() for _ in range(len(lin) + 1)]
+        for x in (0.0, 0.05, 0.1, 0.125, 0.25, 0.5):
+            s = st if abs(x - args.x) < 1e-12 else Step(dak, lin, attn, x, dev)
+            t = time_steps(s.run, 30, 3)
+            rec = {"x": x, "host_bytes": s.host_bytes, "gbps": s.total_bytes / t / 1e9,
+                   "tok_s": args.batch / (t * LAYERS_8B), "ms": t * 1e3,
+                   "roofline_gbps": tier_roofline(s.total_bytes, s.host_bytes / s.total_bytes, b_host, b_hbm) / 1e9}
+            rec["frac"] = rec["gbps"] / rec["roofline_gbps"]
+            if x > 0:
+                s.alloc_staging(dev)
+                tp = time_steps(s.run_prefetch_serial, 10, 2)
+                to = time_steps(lambda: s.run_prefetch_overlap(cs, evs), 10, 2)
+                rec["prefetch_serial_gbps"] = s.total_bytes / tp / 1e9
+                rec["prefetch_overlap_gbps"] = s.total_bytes / to / 1e9
+                rec["vs_prefetch_best"] = rec["gbps"] / max(rec["prefetch_serial_gbps"], rec["prefetch_overlap_gbps"])
+                del s.stage, s.stage_kv
+            per_x.append(rec)
+            if s is not st:
+                s.free()
+            torch.cuda.empty_cache()
+    status3 = dak.dak_last_error()
+
+    pk, pk_src = peaks()
+    att_bytes = kv_bytes + 2 * st.Q.numel() * 2
+    x_eff = st.host_bytes / C
+    att_host = st.kv.host_bytes
+    att_roof = tier_roofline(att_bytes, att_host / att_bytes, b_host, b_hbm)
+    achieved = att_bytes / (att_ms / 1e3)
+    traffic = read_ncu_traffic()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        gbps, sample, _ = cpu_oracle_sample(lin, attn)
+        cpu = {"value": gbps, "unit": "GB/s", "cores": cpu_threads(), "kind": "oracle", "sample": sample}
+
+    n = world
+    value = n * C / t_step / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": n, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"8B-shaped decode layer at batch {args.batch}: dak_gemm over QKV 6144x4096, "
+                               f"O 4096x4096, gate+up 28672x4096, down 4096x14336 + dak_attn over 32 requests, "
+                               f"32/8 heads, D 128, context 8192; bf16, fp32 accumulate",
+                   "x": args.x, "x_effective": x_eff, "bytes_per_step": C, "host_bytes_per_step": st.host_bytes,
+                   "parallelism": f"replicas x{n}", "l2": "inputs larger than L2 (1.5 GB per step)"},
+        "decode_tok_s": n * args.batch / (t_step * LAYERS_8B),
+        "tier_roofline_gbps": tier_roofline(C, x_eff, b_host, b_hbm) / 1e9,
+        "tier_roofline_frac": (C / t_step) / tier_roofline(C, x_eff, b_host, b_hbm),
+        "b_host_gbps": b_host / 1e9, "b_hbm_gbps": b_hbm / 1e9, "concurrent_probe": conc,
+        "roofline": {"bound": "hbm", "kernel": "attn_kernel<128> + split combine (dak_attn)",
+                     "achieved": achieved / 1e9, "peak": att_roof / 1e9, "unit": "GB/s",
+                     "frac": achieved / att_roof, "traffic": traffic,
+                     "peak_kind": "tier-aggregate C/max(xC/B_host,(1-x)C/B_hbm), B_host/B_hbm measured in this run",
+                     "hbm_peak_gbs": pk.get("hbm_gbs"), "hbm_peak_source": pk_src,
+                     "algorithmic_bytes_per_launch": att_bytes, "launch_ms": att_ms},
+        "per_x": per_x,
+        "e2e": {"value": n * C / t_e2e / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": st.launches * args.steps,
+        "clocks": clocks,
+        "status": [status[0], status2[0], status3[0]],
+    }
+    if cpu:
+        line["cpu_baseline"] = cpu
+    st.free()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def read_ncu_traffic():
+    """DRAM bytes per launch of the attention kernel from the committed ncu summary, or None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            return json.load(f).get("attn_kernel_dram_bytes_per_launch")
+    except Exception:
+        return None
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,325 @@
+"""ctypes binding of libdak.so: argument marshalling only, every step runs in the library.
+
+Names match the C ABI in include/dak.h. Tensors are torch tensors (device memory and
+streams come from PyTorch); host-side sources may also be numpy arrays of bf16 bits.
+A missing library raises at import time: there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdak.so")
+
+DAK_OK = 0
+STATUS_NAMES = {
+    0: "DAK_OK", 1: "DAK_ERR_INVALID", 2: "DAK_ERR_ALIGN", 3: "DAK_ERR_HOST_ALLOC",
+    4: "DAK_ERR_DEVICE_ALLOC", 5: "DAK_ERR_CUDA", 6: "DAK_ERR_TIMEOUT", 7: "DAK_ERR_UNSUPPORTED",
+    8: "DAK_ERR_BOUNDS",
+}
+
+# every symbol include/dak.h declares
+EXPORTS = [
+    "dak_status_string", "dak_place_matrix", "dak_place_kv", "dak_free", "dak_placement_info",
+    "dak_gemm", "dak_attn_workspace_bytes", "dak_attn", "dak_attn_default_split", "dak_plan_ratios",
+    "dak_last_error", "dak_sm_count", "dak_probe_read_bw", "dak_probe_concurrent", "dak_prefetch",
+    "dak_gemm_staged", "dak_attn_staged",
+]
+
+
+class DakError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+
+
+class dak_tuning(ctypes.Structure):
+    _fields_ = [("host_ctas", ctypes.c_int), ("window", ctypes.c_int), ("hbm_window", ctypes.c_int),
+                ("chunk_k", ctypes.c_int), ("n_split", ctypes.c_int), ("hbm_ctas", ctypes.c_int)]
+
+
+class dak_op(ctypes.Structure):
+    _fields_ = [("bytes", ctypes.c_double), ("t_comp", ctypes.c_double), ("tile_bytes", ctypes.c_double)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built (run __graft_entry__.build()); "
+                          "the direct-access path has no fallback")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, dbl, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double, ctypes.c_size_t
+    P = ctypes.POINTER
+    sig = {
+        "dak_status_string": (ctypes.c_char_p, [i32]),
+        "dak_place_matrix": (i32, [vp, i32, i64, i64, i64, i32, i32, P(vp)]),
+        "dak_place_kv": (i32, [vp, vp, i32, i32, i32, i32, i32, i32, P(vp)]),
+        "dak_free": (i32, [vp]),
+        "dak_placement_info": (i32, [vp, P(i64), P(i64), P(i64), P(i64)]),
+        "dak_gemm": (i32, [vp, vp, vp, i32, i32, P(dak_tuning), vp]),
+        "dak_gemm_staged": (i32, [vp, vp, vp, vp, i32, i32, P(dak_tuning), vp]),
+        "dak_attn_workspace_bytes": (sz, [i32, i32, i32, i32]),
+        "dak_attn": (i32, [vp, vp, vp, i32, ctypes.c_float, vp, vp, sz, P(dak_tuning), vp]),
+        "dak_attn_staged": (i32, [vp, vp, vp, vp, i32, ctypes.c_float, vp, vp, sz, P(dak_tuning), vp]),
+        "dak_attn_default_split": (i32, [vp]),
+        "dak_plan_ratios": (i32, [P(dak_op), i32, dbl, dbl, dbl, i32, P(dbl), P(dbl)]),
+        "dak_last_error": (i32, [vp, P(ctypes.c_uint64)]),
+        "dak_sm_count": (i32, []),
+        "dak_probe_read_bw": (i32, [i32, i64, i32, i32, i32, i32, i32, P(dbl), P(i32)]),
+        "dak_probe_concurrent": (i32, [i64, i64, i32, i32, i32, i32, i32, i32, P(dbl), P(dbl)]),
+        "dak_prefetch": (i32, [vp, vp, vp]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+def _check(status: int, where: str):
+    if status != DAK_OK:
+        raise DakError(status, where)
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _tuning(t):
+    if t is None:
+        return None
+    if isinstance(t, dak_tuning):
+        return ctypes.byref(t)
+    tt = dak_tuning(**{k: int(v) for k, v in dict(t).items()})
+    return ctypes.byref(tt)
+
+
+def _ptr(x):
+    """Data pointer of a torch tensor or numpy array."""
+    if x is None:
+        return None
+    if isinstance(x, np.ndarray):
+        if not x.flags["C_CONTIGUOUS"]:
+            raise ValueError("numpy source must be C-contiguous")
+        return ctypes.c_void_p(x.ctypes.data)
+    return ctypes.c_void_p(x.data_ptr())
+
+
+def _on_device(x) -> int:
+    return 0 if isinstance(x, np.ndarray) else int(x.is_cuda)
+
+
+class Placement:
+    """A library-owned placement (dak_placement*). Free with .free() or by dropping it."""
+
+    def __init__(self, handle: ctypes.c_void_p, kind: str, **meta):
+        self._h = handle
+        self.kind = kind
+        self.meta = meta
+        hb, gb, u, hu = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        _check(lib.dak_placement_info(handle, ctypes.byref(hb), ctypes.byref(gb), ctypes.byref(u),
+                                      ctypes.byref(hu)), "dak_placement_info")
+        self.host_bytes, self.hbm_bytes = hb.value, gb.value
+        self.units, self.host_units = u.value, hu.value
+
+    @property
+    def handle(self):
+        if self._h is None:
+            raise ValueError("placement already freed")
+        return self._h
+
+    def free(self):
+        if self._h is not None:
+            lib.dak_free(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+# ------------------------------------------------------------------------------- placement
+
+def host_tiles_for_ratio(x: float, M: int, tile_m: int = 64) -> int:
+    """Tile rows to place on the host for offload ratio x: ceil(x * T), T = ceil(M / tile_m),
+    so that at least the fraction x of the rows leaves HBM."""
+    import math
+    T = -(-int(M) // int(tile_m))
+    return max(0, min(T, math.ceil(float(x) * T - 1e-12)))
+
+
+def host_requests_for_ratio(x: float, batch: int) -> int:
+    """Requests whose KV goes to the host for offload ratio x: ceil(x * B)."""
+    import math
+    return max(0, min(int(batch), math.ceil(float(x) * int(batch) - 1e-12)))
+
+
+def dak_place_matrix(A, n_host_tiles: int, tile_m: int = 64) -> Placement:
+    """Place weights A [M][K] (bf16: torch tensor on host or device, or numpy uint16 bits)."""
+    if A.ndim != 2:
+        raise ValueError("A must be 2-D [M][K]")
+    M, K = int(A.shape[0]), int(A.shape[1])
+    out = ctypes.c_void_p()
+    _check(lib.dak_place_matrix(_ptr(A), _on_device(A), M, K, K, tile_m, int(n_host_tiles),
+                                ctypes.byref(out)), "dak_place_matrix")
+    return Placement(out, "matrix", M=M, K=K, tile_m=tile_m)
+
+
+def dak_place_kv(K, V, n_host_requests: int) -> Placement:
+    """Place a KV cache, K and V [B][H_kv][L][D] bf16 (torch or numpy uint16 bits)."""
+    if K.shape != V.shape or K.ndim != 4:
+        raise ValueError("K and V must both be [B][H_kv][L][D]")
+    B, Hkv, L, D = (int(s) for s in K.shape)
+    out = ctypes.c_void_p()
+    _check(lib.dak_place_kv(_ptr(K), _ptr(V), _on_device(K), B, Hkv, L, D, int(n_host_requests),
+                            ctypes.byref(out)), "dak_place_kv")
+    return Placement(out, "kv", B=B, H_kv=Hkv, L=L, D=D)
+
+
+def dak_free(p: Placement):
+    p.free()
+
+
+def dak_placement_info(p: Placement):
+    return dict(host_bytes=p.host_bytes, hbm_bytes=p.hbm_bytes, units=p.units, host_units=p.host_units)
+
+
+# ------------------------------------------------------------------------------- hot path
+
+def _check_bf16_cuda(t, name):
+    import torch
+    if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+
+
+def dak_gemm(A: Placement, B, C=None, c_fp32: bool = False, tuning=None, stream=None):
+    """C [N][M] = B [N][K] . A^T over the tiered placement A (returns C)."""
+    import torch
+    _check_bf16_cuda(B, "B")
+    N = int(B.shape[0])
+    if B.ndim != 2 or int(B.shape[1]) != A.meta["K"]:
+        raise ValueError("B must be [N][K]")
+    if C is None:
+        C = torch.empty((N, A.meta["M"]), dtype=torch.float32 if c_fp32 else torch.bfloat16, device=B.device)
+    _check(lib.dak_gemm(A.handle, _ptr(B), _ptr(C), N, int(bool(c_fp32)), _tuning(tuning), _stream_ptr(stream)),
+           "dak_gemm")
+    return C
+
+
+def dak_gemm_staged(A: Placement, staging, B, C=None, c_fp32: bool = False, tuning=None, stream=None):
+    import torch
+    _check_bf16_cuda(B, "B")
+    N = int(B.shape[0])
+    if C is None:
+        C = torch.empty((N, A.meta["M"]), dtype=torch.float32 if c_fp32 else torch.bfloat16, device=B.device)
+    _check(lib.dak_gemm_staged(A.handle, _ptr(staging), _ptr(B), _ptr(C), N, int(bool(c_fp32)), _tuning(tuning),
+                               _stream_ptr(stream)), "dak_gemm_staged")
+    return C
+
+
+def dak_attn_workspace_bytes(B: int, H_q: int, D: int, n_split: int) -> int:
+    return int(lib.dak_attn_workspace_bytes(B, H_q, D, n_split))
+
+
+def dak_attn_default_split(KV: Placement) -> int:
+    return int(lib.dak_attn_default_split(KV.handle))
+
+
+def _attn_common(Q, KV, O, workspace, tuning):
+    import torch
+    _check_bf16_cuda(Q, "Q")
+    B, Hq, D = (int(s) for s in Q.shape)
+    if B != KV.meta["B"] or D != KV.meta["D"]:
+        raise ValueError("Q does not match the KV placement")
+    n_split = int(dict(tuning or {}).get("n_split", 0) or 0) if not isinstance(tuning, dak_tuning) else tuning.n_split
+    if n_split <= 0:
+        n_split = dak_attn_default_split(KV)
+    ws_bytes = dak_attn_workspace_bytes(B, Hq, D, n_split)
+    if workspace is None and ws_bytes:
+        workspace = torch.empty(ws_bytes // 4, dtype=torch.float32, device=Q.device)
+    if O is None:
+        O = torch.empty_like(Q)
+    tun = dict(tuning or {}) if not isinstance(tuning, dak_tuning) else tuning
+    if not isinstance(tun, dak_tuning):
+        tun["n_split"] = n_split
+    ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return Hq, O, workspace, ws_len, tun
+
+
+def dak_attn(Q, KV: Placement, seq_lens=None, scale: float = 0.0, O=None, workspace=None, tuning=None, stream=None):
+    """Decode attention o [B][Hq][D] over the request-partitioned KV placement (returns O)."""
+    Hq, O, workspace, ws_len, tun = _attn_common(Q, KV, O, workspace, tuning)
+    _check(lib.dak_attn(_ptr(Q), KV.handle, _ptr(seq_lens), Hq, float(scale), _ptr(O), _ptr(workspace), ws_len,
+                        _tuning(tun), _stream_ptr(stream)), "dak_attn")
+    return O
+
+
+def dak_attn_staged(Q, KV: Placement, staging, seq_lens=None, scale: float = 0.0, O=None, workspace=None,
+                    tuning=None, stream=None):
+    Hq, O, workspace, ws_len, tun = _attn_common(Q, KV, O, workspace, tuning)
+    _check(lib.dak_attn_staged(_ptr(Q), KV.handle, _ptr(staging), _ptr(seq_lens), Hq, float(scale), _ptr(O),
+                               _ptr(workspace), ws_len, _tuning(tun), _stream_ptr(stream)), "dak_attn_staged")
+    return O
+
+
+def dak_prefetch(p: Placement, staging, stream=None):
+    _check(lib.dak_prefetch(p.handle, _ptr(staging), _stream_ptr(stream)), "dak_prefetch")
+
+
+# ------------------------------------------------------------------------------- planner
+
+def dak_plan_ratios(ops, b_host: float, b_hbm: float, min_offload_bytes: float, mode: int = 0):
+    """ops: iterable of (bytes, t_comp[, tile_bytes]). Returns (ratios ndarray, model time s)."""
+    ops = list(ops)
+    arr = (dak_op * max(1, len(ops)))()
+    for i, o in enumerate(ops):
+        arr[i].bytes = float(o[0])
+        arr[i].t_comp = float(o[1])
+        arr[i].tile_bytes = float(o[2]) if len(o) > 2 else 0.0
+    ratios = (ctypes.c_double * max(1, len(ops)))()
+    t = ctypes.c_double()
+    _check(lib.dak_plan_ratios(arr, len(ops), float(b_host), float(b_hbm), float(min_offload_bytes), int(mode),
+                               ratios, ctypes.byref(t)), "dak_plan_ratios")
+    return np.array(ratios[:len(ops)], dtype=np.float64), t.value
+
+
+# ------------------------------------------------------------------------------- errors / probes
+
+def dak_last_error(stream=None):
+    """Synchronise and return (status, info) of the device status word (cleared)."""
+    info = ctypes.c_uint64()
+    st = lib.dak_last_error(_stream_ptr(stream), ctypes.byref(info))
+    return int(st), int(info.value)
+
+
+def dak_sm_count() -> int:
+    return int(lib.dak_sm_count())
+
+
+def dak_probe_read_bw(tier: int, nbytes: int, method: int = 0, ctas: int = 16, window: int = 4,
+                      chunk_bytes: int = 32768, iters: int = 5):
+    g = ctypes.c_double()
+    ok = ctypes.c_int()
+    _check(lib.dak_probe_read_bw(tier, nbytes, method, ctas, window, chunk_bytes, iters, ctypes.byref(g),
+                                 ctypes.byref(ok)), "dak_probe_read_bw")
+    return g.value, bool(ok.value)
+
+
+def dak_probe_concurrent(host_bytes: int, hbm_bytes: int, host_ctas: int, host_window: int, hbm_ctas: int,
+                         hbm_window: int, chunk_bytes: int = 32768, iters: int = 5):
+    h, g = ctypes.c_double(), ctypes.c_double()
+    _check(lib.dak_probe_concurrent(host_bytes, hbm_bytes, host_ctas, host_window, hbm_ctas, hbm_window, chunk_bytes,
+                                    iters, ctypes.byref(h), ctypes.byref(g)), "dak_probe_concurrent")
+    return h.value, g.value

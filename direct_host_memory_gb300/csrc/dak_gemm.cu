@@ -1,0 +1,536 @@
+// SplitK_GEMM for decode: C = A x B where the tile rows of A are split between pinned,
+// device-mapped host memory and HBM ("DAK: Direct-Access-Enabled GPU Memory Offloading
+// with Optimal Efficiency for LLM Inference", section 4.1, Fig. 5).
+//
+// One persistent launch. CTAs [0, n_host) take the host tile rows, the others the HBM
+// tile rows; a CTA never reads both tiers (section 4.1, "Kernel over Partitioned
+// Memory"). Inside a CTA one producer thread streams m x kc chunks of its tile row into
+// a ring of shared-memory slots with single bulk asynchronous copies (the copy engine of
+// TMA) while other warps do the math (section 4.1, "Asynchronous TMA Access"). Host CTAs
+// keep at most `host_window` chunks in flight: the static congestion window of section
+// 4.3.1. Each tile row is read by exactly one CTA, which computes all N columns, so no
+// host byte crosses the link twice (the locality half of section 4.3.2's scheduling).
+//
+// Placement layout of a tile row (both tiers): 64 rows x K_pad columns stored k-group
+// major, [K_pad/8][64 rows][8 columns] bf16: every 8 x 8 block (8 rows x 16 bytes) is
+// contiguous, every chunk of kc columns is one contiguous range, and that range is
+// already the no-swizzle K-major operand layout the tcgen05 tensor cores read.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "dak_device.cuh"
+
+namespace dak {
+
+struct GemmParams {
+    const uint8_t* a_host;  // tile rows 0 .. h-1 (device-visible address of the host mapping)
+    const uint8_t* a_hbm;   // tile rows h .. T-1
+    const __nv_bfloat16* B; // [N][K]
+    void* C;                // [N][M]
+    int M, K, K_pad, N, N_pad, T, h;
+    int n_host_ctas, n_hbm_ctas, host_window, hbm_window;
+    int kc;           // chunk width along K (multiple of 64)
+    int stages;       // ring slots in shared memory
+    int stage_bytes;  // bytes per slot
+    int c_fp32;
+    long long tile_bytes;
+    DevStatus* st;
+};
+
+// Tiles of this CTA: role, first tile, stride, count.
+struct TileIter {
+    bool host;
+    int first, stride, count;
+    const uint8_t* base;
+    int window;
+};
+
+__device__ __forceinline__ TileIter tiles_of_cta(const GemmParams& p) {
+    TileIter it;
+    int b = blockIdx.x;
+    if (b < p.n_host_ctas) {
+        it.host = true;
+        it.first = b;
+        it.stride = p.n_host_ctas;
+        it.count = (p.h > b) ? (p.h - b + p.n_host_ctas - 1) / p.n_host_ctas : 0;
+        it.base = p.a_host;
+        it.window = p.host_window;
+    } else {
+        int j = b - p.n_host_ctas;
+        int nh = p.T - p.h;
+        it.host = false;
+        it.first = p.h + j;
+        it.stride = p.n_hbm_ctas;
+        it.count = (nh > j) ? (nh - j + p.n_hbm_ctas - 1) / p.n_hbm_ctas : 0;
+        it.base = p.a_hbm;
+        it.window = p.hbm_window;
+    }
+    return it;
+}
+
+__device__ __forceinline__ const uint8_t* tile_src(const GemmParams& p, const TileIter& it, int t) {
+    int local = it.host ? t : t - p.h;
+    return it.base + static_cast<long long>(local) * p.tile_bytes;
+}
+
+// error location codes (upper 32 bits of the status info)
+enum : uint32_t { W_PROD_EMPTY = 1, W_CONS_FULL = 2, W_MMA_FULL = 3, W_MMA_ACC = 4, W_EPI_ACC = 5, W_DRAIN = 6 };
+
+// Wait (bounded, ignoring the abort flag) for the last fill of every ring slot, so that no
+// bulk copy is still writing shared memory when the CTA exits.
+__device__ __forceinline__ void drain_fills(uint64_t* full, int window, long long issued, DevStatus* st) {
+    volatile int dummy = 0;
+    for (int s = 0; s < window; ++s) {
+        if (issued <= s) break;
+        long long last = ((issued - 1 - s) / window) * window + s;  // last iteration that used slot s
+        uint32_t parity = static_cast<uint32_t>((last / window) & 1);
+        mbar_wait(&full[s], parity, &dummy, st, DAK_ERR_TIMEOUT, W_DRAIN);
+    }
+}
+
+// ======================================================================================
+// CUDA-core path, N in 1..7: warp-level FMA, fp32 accumulation, shuffle reduction.
+// Warps: 0 = producer, 1..8 = consumers (consumer w owns rows 8w .. 8w+7 of the tile).
+// ======================================================================================
+constexpr int kCoreConsumers = 8;
+
+template <int N>
+__global__ void __launch_bounds__(32 * (1 + kCoreConsumers), 1) gemm_core_kernel(const GemmParams p) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    __shared__ uint64_t full[8], empty[8];
+    __shared__ int abort_flag;
+    volatile int* abort = &abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const TileIter it = tiles_of_cta(p);
+    const int W = it.window;
+    const int nch = (p.K_pad + p.kc - 1) / p.kc;
+    uint8_t* smem = smem_raw;
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int s = 0; s < W; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kCoreConsumers);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol_a = policy_evict_first();
+            const uint64_t pol_b = policy_evict_last();
+            long long i = 0;
+            for (int ti = 0; ti < it.count && !*abort; ++ti) {
+                const int t = it.first + ti * it.stride;
+                const uint8_t* src = tile_src(p, it, t);
+                for (int c = 0; c < nch; ++c, ++i) {
+                    const int s = static_cast<int>(i % W);
+                    if (i >= W && !mbar_wait(&empty[s], static_cast<uint32_t>(((i / W) - 1) & 1), abort, p.st,
+                                             DAK_ERR_TIMEOUT, W_PROD_EMPTY)) {
+                        goto producer_done;
+                    }
+                    const int k0 = c * p.kc;
+                    const int kce = min(p.kc, p.K_pad - k0);
+                    const int kreal = min(kce, p.K - k0);
+                    uint8_t* dst = smem + static_cast<size_t>(s) * p.stage_bytes;
+                    const uint32_t a_bytes = static_cast<uint32_t>(kce) * 128u;
+                    const uint32_t b_row = static_cast<uint32_t>(kreal) * 2u;
+                    mbar_arrive_expect_tx(&full[s], a_bytes + b_row * N);
+                    bulk_g2s(dst, src + static_cast<long long>(k0) * 128, a_bytes, &full[s], pol_a);
+#pragma unroll
+                    for (int n = 0; n < N; ++n) {
+                        bulk_g2s(dst + a_bytes + n * p.kc * 2, p.B + static_cast<long long>(n) * p.K + k0, b_row,
+                                 &full[s], pol_b);
+                    }
+                }
+            }
+        producer_done:
+            drain_fills(full, W, i, p.st);
+        }
+        return;
+    }
+
+    // consumers
+    const int w = warp - 1;       // row group 0..7
+    const int r = lane & 7;       // row within the group
+    const int kq = lane >> 3;     // k-group phase 0..3
+    long long i = 0;
+    for (int ti = 0; ti < it.count; ++ti) {
+        const int t = it.first + ti * it.stride;
+        float acc[N];
+#pragma unroll
+        for (int n = 0; n < N; ++n) acc[n] = 0.f;
+        for (int c = 0; c < nch; ++c, ++i) {
+            const int s = static_cast<int>(i % W);
+            if (!mbar_wait(&full[s], static_cast<uint32_t>((i / W) & 1), abort, p.st, DAK_ERR_TIMEOUT, W_CONS_FULL)) {
+                return;
+            }
+            const int k0 = c * p.kc;
+            const int kgr = min(min(p.kc, p.K_pad - k0), p.K - k0) >> 3;  // real k-groups in this chunk
+            const uint8_t* st = smem + static_cast<size_t>(s) * p.stage_bytes;
+            const uint32_t a_bytes = static_cast<uint32_t>(min(p.kc, p.K_pad - k0)) * 128u;
+            for (int kg = kq; kg < kgr; kg += 4) {
+                const uint4 a = *reinterpret_cast<const uint4*>(st + kg * 1024 + w * 128 + r * 16);
+                const float a0 = bf_lo(a.x), a1 = bf_hi(a.x), a2 = bf_lo(a.y), a3 = bf_hi(a.y);
+                const float a4 = bf_lo(a.z), a5 = bf_hi(a.z), a6 = bf_lo(a.w), a7 = bf_hi(a.w);
+#pragma unroll
+                for (int n = 0; n < N; ++n) {
+                    const uint4 b = *reinterpret_cast<const uint4*>(st + a_bytes + n * p.kc * 2 + kg * 16);
+                    float v = acc[n];
+                    v = fmaf(a0, bf_lo(b.x), v);
+                    v = fmaf(a1, bf_hi(b.x), v);
+                    v = fmaf(a2, bf_lo(b.y), v);
+                    v = fmaf(a3, bf_hi(b.y), v);
+                    v = fmaf(a4, bf_lo(b.z), v);
+                    v = fmaf(a5, bf_hi(b.z), v);
+                    v = fmaf(a6, bf_lo(b.w), v);
+                    v = fmaf(a7, bf_hi(b.w), v);
+                    acc[n] = v;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+        // reduce the four k phases: lanes r, r+8, r+16, r+24 hold the same row
+#pragma unroll
+        for (int n = 0; n < N; ++n) {
+            float v = acc[n];
+            v += __shfl_xor_sync(0xffffffffu, v, 8);
+            v += __shfl_xor_sync(0xffffffffu, v, 16);
+            acc[n] = v;
+        }
+        const int row = t * kTileM + w * 8 + r;
+        if (kq == 0 && row < p.M) {
+#pragma unroll
+            for (int n = 0; n < N; ++n) {
+                if (p.c_fp32) {
+                    reinterpret_cast<float*>(p.C)[static_cast<long long>(n) * p.M + row] = acc[n];
+                } else {
+                    reinterpret_cast<__nv_bfloat16*>(p.C)[static_cast<long long>(n) * p.M + row] =
+                        __float2bfloat16_rn(acc[n]);
+                }
+            }
+        }
+    }
+}
+
+// ======================================================================================
+// Tensor-core path, N in 8..256: tcgen05.mma (M = 64 rows of A, N = N_pad hidden-state
+// columns, K = 16 per instruction), fp32 accumulators in TMEM, double-buffered.
+// Warps: 0 = producer (A by bulk copy, B by 128-byte-swizzled tensor-map copies),
+//        1 = TMEM allocator + MMA issuer, 2..5 = epilogue (TMEM -> registers -> C).
+// ======================================================================================
+constexpr int kUmmaThreads = 6 * 32;
+
+// TMEM lane holding output row `row` (0..63) of an M = 64 accumulator: rows 16q .. 16q+15
+// sit in lanes 32q .. 32q+15 of sub-partition q.
+__device__ __forceinline__ int umma_m64_row_of_lane(int q, int lane) { return lane < 16 ? q * 16 + lane : -1; }
+
+__global__ void __launch_bounds__(kUmmaThreads, 1)
+    gemm_umma_kernel(const GemmParams p, const __grid_constant__ CUtensorMap bmap) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ uint64_t full[8], empty[8], acc_full[2], acc_empty[2];
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int abort_flag;
+    volatile int* abort = &abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const TileIter it = tiles_of_cta(p);
+    const int W = it.window;
+    const int nch = (p.K_pad + p.kc - 1) / p.kc;
+    // 1024-byte aligned ring (128-byte swizzle atoms must start on 1024-byte boundaries)
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    const int a_stage_bytes = p.kc * 128;
+    const int bblk_bytes = p.N_pad * 128;  // one 64-column block of B
+    uint32_t tmem_cols = 32;
+    while (tmem_cols < static_cast<uint32_t>(2 * p.N_pad)) tmem_cols <<= 1;
+    const uint32_t acc_stride = tmem_cols >> 1;  // column offset of the second accumulator
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int s = 0; s < W; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 4);
+        }
+        fence_mbar_init();
+        prefetch_tmap(&bmap);
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_base_sh, tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_sh;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol_a = policy_evict_first();
+            long long i = 0;
+            for (int ti = 0; ti < it.count && !*abort; ++ti) {
+                const int t = it.first + ti * it.stride;
+                const uint8_t* src = tile_src(p, it, t);
+                for (int c = 0; c < nch; ++c, ++i) {
+                    const int s = static_cast<int>(i % W);
+                    if (i >= W && !mbar_wait(&empty[s], static_cast<uint32_t>(((i / W) - 1) & 1), abort, p.st,
+                                             DAK_ERR_TIMEOUT, W_PROD_EMPTY)) {
+                        goto producer_done;
+                    }
+                    const int k0 = c * p.kc;
+                    const int kce = min(p.kc, p.K_pad - k0);
+                    const int nblk = (kce + 63) >> 6;
+                    uint8_t* dst = smem + static_cast<size_t>(s) * p.stage_bytes;
+                    const uint32_t a_bytes = static_cast<uint32_t>(kce) * 128u;
+                    mbar_arrive_expect_tx(&full[s], a_bytes + static_cast<uint32_t>(nblk * bblk_bytes));
+                    bulk_g2s(dst, src + static_cast<long long>(k0) * 128, a_bytes, &full[s], pol_a);
+                    for (int b = 0; b < nblk; ++b) {
+                        tma_load_2d(dst + a_stage_bytes + b * bblk_bytes, &bmap, k0 + 64 * b, 0, &full[s]);
+                    }
+                }
+            }
+        producer_done:
+            drain_fills(full, W, i, p.st);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(64, static_cast<uint32_t>(p.N_pad));
+            long long i = 0;
+            uint64_t* last_bar = nullptr;
+            uint32_t last_par = 0;
+            for (int ti = 0; ti < it.count; ++ti) {
+                const int ab = ti & 1;
+                if (ti >= 2 && !mbar_wait(&acc_empty[ab], static_cast<uint32_t>(((ti >> 1) - 1) & 1), abort, p.st,
+                                          DAK_ERR_TIMEOUT, W_MMA_ACC)) {
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + static_cast<uint32_t>(ab) * acc_stride;
+                bool ok = true;
+                for (int c = 0; c < nch; ++c, ++i) {
+                    const int s = static_cast<int>(i % W);
+                    if (!mbar_wait(&full[s], static_cast<uint32_t>((i / W) & 1), abort, p.st, DAK_ERR_TIMEOUT,
+                                   W_MMA_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int kce = min(p.kc, p.K_pad - c * p.kc);
+                    const uint32_t a_base = smem_u32(smem + static_cast<size_t>(s) * p.stage_bytes);
+                    const uint32_t b_base = a_base + static_cast<uint32_t>(a_stage_bytes);
+                    for (int kk = 0; kk < kce; kk += 16) {
+                        // A: no swizzle, K-major; 8x8 blocks of one k-group are 128 B apart
+                        // along M, k-groups are 64 rows x 16 B = 1024 B apart along K.
+                        const uint64_t ad = smem_desc(a_base + static_cast<uint32_t>(kk >> 3) * 1024u, 1024u, 128u, 0u);
+                        // B: 128-byte swizzle, K-major; 8-row groups 1024 B apart, 64-column
+                        // blocks N_pad x 128 B apart, +32 B per 16 columns inside a block.
+                        const uint64_t bd = smem_desc(
+                            b_base + static_cast<uint32_t>((kk >> 6) * bblk_bytes + (kk & 63) * 2), 16u, 1024u, 2u);
+                        umma_bf16(d_tmem, ad, bd, idesc, (c > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(&empty[s]);
+                    last_bar = &empty[s];
+                    last_par = static_cast<uint32_t>((i / W) & 1);
+                }
+                if (!ok) break;
+                umma_commit(&acc_full[ab]);
+                last_bar = &acc_full[ab];
+                last_par = static_cast<uint32_t>((ti >> 1) & 1);
+            }
+            if (last_bar) {  // every issued MMA has finished before TMEM is released
+                volatile int dummy = 0;
+                mbar_wait(last_bar, last_par, &dummy, p.st, DAK_ERR_TIMEOUT, W_DRAIN);
+            }
+        }
+        __syncwarp();
+    } else {
+        // epilogue warps 2..5 -> TMEM sub-partitions 2, 3, 0, 1
+        const int q = warp & 3;
+        const int row_in_tile = umma_m64_row_of_lane(q, lane);
+        for (int ti = 0; ti < it.count; ++ti) {
+            const int ab = ti & 1;
+            if (!mbar_wait(&acc_full[ab], static_cast<uint32_t>((ti >> 1) & 1), abort, p.st, DAK_ERR_TIMEOUT,
+                           W_EPI_ACC)) {
+                break;
+            }
+            tc_fence_after();
+            const int t = it.first + ti * it.stride;
+            const int row = t * kTileM + row_in_tile;
+            const bool valid = row_in_tile >= 0 && row < p.M;
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(ab) * acc_stride;
+            for (int n0 = 0; n0 < p.N_pad; n0 += 8) {
+                uint32_t v[8];
+                tmem_ld8(taddr + static_cast<uint32_t>(n0), v);
+                tmem_wait_ld();
+                if (valid) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int n = n0 + j;
+                        if (n < p.N) {
+                            const float f = __uint_as_float(v[j]);
+                            if (p.c_fp32) {
+                                reinterpret_cast<float*>(p.C)[static_cast<long long>(n) * p.M + row] = f;
+                            } else {
+                                reinterpret_cast<__nv_bfloat16*>(p.C)[static_cast<long long>(n) * p.M + row] =
+                                    __float2bfloat16_rn(f);
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[ab]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, tmem_cols);
+    }
+}
+
+// ======================================================================================
+// host side
+// ======================================================================================
+using EncodeTiledFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess) {
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+        }
+    });
+    return fn;
+}
+
+static bool make_b_map(CUtensorMap* map, const void* B, int K, int N, int N_pad) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(N_pad)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(B), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+constexpr int kSmemBudget = 200 * 1024;
+constexpr int kDefaultHostCtas = 16;
+constexpr int kDefaultHostWindow = 4;
+
+template <int N>
+static cudaError_t launch_core(const GemmParams& p, int grid, int smem, cudaStream_t s) {
+    auto k = gemm_core_kernel<N>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    k<<<grid, 32 * (1 + kCoreConsumers), smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+dak_status launch_gemm(const dak_placement* A, const void* host_src, const void* B, void* C, int N, int c_fp32,
+                       const dak_tuning* t, cudaStream_t stream) {
+    if (!A || A->kind != 0) return DAK_ERR_INVALID;
+    if (N < 1 || N > 256) return DAK_ERR_INVALID;
+    if (A->M == 0 || A->T == 0) return DAK_OK;  // nothing to compute; C may be empty
+    if (!B || !C) return DAK_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(B) & 15) || (reinterpret_cast<uintptr_t>(C) & 15)) return DAK_ERR_ALIGN;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DAK_ERR_CUDA;
+    if (dev != A->device) return DAK_ERR_INVALID;
+
+    GemmParams p{};
+    p.a_host = static_cast<const uint8_t*>(host_src);
+    p.a_hbm = static_cast<const uint8_t*>(A->hbm_ptr);
+    p.B = static_cast<const __nv_bfloat16*>(B);
+    p.C = C;
+    p.M = static_cast<int>(A->M);
+    p.K = static_cast<int>(A->K);
+    p.K_pad = static_cast<int>(A->K_pad);
+    p.N = N;
+    p.N_pad = (N + 7) & ~7;
+    p.T = A->T;
+    p.h = A->h;
+    p.c_fp32 = c_fp32 ? 1 : 0;
+    p.tile_bytes = A->tile_bytes;
+    p.st = status_ptr();
+    if (!p.st) return DAK_ERR_CUDA;
+
+    const bool umma = N >= 8;
+    int kc = (t && t->chunk_k > 0) ? t->chunk_k : (p.N_pad <= 64 ? 256 : (p.N_pad <= 128 ? 128 : 64));
+    if (kc % 64 != 0 || kc > 1024) return DAK_ERR_INVALID;
+    p.kc = kc;
+    int stage = umma ? kc * 128 + ((kc + 63) / 64) * p.N_pad * 128 : kc * 128 + 8 * kc * 2;
+    stage = (stage + 1023) & ~1023;
+    int stages = std::min(8, kSmemBudget / stage);
+    if (stages < 2) return DAK_ERR_INVALID;
+    p.stages = stages;
+    p.stage_bytes = stage;
+    const int smem = stages * stage + (umma ? 1024 : 0);
+
+    Sched sc = schedule(p.h, p.T - p.h, device_sm_count(), t, kDefaultHostCtas, std::min(kDefaultHostWindow, stages),
+                        stages, stages);
+    p.n_host_ctas = sc.n_host_ctas;
+    p.n_hbm_ctas = sc.n_hbm_ctas;
+    p.host_window = sc.host_window;
+    p.hbm_window = sc.hbm_window;
+    const int grid = p.n_host_ctas + p.n_hbm_ctas;
+    if (grid == 0) return DAK_OK;
+    if (p.h > 0 && !p.a_host) return DAK_ERR_INVALID;
+
+    cudaError_t e;
+    if (umma) {
+        alignas(64) CUtensorMap bmap;
+        if (!make_b_map(&bmap, B, p.K, N, p.N_pad)) return DAK_ERR_CUDA;
+        e = cudaFuncSetAttribute(gemm_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return cuda_status(e);
+        gemm_umma_kernel<<<grid, kUmmaThreads, smem, stream>>>(p, bmap);
+        e = cudaGetLastError();
+    } else {
+        switch (N) {
+            case 1: e = launch_core<1>(p, grid, smem, stream); break;
+            case 2: e = launch_core<2>(p, grid, smem, stream); break;
+            case 3: e = launch_core<3>(p, grid, smem, stream); break;
+            case 4: e = launch_core<4>(p, grid, smem, stream); break;
+            case 5: e = launch_core<5>(p, grid, smem, stream); break;
+            case 6: e = launch_core<6>(p, grid, smem, stream); break;
+            default: e = launch_core<7>(p, grid, smem, stream); break;
+        }
+    }
+    return cuda_status(e);
+}
+
+}  // namespace dak
+
+extern "C" dak_status dak_gemm(const dak_placement* A, const void* B, void* C, int N, int c_fp32,
+                               const dak_tuning* tuning, void* stream) {
+    if (!A) return DAK_ERR_INVALID;
+    return dak::launch_gemm(A, A->host_dev, B, C, N, c_fp32, tuning, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" dak_status dak_gemm_staged(const dak_placement* A, const void* staging, const void* B, void* C, int N,
+                                      int c_fp32, const dak_tuning* tuning, void* stream) {
+    if (!A || (A->h > 0 && !staging)) return DAK_ERR_INVALID;
+    if (reinterpret_cast<uintptr_t>(staging) & 15) return DAK_ERR_ALIGN;
+    return dak::launch_gemm(A, staging, B, C, N, c_fp32, tuning, static_cast<cudaStream_t>(stream));
+}

@@ -1,0 +1,67 @@
+// Library-internal declarations shared by the runtime, GEMM and attention translation units.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/dak.h"
+
+struct dak_placement {
+    int kind;    // 0 = matrix (GEMM weights), 1 = KV cache
+    int device;  // device the placement was made on
+    // tier buffers: host part (pinned, device-mapped; host and device addresses) and HBM part
+    void* host_ptr;
+    void* host_dev;
+    void* hbm_ptr;
+    int64_t host_bytes;
+    int64_t hbm_bytes;
+    // matrix
+    int64_t M, K, K_pad;
+    int tile_m;
+    int T;  // tile rows
+    int h;  // tile rows on the host
+    int64_t tile_bytes;
+    // kv
+    int B, H_kv, L, D;
+    int h_r;                // requests on the host
+    int64_t head_bytes;     // L * D * 2: one (request, kv head) slab of K (or V)
+    int64_t kv_tier_half;   // in each tier: K block first, V block after it at this offset
+};
+
+namespace dak {
+
+constexpr int kTileM = 64;
+
+// Device status block: first failure code and where it happened.
+struct DevStatus {
+    int code;
+    int pad;
+    unsigned long long info;
+};
+
+// Device address of the status block of the current device (set up once per device).
+DevStatus* status_ptr();
+
+struct Sched {
+    int n_host_ctas;  // CTAs [0, n_host_ctas) read the host tier
+    int n_hbm_ctas;   // CTAs [n_host_ctas, n_host_ctas + n_hbm_ctas) read HBM
+    int host_window;
+    int hbm_window;
+};
+
+// Split a persistent grid between the two tiers: (1) enough host CTAs for the host
+// units, capped by the congestion limit; (2) whole waves on each side, so that no
+// tail wave runs with a few CTAs; (3) every other SM on the HBM side.
+Sched schedule(int host_units, int hbm_units, int sm_slots, const dak_tuning* t, int default_host_ctas,
+               int default_host_window, int default_hbm_window, int max_window);
+
+int device_sm_count();
+dak_status cuda_status(cudaError_t e);
+
+// kernel launchers (defined in dak_gemm.cu / dak_attn.cu)
+dak_status launch_gemm(const dak_placement* A, const void* host_src, const void* B, void* C, int N, int c_fp32,
+                       const dak_tuning* t, cudaStream_t s);
+dak_status launch_attn(const void* Q, const dak_placement* KV, const void* host_src, const int* seq_lens, int H_q,
+                       float scale, void* O, void* ws, size_t ws_bytes, const dak_tuning* t, cudaStream_t s);
+
+}  // namespace dak

@@ -1,0 +1,689 @@
+// Runtime of the direct-access library: status word, placement of operands across the
+// host and HBM tiers, the persistent-grid split between tiers, tier bandwidth probes and
+// the prefetch baseline's copy.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <chrono>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "dak_device.cuh"
+
+namespace dak {
+
+__device__ DevStatus g_status_block = {0, 0, 0ull};
+
+DevStatus* status_ptr() {
+    static DevStatus* cache[64] = {nullptr};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_status_block) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        cache[dev] = static_cast<DevStatus*>(ptr);
+    }
+    return cache[dev];
+}
+
+dak_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return DAK_OK;
+    if (e == cudaErrorMemoryAllocation) return DAK_ERR_DEVICE_ALLOC;
+    return DAK_ERR_CUDA;
+}
+
+int device_sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    if (!cache[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = n > 0 ? n : 1;
+    }
+    return cache[dev];
+}
+
+static int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+Sched schedule(int host_units, int hbm_units, int sm_slots, const dak_tuning* t, int default_host_ctas,
+               int default_host_window, int default_hbm_window, int max_window) {
+    Sched s{};
+    int cap = (t && t->host_ctas > 0) ? t->host_ctas : default_host_ctas;
+    cap = std::max(1, std::min(cap, sm_slots - (hbm_units > 0 ? 1 : 0)));
+    if (host_units > 0) {
+        const int waves = ceil_div(host_units, cap);
+        s.n_host_ctas = ceil_div(host_units, waves);  // whole waves: no partial tail wave
+    }
+    int hbm_slots = sm_slots - s.n_host_ctas;
+    if (t && t->hbm_ctas > 0) hbm_slots = std::min(hbm_slots, t->hbm_ctas);
+    hbm_slots = std::max(1, hbm_slots);
+    if (hbm_units > 0) {
+        const int waves = ceil_div(hbm_units, hbm_slots);
+        s.n_hbm_ctas = ceil_div(hbm_units, waves);
+    }
+    int hw = (t && t->window > 0) ? t->window : default_host_window;
+    int bw = (t && t->hbm_window > 0) ? t->hbm_window : default_hbm_window;
+    s.host_window = std::max(1, std::min(hw, max_window));
+    s.hbm_window = std::max(1, std::min(bw, max_window));
+    return s;
+}
+
+// ------------------------------------------------------------------------------------
+// placement
+// ------------------------------------------------------------------------------------
+
+// Row-major A rows [rows][lda] (16-byte units of 8 bf16) -> tile rows stored
+// [K_pad/8][64][8]: unit (t, kg, r) at t*KG*64 + kg*64 + r. Rows past `rows` and
+// k-groups past K/8 are zero.
+__global__ void pack_matrix_kernel(const uint4* __restrict__ src, long long lda16, long long rows, int K16, int KG,
+                                   uint4* __restrict__ dst, long long units) {
+    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < units;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long per_tile = static_cast<long long>(KG) * kTileM;
+        const long long t = idx / per_tile;
+        const int rem = static_cast<int>(idx - t * per_tile);
+        const int kg = rem / kTileM;
+        const int r = rem - kg * kTileM;
+        const long long row = t * kTileM + r;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (row < rows && kg < K16) v = src[row * lda16 + kg];
+        dst[idx] = v;
+    }
+}
+
+// K or V rows [n_rows][D] -> same rows with the 16-byte chunks of token j permuted by
+// c -> c ^ (j & 7), so that 8 consecutive tokens' chunk c fall in 8 different bank groups.
+__global__ void pack_kv_kernel(const uint4* __restrict__ src, long long n_units, int D16, int L,
+                               uint4* __restrict__ dst) {
+    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < n_units;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long row = idx / D16;
+        const int c = static_cast<int>(idx - row * D16);
+        const int j = static_cast<int>(row % L);
+        dst[row * D16 + (c ^ (j & 7))] = src[idx];
+    }
+}
+
+static void free_parts(dak_placement* p) {
+    if (!p) return;
+    if (p->host_ptr) cudaFreeHost(p->host_ptr);
+    if (p->hbm_ptr) cudaFree(p->hbm_ptr);
+    p->host_ptr = p->host_dev = p->hbm_ptr = nullptr;
+}
+
+static dak_status alloc_tiers(dak_placement* p) {
+    if (p->host_bytes > 0) {
+        if (cudaHostAlloc(&p->host_ptr, static_cast<size_t>(p->host_bytes),
+                          cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess) {
+            cudaGetLastError();
+            p->host_ptr = nullptr;
+            return DAK_ERR_HOST_ALLOC;
+        }
+        if (cudaHostGetDevicePointer(&p->host_dev, p->host_ptr, 0) != cudaSuccess) {
+            cudaGetLastError();
+            return DAK_ERR_HOST_ALLOC;
+        }
+    }
+    if (p->hbm_bytes > 0) {
+        if (cudaMalloc(&p->hbm_ptr, static_cast<size_t>(p->hbm_bytes)) != cudaSuccess) {
+            cudaGetLastError();
+            p->hbm_ptr = nullptr;
+            return DAK_ERR_DEVICE_ALLOC;
+        }
+    }
+    return DAK_OK;
+}
+
+static int pack_grid(long long units) {
+    long long g = (units + 255) / 256;
+    return static_cast<int>(std::max(1ll, std::min(g, 4096ll)));
+}
+
+}  // namespace dak
+
+using namespace dak;
+
+extern "C" const char* dak_status_string(int s) {
+    switch (s) {
+        case DAK_OK: return "ok";
+        case DAK_ERR_INVALID: return "invalid argument";
+        case DAK_ERR_ALIGN: return "misaligned pointer or size";
+        case DAK_ERR_HOST_ALLOC: return "pinned host allocation failed";
+        case DAK_ERR_DEVICE_ALLOC: return "device allocation failed";
+        case DAK_ERR_CUDA: return "CUDA error";
+        case DAK_ERR_TIMEOUT: return "kernel wait timed out";
+        case DAK_ERR_UNSUPPORTED: return "unsupported shape";
+        case DAK_ERR_BOUNDS: return "kernel index check failed";
+        default: return "unknown status";
+    }
+}
+
+extern "C" dak_status dak_place_matrix(const void* A_src, int src_on_device, int64_t M, int64_t K, int64_t lda,
+                                       int tile_m, int n_host_tiles, dak_placement** out) {
+    if (!out) return DAK_ERR_INVALID;
+    *out = nullptr;
+    if (M < 0 || K <= 0 || lda < K || (M > 0 && !A_src)) return DAK_ERR_INVALID;
+    if (tile_m != kTileM) return DAK_ERR_UNSUPPORTED;
+    if ((K % 8) || (lda % 8) || (reinterpret_cast<uintptr_t>(A_src) & 15)) return DAK_ERR_ALIGN;
+    if (K > (1 << 24) || M > (1ll << 31)) return DAK_ERR_INVALID;
+    const int T = static_cast<int>((M + kTileM - 1) / kTileM);
+    if (n_host_tiles < 0 || n_host_tiles > T) return DAK_ERR_INVALID;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DAK_ERR_CUDA;
+
+    dak_placement* p = new dak_placement();
+    std::memset(p, 0, sizeof(*p));
+    p->kind = 0;
+    p->device = dev;
+    p->M = M;
+    p->K = K;
+    p->K_pad = (K + 15) / 16 * 16;
+    p->tile_m = kTileM;
+    p->T = T;
+    p->h = n_host_tiles;
+    p->tile_bytes = static_cast<int64_t>(kTileM) * p->K_pad * 2;
+    p->host_bytes = p->tile_bytes * p->h;
+    p->hbm_bytes = p->tile_bytes * (T - p->h);
+    dak_status st = alloc_tiers(p);
+    if (st != DAK_OK) {
+        free_parts(p);
+        delete p;
+        return st;
+    }
+
+    // pack in batches of tile rows through a device staging buffer when the source is host memory
+    const int KG = static_cast<int>(p->K_pad / 8);
+    const int K16 = static_cast<int>(K / 8);
+    const long long lda16 = lda / 8;
+    const int batch_tiles = std::max(1, static_cast<int>((256ll << 20) / std::max<int64_t>(1, kTileM * lda * 2)));
+    void* tmp = nullptr;
+    cudaError_t e = cudaSuccess;
+    if (!src_on_device && M > 0) {
+        e = cudaMalloc(&tmp, static_cast<size_t>(batch_tiles) * kTileM * lda * 2);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            free_parts(p);
+            delete p;
+            return DAK_ERR_DEVICE_ALLOC;
+        }
+    }
+    for (int t0 = 0; t0 < T && e == cudaSuccess; t0 += batch_tiles) {
+        const int nt = std::min(batch_tiles, T - t0);
+        const long long row0 = static_cast<long long>(t0) * kTileM;
+        const long long rows = std::min<long long>(static_cast<long long>(nt) * kTileM, M - row0);
+        const uint4* src;
+        if (src_on_device) {
+            src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(A_src) + row0 * lda * 2);
+        } else {
+            e = cudaMemcpy(tmp, static_cast<const uint8_t*>(A_src) + row0 * lda * 2,
+                           static_cast<size_t>(rows * lda * 2), cudaMemcpyHostToDevice);
+            src = reinterpret_cast<const uint4*>(tmp);
+        }
+        if (e != cudaSuccess) break;
+        // destination: tile rows may straddle the tier boundary; pack each tier's part
+        for (int tier = 0; tier < 2; ++tier) {
+            const int lo = tier == 0 ? t0 : std::max(t0, p->h);
+            const int hi = tier == 0 ? std::min(t0 + nt, p->h) : t0 + nt;
+            if (hi <= lo) continue;
+            uint8_t* base = static_cast<uint8_t*>(tier == 0 ? p->host_dev : p->hbm_ptr);
+            const int first = tier == 0 ? 0 : p->h;  // first tile row stored in this tier
+            uint4* dst = reinterpret_cast<uint4*>(base + static_cast<long long>(lo - first) * p->tile_bytes);
+            const long long units = static_cast<long long>(hi - lo) * KG * kTileM;
+            const long long src_row0 = static_cast<long long>(lo - t0) * kTileM;
+            const long long src_rows = std::max(0ll, rows - src_row0);
+            pack_matrix_kernel<<<pack_grid(units), 256>>>(src + src_row0 * lda16, lda16, src_rows, K16, KG, dst,
+                                                          units);
+            e = cudaGetLastError();
+        }
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    }
+    if (tmp) cudaFree(tmp);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        free_parts(p);
+        delete p;
+        return DAK_ERR_CUDA;
+    }
+    *out = p;
+    return DAK_OK;
+}
+
+extern "C" dak_status dak_place_kv(const void* K_src, const void* V_src, int src_on_device, int B, int H_kv, int L,
+                                   int D, int n_host_requests, dak_placement** out) {
+    if (!out) return DAK_ERR_INVALID;
+    *out = nullptr;
+    if (B <= 0 || H_kv <= 0 || L <= 0 || !K_src || !V_src) return DAK_ERR_INVALID;
+    if (D != 64 && D != 128) return DAK_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(K_src) & 15) || (reinterpret_cast<uintptr_t>(V_src) & 15)) return DAK_ERR_ALIGN;
+    if (n_host_requests < 0 || n_host_requests > B) return DAK_ERR_INVALID;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DAK_ERR_CUDA;
+
+    dak_placement* p = new dak_placement();
+    std::memset(p, 0, sizeof(*p));
+    p->kind = 1;
+    p->device = dev;
+    p->B = B;
+    p->H_kv = H_kv;
+    p->L = L;
+    p->D = D;
+    p->h_r = n_host_requests;
+    p->head_bytes = static_cast<int64_t>(L) * D * 2;
+    const int64_t req_bytes = p->head_bytes * H_kv;  // K (or V) of one request
+    p->host_bytes = 2 * req_bytes * p->h_r;
+    p->hbm_bytes = 2 * req_bytes * (B - p->h_r);
+    dak_status st = alloc_tiers(p);
+    if (st != DAK_OK) {
+        free_parts(p);
+        delete p;
+        return st;
+    }
+    const int D16 = D / 8;
+    const int batch = std::max(1, static_cast<int>((256ll << 20) / req_bytes));
+    void* tmp = nullptr;
+    cudaError_t e = cudaSuccess;
+    if (!src_on_device) {
+        e = cudaMalloc(&tmp, static_cast<size_t>(std::min(batch, B)) * req_bytes);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            free_parts(p);
+            delete p;
+            return DAK_ERR_DEVICE_ALLOC;
+        }
+    }
+    for (int kv = 0; kv < 2 && e == cudaSuccess; ++kv) {
+        const uint8_t* srcb = static_cast<const uint8_t*>(kv == 0 ? K_src : V_src);
+        int nb = 0;
+        for (int b0 = 0; b0 < B && e == cudaSuccess; b0 += nb) {
+            // keep a batch within one tier
+            nb = std::min(batch, B - b0);
+            if (b0 < p->h_r) nb = std::min(nb, p->h_r - b0);
+            const uint4* src;
+            if (src_on_device) {
+                src = reinterpret_cast<const uint4*>(srcb + static_cast<long long>(b0) * req_bytes);
+            } else {
+                e = cudaMemcpy(tmp, srcb + static_cast<long long>(b0) * req_bytes, static_cast<size_t>(nb) * req_bytes,
+                               cudaMemcpyHostToDevice);
+                src = reinterpret_cast<const uint4*>(tmp);
+            }
+            if (e != cudaSuccess) break;
+            const bool host = b0 < p->h_r;
+            const int n_tier = host ? p->h_r : B - p->h_r;
+            const int lb = host ? b0 : b0 - p->h_r;
+            uint8_t* tier = static_cast<uint8_t*>(host ? p->host_dev : p->hbm_ptr);
+            uint8_t* dstb = tier + static_cast<long long>(kv) * req_bytes * n_tier + static_cast<long long>(lb) * req_bytes;
+            const long long units = static_cast<long long>(nb) * req_bytes / 16;
+            pack_kv_kernel<<<pack_grid(units), 256>>>(src, units, D16, L, reinterpret_cast<uint4*>(dstb));
+            e = cudaGetLastError();
+            if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        }
+    }
+    if (tmp) cudaFree(tmp);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        free_parts(p);
+        delete p;
+        return DAK_ERR_CUDA;
+    }
+    p->kv_tier_half = 0;  // per-tier offset of V is req_bytes * (requests in that tier)
+    *out = p;
+    return DAK_OK;
+}
+
+extern "C" dak_status dak_free(dak_placement* p) {
+    if (!p) return DAK_OK;
+    free_parts(p);
+    delete p;
+    return DAK_OK;
+}
+
+extern "C" dak_status dak_placement_info(const dak_placement* p, int64_t* host_bytes, int64_t* hbm_bytes,
+                                         int64_t* units, int64_t* host_units) {
+    if (!p) return DAK_ERR_INVALID;
+    if (host_bytes) *host_bytes = p->host_bytes;
+    if (hbm_bytes) *hbm_bytes = p->hbm_bytes;
+    if (units) *units = p->kind == 0 ? p->T : p->B;
+    if (host_units) *host_units = p->kind == 0 ? p->h : p->h_r;
+    return DAK_OK;
+}
+
+extern "C" dak_status dak_last_error(void* stream, uint64_t* info) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return DAK_ERR_CUDA;
+    DevStatus* st = status_ptr();
+    if (!st) return DAK_ERR_CUDA;
+    DevStatus h{};
+    if (cudaMemcpy(&h, st, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return DAK_ERR_CUDA;
+    if (h.code) {
+        const DevStatus zero{};
+        cudaMemcpy(st, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    }
+    if (info) *info = h.info;
+    return static_cast<dak_status>(h.code);
+}
+
+extern "C" int dak_sm_count(void) { return device_sm_count(); }
+
+// ------------------------------------------------------------------------------------
+// tier read-stream probes (Fig. 7 experiments)
+// ------------------------------------------------------------------------------------
+namespace dak {
+
+struct ProbeArgs {
+    const uint8_t* buf[2];  // [0] host mapping, [1] HBM
+    long long bytes[2];
+    int ctas[2];
+    int window[2];
+    int chunk;
+    int method;        // 0 bulk into smem, 1 ld.global.nc.v4, 2 tensor-map 2-D copy
+    int verify;        // sum the words read
+    unsigned long long* sums;     // per CTA
+    unsigned long long* t_start;  // per CTA, globaltimer ns
+    unsigned long long* t_end;
+    DevStatus* st;
+};
+
+constexpr int kProbeThreads = 256;
+
+__global__ void __launch_bounds__(kProbeThreads) probe_kernel(const ProbeArgs a, const __grid_constant__ CUtensorMap map) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ uint64_t full[16];
+    __shared__ int abort_flag;
+    volatile int* abort = &abort_flag;
+    const int tier = blockIdx.x < a.ctas[0] ? 0 : 1;
+    const int cta = tier == 0 ? blockIdx.x : blockIdx.x - a.ctas[0];
+    const int nctas = a.ctas[tier];
+    const int W = a.window[tier];
+    const long long nchunks = a.bytes[tier] / a.chunk;
+    const uint8_t* buf = a.buf[tier];
+    unsigned long long sum = 0;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int s = 0; s < W; ++s) mbar_init(&full[s], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const unsigned long long t0 = globaltimer();
+    if (a.method == 1) {
+        // every thread streams 16-byte non-coherent loads, `W` in flight
+        const long long n16 = a.bytes[tier] / 16;
+        const long long stride = static_cast<long long>(nctas) * kProbeThreads;
+        for (long long base = static_cast<long long>(cta) * kProbeThreads + threadIdx.x; base < n16;
+             base += stride * W) {
+            uint4 v[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const long long idx = base + u * stride;
+                if (u < W && idx < n16) v[u] = ld_nc_v4(buf + idx * 16);
+            }
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const long long idx = base + u * stride;
+                if (u < W && idx < n16) sum += static_cast<unsigned long long>(v[u].x) + v[u].y + v[u].z + v[u].w;
+            }
+        }
+    } else {
+        long long i = 0;
+        for (long long c = cta; c < nchunks; c += nctas, ++i) {
+            const int s = static_cast<int>(i % W);
+            if (threadIdx.x == 0) {
+                if (i >= W) {
+                    // slot reuse: the consumer side below waited for it already
+                }
+                mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(a.chunk));
+                if (a.method == 0) {
+                    bulk_g2s(smem + static_cast<size_t>(s) * a.chunk, buf + c * a.chunk, static_cast<uint32_t>(a.chunk),
+                             &full[s], policy_evict_first());
+                } else {
+                    // view: rows of 512 bytes (256 bf16); one box = chunk / 512 rows
+                    const int rows = a.chunk / 512;
+                    tma_load_2d(smem + static_cast<size_t>(s) * a.chunk, &map, 0, static_cast<int>(c * rows),
+                                &full[s]);
+                }
+            }
+            // keep W chunks in flight: wait for the chunk issued W-1 iterations ago
+            if (i >= W - 1) {
+                const long long j = i - (W - 1);
+                const int sj = static_cast<int>(j % W);
+                if (!mbar_wait(&full[sj], static_cast<uint32_t>((j / W) & 1), abort, a.st, DAK_ERR_TIMEOUT, 100)) break;
+                if (a.verify) {
+                    const uint32_t* w32 = reinterpret_cast<const uint32_t*>(smem + static_cast<size_t>(sj) * a.chunk);
+                    for (int k = threadIdx.x; k < a.chunk / 4; k += kProbeThreads) sum += w32[k];
+                }
+                __syncthreads();  // slot sj may be refilled next iteration
+            }
+        }
+        // drain the last W-1 chunks (bounded waits that ignore the abort flag)
+        const long long issued = i;
+        volatile int drain_flag = 0;
+        for (long long j = issued > W - 1 ? issued - (W - 1) : 0; j < issued; ++j) {
+            const int sj = static_cast<int>(j % W);
+            if (!mbar_wait(&full[sj], static_cast<uint32_t>((j / W) & 1), &drain_flag, a.st, DAK_ERR_TIMEOUT, 101)) break;
+            if (a.verify) {
+                const uint32_t* w32 = reinterpret_cast<const uint32_t*>(smem + static_cast<size_t>(sj) * a.chunk);
+                for (int k = threadIdx.x; k < a.chunk / 4; k += kProbeThreads) sum += w32[k];
+            }
+        }
+    }
+    // block reduction of the checksum
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    __shared__ unsigned long long red[kProbeThreads / 32];
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = sum;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned long long s = 0;
+        for (int k = 0; k < kProbeThreads / 32; ++k) s += red[k];
+        a.sums[blockIdx.x] = s;
+        a.t_start[blockIdx.x] = t0;
+        a.t_end[blockIdx.x] = globaltimer();
+    }
+}
+
+__global__ void fill_pattern_kernel(uint32_t* p, long long n, long long offset) {
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        p[i] = static_cast<uint32_t>((offset + i) * 2654435761ull);
+    }
+}
+
+static unsigned long long pattern_sum(long long n_words) {
+    unsigned long long s = 0;
+    for (long long i = 0; i < n_words; ++i) s += static_cast<uint32_t>(i * 2654435761ull);
+    return s;
+}
+
+using EncodeTiledFn = PFN_cuTensorMapEncodeTiled_v12000;
+static EncodeTiledFn probe_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess) {
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+        }
+    });
+    return fn;
+}
+
+struct ProbeBuffers {
+    void* host = nullptr;
+    void* host_dev = nullptr;
+    void* hbm = nullptr;
+    long long host_bytes = 0, hbm_bytes = 0;
+    ~ProbeBuffers() {
+        if (host) cudaFreeHost(host);
+        if (hbm) cudaFree(hbm);
+    }
+};
+
+static dak_status probe_alloc(ProbeBuffers& b, long long host_bytes, long long hbm_bytes) {
+    if (host_bytes > 0) {
+        if (cudaHostAlloc(&b.host, host_bytes, cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess) {
+            cudaGetLastError();
+            b.host = nullptr;
+            return DAK_ERR_HOST_ALLOC;
+        }
+        cudaHostGetDevicePointer(&b.host_dev, b.host, 0);
+        b.host_bytes = host_bytes;
+        uint32_t* w = static_cast<uint32_t*>(b.host);
+        const long long n = host_bytes / 4;
+        for (long long i = 0; i < n; ++i) w[i] = static_cast<uint32_t>(i * 2654435761ull);
+    }
+    if (hbm_bytes > 0) {
+        if (cudaMalloc(&b.hbm, hbm_bytes) != cudaSuccess) {
+            cudaGetLastError();
+            b.hbm = nullptr;
+            return DAK_ERR_DEVICE_ALLOC;
+        }
+        b.hbm_bytes = hbm_bytes;
+        fill_pattern_kernel<<<1024, 256>>>(static_cast<uint32_t*>(b.hbm), hbm_bytes / 4, 0);
+        if (cudaDeviceSynchronize() != cudaSuccess) return DAK_ERR_CUDA;
+    }
+    return DAK_OK;
+}
+
+// Run the probe kernel `iters` times; per tier keep the best bandwidth (bytes / busy span).
+static dak_status probe_run(ProbeBuffers& b, int method, int host_ctas, int host_window, int hbm_ctas, int hbm_window,
+                            int chunk, int iters, double* gbps_host, double* gbps_hbm, int* ok) {
+    ProbeArgs a{};
+    a.buf[0] = static_cast<const uint8_t*>(b.host_dev);
+    a.buf[1] = static_cast<const uint8_t*>(b.hbm);
+    a.bytes[0] = host_ctas > 0 ? (b.host_bytes / chunk) * chunk : 0;
+    a.bytes[1] = hbm_ctas > 0 ? (b.hbm_bytes / chunk) * chunk : 0;
+    a.ctas[0] = host_ctas;
+    a.ctas[1] = hbm_ctas;
+    a.window[0] = std::max(1, std::min(host_window, 16));
+    a.window[1] = std::max(1, std::min(hbm_window, 16));
+    a.chunk = chunk;
+    a.method = method;
+    a.st = status_ptr();
+    if (!a.st) return DAK_ERR_CUDA;
+    const int grid = host_ctas + hbm_ctas;
+    if (grid <= 0) return DAK_ERR_INVALID;
+    std::vector<unsigned long long> h_sums(grid), h_t0(grid), h_t1(grid);
+    unsigned long long* d = nullptr;
+    if (cudaMalloc(&d, sizeof(unsigned long long) * 3 * grid) != cudaSuccess) return DAK_ERR_DEVICE_ALLOC;
+    a.sums = d;
+    a.t_start = d + grid;
+    a.t_end = d + 2 * grid;
+    alignas(64) CUtensorMap map;
+    std::memset(&map, 0, sizeof(map));
+    if (method == 2) {
+        EncodeTiledFn enc = probe_encode_fn();
+        const uint8_t* tbuf = host_ctas > 0 ? a.buf[0] : a.buf[1];
+        const long long tbytes = host_ctas > 0 ? a.bytes[0] : a.bytes[1];
+        if (!enc || (host_ctas > 0 && hbm_ctas > 0) || chunk % 512 || chunk / 512 > 256) {
+            cudaFree(d);
+            return DAK_ERR_UNSUPPORTED;
+        }
+        cuuint64_t dims[2] = {256, static_cast<cuuint64_t>(tbytes / 512)};
+        cuuint64_t strides[1] = {512};
+        cuuint32_t box[2] = {256, static_cast<cuuint32_t>(chunk / 512)};
+        cuuint32_t estr[2] = {1, 1};
+        if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint8_t*>(tbuf), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+            cudaFree(d);
+            return DAK_ERR_UNSUPPORTED;  // the tensor map does not encode over this memory
+        }
+    }
+    const int smem = method == 1 ? 0 : std::max(a.window[0], a.window[1]) * chunk;
+    if (smem > 220 * 1024) {
+        cudaFree(d);
+        return DAK_ERR_INVALID;
+    }
+    cudaFuncSetAttribute(probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    double best[2] = {0, 0};
+    int data_ok = 1;
+    for (int it = 0; it < iters + 1; ++it) {
+        a.verify = (it == 0) ? 1 : 0;
+        probe_kernel<<<grid, kProbeThreads, smem>>>(a, map);
+        cudaError_t e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) {
+            cudaFree(d);
+            return DAK_ERR_CUDA;
+        }
+        cudaMemcpy(h_sums.data(), a.sums, sizeof(unsigned long long) * grid, cudaMemcpyDeviceToHost);
+        cudaMemcpy(h_t0.data(), a.t_start, sizeof(unsigned long long) * grid, cudaMemcpyDeviceToHost);
+        cudaMemcpy(h_t1.data(), a.t_end, sizeof(unsigned long long) * grid, cudaMemcpyDeviceToHost);
+        for (int tier = 0; tier < 2; ++tier) {
+            const int lo = tier == 0 ? 0 : host_ctas, hi = tier == 0 ? host_ctas : grid;
+            if (hi <= lo || a.bytes[tier] == 0) continue;
+            unsigned long long mn = ~0ull, mx = 0, s = 0;
+            for (int k = lo; k < hi; ++k) {
+                mn = std::min(mn, h_t0[k]);
+                mx = std::max(mx, h_t1[k]);
+                s += h_sums[k];
+            }
+            if (it == 0) {
+                if (s != pattern_sum(a.bytes[tier] / 4)) data_ok = 0;
+                continue;
+            }
+            const double gbps = mx > mn ? static_cast<double>(a.bytes[tier]) / static_cast<double>(mx - mn) : 0.0;
+            best[tier] = std::max(best[tier], gbps);
+        }
+    }
+    cudaFree(d);
+    if (gbps_host) *gbps_host = best[0];
+    if (gbps_hbm) *gbps_hbm = best[1];
+    if (ok) *ok = data_ok;
+    DevStatus h{};
+    cudaMemcpy(&h, a.st, sizeof(h), cudaMemcpyDeviceToHost);
+    if (h.code) {
+        const DevStatus zero{};
+        cudaMemcpy(a.st, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+        return static_cast<dak_status>(h.code);
+    }
+    return DAK_OK;
+}
+
+}  // namespace dak
+
+extern "C" dak_status dak_probe_read_bw(int tier, int64_t bytes, int method, int ctas, int window, int chunk_bytes,
+                                        int iters, double* gbps_out, int* data_ok_out) {
+    if ((tier != 0 && tier != 1) || bytes <= 0 || ctas <= 0 || window <= 0 || chunk_bytes < 16 ||
+        (chunk_bytes % 16) || method < 0 || method > 2 || iters <= 0)
+        return DAK_ERR_INVALID;
+    dak::ProbeBuffers b;
+    dak_status st = dak::probe_alloc(b, tier == 0 ? bytes : 0, tier == 1 ? bytes : 0);
+    if (st != DAK_OK) return st;
+    double h = 0, g = 0;
+    st = dak::probe_run(b, method, tier == 0 ? ctas : 0, window, tier == 1 ? ctas : 0, window, chunk_bytes, iters, &h,
+                        &g, data_ok_out);
+    if (gbps_out) *gbps_out = tier == 0 ? h : g;
+    return st;
+}
+
+extern "C" dak_status dak_probe_concurrent(int64_t host_bytes, int64_t hbm_bytes, int host_ctas, int host_window,
+                                           int hbm_ctas, int hbm_window, int chunk_bytes, int iters, double* host_gbps,
+                                           double* hbm_gbps) {
+    if (host_bytes <= 0 || hbm_bytes <= 0 || host_ctas < 0 || hbm_ctas < 0 || chunk_bytes < 16 ||
+        (chunk_bytes % 16) || iters <= 0)
+        return DAK_ERR_INVALID;
+    dak::ProbeBuffers b;
+    dak_status st = dak::probe_alloc(b, host_bytes, hbm_bytes);
+    if (st != DAK_OK) return st;
+    int ok = 1;
+    return dak::probe_run(b, 0, host_ctas, host_window, hbm_ctas, hbm_window, chunk_bytes, iters, host_gbps, hbm_gbps,
+                          &ok);
+}
+
+extern "C" dak_status dak_prefetch(const dak_placement* p, void* staging, void* stream) {
+    if (!p) return DAK_ERR_INVALID;
+    if (p->host_bytes == 0) return DAK_OK;
+    if (!staging) return DAK_ERR_INVALID;
+    return dak::cuda_status(cudaMemcpyAsync(staging, p->host_ptr, static_cast<size_t>(p->host_bytes),
+                                            cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream)));
+}

@@ -1,0 +1,211 @@
+/*
+ * dak.h -- C ABI of the direct-access tiered-memory decode library (GB300, sm_103a).
+ *
+ * Method: "DAK: Direct-Access-Enabled GPU Memory Offloading with Optimal Efficiency for
+ * LLM Inference" (arXiv 2604.26074v1). Part of each operand lives in pinned,
+ * device-mapped host memory and the rest in HBM; CTAs read each tier straight into
+ * shared memory, with no staging copy in HBM (section 2.4, section 4.1).
+ *
+ * Conventions for every call below:
+ *  - Plain pointers and sizes only. A `stream` argument is a cudaStream_t passed as
+ *    void* (NULL = the legacy default stream).
+ *  - Errors are returned as dak_status at once for bad arguments and launch failures;
+ *    faults found on the device (a bounded wait that ran out, an index check that
+ *    failed) are recorded in a device status word that dak_last_error() reads after
+ *    synchronising the stream. Nothing aborts, throws or prints.
+ *  - Placements (dak_placement) are owned by the library and freed by dak_free().
+ *    Every other buffer (hidden states, outputs, queries, workspace) is owned by the
+ *    caller and must be device memory unless stated otherwise.
+ *  - All GPU work is asynchronous on `stream`. There is no CPU fallback: without a
+ *    CUDA device every GPU call returns DAK_ERR_CUDA.
+ */
+#ifndef DAK_H
+#define DAK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DAK_OK = 0,
+    DAK_ERR_INVALID = 1,      /* bad argument: null pointer, size out of range, wrong placement kind */
+    DAK_ERR_ALIGN = 2,        /* pointer or row pitch not 16-byte aligned, K not a multiple of 8 */
+    DAK_ERR_HOST_ALLOC = 3,   /* pinned, device-mapped host allocation failed */
+    DAK_ERR_DEVICE_ALLOC = 4, /* HBM allocation failed */
+    DAK_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed (no device, launch error, ...) */
+    DAK_ERR_TIMEOUT = 6,      /* a kernel's bounded wait ran out (reported by dak_last_error) */
+    DAK_ERR_UNSUPPORTED = 7,  /* valid but not implemented shape (tile_m != 64, head dim not 64/128) */
+    DAK_ERR_BOUNDS = 8        /* a kernel's index check failed (reported by dak_last_error) */
+} dak_status;
+
+const char* dak_status_string(int status);
+
+/* Opaque, library-owned placement of one operand across the two memory tiers. */
+typedef struct dak_placement dak_placement;
+
+/* Launch tuning. Any field <= 0 takes the library default.
+ *   host_ctas : CTAs that read host-resident tiles/requests; caps the number of SMs
+ *               issuing host requests (section 4.3.1, "Congestion Control Strategy").
+ *   window    : in-flight chunks per host CTA, the static congestion window (section 4.3.1).
+ *   hbm_window: in-flight chunks per HBM CTA.
+ *   chunk_k   : GEMM chunk width along K in elements (multiple of 64), the TMA chunk size
+ *               exposed as a tunable in section 5 ("Cross-Architecture Adaptation").
+ *   n_split   : attention context splits per (request, kv head); fixed per call and
+ *               independent of the placement, so results do not depend on the offload ratio.
+ *   hbm_ctas  : cap on CTAs reading HBM (0 = every remaining SM).
+ */
+typedef struct {
+    int host_ctas;
+    int window;
+    int hbm_window;
+    int chunk_k;
+    int n_split;
+    int hbm_ctas;
+} dak_tuning;
+
+/* ---------------------------------------------------------------------------------- *
+ * Placement (setup, untimed)
+ * ---------------------------------------------------------------------------------- */
+
+/* Place a weight matrix A (M x K, bf16, row-major with row pitch `lda` elements) for
+ * C = A x B. Section 4.1 "Data Partition" and Fig. 5a: A is cut along M into tile rows of
+ * tile_m x K; tile rows 0 .. n_host_tiles-1 go to pinned, device-mapped host memory and
+ * the remaining ceil(M/tile_m) - n_host_tiles rows to HBM.
+ *   A_src        : source data; host memory if src_on_device == 0, else device memory.
+ *                  Read once; the caller keeps ownership.
+ *   tile_m       : 64 (the only tile height implemented).
+ *   n_host_tiles : 0 .. ceil(M/64); the caller turns a ratio x into tiles (the library's
+ *                  own reading is ceil(x * T)).
+ * Requirements: K % 8 == 0, lda % 8 == 0, A_src 16-byte aligned (else DAK_ERR_ALIGN).
+ * Internally each tier stores its tile rows in a k-group-major layout (8 x 8 core
+ * blocks) that the kernels copy into shared memory with single bulk copies.
+ * On success *out holds a new placement (free with dak_free). Synchronous. */
+dak_status dak_place_matrix(const void* A_src, int src_on_device, int64_t M, int64_t K, int64_t lda,
+                            int tile_m, int n_host_tiles, dak_placement** out);
+
+/* Place a KV cache, K and V each [B][H_kv][L][D] bf16 contiguous (the pre-allocated,
+ * per-request static cache of section 5). Section 5 "Supporting FlashAttention": the
+ * cache is split along the batch dimension; requests 0 .. n_host_requests-1 go to pinned,
+ * device-mapped host memory and the rest to HBM, so every request attends within one tier.
+ * Requirements: D in {64, 128}; pointers 16-byte aligned. Synchronous. */
+dak_status dak_place_kv(const void* K_src, const void* V_src, int src_on_device, int B, int H_kv, int L, int D,
+                        int n_host_requests, dak_placement** out);
+
+/* Release a placement (host and HBM parts). NULL is accepted. */
+dak_status dak_free(dak_placement* p);
+
+/* Sizes of a placement: bytes in host memory and in HBM, number of units (tile rows or
+ * requests) and how many are on the host. Any output pointer may be NULL. */
+dak_status dak_placement_info(const dak_placement* p, int64_t* host_bytes, int64_t* hbm_bytes, int64_t* units,
+                              int64_t* host_units);
+
+/* ---------------------------------------------------------------------------------- *
+ * Hot path
+ * ---------------------------------------------------------------------------------- */
+
+/* C = A x B over a tiered placement (SplitK_GEMM; section 4.1 "Kernel over Partitioned
+ * Memory", "Asynchronous TMA Access", Fig. 5b).
+ *   B : hidden states, bf16 [N][K] row-major (device), 16-byte aligned.
+ *   C : output [N][M] row-major (device); bf16 if c_fp32 == 0, else fp32.
+ *   N : 1 .. 256.
+ * One persistent launch: `host_ctas` CTAs stream the host tile rows and the other CTAs
+ * the HBM tile rows; every CTA reads from exactly one tier and writes disjoint rows of
+ * C. Each output row is accumulated in fp32 over K in the same order whatever tier its
+ * tile row is in, so the result does not depend on n_host_tiles. N < 8 runs on CUDA
+ * cores; N >= 8 on the tcgen05 tensor cores. */
+dak_status dak_gemm(const dak_placement* A, const void* B, void* C, int N, int c_fp32, const dak_tuning* tuning,
+                    void* stream);
+
+/* Workspace bytes dak_attn needs for B requests, H_q query heads, head dim D and
+ * n_split context splits (0 when n_split == 1). */
+size_t dak_attn_workspace_bytes(int B, int H_q, int D, int n_split);
+
+/* Single-query decode attention over a request-partitioned KV cache (SplitK_FlashAttn;
+ * section 5). SDPA semantics for one query token per request, no mask:
+ *   o[b,h] = softmax_j(scale * q[b,h] . k[b,g,j]) v[b,g,j],  g = h / (H_q / H_kv), j < L_b
+ *   Q        : bf16 [B][H_q][D] (device).
+ *   seq_lens : int32 [B] (device) with 1 <= L_b <= L, or NULL for all L.
+ *   scale    : softmax scale; <= 0 means 1/sqrt(D).
+ *   O        : bf16 [B][H_q][D] (device).
+ *   workspace: device scratch of dak_attn_workspace_bytes(B, H_q, D, n_split) bytes
+ *              (NULL allowed when that is 0), caller-owned; its contents on entry do
+ *              not matter.
+ * Requires H_q a multiple of H_kv with H_q / H_kv <= 16. */
+dak_status dak_attn(const void* Q, const dak_placement* KV, const int* seq_lens, int H_q, float scale, void* O,
+                    void* workspace, size_t ws_bytes, const dak_tuning* tuning, void* stream);
+
+/* The n_split dak_attn uses for a placement when tuning->n_split <= 0. */
+int dak_attn_default_split(const dak_placement* KV);
+
+/* ---------------------------------------------------------------------------------- *
+ * Planner (host only; section 4.2 and Appendix A)
+ * ---------------------------------------------------------------------------------- */
+typedef struct {
+    double bytes;      /* C_i: bytes of weights or KV the operation reads */
+    double t_comp;     /* T_comp,i: pure compute time, seconds */
+    double tile_bytes; /* placement granularity in bytes (tile row or request); <= 0: continuous */
+} dak_op;
+
+/* Per-operation offload ratios minimising sum_i max(T_comp,i, (1-x_i) C_i / B_hbm,
+ * x_i C_i / B_host) subject to sum_i x_i C_i >= min_offload_bytes (mode 0, the capacity
+ * constraint) or == min_offload_bytes (mode 1, eq. (1) of Appendix A).
+ * mode 0 and 1 solve the continuous problem with the paper's three greedy phases
+ * (memory-bound operations up to their peaks, compute-bound operations up to their
+ * thresholds, then any split). mode 2 solves the ">=" problem exactly over whole tiles
+ * (x_i C_i a multiple of tile_bytes, capped at C_i) by dynamic programming.
+ * Outputs: ratios_out[n] (x_i), model_time_out (objective, seconds; may be NULL).
+ * DAK_ERR_INVALID if the budget exceeds sum C_i or an argument is out of range. */
+dak_status dak_plan_ratios(const dak_op* ops, int n, double b_host, double b_hbm, double min_offload_bytes,
+                           int mode, double* ratios_out, double* model_time_out);
+
+/* ---------------------------------------------------------------------------------- *
+ * Errors, device info, measurement helpers
+ * ---------------------------------------------------------------------------------- */
+
+/* Synchronise `stream`, then read and clear the device status word. Returns DAK_OK,
+ * DAK_ERR_TIMEOUT or DAK_ERR_BOUNDS (with *info, if not NULL, holding a location code). */
+dak_status dak_last_error(void* stream, uint64_t* info);
+
+/* SM count of the current device. */
+int dak_sm_count(void);
+
+/* Read-stream microbenchmark of one tier (the SM read paths the kernels use; section
+ * 4.3.1 Fig. 7). Reads `bytes` from a library-allocated buffer in host memory (tier 0)
+ * or HBM (tier 1) with `ctas` CTAs and `window` chunks of `chunk_bytes` in flight each,
+ * `iters` times. method 0: bulk asynchronous copies into shared memory; method 1:
+ * 16-byte non-coherent loads into registers; method 2: 2-D tensor-map copies.
+ * Outputs the best GB/s over the iterations and whether the data read back correctly.
+ * Synchronous. */
+dak_status dak_probe_read_bw(int tier, int64_t bytes, int method, int ctas, int window, int chunk_bytes,
+                             int iters, double* gbps_out, int* data_ok_out);
+
+/* The congestion experiment of Fig. 7: `host_ctas` CTAs read host memory while
+ * `hbm_ctas` CTAs read HBM, concurrently, with the given windows. Outputs each tier's
+ * bandwidth in GB/s (bytes of that tier / that tier's busy time). Synchronous. */
+dak_status dak_probe_concurrent(int64_t host_bytes, int64_t hbm_bytes, int host_ctas, int host_window,
+                                int hbm_ctas, int hbm_window, int chunk_bytes, int iters, double* host_gbps,
+                                double* hbm_gbps);
+
+/* Prefetch baseline (section 2.2-2.3, Fig. 2-3): copy a placement's host-resident part into
+ * a caller-provided HBM staging buffer (cudaMemcpyAsync on `stream`), so that a following
+ * dak_gemm_staged / dak_attn_staged call reads every tile from HBM. staging must hold
+ * the placement's host bytes. */
+dak_status dak_prefetch(const dak_placement* p, void* staging, void* stream);
+
+/* dak_gemm / dak_attn with the host-resident tiles or requests read from `staging`
+ * (filled by dak_prefetch) instead of host memory: the all-HBM half of the prefetch
+ * baseline. */
+dak_status dak_gemm_staged(const dak_placement* A, const void* staging, const void* B, void* C, int N, int c_fp32,
+                           const dak_tuning* tuning, void* stream);
+dak_status dak_attn_staged(const void* Q, const dak_placement* KV, const void* staging, const int* seq_lens,
+                           int H_q, float scale, void* O, void* workspace, size_t ws_bytes,
+                           const dak_tuning* tuning, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DAK_H */

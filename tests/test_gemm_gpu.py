@@ -1,0 +1,156 @@
+"""SplitK_GEMM on the GPU against the CPU oracle, through the C ABI."""
+import numpy as np
+import pytest
+
+import synth
+from gpu_util import FP32_OUT_TOL, REL_TOL, bits_of, to_dev, to_np
+from oracle import bf16 as obf
+from oracle import gemm as og
+from oracle import placement as opl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dak(cuda_ok):
+    import __graft_entry__
+    __graft_entry__.build()
+    import direct_host_memory_gb300 as m
+    return m
+
+
+def _run(dak, A, B, h, fp32=True, tuning=None, device_src=False):
+    import torch
+    src = to_dev(A) if device_src else A
+    p = dak.dak_place_matrix(src, h)
+    C = dak.dak_gemm(p, to_dev(B), c_fp32=fp32, tuning=tuning)
+    st, info = dak.dak_last_error()
+    assert st == 0, f"device status {st} info {info:#x}"
+    p.free()
+    torch.cuda.synchronize()
+    return C
+
+
+def test_gemv_decode_1024(dak):
+    """A 1024x1024 ~N(0,0.02), B 1x1024 ~N(0,1), m = 64, x = 0.25 (4 of 16 tile rows on the host)."""
+    A, B = synth.gemm_inputs(1024, 1024, 1, seed=0)
+    h = opl.n_host_tiles(0.25, 1024, 64)
+    assert h == 4
+    ref = og.gemm_ref(A, B)
+    C32 = _run(dak, A, B, h, fp32=True)
+    assert og.rel_err(to_np(C32), ref) <= FP32_OUT_TOL
+    C16 = _run(dak, A, B, h, fp32=False)
+    assert og.rel_err(to_np(C16), ref) <= REL_TOL
+    # bf16 output is the fp32 result rounded to nearest even
+    assert np.array_equal(bits_of(C16), obf.round_f32_to_bf16(C32.cpu().numpy()))
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 7, 8, 16, 24, 32, 64, 72, 128, 256])
+def test_widths(dak, N):
+    M, K = 320, 1280  # 5 tile rows, 5 chunks of 256 (and 20 of 64)
+    A, B = synth.gemm_inputs(M, K, N, seed=N)
+    ref = og.gemm_ref(A, B)
+    C = _run(dak, A, B, 2)
+    assert og.rel_err(to_np(C), ref) <= FP32_OUT_TOL
+    C16 = _run(dak, A, B, 2, fp32=False)
+    assert og.rel_err(to_np(C16), ref) <= REL_TOL
+
+
+@pytest.mark.parametrize("M,K", [(200, 520), (64, 8), (130, 1000), (1, 16), (65, 4104), (1000, 24)])
+@pytest.mark.parametrize("N", [1, 8, 13])
+def test_ragged_shapes(dak, M, K, N):
+    A, B = synth.gemm_inputs(M, K, N, seed=M + K)
+    T = opl.n_tiles(M, 64)
+    ref = og.gemm_ref(A, B)
+    for h in sorted({0, T // 2, T}):
+        C = _run(dak, A, B, h)
+        assert og.rel_err(to_np(C), ref) <= FP32_OUT_TOL, (h,)
+
+
+@pytest.mark.parametrize("N", [1, 8, 64])
+def test_integer_inputs_bit_exact(dak, N):
+    """Integer-valued bf16 inputs in [-8, 8]: every partial sum is exact in fp32."""
+    M, K = 256, 4096
+    A, B = synth.gemm_inputs(M, K, N, seed=7, integer=True)
+    ref = og.gemm_ref(A, B)
+    C = _run(dak, A, B, 1)
+    assert np.array_equal(to_np(C), ref)
+    C16 = _run(dak, A, B, 1, fp32=False)
+    assert np.array_equal(bits_of(C16), obf.round_f64_to_bf16(ref))
+
+
+@pytest.mark.parametrize("N", [1, 4, 16, 64])
+def test_bit_identical_across_offload_ratio(dak, N):
+    M, K = 640, 2048
+    A, B = synth.gemm_inputs(M, K, N, seed=3)
+    base = bits_of(_run(dak, A, B, 0))
+    for h in range(1, 11):
+        assert np.array_equal(bits_of(_run(dak, A, B, h)), base), h
+
+
+@pytest.mark.parametrize("N", [1, 16])
+def test_bit_identical_across_tuning(dak, N):
+    M, K = 640, 2048
+    A, B = synth.gemm_inputs(M, K, N, seed=4)
+    base = bits_of(_run(dak, A, B, 4))
+    for tun in [dict(host_ctas=1), dict(host_ctas=3, window=1), dict(window=2, hbm_window=2),
+                dict(chunk_k=64), dict(chunk_k=128, hbm_ctas=3)]:
+        assert np.array_equal(bits_of(_run(dak, A, B, 4, tuning=tun)), base), tun
+
+
+def test_device_source_placement(dak):
+    A, B = synth.gemm_inputs(384, 512, 8, seed=5)
+    a = bits_of(_run(dak, A, B, 3))
+    b = bits_of(_run(dak, A, B, 3, device_src=True))
+    assert np.array_equal(a, b)
+
+
+def test_prefetch_staged_equals_direct(dak):
+    import torch
+    A, B = synth.gemm_inputs(512, 1024, 8, seed=6)
+    p = dak.dak_place_matrix(A, 5)
+    Bt = to_dev(B)
+    direct = dak.dak_gemm(p, Bt, c_fp32=True)
+    staging = torch.empty(p.host_bytes, dtype=torch.uint8, device="cuda")
+    dak.dak_prefetch(p, staging)
+    staged = dak.dak_gemm_staged(p, staging, Bt, c_fp32=True)
+    assert dak.dak_last_error()[0] == 0
+    assert torch.equal(direct, staged)
+    p.free()
+
+
+def test_empty_and_errors(dak):
+    import torch
+    A = np.zeros((0, 64), dtype=np.uint16)
+    p = dak.dak_place_matrix(A, 0)
+    assert p.units == 0
+    C = torch.empty((1, 0), dtype=torch.bfloat16, device="cuda")
+    dak.dak_gemm(p, torch.zeros((1, 64), dtype=torch.bfloat16, device="cuda"), C)
+    p.free()
+    A2, _ = synth.gemm_inputs(64, 64, 1)
+    with pytest.raises(dak.DakError):
+        dak.dak_place_matrix(A2, 2)  # more host tiles than tiles
+    with pytest.raises(dak.DakError):
+        dak.dak_place_matrix(np.zeros((64, 60), dtype=np.uint16), 0)  # K % 8 != 0
+    p = dak.dak_place_matrix(A2, 1)
+    with pytest.raises(dak.DakError):
+        dak.dak_gemm(p, torch.zeros((300, 64), dtype=torch.bfloat16, device="cuda"))  # N > 256
+    p.free()
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", list(synth.LINEARS_8B))
+@pytest.mark.parametrize("N", [1, 8, 64])
+def test_8b_linears_full_size_sampled(dak, name, N):
+    """Full-size 8B-shaped linear at x = 0.25, in the bench's launch configuration; 96
+    sampled output rows (all N columns) against the oracle computed row by row."""
+    M, K = synth.LINEARS_8B[name]
+    A, B = synth.gemm_inputs(M, K, N, seed=0, tensor_index=list(synth.LINEARS_8B).index(name))
+    h = opl.n_host_tiles(0.25, M, 64)
+    C = to_np(_run(dak, A, B, h, fp32=False))
+    rows = np.unique(np.concatenate([
+        (synth.uniform_f64(1, 9, 80) * M).astype(int),
+        [0, 63, 64, h * 64 - 1, h * 64, M - 1]]))
+    rows = rows[(rows >= 0) & (rows < M)]
+    ref = og.gemm_ref(A[rows], B)
+    assert og.rel_err(C[:, rows], ref) <= REL_TOL

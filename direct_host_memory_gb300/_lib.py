@@ -26,8 +26,11 @@ EXPORTS = [
     "dak_status_string", "dak_place_matrix", "dak_place_kv", "dak_free", "dak_placement_info",
     "dak_gemm", "dak_attn_workspace_bytes", "dak_attn", "dak_attn_default_split", "dak_plan_ratios",
     "dak_last_error", "dak_sm_count", "dak_probe_read_bw", "dak_probe_concurrent", "dak_prefetch",
-    "dak_gemm_staged", "dak_attn_staged",
+    "dak_gemm_staged", "dak_attn_staged", "dak_attn_noalloc",
 ]
+
+# size of the fixed device array dak_attn_noalloc uses (DAK_NOALLOC_SCRATCH_BYTES in dak.h)
+NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
 class DakError(RuntimeError):
@@ -70,6 +73,7 @@ def _load():
         "dak_probe_read_bw": (i32, [i32, i64, i32, i32, i32, i32, i32, P(dbl), P(i32)]),
         "dak_probe_concurrent": (i32, [i64, i64, i32, i32, i32, i32, i32, i32, P(dbl), P(dbl)]),
         "dak_prefetch": (i32, [vp, vp, vp]),
+        "dak_attn_noalloc": (i32, [vp, vp, vp, i32, ctypes.c_float, vp, P(dak_tuning), vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -271,6 +275,30 @@ def dak_attn_staged(Q, KV: Placement, staging, seq_lens=None, scale: float = 0.0
     Hq, O, workspace, ws_len, tun = _attn_common(Q, KV, O, workspace, tuning)
     _check(lib.dak_attn_staged(_ptr(Q), KV.handle, _ptr(staging), _ptr(seq_lens), Hq, float(scale), _ptr(O),
                                _ptr(workspace), ws_len, _tuning(tun), _stream_ptr(stream)), "dak_attn_staged")
+    return O
+
+
+def dak_attn_noalloc(Q, KV: Placement, O, seq_lens=None, scale: float = 0.0, tuning=None, stream=None):
+    """dak_attn without a workspace argument, for callers that cannot allocate device memory
+    (an engine whose pools already hold the device's memory, code without access to the
+    process's allocator, a loop where an allocation would synchronise the device). The
+    library takes the split workspace from its fixed NOALLOC_SCRATCH_BYTES device array,
+    shared by all calls: calls that overlap on the GPU race on it. O must be preallocated."""
+    _check_bf16_cuda(Q, "Q")
+    _check_bf16_cuda(O, "O")
+    B, Hq, D = (int(s) for s in Q.shape)
+    if B != KV.meta["B"] or D != KV.meta["D"] or tuple(O.shape) != tuple(Q.shape):
+        raise ValueError("Q / O do not match the KV placement")
+    tun = tuning if isinstance(tuning, dak_tuning) else dict(tuning or {})
+    n_split = tun.n_split if isinstance(tun, dak_tuning) else int(tun.get("n_split", 0) or 0)
+    if n_split <= 0:
+        n_split = dak_attn_default_split(KV)
+    need = dak_attn_workspace_bytes(B, Hq, D, n_split)
+    if need > NOALLOC_SCRATCH_BYTES:
+        raise DakError(1, f"dak_attn_noalloc: needs {need} bytes of workspace, more than the fixed "
+                          f"{NOALLOC_SCRATCH_BYTES}-byte array; use dak_attn with a workspace")
+    _check(lib.dak_attn_noalloc(_ptr(Q), KV.handle, _ptr(seq_lens), Hq, float(scale), _ptr(O), _tuning(tuning),
+                                _stream_ptr(stream)), "dak_attn_noalloc")
     return O
 
 

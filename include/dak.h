@@ -140,6 +140,31 @@ dak_status dak_attn(const void* Q, const dak_placement* KV, const int* seq_lens,
 /* The n_split dak_attn uses for a placement when tuning->n_split <= 0. */
 int dak_attn_default_split(const dak_placement* KV);
 
+/* Size of the fixed device array dak_attn_noalloc takes its workspace from: 4 MiB per
+ * device (enough for B * H_q * n_split <= 8065 rows at D = 128, e.g. 32 requests x 32
+ * heads x 4 splits). */
+#define DAK_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* dak_attn for callers that cannot allocate device memory. The paper has no counterpart;
+ * this is a library convenience. An engine that has already reserved the device's memory
+ * for its own pools, code without access to the process's allocator, or a latency-critical
+ * loop where cudaMalloc / cudaFree would synchronise the device can call this instead:
+ * it allocates nothing (no cudaMalloc, cudaFree or allocating library call) and takes the
+ * split workspace from a fixed array of DAK_NOALLOC_SCRATCH_BYTES compiled into the
+ * library, which every device that loads the library's device code holds until exit.
+ *   Arguments: as dak_attn, without workspace / ws_bytes. Q, O and seq_lens stay
+ *   caller-owned device buffers.
+ *   Errors: DAK_ERR_INVALID when the call would need more than DAK_NOALLOC_SCRATCH_BYTES
+ *   (dak_attn_workspace_bytes(B, H_q, D, n_split) > DAK_NOALLOC_SCRATCH_BYTES); use
+ *   dak_attn with a caller-provided workspace, or a smaller n_split, then.
+ *   The first call on a device looks up the array's device address (cudaGetSymbolAddress,
+ *   with that device current) and keeps it; make that first call before any stream
+ *   capture. All calls share the array and it keeps the last call's contents (nothing in
+ *   it has to start at zero): calls that overlap on the GPU race on it, so order them on
+ *   one stream or with events. */
+dak_status dak_attn_noalloc(const void* Q, const dak_placement* KV, const int* seq_lens, int H_q, float scale,
+                            void* O, const dak_tuning* tuning, void* stream);
+
 /* ---------------------------------------------------------------------------------- *
  * Planner (host only; section 4.2 and Appendix A)
  * ---------------------------------------------------------------------------------- */

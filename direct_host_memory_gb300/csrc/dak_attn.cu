@@ -16,9 +16,10 @@
 // with online softmax in fp32 (base-2 exponentials, the scale folded with log2 e).
 // Partial results of the splits are merged by a log-sum-exp combine in fixed order.
 //
-// KV placement layout: [requests of the tier][H_kv][L][D] bf16 for K, the same for V after
-// it; inside every token row the 16-byte chunk c is stored at c ^ (token & 7) so that
-// ldmatrix reads of 8 consecutive tokens hit 8 different bank groups.
+// KV placement layout: per tier [requests][H_kv] slabs; a slab is ceil(L/64) chunks of 64
+// tokens stored [K 64 x D][V 64 x D] bf16 (last chunk zero-padded), so that one bulk copy
+// brings a whole stage; inside every token row the 16-byte piece c sits at c ^ (token & 7)
+// so that ldmatrix reads of 8 consecutive tokens hit 8 different bank groups.
 #include <algorithm>
 #include <cmath>
 
@@ -29,13 +30,12 @@ namespace dak {
 struct AttnParams {
     const __nv_bfloat16* Q;  // [B][Hq][D]
     const uint8_t* kv[2];    // [0] host tier (device-visible), [1] HBM tier
-    long long v_off[2];      // offset of the V block inside each tier
     const int* seq_lens;
     __nv_bfloat16* O;        // [B][Hq][D]
     float* ws;               // [B][Hq][n_split][D + 2] partials: m (log2 domain), l, o[D]
     int B, Hq, Hkv, G, L, h_r, n_split, split_len;
     float scale_log2;
-    long long head_bytes;    // L * D * 2
+    long long head_bytes;    // bytes of one (request, kv head) slab
     int n_host_ctas, n_hbm_ctas, host_window, hbm_window;
     long long host_units, hbm_units;
     DevStatus* st;
@@ -72,8 +72,7 @@ __device__ __forceinline__ UnitRange units_of_cta(const AttnParams& p) {
 struct Unit {
     int b, g, s;
     int t0, t1;  // token range
-    const uint8_t* kbase;
-    const uint8_t* vbase;
+    const uint8_t* base;  // the (request, kv head) slab
 };
 
 __device__ __forceinline__ Unit decode_unit(const AttnParams& p, long long u, int tier) {
@@ -89,8 +88,7 @@ __device__ __forceinline__ Unit decode_unit(const AttnParams& p, long long u, in
     x.t1 = min(Lb, x.t0 + p.split_len);
     const int lb = tier == 0 ? x.b : x.b - p.h_r;
     const long long head = static_cast<long long>(lb) * p.Hkv + x.g;
-    x.kbase = p.kv[tier] + head * p.head_bytes;
-    x.vbase = p.kv[tier] + p.v_off[tier] + head * p.head_bytes;
+    x.base = p.kv[tier] + head * p.head_bytes;
     return x;
 }
 
@@ -101,7 +99,7 @@ __device__ __forceinline__ void named_bar_consumers() {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnParams p) {
     constexpr int KS = D / 16;                       // k-steps of the score MMA
     constexpr int NB = D / 8;                        // 8-wide column blocks of O
     constexpr int CHUNK_BYTES = kChunkTok * D * 2;   // K (or V) bytes of one chunk
@@ -114,13 +112,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const UnitRange ur = units_of_cta(p);
     const int W = ur.window;
-    float* comb = reinterpret_cast<float*>(smem + static_cast<size_t>(W) * STAGE);  // [4 warps][16][D + 2]
+    float* comb = reinterpret_cast<float*>(smem + static_cast<size_t>(W) * STAGE);  // [4 warps][G][D + 2]
 
-    // zero the ring once so that stale lanes of a ragged last chunk hold finite values
-    for (int i = threadIdx.x; i < W * STAGE / 16; i += blockDim.x) {
-        reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
-    }
-    fence_proxy_async_smem();
     if (threadIdx.x == 0) {
         abort_flag = 0;
         for (int s = 0; s < W; ++s) {
@@ -143,12 +136,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
                                              DAK_ERR_TIMEOUT, A_PROD_EMPTY)) {
                         goto producer_done;
                     }
-                    const int nt = min(kChunkTok, x.t1 - t);
-                    const uint32_t bytes = static_cast<uint32_t>(nt * D * 2);
                     uint8_t* dst = smem + static_cast<size_t>(s) * STAGE;
-                    mbar_arrive_expect_tx(&full[s], 2 * bytes);
-                    bulk_g2s(dst, x.kbase + static_cast<long long>(t) * D * 2, bytes, &full[s], pol);
-                    bulk_g2s(dst + CHUNK_BYTES, x.vbase + static_cast<long long>(t) * D * 2, bytes, &full[s], pol);
+                    mbar_arrive_expect_tx(&full[s], STAGE);
+                    bulk_g2s(dst, x.base + static_cast<long long>(t / kChunkTok) * STAGE, STAGE, &full[s], pol);
                 }
             }
         producer_done:
@@ -286,20 +276,30 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
         l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
         l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
         l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
-        float* cw = comb + static_cast<size_t>(w) * 16 * (D + 2);
+        float* cw = comb + static_cast<size_t>(w) * p.G * (D + 2);
+        if (ra < p.G) {
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-            const int d = nb * 8 + 2 * q4;
-            cw[ra * (D + 2) + d] = o[nb][0];
-            cw[ra * (D + 2) + d + 1] = o[nb][1];
-            cw[(ra + 8) * (D + 2) + d] = o[nb][2];
-            cw[(ra + 8) * (D + 2) + d + 1] = o[nb][3];
+            for (int nb = 0; nb < NB; ++nb) {
+                const int d = nb * 8 + 2 * q4;
+                cw[ra * (D + 2) + d] = o[nb][0];
+                cw[ra * (D + 2) + d + 1] = o[nb][1];
+            }
+            if (q4 == 0) {
+                cw[ra * (D + 2) + D] = m_a;
+                cw[ra * (D + 2) + D + 1] = l_a;
+            }
         }
-        if (q4 == 0) {
-            cw[ra * (D + 2) + D] = m_a;
-            cw[ra * (D + 2) + D + 1] = l_a;
-            cw[(ra + 8) * (D + 2) + D] = m_b;
-            cw[(ra + 8) * (D + 2) + D + 1] = l_b;
+        if (ra + 8 < p.G) {
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+                const int d = nb * 8 + 2 * q4;
+                cw[(ra + 8) * (D + 2) + d] = o[nb][2];
+                cw[(ra + 8) * (D + 2) + d + 1] = o[nb][3];
+            }
+            if (q4 == 0) {
+                cw[(ra + 8) * (D + 2) + D] = m_b;
+                cw[(ra + 8) * (D + 2) + D + 1] = l_b;
+            }
         }
         named_bar_consumers();
         const int ctid = threadIdx.x - 32;
@@ -307,12 +307,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
             const int r = e / D, d = e - r * D;
             float M = -INFINITY;
 #pragma unroll
-            for (int ww = 0; ww < kAttnConsumers; ++ww) M = fmaxf(M, comb[(ww * 16 + r) * (D + 2) + D]);
+            for (int ww = 0; ww < kAttnConsumers; ++ww) M = fmaxf(M, comb[(ww * p.G + r) * (D + 2) + D]);
             const float base = M == -INFINITY ? 0.f : M;
             float acc = 0.f, lsum = 0.f;
 #pragma unroll
             for (int ww = 0; ww < kAttnConsumers; ++ww) {
-                const float* row = comb + (ww * 16 + r) * (D + 2);
+                const float* row = comb + (ww * p.G + r) * (D + 2);
                 const float f = exp2f(row[D] - base);
                 acc += f * row[d];
                 lsum += f * row[D + 1];
@@ -364,7 +364,8 @@ __global__ void attn_combine_kernel(const float* __restrict__ ws, __nv_bfloat16*
 
 constexpr int kAttnDefaultHostCtas = 16;
 constexpr int kAttnDefaultHostWindow = 4;
-constexpr int kAttnStages = 4;
+constexpr int kAttnStages = 3;     // default ring depth: two CTAs fit on an SM
+constexpr int kAttnMaxStages = 5;
 
 static int default_split(int B, int Hkv, int L) {
     const int sms = device_sm_count();
@@ -374,8 +375,27 @@ static int default_split(int B, int Hkv, int L) {
 }
 
 template <int D>
+static int attn_smem_bytes(int W, int G) {
+    return W * 2 * kChunkTok * D * 2 + kAttnConsumers * G * (D + 2) * 4;
+}
+
+// CTAs of this kernel that fit on one SM with the given ring depth (each CTA streams its own
+// copies, so two per SM double the copy streams an SM keeps in flight).
+template <int D>
+static int attn_ctas_per_sm(int W, int G) {
+    int n = 0;
+    const int smem = attn_smem_bytes<D>(W, G);
+    if (cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<D>, kAttnThreads, smem) != cudaSuccess) {
+        cudaGetLastError();
+        return 1;
+    }
+    return std::max(1, n);
+}
+
+template <int D>
 static cudaError_t launch_attn_d(const AttnParams& p, int grid, int W, cudaStream_t s) {
-    const int smem = W * 2 * kChunkTok * D * 2 + kAttnConsumers * 16 * (D + 2) * 4;
+    const int smem = attn_smem_bytes<D>(W, p.G);
     cudaError_t e = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attn_kernel<D><<<grid, kAttnThreads, smem, s>>>(p);
@@ -406,9 +426,6 @@ dak_status launch_attn(const void* Q, const dak_placement* KV, const void* host_
     p.Q = static_cast<const __nv_bfloat16*>(Q);
     p.kv[0] = static_cast<const uint8_t*>(host_src);
     p.kv[1] = static_cast<const uint8_t*>(KV->hbm_ptr);
-    const long long req_bytes = KV->head_bytes * KV->H_kv;
-    p.v_off[0] = req_bytes * KV->h_r;
-    p.v_off[1] = req_bytes * (KV->B - KV->h_r);
     p.seq_lens = seq_lens;
     p.O = static_cast<__nv_bfloat16*>(O);
     p.ws = static_cast<float*>(ws);
@@ -429,8 +446,11 @@ dak_status launch_attn(const void* Q, const dak_placement* KV, const void* host_
     p.hbm_units = static_cast<long long>(KV->B - KV->h_r) * KV->H_kv * n_split;
     const int host_units_i = static_cast<int>(std::min<long long>(p.host_units, 1 << 30));
     const int hbm_units_i = static_cast<int>(std::min<long long>(p.hbm_units, 1 << 30));
-    Sched sc2 = schedule(host_units_i, hbm_units_i, device_sm_count(), t, kAttnDefaultHostCtas, kAttnDefaultHostWindow,
-                         kAttnStages, kAttnStages);
+    int W_ring = (t && t->hbm_window > 0) ? std::min(t->hbm_window, kAttnMaxStages) : kAttnStages;
+    if (t && t->window > 0) W_ring = std::max(W_ring, std::min(t->window, kAttnMaxStages));
+    const int per_sm = KV->D == 128 ? attn_ctas_per_sm<128>(W_ring, G) : attn_ctas_per_sm<64>(W_ring, G);
+    Sched sc2 = schedule(host_units_i, hbm_units_i, device_sm_count() * per_sm, t, kAttnDefaultHostCtas,
+                         std::min(kAttnDefaultHostWindow, W_ring), W_ring, W_ring);
     p.n_host_ctas = sc2.n_host_ctas;
     p.n_hbm_ctas = sc2.n_hbm_ctas;
     p.host_window = sc2.host_window;

@@ -38,6 +38,7 @@ struct GemmParams {
     int c_fp32;
     long long tile_bytes;
     DevStatus* st;
+    int b3d;  // B arrives in one 3-D tensor copy per stage (else several 2-D copies)
 };
 
 // Tiles of this CTA: role, first tile, stride, count.
@@ -77,7 +78,9 @@ __device__ __forceinline__ const uint8_t* tile_src(const GemmParams& p, const Ti
 }
 
 // error location codes (upper 32 bits of the status info)
-enum : uint32_t { W_PROD_EMPTY = 1, W_CONS_FULL = 2, W_MMA_FULL = 3, W_MMA_ACC = 4, W_EPI_ACC = 5, W_DRAIN = 6 };
+enum : uint32_t {
+    W_PROD_EMPTY = 1, W_CONS_FULL = 2, W_MMA_FULL = 3, W_MMA_ACC = 4, W_EPI_ACC = 5, W_DRAIN = 6, W_BPROD_EMPTY = 7
+};
 
 // Wait (bounded, ignoring the abort flag) for the last fill of every ring slot, so that no
 // bulk copy is still writing shared memory when the CTA exits.
@@ -92,13 +95,78 @@ __device__ __forceinline__ void drain_fills(uint64_t* full, int window, long lon
 }
 
 // ======================================================================================
+// Loading B (the hidden states, shared by every CTA and L2-resident). Each stage's B chunk
+// is one tensor-map copy issued by its own thread, so that the stream of A copies is never
+// held up behind several smaller copies (on this GPU every bulk copy costs a CTA a fixed
+// ~0.2-0.4 us, and a CTA's copies overlap only partly).
+//   kUmmaB : 128-byte swizzled K-major blocks [kc/64][N_pad rows][64 columns] (the tcgen05
+//            B operand); a 3-D box {64, N_pad, kc/64} when K % 64 == 0, else kc/64 2-D boxes.
+//   kCoreB : plain blocks [kc/256][N rows][256 columns]; a 3-D box {256, N, kc/256} when
+//            K % 256 == 0, else kc/256 2-D boxes.
+// Columns past K and rows past N read as zero (tensor-map bounds fill).
+// ======================================================================================
+enum BKind { kCoreB = 0, kUmmaB = 1 };
+
+__device__ __forceinline__ void issue_b(const GemmParams& p, const CUtensorMap* bmap, uint8_t* dst, int k0,
+                                        uint64_t* bar, int kind) {
+    const int blk = kind == kUmmaB ? 64 : 256;
+    const int rows = kind == kUmmaB ? p.N_pad : p.N;
+    const int nblk = p.kc / blk;
+    if (p.b3d) {
+        tma_load_3d(dst, bmap, 0, 0, k0 / blk, bar);
+    } else {
+        for (int b = 0; b < nblk; ++b) tma_load_2d(dst + b * rows * blk * 2, bmap, k0 + blk * b, 0, bar);
+    }
+}
+
+__device__ __forceinline__ uint32_t b_stage_bytes(const GemmParams& p, int kind) {
+    return static_cast<uint32_t>(p.kc) * 2u * static_cast<uint32_t>(kind == kUmmaB ? p.N_pad : p.N);
+}
+
+// Producer loops. `is_a` streams the tile rows of A (one bulk copy per stage), otherwise the
+// matching chunk of B. Both wait for the slot to be released and then arm the stage's full
+// barrier with their own byte count.
+__device__ __forceinline__ void produce(const GemmParams& p, const TileIter& it, const CUtensorMap* bmap, uint8_t* smem,
+                                        uint64_t* full, uint64_t* empty, volatile int* abort, bool is_a, int kind) {
+    const int W = it.window;
+    const int nch = (p.K_pad + p.kc - 1) / p.kc;
+    const uint64_t pol_a = policy_evict_first();
+    long long i = 0;
+    for (int ti = 0; ti < it.count && !*abort; ++ti) {
+        const int t = it.first + ti * it.stride;
+        const uint8_t* src = tile_src(p, it, t);
+        for (int c = 0; c < nch; ++c, ++i) {
+            const int s = static_cast<int>(i % W);
+            if (i >= W && !mbar_wait(&empty[s], static_cast<uint32_t>(((i / W) - 1) & 1), abort, p.st,
+                                     DAK_ERR_TIMEOUT, is_a ? W_PROD_EMPTY : W_BPROD_EMPTY)) {
+                goto done;
+            }
+            const int k0 = c * p.kc;
+            uint8_t* dst = smem + static_cast<size_t>(s) * p.stage_bytes;
+            if (is_a) {
+                const uint32_t a_bytes = static_cast<uint32_t>(min(p.kc, p.K_pad - k0)) * 128u;
+                mbar_arrive_expect_tx(&full[s], a_bytes);
+                bulk_g2s(dst, src + static_cast<long long>(k0) * 128, a_bytes, &full[s], pol_a);
+            } else {
+                mbar_arrive_expect_tx(&full[s], b_stage_bytes(p, kind));
+                issue_b(p, bmap, dst + p.kc * 128, k0, &full[s], kind);
+            }
+        }
+    }
+done:
+    drain_fills(full, W, i, p.st);
+}
+
+// ======================================================================================
 // CUDA-core path, N in 1..7: warp-level FMA, fp32 accumulation, shuffle reduction.
-// Warps: 0 = producer, 1..8 = consumers (consumer w owns rows 8w .. 8w+7 of the tile).
+// Warps: 0 = A producer, 1 = B producer, 2..9 = consumers (consumer w owns rows 8w .. 8w+7).
 // ======================================================================================
 constexpr int kCoreConsumers = 8;
+constexpr int kCoreThreads = 32 * (2 + kCoreConsumers);
 
 template <int N>
-__global__ void __launch_bounds__(32 * (1 + kCoreConsumers), 1) gemm_core_kernel(const GemmParams p) {
+__global__ void __launch_bounds__(kCoreThreads, 1)
+    gemm_core_kernel(const GemmParams p, const __grid_constant__ CUtensorMap bmap) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     __shared__ uint64_t full[8], empty[8];
     __shared__ int abort_flag;
@@ -113,50 +181,21 @@ __global__ void __launch_bounds__(32 * (1 + kCoreConsumers), 1) gemm_core_kernel
     if (threadIdx.x == 0) {
         abort_flag = 0;
         for (int s = 0; s < W; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], 2);  // A producer + B producer
             mbar_init(&empty[s], kCoreConsumers);
         }
         fence_mbar_init();
+        prefetch_tmap(&bmap);
     }
     __syncthreads();
 
-    if (warp == 0) {
-        if (lane == 0) {
-            const uint64_t pol_a = policy_evict_first();
-            const uint64_t pol_b = policy_evict_last();
-            long long i = 0;
-            for (int ti = 0; ti < it.count && !*abort; ++ti) {
-                const int t = it.first + ti * it.stride;
-                const uint8_t* src = tile_src(p, it, t);
-                for (int c = 0; c < nch; ++c, ++i) {
-                    const int s = static_cast<int>(i % W);
-                    if (i >= W && !mbar_wait(&empty[s], static_cast<uint32_t>(((i / W) - 1) & 1), abort, p.st,
-                                             DAK_ERR_TIMEOUT, W_PROD_EMPTY)) {
-                        goto producer_done;
-                    }
-                    const int k0 = c * p.kc;
-                    const int kce = min(p.kc, p.K_pad - k0);
-                    const int kreal = min(kce, p.K - k0);
-                    uint8_t* dst = smem + static_cast<size_t>(s) * p.stage_bytes;
-                    const uint32_t a_bytes = static_cast<uint32_t>(kce) * 128u;
-                    const uint32_t b_row = static_cast<uint32_t>(kreal) * 2u;
-                    mbar_arrive_expect_tx(&full[s], a_bytes + b_row * N);
-                    bulk_g2s(dst, src + static_cast<long long>(k0) * 128, a_bytes, &full[s], pol_a);
-#pragma unroll
-                    for (int n = 0; n < N; ++n) {
-                        bulk_g2s(dst + a_bytes + n * p.kc * 2, p.B + static_cast<long long>(n) * p.K + k0, b_row,
-                                 &full[s], pol_b);
-                    }
-                }
-            }
-        producer_done:
-            drain_fills(full, W, i, p.st);
-        }
+    if (warp < 2) {
+        if (lane == 0) produce(p, it, &bmap, smem, full, empty, abort, warp == 0, kCoreB);
         return;
     }
 
     // consumers
-    const int w = warp - 1;       // row group 0..7
+    const int w = warp - 2;       // row group 0..7
     const int r = lane & 7;       // row within the group
     const int kq = lane >> 3;     // k-group phase 0..3
     long long i = 0;
@@ -173,14 +212,16 @@ __global__ void __launch_bounds__(32 * (1 + kCoreConsumers), 1) gemm_core_kernel
             const int k0 = c * p.kc;
             const int kgr = min(min(p.kc, p.K_pad - k0), p.K - k0) >> 3;  // real k-groups in this chunk
             const uint8_t* st = smem + static_cast<size_t>(s) * p.stage_bytes;
-            const uint32_t a_bytes = static_cast<uint32_t>(min(p.kc, p.K_pad - k0)) * 128u;
+            const uint8_t* bst = st + p.kc * 128;
             for (int kg = kq; kg < kgr; kg += 4) {
                 const uint4 a = *reinterpret_cast<const uint4*>(st + kg * 1024 + w * 128 + r * 16);
                 const float a0 = bf_lo(a.x), a1 = bf_hi(a.x), a2 = bf_lo(a.y), a3 = bf_hi(a.y);
                 const float a4 = bf_lo(a.z), a5 = bf_hi(a.z), a6 = bf_lo(a.w), a7 = bf_hi(a.w);
+                // B block of 256 columns holding this k-group: [N rows][512 bytes]
+                const uint8_t* bb = bst + (kg >> 5) * (N * 512) + (kg & 31) * 16;
 #pragma unroll
                 for (int n = 0; n < N; ++n) {
-                    const uint4 b = *reinterpret_cast<const uint4*>(st + a_bytes + n * p.kc * 2 + kg * 16);
+                    const uint4 b = *reinterpret_cast<const uint4*>(bb + n * 512);
                     float v = acc[n];
                     v = fmaf(a0, bf_lo(b.x), v);
                     v = fmaf(a1, bf_hi(b.x), v);
@@ -222,10 +263,10 @@ __global__ void __launch_bounds__(32 * (1 + kCoreConsumers), 1) gemm_core_kernel
 // ======================================================================================
 // Tensor-core path, N in 8..256: tcgen05.mma (M = 64 rows of A, N = N_pad hidden-state
 // columns, K = 16 per instruction), fp32 accumulators in TMEM, double-buffered.
-// Warps: 0 = producer (A by bulk copy, B by 128-byte-swizzled tensor-map copies),
-//        1 = TMEM allocator + MMA issuer, 2..5 = epilogue (TMEM -> registers -> C).
+// Warps: 0 = A producer (bulk copies), 1 = TMEM allocator + MMA issuer,
+//        2..5 = epilogue (TMEM -> registers -> C), 6 = B producer (tensor-map copies).
 // ======================================================================================
-constexpr int kUmmaThreads = 6 * 32;
+constexpr int kUmmaThreads = 7 * 32;
 
 // TMEM lane holding output row `row` (0..63) of an M = 64 accumulator: rows 16q .. 16q+15
 // sit in lanes 32q .. 32q+15 of sub-partition q.
@@ -255,7 +296,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     if (threadIdx.x == 0) {
         abort_flag = 0;
         for (int s = 0; s < W; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], 2);  // A producer + B producer
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -274,83 +315,70 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
 
-    if (warp == 0) {
-        if (lane == 0) {
-            const uint64_t pol_a = policy_evict_first();
-            long long i = 0;
-            for (int ti = 0; ti < it.count && !*abort; ++ti) {
-                const int t = it.first + ti * it.stride;
-                const uint8_t* src = tile_src(p, it, t);
-                for (int c = 0; c < nch; ++c, ++i) {
-                    const int s = static_cast<int>(i % W);
-                    if (i >= W && !mbar_wait(&empty[s], static_cast<uint32_t>(((i / W) - 1) & 1), abort, p.st,
-                                             DAK_ERR_TIMEOUT, W_PROD_EMPTY)) {
-                        goto producer_done;
-                    }
-                    const int k0 = c * p.kc;
-                    const int kce = min(p.kc, p.K_pad - k0);
-                    const int nblk = (kce + 63) >> 6;
-                    uint8_t* dst = smem + static_cast<size_t>(s) * p.stage_bytes;
-                    const uint32_t a_bytes = static_cast<uint32_t>(kce) * 128u;
-                    mbar_arrive_expect_tx(&full[s], a_bytes + static_cast<uint32_t>(nblk * bblk_bytes));
-                    bulk_g2s(dst, src + static_cast<long long>(k0) * 128, a_bytes, &full[s], pol_a);
-                    for (int b = 0; b < nblk; ++b) {
-                        tma_load_2d(dst + a_stage_bytes + b * bblk_bytes, &bmap, k0 + 64 * b, 0, &full[s]);
-                    }
-                }
-            }
-        producer_done:
-            drain_fills(full, W, i, p.st);
-        }
+    if (warp == 0 || warp == 6) {
+        if (lane == 0) produce(p, it, &bmap, smem, full, empty, abort, warp == 0, kUmmaB);
     } else if (warp == 1) {
-        if (lane == 0) {
-            const uint32_t idesc = idesc_bf16_f32(64, static_cast<uint32_t>(p.N_pad));
-            long long i = 0;
-            uint64_t* last_bar = nullptr;
-            uint32_t last_par = 0;
-            for (int ti = 0; ti < it.count; ++ti) {
-                const int ab = ti & 1;
-                if (ti >= 2 && !mbar_wait(&acc_empty[ab], static_cast<uint32_t>(((ti >> 1) - 1) & 1), abort, p.st,
-                                          DAK_ERR_TIMEOUT, W_MMA_ACC)) {
+        // The whole warp runs the loop (so that loop state and descriptors stay warp-uniform);
+        // one elected lane issues the MMAs and commits.
+        const uint32_t idesc = idesc_bf16_f32(64, static_cast<uint32_t>(p.N_pad));
+        const bool leader = elect_one();
+        long long i = 0;
+        uint64_t* last_bar = nullptr;
+        uint32_t last_par = 0;
+        for (int ti = 0; ti < it.count; ++ti) {
+            const int ab = ti & 1;
+            if (ti >= 2 && !mbar_wait(&acc_empty[ab], static_cast<uint32_t>(((ti >> 1) - 1) & 1), abort, p.st,
+                                      DAK_ERR_TIMEOUT, W_MMA_ACC)) {
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem + static_cast<uint32_t>(ab) * acc_stride;
+            bool ok = true;
+            for (int c = 0; c < nch; ++c, ++i) {
+                const int s = static_cast<int>(i % W);
+                if (!mbar_wait(&full[s], static_cast<uint32_t>((i / W) & 1), abort, p.st, DAK_ERR_TIMEOUT,
+                               W_MMA_FULL)) {
+                    ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem + static_cast<uint32_t>(ab) * acc_stride;
-                bool ok = true;
-                for (int c = 0; c < nch; ++c, ++i) {
-                    const int s = static_cast<int>(i % W);
-                    if (!mbar_wait(&full[s], static_cast<uint32_t>((i / W) & 1), abort, p.st, DAK_ERR_TIMEOUT,
-                                   W_MMA_FULL)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const int kce = min(p.kc, p.K_pad - c * p.kc);
-                    const uint32_t a_base = smem_u32(smem + static_cast<size_t>(s) * p.stage_bytes);
-                    const uint32_t b_base = a_base + static_cast<uint32_t>(a_stage_bytes);
-                    for (int kk = 0; kk < kce; kk += 16) {
-                        // A: no swizzle, K-major; 8x8 blocks of one k-group are 128 B apart
-                        // along M, k-groups are 64 rows x 16 B = 1024 B apart along K.
-                        const uint64_t ad = smem_desc(a_base + static_cast<uint32_t>(kk >> 3) * 1024u, 1024u, 128u, 0u);
-                        // B: 128-byte swizzle, K-major; 8-row groups 1024 B apart, 64-column
-                        // blocks N_pad x 128 B apart, +32 B per 16 columns inside a block.
-                        const uint64_t bd = smem_desc(
-                            b_base + static_cast<uint32_t>((kk >> 6) * bblk_bytes + (kk & 63) * 2), 16u, 1024u, 2u);
-                        umma_bf16(d_tmem, ad, bd, idesc, (c > 0 || kk > 0) ? 1u : 0u);
+                const int kce = min(p.kc, p.K_pad - c * p.kc);
+                const uint32_t a_base = smem_u32(smem + static_cast<size_t>(s) * p.stage_bytes);
+                const uint32_t b_base = a_base + static_cast<uint32_t>(a_stage_bytes);
+                // A: no swizzle, K-major; 8x8 blocks of one k-group are 128 B apart along M,
+                // k-groups are 64 rows x 16 B = 1024 B apart along K (+2048 B per MMA).
+                // B: 128-byte swizzle, K-major; 8-row groups 1024 B apart, 64-column blocks
+                // N_pad x 128 B apart, +32 B per 16 columns inside a block.
+                const uint64_t ad0 = smem_desc(a_base, 1024u, 128u, 0u);
+                const uint64_t bd0 = smem_desc(b_base, 16u, 1024u, 2u);
+                if (leader) {
+                    for (int kb = 0; kb < kce; kb += 64) {
+                        const uint64_t bdb = bd0 + (static_cast<uint64_t>((kb >> 6) * bblk_bytes) >> 4);
+                        const uint64_t adb = ad0 + (static_cast<uint64_t>(kb >> 3) * 1024u >> 4);
+                        const int nk = min(4, (kce - kb) >> 4);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            if (j < nk) {
+                                umma_bf16(d_tmem, adb + static_cast<uint64_t>(j * 128), bdb + static_cast<uint64_t>(j * 2),
+                                          idesc, (c > 0 || kb > 0 || j > 0) ? 1u : 0u);
+                            }
+                        }
                     }
                     umma_commit(&empty[s]);
-                    last_bar = &empty[s];
-                    last_par = static_cast<uint32_t>((i / W) & 1);
                 }
-                if (!ok) break;
-                umma_commit(&acc_full[ab]);
-                last_bar = &acc_full[ab];
-                last_par = static_cast<uint32_t>((ti >> 1) & 1);
+                __syncwarp();
+                last_bar = &empty[s];
+                last_par = static_cast<uint32_t>((i / W) & 1);
             }
-            if (last_bar) {  // every issued MMA has finished before TMEM is released
-                volatile int dummy = 0;
-                mbar_wait(last_bar, last_par, &dummy, p.st, DAK_ERR_TIMEOUT, W_DRAIN);
-            }
+            if (!ok) break;
+            if (leader) umma_commit(&acc_full[ab]);
+            __syncwarp();
+            last_bar = &acc_full[ab];
+            last_par = static_cast<uint32_t>((ti >> 1) & 1);
+        }
+        if (last_bar) {  // every issued MMA has finished before TMEM is released
+            volatile int dummy = 0;
+            mbar_wait(last_bar, last_par, &dummy, p.st, DAK_ERR_TIMEOUT, W_DRAIN);
         }
         __syncwarp();
     } else {
@@ -422,29 +450,47 @@ static EncodeTiledFn encode_fn() {
     return fn;
 }
 
-static bool make_b_map(CUtensorMap* map, const void* B, int K, int N, int N_pad) {
+// Tensor map over B [N][K] for one kind of stage layout. Uses a single 3-D box per stage when
+// K is a multiple of the block width (then every box element inside the map's bounds is an
+// element of B); otherwise 2-D boxes. Sets *b3d accordingly.
+static bool make_b_map(CUtensorMap* map, const void* B, int K, int N, int N_pad, int kc, int kind, int* b3d) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
+    const int blk = kind == kUmmaB ? 64 : 256;
+    const int rows = kind == kUmmaB ? N_pad : N;
+    const CUtensorMapSwizzle swz = kind == kUmmaB ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+    if (K % blk == 0) {
+        cuuint64_t dims[3] = {static_cast<cuuint64_t>(blk), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K / blk)};
+        cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, static_cast<cuuint64_t>(blk) * 2};
+        cuuint32_t box[3] = {static_cast<cuuint32_t>(blk), static_cast<cuuint32_t>(rows), static_cast<cuuint32_t>(kc / blk)};
+        cuuint32_t estr[3] = {1, 1, 1};
+        if (enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(B), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS) {
+            *b3d = 1;
+            return true;
+        }
+    }
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(N_pad)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(blk), static_cast<cuuint32_t>(rows)};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(B), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    *b3d = 0;
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(B), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr int kSmemBudget = 200 * 1024;
+constexpr int kSmemBudget = 216 * 1024;
 constexpr int kDefaultHostCtas = 16;
 constexpr int kDefaultHostWindow = 4;
 
 template <int N>
-static cudaError_t launch_core(const GemmParams& p, int grid, int smem, cudaStream_t s) {
+static cudaError_t launch_core(const GemmParams& p, const CUtensorMap& bmap, int grid, int smem, cudaStream_t s) {
     auto k = gemm_core_kernel<N>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    k<<<grid, 32 * (1 + kCoreConsumers), smem, s>>>(p);
+    k<<<grid, kCoreThreads, smem, s>>>(p, bmap);
     return cudaGetLastError();
 }
 
@@ -477,13 +523,16 @@ dak_status launch_gemm(const dak_placement* A, const void* host_src, const void*
     if (!p.st) return DAK_ERR_CUDA;
 
     const bool umma = N >= 8;
-    int kc = (t && t->chunk_k > 0) ? t->chunk_k : (p.N_pad <= 64 ? 256 : (p.N_pad <= 128 ? 128 : 64));
-    if (kc % 64 != 0 || kc > 1024) return DAK_ERR_INVALID;
+    const int kind = umma ? kUmmaB : kCoreB;
+    // chunk width: 64 KiB A copies where two such stages fit, 32 KiB otherwise
+    int kc = umma ? (p.N_pad <= 32 ? 512 : (p.N_pad <= 64 ? 256 : (p.N_pad <= 128 ? 128 : 64))) : 512;
+    if (t && t->chunk_k > 0) kc = t->chunk_k;
+    if (kc % 64 != 0 || kc > 1024 || (!umma && kc % 256 != 0)) return DAK_ERR_INVALID;
     p.kc = kc;
-    int stage = umma ? kc * 128 + ((kc + 63) / 64) * p.N_pad * 128 : kc * 128 + 8 * kc * 2;
+    int stage = kc * 128 + kc * 2 * (umma ? p.N_pad : N);
     stage = (stage + 1023) & ~1023;
     int stages = std::min(8, kSmemBudget / stage);
-    if (stages < 2) return DAK_ERR_INVALID;
+    if (stages < 1 || (stages < 2 && !(t && t->chunk_k > 0))) return DAK_ERR_INVALID;
     p.stages = stages;
     p.stage_bytes = stage;
     const int smem = stages * stage + (umma ? 1024 : 0);
@@ -498,23 +547,26 @@ dak_status launch_gemm(const dak_placement* A, const void* host_src, const void*
     if (grid == 0) return DAK_OK;
     if (p.h > 0 && !p.a_host) return DAK_ERR_INVALID;
 
+    alignas(64) CUtensorMap bmap;
+    int b3d = 0;
+    if (!make_b_map(&bmap, B, p.K, N, p.N_pad, kc, kind, &b3d)) return DAK_ERR_CUDA;
+    p.b3d = b3d;
+
     cudaError_t e;
     if (umma) {
-        alignas(64) CUtensorMap bmap;
-        if (!make_b_map(&bmap, B, p.K, N, p.N_pad)) return DAK_ERR_CUDA;
         e = cudaFuncSetAttribute(gemm_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return cuda_status(e);
         gemm_umma_kernel<<<grid, kUmmaThreads, smem, stream>>>(p, bmap);
         e = cudaGetLastError();
     } else {
         switch (N) {
-            case 1: e = launch_core<1>(p, grid, smem, stream); break;
-            case 2: e = launch_core<2>(p, grid, smem, stream); break;
-            case 3: e = launch_core<3>(p, grid, smem, stream); break;
-            case 4: e = launch_core<4>(p, grid, smem, stream); break;
-            case 5: e = launch_core<5>(p, grid, smem, stream); break;
-            case 6: e = launch_core<6>(p, grid, smem, stream); break;
-            default: e = launch_core<7>(p, grid, smem, stream); break;
+            case 1: e = launch_core<1>(p, bmap, grid, smem, stream); break;
+            case 2: e = launch_core<2>(p, bmap, grid, smem, stream); break;
+            case 3: e = launch_core<3>(p, bmap, grid, smem, stream); break;
+            case 4: e = launch_core<4>(p, bmap, grid, smem, stream); break;
+            case 5: e = launch_core<5>(p, bmap, grid, smem, stream); break;
+            case 6: e = launch_core<6>(p, bmap, grid, smem, stream); break;
+            default: e = launch_core<7>(p, bmap, grid, smem, stream); break;
         }
     }
     return cuda_status(e);

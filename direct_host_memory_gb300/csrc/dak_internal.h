@@ -24,8 +24,7 @@ struct dak_placement {
     // kv
     int B, H_kv, L, D;
     int h_r;                // requests on the host
-    int64_t head_bytes;     // L * D * 2: one (request, kv head) slab of K (or V)
-    int64_t kv_tier_half;   // in each tier: K block first, V block after it at this offset
+    int64_t head_bytes;     // one (request, kv head) slab: ceil(L/64) chunks of [K 64 x D][V 64 x D] bf16
 };
 
 namespace dak {

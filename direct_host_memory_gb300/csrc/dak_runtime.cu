@@ -100,16 +100,25 @@ __global__ void pack_matrix_kernel(const uint4* __restrict__ src, long long lda1
     }
 }
 
-// K or V rows [n_rows][D] -> same rows with the 16-byte chunks of token j permuted by
-// c -> c ^ (j & 7), so that 8 consecutive tokens' chunk c fall in 8 different bank groups.
-__global__ void pack_kv_kernel(const uint4* __restrict__ src, long long n_units, int D16, int L,
-                               uint4* __restrict__ dst) {
+// K or V rows of `n_heads` (request, kv head) slabs, [n_heads][L][D] -> the chunked slab
+// layout of the placement: per slab, chunks of 64 tokens [K 64 x D][V 64 x D] (last chunk
+// zero-padded), and inside a token row the 16-byte piece c stored at c ^ (token & 7) so that
+// ldmatrix reads of 8 consecutive tokens hit 8 different bank groups. `is_v` selects the
+// half of each chunk.
+__global__ void pack_kv_kernel(const uint4* __restrict__ src, long long n_heads, int L, int D16, int is_v,
+                               long long slab16, uint4* __restrict__ dst) {
+    const long long per_head = static_cast<long long>(L) * D16;
+    const long long n_units = n_heads * per_head;
     for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < n_units;
          idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const long long row = idx / D16;
-        const int c = static_cast<int>(idx - row * D16);
-        const int j = static_cast<int>(row % L);
-        dst[row * D16 + (c ^ (j & 7))] = src[idx];
+        const long long head = idx / per_head;
+        const long long rem = idx - head * per_head;
+        const int j = static_cast<int>(rem / D16);
+        const int c = static_cast<int>(rem - static_cast<long long>(j) * D16);
+        const long long chunk = j >> 6;
+        const long long off = head * slab16 + chunk * (2ll * 64 * D16) + (is_v ? 64ll * D16 : 0ll) +
+                              static_cast<long long>(j & 63) * D16 + (c ^ (j & 7));
+        dst[off] = src[idx];
     }
 }
 
@@ -277,22 +286,27 @@ extern "C" dak_status dak_place_kv(const void* K_src, const void* V_src, int src
     p->L = L;
     p->D = D;
     p->h_r = n_host_requests;
-    p->head_bytes = static_cast<int64_t>(L) * D * 2;
-    const int64_t req_bytes = p->head_bytes * H_kv;  // K (or V) of one request
-    p->host_bytes = 2 * req_bytes * p->h_r;
-    p->hbm_bytes = 2 * req_bytes * (B - p->h_r);
+    const int64_t n_chunks = (L + 63) / 64;
+    p->head_bytes = n_chunks * 2 * 64 * D * 2;  // one (request, kv head) slab: K and V chunks
+    const int64_t req_bytes = p->head_bytes * H_kv;
+    const int64_t src_req_bytes = static_cast<int64_t>(L) * D * 2 * H_kv;  // K (or V) of one request in the source
+    p->host_bytes = req_bytes * p->h_r;
+    p->hbm_bytes = req_bytes * (B - p->h_r);
     dak_status st = alloc_tiers(p);
     if (st != DAK_OK) {
         free_parts(p);
         delete p;
         return st;
     }
-    const int D16 = D / 8;
-    const int batch = std::max(1, static_cast<int>((256ll << 20) / req_bytes));
-    void* tmp = nullptr;
+    // zero both tiers first: the padding rows of every last chunk must hold finite values
     cudaError_t e = cudaSuccess;
-    if (!src_on_device) {
-        e = cudaMalloc(&tmp, static_cast<size_t>(std::min(batch, B)) * req_bytes);
+    if (p->host_bytes) std::memset(p->host_ptr, 0, static_cast<size_t>(p->host_bytes));
+    if (p->hbm_bytes) e = cudaMemset(p->hbm_ptr, 0, static_cast<size_t>(p->hbm_bytes));
+    const int D16 = D / 8;
+    const int batch = std::max(1, static_cast<int>((256ll << 20) / src_req_bytes));
+    void* tmp = nullptr;
+    if (!src_on_device && e == cudaSuccess) {
+        e = cudaMalloc(&tmp, static_cast<size_t>(std::min(batch, B)) * src_req_bytes);
         if (e != cudaSuccess) {
             cudaGetLastError();
             free_parts(p);
@@ -309,20 +323,21 @@ extern "C" dak_status dak_place_kv(const void* K_src, const void* V_src, int src
             if (b0 < p->h_r) nb = std::min(nb, p->h_r - b0);
             const uint4* src;
             if (src_on_device) {
-                src = reinterpret_cast<const uint4*>(srcb + static_cast<long long>(b0) * req_bytes);
+                src = reinterpret_cast<const uint4*>(srcb + static_cast<long long>(b0) * src_req_bytes);
             } else {
-                e = cudaMemcpy(tmp, srcb + static_cast<long long>(b0) * req_bytes, static_cast<size_t>(nb) * req_bytes,
-                               cudaMemcpyHostToDevice);
+                e = cudaMemcpy(tmp, srcb + static_cast<long long>(b0) * src_req_bytes,
+                               static_cast<size_t>(nb) * src_req_bytes, cudaMemcpyHostToDevice);
                 src = reinterpret_cast<const uint4*>(tmp);
             }
             if (e != cudaSuccess) break;
             const bool host = b0 < p->h_r;
-            const int n_tier = host ? p->h_r : B - p->h_r;
             const int lb = host ? b0 : b0 - p->h_r;
             uint8_t* tier = static_cast<uint8_t*>(host ? p->host_dev : p->hbm_ptr);
-            uint8_t* dstb = tier + static_cast<long long>(kv) * req_bytes * n_tier + static_cast<long long>(lb) * req_bytes;
-            const long long units = static_cast<long long>(nb) * req_bytes / 16;
-            pack_kv_kernel<<<pack_grid(units), 256>>>(src, units, D16, L, reinterpret_cast<uint4*>(dstb));
+            uint8_t* dstb = tier + static_cast<long long>(lb) * req_bytes;
+            const long long n_heads = static_cast<long long>(nb) * H_kv;
+            const long long units = n_heads * L * D16;
+            pack_kv_kernel<<<pack_grid(units), 256>>>(src, n_heads, L, D16, kv, p->head_bytes / 16,
+                                                      reinterpret_cast<uint4*>(dstb));
             e = cudaGetLastError();
             if (e == cudaSuccess) e = cudaDeviceSynchronize();
         }
@@ -334,7 +349,6 @@ extern "C" dak_status dak_place_kv(const void* K_src, const void* V_src, int src
         delete p;
         return DAK_ERR_CUDA;
     }
-    p->kv_tier_half = 0;  // per-tier offset of V is req_bytes * (requests in that tier)
     *out = p;
     return DAK_OK;
 }

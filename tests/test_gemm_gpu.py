@@ -93,8 +93,9 @@ def test_bit_identical_across_tuning(dak, N):
     M, K = 640, 2048
     A, B = synth.gemm_inputs(M, K, N, seed=4)
     base = bits_of(_run(dak, A, B, 4))
-    for tun in [dict(host_ctas=1), dict(host_ctas=3, window=1), dict(window=2, hbm_window=2),
-                dict(chunk_k=64), dict(chunk_k=128, hbm_ctas=3)]:
+    chunks = [dict(chunk_k=256), dict(chunk_k=512, hbm_ctas=3)] if N < 8 else \
+        [dict(chunk_k=64), dict(chunk_k=128, hbm_ctas=3), dict(chunk_k=256)]
+    for tun in [dict(host_ctas=1), dict(host_ctas=3, window=1), dict(window=2, hbm_window=2)] + chunks:
         assert np.array_equal(bits_of(_run(dak, A, B, 4, tuning=tun)), base), tun
 
 

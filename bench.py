@@ -41,6 +41,8 @@ def _args():
     ap.add_argument("--batch", type=int, default=32)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--profile", default=None, choices=["attn", "qkv", "o", "gate_up", "down"],
+                    help="place one operation of the step at --x and launch it --steps times (for ncu)")
     return ap.parse_args()
 
 
@@ -234,6 +236,29 @@ def time_steps(fn, steps, warmup, sync_all=None):
     return e0.elapsed_time(e1) / 1e3 / steps
 
 
+def aggregate_replicas(t_step, bytes_per_step, dist=None):
+    """Replicas: every rank runs the same step on its own GPU. The job time is the slowest
+    rank's; the job moves world x bytes_per_step per step. Returns (GB/s, max step time)."""
+    world = 1
+    if dist is not None and dist.is_initialized():
+        import torch
+        world = dist.get_world_size()
+        dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+        tt = torch.tensor([float(t_step)], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_step = float(tt.item())
+    return world * bytes_per_step / t_step / 1e9, t_step
+
+
+def step_config(args, world):
+    """The workload both arms report (identical for --impl dak and --impl reference)."""
+    return {"workload": f"8B-shaped decode layer at batch {args.batch}: linears QKV 6144x4096, O 4096x4096, "
+                        f"gate+up 28672x4096, down 4096x14336 + GQA decode attention over 32 requests, 32/8 heads, "
+                        f"D 128, context 8192; bf16 weights/KV, fp32 accumulate",
+            "x": args.x, "batch": args.batch, "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (1.51 GB of weights and KV per step)"}
+
+
 def tier_roofline(C, x, bh, bg):
     t = max(x * C / bh, (1 - x) * C / bg)
     return C / t
@@ -266,7 +291,7 @@ def cpu_oracle_sample(lin, attn, frac_rows=1 / 32):
     oa.decode_attention_ref(q[:nreq], k[:nreq], v[:nreq])
     nbytes += 2 * k[:nreq].size * 2
     dt = time.perf_counter() - t0
-    return nbytes / dt / 1e9, f"1/{int(1 / frac_rows)} of the step: every {int(1 / frac_rows)}th 64-row tile of each " \
+    return nbytes / dt / 1e9, f"1/{int(1 / frac_rows)} of the step: one 64-row tile in {int(1 / frac_rows)} of each " \
                               f"linear and {nreq} of {q.shape[0]} attention requests ({nbytes / 1e6:.0f} MB)", dt
 
 
@@ -303,9 +328,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(dts),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"8B-shaped decode layer, batch {args.batch}: QKV/O/gate+up/down linears + GQA "
-                               f"attention 32x(32/8 heads, D 128, ctx 8192); bounded sample per step",
-                   "x": args.x, "l2": "inputs larger than L2"},
+        "config": step_config(args, world),
         "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cpu_threads(), "kind": "oracle", "sample": sample},
         "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -321,6 +344,9 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl" if args.impl == "dak" else "gloo")
+    if args.profile:
+        run_profile(args)
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
         if dist:
@@ -363,11 +389,7 @@ def main():
     torch.cuda.synchronize()
     t_wall1 = time.time()
     sync_all()
-    t_step = e0.elapsed_time(e1) / 1e3 / args.steps
-    if dist:
-        tt = torch.tensor([t_step], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_step = float(tt.item())
+    value, t_step = aggregate_replicas(e0.elapsed_time(e1) / 1e3 / args.steps, st.total_bytes, dist)
     att_ms = statistics.mean(a.elapsed_time(b) for a, b in att_ev)
     time.sleep(0.3)
     sampler.stop()
@@ -392,7 +414,7 @@ def main():
             hostC[n].copy_(st.C[n], non_blocking=True)
         hostO.copy_(st.O, non_blocking=True)
 
-    t_e2e = time_steps(e2e_step, max(10, args.steps // 3), 3, sync_all)
+    e2e_value, t_e2e = aggregate_replicas(time_steps(e2e_step, max(10, args.steps // 3), 3, sync_all), C, dist)
 
     # per-x sweep with the prefetch baselines
     per_x = []
@@ -434,16 +456,13 @@ def main():
         cpu = {"value": gbps, "unit": "GB/s", "cores": cpu_threads(), "kind": "oracle", "sample": sample}
 
     n = world
-    value = n * C / t_step / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": n, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"8B-shaped decode layer at batch {args.batch}: dak_gemm over QKV 6144x4096, "
-                               f"O 4096x4096, gate+up 28672x4096, down 4096x14336 + dak_attn over 32 requests, "
-                               f"32/8 heads, D 128, context 8192; bf16, fp32 accumulate",
-                   "x": args.x, "x_effective": x_eff, "bytes_per_step": C, "host_bytes_per_step": st.host_bytes,
-                   "parallelism": f"replicas x{n}", "l2": "inputs larger than L2 (1.5 GB per step)"},
+        "config": step_config(args, world),
+        "step": {"x_effective": x_eff, "bytes_per_step": C, "host_bytes_per_step": st.host_bytes,
+                 "kernels": "dak_gemm x4 (tcgen05 for N >= 8) + dak_attn (+ split combine)"},
         "decode_tok_s": n * args.batch / (t_step * LAYERS_8B),
         "tier_roofline_gbps": tier_roofline(C, x_eff, b_host, b_hbm) / 1e9,
         "tier_roofline_frac": (C / t_step) / tier_roofline(C, x_eff, b_host, b_hbm),
@@ -455,7 +474,7 @@ def main():
                      "hbm_peak_gbs": pk.get("hbm_gbs"), "hbm_peak_source": pk_src,
                      "algorithmic_bytes_per_launch": att_bytes, "launch_ms": att_ms},
         "per_x": per_x,
-        "e2e": {"value": n * C / t_e2e / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": st.launches * args.steps,
         "clocks": clocks,
         "status": [status[0], status2[0], status3[0]],
@@ -470,14 +489,62 @@ def main():
         dist.destroy_process_group()
 
 
+KERNEL_SOURCES = ["direct_host_memory_gb300/csrc/dak_attn.cu", "direct_host_memory_gb300/csrc/dak_device.cuh"]
+
+
+def kernel_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def read_ncu_traffic():
-    """DRAM bytes per launch of the attention kernel from the committed ncu summary, or None."""
+    """DRAM bytes per launch of the attention kernel at this workload from the committed ncu
+    summary, or None when there is none or the kernel source changed since it was taken."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
-            return json.load(f).get("attn_kernel_dram_bytes_per_launch")
+            t = json.load(f)
+        if t.get("source_hash") != kernel_source_hash():
+            return None
+        return t.get("attn_kernel_dram_bytes_per_launch")
     except Exception:
         return None
+
+
+def run_profile(args):
+    """One operation of the step, placed at --x, launched --warmup + --steps times."""
+    import torch
+    import direct_host_memory_gb300 as dak
+    import synth
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    if args.profile == "attn":
+        c = synth.ATTN_DECODE
+        q, k, v = synth.attn_inputs(c["batch"], c["h_q"], c["h_kv"], c["head_dim"], c["context"], seed=0,
+                                    tensor_index=len(synth.LINEARS_8B))
+        p = dak.dak_place_kv(k, v, dak.host_requests_for_ratio(args.x, c["batch"]))
+        Q = torch.from_numpy(q.view("int16")).view(torch.bfloat16).to(dev)
+        O = torch.empty_like(Q)
+        fn = lambda: dak.dak_attn(Q, p, O=O)  # noqa: E731
+        nbytes = k.nbytes * 2
+    else:
+        M, K = synth.LINEARS_8B[args.profile]
+        A, B = synth.gemm_inputs(M, K, args.batch, seed=0, tensor_index=list(synth.LINEARS_8B).index(args.profile))
+        p = dak.dak_place_matrix(A, dak.host_tiles_for_ratio(args.x, M))
+        Bt = torch.from_numpy(B.view("int16")).view(torch.bfloat16).to(dev)
+        C = torch.empty((args.batch, M), dtype=torch.bfloat16, device=dev)
+        fn = lambda: dak.dak_gemm(p, Bt, C)  # noqa: E731
+        nbytes = A.nbytes
+    t = time_steps(fn, args.steps, args.warmup)
+    st = dak.dak_last_error()
+    print(json.dumps({"profile": args.profile, "x": args.x, "batch": args.batch, "us_per_launch": t * 1e6,
+                      "gbps": nbytes / t / 1e9, "host_bytes": p.host_bytes, "status": st[0],
+                      "source_hash": kernel_source_hash()}))
+    p.free()
 
 
 if __name__ == "__main__":

@@ -10,6 +10,6 @@ from ._lib import (  # noqa: F401
     dak_attn_noalloc, dak_attn_staged,
     dak_attn_workspace_bytes, dak_free, dak_gemm, dak_gemm_staged, dak_last_error, dak_op,
     dak_place_kv, dak_place_matrix, dak_placement_info, dak_plan_ratios, dak_prefetch,
-    dak_probe_concurrent, dak_probe_read_bw, dak_sm_count, dak_tuning, host_requests_for_ratio,
+    dak_probe_concurrent, dak_probe_read_bw, dak_selftest_wait, dak_sm_count, dak_tuning, host_requests_for_ratio,
     host_tiles_for_ratio, lib,
 )

@@ -26,7 +26,7 @@ EXPORTS = [
     "dak_status_string", "dak_place_matrix", "dak_place_kv", "dak_free", "dak_placement_info",
     "dak_gemm", "dak_attn_workspace_bytes", "dak_attn", "dak_attn_default_split", "dak_plan_ratios",
     "dak_last_error", "dak_sm_count", "dak_probe_read_bw", "dak_probe_concurrent", "dak_prefetch",
-    "dak_gemm_staged", "dak_attn_staged", "dak_attn_noalloc",
+    "dak_gemm_staged", "dak_attn_staged", "dak_attn_noalloc", "dak_selftest_wait",
 ]
 
 # size of the fixed device array dak_attn_noalloc uses (DAK_NOALLOC_SCRATCH_BYTES in dak.h)
@@ -74,6 +74,7 @@ def _load():
         "dak_probe_concurrent": (i32, [i64, i64, i32, i32, i32, i32, i32, i32, P(dbl), P(dbl)]),
         "dak_prefetch": (i32, [vp, vp, vp]),
         "dak_attn_noalloc": (i32, [vp, vp, vp, i32, ctypes.c_float, vp, P(dak_tuning), vp]),
+        "dak_selftest_wait": (i32, [vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -330,6 +331,11 @@ def dak_last_error(stream=None):
     info = ctypes.c_uint64()
     st = lib.dak_last_error(_stream_ptr(stream), ctypes.byref(info))
     return int(st), int(info.value)
+
+
+def dak_selftest_wait(stream=None):
+    """Launch the bounded-wait self-test kernel (its wait must time out after ~2 s)."""
+    _check(lib.dak_selftest_wait(_stream_ptr(stream)), "dak_selftest_wait")
 
 
 def dak_sm_count() -> int:

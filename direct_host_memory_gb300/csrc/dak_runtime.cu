@@ -694,6 +694,27 @@ extern "C" dak_status dak_probe_concurrent(int64_t host_bytes, int64_t hbm_bytes
                           &ok);
 }
 
+// One CTA waits on an mbarrier that nothing arrives at: the bounded wait must run out,
+// record DAK_ERR_TIMEOUT and let the kernel return normally.
+__global__ void selftest_wait_kernel(DevStatus* st) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    mbar_wait(&bar, 0, &abort_flag, st, DAK_ERR_TIMEOUT, 0x5E1Fu);
+}
+
+extern "C" dak_status dak_selftest_wait(void* stream) {
+    DevStatus* st = status_ptr();
+    if (!st) return DAK_ERR_CUDA;
+    selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(st);
+    return cuda_status(cudaGetLastError());
+}
+
 extern "C" dak_status dak_prefetch(const dak_placement* p, void* staging, void* stream) {
     if (!p) return DAK_ERR_INVALID;
     if (p->host_bytes == 0) return DAK_OK;

@@ -214,6 +214,12 @@ dak_status dak_probe_concurrent(int64_t host_bytes, int64_t hbm_bytes, int host_
                                 int hbm_ctas, int hbm_window, int chunk_bytes, int iters, double* host_gbps,
                                 double* hbm_gbps);
 
+/* Self-test of the kernels' failure path: launches one CTA whose bounded wait on an
+ * mbarrier that nothing arrives at runs out after about 2 s. The launch returns DAK_OK;
+ * a following dak_last_error() must report DAK_ERR_TIMEOUT (info 0x5E1F in the upper 32
+ * bits) and the CUDA context stays usable. The paper has no counterpart. */
+dak_status dak_selftest_wait(void* stream);
+
 /* Prefetch baseline (section 2.2-2.3, Fig. 2-3): copy a placement's host-resident part into
  * a caller-provided HBM staging buffer (cudaMemcpyAsync on `stream`), so that a following
  * dak_gemm_staged / dak_attn_staged call reads every tile from HBM. staging must hold

@@ -87,7 +87,9 @@ class Step:
         self.n_split = dak.dak_attn_default_split(self.kv)
         ws = dak.dak_attn_workspace_bytes(q.shape[0], q.shape[1], q.shape[2], self.n_split)
         self.ws = torch.empty(max(1, ws // 4), dtype=torch.float32, device=dev)
-        self.tun = dict(n_split=self.n_split)
+        # programmatic launch: no op of the step writes the weights or KV cache another op streams
+        self.tun = dict(n_split=self.n_split, pdl=1)
+        self.gtun = dict(pdl=1)
         self.host_bytes = sum(p.host_bytes for p in self.pl.values()) + self.kv.host_bytes
         self.total_bytes = sum(p.host_bytes + p.hbm_bytes for p in self.pl.values()) + \
             self.kv.host_bytes + self.kv.hbm_bytes
@@ -96,7 +98,7 @@ class Step:
     def run(self, ev=None):
         d = self.dak
         for name, p in self.pl.items():
-            d.dak_gemm(p, self.B[name], self.C[name])
+            d.dak_gemm(p, self.B[name], self.C[name], tuning=self.gtun)
         if ev is not None:
             ev[0].record()
         d.dak_attn(self.Q, self.kv, O=self.O, workspace=self.ws, tuning=self.tun)
@@ -115,7 +117,7 @@ class Step:
             d.dak_prefetch(p, self.stage[name])
         d.dak_prefetch(self.kv, self.stage_kv)
         for name, p in self.pl.items():
-            d.dak_gemm_staged(p, self.stage[name], self.B[name], self.C[name])
+            d.dak_gemm_staged(p, self.stage[name], self.B[name], self.C[name], tuning=self.gtun)
         d.dak_attn_staged(self.Q, self.kv, self.stage_kv, O=self.O, workspace=self.ws, tuning=self.tun)
 
     def run_prefetch_overlap(self, copy_stream, events):
@@ -134,7 +136,7 @@ class Step:
             events[len(names)].record(copy_stream)
         for i, name in enumerate(names):
             cur.wait_event(events[i])
-            d.dak_gemm_staged(self.pl[name], self.stage[name], self.B[name], self.C[name])
+            d.dak_gemm_staged(self.pl[name], self.stage[name], self.B[name], self.C[name], tuning=self.gtun)
         cur.wait_event(events[len(names)])
         d.dak_attn_staged(self.Q, self.kv, self.stage_kv, O=self.O, workspace=self.ws, tuning=self.tun)
 

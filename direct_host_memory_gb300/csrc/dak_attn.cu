@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnParams 
         fence_mbar_init();
     }
     __syncthreads();
+    grid_dep_launch();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -152,6 +153,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnParams 
     }
 
     // ---------------------------------------------------------------- consumers
+    // Q (and the outputs) may belong to the previous kernel of the stream; the KV cache
+    // streamed above is, with programmatic launch, taken to be written earlier than that
+    grid_dep_wait();
     const int w = warp - 1;
     const int q4 = lane & 3;      // column pair within an 8-wide block
     const int ra = lane >> 2;     // MMA row of c0/c1 (c2/c3: ra + 8)
@@ -394,12 +398,26 @@ static int attn_ctas_per_sm(int W, int G) {
 }
 
 template <int D>
-static cudaError_t launch_attn_d(const AttnParams& p, int grid, int W, cudaStream_t s) {
+static cudaError_t launch_attn_d(const AttnParams& p, int grid, int W, bool pdl, cudaStream_t s) {
     const int smem = attn_smem_bytes<D>(W, p.G);
     cudaError_t e = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    attn_kernel<D><<<grid, kAttnThreads, smem, s>>>(p);
-    e = cudaGetLastError();
+    if (pdl) {
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(static_cast<unsigned>(grid));
+        cfg.blockDim = dim3(kAttnThreads);
+        cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, attn_kernel<D>, p);
+    } else {
+        attn_kernel<D><<<grid, kAttnThreads, smem, s>>>(p);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess || p.n_split == 1) return e;
     const int rows = p.B * p.Hq;
     attn_combine_kernel<D><<<(rows + 7) / 8, 256, 0, s>>>(p.ws, p.O, rows, p.n_split);
@@ -458,7 +476,8 @@ dak_status launch_attn(const void* Q, const dak_placement* KV, const void* host_
     const int grid = p.n_host_ctas + p.n_hbm_ctas;
     if (grid == 0) return DAK_OK;
     const int W = std::max(p.host_window, p.hbm_window);
-    cudaError_t e = KV->D == 128 ? launch_attn_d<128>(p, grid, W, stream) : launch_attn_d<64>(p, grid, W, stream);
+    const bool pdl = t && t->pdl > 0;
+    cudaError_t e = KV->D == 128 ? launch_attn_d<128>(p, grid, W, pdl, stream) : launch_attn_d<64>(p, grid, W, pdl, stream);
     return cuda_status(e);
 }
 

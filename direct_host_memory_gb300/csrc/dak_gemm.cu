@@ -31,27 +31,35 @@ struct GemmParams {
     const __nv_bfloat16* B; // [N][K]
     void* C;                // [N][M]
     int M, K, K_pad, N, N_pad, T, h;
-    int n_host_ctas, n_hbm_ctas, host_window, hbm_window;
+    int n_host_ctas, n_hbm_ctas, host_window, hbm_window;  // host/HBM counts are in clusters of S CTAs
     int kc;           // chunk width along K (multiple of 64)
     int stages;       // ring slots in shared memory
     int stage_bytes;  // bytes per slot
     int c_fp32;
     long long tile_bytes;
     DevStatus* st;
-    int b3d;  // B arrives in one 3-D tensor copy per stage (else several 2-D copies)
+    int b3d;      // B arrives in one 3-D tensor copy per stage (else several 2-D copies)
+    int S;        // CTAs per cluster splitting each tile row's K range (1 = no split)
+    int red_off;  // byte offset (from the aligned ring base) of the partial-sum area, S > 1
 };
 
-// Tiles of this CTA: role, first tile, stride, count.
+// Tiles of this CTA: role, first tile, stride, count, and the chunk range [c_lo, c_hi) of
+// every tile row that this CTA (rank `rank` of its cluster) accumulates.
 struct TileIter {
     bool host;
     int first, stride, count;
     const uint8_t* base;
     int window;
+    int rank, c_lo, c_hi;
 };
 
 __device__ __forceinline__ TileIter tiles_of_cta(const GemmParams& p) {
     TileIter it;
-    int b = blockIdx.x;
+    const int b = blockIdx.x / p.S;  // cluster index
+    const int nch = (p.K_pad + p.kc - 1) / p.kc;
+    it.rank = p.S > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    it.c_lo = it.rank * nch / p.S;
+    it.c_hi = (it.rank + 1) * nch / p.S;
     if (b < p.n_host_ctas) {
         it.host = true;
         it.first = b;
@@ -79,7 +87,8 @@ __device__ __forceinline__ const uint8_t* tile_src(const GemmParams& p, const Ti
 
 // error location codes (upper 32 bits of the status info)
 enum : uint32_t {
-    W_PROD_EMPTY = 1, W_CONS_FULL = 2, W_MMA_FULL = 3, W_MMA_ACC = 4, W_EPI_ACC = 5, W_DRAIN = 6, W_BPROD_EMPTY = 7
+    W_PROD_EMPTY = 1, W_CONS_FULL = 2, W_MMA_FULL = 3, W_MMA_ACC = 4, W_EPI_ACC = 5, W_DRAIN = 6, W_BPROD_EMPTY = 7,
+    W_RED_FULL = 8, W_RED_EMPTY = 9
 };
 
 // Wait (bounded, ignoring the abort flag) for the last fill of every ring slot, so that no
@@ -129,13 +138,14 @@ __device__ __forceinline__ uint32_t b_stage_bytes(const GemmParams& p, int kind)
 __device__ __forceinline__ void produce(const GemmParams& p, const TileIter& it, const CUtensorMap* bmap, uint8_t* smem,
                                         uint64_t* full, uint64_t* empty, volatile int* abort, bool is_a, int kind) {
     const int W = it.window;
-    const int nch = (p.K_pad + p.kc - 1) / p.kc;
     const uint64_t pol_a = policy_evict_first();
+    // the weights never depend on the previous kernel of the stream; the hidden states may
+    if (!is_a) grid_dep_wait();
     long long i = 0;
     for (int ti = 0; ti < it.count && !*abort; ++ti) {
         const int t = it.first + ti * it.stride;
         const uint8_t* src = tile_src(p, it, t);
-        for (int c = 0; c < nch; ++c, ++i) {
+        for (int c = it.c_lo; c < it.c_hi; ++c, ++i) {
             const int s = static_cast<int>(i % W);
             if (i >= W && !mbar_wait(&empty[s], static_cast<uint32_t>(((i / W) - 1) & 1), abort, p.st,
                                      DAK_ERR_TIMEOUT, is_a ? W_PROD_EMPTY : W_BPROD_EMPTY)) {
@@ -188,13 +198,15 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
         prefetch_tmap(&bmap);
     }
     __syncthreads();
+    grid_dep_launch();
 
     if (warp < 2) {
         if (lane == 0) produce(p, it, &bmap, smem, full, empty, abort, warp == 0, kCoreB);
         return;
     }
 
-    // consumers
+    // consumers (C may be read by the previous kernel of the stream: wait before writing it)
+    grid_dep_wait();
     const int w = warp - 2;       // row group 0..7
     const int r = lane & 7;       // row within the group
     const int kq = lane >> 3;     // k-group phase 0..3
@@ -204,7 +216,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
         float acc[N];
 #pragma unroll
         for (int n = 0; n < N; ++n) acc[n] = 0.f;
-        for (int c = 0; c < nch; ++c, ++i) {
+        for (int c = it.c_lo; c < it.c_hi; ++c, ++i) {
             const int s = static_cast<int>(i % W);
             if (!mbar_wait(&full[s], static_cast<uint32_t>((i / W) & 1), abort, p.st, DAK_ERR_TIMEOUT, W_CONS_FULL)) {
                 return;
@@ -276,6 +288,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     gemm_umma_kernel(const GemmParams p, const __grid_constant__ CUtensorMap bmap) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ uint64_t full[8], empty[8], acc_full[2], acc_empty[2];
+    __shared__ uint64_t red_full, red_empty;  // cluster split: partials in / partial buffer free
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
     volatile int* abort = &abort_flag;
@@ -303,6 +316,10 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_empty[b], 4);
         }
+        if (p.S > 1) {
+            mbar_init(&red_full, (p.S - 1) * 128);  // every epilogue thread of every partner, per tile
+            mbar_init(&red_empty, 128);             // every epilogue thread of the leader, per tile
+        }
         fence_mbar_init();
         prefetch_tmap(&bmap);
     }
@@ -313,6 +330,8 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (p.S > 1) cluster_sync_all();  // partners' barriers exist before any remote arrive
+    grid_dep_launch();
     const uint32_t tmem = tmem_base_sh;
 
     if (warp == 0 || warp == 6) {
@@ -334,7 +353,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
             tc_fence_after();
             const uint32_t d_tmem = tmem + static_cast<uint32_t>(ab) * acc_stride;
             bool ok = true;
-            for (int c = 0; c < nch; ++c, ++i) {
+            for (int c = it.c_lo; c < it.c_hi; ++c, ++i) {
                 const int s = static_cast<int>(i % W);
                 if (!mbar_wait(&full[s], static_cast<uint32_t>((i / W) & 1), abort, p.st, DAK_ERR_TIMEOUT,
                                W_MMA_FULL)) {
@@ -360,7 +379,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
                         for (int j = 0; j < 4; ++j) {
                             if (j < nk) {
                                 umma_bf16(d_tmem, adb + static_cast<uint64_t>(j * 128), bdb + static_cast<uint64_t>(j * 2),
-                                          idesc, (c > 0 || kb > 0 || j > 0) ? 1u : 0u);
+                                          idesc, (c > it.c_lo || kb > 0 || j > 0) ? 1u : 0u);
                             }
                         }
                     }
@@ -382,9 +401,14 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         }
         __syncwarp();
     } else {
-        // epilogue warps 2..5 -> TMEM sub-partitions 2, 3, 0, 1
+        // epilogue warps 2..5 -> TMEM sub-partitions 2, 3, 0, 1. With a cluster split the
+        // partners send their fp32 partial tiles into the leader's shared memory; the leader
+        // adds them to its own in rank order (a fixed order, independent of the placement).
         const int q = warp & 3;
         const int row_in_tile = umma_m64_row_of_lane(q, lane);
+        const bool leader = it.rank == 0;
+        grid_dep_wait();  // C may be read by the previous kernel of the stream
+        float* red = reinterpret_cast<float*>(smem + p.red_off);  // [S-1][64 rows][N_pad] on the leader
         for (int ti = 0; ti < it.count; ++ti) {
             const int ab = ti & 1;
             if (!mbar_wait(&acc_full[ab], static_cast<uint32_t>((ti >> 1) & 1), abort, p.st, DAK_ERR_TIMEOUT,
@@ -396,21 +420,60 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
             const int row = t * kTileM + row_in_tile;
             const bool valid = row_in_tile >= 0 && row < p.M;
             const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(ab) * acc_stride;
+            if (!leader) {
+                // wait until the leader has consumed this CTA's previous partial
+                if (ti > 0 && !mbar_wait_cluster(&red_empty, static_cast<uint32_t>((ti - 1) & 1), abort, p.st,
+                                                 DAK_ERR_TIMEOUT, W_RED_EMPTY)) {
+                    break;
+                }
+                const int r_own = row_in_tile >= 0 ? row_in_tile : 0;
+                const uint32_t dst =
+                    mapa_shared(smem_u32(red + static_cast<size_t>((it.rank - 1) * kTileM + r_own) * p.N_pad), 0);
+                for (int n0 = 0; n0 < p.N_pad; n0 += 8) {
+                    uint32_t v[8];
+                    tmem_ld8(taddr + static_cast<uint32_t>(n0), v);
+                    tmem_wait_ld();
+                    if (row_in_tile >= 0) {
+                        st_cluster_v4(dst + n0 * 4, __uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]),
+                                      __uint_as_float(v[3]));
+                        st_cluster_v4(dst + n0 * 4 + 16, __uint_as_float(v[4]), __uint_as_float(v[5]),
+                                      __uint_as_float(v[6]), __uint_as_float(v[7]));
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[ab]);
+                mbar_arrive_remote(mapa_shared(smem_u32(&red_full), 0));
+                continue;
+            }
+            if (p.S > 1 && !mbar_wait_cluster(&red_full, static_cast<uint32_t>(ti & 1), abort, p.st, DAK_ERR_TIMEOUT,
+                                              W_RED_FULL)) {
+                break;
+            }
             for (int n0 = 0; n0 < p.N_pad; n0 += 8) {
                 uint32_t v[8];
                 tmem_ld8(taddr + static_cast<uint32_t>(n0), v);
                 tmem_wait_ld();
                 if (valid) {
+                    float f[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(v[j]);
+                    for (int r = 1; r < p.S; ++r) {
+                        const float4* pr = reinterpret_cast<const float4*>(
+                            red + static_cast<size_t>((r - 1) * kTileM + row_in_tile) * p.N_pad + n0);
+                        const float4 x0 = pr[0], x1 = pr[1];
+                        f[0] += x0.x; f[1] += x0.y; f[2] += x0.z; f[3] += x0.w;
+                        f[4] += x1.x; f[5] += x1.y; f[6] += x1.z; f[7] += x1.w;
+                    }
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const int n = n0 + j;
                         if (n < p.N) {
-                            const float f = __uint_as_float(v[j]);
                             if (p.c_fp32) {
-                                reinterpret_cast<float*>(p.C)[static_cast<long long>(n) * p.M + row] = f;
+                                reinterpret_cast<float*>(p.C)[static_cast<long long>(n) * p.M + row] = f[j];
                             } else {
                                 reinterpret_cast<__nv_bfloat16*>(p.C)[static_cast<long long>(n) * p.M + row] =
-                                    __float2bfloat16_rn(f);
+                                    __float2bfloat16_rn(f[j]);
                             }
                         }
                     }
@@ -419,11 +482,13 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[ab]);
+            for (int r = 1; r < p.S; ++r) mbar_arrive_remote(mapa_shared(smem_u32(&red_empty), static_cast<uint32_t>(r)));
         }
     }
 
     tc_fence_before();
     __syncthreads();
+    if (p.S > 1) cluster_sync_all();  // no CTA leaves while a partner may still touch its shared memory
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, tmem_cols);
@@ -481,17 +546,39 @@ static bool make_b_map(CUtensorMap* map, const void* B, int K, int N, int N_pad,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr int kSmemBudget = 216 * 1024;
+constexpr int kSmemBudget = 216 * 1024;           // one CTA per SM
+constexpr int kSmemBudgetTwoPerSm = 108 * 1024;  // two CTAs per SM
 constexpr int kDefaultHostCtas = 16;
 constexpr int kDefaultHostWindow = 4;
 
-template <int N>
-static cudaError_t launch_core(const GemmParams& p, const CUtensorMap& bmap, int grid, int smem, cudaStream_t s) {
-    auto k = gemm_core_kernel<N>;
+// Launch with the optional cluster dimension and programmatic-dependent-launch attribute.
+template <typename Kernel>
+static cudaError_t launch_ex(Kernel k, int grid, int threads, int smem, int cluster, bool pdl, cudaStream_t s,
+                             const GemmParams& p, const CUtensorMap& bmap) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    k<<<grid, kCoreThreads, smem, s>>>(p, bmap);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = static_cast<unsigned>(cluster);
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = static_cast<unsigned>(n);
+    return cudaLaunchKernelEx(&cfg, k, p, bmap);
 }
 
 dak_status launch_gemm(const dak_placement* A, const void* host_src, const void* B, void* C, int N, int c_fp32,
@@ -519,31 +606,89 @@ dak_status launch_gemm(const dak_placement* A, const void* host_src, const void*
     p.h = A->h;
     p.c_fp32 = c_fp32 ? 1 : 0;
     p.tile_bytes = A->tile_bytes;
+    p.S = 1;
     p.st = status_ptr();
     if (!p.st) return DAK_ERR_CUDA;
 
     const bool umma = N >= 8;
     const int kind = umma ? kUmmaB : kCoreB;
-    // chunk width: 64 KiB A copies where two such stages fit, 32 KiB otherwise
-    int kc = umma ? (p.N_pad <= 32 ? 512 : (p.N_pad <= 64 ? 256 : (p.N_pad <= 128 ? 128 : 64))) : 512;
-    if (t && t->chunk_k > 0) kc = t->chunk_k;
+    const int sms = device_sm_count();
+    const int rows_b = umma ? p.N_pad : N;
+    auto stage_of = [&](int k) { return (k * 128 + k * 2 * rows_b + 1023) & ~1023; };
+
+    // Cluster split of each tile row's K range, chosen from the shape only (never from the
+    // placement, so that results are bit-identical across offload ratios): when there are
+    // fewer tile rows than SMs, S CTAs share a tile row and two CTAs run on each SM, which
+    // multiplies the copy streams that keep HBM busy.
+    auto red_of = [&](int s_) { return (s_ - 1) * kTileM * p.N_pad * 4; };
+    // two stages of at least 128 columns beside the partial-sum area
+    auto fits = [&](int s_, int budget_) { return 2 * stage_of(128) + red_of(s_) + 1024 <= budget_; };
+    // CTAs of one cluster wait on each other, so they must never wait for TMEM: a split is
+    // used only while two CTAs' accumulators (2 x 2 x N_pad columns) fit in one SM's TMEM.
+    const bool can_split = umma && p.N_pad <= 128 && !(t && t->split_k == 1);
+    int S = 1, per_sm = 1;
+    if (can_split && (p.T < sms || (t && t->split_k > 1))) {
+        const bool user = t && t->split_k > 1;
+        // automatic: enough CTAs for two per SM, but each CTA still streams >= ~448 KiB of its
+        // tile row (shorter slices are dominated by per-launch and pipeline-fill costs)
+        const int by_bytes = static_cast<int>(p.tile_bytes / (448 * 1024));
+        const int want = user ? std::min(8, t->split_k)
+                              : std::max(1, std::min(8, std::min((2 * sms) / p.T, by_bytes)));
+        if (fits(want, kSmemBudgetTwoPerSm)) {
+            S = want;
+            per_sm = want > 1 ? 2 : 1;
+        } else {
+            S = user ? want : std::max(1, std::min(8, sms / p.T));
+            while (S > 1 && red_of(S) + 2 * stage_of(64) + 1024 > kSmemBudget) --S;
+        }
+    }
+    const int budget = per_sm == 2 ? kSmemBudgetTwoPerSm : kSmemBudget;
+    int kc;
+    if (t && t->chunk_k > 0) {
+        kc = t->chunk_k;
+    } else if (!umma) {
+        kc = 512;
+    } else if (S > 1) {
+        // the widest chunk that leaves two stages beside the partial-sum area
+        kc = 64;
+        for (int cand : {512, 384, 256, 192, 128}) {
+            if (2 * stage_of(cand) + red_of(S) + 1024 <= budget) {
+                kc = cand;
+                break;
+            }
+        }
+    } else {
+        // 64 KiB A copies where two such stages fit, 32 KiB otherwise
+        kc = p.N_pad <= 32 ? 512 : (p.N_pad <= 64 ? 256 : (p.N_pad <= 128 ? 128 : 64));
+    }
     if (kc % 64 != 0 || kc > 1024 || (!umma && kc % 256 != 0)) return DAK_ERR_INVALID;
     p.kc = kc;
-    int stage = kc * 128 + kc * 2 * (umma ? p.N_pad : N);
-    stage = (stage + 1023) & ~1023;
-    int stages = std::min(8, kSmemBudget / stage);
+    const int nch = (p.K_pad + kc - 1) / kc;
+    S = std::min(S, nch);
+    if (S == 1) per_sm = 1;
+    p.S = S;
+    const int red_bytes = S > 1 ? red_of(S) : 0;
+    const int stage = stage_of(kc);
+    const int ring_budget = per_sm == 2 ? kSmemBudgetTwoPerSm : kSmemBudget;
+    const int stages = std::min(8, (ring_budget - red_bytes - (umma ? 1024 : 0)) / stage);
     if (stages < 1 || (stages < 2 && !(t && t->chunk_k > 0))) return DAK_ERR_INVALID;
     p.stages = stages;
     p.stage_bytes = stage;
-    const int smem = stages * stage + (umma ? 1024 : 0);
+    p.red_off = stages * stage;
+    const int smem = stages * stage + red_bytes + (umma ? 1024 : 0);
 
-    Sched sc = schedule(p.h, p.T - p.h, device_sm_count(), t, kDefaultHostCtas, std::min(kDefaultHostWindow, stages),
-                        stages, stages);
+    // schedule in cluster units
+    dak_tuning tc{};
+    if (t) tc = *t;
+    tc.host_ctas = std::max(1, (tc.host_ctas > 0 ? tc.host_ctas : kDefaultHostCtas) / S);
+    if (tc.hbm_ctas > 0) tc.hbm_ctas = std::max(1, tc.hbm_ctas / S);
+    Sched sc = schedule(p.h, p.T - p.h, (sms * per_sm) / S, &tc, kDefaultHostCtas,
+                        std::min(kDefaultHostWindow, stages), stages, stages);
     p.n_host_ctas = sc.n_host_ctas;
     p.n_hbm_ctas = sc.n_hbm_ctas;
     p.host_window = sc.host_window;
     p.hbm_window = sc.hbm_window;
-    const int grid = p.n_host_ctas + p.n_hbm_ctas;
+    const int grid = (p.n_host_ctas + p.n_hbm_ctas) * S;
     if (grid == 0) return DAK_OK;
     if (p.h > 0 && !p.a_host) return DAK_ERR_INVALID;
 
@@ -552,21 +697,19 @@ dak_status launch_gemm(const dak_placement* A, const void* host_src, const void*
     if (!make_b_map(&bmap, B, p.K, N, p.N_pad, kc, kind, &b3d)) return DAK_ERR_CUDA;
     p.b3d = b3d;
 
+    const bool pdl = t && t->pdl > 0;
     cudaError_t e;
     if (umma) {
-        e = cudaFuncSetAttribute(gemm_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return cuda_status(e);
-        gemm_umma_kernel<<<grid, kUmmaThreads, smem, stream>>>(p, bmap);
-        e = cudaGetLastError();
+        e = launch_ex(gemm_umma_kernel, grid, kUmmaThreads, smem, S, pdl, stream, p, bmap);
     } else {
         switch (N) {
-            case 1: e = launch_core<1>(p, bmap, grid, smem, stream); break;
-            case 2: e = launch_core<2>(p, bmap, grid, smem, stream); break;
-            case 3: e = launch_core<3>(p, bmap, grid, smem, stream); break;
-            case 4: e = launch_core<4>(p, bmap, grid, smem, stream); break;
-            case 5: e = launch_core<5>(p, bmap, grid, smem, stream); break;
-            case 6: e = launch_core<6>(p, bmap, grid, smem, stream); break;
-            default: e = launch_core<7>(p, bmap, grid, smem, stream); break;
+            case 1: e = launch_ex(gemm_core_kernel<1>, grid, kCoreThreads, smem, 1, pdl, stream, p, bmap); break;
+            case 2: e = launch_ex(gemm_core_kernel<2>, grid, kCoreThreads, smem, 1, pdl, stream, p, bmap); break;
+            case 3: e = launch_ex(gemm_core_kernel<3>, grid, kCoreThreads, smem, 1, pdl, stream, p, bmap); break;
+            case 4: e = launch_ex(gemm_core_kernel<4>, grid, kCoreThreads, smem, 1, pdl, stream, p, bmap); break;
+            case 5: e = launch_ex(gemm_core_kernel<5>, grid, kCoreThreads, smem, 1, pdl, stream, p, bmap); break;
+            case 6: e = launch_ex(gemm_core_kernel<6>, grid, kCoreThreads, smem, 1, pdl, stream, p, bmap); break;
+            default: e = launch_ex(gemm_core_kernel<7>, grid, kCoreThreads, smem, 1, pdl, stream, p, bmap); break;
         }
     }
     return cuda_status(e);

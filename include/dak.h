@@ -56,6 +56,14 @@ typedef struct dak_placement dak_placement;
  *   n_split   : attention context splits per (request, kv head); fixed per call and
  *               independent of the placement, so results do not depend on the offload ratio.
  *   hbm_ctas  : cap on CTAs reading HBM (0 = every remaining SM).
+ *   split_k   : GEMM CTAs per tile row (a thread-block cluster that splits the K range and
+ *               reduces in fixed rank order); 0 = chosen from the shape, 1 = no split.
+ *               Like chunk_k it changes the summation order, never with the offload ratio.
+ *   pdl       : 1 = programmatic dependent launch: the kernel may start while the previous
+ *               kernel of the stream is still running; it streams the weights / KV cache at
+ *               once and waits for that kernel only before reading B / Q and writing C / O.
+ *               Set it only when the previous kernel does not write the operand being
+ *               streamed (e.g. not right after a KV-cache append for dak_attn). 0 = off.
  */
 typedef struct {
     int host_ctas;
@@ -64,6 +72,8 @@ typedef struct {
     int chunk_k;
     int n_split;
     int hbm_ctas;
+    int split_k;
+    int pdl;
 } dak_tuning;
 
 /* ---------------------------------------------------------------------------------- *
@@ -113,9 +123,11 @@ dak_status dak_placement_info(const dak_placement* p, int64_t* host_bytes, int64
  *   N : 1 .. 256.
  * One persistent launch: `host_ctas` CTAs stream the host tile rows and the other CTAs
  * the HBM tile rows; every CTA reads from exactly one tier and writes disjoint rows of
- * C. Each output row is accumulated in fp32 over K in the same order whatever tier its
- * tile row is in, so the result does not depend on n_host_tiles. N < 8 runs on CUDA
- * cores; N >= 8 on the tcgen05 tensor cores. */
+ * C. When the matrix has fewer tile rows than SMs, a cluster of CTAs shares each tile row,
+ * each accumulating a fixed part of K, and the cluster's leader adds the partial tiles in
+ * rank order through distributed shared memory. Every output row is accumulated in fp32
+ * in an order fixed by the shape alone, so the result does not depend on n_host_tiles.
+ * N < 8 runs on CUDA cores; N >= 8 on the tcgen05 tensor cores. */
 dak_status dak_gemm(const dak_placement* A, const void* B, void* C, int N, int c_fp32, const dak_tuning* tuning,
                     void* stream);
 

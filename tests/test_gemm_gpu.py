@@ -90,13 +90,42 @@ def test_bit_identical_across_offload_ratio(dak, N):
 
 @pytest.mark.parametrize("N", [1, 16])
 def test_bit_identical_across_tuning(dak, N):
+    """Knobs that only move work between CTAs (host CTA count, windows, HBM CTA cap) leave
+    every bit of the result unchanged; chunk width and split count change the summation
+    order and are checked against the oracle instead."""
     M, K = 640, 2048
     A, B = synth.gemm_inputs(M, K, N, seed=4)
     base = bits_of(_run(dak, A, B, 4))
-    chunks = [dict(chunk_k=256), dict(chunk_k=512, hbm_ctas=3)] if N < 8 else \
-        [dict(chunk_k=64), dict(chunk_k=128, hbm_ctas=3), dict(chunk_k=256)]
-    for tun in [dict(host_ctas=1), dict(host_ctas=3, window=1), dict(window=2, hbm_window=2)] + chunks:
+    for tun in [dict(host_ctas=1), dict(host_ctas=3, window=1), dict(window=2, hbm_window=2), dict(hbm_ctas=3)]:
         assert np.array_equal(bits_of(_run(dak, A, B, 4, tuning=tun)), base), tun
+    ref = og.gemm_ref(A, B)
+    chunks = [dict(chunk_k=256), dict(chunk_k=512)] if N < 8 else \
+        [dict(chunk_k=64), dict(chunk_k=128, split_k=1), dict(chunk_k=256, split_k=2)]
+    for tun in chunks:
+        assert og.rel_err(to_np(_run(dak, A, B, 4, tuning=tun)), ref) <= FP32_OUT_TOL, tun
+
+
+@pytest.mark.parametrize("N", [8, 32, 64])
+@pytest.mark.parametrize("S", [1, 2, 3, 4, 8])
+def test_cluster_split_k(dak, N, S):
+    """Each tile row's K range split over S CTAs of a cluster, partials reduced by the
+    leader in rank order: matches the oracle and is identical for every offload ratio."""
+    M, K = 384, 3072  # 6 tile rows
+    A, B = synth.gemm_inputs(M, K, N, seed=S * 100 + N)
+    ref = og.gemm_ref(A, B)
+    tun = dict(split_k=S)
+    base = _run(dak, A, B, 0, tuning=tun)
+    assert og.rel_err(to_np(base), ref) <= FP32_OUT_TOL
+    for h in (1, 3, 6):
+        assert np.array_equal(bits_of(_run(dak, A, B, h, tuning=tun)), bits_of(base)), h
+
+
+def test_split_k_integer_exact(dak):
+    M, K, N = 256, 4096, 32
+    A, B = synth.gemm_inputs(M, K, N, seed=17, integer=True)
+    for S in (2, 4, 8):
+        C = _run(dak, A, B, 1, tuning=dict(split_k=S))
+        assert np.array_equal(to_np(C), og.gemm_ref(A, B)), S
 
 
 def test_device_source_placement(dak):
@@ -155,3 +184,31 @@ def test_8b_linears_full_size_sampled(dak, name, N):
     rows = rows[(rows >= 0) & (rows < M)]
     ref = og.gemm_ref(A[rows], B)
     assert og.rel_err(C[:, rows], ref) <= REL_TOL
+
+
+def test_programmatic_launch_chain(dak):
+    """pdl = 1 lets a kernel start while the previous one runs; the hidden states (and Q)
+    are read only after it finishes. Chain: C1 = A1.B, C2 = A2.C1, attention over Q = C1;
+    every result must equal the plainly launched one bit for bit."""
+    import torch
+    A1, B = synth.gemm_inputs(1024, 512, 16, seed=31)
+    A2, _ = synth.gemm_inputs(256, 1024, 16, seed=32)
+    _, k, v = synth.attn_inputs(16, 16, 4, 64, 300, seed=33)
+    p1, p2 = dak.dak_place_matrix(A1, 3), dak.dak_place_matrix(A2, 1)
+    kv = dak.dak_place_kv(k, v, 5)
+    Bt = to_dev(B)
+    outs = []
+    for pdl in (0, 1):
+        tun = dict(pdl=pdl)
+        C1 = dak.dak_gemm(p1, Bt, tuning=tun)
+        C2 = dak.dak_gemm(p2, C1, tuning=tun)
+        O = dak.dak_attn(C1.view(16, 16, 64), kv, tuning=tun)
+        C3 = dak.dak_gemm(p2, C1, tuning=dict(pdl=pdl, split_k=4))
+        assert dak.dak_last_error()[0] == 0
+        outs.append([bits_of(x) for x in (C1, C2, O, C3)])
+    for a, b in zip(*outs):
+        assert np.array_equal(a, b)
+    assert og.rel_err(to_np(torch.from_numpy(outs[0][1].view(np.int16)).view(torch.bfloat16)),
+                      og.gemm_ref(A2, outs[0][0])) <= REL_TOL
+    for p in (p1, p2, kv):
+        p.free()

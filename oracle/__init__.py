@@ -17,7 +17,9 @@ Modules:
 * ``placement``  -- tile rows / requests per tier, global offload ratio, host-link traffic.
 * ``planner``    -- the per-operation offload optimisation problem ([DAK] section 4.2,
   Appendix A eq. (1)) solved by exhaustive search.
+* ``decoder``    -- one decode step of a Llama-shaped transformer around those two
+  operations ([DAK] sections 3, 5 and 6.1).
 
 Parity status of each function is stated in its module docstring; none is unpinned.
 """
-from . import bf16, gemm, attention, placement, planner  # noqa: F401
+from . import bf16, gemm, attention, placement, planner, decoder  # noqa: F401

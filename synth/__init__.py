@@ -134,3 +134,58 @@ def attn_kv_request(b: int, h_kv: int, head_dim: int, context: int, seed: int = 
     k = normal_bf16(s, 12, per, offset=b * per).reshape(h_kv, context, head_dim)
     v = normal_bf16(s, 13, per, offset=b * per).reshape(h_kv, context, head_dim)
     return k, v
+
+
+# Decode step of a Llama-shaped transformer. Weights ~N(0, 0.02); RMSNorm gains ~N(1, 0.1)
+# (not all ones, so that a dropped gain shows); hidden states and the cached keys and values
+# ~N(0, 1). Tensor t of layer l uses stream 1000 + 16 l + t.
+DECODER_8B = dict(n_layers=32, hidden=4096, n_heads=32, n_kv_heads=8, head_dim=128, ffn=14336,
+                  batch=16, context=4096, rms_eps=1e-5, rope_theta=500000.0)
+DECODER_70B = dict(n_layers=80, hidden=8192, n_heads=64, n_kv_heads=8, head_dim=128, ffn=28672,
+                   batch=16, context=16384, rms_eps=1e-5, rope_theta=500000.0)
+NORM_STD = 0.1
+
+_DEC_TENSORS = ("qkv", "o", "gate_up", "down", "attn_norm", "mlp_norm", "k_cache", "v_cache")
+
+
+def decoder_shapes(cfg: dict) -> dict:
+    """[out][in] shape of each weight of one layer, and [d] of each norm gain."""
+    d, Hq, Hkv, D, f = (cfg["hidden"], cfg["n_heads"], cfg["n_kv_heads"], cfg["head_dim"],
+                        cfg["ffn"])
+    return {"qkv": ((Hq + 2 * Hkv) * D, d), "o": (d, Hq * D), "gate_up": (2 * f, d),
+            "down": (d, f), "attn_norm": (d,), "mlp_norm": (d,)}
+
+
+def decoder_stream(layer: int, name: str) -> int:
+    return 1000 + 16 * layer + _DEC_TENSORS.index(name)
+
+
+def decoder_tensor(cfg: dict, layer: int, name: str, seed: int = 0) -> np.ndarray:
+    """One weight ([out][in]) or norm gain ([d]) of layer `layer`, as bf16 bits."""
+    shape = decoder_shapes(cfg)[name]
+    n = int(np.prod(shape))
+    if name.endswith("_norm"):
+        return normal_bf16(seed, decoder_stream(layer, name), n, 1.0, NORM_STD).reshape(shape)
+    return normal_bf16(seed, decoder_stream(layer, name), n, 0.0, WEIGHT_STD).reshape(shape)
+
+
+def decoder_layer(cfg: dict, layer: int, seed: int = 0) -> dict:
+    return {name: decoder_tensor(cfg, layer, name, seed) for name in decoder_shapes(cfg)}
+
+
+def decoder_final_norm(cfg: dict, seed: int = 0) -> np.ndarray:
+    return normal_bf16(seed, 999, cfg["hidden"], 1.0, NORM_STD)
+
+
+def decoder_x0(cfg: dict, batch: int, seed: int = 0) -> np.ndarray:
+    """Hidden states entering layer 0 (the embedding output), [batch][d]."""
+    return normal_bf16(seed, 998, batch * cfg["hidden"]).reshape(batch, cfg["hidden"])
+
+
+def decoder_kv(cfg: dict, layer: int, batch: int, capacity: int, seed: int = 0):
+    """Cached keys and values of layer `layer`, [batch][Hkv][capacity][D] each ~N(0, 1)."""
+    n = batch * cfg["n_kv_heads"] * capacity * cfg["head_dim"]
+    shape = (batch, cfg["n_kv_heads"], capacity, cfg["head_dim"])
+    k = normal_bf16(seed, decoder_stream(layer, "k_cache"), n).reshape(shape)
+    v = normal_bf16(seed, decoder_stream(layer, "v_cache"), n).reshape(shape)
+    return k, v

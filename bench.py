@@ -41,6 +41,10 @@ def _args():
     ap.add_argument("--batch", type=int, default=32)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--decode", default="8b", choices=["8b", "70b", "none"],
+                    help="also time a full decode step of this model (planner ratios at --decode-x)")
+    ap.add_argument("--decode-x", type=float, default=0.3, help="x_global of the decode step's HBM cap")
+    ap.add_argument("--decode-steps", type=int, default=20)
     ap.add_argument("--profile", default=None, choices=["attn", "qkv", "o", "gate_up", "down"],
                     help="place one operation of the step at --x and launch it --steps times (for ncu)")
     return ap.parse_args()
@@ -144,6 +148,147 @@ class Step:
         for p in self.pl.values():
             p.free()
         self.kv.free()
+
+
+# ------------------------------------------------------------------------------ decode step
+
+def decode_ops(cfg, peak_flops):
+    """The planner's view of one decode step, one entry per operation type (every layer is
+    alike, so each type gets one ratio for all layers): the four weight products and the
+    attention over the KV cache, with their bytes and compute time over all layers at
+    peak_flops, and their placement unit (a 64-row tile row or one request's KV)."""
+    import synth
+    sh = synth.decoder_shapes(cfg)
+    nl, B, L, D = cfg["n_layers"], cfg["batch"], cfg["context"], cfg["head_dim"]
+    kv_req = 2 * cfg["n_kv_heads"] * L * D * 2
+    ops, meta = [], []
+    for k in ("qkv", "o", "gate_up", "down"):
+        M, K = sh[k]
+        ops.append((nl * M * K * 2, nl * 2.0 * M * K * B / peak_flops, 64 * K * 2))
+        meta.append((k, -(-M // 64)))
+    ops.append((nl * B * kv_req, nl * 4.0 * B * cfg["n_heads"] * L * D / peak_flops, kv_req))
+    meta.append(("kv", B))
+    return ops, meta
+
+
+def decode_plan(dak, cfg, b_host, b_hbm, x_global, peak_flops):
+    """Host units per operation type (tile rows or requests, the same in every layer) for an
+    HBM cap of (1 - x_global) of all bytes: the planner's greedy ratios (">=" budget), whose
+    tie-break gives every operation the same fraction of its segment, floored to whole
+    units and topped up one unit at a time where the model time grows least (to the
+    picosecond; ties go to the operation whose ratio stays lowest) until the budget is met.
+    x_global = 0: no offload."""
+    ops, meta = decode_ops(cfg, peak_flops)
+    nl = cfg["n_layers"]
+    if x_global <= 0:
+        return [{k: 0 for k, _ in meta} for _ in range(nl)], sum(o[0] for o in ops) / b_hbm
+    total = sum(o[0] for o in ops)
+    D = x_global * total
+    ratios, _ = dak.dak_plan_ratios(ops, b_host, b_hbm, D, 0)
+    counts = [min(n, int(r * n + 1e-9)) for (k, n), r in zip(meta, ratios)]
+
+    def t_op(i, c):
+        C, tc, _ = ops[i]
+        b = C * c / meta[i][1]
+        return max(tc, (C - b) / b_hbm, b / b_host)
+
+    def host():
+        return sum(o[0] * c / m[1] for o, c, m in zip(ops, counts, meta))
+
+    while host() < D * (1 - 1e-12):
+        best = min((i for i in range(len(ops)) if counts[i] < meta[i][1]),
+                   key=lambda i: (round((t_op(i, counts[i] + 1) - t_op(i, counts[i])) * 1e12),
+                                  (counts[i] + 1) / meta[i][1]))
+        counts[best] += 1
+    tmodel = sum(t_op(i, c) for i, c in enumerate(counts))
+    return [{k: int(c) for (k, _), c in zip(meta, counts)} for _ in range(nl)], tmodel
+
+
+def build_decoder(dak, cfg, units, seed=0):
+    """Random-init bf16 weights and KV cache drawn on the GPU, placed layer by layer."""
+    import synth
+    layers = []
+    for l in range(cfg["n_layers"]):
+        w = {k: synth.decoder_tensor_dev(cfg, l, k, seed) for k in synth.decoder_shapes(cfg)}
+        kv = synth.decoder_kv_dev(cfg, l, cfg["batch"], cfg["context"], seed)
+        layers.append(dak.place_decoder_layer(w, kv, units[l]))
+        del w, kv
+    fn = synth.dev_normal_bf16(seed, 999, cfg["hidden"], 1.0, synth.NORM_STD)
+    return dak.Decoder(cfg, layers, fn)
+
+
+def run_decode(dak, args, b_host, b_hbm, dev, sync_all, local):
+    """Full decode step: planner-chosen per-op ratios at x_global, one CUDA graph per mode."""
+    import torch
+    import synth
+    cfg = dict(synth.DECODER_8B if args.decode == "8b" else synth.DECODER_70B)
+    pk, _ = peaks()
+    peak_flops = pk.get("bf16_tflops_sustained", 1700.0) * 1e12
+    B, d, L = cfg["batch"], cfg["hidden"], cfg["context"]
+    x_in = torch.from_numpy(synth.decoder_x0(cfg, B).view("int16")).view(torch.bfloat16).to(dev)
+    pos = torch.full((B,), L - 1, dtype=torch.int32, device=dev)  # context L: L - 1 cached + the new token
+    out = torch.empty_like(x_in)
+    res = {"workload": f"{cfg['n_layers']}-layer {args.decode.upper()}-shaped decode step (hidden {d}, GQA "
+                       f"{cfg['n_heads']}/{cfg['n_kv_heads']}, head dim {cfg['head_dim']}, FFN {cfg['ffn']}, "
+                       f"RMSNorm, RoPE, SwiGLU), random-init bf16, batch {B}, context {L}",
+           "batch": B, "context": L, "x_global_target": args.decode_x}
+    for xg, key in ((args.decode_x, None), (0.0, "hbm_only")):
+        t0 = time.time()
+        units, tmodel = decode_plan(dak, cfg, b_host, b_hbm, xg, peak_flops)
+        dec = build_decoder(dak, cfg, units)
+        build_s = time.time() - t0
+        C = sum(L_[k].host_bytes + L_[k].hbm_bytes for L_ in dec.layers for k in dak.DECODER_OPS)
+        H = dec.host_bytes()
+        dec.capture(x_in, pos, out, dak.MODE_DIRECT)
+        for _ in range(3):
+            dec.replay()
+        torch.cuda.synchronize()
+        st0 = dak.dak_last_error()[0]
+        sampler = ClockSampler(local)
+        sampler.start()
+        time.sleep(0.2)
+        tw0 = time.time()
+        t = time_steps(dec.replay, args.decode_steps, 2, sync_all)
+        tw1 = time.time()
+        time.sleep(0.2)
+        sampler.stop()
+        roof = tier_roofline(C, H / C, b_host, b_hbm)
+        rec = {"x_effective": H / C, "bytes_per_step": C, "host_bytes_per_step": H, "ms_per_step": t * 1e3,
+               "tok_s": B / t, "eff_gbps": C / t / 1e9, "roofline_gbps": roof / 1e9, "frac": (C / t) / roof,
+               "planner_model_ms": tmodel * 1e3, "host_units_per_layer": units[0] if units else {},
+               "build_s": build_s,
+               "launches_per_step": dec.launches(), "clocks": sampler.summary(tw0, tw1)}
+        if xg > 0:
+            for mode, name in ((dak.MODE_PREFETCH_SERIAL, "prefetch_serial"), (dak.MODE_PREFETCH_OVERLAP,
+                                                                                 "prefetch_overlap")):
+                dec.capture(x_in, pos, out, mode)
+                tp = time_steps(dec.replay, max(5, args.decode_steps // 2), 2, sync_all)
+                rec[name + "_tok_s"] = B / tp
+            rec["vs_prefetch_best"] = rec["tok_s"] / max(rec["prefetch_serial_tok_s"], rec["prefetch_overlap_tok_s"])
+            # end to end: the step's hidden states and positions copied in from pinned host
+            # memory and its output copied back, every step
+            dec.capture(x_in, pos, out, dak.MODE_DIRECT)
+            hx, hp = x_in.cpu().pin_memory(), pos.cpu().pin_memory()
+            ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+            def e2e():
+                x_in.copy_(hx, non_blocking=True)
+                pos.copy_(hp, non_blocking=True)
+                dec.replay()
+                ho.copy_(out, non_blocking=True)
+
+            te = time_steps(e2e, max(5, args.decode_steps // 2), 2, sync_all)
+            rec["e2e"] = {"tok_s": B / te, "eff_gbps": C / te / 1e9, "h2d_bytes_per_step": hx.numel() * 2 + B * 4,
+                          "d2h_bytes_per_step": ho.numel() * 2}
+        rec["status"] = [st0, dak.dak_last_error()[0]]
+        dec.free()
+        del dec
+        torch.cuda.empty_cache()
+        if key:
+            res[key] = rec
+        else:
+            res.update(rec)
+    return res
 
 
 # ------------------------------------------------------------------------------ clocks
@@ -452,6 +597,8 @@ def main():
     achieved = att_bytes / (att_ms / 1e3)
     traffic = read_ncu_traffic()
 
+    decode = run_decode(dak, args, b_host, b_hbm, dev, sync_all, local) if args.decode != "none" else None
+
     cpu = None
     if rank == 0 and not args.no_cpu:
         gbps, sample, _ = cpu_oracle_sample(lin, attn)
@@ -481,6 +628,8 @@ def main():
         "clocks": clocks,
         "status": [status[0], status2[0], status3[0]],
     }
+    if decode:
+        line["decode_step"] = decode
     if cpu:
         line["cpu_baseline"] = cpu
     st.free()

@@ -27,6 +27,8 @@ EXPORTS = [
     "dak_gemm", "dak_attn_workspace_bytes", "dak_attn", "dak_attn_default_split", "dak_plan_ratios",
     "dak_last_error", "dak_sm_count", "dak_probe_read_bw", "dak_probe_concurrent", "dak_prefetch",
     "dak_gemm_staged", "dak_attn_staged", "dak_attn_noalloc", "dak_selftest_wait",
+    "dak_decoder_create", "dak_decoder_batch", "dak_decoder_step", "dak_decoder_capture",
+    "dak_decoder_replay", "dak_decoder_launches", "dak_decoder_free",
 ]
 
 # size of the fixed device array dak_attn_noalloc uses (DAK_NOALLOC_SCRATCH_BYTES in dak.h)
@@ -47,6 +49,19 @@ class dak_tuning(ctypes.Structure):
 
 class dak_op(ctypes.Structure):
     _fields_ = [("bytes", ctypes.c_double), ("t_comp", ctypes.c_double), ("tile_bytes", ctypes.c_double)]
+
+
+class dak_decoder_config(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int), ("hidden", ctypes.c_int), ("n_heads", ctypes.c_int),
+                ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("ffn", ctypes.c_int),
+                ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float), ("n_split", ctypes.c_int),
+                ("plain_launch", ctypes.c_int)]
+
+
+class dak_decoder_layer(ctypes.Structure):
+    _fields_ = [("qkv", ctypes.c_void_p), ("o", ctypes.c_void_p), ("gate_up", ctypes.c_void_p),
+                ("down", ctypes.c_void_p), ("kv", ctypes.c_void_p), ("attn_norm", ctypes.c_void_p),
+                ("mlp_norm", ctypes.c_void_p)]
 
 
 def _load():
@@ -76,6 +91,13 @@ def _load():
         "dak_prefetch": (i32, [vp, vp, vp]),
         "dak_attn_noalloc": (i32, [vp, vp, vp, i32, ctypes.c_float, vp, P(dak_tuning), vp]),
         "dak_selftest_wait": (i32, [vp]),
+        "dak_decoder_create": (i32, [P(dak_decoder_config), P(dak_decoder_layer), vp, P(vp)]),
+        "dak_decoder_batch": (i32, [vp]),
+        "dak_decoder_step": (i32, [vp, vp, vp, vp, i32, vp]),
+        "dak_decoder_capture": (i32, [vp, vp, vp, vp, i32]),
+        "dak_decoder_replay": (i32, [vp, vp]),
+        "dak_decoder_launches": (i32, [vp, i32]),
+        "dak_decoder_free": (i32, [vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -358,3 +380,101 @@ def dak_probe_concurrent(host_bytes: int, hbm_bytes: int, host_ctas: int, host_w
     _check(lib.dak_probe_concurrent(host_bytes, hbm_bytes, host_ctas, host_window, hbm_ctas, hbm_window, chunk_bytes,
                                     iters, ctypes.byref(h), ctypes.byref(g)), "dak_probe_concurrent")
     return h.value, g.value
+
+
+# ------------------------------------------------------------------------------- decode step
+
+DECODER_OPS = ("qkv", "o", "gate_up", "down", "kv")
+MODE_DIRECT, MODE_PREFETCH_SERIAL, MODE_PREFETCH_OVERLAP = 0, 1, 2
+
+
+class Decoder:
+    """A dak_decoder over placed layers. `layers` is a list of dicts with the placements
+    'qkv', 'o', 'gate_up', 'down', 'kv' and the bf16 CUDA gains 'attn_norm', 'mlp_norm';
+    the decoder keeps references to them (and frees the placements in .free())."""
+
+    def __init__(self, cfg: dict, layers, final_norm, n_split: int = 0, plain_launch: bool = False):
+        c = dak_decoder_config(n_layers=len(layers), hidden=int(cfg["hidden"]), n_heads=int(cfg["n_heads"]),
+                               n_kv_heads=int(cfg["n_kv_heads"]), head_dim=int(cfg["head_dim"]),
+                               ffn=int(cfg["ffn"]), rms_eps=float(cfg.get("rms_eps", 1e-5)),
+                               rope_theta=float(cfg.get("rope_theta", 500000.0)), n_split=int(n_split),
+                               plain_launch=int(bool(plain_launch)))
+        for L in layers:
+            _check_bf16_cuda(L["attn_norm"], "attn_norm")
+            _check_bf16_cuda(L["mlp_norm"], "mlp_norm")
+        _check_bf16_cuda(final_norm, "final_norm")
+        arr = (dak_decoder_layer * max(1, len(layers)))()
+        for i, L in enumerate(layers):
+            arr[i] = dak_decoder_layer(L["qkv"].handle, L["o"].handle, L["gate_up"].handle, L["down"].handle,
+                                       L["kv"].handle, L["attn_norm"].data_ptr(), L["mlp_norm"].data_ptr())
+        out = ctypes.c_void_p()
+        _check(lib.dak_decoder_create(ctypes.byref(c), arr, _ptr(final_norm), ctypes.byref(out)),
+               "dak_decoder_create")
+        self._h = out
+        self.cfg = dict(cfg)
+        self.layers = list(layers)
+        self.final_norm = final_norm
+        self.batch = int(lib.dak_decoder_batch(out))
+
+    @property
+    def handle(self):
+        if self._h is None:
+            raise ValueError("decoder already freed")
+        return self._h
+
+    def launches(self, mode: int = MODE_DIRECT) -> int:
+        return int(lib.dak_decoder_launches(self.handle, int(mode)))
+
+    def host_bytes(self) -> int:
+        return sum(L[k].host_bytes for L in self.layers for k in DECODER_OPS)
+
+    def step(self, x_in, positions, out=None, mode: int = MODE_DIRECT, stream=None):
+        """One decode step: x_in bf16 [B][d], positions int32 [B] (CUDA) -> out bf16 [B][d]."""
+        import torch
+        _check_bf16_cuda(x_in, "x_in")
+        if out is None:
+            out = torch.empty_like(x_in)
+        _check(lib.dak_decoder_step(self.handle, _ptr(x_in), _ptr(positions), _ptr(out), int(mode),
+                                    _stream_ptr(stream)), "dak_decoder_step")
+        return out
+
+    def capture(self, x_in, positions, out, mode: int = MODE_DIRECT):
+        """Capture one step with these buffers into the decoder's CUDA graph."""
+        _check(lib.dak_decoder_capture(self.handle, _ptr(x_in), _ptr(positions), _ptr(out), int(mode)),
+               "dak_decoder_capture")
+
+    def replay(self, stream=None):
+        _check(lib.dak_decoder_replay(self.handle, _stream_ptr(stream)), "dak_decoder_replay")
+
+    def free(self, placements: bool = True):
+        if self._h is not None:
+            lib.dak_decoder_free(self._h)
+            self._h = None
+        if placements:
+            for L in self.layers:
+                for k in DECODER_OPS:
+                    L[k].free()
+
+    def __del__(self):
+        try:
+            self.free(placements=False)
+        except Exception:
+            pass
+
+
+def place_decoder_layer(weights: dict, kv, host_units: dict, device=None) -> dict:
+    """Place one layer: weights maps 'qkv', 'o', 'gate_up', 'down' to [out][in] bf16 sources
+    (numpy bits or torch) and 'attn_norm', 'mlp_norm' to [d] gains; kv = (K, V) sources
+    [B][H_kv][L][D]; host_units maps each of DECODER_OPS to its host tile rows / requests."""
+    import torch
+    dev = device or torch.device("cuda")
+    L = {}
+    for k in ("qkv", "o", "gate_up", "down"):
+        L[k] = dak_place_matrix(weights[k], int(host_units[k]))
+    L["kv"] = dak_place_kv(kv[0], kv[1], int(host_units["kv"]))
+    for k in ("attn_norm", "mlp_norm"):
+        g = weights[k]
+        if isinstance(g, np.ndarray):
+            g = torch.from_numpy(g.view(np.int16)).view(torch.bfloat16)
+        L[k] = g.to(dev).contiguous()
+    return L

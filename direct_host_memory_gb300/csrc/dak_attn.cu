@@ -34,6 +34,7 @@ struct AttnParams {
     __nv_bfloat16* O;        // [B][Hq][D]
     float* ws;               // [B][Hq][n_split][D + 2] partials: m (log2 domain), l, o[D]
     int B, Hq, Hkv, G, L, h_r, n_split, split_len;
+    int wait_newest;         // stream the chunk holding token L_b - 1 only after the previous kernel
     float scale_log2;
     long long head_bytes;    // bytes of one (request, kv head) slab
     int n_host_ctas, n_hbm_ctas, host_window, hbm_window;
@@ -72,6 +73,7 @@ __device__ __forceinline__ UnitRange units_of_cta(const AttnParams& p) {
 struct Unit {
     int b, g, s;
     int t0, t1;  // token range
+    int Lb;      // tokens of the request
     const uint8_t* base;  // the (request, kv head) slab
 };
 
@@ -84,6 +86,7 @@ __device__ __forceinline__ Unit decode_unit(const AttnParams& p, long long u, in
     x.s = rem - x.g * p.n_split;
     int Lb = p.L;
     if (p.seq_lens) Lb = min(max(p.seq_lens[x.b], 0), p.L);
+    x.Lb = Lb;
     x.t0 = x.s * p.split_len;
     x.t1 = min(Lb, x.t0 + p.split_len);
     const int lb = tier == 0 ? x.b : x.b - p.h_r;
@@ -129,10 +132,15 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnParams 
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
             long long i = 0;
+            bool waited = false;
             for (long long u = ur.begin; u < ur.end && !*abort; ++u) {
                 const Unit x = decode_unit(p, u, ur.tier);
                 for (int t = x.t0; t < x.t1; t += kChunkTok, ++i) {
                     const int s = static_cast<int>(i % W);
+                    if (p.wait_newest && !waited && t + kChunkTok >= x.Lb) {
+                        grid_dep_wait();  // this chunk holds the newest token, which the previous kernel writes
+                        waited = true;
+                    }
                     if (i >= W && !mbar_wait(&empty[s], static_cast<uint32_t>(((i / W) - 1) & 1), abort, p.st,
                                              DAK_ERR_TIMEOUT, A_PROD_EMPTY)) {
                         goto producer_done;
@@ -342,6 +350,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnParams 
 template <int D>
 __global__ void attn_combine_kernel(const float* __restrict__ ws, __nv_bfloat16* __restrict__ O, int rows,
                                     int n_split) {
+    grid_dep_wait();  // the partials come from the attention kernel just before
+    grid_dep_launch();
     const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -397,31 +407,34 @@ static int attn_ctas_per_sm(int W, int G) {
     return std::max(1, n);
 }
 
+// Launch with or without programmatic dependent launch (the kernel may start while the
+// previous kernel of the stream still runs; it calls griddepcontrol.wait where it must not).
+template <typename Kernel, typename... Args>
+static cudaError_t launch_maybe_pdl(Kernel k, int grid, int threads, int smem, bool pdl, cudaStream_t s,
+                                    Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k, args...);
+}
+
 template <int D>
 static cudaError_t launch_attn_d(const AttnParams& p, int grid, int W, bool pdl, cudaStream_t s) {
     const int smem = attn_smem_bytes<D>(W, p.G);
     cudaError_t e = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    if (pdl) {
-        cudaLaunchConfig_t cfg{};
-        cfg.gridDim = dim3(static_cast<unsigned>(grid));
-        cfg.blockDim = dim3(kAttnThreads);
-        cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-        cfg.stream = s;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, attn_kernel<D>, p);
-    } else {
-        attn_kernel<D><<<grid, kAttnThreads, smem, s>>>(p);
-        e = cudaGetLastError();
-    }
+    e = launch_maybe_pdl(attn_kernel<D>, grid, kAttnThreads, smem, pdl, s, p);
     if (e != cudaSuccess || p.n_split == 1) return e;
     const int rows = p.B * p.Hq;
-    attn_combine_kernel<D><<<(rows + 7) / 8, 256, 0, s>>>(p.ws, p.O, rows, p.n_split);
-    return cudaGetLastError();
+    return launch_maybe_pdl(attn_combine_kernel<D>, (rows + 7) / 8, 256, 0, pdl, s,
+                            static_cast<const float*>(p.ws), p.O, rows, p.n_split);
 }
 
 dak_status launch_attn(const void* Q, const dak_placement* KV, const void* host_src, const int* seq_lens, int H_q,
@@ -477,6 +490,7 @@ dak_status launch_attn(const void* Q, const dak_placement* KV, const void* host_
     if (grid == 0) return DAK_OK;
     const int W = std::max(p.host_window, p.hbm_window);
     const bool pdl = t && t->pdl > 0;
+    p.wait_newest = t && t->pdl == 2;
     cudaError_t e = KV->D == 128 ? launch_attn_d<128>(p, grid, W, pdl, stream) : launch_attn_d<64>(p, grid, W, pdl, stream);
     return cuda_status(e);
 }

@@ -62,8 +62,11 @@ typedef struct dak_placement dak_placement;
  *   pdl       : 1 = programmatic dependent launch: the kernel may start while the previous
  *               kernel of the stream is still running; it streams the weights / KV cache at
  *               once and waits for that kernel only before reading B / Q and writing C / O.
- *               Set it only when the previous kernel does not write the operand being
- *               streamed (e.g. not right after a KV-cache append for dak_attn). 0 = off.
+ *               Set it only when no kernel that may still be running writes the operand
+ *               being streamed or (dak_attn) seq_lens. 0 = off.
+ *               2 (dak_attn only) = as 1, except that the previous kernel may write the
+ *               newest token (index L_b - 1) of each request, e.g. a KV-cache append: the
+ *               chunk holding it is streamed only after that kernel has finished.
  */
 typedef struct {
     int host_ctas;
@@ -176,6 +179,104 @@ int dak_attn_default_split(const dak_placement* KV);
  *   one stream or with events. */
 dak_status dak_attn_noalloc(const void* Q, const dak_placement* KV, const int* seq_lens, int H_q, float scale,
                             void* O, const dak_tuning* tuning, void* stream);
+
+/* ---------------------------------------------------------------------------------- *
+ * Decode step of a Llama-shaped transformer around the two operations (sections 3, 5, 6.1)
+ * ---------------------------------------------------------------------------------- */
+
+/* Shape and numerics of the decoder. Fields <= 0 marked "default" take that default.
+ *   n_layers, hidden (d), n_heads (H_q), n_kv_heads (H_kv), head_dim (D: 64 or 128), ffn (f).
+ *   rms_eps   : RMSNorm epsilon (default 1e-5).
+ *   rope_theta: RoPE base (default 500000).
+ *   n_split   : attention context splits (default dak_attn_default_split of layer 0's cache).
+ *   plain_launch: 0 = the step's kernels use programmatic dependent launch, so that each
+ *               one streams its weights / KV cache while the previous one finishes;
+ *               1 = ordinary stream-ordered launches. */
+typedef struct {
+    int n_layers;
+    int hidden;
+    int n_heads;
+    int n_kv_heads;
+    int head_dim;
+    int ffn;
+    float rms_eps;
+    float rope_theta;
+    int n_split;
+    int plain_launch;
+} dak_decoder_config;
+
+/* One layer's operands, all placed by the caller beforehand (dak_place_matrix with the
+ * offload ratio of each operation, e.g. from dak_plan_ratios; dak_place_kv for the cache)
+ * and still owned by the caller, who frees them after dak_decoder_free.
+ *   qkv    : [(H_q + 2 H_kv) D] x d: query rows (head-major), then key rows, then value rows.
+ *   o      : d x (H_q D).
+ *   gate_up: 2f x d: the f gate rows, then the f up rows.
+ *   down   : d x f.
+ *   kv     : the layer's KV cache (B requests, H_kv heads, capacity L, head dim D); every
+ *            layer's cache has the same B, which is the step's batch.
+ *   attn_norm, mlp_norm: RMSNorm gains, bf16 [d], device memory. */
+typedef struct {
+    const dak_placement* qkv;
+    const dak_placement* o;
+    const dak_placement* gate_up;
+    const dak_placement* down;
+    const dak_placement* kv;
+    const void* attn_norm;
+    const void* mlp_norm;
+} dak_decoder_layer;
+
+typedef struct dak_decoder dak_decoder;
+
+/* Check the shapes, copy the layer table (not the operands) and allocate the step's
+ * activations in HBM (a few MB). final_norm: bf16 [d], device. The decoder is tied to
+ * the current device. */
+dak_status dak_decoder_create(const dak_decoder_config* cfg, const dak_decoder_layer* layers,
+                              const void* final_norm, dak_decoder** out);
+
+/* Batch (requests per step) of a decoder: the B of its KV caches. */
+int dak_decoder_batch(const dak_decoder* dec);
+
+/* One decode step for the decoder's B requests: every layer computes
+ *     h = rmsnorm(x) g_attn; [q|k|v] = h Wqkv^T; q, k = rope(q, k; pos)   (pairs i, i + D/2,
+ *     angle pos * theta^(-2i/D)); append k, v to the cache at pos;
+ *     x += attention(q; cache positions 0..pos) Wo^T; h = rmsnorm(x) g_mlp;
+ *     x += (silu(gate) * up) Wdown^T          with [gate|up] = h Wgu^T,
+ * then out = rmsnorm(x) g_final. The weight products are dak_gemm and the attention is
+ * dak_attn over the tiered placements; RMSNorm, RoPE + KV append and SwiGLU are small
+ * kernels of this library. The residual stream x is fp32; h, q, the attention output and
+ * silu(gate) * up are bf16; projections accumulate in fp32.
+ *   x_in     : bf16 [B][d] (device), the hidden states entering layer 0.
+ *   positions: int32 [B] (device), the position of each request's new token, 0 <= pos < L
+ *              (a position outside the cache is skipped and reported as DAK_ERR_BOUNDS by
+ *              dak_last_error).
+ *   out      : bf16 [B][d] (device).
+ *   mode     : 0 = direct access (host-resident tiles and requests read in place);
+ *              1 = prefetch baseline, serial: each layer's host-resident parts are first
+ *                  copied into an HBM staging buffer, then the layer runs from HBM;
+ *              2 = prefetch baseline, overlapped: layer l+1's copy runs on a second stream
+ *                  while layer l computes (two staging buffers).
+ *              Modes 1 and 2 allocate their staging buffers on first use (two buffers of
+ *              the largest per-layer host bytes).
+ * Only kernel launches and copies are issued on `stream` (plus the decoder's own copy
+ * stream in mode 2): the call can be captured into a CUDA graph (see dak_decoder_capture),
+ * once the staging buffers of modes 1 and 2 exist. */
+dak_status dak_decoder_step(dak_decoder* dec, const void* x_in, const int* positions, void* out, int mode,
+                            void* stream);
+
+/* Capture one dak_decoder_step with these arguments into a CUDA graph held by the decoder
+ * (replacing any earlier one). The graph reads x_in and positions and writes out at
+ * replay time, so the caller refills those buffers between replays. */
+dak_status dak_decoder_capture(dak_decoder* dec, const void* x_in, const int* positions, void* out, int mode);
+
+/* Launch the captured graph on `stream`. DAK_ERR_INVALID if nothing was captured. */
+dak_status dak_decoder_replay(dak_decoder* dec, void* stream);
+
+/* Kernels one step launches in the given mode (for launch accounting). */
+int dak_decoder_launches(const dak_decoder* dec, int mode);
+
+/* Release the decoder's activations, staging buffers, streams and graph (not the
+ * placements or norm gains). NULL is accepted. */
+dak_status dak_decoder_free(dak_decoder* dec);
 
 /* ---------------------------------------------------------------------------------- *
  * Planner (host only; section 4.2 and Appendix A)

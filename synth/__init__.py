@@ -26,8 +26,10 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gen.c")
 _LIB = os.path.join(_HERE, "_gen.so")
+_DEV_SRC = os.path.join(_HERE, "gen_dev.cu")
 _lock = threading.Lock()
 _lib = None
+_dev_lib = None
 
 
 def build(force: bool = False) -> str:
@@ -37,6 +39,50 @@ def build(force: bool = False) -> str:
         subprocess.check_call(["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
+
+
+def _dev_lib_path() -> str:
+    import platform
+    return os.path.join(_HERE, f"_gen_dev_{platform.machine()}.so")
+
+
+def build_dev(force: bool = False) -> str:
+    """Compile gen_dev.cu (the device twin of the generator) with nvcc for sm_103a."""
+    lib = _dev_lib_path()
+    if force or not os.path.exists(lib) or os.path.getmtime(lib) < os.path.getmtime(_DEV_SRC):
+        import shutil
+        nvcc = os.environ.get("NVCC") or shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+        tmp = lib + f".tmp{os.getpid()}"
+        subprocess.check_call([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-shared",
+                               "-Xcompiler", "-fPIC", "-o", tmp, _DEV_SRC])
+        os.replace(tmp, lib)
+    return lib
+
+
+def _load_dev():
+    global _dev_lib
+    with _lock:
+        if _dev_lib is None:
+            lib = ctypes.CDLL(build_dev())
+            u64, dbl, vp = ctypes.c_uint64, ctypes.c_double, ctypes.c_void_p
+            lib.synth_dev_normal_bf16.argtypes = [u64, u64, dbl, dbl, u64, u64, vp, vp]
+            lib.synth_dev_normal_bf16.restype = ctypes.c_int
+            _dev_lib = lib
+    return _dev_lib
+
+
+def dev_normal_bf16(seed: int, stream: int, n: int, mean: float = 0.0, std: float = 1.0, offset: int = 0,
+                    out=None, cuda_stream=None):
+    """The values of normal_bf16, drawn on the GPU into a bf16 torch tensor (or `out`)."""
+    import torch
+    if out is None:
+        out = torch.empty(int(n), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream if cuda_stream is None else cuda_stream
+    err = _load_dev().synth_dev_normal_bf16(seed, stream, float(mean), float(std), int(offset), int(n),
+                                             out.data_ptr(), s)
+    if err:
+        raise RuntimeError(f"synth_dev_normal_bf16: CUDA error {err}")
+    return out
 
 
 def _load():
@@ -188,4 +234,21 @@ def decoder_kv(cfg: dict, layer: int, batch: int, capacity: int, seed: int = 0):
     shape = (batch, cfg["n_kv_heads"], capacity, cfg["head_dim"])
     k = normal_bf16(seed, decoder_stream(layer, "k_cache"), n).reshape(shape)
     v = normal_bf16(seed, decoder_stream(layer, "v_cache"), n).reshape(shape)
+    return k, v
+
+
+def decoder_tensor_dev(cfg: dict, layer: int, name: str, seed: int = 0):
+    """decoder_tensor drawn on the GPU (bf16 torch tensor of the same shape)."""
+    shape = decoder_shapes(cfg)[name]
+    n = int(np.prod(shape))
+    mean, std = (1.0, NORM_STD) if name.endswith("_norm") else (0.0, WEIGHT_STD)
+    return dev_normal_bf16(seed, decoder_stream(layer, name), n, mean, std).view(*shape)
+
+
+def decoder_kv_dev(cfg: dict, layer: int, batch: int, capacity: int, seed: int = 0):
+    """decoder_kv drawn on the GPU (bf16 torch tensors)."""
+    n = batch * cfg["n_kv_heads"] * capacity * cfg["head_dim"]
+    shape = (batch, cfg["n_kv_heads"], capacity, cfg["head_dim"])
+    k = dev_normal_bf16(seed, decoder_stream(layer, "k_cache"), n).view(*shape)
+    v = dev_normal_bf16(seed, decoder_stream(layer, "v_cache"), n).view(*shape)
     return k, v

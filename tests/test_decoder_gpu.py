@@ -1,0 +1,180 @@
+"""Decode step (RMSNorm, QKV, RoPE + KV append, attention, O, SwiGLU MLP) on the GPU against
+the CPU oracle, through the C ABI."""
+import numpy as np
+import pytest
+
+import synth
+from gpu_util import REL_TOL, bits_of, to_np
+from oracle import decoder as od
+from oracle import gemm as og
+
+pytestmark = pytest.mark.gpu
+
+# hidden = H_q * D as in Llama; capacities and positions cut across 64-token chunks
+SMALL64 = dict(n_layers=3, hidden=256, n_heads=4, n_kv_heads=2, head_dim=64, ffn=512, rms_eps=1e-5,
+               rope_theta=10000.0)
+SMALL128 = dict(n_layers=2, hidden=512, n_heads=4, n_kv_heads=1, head_dim=128, ffn=1024, rms_eps=1e-5,
+                rope_theta=500000.0)
+
+
+@pytest.fixture(scope="module")
+def dak(cuda_ok):
+    import __graft_entry__
+    __graft_entry__.build()
+    import direct_host_memory_gb300 as m
+    return m
+
+
+def _ocfg(c):
+    return od.Config(c["n_layers"], c["hidden"], c["n_heads"], c["n_kv_heads"], c["head_dim"], c["ffn"],
+                     c["rms_eps"], c["rope_theta"])
+
+
+def _inputs(cfg, B, L, seed):
+    layers = [synth.decoder_layer(cfg, l, seed) for l in range(cfg["n_layers"])]
+    caches = [synth.decoder_kv(cfg, l, B, L, seed) for l in range(cfg["n_layers"])]
+    return layers, caches, synth.decoder_final_norm(cfg, seed), synth.decoder_x0(cfg, B, seed)
+
+
+def _host_units(cfg, B, frac):
+    """Host tile rows / requests for offload fraction frac of every operation."""
+    import math
+    sh = synth.decoder_shapes(cfg)
+    u = {k: math.ceil(frac * math.ceil(sh[k][0] / 64)) for k in ("qkv", "o", "gate_up", "down")}
+    u["kv"] = math.ceil(frac * B)
+    return u
+
+
+def _build(dak, cfg, layers, caches, fnorm, units, **kw):
+    import torch
+    placed = []
+    for l, (w, kv) in enumerate(zip(layers, caches)):
+        u = units[l] if isinstance(units, list) else units
+        placed.append(dak.place_decoder_layer(w, kv, u))
+    g = torch.from_numpy(fnorm.view(np.int16)).view(torch.bfloat16).cuda()
+    return dak.Decoder(cfg, placed, g, **kw)
+
+
+def _dev(x):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def _pos(p):
+    import torch
+    return torch.tensor(np.asarray(p, dtype=np.int32), device="cuda")
+
+
+def _run(dak, dec, x0, pos, mode=0, graph=False):
+    import torch
+    x = _dev(x0)
+    p = _pos(pos)
+    out = torch.empty_like(x)
+    if graph:
+        dec.capture(x, p, out, mode)
+        dec.replay()
+    else:
+        dec.step(x, p, out, mode)
+    st, info = dak.dak_last_error()
+    assert st == 0, f"device status {st} info {info:#x}"
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("cfg,B,L,pos", [
+    (SMALL64, 5, 200, [0, 63, 64, 130, 199]),
+    (SMALL128, 3, 300, [299, 0, 128]),
+])
+@pytest.mark.parametrize("frac", [0.0, 0.3, 1.0])
+def test_decoder_small_parity(dak, cfg, B, L, pos, frac):
+    layers, caches, fnorm, x0 = _inputs(cfg, B, L, seed=11)
+    ref, _ = od.decode_step(_ocfg(cfg), x0, layers, caches, np.array(pos), fnorm)
+    dec = _build(dak, cfg, layers, caches, fnorm, _host_units(cfg, B, frac))
+    out = _run(dak, dec, x0, pos)
+    assert og.rel_err(to_np(out), ref) <= REL_TOL
+    dec.free()
+
+
+def test_decoder_bit_identical_across_placement_modes_and_launches(dak):
+    """Offload ratio, prefetch baselines, CUDA graph and plain launches change where bytes
+    come from and when kernels start, never the result."""
+    cfg, B, L, pos = SMALL64, 5, 200, [0, 63, 64, 130, 199]
+    layers, caches, fnorm, x0 = _inputs(cfg, B, L, seed=12)
+    base = None
+    mixed = [_host_units(cfg, B, f) for f in (0.1, 0.5, 0.9)]
+    for units in (_host_units(cfg, B, 0.0), mixed, _host_units(cfg, B, 1.0)):
+        for plain in (False, True):
+            dec = _build(dak, cfg, layers, caches, fnorm, units, plain_launch=plain)
+            for mode in (0, 1, 2):
+                for graph in (False, True):
+                    b = bits_of(_run(dak, dec, x0, pos, mode, graph))
+                    if base is None:
+                        base = b
+                    assert np.array_equal(b, base), (units, plain, mode, graph)
+            dec.free()
+
+
+def test_decoder_consecutive_steps(dak):
+    """Three steps in a row: each step's key and value stay in the cache for the next."""
+    cfg, B, L = SMALL64, 4, 150
+    layers, caches, fnorm, _ = _inputs(cfg, B, L, seed=13)
+    dec = _build(dak, cfg, layers, caches, fnorm, _host_units(cfg, B, 0.5))
+    ocfg = _ocfg(cfg)
+    pos = np.array([10, 70, 0, 140])
+    ocaches = caches
+    for t in range(3):
+        x = synth.normal_bf16(13, 500 + t, B * cfg["hidden"]).reshape(B, cfg["hidden"])
+        ref, ocaches = od.decode_step(ocfg, x, layers, ocaches, pos + t, fnorm)
+        out = _run(dak, dec, x, pos + t, graph=(t == 2))
+        assert og.rel_err(to_np(out), ref) <= REL_TOL, t
+    dec.free()
+
+
+def test_decoder_position_out_of_range_reported(dak):
+    import torch
+    cfg, B, L = SMALL64, 2, 64
+    layers, caches, fnorm, x0 = _inputs(cfg, B, L, seed=14)
+    dec = _build(dak, cfg, layers, caches, fnorm, _host_units(cfg, B, 0.0))
+    x = _dev(x0)
+    out = torch.empty_like(x)
+    dec.step(x, _pos([3, 64]), out)
+    st, info = dak.dak_last_error()
+    assert st == 8  # DAK_ERR_BOUNDS, request 1
+    assert info & 0xFFFFFFFF == 1
+    # the context is still usable
+    dec.step(x, _pos([3, 5]), out)
+    assert dak.dak_last_error()[0] == 0
+    dec.free()
+
+
+def test_decoder_errors(dak):
+    import torch
+    cfg, B, L = SMALL64, 2, 64
+    layers, caches, fnorm, _ = _inputs(cfg, B, L, seed=15)
+    bad = dict(cfg, hidden=cfg["hidden"] + 8)
+    with pytest.raises(dak.DakError):
+        _build(dak, bad, layers, caches, fnorm, _host_units(cfg, B, 0.0))
+    dec = _build(dak, cfg, layers, caches, fnorm, _host_units(cfg, B, 0.0))
+    x = torch.zeros((B, cfg["hidden"]), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(dak.DakError):
+        dec.replay()  # nothing captured
+    assert dak.lib.dak_decoder_step(dec.handle, None, None, None, 0, None) == 1
+    with pytest.raises(dak.DakError):
+        dec.step(x, _pos([0, 0]), torch.empty_like(x), mode=3)
+    dec.free()
+
+
+@pytest.mark.slow
+def test_decoder_8b_width_two_layers(dak):
+    """Two layers at the 8B shape (hidden 4096, GQA 32/8, FFN 14336), 16 requests with
+    contexts up to 4096, every operation offloaded about 30% as the planner does at
+    x_global = 0.3, in the launch configuration the benchmark times."""
+    cfg = dict(synth.DECODER_8B, n_layers=2)
+    B, L = cfg["batch"], cfg["context"]
+    pos = np.array([L - 1 - 97 * b for b in range(B)])
+    layers, caches, fnorm, x0 = _inputs(cfg, B, L, seed=0)
+    dec = _build(dak, cfg, layers, caches, fnorm, _host_units(cfg, B, 0.3))
+    out = _run(dak, dec, x0, pos, graph=True)
+    dec.free()
+    ref, _ = od.decode_step(_ocfg(cfg), x0, layers, caches, pos, fnorm)
+    assert og.rel_err(to_np(out), ref) <= REL_TOL

@@ -45,7 +45,9 @@ def _args():
                     help="also time a full decode step of this model (planner ratios at --decode-x)")
     ap.add_argument("--decode-x", type=float, default=0.3, help="x_global of the decode step's HBM cap")
     ap.add_argument("--decode-steps", type=int, default=20)
-    ap.add_argument("--profile", default=None, choices=["attn", "qkv", "o", "gate_up", "down"],
+    ap.add_argument("--plain-launch", action="store_true",
+                    help="--profile decode: eager steps with ordinary launches (no graph, no programmatic launch)")
+    ap.add_argument("--profile", default=None, choices=["attn", "qkv", "o", "gate_up", "down", "decode"],
                     help="place one operation of the step at --x and launch it --steps times (for ncu)")
     return ap.parse_args()
 
@@ -204,7 +206,7 @@ def decode_plan(dak, cfg, b_host, b_hbm, x_global, peak_flops):
     return [{k: int(c) for (k, _), c in zip(meta, counts)} for _ in range(nl)], tmodel
 
 
-def build_decoder(dak, cfg, units, seed=0):
+def build_decoder(dak, cfg, units, seed=0, plain_launch=False):
     """Random-init bf16 weights and KV cache drawn on the GPU, placed layer by layer."""
     import synth
     layers = []
@@ -214,7 +216,7 @@ def build_decoder(dak, cfg, units, seed=0):
         layers.append(dak.place_decoder_layer(w, kv, units[l]))
         del w, kv
     fn = synth.dev_normal_bf16(seed, 999, cfg["hidden"], 1.0, synth.NORM_STD)
-    return dak.Decoder(cfg, layers, fn)
+    return dak.Decoder(cfg, layers, fn, plain_launch=plain_launch)
 
 
 def run_decode(dak, args, b_host, b_hbm, dev, sync_all, local):
@@ -673,6 +675,27 @@ def run_profile(args):
     import synth
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
+    if args.profile == "decode":
+        # the 8B-shaped decode step at x_global = --x (planner ratios), one graph replay per step
+        cfg = dict(synth.DECODER_8B)
+        b_host, b_hbm, _ = measure_tiers(dak) if args.x > 0 else (211e9, 7.3e12, None)
+        pk, _ = peaks()
+        units, _ = decode_plan(dak, cfg, b_host, b_hbm, args.x, pk.get("bf16_tflops_sustained", 1700.0) * 1e12)
+        dec = build_decoder(dak, cfg, units, plain_launch=args.plain_launch)
+        x_in = torch.from_numpy(synth.decoder_x0(cfg, cfg["batch"]).view("int16")).view(torch.bfloat16).to(dev)
+        pos = torch.full((cfg["batch"],), cfg["context"] - 1, dtype=torch.int32, device=dev)
+        out = torch.empty_like(x_in)
+        if args.plain_launch:
+            t = time_steps(lambda: dec.step(x_in, pos, out), args.steps, args.warmup)
+        else:
+            dec.capture(x_in, pos, out, dak.MODE_DIRECT)
+            t = time_steps(dec.replay, args.steps, args.warmup)
+        st = dak.dak_last_error()
+        print(json.dumps({"profile": "decode", "x_global": args.x, "ms_per_step": t * 1e3,
+                          "tok_s": cfg["batch"] / t, "launches_per_step": dec.launches(), "status": st[0],
+                          "host_units_per_layer": units[0]}))
+        dec.free()
+        return
     if args.profile == "attn":
         c = synth.ATTN_DECODE
         q, k, v = synth.attn_inputs(c["batch"], c["h_q"], c["h_kv"], c["head_dim"], c["context"], seed=0,

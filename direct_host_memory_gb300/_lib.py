@@ -54,8 +54,8 @@ class dak_op(ctypes.Structure):
 class dak_decoder_config(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int), ("hidden", ctypes.c_int), ("n_heads", ctypes.c_int),
                 ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("ffn", ctypes.c_int),
-                ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float), ("n_split", ctypes.c_int),
-                ("plain_launch", ctypes.c_int)]
+                ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float), ("plain_launch", ctypes.c_int),
+                ("op_tuning", dak_tuning * 5)]
 
 
 class dak_decoder_layer(ctypes.Structure):
@@ -393,12 +393,20 @@ class Decoder:
     'qkv', 'o', 'gate_up', 'down', 'kv' and the bf16 CUDA gains 'attn_norm', 'mlp_norm';
     the decoder keeps references to them (and frees the placements in .free())."""
 
-    def __init__(self, cfg: dict, layers, final_norm, n_split: int = 0, plain_launch: bool = False):
+    def __init__(self, cfg: dict, layers, final_norm, n_split: int = 0, plain_launch: bool = False,
+                 op_tuning=None):
+        """op_tuning: optional dict mapping 'qkv', 'o', 'gate_up', 'down', 'attn' to dak_tuning
+        fields (dicts); n_split sets the attention's context splits (0 = library default)."""
         c = dak_decoder_config(n_layers=len(layers), hidden=int(cfg["hidden"]), n_heads=int(cfg["n_heads"]),
                                n_kv_heads=int(cfg["n_kv_heads"]), head_dim=int(cfg["head_dim"]),
                                ffn=int(cfg["ffn"]), rms_eps=float(cfg.get("rms_eps", 1e-5)),
-                               rope_theta=float(cfg.get("rope_theta", 500000.0)), n_split=int(n_split),
+                               rope_theta=float(cfg.get("rope_theta", 500000.0)),
                                plain_launch=int(bool(plain_launch)))
+        for i, name in enumerate(("qkv", "o", "gate_up", "down", "attn")):
+            for k, v in dict((op_tuning or {}).get(name, {})).items():
+                setattr(c.op_tuning[i], k, int(v))
+        if n_split:
+            c.op_tuning[4].n_split = int(n_split)
         for L in layers:
             _check_bf16_cuda(L["attn_norm"], "attn_norm")
             _check_bf16_cuda(L["mlp_norm"], "mlp_norm")

@@ -350,8 +350,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnParams 
 template <int D>
 __global__ void attn_combine_kernel(const float* __restrict__ ws, __nv_bfloat16* __restrict__ O, int rows,
                                     int n_split) {
-    grid_dep_wait();  // the partials come from the attention kernel just before
     grid_dep_launch();
+    grid_dep_wait();  // the partials come from the attention kernel just before
     const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;

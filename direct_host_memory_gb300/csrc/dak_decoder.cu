@@ -15,11 +15,12 @@
 //   swiglu    silu(gate) * up -> act (bf16)                 [this file]
 //   dak_gemm  Wdown . act -> x +=
 // and a final rmsnorm writes the output. With programmatic dependent launch every kernel
-// starts while its predecessor drains: the GEMMs and the attention stream their weights
-// and KV chunks at once and wait only before reading activations, and the small kernels
-// here wait first and signal their dependents after that, so no kernel runs ahead of a
-// small kernel that has not started its work (the weights, the old KV entries, the
-// sequence lengths and the RoPE table are never written by a kernel that can still run).
+// starts while its predecessors drain. Before its own griddepcontrol.wait a kernel reads
+// only what no kernel of the step writes (weights, KV entries older than the new token,
+// the sequence lengths and the RoPE table) and writes nothing to global memory; after
+// the wait its predecessor, and so every earlier kernel, has finished. The step's first
+// kernel writes the sequence lengths and the RoPE table and does not signal its
+// dependents, so nothing of the step starts before those are complete.
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -88,8 +89,8 @@ struct NormArgs {
 // The sum of squares has a fixed order (per thread, butterfly within a warp, warps in
 // order), so the result does not depend on anything but the inputs.
 __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const NormArgs a, const int first) {
+    if (!first) grid_dep_launch();  // the first kernel lets its dependents start only when it is done
     grid_dep_wait();
-    grid_dep_launch();
     __shared__ float warp_ss[kNormThreads / 32];
     const int b = blockIdx.x;
     float* xr = a.x + static_cast<long long>(b) * a.d;
@@ -177,8 +178,8 @@ struct RopeArgs {
 // Query heads go to q; the new key (rotated) and value are written into the cache slab of
 // their (request, kv head) at the token's row, in the cache's 16-byte-piece layout.
 __global__ void __launch_bounds__(64) rope_append_kernel(const RopeArgs a) {
-    grid_dep_wait();
     grid_dep_launch();
+    grid_dep_wait();
     __shared__ __align__(16) __nv_bfloat16 row[128];
     const int b = blockIdx.x, hh = blockIdx.y, i = threadIdx.x;
     const int half = a.D / 2;
@@ -222,8 +223,8 @@ __global__ void __launch_bounds__(64) rope_append_kernel(const RopeArgs a) {
 // act[b][j] = bf16(silu(gate) * up), gate = gu[b][j], up = gu[b][f + j]; f % 4 == 0.
 __global__ void __launch_bounds__(256) swiglu_kernel(const float* __restrict__ gu, __nv_bfloat16* __restrict__ act,
                                                      int B, int f) {
-    grid_dep_wait();
     grid_dep_launch();
+    grid_dep_wait();
     const long long n4 = static_cast<long long>(B) * f / 4;
     for (long long idx = blockIdx.x * 256ll + threadIdx.x; idx < n4; idx += static_cast<long long>(gridDim.x) * 256) {
         const long long e = idx * 4;
@@ -334,9 +335,12 @@ dak_status enqueue_step(dak_decoder* d, const void* x_in, const int* positions, 
     const bool pdl = c.plain_launch == 0;
     DevStatus* st = status_ptr();
     if (!st) return DAK_ERR_CUDA;
-    dak_tuning tg{};
-    tg.pdl = pdl ? 1 : 0;
-    dak_tuning ta{};
+    dak_tuning tg[4];
+    for (int i = 0; i < 4; ++i) {
+        tg[i] = c.op_tuning[i];
+        tg[i].pdl = pdl ? 1 : 0;
+    }
+    dak_tuning ta = c.op_tuning[4];
     ta.n_split = d->n_split;
     ta.pdl = pdl ? 2 : 0;  // the previous kernel appends the newest token
     const int nl = c.n_layers;
@@ -391,7 +395,7 @@ dak_status enqueue_step(dak_decoder* d, const void* x_in, const int* positions, 
             return stg ? static_cast<const void*>(stg + staging_offset(L, i)) : p->host_dev;
         };
         const int Hq = c.n_heads, Hkv = c.n_kv_heads, D = c.head_dim, B = d->B;
-        if ((r = launch_gemm(L.qkv, src(0), d->h, d->qkv, B, 1, &tg, s)) != DAK_OK) return r;
+        if ((r = launch_gemm(L.qkv, src(0), d->h, d->qkv, B, 1, &tg[0], s)) != DAK_OK) return r;
         RopeArgs ra{};
         ra.qkv = d->qkv;
         ra.cs = d->rope_cs;
@@ -412,7 +416,7 @@ dak_status enqueue_step(dak_decoder* d, const void* x_in, const int* positions, 
             return r;
         if ((r = launch_attn(d->q, L.kv, src(4), d->seq_lens, Hq, 0.f, d->att, d->ws, d->ws_bytes, &ta, s)) != DAK_OK)
             return r;
-        if ((r = launch_gemm(L.o, src(1), d->att, d->ao, B, 1, &tg, s)) != DAK_OK) return r;
+        if ((r = launch_gemm(L.o, src(1), d->att, d->ao, B, 1, &tg[1], s)) != DAK_OK) return r;
         NormArgs nb{};
         nb.x = d->x;
         nb.delta = d->ao;
@@ -421,13 +425,13 @@ dak_status enqueue_step(dak_decoder* d, const void* x_in, const int* positions, 
         nb.d = c.hidden;
         nb.eps = c.rms_eps;
         if ((r = norm(d, nb, 0, pdl, s)) != DAK_OK) return r;
-        if ((r = launch_gemm(L.gate_up, src(2), d->h, d->gu, B, 1, &tg, s)) != DAK_OK) return r;
+        if ((r = launch_gemm(L.gate_up, src(2), d->h, d->gu, B, 1, &tg[2], s)) != DAK_OK) return r;
         const long long n4 = static_cast<long long>(B) * c.ffn / 4;
         const int sg = static_cast<int>(std::min<long long>((n4 + 255) / 256, 4ll * device_sm_count()));
         if ((r = cuda_status(launch(swiglu_kernel, dim3(static_cast<unsigned>(std::max(sg, 1))), 256, pdl, s,
                                     static_cast<const float*>(d->gu), d->act, B, c.ffn))) != DAK_OK)
             return r;
-        if ((r = launch_gemm(L.down, src(3), d->act, d->dn, B, 1, &tg, s)) != DAK_OK) return r;
+        if ((r = launch_gemm(L.down, src(3), d->act, d->dn, B, 1, &tg[3], s)) != DAK_OK) return r;
         if (mode == 2 && cudaEventRecord(d->ev_consumed[l & 1], s) != cudaSuccess) return DAK_ERR_CUDA;
         NormArgs nc{};
         nc.x = d->x;
@@ -498,7 +502,8 @@ extern "C" dak_status dak_decoder_create(const dak_decoder_config* cfg, const da
     dd->qkv_rows = static_cast<int>(qkv_rows);
     dd->layers.assign(layers, layers + c.n_layers);
     dd->final_norm = final_norm;
-    dd->n_split = c.n_split > 0 ? c.n_split : (c.n_layers > 0 ? dak_attn_default_split(layers[0].kv) : 1);
+    dd->n_split = c.op_tuning[4].n_split > 0 ? c.op_tuning[4].n_split
+                                              : (c.n_layers > 0 ? dak_attn_default_split(layers[0].kv) : 1);
     const size_t Bs = static_cast<size_t>(B);
     cudaError_t e = cudaSuccess;
     auto chk = [&](cudaError_t x) {

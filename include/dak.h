@@ -188,10 +188,12 @@ dak_status dak_attn_noalloc(const void* Q, const dak_placement* KV, const int* s
  *   n_layers, hidden (d), n_heads (H_q), n_kv_heads (H_kv), head_dim (D: 64 or 128), ffn (f).
  *   rms_eps   : RMSNorm epsilon (default 1e-5).
  *   rope_theta: RoPE base (default 500000).
- *   n_split   : attention context splits (default dak_attn_default_split of layer 0's cache).
  *   plain_launch: 0 = the step's kernels use programmatic dependent launch, so that each
  *               one streams its weights / KV cache while the previous one finishes;
- *               1 = ordinary stream-ordered launches. */
+ *               1 = ordinary stream-ordered launches.
+ *   op_tuning : launch tuning of the operations qkv, o, gate_up, down (dak_gemm) and the
+ *               attention (dak_attn; its n_split defaults to dak_attn_default_split of
+ *               layer 0's cache), as in dak_tuning; the pdl field is set by the decoder. */
 typedef struct {
     int n_layers;
     int hidden;
@@ -201,8 +203,8 @@ typedef struct {
     int ffn;
     float rms_eps;
     float rope_theta;
-    int n_split;
     int plain_launch;
+    dak_tuning op_tuning[5];
 } dak_decoder_config;
 
 /* One layer's operands, all placed by the caller beforehand (dak_place_matrix with the

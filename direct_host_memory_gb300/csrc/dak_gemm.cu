@@ -642,13 +642,14 @@ dak_status launch_gemm(const dak_placement* A, const void* host_src, const void*
             while (S > 1 && red_of(S) + 2 * stage_of(64) + 1024 > kSmemBudget) --S;
         }
     }
+    if (umma && t && (t->ctas_per_sm == 1 || t->ctas_per_sm == 2)) per_sm = t->ctas_per_sm;
     const int budget = per_sm == 2 ? kSmemBudgetTwoPerSm : kSmemBudget;
     int kc;
     if (t && t->chunk_k > 0) {
         kc = t->chunk_k;
     } else if (!umma) {
         kc = 512;
-    } else if (S > 1) {
+    } else if (S > 1 || per_sm == 2) {
         // the widest chunk that leaves two stages beside the partial-sum area
         kc = 64;
         for (int cand : {512, 384, 256, 192, 128}) {
@@ -666,6 +667,7 @@ dak_status launch_gemm(const dak_placement* A, const void* host_src, const void*
     const int nch = (p.K_pad + kc - 1) / kc;
     S = std::min(S, nch);
     if (S == 1) per_sm = 1;
+    if (umma && t && (t->ctas_per_sm == 1 || t->ctas_per_sm == 2)) per_sm = t->ctas_per_sm;
     p.S = S;
     const int red_bytes = S > 1 ? red_of(S) : 0;
     const int stage = stage_of(kc);

@@ -67,6 +67,9 @@ typedef struct dak_placement dak_placement;
  *               2 (dak_attn only) = as 1, except that the previous kernel may write the
  *               newest token (index L_b - 1) of each request, e.g. a KV-cache append: the
  *               chunk holding it is streamed only after that kernel has finished.
+ *   ctas_per_sm: dak_gemm only: size the shared-memory ring so that this many CTAs (1 or
+ *               2) fit on one SM; with 2, a programmatically launched next kernel can start
+ *               beside a running CTA. 0 = chosen by the library.
  */
 typedef struct {
     int host_ctas;
@@ -77,6 +80,7 @@ typedef struct {
     int hbm_ctas;
     int split_k;
     int pdl;
+    int ctas_per_sm;
 } dak_tuning;
 
 /* ---------------------------------------------------------------------------------- *

@@ -45,6 +45,8 @@ def _args():
                     help="also time a full decode step of this model (planner ratios at --decode-x)")
     ap.add_argument("--decode-x", type=float, default=0.3, help="x_global of the decode step's HBM cap")
     ap.add_argument("--decode-steps", type=int, default=20)
+    ap.add_argument("--no-planner-check", action="store_true",
+                    help="skip the compute-bound / greedy-vs-uniform planner measurement")
     ap.add_argument("--plain-launch", action="store_true",
                     help="--profile decode: eager steps with ordinary launches (no graph, no programmatic launch)")
     ap.add_argument("--profile", default=None, choices=["attn", "qkv", "o", "gate_up", "down", "decode"],
@@ -219,6 +221,30 @@ def build_decoder(dak, cfg, units, seed=0, plain_launch=False):
     return dak.Decoder(cfg, layers, fn, plain_launch=plain_launch)
 
 
+def tune_decoder_ops(dak, cfg, dec, dev):
+    """dak_tune_gemm / dak_tune_attn on layer 0 of a placed decoder (same shapes and
+    placement in every layer); returns the per-operation results and the tuning table."""
+    import torch
+    import synth
+    B = cfg["batch"]
+    L0 = dec.layers[0]
+    sh = synth.decoder_shapes(cfg)
+    res, table = {}, {}
+    for k in ("qkv", "o", "gate_up", "down"):
+        M, K = sh[k]
+        Bt = torch.randn(B, K, device=dev).to(torch.bfloat16)
+        Ct = torch.empty(B, M, device=dev, dtype=torch.float32)
+        r = dak.dak_tune_gemm(L0[k], Bt, Ct, c_fp32=True, reps=5, base=dict(pdl=1))
+        res[k] = r
+        table[k] = {f: v for f, v in r["best"].items() if f != "pdl"}
+    Q = torch.randn(B, cfg["n_heads"], cfg["head_dim"], device=dev).to(torch.bfloat16)
+    O = torch.empty_like(Q)
+    r = dak.dak_tune_attn(Q, L0["kv"], O, reps=5, base=dict(pdl=1))
+    res["attn"] = r
+    table["attn"] = {f: v for f, v in r["best"].items() if f != "pdl"}
+    return res, table
+
+
 def run_decode(dak, args, b_host, b_hbm, dev, sync_all, local):
     """Full decode step: planner-chosen per-op ratios at x_global, one CUDA graph per mode."""
     import torch
@@ -261,6 +287,15 @@ def run_decode(dak, args, b_host, b_hbm, dev, sync_all, local):
                "build_s": build_s,
                "launches_per_step": dec.launches(), "clocks": sampler.summary(tw0, tw1)}
         if xg > 0:
+            # launch tuner per operation type on layer 0's placements, then the step with its choices
+            tuned, table = tune_decoder_ops(dak, cfg, dec, dev)
+            rec["tuner"] = tuned
+            dec_t = dak.Decoder(cfg, dec.layers, dec.final_norm, op_tuning=table)
+            dec_t.capture(x_in, pos, out, dak.MODE_DIRECT)
+            tt = time_steps(dec_t.replay, args.decode_steps, 2, sync_all)
+            rec["tuned_tok_s"] = B / tt
+            rec["tuned_frac"] = (C / tt) / roof
+            dec_t.free(placements=False)
             for mode, name in ((dak.MODE_PREFETCH_SERIAL, "prefetch_serial"), (dak.MODE_PREFETCH_OVERLAP,
                                                                                  "prefetch_overlap")):
                 dec.capture(x_in, pos, out, mode)
@@ -290,6 +325,124 @@ def run_decode(dak, args, b_host, b_hbm, dev, sync_all, local):
             res[key] = rec
         else:
             res.update(rec)
+    return res
+
+
+# ------------------------------------------------------------------------------ planner check
+
+PLANNER_N = 256  # batch at which the 8B-shaped linears become tensor-bound
+
+
+def _time_fn(fn, reps=20, warmup=3):
+    return time_steps(fn, reps, warmup)
+
+
+def run_planner_check(dak, lin, attn, b_host, b_hbm, dev, x_global=0.1):
+    """The planner outside the all-memory-bound regime ([DAK] section 4.2, Fig. 6 and 11):
+    (1) t(x) of the 8B gate+up linear at N = 256 against the model max(T_c, (1-x)C/B_hbm,
+    xC/B_host) with T_c its measured all-HBM time; (2) one step of the four linears at
+    N = 256 plus the 32-request attention, placed by the greedy planner and uniformly at
+    the same x_global, both timed."""
+    import math
+    import numpy as np
+    import torch
+    import synth
+    N = PLANNER_N
+    res = {"batch": N, "x_global": x_global}
+    Bs, Cs = {}, {}
+    for i, (name, (A, _)) in enumerate(lin.items()):
+        K = A.shape[1]
+        Bs[name] = torch.from_numpy(synth.normal_bf16(0 + i, 2, N * K).view("int16")).view(torch.bfloat16) \
+            .to(dev).view(N, K)
+        Cs[name] = torch.empty((N, A.shape[0]), dtype=torch.bfloat16, device=dev)
+    gt = dict(pdl=1)
+
+    # (1) flat segment of a tensor-bound operation
+    A = lin["gate_up"][0]
+    M, K = A.shape
+    C = M * K * 2
+    curve = []
+    t0 = None
+    for x in (0.0, 0.02, 0.04, 0.06, 0.08, 0.12, 0.2):
+        p = dak.dak_place_matrix(A, dak.host_tiles_for_ratio(x, M))
+        t = _time_fn(lambda: dak.dak_gemm(p, Bs["gate_up"], Cs["gate_up"], tuning=gt))
+        xe = p.host_bytes / C
+        if t0 is None:
+            t0 = t
+        curve.append({"x": xe, "us": t * 1e6,
+                      "model_us": 1e6 * max(t0, (1 - xe) * C / b_hbm, xe * C / b_host)})
+        p.free()
+    res["gate_up_curve"] = curve
+    res["gate_up_t_comp_us"] = t0 * 1e6
+    res["gate_up_memory_us"] = C / b_hbm * 1e6
+    res["gate_up_flat_until_x"] = t0 * b_host / C
+
+    # (2) greedy vs uniform on a mixed step
+    q, k, v = attn
+    Q = torch.from_numpy(q.view("int16")).view(torch.bfloat16).to(dev)
+    O = torch.empty_like(Q)
+    kv_req = 2 * k.shape[1] * k.shape[2] * k.shape[3] * 2
+    names = list(lin) + ["attn"]
+    # T_c per operation: the measured all-HBM time where it is clearly above the memory time
+    # (tensor-bound), else the FLOP count at the sustained tensor rate
+    pk, _ = peaks()
+    P = pk.get("bf16_tflops_sustained", 1700.0) * 1e12
+    ops, units = [], []
+    pl0 = {}
+    for name in names:
+        if name == "attn":
+            pl0[name] = dak.dak_place_kv(k, v, 0)
+            nb = k.shape[0] * kv_req
+            ws = torch.empty(max(1, dak.dak_attn_workspace_bytes(q.shape[0], q.shape[1], q.shape[2],
+                                                               dak.dak_attn_default_split(pl0[name])) // 4),
+                             dtype=torch.float32, device=dev)
+            t = _time_fn(lambda: dak.dak_attn(Q, pl0["attn"], O=O, workspace=ws, tuning=dict(pdl=1)))
+            flops = 4.0 * q.shape[0] * q.shape[1] * k.shape[2] * k.shape[3]
+            ops.append((nb, t if t > 1.15 * nb / b_hbm else flops / P, kv_req))
+            units.append(k.shape[0])
+        else:
+            A = lin[name][0]
+            pl0[name] = dak.dak_place_matrix(A, 0)
+            nb = A.shape[0] * A.shape[1] * 2
+            t = _time_fn(lambda: dak.dak_gemm(pl0[name], Bs[name], Cs[name], tuning=gt))
+            flops = 2.0 * A.shape[0] * A.shape[1] * N
+            ops.append((nb, t if t > 1.15 * nb / b_hbm else flops / P, 64 * A.shape[1] * 2))
+            units.append(-(-A.shape[0] // 64))
+        res.setdefault("t_comp_us", {})[name] = ops[-1][1] * 1e6
+    for p in pl0.values():
+        p.free()
+    total = sum(o[0] for o in ops)
+    budget = x_global * total
+    r_greedy, t_greedy_model = dak.dak_plan_ratios(ops, b_host, b_hbm, budget, 0)
+    plans = {"greedy": [min(u, math.ceil(r * u - 1e-9)) for r, u in zip(r_greedy, units)],
+             "uniform": [min(u, math.ceil(x_global * u - 1e-9)) for u in units]}
+
+    def model(counts):
+        t = 0.0
+        for (c, tc, _), h, u in zip(ops, counts, units):
+            b = c * h / u
+            t += max(tc, (c - b) / b_hbm, b / b_host)
+        return t
+
+    for pname, counts in plans.items():
+        pl = {}
+        for name, h in zip(names, counts):
+            pl[name] = dak.dak_place_kv(k, v, h) if name == "attn" else dak.dak_place_matrix(lin[name][0], h)
+
+        def step():
+            for name in lin:
+                dak.dak_gemm(pl[name], Bs[name], Cs[name], tuning=gt)
+            dak.dak_attn(Q, pl["attn"], O=O, workspace=ws, tuning=dict(pdl=1))
+
+        t = _time_fn(step, 10, 2)
+        host = sum(pl[n].host_bytes for n in names)
+        res[pname] = {"host_units": dict(zip(names, counts)), "x_effective": host / total, "ms": t * 1e3,
+                      "model_ms": model(counts) * 1e3}
+        for p in pl.values():
+            p.free()
+    res["greedy_vs_uniform"] = res["uniform"]["ms"] / res["greedy"]["ms"]
+    res["status"] = dak.dak_last_error()[0]
+    torch.cuda.empty_cache()
     return res
 
 
@@ -600,6 +753,7 @@ def main():
     traffic = read_ncu_traffic()
 
     decode = run_decode(dak, args, b_host, b_hbm, dev, sync_all, local) if args.decode != "none" else None
+    planner_check = None if args.no_planner_check else run_planner_check(dak, lin, attn, b_host, b_hbm, dev)
 
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -632,6 +786,8 @@ def main():
     }
     if decode:
         line["decode_step"] = decode
+    if planner_check:
+        line["planner_check"] = planner_check
     if cpu:
         line["cpu_baseline"] = cpu
     st.free()

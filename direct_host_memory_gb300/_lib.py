@@ -28,7 +28,7 @@ EXPORTS = [
     "dak_last_error", "dak_sm_count", "dak_probe_read_bw", "dak_probe_concurrent", "dak_prefetch",
     "dak_gemm_staged", "dak_attn_staged", "dak_attn_noalloc", "dak_selftest_wait",
     "dak_decoder_create", "dak_decoder_batch", "dak_decoder_step", "dak_decoder_capture",
-    "dak_decoder_replay", "dak_decoder_launches", "dak_decoder_free",
+    "dak_decoder_replay", "dak_decoder_launches", "dak_decoder_free", "dak_tune_gemm", "dak_tune_attn",
 ]
 
 # size of the fixed device array dak_attn_noalloc uses (DAK_NOALLOC_SCRATCH_BYTES in dak.h)
@@ -44,11 +44,17 @@ class DakError(RuntimeError):
 class dak_tuning(ctypes.Structure):
     _fields_ = [("host_ctas", ctypes.c_int), ("window", ctypes.c_int), ("hbm_window", ctypes.c_int),
                 ("chunk_k", ctypes.c_int), ("n_split", ctypes.c_int), ("hbm_ctas", ctypes.c_int),
-                ("split_k", ctypes.c_int), ("pdl", ctypes.c_int), ("ctas_per_sm", ctypes.c_int)]
+                ("split_k", ctypes.c_int), ("pdl", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
+                ("no_wave_align", ctypes.c_int)]
 
 
 class dak_op(ctypes.Structure):
     _fields_ = [("bytes", ctypes.c_double), ("t_comp", ctypes.c_double), ("tile_bytes", ctypes.c_double)]
+
+
+class dak_tune_result(ctypes.Structure):
+    _fields_ = [("best", dak_tuning), ("best_us", ctypes.c_double), ("default_us", ctypes.c_double),
+                ("cc_off_us", ctypes.c_double), ("no_align_us", ctypes.c_double), ("candidates", ctypes.c_int)]
 
 
 class dak_decoder_config(ctypes.Structure):
@@ -98,6 +104,8 @@ def _load():
         "dak_decoder_replay": (i32, [vp, vp]),
         "dak_decoder_launches": (i32, [vp, i32]),
         "dak_decoder_free": (i32, [vp]),
+        "dak_tune_gemm": (i32, [vp, vp, vp, i32, i32, i32, P(dak_tuning), P(dak_tune_result)]),
+        "dak_tune_attn": (i32, [vp, vp, vp, i32, vp, vp, sz, i32, P(dak_tuning), P(dak_tune_result)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -486,3 +494,60 @@ def place_decoder_layer(weights: dict, kv, host_units: dict, device=None) -> dic
             g = torch.from_numpy(g.view(np.int16)).view(torch.bfloat16)
         L[k] = g.to(dev).contiguous()
     return L
+
+
+# ------------------------------------------------------------------------------- launch tuner
+
+TUNING_FIELDS = [f for f, _ in dak_tuning._fields_]
+
+
+def tuning_to_dict(t: dak_tuning, keep_zero: bool = False) -> dict:
+    return {f: int(getattr(t, f)) for f in TUNING_FIELDS if keep_zero or getattr(t, f)}
+
+
+def _tune_result(r: dak_tune_result) -> dict:
+    return {"best": tuning_to_dict(r.best), "best_us": r.best_us, "default_us": r.default_us,
+            "cc_off_us": r.cc_off_us, "no_align_us": r.no_align_us, "candidates": r.candidates}
+
+
+def dak_tune_gemm(A: Placement, B, C, c_fp32: bool = False, reps: int = 5, base=None) -> dict:
+    """Time dak_gemm over the tuner's candidates (host CTAs x window x chunk) and the
+    congestion-control and wave-alignment ablations; returns the fastest tuning and times."""
+    _check_bf16_cuda(B, "B")
+    r = dak_tune_result()
+    _check(lib.dak_tune_gemm(A.handle, _ptr(B), _ptr(C), int(B.shape[0]), int(bool(c_fp32)), int(reps),
+                             _tuning(base), ctypes.byref(r)), "dak_tune_gemm")
+    return _tune_result(r)
+
+
+def dak_tune_attn(Q, KV: Placement, O, workspace=None, seq_lens=None, reps: int = 5, base=None) -> dict:
+    """dak_tune_gemm for dak_attn (host CTAs x window; n_split from base or the default)."""
+    Hq, O, workspace, ws_len, tun = _attn_common(Q, KV, O, workspace, base)
+    r = dak_tune_result()
+    _check(lib.dak_tune_attn(_ptr(Q), KV.handle, _ptr(seq_lens), Hq, _ptr(O), _ptr(workspace), ws_len, int(reps),
+                             _tuning(tun), ctypes.byref(r)), "dak_tune_attn")
+    return _tune_result(r)
+
+
+def save_tuning(path: str, table: dict, meta: dict = None):
+    """Persist a table {operation name: tuning fields} (e.g. the tuner's choices) as JSON."""
+    import json
+    doc = {"tuning": {k: {f: int(v) for f, v in dict(t).items() if f in TUNING_FIELDS} for k, t in table.items()}}
+    if meta:
+        doc["meta"] = meta
+    with open(path, "w") as f:
+        json.dump(doc, f, indent=1, sort_keys=True)
+
+
+def load_tuning(path: str) -> dict:
+    """Read a table written by save_tuning; unknown fields are rejected."""
+    import json
+    with open(path) as f:
+        doc = json.load(f)
+    table = {}
+    for k, t in doc.get("tuning", {}).items():
+        bad = set(t) - set(TUNING_FIELDS)
+        if bad:
+            raise ValueError(f"{path}: unknown tuning fields {sorted(bad)} for {k}")
+        table[k] = {f: int(v) for f, v in t.items()}
+    return table

@@ -59,16 +59,26 @@ Sched schedule(int host_units, int hbm_units, int sm_slots, const dak_tuning* t,
     Sched s{};
     int cap = (t && t->host_ctas > 0) ? t->host_ctas : default_host_ctas;
     cap = std::max(1, std::min(cap, sm_slots - (hbm_units > 0 ? 1 : 0)));
+    if (host_units > 0 && hbm_units > 0 && !(t && (t->host_ctas > 0 || t->no_wave_align))) {
+        // keep the HBM side at the wave count the whole operation would have on all slots:
+        // host CTAs come out of the slack only (when a unit is compute-bound, one more HBM
+        // wave costs a whole unit time, more than the host side saves)
+        const int w0 = ceil_div(host_units + hbm_units, sm_slots);
+        const int slack = sm_slots - ceil_div(hbm_units, w0);
+        cap = std::max(1, std::min(cap, slack));
+    }
+    const bool align = !(t && t->no_wave_align);
     if (host_units > 0) {
         const int waves = ceil_div(host_units, cap);
-        s.n_host_ctas = ceil_div(host_units, waves);  // whole waves: no partial tail wave
+        // whole waves: no partial tail wave
+        s.n_host_ctas = align ? ceil_div(host_units, waves) : std::min(cap, host_units);
     }
     int hbm_slots = sm_slots - s.n_host_ctas;
     if (t && t->hbm_ctas > 0) hbm_slots = std::min(hbm_slots, t->hbm_ctas);
     hbm_slots = std::max(1, hbm_slots);
     if (hbm_units > 0) {
         const int waves = ceil_div(hbm_units, hbm_slots);
-        s.n_hbm_ctas = ceil_div(hbm_units, waves);
+        s.n_hbm_ctas = align ? ceil_div(hbm_units, waves) : std::min(hbm_slots, hbm_units);
     }
     int hw = (t && t->window > 0) ? t->window : default_host_window;
     int bw = (t && t->hbm_window > 0) ? t->hbm_window : default_hbm_window;

@@ -70,6 +70,9 @@ typedef struct dak_placement dak_placement;
  *   ctas_per_sm: dak_gemm only: size the shared-memory ring so that this many CTAs (1 or
  *               2) fit on one SM; with 2, a programmatically launched next kernel can start
  *               beside a running CTA. 0 = chosen by the library.
+ *   no_wave_align: 1 = ablation of the wave alignment of section 4.1 (factor 2, Fig. 12b):
+ *               host CTAs = the cap and HBM CTAs = every remaining slot, without rounding
+ *               either role to whole waves. 0 = aligned (default).
  */
 typedef struct {
     int host_ctas;
@@ -81,6 +84,7 @@ typedef struct {
     int split_k;
     int pdl;
     int ctas_per_sm;
+    int no_wave_align;
 } dak_tuning;
 
 /* ---------------------------------------------------------------------------------- *
@@ -183,6 +187,36 @@ int dak_attn_default_split(const dak_placement* KV);
  *   one stream or with events. */
 dak_status dak_attn_noalloc(const void* Q, const dak_placement* KV, const int* seq_lens, int H_q, float scale,
                             void* O, const dak_tuning* tuning, void* stream);
+
+/* ---------------------------------------------------------------------------------- *
+ * Launch tuner (section 4.3.1, "Congestion Control Strategy": the host-SM cap and the
+ * in-flight window are profiled per operation before launch; section 6.2, Fig. 12)
+ * ---------------------------------------------------------------------------------- */
+
+/* Result of one tuning run. */
+typedef struct {
+    dak_tuning best;       /* fastest candidate (base with host_ctas / window / chunk_k set) */
+    double best_us;        /* its mean time per launch */
+    double default_us;     /* the base tuning as given */
+    double cc_off_us;      /* congestion control off: every SM may read the host, window 8 */
+    double no_align_us;    /* wave alignment off (no_wave_align = 1) */
+    int candidates;        /* candidates timed */
+} dak_tune_result;
+
+/* Time dak_gemm(A, B, C, N, c_fp32) with `reps` launches per candidate (after one warm-up
+ * launch) on a private stream, over host_ctas in {4, 8, 12, 16, 24, 32} x window in
+ * {2, 3, 4, 6, 8} (when A has host tiles) x chunk_k in {library default, 256, 512}, each
+ * applied on top of *base (NULL = defaults); candidates the launcher rejects are skipped.
+ * Synchronous; overwrites C. The chosen knobs move work between CTAs only, except
+ * chunk_k, which changes the summation order of every output the same way at any
+ * offload ratio. */
+dak_status dak_tune_gemm(const dak_placement* A, const void* B, void* C, int N, int c_fp32, int reps,
+                         const dak_tuning* base, dak_tune_result* out);
+
+/* The same for dak_attn (host_ctas x window; n_split stays base's, default when <= 0). */
+dak_status dak_tune_attn(const void* Q, const dak_placement* KV, const int* seq_lens, int H_q, void* O,
+                         void* workspace, size_t ws_bytes, int reps, const dak_tuning* base,
+                         dak_tune_result* out);
 
 /* ---------------------------------------------------------------------------------- *
  * Decode step of a Llama-shaped transformer around the two operations (sections 3, 5, 6.1)

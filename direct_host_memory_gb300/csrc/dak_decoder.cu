@@ -323,6 +323,7 @@ dak_status prefetch_layer(dak_decoder* d, int l, uint8_t* buf, cudaStream_t s) {
     for (int i = 0; i < 5; ++i) {
         const dak_placement* p = part(L, i);
         if (p->host_bytes == 0) continue;
+        // the device-visible alias with cudaMemcpyDefault: the form that copied fastest here
         const cudaError_t e = cudaMemcpyAsync(buf + staging_offset(L, i), p->host_dev, static_cast<size_t>(p->host_bytes),
                                               cudaMemcpyDefault, s);
         if (e != cudaSuccess) return cuda_status(e);

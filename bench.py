@@ -446,6 +446,36 @@ def run_planner_check(dak, lin, attn, b_host, b_hbm, dev, x_global=0.1):
     return res
 
 
+# ------------------------------------------------------------------------------ large N
+
+def run_large_n(dak, lin, b_host, b_hbm, dev, x=0.25):
+    """dak_gemm beyond one CTA's 256 hidden-state rows: the 8B gate+up linear at x, N in
+    {256, 512, 1024, 2048}. A cluster of ceil(N/256) CTAs shares each tile row, rank 0
+    forwarding every A chunk through distributed shared memory, so the host link carries
+    the host bytes once per launch of up to 2048 rows. Reported against the
+    traffic-amplified model of separate 256-row launches (host bytes x ceil(N/256) /
+    B_host, as [DAK] Table 1 counts it without multicast) and the single-read model."""
+    import torch
+    import synth
+    A = lin["gate_up"][0]
+    M, K = A.shape
+    p = dak.dak_place_matrix(A, dak.host_tiles_for_ratio(x, M))
+    rows = []
+    for N in (256, 512, 1024, 2048):
+        B = torch.from_numpy(synth.normal_bf16(7, 2, N * K).view("int16")).view(torch.bfloat16).to(dev).view(N, K)
+        C = torch.empty((N, M), dtype=torch.bfloat16, device=dev)
+        t = time_steps(lambda: dak.dak_gemm(p, B, C, tuning=dict(pdl=1)), 10, 2)
+        blocks = -(-N // 256)
+        launches = -(-N // 2048)
+        rows.append({"N": N, "us": t * 1e6, "host_link_bytes": p.host_bytes * launches,
+                     "host_link_gbps": p.host_bytes * launches / t / 1e9,
+                     "model_single_read_us": 1e6 * launches * max(p.host_bytes / b_host, p.hbm_bytes / b_hbm),
+                     "model_per_256_rows_us": 1e6 * blocks * max(p.host_bytes / b_host, p.hbm_bytes / b_hbm)})
+    p.free()
+    return {"op": "gate_up 28672x4096", "x": x, "host_bytes": p.host_bytes, "rows": rows,
+            "status": dak.dak_last_error()[0]}
+
+
 # ------------------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -754,6 +784,7 @@ def main():
 
     decode = run_decode(dak, args, b_host, b_hbm, dev, sync_all, local) if args.decode != "none" else None
     planner_check = None if args.no_planner_check else run_planner_check(dak, lin, attn, b_host, b_hbm, dev)
+    large_n = None if args.no_planner_check else run_large_n(dak, lin, b_host, b_hbm, dev)
 
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -788,6 +819,8 @@ def main():
         line["decode_step"] = decode
     if planner_check:
         line["planner_check"] = planner_check
+    if large_n:
+        line["large_n"] = large_n
     if cpu:
         line["cpu_baseline"] = cpu
     st.free()

@@ -41,6 +41,7 @@ struct GemmParams {
     int b3d;      // B arrives in one 3-D tensor copy per stage (else several 2-D copies)
     int S;        // CTAs per cluster splitting each tile row's K range (1 = no split)
     int red_off;  // byte offset (from the aligned ring base) of the partial-sum area, S > 1
+    int NC;       // CTAs per cluster sharing each tile row across 256-row blocks of B (1 = off)
 };
 
 // Tiles of this CTA: role, first tile, stride, count, and the chunk range [c_lo, c_hi) of
@@ -55,11 +56,12 @@ struct TileIter {
 
 __device__ __forceinline__ TileIter tiles_of_cta(const GemmParams& p) {
     TileIter it;
-    const int b = blockIdx.x / p.S;  // cluster index
+    const int cl = p.S > 1 ? p.S : p.NC;  // CTAs per cluster
+    const int b = blockIdx.x / cl;        // cluster index
     const int nch = (p.K_pad + p.kc - 1) / p.kc;
-    it.rank = p.S > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-    it.c_lo = it.rank * nch / p.S;
-    it.c_hi = (it.rank + 1) * nch / p.S;
+    it.rank = cl > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    it.c_lo = p.S > 1 ? it.rank * nch / p.S : 0;
+    it.c_hi = p.S > 1 ? (it.rank + 1) * nch / p.S : nch;
     if (b < p.n_host_ctas) {
         it.host = true;
         it.first = b;
@@ -88,7 +90,7 @@ __device__ __forceinline__ const uint8_t* tile_src(const GemmParams& p, const Ti
 // error location codes (upper 32 bits of the status info)
 enum : uint32_t {
     W_PROD_EMPTY = 1, W_CONS_FULL = 2, W_MMA_FULL = 3, W_MMA_ACC = 4, W_EPI_ACC = 5, W_DRAIN = 6, W_BPROD_EMPTY = 7,
-    W_RED_FULL = 8, W_RED_EMPTY = 9
+    W_RED_FULL = 8, W_RED_EMPTY = 9, W_FWD_FULL = 10, W_FWD_PEER = 11, W_ARM_EMPTY = 12
 };
 
 // Wait (bounded, ignoring the abort flag) for the last fill of every ring slot, so that no
@@ -117,14 +119,14 @@ __device__ __forceinline__ void drain_fills(uint64_t* full, int window, long lon
 enum BKind { kCoreB = 0, kUmmaB = 1 };
 
 __device__ __forceinline__ void issue_b(const GemmParams& p, const CUtensorMap* bmap, uint8_t* dst, int k0,
-                                        uint64_t* bar, int kind) {
+                                        uint64_t* bar, int kind, int row0) {
     const int blk = kind == kUmmaB ? 64 : 256;
     const int rows = kind == kUmmaB ? p.N_pad : p.N;
     const int nblk = p.kc / blk;
     if (p.b3d) {
-        tma_load_3d(dst, bmap, 0, 0, k0 / blk, bar);
+        tma_load_3d(dst, bmap, 0, row0, k0 / blk, bar);
     } else {
-        for (int b = 0; b < nblk; ++b) tma_load_2d(dst + b * rows * blk * 2, bmap, k0 + blk * b, 0, bar);
+        for (int b = 0; b < nblk; ++b) tma_load_2d(dst + b * rows * blk * 2, bmap, k0 + blk * b, row0, bar);
     }
 }
 
@@ -159,8 +161,70 @@ __device__ __forceinline__ void produce(const GemmParams& p, const TileIter& it,
                 bulk_g2s(dst, src + static_cast<long long>(k0) * 128, a_bytes, &full[s], pol_a);
             } else {
                 mbar_arrive_expect_tx(&full[s], b_stage_bytes(p, kind));
-                issue_b(p, bmap, dst + p.kc * 128, k0, &full[s], kind);
+                issue_b(p, bmap, dst + p.kc * 128, k0, &full[s], kind, p.NC > 1 ? it.rank * p.N_pad : 0);
             }
+        }
+    }
+done:
+    drain_fills(full, W, i, p.st);
+}
+
+// Shared tile rows across the 256-row blocks of a wide B (NC > 1). Rank 0 of the cluster
+// fetches every A chunk (host or HBM) once; its forwarder copies each arrived chunk from its
+// ring slot into the same slot of every other rank with shared-to-shared bulk copies, waits
+// until the copies have read the slot, and then releases it. The other ranks only arm their
+// full barrier with the chunk's byte count and, once their MMAs have finished with a slot,
+// tell rank 0 that it may be refilled. Each host byte therefore crosses the host link once
+// however many 256-row blocks B has (no multicast is involved).
+// Run by the whole forwarder warp of rank 0: lane r - 1 copies to rank r, so the copies to
+// the NC - 1 other ranks are issued in parallel.
+__device__ __forceinline__ void forward_a(const GemmParams& p, const TileIter& it, uint8_t* smem, uint64_t* full,
+                                          uint64_t* empty, uint64_t* peer_empty, volatile int* abort) {
+    const int W = it.window;
+    const int lane = threadIdx.x & 31;
+    const int r = lane + 1;  // the rank this lane forwards to
+    long long i = 0;
+    for (int ti = 0; ti < it.count; ++ti) {
+        for (int c = it.c_lo; c < it.c_hi; ++c, ++i) {
+            const int s = static_cast<int>(i % W);
+            bool ok = mbar_wait(&full[s], static_cast<uint32_t>((i / W) & 1), abort, p.st, DAK_ERR_TIMEOUT, W_FWD_FULL);
+            if (ok && i >= W)
+                ok = mbar_wait_cluster(&peer_empty[s], static_cast<uint32_t>(((i / W) - 1) & 1), abort, p.st,
+                                       DAK_ERR_TIMEOUT, W_FWD_PEER);
+            if (!__all_sync(0xffffffffu, ok)) goto done;
+            if (r < p.NC) {
+                const int k0 = c * p.kc;
+                const uint32_t a_bytes = static_cast<uint32_t>(min(p.kc, p.K_pad - k0)) * 128u;
+                uint8_t* slot = smem + static_cast<size_t>(s) * p.stage_bytes;
+                bulk_s2s_cluster(mapa_shared(smem_u32(slot), static_cast<uint32_t>(r)), slot, a_bytes,
+                                 mapa_shared(smem_u32(&full[s]), static_cast<uint32_t>(r)));
+                bulk_commit_group();
+                bulk_wait_group_read0();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+    }
+done:
+    if (r < p.NC) bulk_wait_group0();
+    __syncwarp();
+}
+
+__device__ __forceinline__ void arm_forwarded_a(const GemmParams& p, const TileIter& it, uint64_t* full,
+                                                uint64_t* empty, uint64_t* peer_empty, volatile int* abort) {
+    const int W = it.window;
+    long long i = 0;
+    for (int ti = 0; ti < it.count && !*abort; ++ti) {
+        for (int c = it.c_lo; c < it.c_hi; ++c, ++i) {
+            const int s = static_cast<int>(i % W);
+            if (i >= W) {
+                if (!mbar_wait(&empty[s], static_cast<uint32_t>(((i / W) - 1) & 1), abort, p.st, DAK_ERR_TIMEOUT,
+                               W_ARM_EMPTY))
+                    goto done;
+                mbar_arrive_remote(mapa_shared(smem_u32(&peer_empty[s]), 0));
+            }
+            const int k0 = c * p.kc;
+            mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(min(p.kc, p.K_pad - k0)) * 128u);
         }
     }
 done:
@@ -278,7 +342,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
 // Warps: 0 = A producer (bulk copies), 1 = TMEM allocator + MMA issuer,
 //        2..5 = epilogue (TMEM -> registers -> C), 6 = B producer (tensor-map copies).
 // ======================================================================================
-constexpr int kUmmaThreads = 7 * 32;
+constexpr int kUmmaThreads = 8 * 32;
 
 // TMEM lane holding output row `row` (0..63) of an M = 64 accumulator: rows 16q .. 16q+15
 // sit in lanes 32q .. 32q+15 of sub-partition q.
@@ -289,6 +353,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ uint64_t full[8], empty[8], acc_full[2], acc_empty[2];
     __shared__ uint64_t red_full, red_empty;  // cluster split: partials in / partial buffer free
+    __shared__ uint64_t peer_empty[8];        // wide B, rank 0: every other rank has freed the slot
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
     volatile int* abort = &abort_flag;
@@ -308,9 +373,11 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
+        const bool fwd = p.NC > 1 && it.rank == 0;
         for (int s = 0; s < W; ++s) {
-            mbar_init(&full[s], 2);  // A producer + B producer
-            mbar_init(&empty[s], 1);
+            mbar_init(&full[s], 2);              // A producer (or A arming) + B producer
+            mbar_init(&empty[s], fwd ? 2 : 1);   // MMA commit (+ the forwarder on rank 0)
+            if (fwd) mbar_init(&peer_empty[s], p.NC - 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
@@ -330,12 +397,20 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (p.S > 1) cluster_sync_all();  // partners' barriers exist before any remote arrive
+    if (p.S > 1 || p.NC > 1) cluster_sync_all();  // partners' barriers exist before any remote access
     grid_dep_launch();
     const uint32_t tmem = tmem_base_sh;
 
     if (warp == 0 || warp == 6) {
-        if (lane == 0) produce(p, it, &bmap, smem, full, empty, abort, warp == 0, kUmmaB);
+        if (lane == 0) {
+            if (warp == 0 && p.NC > 1 && it.rank > 0) {
+                arm_forwarded_a(p, it, full, empty, peer_empty, abort);
+            } else {
+                produce(p, it, &bmap, smem, full, empty, abort, warp == 0, kUmmaB);
+            }
+        }
+    } else if (warp == 7) {
+        if (p.NC > 1 && it.rank == 0) forward_a(p, it, smem, full, empty, peer_empty, abort);
     } else if (warp == 1) {
         // The whole warp runs the loop (so that loop state and descriptors stay warp-uniform);
         // one elected lane issues the MMAs and commits.
@@ -355,8 +430,12 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
             bool ok = true;
             for (int c = it.c_lo; c < it.c_hi; ++c, ++i) {
                 const int s = static_cast<int>(i % W);
-                if (!mbar_wait(&full[s], static_cast<uint32_t>((i / W) & 1), abort, p.st, DAK_ERR_TIMEOUT,
-                               W_MMA_FULL)) {
+                // a forwarded A chunk is written by another CTA of the cluster
+                const bool got = p.NC > 1 ? mbar_wait_cluster(&full[s], static_cast<uint32_t>((i / W) & 1), abort,
+                                                              p.st, DAK_ERR_TIMEOUT, W_MMA_FULL)
+                                          : mbar_wait(&full[s], static_cast<uint32_t>((i / W) & 1), abort, p.st,
+                                                      DAK_ERR_TIMEOUT, W_MMA_FULL);
+                if (!got) {
                     ok = false;
                     break;
                 }
@@ -406,7 +485,8 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         // adds them to its own in rank order (a fixed order, independent of the placement).
         const int q = warp & 3;
         const int row_in_tile = umma_m64_row_of_lane(q, lane);
-        const bool leader = it.rank == 0;
+        const bool leader = p.S > 1 ? it.rank == 0 : true;  // wide B: every rank writes its own rows
+        const int n_off = p.NC > 1 ? it.rank * p.N_pad : 0;  // first hidden-state row of this CTA's block
         grid_dep_wait();  // C may be read by the previous kernel of the stream
         float* red = reinterpret_cast<float*>(smem + p.red_off);  // [S-1][64 rows][N_pad] on the leader
         for (int ti = 0; ti < it.count; ++ti) {
@@ -467,7 +547,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
                     }
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        const int n = n0 + j;
+                        const int n = n_off + n0 + j;
                         if (n < p.N) {
                             if (p.c_fp32) {
                                 reinterpret_cast<float*>(p.C)[static_cast<long long>(n) * p.M + row] = f[j];
@@ -488,7 +568,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (p.S > 1) cluster_sync_all();  // no CTA leaves while a partner may still touch its shared memory
+    if (p.S > 1 || p.NC > 1) cluster_sync_all();  // no CTA leaves while a partner may still touch its shared memory
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, tmem_cols);
@@ -549,6 +629,8 @@ static bool make_b_map(CUtensorMap* map, const void* B, int K, int N, int N_pad,
 constexpr int kSmemBudget = 216 * 1024;           // one CTA per SM
 constexpr int kSmemBudgetTwoPerSm = 108 * 1024;  // two CTAs per SM
 constexpr int kDefaultHostCtas = 16;
+constexpr int kMaxBlockN = 256;          // hidden-state rows of one CTA's tile
+constexpr int kMaxWideN = 8 * kMaxBlockN;  // rows of one launch: a cluster of up to 8 CTAs shares A
 constexpr int kDefaultHostWindow = 4;
 
 // Launch with the optional cluster dimension and programmatic-dependent-launch attribute.
@@ -581,10 +663,12 @@ static cudaError_t launch_ex(Kernel k, int grid, int threads, int smem, int clus
     return cudaLaunchKernelEx(&cfg, k, p, bmap);
 }
 
-dak_status launch_gemm(const dak_placement* A, const void* host_src, const void* B, void* C, int N, int c_fp32,
-                       const dak_tuning* t, cudaStream_t stream) {
+// One launch over up to kMaxWideN hidden-state rows: one CTA per tile row up to 256 rows
+// (the widest tcgen05 tile used here), a cluster of ceil(N / 256) CTAs per tile row beyond.
+static dak_status launch_gemm_block(const dak_placement* A, const void* host_src, const void* B, void* C, int N,
+                                    int c_fp32, const dak_tuning* t, cudaStream_t stream) {
     if (!A || A->kind != 0) return DAK_ERR_INVALID;
-    if (N < 1 || N > 256) return DAK_ERR_INVALID;
+    if (N < 1 || N > kMaxWideN) return DAK_ERR_INVALID;
     if (A->M == 0 || A->T == 0) return DAK_OK;  // nothing to compute; C may be empty
     if (!B || !C) return DAK_ERR_INVALID;
     if ((reinterpret_cast<uintptr_t>(B) & 15) || (reinterpret_cast<uintptr_t>(C) & 15)) return DAK_ERR_ALIGN;
@@ -601,7 +685,9 @@ dak_status launch_gemm(const dak_placement* A, const void* host_src, const void*
     p.K = static_cast<int>(A->K);
     p.K_pad = static_cast<int>(A->K_pad);
     p.N = N;
-    p.N_pad = (N + 7) & ~7;
+    // wide B: NC CTAs of a cluster share each tile row, CTA r computing rows [256 r, 256 r + 256)
+    p.NC = N > kMaxBlockN ? (N + kMaxBlockN - 1) / kMaxBlockN : 1;
+    p.N_pad = N > kMaxBlockN ? kMaxBlockN : (N + 7) & ~7;
     p.T = A->T;
     p.h = A->h;
     p.c_fp32 = c_fp32 ? 1 : 0;
@@ -614,6 +700,7 @@ dak_status launch_gemm(const dak_placement* A, const void* host_src, const void*
     const int kind = umma ? kUmmaB : kCoreB;
     const int sms = device_sm_count();
     const int rows_b = umma ? p.N_pad : N;
+    const int NC = p.NC;
     auto stage_of = [&](int k) { return (k * 128 + k * 2 * rows_b + 1023) & ~1023; };
 
     // Cluster split of each tile row's K range, chosen from the shape only (never from the
@@ -668,7 +755,9 @@ dak_status launch_gemm(const dak_placement* A, const void* host_src, const void*
     S = std::min(S, nch);
     if (S == 1) per_sm = 1;
     if (umma && t && (t->ctas_per_sm == 1 || t->ctas_per_sm == 2)) per_sm = t->ctas_per_sm;
+    if (NC > 1) per_sm = 1;  // each CTA holds 2 x 256 TMEM columns, the whole TMEM of an SM
     p.S = S;
+    const int CL = S > 1 ? S : NC;  // CTAs per cluster
     const int red_bytes = S > 1 ? red_of(S) : 0;
     const int stage = stage_of(kc);
     const int ring_budget = per_sm == 2 ? kSmemBudgetTwoPerSm : kSmemBudget;
@@ -682,15 +771,15 @@ dak_status launch_gemm(const dak_placement* A, const void* host_src, const void*
     // schedule in cluster units
     dak_tuning tc{};
     if (t) tc = *t;
-    tc.host_ctas = std::max(1, (tc.host_ctas > 0 ? tc.host_ctas : kDefaultHostCtas) / S);
-    if (tc.hbm_ctas > 0) tc.hbm_ctas = std::max(1, tc.hbm_ctas / S);
-    Sched sc = schedule(p.h, p.T - p.h, (sms * per_sm) / S, &tc, kDefaultHostCtas,
+    tc.host_ctas = std::max(1, (tc.host_ctas > 0 ? tc.host_ctas : kDefaultHostCtas) / CL);
+    if (tc.hbm_ctas > 0) tc.hbm_ctas = std::max(1, tc.hbm_ctas / CL);
+    Sched sc = schedule(p.h, p.T - p.h, std::max(1, (sms * per_sm) / CL), &tc, std::max(1, kDefaultHostCtas / CL),
                         std::min(kDefaultHostWindow, stages), stages, stages);
     p.n_host_ctas = sc.n_host_ctas;
     p.n_hbm_ctas = sc.n_hbm_ctas;
     p.host_window = sc.host_window;
     p.hbm_window = sc.hbm_window;
-    const int grid = (p.n_host_ctas + p.n_hbm_ctas) * S;
+    const int grid = (p.n_host_ctas + p.n_hbm_ctas) * CL;
     if (grid == 0) return DAK_OK;
     if (p.h > 0 && !p.a_host) return DAK_ERR_INVALID;
 
@@ -702,7 +791,7 @@ dak_status launch_gemm(const dak_placement* A, const void* host_src, const void*
     const bool pdl = t && t->pdl > 0;
     cudaError_t e;
     if (umma) {
-        e = launch_ex(gemm_umma_kernel, grid, kUmmaThreads, smem, S, pdl, stream, p, bmap);
+        e = launch_ex(gemm_umma_kernel, grid, kUmmaThreads, smem, CL, pdl, stream, p, bmap);
     } else {
         switch (N) {
             case 1: e = launch_ex(gemm_core_kernel<1>, grid, kCoreThreads, smem, 1, pdl, stream, p, bmap); break;
@@ -715,6 +804,25 @@ dak_status launch_gemm(const dak_placement* A, const void* host_src, const void*
         }
     }
     return cuda_status(e);
+}
+
+// Any N: up to kMaxWideN hidden-state rows per launch (a cluster shares each tile row, so
+// host tiles cross the link once), larger N in column blocks of kMaxWideN rows, one launch
+// each (B rows and C rows of a block are contiguous; every block reads the host tiles again).
+dak_status launch_gemm(const dak_placement* A, const void* host_src, const void* B, void* C, int N, int c_fp32,
+                       const dak_tuning* t, cudaStream_t stream) {
+    if (!A || A->kind != 0) return DAK_ERR_INVALID;
+    if (N <= kMaxWideN) return launch_gemm_block(A, host_src, B, C, N, c_fp32, t, stream);
+    if (!B || !C) return DAK_ERR_INVALID;
+    const size_t b_row = static_cast<size_t>(A->K) * 2;
+    const size_t c_row = static_cast<size_t>(A->M) * (c_fp32 ? 4 : 2);
+    for (int n0 = 0; n0 < N; n0 += kMaxWideN) {
+        const int nb = std::min(kMaxWideN, N - n0);
+        const dak_status r = launch_gemm_block(A, host_src, static_cast<const uint8_t*>(B) + n0 * b_row,
+                                               static_cast<uint8_t*>(C) + n0 * c_row, nb, c_fp32, t, stream);
+        if (r != DAK_OK) return r;
+    }
+    return DAK_OK;
 }
 
 }  // namespace dak

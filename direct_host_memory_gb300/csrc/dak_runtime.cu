@@ -58,6 +58,13 @@ Sched schedule(int host_units, int hbm_units, int sm_slots, const dak_tuning* t,
                int default_host_window, int default_hbm_window, int max_window) {
     Sched s{};
     int cap = (t && t->host_ctas > 0) ? t->host_ctas : default_host_ctas;
+    if (!(t && t->host_ctas > 0) && host_units > 0) {
+        // at least the host units' share of the slots: when units are compute-heavy the host
+        // side needs its share of SMs, and on this GPU more host CTAs do not congest HBM
+        const long long share = (static_cast<long long>(sm_slots) * host_units + host_units + hbm_units - 1) /
+                                (static_cast<long long>(host_units) + hbm_units);
+        cap = std::max(cap, static_cast<int>(share));
+    }
     cap = std::max(1, std::min(cap, sm_slots - (hbm_units > 0 ? 1 : 0)));
     if (host_units > 0 && hbm_units > 0 && !(t && (t->host_ctas > 0 || t->no_wave_align))) {
         // keep the HBM side at the wave count the whole operation would have on all slots:

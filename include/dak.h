@@ -131,7 +131,9 @@ dak_status dak_placement_info(const dak_placement* p, int64_t* host_bytes, int64
  * Memory", "Asynchronous TMA Access", Fig. 5b).
  *   B : hidden states, bf16 [N][K] row-major (device), 16-byte aligned.
  *   C : output [N][M] row-major (device); bf16 if c_fp32 == 0, else fp32.
- *   N : 1 .. 256.
+ *   N : >= 1. Up to 256 rows run as one launch; a larger N runs as column blocks of 256
+ *       rows, one launch each, and every block reads the host tiles again (host-link
+ *       bytes = host bytes x ceil(N / 256); no multicast, section 4.3.2, Table 1).
  * One persistent launch: `host_ctas` CTAs stream the host tile rows and the other CTAs
  * the HBM tile rows; every CTA reads from exactly one tier and writes disjoint rows of
  * C. When the matrix has fewer tile rows than SMs, a cluster of CTAs shares each tile row,

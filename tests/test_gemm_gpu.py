@@ -164,7 +164,8 @@ def test_empty_and_errors(dak):
         dak.dak_place_matrix(np.zeros((64, 60), dtype=np.uint16), 0)  # K % 8 != 0
     p = dak.dak_place_matrix(A2, 1)
     with pytest.raises(dak.DakError):
-        dak.dak_gemm(p, torch.zeros((300, 64), dtype=torch.bfloat16, device="cuda"))  # N > 256
+        dak.dak_gemm(p, torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda"),
+                     torch.zeros((1, 64), dtype=torch.bfloat16, device="cuda"))  # N = 0
     p.free()
 
 
@@ -212,3 +213,37 @@ def test_programmatic_launch_chain(dak):
                       og.gemm_ref(A2, outs[0][0])) <= REL_TOL
     for p in (p1, p2, kv):
         p.free()
+
+
+@pytest.mark.parametrize("N", [257, 300, 512, 777, 2048, 2100])
+def test_large_n_shared_tiles(dak, N):
+    """N > 256: a cluster of ceil(N/256) CTAs shares each tile row (rank 0 fetches every A
+    chunk and forwards it through distributed shared memory), N > 2048 in launches of
+    2048 rows; matches the oracle and stays identical across offload ratios."""
+    M, K = 320, 1280
+    A, B = synth.gemm_inputs(M, K, N, seed=N + 1)
+    ref = og.gemm_ref(A, B)
+    base = _run(dak, A, B, 0)
+    assert og.rel_err(to_np(base), ref) <= FP32_OUT_TOL
+    for h in (2, 5):
+        assert np.array_equal(bits_of(_run(dak, A, B, h)), bits_of(base)), h
+    C16 = _run(dak, A, B, 3, fp32=False)
+    assert og.rel_err(to_np(C16), ref) <= REL_TOL
+
+
+def test_large_n_integer_exact(dak):
+    M, K, N = 192, 2048, 520
+    A, B = synth.gemm_inputs(M, K, N, seed=9, integer=True)
+    C = _run(dak, A, B, 1, tuning=dict(pdl=1))
+    assert np.array_equal(to_np(C), og.gemm_ref(A, B))
+
+
+def test_large_n_ragged_k_and_tuning(dak):
+    """K not a multiple of 64 (2-D B boxes), tuning knobs that only move work."""
+    M, K, N = 200, 520, 600
+    A, B = synth.gemm_inputs(M, K, N, seed=77)
+    ref = og.gemm_ref(A, B)
+    base = _run(dak, A, B, 1)
+    assert og.rel_err(to_np(base), ref) <= FP32_OUT_TOL
+    for tun in (dict(host_ctas=1, window=2), dict(no_wave_align=1), dict(pdl=1)):
+        assert np.array_equal(bits_of(_run(dak, A, B, 2, tuning=tun)), bits_of(base)), tun

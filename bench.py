@@ -450,11 +450,10 @@ def run_planner_check(dak, lin, attn, b_host, b_hbm, dev, x_global=0.1):
 
 def run_large_n(dak, lin, b_host, b_hbm, dev, x=0.25):
     """dak_gemm beyond one CTA's 256 hidden-state rows: the 8B gate+up linear at x, N in
-    {256, 512, 1024, 2048}. A cluster of ceil(N/256) CTAs shares each tile row, rank 0
-    forwarding every A chunk through distributed shared memory, so the host link carries
-    the host bytes once per launch of up to 2048 rows. Reported against the
-    traffic-amplified model of separate 256-row launches (host bytes x ceil(N/256) /
-    B_host, as [DAK] Table 1 counts it without multicast) and the single-read model."""
+    {256, 512, 1024, 2048}, both ways: column blocks of 256 rows (host bytes read once per
+    block, as [DAK] Table 1 counts traffic without multicast) and shared tile rows (a
+    cluster of ceil(N/256) CTAs, rank 0 forwarding every A chunk through distributed
+    shared memory, host bytes read once), against both traffic models."""
     import torch
     import synth
     A = lin["gate_up"][0]
@@ -464,13 +463,16 @@ def run_large_n(dak, lin, b_host, b_hbm, dev, x=0.25):
     for N in (256, 512, 1024, 2048):
         B = torch.from_numpy(synth.normal_bf16(7, 2, N * K).view("int16")).view(torch.bfloat16).to(dev).view(N, K)
         C = torch.empty((N, M), dtype=torch.bfloat16, device=dev)
-        t = time_steps(lambda: dak.dak_gemm(p, B, C, tuning=dict(pdl=1)), 10, 2)
         blocks = -(-N // 256)
         launches = -(-N // 2048)
-        rows.append({"N": N, "us": t * 1e6, "host_link_bytes": p.host_bytes * launches,
-                     "host_link_gbps": p.host_bytes * launches / t / 1e9,
-                     "model_single_read_us": 1e6 * launches * max(p.host_bytes / b_host, p.hbm_bytes / b_hbm),
-                     "model_per_256_rows_us": 1e6 * blocks * max(p.host_bytes / b_host, p.hbm_bytes / b_hbm)})
+        rec = {"N": N,
+               "model_per_256_rows_us": 1e6 * blocks * max(p.host_bytes / b_host, p.hbm_bytes / b_hbm),
+               "model_single_read_us": 1e6 * launches * max(p.host_bytes / b_host, p.hbm_bytes / b_hbm)}
+        for wide, key in ((0, "column_blocks"), (1, "shared_tiles")):
+            t = time_steps(lambda: dak.dak_gemm(p, B, C, tuning=dict(pdl=1, wide_b=wide)), 5, 1)
+            link = p.host_bytes * (launches if wide else blocks)
+            rec[key] = {"us": t * 1e6, "host_link_bytes": link, "host_link_gbps": link / t / 1e9}
+        rows.append(rec)
     p.free()
     return {"op": "gate_up 28672x4096", "x": x, "host_bytes": p.host_bytes, "rows": rows,
             "status": dak.dak_last_error()[0]}

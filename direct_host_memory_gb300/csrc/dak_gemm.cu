@@ -806,18 +806,22 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
     return cuda_status(e);
 }
 
-// Any N: up to kMaxWideN hidden-state rows per launch (a cluster shares each tile row, so
-// host tiles cross the link once), larger N in column blocks of kMaxWideN rows, one launch
-// each (B rows and C rows of a block are contiguous; every block reads the host tiles again).
+// Any N, in column blocks of hidden-state rows (B rows and C rows of a block are
+// contiguous), one launch each: blocks of 256 rows by default, every block reading the host
+// tiles again; with wide_b blocks of up to kMaxWideN rows in which a cluster shares each
+// tile row, so the host tiles cross the link once per block. On GB300, with M = 64 tiles,
+// the 256-row blocks measured faster: at N >= 512 B fills the ring and the forwarded A
+// chunks are only 8 KiB, so the forwarding round trip bounds each cluster's stream.
 dak_status launch_gemm(const dak_placement* A, const void* host_src, const void* B, void* C, int N, int c_fp32,
                        const dak_tuning* t, cudaStream_t stream) {
     if (!A || A->kind != 0) return DAK_ERR_INVALID;
-    if (N <= kMaxWideN) return launch_gemm_block(A, host_src, B, C, N, c_fp32, t, stream);
+    const int block = (t && t->wide_b == 1) ? kMaxWideN : kMaxBlockN;
+    if (N <= block) return launch_gemm_block(A, host_src, B, C, N, c_fp32, t, stream);
     if (!B || !C) return DAK_ERR_INVALID;
     const size_t b_row = static_cast<size_t>(A->K) * 2;
     const size_t c_row = static_cast<size_t>(A->M) * (c_fp32 ? 4 : 2);
-    for (int n0 = 0; n0 < N; n0 += kMaxWideN) {
-        const int nb = std::min(kMaxWideN, N - n0);
+    for (int n0 = 0; n0 < N; n0 += block) {
+        const int nb = std::min(block, N - n0);
         const dak_status r = launch_gemm_block(A, host_src, static_cast<const uint8_t*>(B) + n0 * b_row,
                                                static_cast<uint8_t*>(C) + n0 * c_row, nb, c_fp32, t, stream);
         if (r != DAK_OK) return r;

@@ -215,35 +215,41 @@ def test_programmatic_launch_chain(dak):
         p.free()
 
 
+@pytest.mark.parametrize("wide", [0, 1])
 @pytest.mark.parametrize("N", [257, 300, 512, 777, 2048, 2100])
-def test_large_n_shared_tiles(dak, N):
-    """N > 256: a cluster of ceil(N/256) CTAs shares each tile row (rank 0 fetches every A
-    chunk and forwards it through distributed shared memory), N > 2048 in launches of
-    2048 rows; matches the oracle and stays identical across offload ratios."""
+def test_large_n(dak, N, wide):
+    """N > 256, as column blocks of 256 rows (wide = 0) or as cluster launches of up to 2048
+    rows in which rank 0 fetches every A chunk and forwards it to the other CTAs through
+    distributed shared memory (wide = 1); matches the oracle and stays identical across
+    offload ratios."""
     M, K = 320, 1280
     A, B = synth.gemm_inputs(M, K, N, seed=N + 1)
     ref = og.gemm_ref(A, B)
-    base = _run(dak, A, B, 0)
+    tun = dict(wide_b=wide)
+    base = _run(dak, A, B, 0, tuning=tun)
     assert og.rel_err(to_np(base), ref) <= FP32_OUT_TOL
     for h in (2, 5):
-        assert np.array_equal(bits_of(_run(dak, A, B, h)), bits_of(base)), h
-    C16 = _run(dak, A, B, 3, fp32=False)
+        assert np.array_equal(bits_of(_run(dak, A, B, h, tuning=tun)), bits_of(base)), h
+    C16 = _run(dak, A, B, 3, fp32=False, tuning=tun)
     assert og.rel_err(to_np(C16), ref) <= REL_TOL
 
 
 def test_large_n_integer_exact(dak):
     M, K, N = 192, 2048, 520
     A, B = synth.gemm_inputs(M, K, N, seed=9, integer=True)
-    C = _run(dak, A, B, 1, tuning=dict(pdl=1))
-    assert np.array_equal(to_np(C), og.gemm_ref(A, B))
+    for wide in (0, 1):
+        C = _run(dak, A, B, 1, tuning=dict(pdl=1, wide_b=wide))
+        assert np.array_equal(to_np(C), og.gemm_ref(A, B)), wide
 
 
-def test_large_n_ragged_k_and_tuning(dak):
+@pytest.mark.parametrize("wide", [0, 1])
+def test_large_n_ragged_k_and_tuning(dak, wide):
     """K not a multiple of 64 (2-D B boxes), tuning knobs that only move work."""
     M, K, N = 200, 520, 600
     A, B = synth.gemm_inputs(M, K, N, seed=77)
     ref = og.gemm_ref(A, B)
-    base = _run(dak, A, B, 1)
+    base = _run(dak, A, B, 1, tuning=dict(wide_b=wide))
     assert og.rel_err(to_np(base), ref) <= FP32_OUT_TOL
     for tun in (dict(host_ctas=1, window=2), dict(no_wave_align=1), dict(pdl=1)):
+        tun["wide_b"] = wide
         assert np.array_equal(bits_of(_run(dak, A, B, 2, tuning=tun)), bits_of(base)), tun

@@ -29,6 +29,7 @@ EXPORTS = [
     "dak_gemm_staged", "dak_attn_staged", "dak_attn_noalloc", "dak_selftest_wait",
     "dak_decoder_create", "dak_decoder_batch", "dak_decoder_step", "dak_decoder_capture",
     "dak_decoder_replay", "dak_decoder_launches", "dak_decoder_free", "dak_tune_gemm", "dak_tune_attn",
+    "dak_place_matrix_glu",
 ]
 
 # size of the fixed device array dak_attn_noalloc uses (DAK_NOALLOC_SCRATCH_BYTES in dak.h)
@@ -81,6 +82,7 @@ def _load():
         "dak_status_string": (ctypes.c_char_p, [i32]),
         "dak_place_matrix": (i32, [vp, i32, i64, i64, i64, i32, i32, P(vp)]),
         "dak_place_kv": (i32, [vp, vp, i32, i32, i32, i32, i32, i32, P(vp)]),
+        "dak_place_matrix_glu": (i32, [vp, i32, i64, i64, i64, i32, i32, P(vp)]),
         "dak_free": (i32, [vp]),
         "dak_placement_info": (i32, [vp, P(i64), P(i64), P(i64), P(i64)]),
         "dak_gemm": (i32, [vp, vp, vp, i32, i32, P(dak_tuning), vp]),
@@ -213,6 +215,18 @@ def dak_place_matrix(A, n_host_tiles: int, tile_m: int = 64) -> Placement:
     return Placement(out, "matrix", M=M, K=K, tile_m=tile_m)
 
 
+def dak_place_matrix_glu(A, n_host_tiles: int, tile_m: int = 64) -> Placement:
+    """Place a SwiGLU weight A [2f][K] (f gate rows, then f up rows) interleaved, so that
+    dak_gemm over it returns silu(gate) * up [N][f]."""
+    if A.ndim != 2 or int(A.shape[0]) % 2:
+        raise ValueError("A must be 2-D [2f][K]")
+    M, K = int(A.shape[0]), int(A.shape[1])
+    out = ctypes.c_void_p()
+    _check(lib.dak_place_matrix_glu(_ptr(A), _on_device(A), M // 2, K, K, tile_m, int(n_host_tiles),
+                                    ctypes.byref(out)), "dak_place_matrix_glu")
+    return Placement(out, "matrix", M=M, K=K, tile_m=tile_m, glu=True)
+
+
 def dak_place_kv(K, V, n_host_requests: int) -> Placement:
     """Place a KV cache, K and V [B][H_kv][L][D] bf16 (torch or numpy uint16 bits)."""
     if K.shape != V.shape or K.ndim != 4:
@@ -248,7 +262,8 @@ def dak_gemm(A: Placement, B, C=None, c_fp32: bool = False, tuning=None, stream=
     if B.ndim != 2 or int(B.shape[1]) != A.meta["K"]:
         raise ValueError("B must be [N][K]")
     if C is None:
-        C = torch.empty((N, A.meta["M"]), dtype=torch.float32 if c_fp32 else torch.bfloat16, device=B.device)
+        cols = A.meta["M"] // 2 if A.meta.get("glu") else A.meta["M"]
+        C = torch.empty((N, cols), dtype=torch.float32 if c_fp32 else torch.bfloat16, device=B.device)
     _check(lib.dak_gemm(A.handle, _ptr(B), _ptr(C), N, int(bool(c_fp32)), _tuning(tuning), _stream_ptr(stream)),
            "dak_gemm")
     return C
@@ -478,15 +493,19 @@ class Decoder:
             pass
 
 
-def place_decoder_layer(weights: dict, kv, host_units: dict, device=None) -> dict:
+def place_decoder_layer(weights: dict, kv, host_units: dict, device=None, glu: bool = True) -> dict:
     """Place one layer: weights maps 'qkv', 'o', 'gate_up', 'down' to [out][in] bf16 sources
     (numpy bits or torch) and 'attn_norm', 'mlp_norm' to [d] gains; kv = (K, V) sources
-    [B][H_kv][L][D]; host_units maps each of DECODER_OPS to its host tile rows / requests."""
+    [B][H_kv][L][D]; host_units maps each of DECODER_OPS to its host tile rows / requests.
+    glu places gate_up interleaved so that the SwiGLU runs in the GEMM's epilogue."""
     import torch
     dev = device or torch.device("cuda")
     L = {}
     for k in ("qkv", "o", "gate_up", "down"):
-        L[k] = dak_place_matrix(weights[k], int(host_units[k]))
+        if k == "gate_up" and glu:
+            L[k] = dak_place_matrix_glu(weights[k], int(host_units[k]))
+        else:
+            L[k] = dak_place_matrix(weights[k], int(host_units[k]))
     L["kv"] = dak_place_kv(kv[0], kv[1], int(host_units["kv"]))
     for k in ("attn_norm", "mlp_norm"):
         g = weights[k]

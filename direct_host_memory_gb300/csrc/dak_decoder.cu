@@ -11,8 +11,9 @@
 //   dak_attn  q over the cache -> a (bf16)
 //   dak_gemm  Wo . a -> x += (fp32)                         [added by the next rmsnorm]
 //   rmsnorm   x -> h
-//   dak_gemm  Wgu . h -> gu (fp32)
-//   swiglu    silu(gate) * up -> act (bf16)                 [this file]
+//   dak_gemm  Wgu . h -> act = silu(gate) * up (bf16)      [fused in the GEMM's epilogue when
+//                                                            Wgu is placed gate/up interleaved;
+//                                                            else gu (fp32) + swiglu here]
 //   dak_gemm  Wdown . act -> x +=
 // and a final rmsnorm writes the output. With programmatic dependent launch every kernel
 // starts while its predecessors drain. Before its own griddepcontrol.wait a kernel reads
@@ -426,12 +427,17 @@ dak_status enqueue_step(dak_decoder* d, const void* x_in, const int* positions, 
         nb.d = c.hidden;
         nb.eps = c.rms_eps;
         if ((r = norm(d, nb, 0, pdl, s)) != DAK_OK) return r;
-        if ((r = launch_gemm(L.gate_up, src(2), d->h, d->gu, B, 1, &tg[2], s)) != DAK_OK) return r;
-        const long long n4 = static_cast<long long>(B) * c.ffn / 4;
-        const int sg = static_cast<int>(std::min<long long>((n4 + 255) / 256, 4ll * device_sm_count()));
-        if ((r = cuda_status(launch(swiglu_kernel, dim3(static_cast<unsigned>(std::max(sg, 1))), 256, pdl, s,
-                                    static_cast<const float*>(d->gu), d->act, B, c.ffn))) != DAK_OK)
-            return r;
+        if (L.gate_up->glu) {
+            // gate/up interleaved placement: the GEMM's epilogue writes silu(gate) * up itself
+            if ((r = launch_gemm(L.gate_up, src(2), d->h, d->act, B, 0, &tg[2], s)) != DAK_OK) return r;
+        } else {
+            if ((r = launch_gemm(L.gate_up, src(2), d->h, d->gu, B, 1, &tg[2], s)) != DAK_OK) return r;
+            const long long n4 = static_cast<long long>(B) * c.ffn / 4;
+            const int sg = static_cast<int>(std::min<long long>((n4 + 255) / 256, 4ll * device_sm_count()));
+            if ((r = cuda_status(launch(swiglu_kernel, dim3(static_cast<unsigned>(std::max(sg, 1))), 256, pdl, s,
+                                        static_cast<const float*>(d->gu), d->act, B, c.ffn))) != DAK_OK)
+                return r;
+        }
         if ((r = launch_gemm(L.down, src(3), d->act, d->dn, B, 1, &tg[3], s)) != DAK_OK) return r;
         if (mode == 2 && cudaEventRecord(d->ev_consumed[l & 1], s) != cudaSuccess) return DAK_ERR_CUDA;
         NormArgs nc{};
@@ -608,8 +614,9 @@ extern "C" dak_status dak_decoder_replay(dak_decoder* dec, void* stream) {
 extern "C" int dak_decoder_launches(const dak_decoder* dec, int mode) {
     (void)mode;
     if (!dec) return 0;
-    const int per_layer = 9 + (dec->n_split > 1 ? 1 : 0);
-    return 1 + dec->cfg.n_layers * per_layer;
+    int n = 1;
+    for (const auto& L : dec->layers) n += 8 + (dec->n_split > 1 ? 1 : 0) + (L.gate_up->glu ? 0 : 1);
+    return n;
 }
 
 extern "C" dak_status dak_decoder_free(dak_decoder* dec) {

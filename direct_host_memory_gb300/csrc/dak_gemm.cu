@@ -42,7 +42,11 @@ struct GemmParams {
     int S;        // CTAs per cluster splitting each tile row's K range (1 = no split)
     int red_off;  // byte offset (from the aligned ring base) of the partial-sum area, S > 1
     int NC;       // CTAs per cluster sharing each tile row across 256-row blocks of B (1 = off)
+    int glu;      // rows interleaved gate/up: C[n][row/2] = silu(gate) * up, C is [N][M/2]
 };
+
+// SwiGLU of one gate / up pair (the same expression as the decoder's standalone kernel)
+__device__ __forceinline__ float swiglu_pair(float g, float u) { return g / (1.f + expf(-g)) * u; }
 
 // Tiles of this CTA: role, first tile, stride, count, and the chunk range [c_lo, c_hi) of
 // every tile row that this CTA (rank `rank` of its cluster) accumulates.
@@ -322,7 +326,25 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
             acc[n] = v;
         }
         const int row = t * kTileM + w * 8 + r;
-        if (kq == 0 && row < p.M) {
+        if (p.glu) {
+            // rows 2j (gate) and 2j + 1 (up) are lanes r and r ^ 1 of this group
+            float up[N];
+#pragma unroll
+            for (int n = 0; n < N; ++n) up[n] = __shfl_xor_sync(0xffffffffu, acc[n], 1);
+            if (kq == 0 && row < p.M && !(row & 1)) {
+                const int half = p.M >> 1, col = row >> 1;
+#pragma unroll
+                for (int n = 0; n < N; ++n) {
+                    const float a = swiglu_pair(acc[n], up[n]);
+                    if (p.c_fp32) {
+                        reinterpret_cast<float*>(p.C)[static_cast<long long>(n) * half + col] = a;
+                    } else {
+                        reinterpret_cast<__nv_bfloat16*>(p.C)[static_cast<long long>(n) * half + col] =
+                            __float2bfloat16_rn(a);
+                    }
+                }
+            }
+        } else if (kq == 0 && row < p.M) {
 #pragma unroll
             for (int n = 0; n < N; ++n) {
                 if (p.c_fp32) {
@@ -534,10 +556,10 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
                 uint32_t v[8];
                 tmem_ld8(taddr + static_cast<uint32_t>(n0), v);
                 tmem_wait_ld();
-                if (valid) {
-                    float f[8];
+                float f[8];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(v[j]);
+                for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(v[j]);
+                if (valid) {
                     for (int r = 1; r < p.S; ++r) {
                         const float4* pr = reinterpret_cast<const float4*>(
                             red + static_cast<size_t>((r - 1) * kTileM + row_in_tile) * p.N_pad + n0);
@@ -545,6 +567,29 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
                         f[0] += x0.x; f[1] += x0.y; f[2] += x0.z; f[3] += x0.w;
                         f[4] += x1.x; f[5] += x1.y; f[6] += x1.z; f[7] += x1.w;
                     }
+                }
+                if (p.glu) {
+                    // rows 2j (gate) and 2j + 1 (up) sit in neighbouring lanes of this sub-partition
+                    float up[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) up[j] = __shfl_xor_sync(0xffffffffu, f[j], 1);
+                    if (valid && !(row_in_tile & 1)) {
+                        const int half = p.M >> 1, col = row >> 1;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int n = n_off + n0 + j;
+                            if (n < p.N) {
+                                const float a = swiglu_pair(f[j], up[j]);
+                                if (p.c_fp32) {
+                                    reinterpret_cast<float*>(p.C)[static_cast<long long>(n) * half + col] = a;
+                                } else {
+                                    reinterpret_cast<__nv_bfloat16*>(p.C)[static_cast<long long>(n) * half + col] =
+                                        __float2bfloat16_rn(a);
+                                }
+                            }
+                        }
+                    }
+                } else if (valid) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const int n = n_off + n0 + j;
@@ -692,6 +737,7 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
     p.h = A->h;
     p.c_fp32 = c_fp32 ? 1 : 0;
     p.tile_bytes = A->tile_bytes;
+    p.glu = A->glu;
     p.S = 1;
     p.st = status_ptr();
     if (!p.st) return DAK_ERR_CUDA;
@@ -819,7 +865,7 @@ dak_status launch_gemm(const dak_placement* A, const void* host_src, const void*
     if (N <= block) return launch_gemm_block(A, host_src, B, C, N, c_fp32, t, stream);
     if (!B || !C) return DAK_ERR_INVALID;
     const size_t b_row = static_cast<size_t>(A->K) * 2;
-    const size_t c_row = static_cast<size_t>(A->M) * (c_fp32 ? 4 : 2);
+    const size_t c_row = static_cast<size_t>(A->glu ? A->M / 2 : A->M) * (c_fp32 ? 4 : 2);
     for (int n0 = 0; n0 < N; n0 += block) {
         const int nb = std::min(block, N - n0);
         const dak_status r = launch_gemm_block(A, host_src, static_cast<const uint8_t*>(B) + n0 * b_row,

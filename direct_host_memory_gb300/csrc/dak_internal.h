@@ -9,6 +9,7 @@
 struct dak_placement {
     int kind;    // 0 = matrix (GEMM weights), 1 = KV cache
     int device;  // device the placement was made on
+    int glu;     // matrix: gate/up rows interleaved (row 2j gate j, row 2j+1 up j); dak_gemm applies SwiGLU
     // tier buffers: host part (pinned, device-mapped; host and device addresses) and HBM part
     void* host_ptr;
     void* host_dev;

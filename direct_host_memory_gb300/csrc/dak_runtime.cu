@@ -100,9 +100,10 @@ Sched schedule(int host_units, int hbm_units, int sm_slots, const dak_tuning* t,
 
 // Row-major A rows [rows][lda] (16-byte units of 8 bf16) -> tile rows stored
 // [K_pad/8][64][8]: unit (t, kg, r) at t*KG*64 + kg*64 + r. Rows past `rows` and
-// k-groups past K/8 are zero.
-__global__ void pack_matrix_kernel(const uint4* __restrict__ src, long long lda16, long long rows, int K16, int KG,
-                                   uint4* __restrict__ dst, long long units) {
+// k-groups past K/8 are zero. With src_b set, packed row j comes from row j/2 of src
+// (j even) or of src_b (j odd): the gate/up interleave of a SwiGLU weight.
+__global__ void pack_matrix_kernel(const uint4* __restrict__ src, const uint4* __restrict__ src_b, long long lda16,
+                                   long long rows, int K16, int KG, uint4* __restrict__ dst, long long units) {
     for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < units;
          idx += static_cast<long long>(gridDim.x) * blockDim.x) {
         const long long per_tile = static_cast<long long>(KG) * kTileM;
@@ -112,7 +113,9 @@ __global__ void pack_matrix_kernel(const uint4* __restrict__ src, long long lda1
         const int r = rem - kg * kTileM;
         const long long row = t * kTileM + r;
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (row < rows && kg < K16) v = src[row * lda16 + kg];
+        if (row < rows && kg < K16) {
+            v = src_b ? ((row & 1) ? src_b : src)[(row >> 1) * lda16 + kg] : src[row * lda16 + kg];
+        }
         dst[idx] = v;
     }
 }
@@ -193,11 +196,14 @@ extern "C" const char* dak_status_string(int s) {
     }
 }
 
-extern "C" dak_status dak_place_matrix(const void* A_src, int src_on_device, int64_t M, int64_t K, int64_t lda,
-                                       int tile_m, int n_host_tiles, dak_placement** out) {
+// glu: A_src holds [2f][K] (f gate rows, then f up rows) with M = 2f; the placement stores
+// them interleaved (row 2j = gate j, row 2j + 1 = up j).
+static dak_status place_matrix(const void* A_src, int src_on_device, int64_t M, int64_t K, int64_t lda, int tile_m,
+                               int n_host_tiles, bool glu, dak_placement** out) {
     if (!out) return DAK_ERR_INVALID;
     *out = nullptr;
     if (M < 0 || K <= 0 || lda < K || (M > 0 && !A_src)) return DAK_ERR_INVALID;
+    if (glu && (M % (2 * kTileM))) return DAK_ERR_INVALID;  // whole tiles of 32 gate + 32 up rows
     if (tile_m != kTileM) return DAK_ERR_UNSUPPORTED;
     if ((K % 8) || (lda % 8) || (reinterpret_cast<uintptr_t>(A_src) & 15)) return DAK_ERR_ALIGN;
     if (K > (1 << 24) || M > (1ll << 31)) return DAK_ERR_INVALID;
@@ -210,6 +216,7 @@ extern "C" dak_status dak_place_matrix(const void* A_src, int src_on_device, int
     std::memset(p, 0, sizeof(*p));
     p->kind = 0;
     p->device = dev;
+    p->glu = glu ? 1 : 0;
     p->M = M;
     p->K = K;
     p->K_pad = (K + 15) / 16 * 16;
@@ -242,16 +249,32 @@ extern "C" dak_status dak_place_matrix(const void* A_src, int src_on_device, int
             return DAK_ERR_DEVICE_ALLOC;
         }
     }
+    const int64_t f = M / 2;
     for (int t0 = 0; t0 < T && e == cudaSuccess; t0 += batch_tiles) {
         const int nt = std::min(batch_tiles, T - t0);
         const long long row0 = static_cast<long long>(t0) * kTileM;
         const long long rows = std::min<long long>(static_cast<long long>(nt) * kTileM, M - row0);
+        const uint8_t* a8 = static_cast<const uint8_t*>(A_src);
         const uint4* src;
-        if (src_on_device) {
-            src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(A_src) + row0 * lda * 2);
+        const uint4* src_b = nullptr;  // glu: the up rows (src: the gate rows)
+        if (glu) {
+            const long long g0 = row0 / 2, n_rows = rows / 2;
+            if (src_on_device) {
+                src = reinterpret_cast<const uint4*>(a8 + g0 * lda * 2);
+                src_b = reinterpret_cast<const uint4*>(a8 + (f + g0) * lda * 2);
+            } else {
+                uint8_t* t8 = static_cast<uint8_t*>(tmp);
+                e = cudaMemcpy(t8, a8 + g0 * lda * 2, static_cast<size_t>(n_rows * lda * 2), cudaMemcpyHostToDevice);
+                if (e == cudaSuccess)
+                    e = cudaMemcpy(t8 + n_rows * lda * 2, a8 + (f + g0) * lda * 2, static_cast<size_t>(n_rows * lda * 2),
+                                   cudaMemcpyHostToDevice);
+                src = reinterpret_cast<const uint4*>(t8);
+                src_b = reinterpret_cast<const uint4*>(t8 + n_rows * lda * 2);
+            }
+        } else if (src_on_device) {
+            src = reinterpret_cast<const uint4*>(a8 + row0 * lda * 2);
         } else {
-            e = cudaMemcpy(tmp, static_cast<const uint8_t*>(A_src) + row0 * lda * 2,
-                           static_cast<size_t>(rows * lda * 2), cudaMemcpyHostToDevice);
+            e = cudaMemcpy(tmp, a8 + row0 * lda * 2, static_cast<size_t>(rows * lda * 2), cudaMemcpyHostToDevice);
             src = reinterpret_cast<const uint4*>(tmp);
         }
         if (e != cudaSuccess) break;
@@ -266,8 +289,10 @@ extern "C" dak_status dak_place_matrix(const void* A_src, int src_on_device, int
             const long long units = static_cast<long long>(hi - lo) * KG * kTileM;
             const long long src_row0 = static_cast<long long>(lo - t0) * kTileM;
             const long long src_rows = std::max(0ll, rows - src_row0);
-            pack_matrix_kernel<<<pack_grid(units), 256>>>(src + src_row0 * lda16, lda16, src_rows, K16, KG, dst,
-                                                          units);
+            // glu: packed row j of this part reads row j/2 of the gate or up block
+            const long long off = glu ? (src_row0 / 2) * lda16 : src_row0 * lda16;
+            pack_matrix_kernel<<<pack_grid(units), 256>>>(src + off, src_b ? src_b + off : nullptr, lda16, src_rows,
+                                                          K16, KG, dst, units);
             e = cudaGetLastError();
         }
         if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -281,6 +306,20 @@ extern "C" dak_status dak_place_matrix(const void* A_src, int src_on_device, int
     }
     *out = p;
     return DAK_OK;
+}
+
+extern "C" dak_status dak_place_matrix(const void* A_src, int src_on_device, int64_t M, int64_t K, int64_t lda,
+                                       int tile_m, int n_host_tiles, dak_placement** out) {
+    return place_matrix(A_src, src_on_device, M, K, lda, tile_m, n_host_tiles, false, out);
+}
+
+extern "C" dak_status dak_place_matrix_glu(const void* A_src, int src_on_device, int64_t f, int64_t K, int64_t lda,
+                                           int tile_m, int n_host_tiles, dak_placement** out) {
+    if (f <= 0) {
+        if (out) *out = nullptr;
+        return DAK_ERR_INVALID;
+    }
+    return place_matrix(A_src, src_on_device, 2 * f, K, lda, tile_m, n_host_tiles, true, out);
 }
 
 extern "C" dak_status dak_place_kv(const void* K_src, const void* V_src, int src_on_device, int B, int H_kv, int L,

@@ -115,6 +115,16 @@ typedef struct {
 dak_status dak_place_matrix(const void* A_src, int src_on_device, int64_t M, int64_t K, int64_t lda,
                             int tile_m, int n_host_tiles, dak_placement** out);
 
+/* Place the weight of a SwiGLU projection for a fused epilogue: A_src is [2f][K] bf16 (row
+ * pitch lda), the f gate rows followed by the f up rows (f a multiple of 32). The placement
+ * stores them interleaved (row 2j = gate j, row 2j + 1 = up j, so every tile row holds 32
+ * gate/up pairs); dak_gemm over it then writes C [N][f] = silu(gate) * up with
+ * silu(z) = z / (1 + e^-z), computed in fp32 from the fp32 accumulators, instead of the
+ * [N][2f] product. Otherwise as dak_place_matrix (tile rows 0 .. n_host_tiles-1 on the
+ * host; 2f / 64 tile rows in all). */
+dak_status dak_place_matrix_glu(const void* A_src, int src_on_device, int64_t f, int64_t K, int64_t lda, int tile_m,
+                                int n_host_tiles, dak_placement** out);
+
 /* Place a KV cache, K and V each [B][H_kv][L][D] bf16 contiguous (the pre-allocated,
  * per-request static cache of section 5). Section 5 "Supporting FlashAttention": the
  * cache is split along the batch dimension; requests 0 .. n_host_requests-1 go to pinned,
@@ -138,7 +148,8 @@ dak_status dak_placement_info(const dak_placement* p, int64_t* host_bytes, int64
 /* C = A x B over a tiered placement (SplitK_GEMM; section 4.1 "Kernel over Partitioned
  * Memory", "Asynchronous TMA Access", Fig. 5b).
  *   B : hidden states, bf16 [N][K] row-major (device), 16-byte aligned.
- *   C : output [N][M] row-major (device); bf16 if c_fp32 == 0, else fp32.
+ *   C : output [N][M] row-major (device); bf16 if c_fp32 == 0, else fp32 ([N][M/2] of
+ *       silu(gate) * up for a placement made by dak_place_matrix_glu).
  *   N : >= 1. Up to 256 rows run as one launch; a larger N runs as column blocks of 256
  *       rows, one launch each, every block reading the host tiles again (host-link bytes =
  *       host bytes x ceil(N / 256); no multicast, section 4.3.2, Table 1), or with
@@ -261,7 +272,8 @@ typedef struct {
  * and still owned by the caller, who frees them after dak_decoder_free.
  *   qkv    : [(H_q + 2 H_kv) D] x d: query rows (head-major), then key rows, then value rows.
  *   o      : d x (H_q D).
- *   gate_up: 2f x d: the f gate rows, then the f up rows.
+ *   gate_up: 2f x d: the f gate rows, then the f up rows. Placed with dak_place_matrix_glu,
+ *            the SwiGLU runs in the GEMM's epilogue (one launch less per layer).
  *   down   : d x f.
  *   kv     : the layer's KV cache (B requests, H_kv heads, capacity L, head dim D); every
  *            layer's cache has the same B, which is the step's batch.

@@ -45,12 +45,12 @@ def _host_units(cfg, B, frac):
     return u
 
 
-def _build(dak, cfg, layers, caches, fnorm, units, **kw):
+def _build(dak, cfg, layers, caches, fnorm, units, glu=True, **kw):
     import torch
     placed = []
     for l, (w, kv) in enumerate(zip(layers, caches)):
         u = units[l] if isinstance(units, list) else units
-        placed.append(dak.place_decoder_layer(w, kv, u))
+        placed.append(dak.place_decoder_layer(w, kv, u, glu=glu))
     g = torch.from_numpy(fnorm.view(np.int16)).view(torch.bfloat16).cuda()
     return dak.Decoder(cfg, placed, g, **kw)
 
@@ -112,6 +112,21 @@ def test_decoder_bit_identical_across_placement_modes_and_launches(dak):
                         base = b
                     assert np.array_equal(b, base), (units, plain, mode, graph)
             dec.free()
+
+
+def test_decoder_fused_swiglu_matches_separate_kernel(dak):
+    """SwiGLU in the gate/up GEMM's epilogue (interleaved placement) against the separate
+    SwiGLU kernel: same expression on the same fp32 accumulators, identical outputs."""
+    cfg, B, L, pos = SMALL128, 3, 300, [299, 0, 128]
+    layers, caches, fnorm, x0 = _inputs(cfg, B, L, seed=16)
+    outs = []
+    for glu in (True, False):
+        dec = _build(dak, cfg, layers, caches, fnorm, _host_units(cfg, B, 0.3), glu=glu)
+        outs.append(bits_of(_run(dak, dec, x0, pos)))
+        combine = 1 if dak.dak_attn_default_split(dec.layers[0]["kv"]) > 1 else 0
+        assert dec.launches() == 1 + cfg["n_layers"] * (8 + combine + (0 if glu else 1))
+        dec.free()
+    assert np.array_equal(outs[0], outs[1])
 
 
 def test_decoder_consecutive_steps(dak):

@@ -253,3 +253,33 @@ def test_large_n_ragged_k_and_tuning(dak, wide):
     for tun in (dict(host_ctas=1, window=2), dict(no_wave_align=1), dict(pdl=1)):
         tun["wide_b"] = wide
         assert np.array_equal(bits_of(_run(dak, A, B, 2, tuning=tun)), bits_of(base)), tun
+
+
+@pytest.mark.parametrize("N", [1, 5, 16, 64, 300])
+def test_glu_placement_fused_swiglu(dak, N):
+    """Gate/up interleaved placement: dak_gemm returns silu(gate) * up straight from its
+    accumulators; matches the oracle's swiglu of the plain product, identical across
+    offload ratios."""
+    from oracle import decoder as od
+    f, K = 256, 640  # 2f = 512 rows = 8 tile rows
+    A, B = synth.gemm_inputs(2 * f, K, N, seed=500 + N)
+    ref = od.swiglu(og.gemm_ref(A, B), f)
+    outs = []
+    for h in (0, 3, 8):
+        p = dak.dak_place_matrix_glu(A, h)
+        C = dak.dak_gemm(p, to_dev(B), c_fp32=True)
+        C16 = dak.dak_gemm(p, to_dev(B), c_fp32=False)
+        assert dak.dak_last_error()[0] == 0
+        assert tuple(C.shape) == (N, f)
+        assert og.rel_err(to_np(C), ref) <= FP32_OUT_TOL, h
+        assert og.rel_err(to_np(C16), ref) <= REL_TOL, h
+        outs.append(bits_of(C))
+        p.free()
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
+
+
+def test_glu_placement_rejects_bad_shapes(dak):
+    A = np.zeros((96, 64), dtype=np.uint16)  # 2f = 96: not whole tiles of 32 gate/up pairs
+    with pytest.raises(dak.DakError):
+        dak.dak_place_matrix_glu(A, 0)

@@ -549,7 +549,27 @@ def measure_tiers(dak):
             best_g = max(best_g, g)
     hc = 16
     ch, cg = dak.dak_probe_concurrent(G, 4 * G, hc, 4, dak.dak_sm_count() - hc, 4, 32768, 3)
-    return best_h * 1e9, best_g * 1e9, {"host_ctas": hc, "host_gbps": ch, "hbm_gbps": cg}
+    return best_h * 1e9, best_g * 1e9, {"host_ctas": hc, "host_gbps": ch, "hbm_gbps": cg,
+                                        "h2d_copy_gbps": h2d_copy_gbps()}
+
+
+def h2d_copy_gbps(nbytes=1 << 30, reps=3):
+    """cudaMemcpy host-to-device rate from pinned memory (the copy engine's path), recorded
+    beside the SM read probes for comparison."""
+    import torch
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    d.copy_(h, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        d.copy_(h, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    gbps = reps * nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9
+    del h, d
+    return gbps
 
 
 def time_steps(fn, steps, warmup, sync_all=None):
@@ -715,13 +735,20 @@ def main():
     sampler.start()
     time.sleep(0.3)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     t_wall0 = time.time()
     e0.record()
+    step_ev[0].record()
     for i in range(args.steps):
         st.run(att_ev[i])
+        step_ev[i + 1].record()
     e1.record()
     torch.cuda.synchronize()
     t_wall1 = time.time()
+    per_step = sorted(step_ev[i].elapsed_time(step_ev[i + 1]) for i in range(args.steps))
+
+    def pct(q):
+        return per_step[min(len(per_step) - 1, int(q * (len(per_step) - 1) + 0.5))]
     sync_all()
     value, t_step = aggregate_replicas(e0.elapsed_time(e1) / 1e3 / args.steps, st.total_bytes, dist)
     att_ms = statistics.mean(a.elapsed_time(b) for a, b in att_ev)
@@ -799,6 +826,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": step_config(args, world),
+        "ms_per_step_p10_p50_p90": [pct(0.1), pct(0.5), pct(0.9)],
         "step": {"x_effective": x_eff, "bytes_per_step": C, "host_bytes_per_step": st.host_bytes,
                  "kernels": "dak_gemm x4 (tcgen05 for N >= 8) + dak_attn (+ split combine)"},
         "decode_tok_s": n * args.batch / (t_step * LAYERS_8B),

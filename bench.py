@@ -45,6 +45,8 @@ def _args():
                     help="also time a full decode step of this model (planner ratios at --decode-x)")
     ap.add_argument("--decode-x", type=float, default=0.3, help="x_global of the decode step's HBM cap")
     ap.add_argument("--decode-steps", type=int, default=20)
+    ap.add_argument("--decode-sweep", default="0.1,0.2,0.5",
+                    help="further x_global values for the decode step (comma list, empty = none)")
     ap.add_argument("--no-planner-check", action="store_true",
                     help="skip the compute-bound / greedy-vs-uniform planner measurement")
     ap.add_argument("--plain-launch", action="store_true",
@@ -325,6 +327,31 @@ def run_decode(dak, args, b_host, b_hbm, dev, sync_all, local):
             res[key] = rec
         else:
             res.update(rec)
+    # per-x sweep of the step with both prefetch baselines (planner ratios at each x_global)
+    sweep = []
+    for xs in [float(v) for v in args.decode_sweep.split(",") if v.strip()]:
+        units, tmodel = decode_plan(dak, cfg, b_host, b_hbm, xs, peak_flops)
+        dec = build_decoder(dak, cfg, units)
+        C = sum(L_[k].host_bytes + L_[k].hbm_bytes for L_ in dec.layers for k in dak.DECODER_OPS)
+        H = dec.host_bytes()
+        roof = tier_roofline(C, H / C, b_host, b_hbm)
+        rec = {"x_global": xs, "x_effective": H / C}
+        for mode, name in ((dak.MODE_DIRECT, "dak"), (dak.MODE_PREFETCH_SERIAL, "prefetch_serial"),
+                           (dak.MODE_PREFETCH_OVERLAP, "prefetch_overlap")):
+            dec.capture(x_in, pos, out, mode)
+            t = time_steps(dec.replay, max(4, args.decode_steps // 4), 2, sync_all)
+            rec[name + "_tok_s"] = B / t
+            if mode == dak.MODE_DIRECT:
+                rec["frac"] = (C / t) / roof
+                rec["eff_gbps"] = C / t / 1e9
+        rec["vs_prefetch_best"] = rec["dak_tok_s"] / max(rec["prefetch_serial_tok_s"], rec["prefetch_overlap_tok_s"])
+        rec["planner_model_ms"] = tmodel * 1e3
+        rec["status"] = dak.dak_last_error()[0]
+        sweep.append(rec)
+        dec.free()
+        del dec
+        torch.cuda.empty_cache()
+    res["per_x"] = sweep
     return res
 
 

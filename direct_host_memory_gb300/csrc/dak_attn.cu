@@ -376,7 +376,7 @@ __global__ void attn_combine_kernel(const float* __restrict__ ws, __nv_bfloat16*
     }
 }
 
-constexpr int kAttnDefaultHostCtas = 16;
+constexpr int kAttnDefaultHostCtas = 32;
 constexpr int kAttnDefaultHostWindow = 4;
 constexpr int kAttnStages = 3;     // default ring depth: two CTAs fit on an SM
 constexpr int kAttnMaxStages = 5;

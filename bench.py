@@ -477,10 +477,11 @@ def run_planner_check(dak, lin, attn, b_host, b_hbm, dev, x_global=0.1):
 
 def run_large_n(dak, lin, b_host, b_hbm, dev, x=0.25):
     """dak_gemm beyond one CTA's 256 hidden-state rows: the 8B gate+up linear at x, N in
-    {256, 512, 1024, 2048}, both ways: column blocks of 256 rows (host bytes read once per
-    block, as [DAK] Table 1 counts traffic without multicast) and shared tile rows (a
-    cluster of ceil(N/256) CTAs, rank 0 forwarding every A chunk through distributed
-    shared memory, host bytes read once), against both traffic models."""
+    {256, 512, 1024, 2048}, both ways: shared tile rows (the default: a cluster of
+    ceil(N/256) CTAs, at most 4, rank 0 forwarding every A chunk through distributed shared
+    memory, host bytes read once per launch of up to 1024 rows) and column blocks of 256
+    rows (host bytes read once per block, as [DAK] Table 1 counts traffic without
+    multicast), against both traffic models."""
     import torch
     import synth
     A = lin["gate_up"][0]
@@ -491,13 +492,13 @@ def run_large_n(dak, lin, b_host, b_hbm, dev, x=0.25):
         B = torch.from_numpy(synth.normal_bf16(7, 2, N * K).view("int16")).view(torch.bfloat16).to(dev).view(N, K)
         C = torch.empty((N, M), dtype=torch.bfloat16, device=dev)
         blocks = -(-N // 256)
-        launches = -(-N // 2048)
+        launches = -(-N // 1024)
         rec = {"N": N,
                "model_per_256_rows_us": 1e6 * blocks * max(p.host_bytes / b_host, p.hbm_bytes / b_hbm),
                "model_single_read_us": 1e6 * launches * max(p.host_bytes / b_host, p.hbm_bytes / b_hbm)}
-        for wide, key in ((0, "column_blocks"), (1, "shared_tiles")):
-            t = time_steps(lambda: dak.dak_gemm(p, B, C, tuning=dict(pdl=1, wide_b=wide)), 5, 1)
-            link = p.host_bytes * (launches if wide else blocks)
+        for cols, key in ((1, "column_blocks"), (0, "shared_tiles")):
+            t = time_steps(lambda: dak.dak_gemm(p, B, C, tuning=dict(pdl=1, column_blocks=cols)), 5, 1)
+            link = p.host_bytes * (blocks if cols else launches)
             rec[key] = {"us": t * 1e6, "host_link_bytes": link, "host_link_gbps": link / t / 1e9}
         rows.append(rec)
     p.free()
@@ -839,7 +840,15 @@ def main():
     traffic = read_ncu_traffic()
 
     decode = run_decode(dak, args, b_host, b_hbm, dev, sync_all, local) if args.decode != "none" else None
-    planner_check = None if args.no_planner_check else run_planner_check(dak, lin, attn, b_host, b_hbm, dev)
+    planner_check = None
+    if not args.no_planner_check:
+        pc_sampler = ClockSampler(local)
+        pc_sampler.start()
+        tw0 = time.time()
+        planner_check = run_planner_check(dak, lin, attn, b_host, b_hbm, dev)
+        tw1 = time.time()
+        pc_sampler.stop()
+        planner_check["clocks"] = pc_sampler.summary(tw0, tw1)  # tensor-bound timings follow the SM clock
     large_n = None if args.no_planner_check else run_large_n(dak, lin, b_host, b_hbm, dev)
 
     cpu = None

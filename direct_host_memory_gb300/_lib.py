@@ -46,7 +46,7 @@ class dak_tuning(ctypes.Structure):
     _fields_ = [("host_ctas", ctypes.c_int), ("window", ctypes.c_int), ("hbm_window", ctypes.c_int),
                 ("chunk_k", ctypes.c_int), ("n_split", ctypes.c_int), ("hbm_ctas", ctypes.c_int),
                 ("split_k", ctypes.c_int), ("pdl", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
-                ("no_wave_align", ctypes.c_int), ("wide_b", ctypes.c_int)]
+                ("no_wave_align", ctypes.c_int), ("column_blocks", ctypes.c_int)]
 
 
 class dak_op(ctypes.Structure):

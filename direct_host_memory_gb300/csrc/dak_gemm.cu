@@ -43,6 +43,10 @@ struct GemmParams {
     int red_off;  // byte offset (from the aligned ring base) of the partial-sum area, S > 1
     int NC;       // CTAs per cluster sharing each tile row across 256-row blocks of B (1 = off)
     int glu;      // rows interleaved gate/up: C[n][row/2] = silu(gate) * up, C is [N][M/2]
+    // B chunk width. kcb == kc: each ring stage holds its A chunk and the matching B chunk.
+    // kcb < kc (wide B, N_pad > 128): the A ring holds kc-wide chunks only and B streams
+    // through its own ring of wb slots of kcb columns, kc / kcb of them per A chunk.
+    int kcb, wb, b_ring_off, b_slot_bytes;
 };
 
 // SwiGLU of one gate / up pair (the same expression as the decoder's standalone kernel)
@@ -126,7 +130,7 @@ __device__ __forceinline__ void issue_b(const GemmParams& p, const CUtensorMap* 
                                         uint64_t* bar, int kind, int row0) {
     const int blk = kind == kUmmaB ? 64 : 256;
     const int rows = kind == kUmmaB ? p.N_pad : p.N;
-    const int nblk = p.kc / blk;
+    const int nblk = p.kcb / blk;
     if (p.b3d) {
         tma_load_3d(dst, bmap, 0, row0, k0 / blk, bar);
     } else {
@@ -135,7 +139,7 @@ __device__ __forceinline__ void issue_b(const GemmParams& p, const CUtensorMap* 
 }
 
 __device__ __forceinline__ uint32_t b_stage_bytes(const GemmParams& p, int kind) {
-    return static_cast<uint32_t>(p.kc) * 2u * static_cast<uint32_t>(kind == kUmmaB ? p.N_pad : p.N);
+    return static_cast<uint32_t>(p.kcb) * 2u * static_cast<uint32_t>(kind == kUmmaB ? p.N_pad : p.N);
 }
 
 // Producer loops. `is_a` streams the tile rows of A (one bulk copy per stage), otherwise the
@@ -171,6 +175,34 @@ __device__ __forceinline__ void produce(const GemmParams& p, const TileIter& it,
     }
 done:
     drain_fills(full, W, i, p.st);
+}
+
+// B producer of the wide-B layout (kcb < kc): every A chunk's kc columns of B arrive as
+// kc / kcb copies into B's own ring, each arming its slot's full barrier.
+__device__ __forceinline__ void produce_b_ring(const GemmParams& p, const TileIter& it, const CUtensorMap* bmap,
+                                               uint8_t* smem, uint64_t* b_full, uint64_t* b_empty,
+                                               volatile int* abort) {
+    grid_dep_wait();  // the hidden states may come from the previous kernel of the stream
+    const int WB = p.wb;
+    const int row0 = p.NC > 1 ? it.rank * p.N_pad : 0;
+    long long ib = 0;
+    for (int ti = 0; ti < it.count && !*abort; ++ti) {
+        for (int c = it.c_lo; c < it.c_hi; ++c) {
+            const int kce = min(p.kc, p.K_pad - c * p.kc);
+            for (int sub = 0; sub * p.kcb < kce; ++sub, ++ib) {
+                const int sb = static_cast<int>(ib % WB);
+                if (ib >= WB && !mbar_wait(&b_empty[sb], static_cast<uint32_t>(((ib / WB) - 1) & 1), abort, p.st,
+                                           DAK_ERR_TIMEOUT, W_BPROD_EMPTY)) {
+                    goto done;
+                }
+                mbar_arrive_expect_tx(&b_full[sb], b_stage_bytes(p, kUmmaB));
+                issue_b(p, bmap, smem + p.b_ring_off + static_cast<size_t>(sb) * p.b_slot_bytes, c * p.kc + sub * p.kcb,
+                        &b_full[sb], kUmmaB, row0);
+            }
+        }
+    }
+done:
+    drain_fills(b_full, WB, ib, p.st);
 }
 
 // Shared tile rows across the 256-row blocks of a wide B (NC > 1). Rank 0 of the cluster
@@ -376,6 +408,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     __shared__ uint64_t full[8], empty[8], acc_full[2], acc_empty[2];
     __shared__ uint64_t red_full, red_empty;  // cluster split: partials in / partial buffer free
     __shared__ uint64_t peer_empty[8];        // wide B, rank 0: every other rank has freed the slot
+    __shared__ uint64_t b_full[8], b_empty[8];  // wide B: B's own ring
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
     volatile int* abort = &abort_flag;
@@ -396,10 +429,17 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     if (threadIdx.x == 0) {
         abort_flag = 0;
         const bool fwd = p.NC > 1 && it.rank == 0;
+        const bool b_ring = p.kcb < p.kc;
         for (int s = 0; s < W; ++s) {
-            mbar_init(&full[s], 2);              // A producer (or A arming) + B producer
-            mbar_init(&empty[s], fwd ? 2 : 1);   // MMA commit (+ the forwarder on rank 0)
+            mbar_init(&full[s], b_ring ? 1 : 2);  // A producer (or A arming) [+ B producer]
+            mbar_init(&empty[s], fwd ? 2 : 1);    // MMA commit (+ the forwarder on rank 0)
             if (fwd) mbar_init(&peer_empty[s], p.NC - 1);
+        }
+        if (b_ring) {
+            for (int s = 0; s < p.wb; ++s) {
+                mbar_init(&b_full[s], 1);
+                mbar_init(&b_empty[s], 1);
+            }
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
@@ -427,6 +467,8 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         if (lane == 0) {
             if (warp == 0 && p.NC > 1 && it.rank > 0) {
                 arm_forwarded_a(p, it, full, empty, peer_empty, abort);
+            } else if (warp == 6 && p.kcb < p.kc) {
+                produce_b_ring(p, it, &bmap, smem, b_full, b_empty, abort);
             } else {
                 produce(p, it, &bmap, smem, full, empty, abort, warp == 0, kUmmaB);
             }
@@ -438,7 +480,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         // one elected lane issues the MMAs and commits.
         const uint32_t idesc = idesc_bf16_f32(64, static_cast<uint32_t>(p.N_pad));
         const bool leader = elect_one();
-        long long i = 0;
+        long long i = 0, ib = 0;
         uint64_t* last_bar = nullptr;
         uint32_t last_par = 0;
         for (int ti = 0; ti < it.count; ++ti) {
@@ -464,28 +506,52 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
                 tc_fence_after();
                 const int kce = min(p.kc, p.K_pad - c * p.kc);
                 const uint32_t a_base = smem_u32(smem + static_cast<size_t>(s) * p.stage_bytes);
-                const uint32_t b_base = a_base + static_cast<uint32_t>(a_stage_bytes);
                 // A: no swizzle, K-major; 8x8 blocks of one k-group are 128 B apart along M,
                 // k-groups are 64 rows x 16 B = 1024 B apart along K (+2048 B per MMA).
                 // B: 128-byte swizzle, K-major; 8-row groups 1024 B apart, 64-column blocks
                 // N_pad x 128 B apart, +32 B per 16 columns inside a block.
-                const uint64_t ad0 = smem_desc(a_base, 1024u, 128u, 0u);
-                const uint64_t bd0 = smem_desc(b_base, 16u, 1024u, 2u);
-                if (leader) {
-                    for (int kb = 0; kb < kce; kb += 64) {
-                        const uint64_t bdb = bd0 + (static_cast<uint64_t>((kb >> 6) * bblk_bytes) >> 4);
-                        const uint64_t adb = ad0 + (static_cast<uint64_t>(kb >> 3) * 1024u >> 4);
-                        const int nk = min(4, (kce - kb) >> 4);
+                for (int sub = 0; sub * p.kcb < kce && ok; ++sub) {
+                    uint32_t b_base = a_base + static_cast<uint32_t>(a_stage_bytes);
+                    int sb = -1;
+                    if (p.kcb < p.kc) {  // wide B: this sub-chunk's B comes from B's own ring
+                        sb = static_cast<int>(ib % p.wb);
+                        if (!mbar_wait(&b_full[sb], static_cast<uint32_t>((ib / p.wb) & 1), abort, p.st,
+                                       DAK_ERR_TIMEOUT, W_MMA_FULL)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        b_base = smem_u32(smem + p.b_ring_off + static_cast<size_t>(sb) * p.b_slot_bytes);
+                    }
+                    const int k_sub = sub * p.kcb;
+                    const int kcs = min(p.kcb, kce - k_sub);
+                    const uint64_t ad0 = smem_desc(a_base + static_cast<uint32_t>((k_sub >> 3) * 1024), 1024u, 128u, 0u);
+                    const uint64_t bd0 = smem_desc(b_base, 16u, 1024u, 2u);
+                    if (leader) {
+                        for (int kb = 0; kb < kcs; kb += 64) {
+                            const uint64_t bdb = bd0 + (static_cast<uint64_t>((kb >> 6) * bblk_bytes) >> 4);
+                            const uint64_t adb = ad0 + (static_cast<uint64_t>(kb >> 3) * 1024u >> 4);
+                            const int nk = min(4, (kcs - kb) >> 4);
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            if (j < nk) {
-                                umma_bf16(d_tmem, adb + static_cast<uint64_t>(j * 128), bdb + static_cast<uint64_t>(j * 2),
-                                          idesc, (c > it.c_lo || kb > 0 || j > 0) ? 1u : 0u);
+                            for (int j = 0; j < 4; ++j) {
+                                if (j < nk) {
+                                    umma_bf16(d_tmem, adb + static_cast<uint64_t>(j * 128),
+                                              bdb + static_cast<uint64_t>(j * 2), idesc,
+                                              (c > it.c_lo || k_sub > 0 || kb > 0 || j > 0) ? 1u : 0u);
+                                }
                             }
                         }
+                        if (sb >= 0) umma_commit(&b_empty[sb]);
                     }
-                    umma_commit(&empty[s]);
+                    __syncwarp();
+                    if (sb >= 0) {
+                        ++ib;
+                        last_bar = &b_empty[sb];
+                        last_par = static_cast<uint32_t>(((ib - 1) / p.wb) & 1);
+                    }
                 }
+                if (!ok) break;
+                if (leader) umma_commit(&empty[s]);
                 __syncwarp();
                 last_bar = &empty[s];
                 last_par = static_cast<uint32_t>((i / W) & 1);
@@ -675,7 +741,7 @@ constexpr int kSmemBudget = 216 * 1024;           // one CTA per SM
 constexpr int kSmemBudgetTwoPerSm = 108 * 1024;  // two CTAs per SM
 constexpr int kDefaultHostCtas = 32;
 constexpr int kMaxBlockN = 256;          // hidden-state rows of one CTA's tile
-constexpr int kMaxWideN = 8 * kMaxBlockN;  // rows of one launch: a cluster of up to 8 CTAs shares A
+constexpr int kMaxWideN = 4 * kMaxBlockN;  // rows of one launch: a cluster of up to 4 CTAs shares A
 constexpr int kDefaultHostWindow = 4;
 
 // Launch with the optional cluster dimension and programmatic-dependent-launch attribute.
@@ -796,7 +862,15 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
         kc = p.N_pad <= 32 ? 512 : (p.N_pad <= 64 ? 256 : (p.N_pad <= 128 ? 128 : 64));
     }
     if (kc % 64 != 0 || kc > 1024 || (!umma && kc % 256 != 0)) return DAK_ERR_INVALID;
+    // shared tile rows (NC > 1): A in 256-column chunks, B through its own ring of 64-column
+    // chunks, so that A copies and forwards stay large while B fills the rest (with one CTA
+    // per tile row the unified ring measured faster: it keeps more B in flight)
+    const bool b_ring = umma && NC > 1;
+    if (b_ring && !(t && t->chunk_k > 0)) kc = 256;
+    if (b_ring && kc % 64) return DAK_ERR_INVALID;
+    const int kcb = b_ring ? 64 : kc;
     p.kc = kc;
+    p.kcb = kcb;
     const int nch = (p.K_pad + kc - 1) / kc;
     S = std::min(S, nch);
     if (S == 1) per_sm = 1;
@@ -805,14 +879,31 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
     p.S = S;
     const int CL = S > 1 ? S : NC;  // CTAs per cluster
     const int red_bytes = S > 1 ? red_of(S) : 0;
-    const int stage = stage_of(kc);
     const int ring_budget = per_sm == 2 ? kSmemBudgetTwoPerSm : kSmemBudget;
-    const int stages = std::min(8, (ring_budget - red_bytes - (umma ? 1024 : 0)) / stage);
-    if (stages < 1 || (stages < 2 && !(t && t->chunk_k > 0))) return DAK_ERR_INVALID;
+    int stage, stages, wb = 0, b_slot = 0;
+    if (b_ring) {
+        stage = (kc * 128 + 1023) & ~1023;
+        b_slot = (p.N_pad * kcb * 2 + 1023) & ~1023;
+        const int avail = ring_budget - red_bytes - 1024;
+        stages = std::min(4, std::max(2, avail / 2 / stage));  // about half for A
+        wb = std::min(8, (avail - stages * stage) / b_slot);
+        if (wb < 2) {
+            stages = 2;
+            wb = std::min(8, (avail - stages * stage) / b_slot);
+        }
+        if (wb < 2) return DAK_ERR_INVALID;
+    } else {
+        stage = stage_of(kc);
+        stages = std::min(8, (ring_budget - red_bytes - (umma ? 1024 : 0)) / stage);
+        if (stages < 1 || (stages < 2 && !(t && t->chunk_k > 0))) return DAK_ERR_INVALID;
+    }
     p.stages = stages;
     p.stage_bytes = stage;
-    p.red_off = stages * stage;
-    const int smem = stages * stage + red_bytes + (umma ? 1024 : 0);
+    p.wb = wb;
+    p.b_slot_bytes = b_slot;
+    p.b_ring_off = stages * stage;
+    p.red_off = stages * stage + wb * b_slot;
+    const int smem = stages * stage + wb * b_slot + red_bytes + (umma ? 1024 : 0);
 
     // schedule in cluster units
     dak_tuning tc{};
@@ -831,7 +922,7 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
 
     alignas(64) CUtensorMap bmap;
     int b3d = 0;
-    if (!make_b_map(&bmap, B, p.K, N, p.N_pad, kc, kind, &b3d)) return DAK_ERR_CUDA;
+    if (!make_b_map(&bmap, B, p.K, N, p.N_pad, kcb, kind, &b3d)) return DAK_ERR_CUDA;
     p.b3d = b3d;
 
     const bool pdl = t && t->pdl > 0;
@@ -853,15 +944,15 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
 }
 
 // Any N, in column blocks of hidden-state rows (B rows and C rows of a block are
-// contiguous), one launch each: blocks of 256 rows by default, every block reading the host
-// tiles again; with wide_b blocks of up to kMaxWideN rows in which a cluster shares each
-// tile row, so the host tiles cross the link once per block. On GB300, with M = 64 tiles,
-// the 256-row blocks measured faster: at N >= 512 B fills the ring and the forwarded A
-// chunks are only 8 KiB, so the forwarding round trip bounds each cluster's stream.
+// contiguous), one launch each: by default blocks of up to kMaxWideN rows in which a
+// cluster of ceil(rows / 256) CTAs shares each tile row, so the host tiles cross the link
+// once per block; with column_blocks, blocks of 256 rows that each read the host tiles
+// again. Clusters stop at 4 CTAs: forwarding every A chunk to 7 peers measured slower than
+// two launches of 1024 rows.
 dak_status launch_gemm(const dak_placement* A, const void* host_src, const void* B, void* C, int N, int c_fp32,
                        const dak_tuning* t, cudaStream_t stream) {
     if (!A || A->kind != 0) return DAK_ERR_INVALID;
-    const int block = (t && t->wide_b == 1) ? kMaxWideN : kMaxBlockN;
+    const int block = (t && t->column_blocks == 1) ? kMaxBlockN : kMaxWideN;
     if (N <= block) return launch_gemm_block(A, host_src, B, C, N, c_fp32, t, stream);
     if (!B || !C) return DAK_ERR_INVALID;
     const size_t b_row = static_cast<size_t>(A->K) * 2;

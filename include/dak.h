@@ -73,13 +73,14 @@ typedef struct dak_placement dak_placement;
  *   no_wave_align: 1 = ablation of the wave alignment of section 4.1 (factor 2, Fig. 12b):
  *               host CTAs = the cap and HBM CTAs = every remaining slot, without rounding
  *               either role to whole waves. 0 = aligned (default).
- *   wide_b    : dak_gemm with N > 256 only. 0 (default) = column blocks of 256 hidden-state
- *               rows, one launch each, every block reading the host tiles again (host-link
- *               bytes = host bytes x ceil(N/256)). 1 = launches of up to 2048 rows in which
- *               a cluster of ceil(N/256) CTAs shares each tile row: one CTA fetches every
- *               A chunk and forwards it to the others through distributed shared memory,
- *               so host bytes cross the link once per launch. Like chunk_k it may change
- *               the summation order of the last, partial block (never with the offload ratio).
+ *   column_blocks: dak_gemm with N > 256 only. 0 (default) = launches of up to 1024
+ *               hidden-state rows in which a cluster of ceil(rows / 256) CTAs shares each
+ *               tile row: one CTA fetches every A chunk and forwards it to the others through
+ *               distributed shared memory, so host bytes cross the link once per launch.
+ *               1 = column blocks of 256 rows, one launch each, every block reading the
+ *               host tiles again (host-link bytes = host bytes x ceil(N/256)). Like chunk_k
+ *               it may change the summation order of the last, partial block (never with
+ *               the offload ratio).
  */
 typedef struct {
     int host_ctas;
@@ -92,7 +93,7 @@ typedef struct {
     int pdl;
     int ctas_per_sm;
     int no_wave_align;
-    int wide_b;
+    int column_blocks;
 } dak_tuning;
 
 /* ---------------------------------------------------------------------------------- *
@@ -150,10 +151,10 @@ dak_status dak_placement_info(const dak_placement* p, int64_t* host_bytes, int64
  *   B : hidden states, bf16 [N][K] row-major (device), 16-byte aligned.
  *   C : output [N][M] row-major (device); bf16 if c_fp32 == 0, else fp32 ([N][M/2] of
  *       silu(gate) * up for a placement made by dak_place_matrix_glu).
- *   N : >= 1. Up to 256 rows run as one launch; a larger N runs as column blocks of 256
- *       rows, one launch each, every block reading the host tiles again (host-link bytes =
- *       host bytes x ceil(N / 256); no multicast, section 4.3.2, Table 1), or with
- *       tuning->wide_b = 1 as cluster launches that read each host byte once.
+ *   N : >= 1. Up to 256 rows run with one CTA per tile row; up to 1024 rows with a
+ *       cluster of ceil(N / 256) CTAs per tile row that reads each host byte once (section
+ *       4.3.2's read amplification without multicast); larger N in launches of 1024 rows
+ *       (tuning->column_blocks = 1: launches of 256 rows, each re-reading the host tiles).
  * One persistent launch: `host_ctas` CTAs stream the host tile rows and the other CTAs
  * the HBM tile rows; every CTA reads from exactly one tier and writes disjoint rows of
  * C. When the matrix has fewer tile rows than SMs, a cluster of CTAs shares each tile row,

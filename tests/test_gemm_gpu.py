@@ -215,17 +215,17 @@ def test_programmatic_launch_chain(dak):
         p.free()
 
 
-@pytest.mark.parametrize("wide", [0, 1])
-@pytest.mark.parametrize("N", [257, 300, 512, 777, 2048, 2100])
-def test_large_n(dak, N, wide):
-    """N > 256, as column blocks of 256 rows (wide = 0) or as cluster launches of up to 2048
-    rows in which rank 0 fetches every A chunk and forwards it to the other CTAs through
-    distributed shared memory (wide = 1); matches the oracle and stays identical across
-    offload ratios."""
+@pytest.mark.parametrize("cols", [0, 1])
+@pytest.mark.parametrize("N", [257, 300, 512, 777, 1024, 2100])
+def test_large_n(dak, N, cols):
+    """N > 256, as cluster launches of up to 1024 rows in which rank 0 fetches every A chunk
+    and forwards it to the other CTAs through distributed shared memory (default), or as
+    column blocks of 256 rows (column_blocks = 1); matches the oracle and stays identical
+    across offload ratios."""
     M, K = 320, 1280
     A, B = synth.gemm_inputs(M, K, N, seed=N + 1)
     ref = og.gemm_ref(A, B)
-    tun = dict(wide_b=wide)
+    tun = dict(column_blocks=cols)
     base = _run(dak, A, B, 0, tuning=tun)
     assert og.rel_err(to_np(base), ref) <= FP32_OUT_TOL
     for h in (2, 5):
@@ -237,21 +237,21 @@ def test_large_n(dak, N, wide):
 def test_large_n_integer_exact(dak):
     M, K, N = 192, 2048, 520
     A, B = synth.gemm_inputs(M, K, N, seed=9, integer=True)
-    for wide in (0, 1):
-        C = _run(dak, A, B, 1, tuning=dict(pdl=1, wide_b=wide))
-        assert np.array_equal(to_np(C), og.gemm_ref(A, B)), wide
+    for cols in (0, 1):
+        C = _run(dak, A, B, 1, tuning=dict(pdl=1, column_blocks=cols))
+        assert np.array_equal(to_np(C), og.gemm_ref(A, B)), cols
 
 
-@pytest.mark.parametrize("wide", [0, 1])
-def test_large_n_ragged_k_and_tuning(dak, wide):
+@pytest.mark.parametrize("cols", [0, 1])
+def test_large_n_ragged_k_and_tuning(dak, cols):
     """K not a multiple of 64 (2-D B boxes), tuning knobs that only move work."""
     M, K, N = 200, 520, 600
     A, B = synth.gemm_inputs(M, K, N, seed=77)
     ref = og.gemm_ref(A, B)
-    base = _run(dak, A, B, 1, tuning=dict(wide_b=wide))
+    base = _run(dak, A, B, 1, tuning=dict(column_blocks=cols))
     assert og.rel_err(to_np(base), ref) <= FP32_OUT_TOL
     for tun in (dict(host_ctas=1, window=2), dict(no_wave_align=1), dict(pdl=1)):
-        tun["wide_b"] = wide
+        tun["column_blocks"] = cols
         assert np.array_equal(bits_of(_run(dak, A, B, 2, tuning=tun)), bits_of(base)), tun
 
 

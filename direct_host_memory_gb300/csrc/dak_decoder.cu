@@ -500,7 +500,6 @@ extern "C" dak_status dak_decoder_create(const dak_decoder_config* cfg, const da
             if (p->device != dev) return DAK_ERR_INVALID;
     }
     if (c.n_layers == 0) B = 1;
-    if (B > 256) return DAK_ERR_UNSUPPORTED;  // the GEMMs take N <= 256 hidden-state rows
 
     dak_decoder* dd = new dak_decoder();
     dd->cfg = c;

@@ -145,6 +145,19 @@ def test_decoder_consecutive_steps(dak):
     dec.free()
 
 
+def test_decoder_many_requests(dak):
+    """300 requests per step: the projections run with more than 256 hidden-state rows
+    (clusters sharing each tile row) and the cache spans tiers."""
+    cfg, B, L = dict(SMALL64, n_layers=2), 300, 70
+    layers, caches, fnorm, x0 = _inputs(cfg, B, L, seed=17)
+    pos = np.array([(37 * b) % L for b in range(B)])
+    ref, _ = od.decode_step(_ocfg(cfg), x0, layers, caches, pos, fnorm)
+    dec = _build(dak, cfg, layers, caches, fnorm, _host_units(cfg, B, 0.3))
+    out = _run(dak, dec, x0, pos, graph=True)
+    assert og.rel_err(to_np(out), ref) <= REL_TOL
+    dec.free()
+
+
 def test_decoder_position_out_of_range_reported(dak):
     import torch
     cfg, B, L = SMALL64, 2, 64

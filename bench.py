@@ -179,35 +179,18 @@ def decode_ops(cfg, peak_flops):
 
 def decode_plan(dak, cfg, b_host, b_hbm, x_global, peak_flops):
     """Host units per operation type (tile rows or requests, the same in every layer) for an
-    HBM cap of (1 - x_global) of all bytes: the planner's greedy ratios (">=" budget), whose
-    tie-break gives every operation the same fraction of its segment, floored to whole
-    units and topped up one unit at a time where the model time grows least (to the
-    picosecond; ties go to the operation whose ratio stays lowest) until the budget is met.
-    x_global = 0: no offload."""
+    HBM cap of (1 - x_global) of all bytes, from the library's whole-unit planner
+    (dak_plan_units: the greedy ratios floored to whole units and topped up where the model
+    time grows least). x_global = 0: no offload."""
     ops, meta = decode_ops(cfg, peak_flops)
     nl = cfg["n_layers"]
     if x_global <= 0:
         return [{k: 0 for k, _ in meta} for _ in range(nl)], sum(o[0] for o in ops) / b_hbm
     total = sum(o[0] for o in ops)
-    D = x_global * total
-    ratios, _ = dak.dak_plan_ratios(ops, b_host, b_hbm, D, 0)
-    counts = [min(n, int(r * n + 1e-9)) for (k, n), r in zip(meta, ratios)]
-
-    def t_op(i, c):
-        C, tc, _ = ops[i]
-        b = C * c / meta[i][1]
-        return max(tc, (C - b) / b_hbm, b / b_host)
-
-    def host():
-        return sum(o[0] * c / m[1] for o, c, m in zip(ops, counts, meta))
-
-    while host() < D * (1 - 1e-12):
-        best = min((i for i in range(len(ops)) if counts[i] < meta[i][1]),
-                   key=lambda i: (round((t_op(i, counts[i] + 1) - t_op(i, counts[i])) * 1e12),
-                                  (counts[i] + 1) / meta[i][1]))
-        counts[best] += 1
-    tmodel = sum(t_op(i, c) for i, c in enumerate(counts))
-    return [{k: int(c) for (k, _), c in zip(meta, counts)} for _ in range(nl)], tmodel
+    # one unit of an operation type = that unit in every layer
+    units, tmodel = dak.dak_plan_units([(C, tc, tile * nl) for C, tc, tile in ops], b_host, b_hbm,
+                                       x_global * total)
+    return [{k: int(u) for (k, _), u in zip(meta, units)} for _ in range(nl)], tmodel
 
 
 def build_decoder(dak, cfg, units, seed=0, plain_launch=False):

@@ -29,7 +29,7 @@ EXPORTS = [
     "dak_gemm_staged", "dak_attn_staged", "dak_attn_noalloc", "dak_selftest_wait",
     "dak_decoder_create", "dak_decoder_batch", "dak_decoder_step", "dak_decoder_capture",
     "dak_decoder_replay", "dak_decoder_launches", "dak_decoder_free", "dak_tune_gemm", "dak_tune_attn",
-    "dak_place_matrix_glu",
+    "dak_place_matrix_glu", "dak_plan_units",
 ]
 
 # size of the fixed device array dak_attn_noalloc uses (DAK_NOALLOC_SCRATCH_BYTES in dak.h)
@@ -92,6 +92,7 @@ def _load():
         "dak_attn_staged": (i32, [vp, vp, vp, vp, i32, ctypes.c_float, vp, vp, sz, P(dak_tuning), vp]),
         "dak_attn_default_split": (i32, [vp]),
         "dak_plan_ratios": (i32, [P(dak_op), i32, dbl, dbl, dbl, i32, P(dbl), P(dbl)]),
+        "dak_plan_units": (i32, [P(dak_op), i32, dbl, dbl, dbl, P(i64), P(dbl)]),
         "dak_last_error": (i32, [vp, P(ctypes.c_uint64)]),
         "dak_sm_count": (i32, []),
         "dak_probe_read_bw": (i32, [i32, i64, i32, i32, i32, i32, i32, P(dbl), P(i32)]),
@@ -368,6 +369,19 @@ def dak_plan_ratios(ops, b_host: float, b_hbm: float, min_offload_bytes: float, 
     _check(lib.dak_plan_ratios(arr, len(ops), float(b_host), float(b_hbm), float(min_offload_bytes), int(mode),
                                ratios, ctypes.byref(t)), "dak_plan_ratios")
     return np.array(ratios[:len(ops)], dtype=np.float64), t.value
+
+
+def dak_plan_units(ops, b_host: float, b_hbm: float, min_offload_bytes: float):
+    """ops: iterable of (bytes, t_comp, unit_bytes). Returns (host units ndarray int64, model time s)."""
+    ops = list(ops)
+    arr = (dak_op * max(1, len(ops)))()
+    for i, o in enumerate(ops):
+        arr[i].bytes, arr[i].t_comp, arr[i].tile_bytes = float(o[0]), float(o[1]), float(o[2])
+    out = (ctypes.c_int64 * max(1, len(ops)))()
+    t = ctypes.c_double()
+    _check(lib.dak_plan_units(arr, len(ops), float(b_host), float(b_hbm), float(min_offload_bytes), out,
+                              ctypes.byref(t)), "dak_plan_units")
+    return np.array(out[:len(ops)], dtype=np.int64), t.value
 
 
 # ------------------------------------------------------------------------------- errors / probes

@@ -150,3 +150,61 @@ extern "C" dak_status dak_plan_ratios(const dak_op* ops, int n, double b_host, d
     return plan_continuous(ops, n, b_host, b_hbm, std::min(min_offload_bytes, total), mode == 1, ratios_out,
                            model_time_out);
 }
+
+// Whole-unit placement for any number of operations: the greedy ratios floored to whole
+// units, then one unit at a time added where the model time grows least (to the
+// picosecond; ties go to the operation whose ratio stays lowest) until the budget is met.
+extern "C" dak_status dak_plan_units(const dak_op* ops, int n, double b_host, double b_hbm, double min_offload_bytes,
+                                     int64_t* host_units_out, double* model_time_out) {
+    if (n < 0 || (n > 0 && (!ops || !host_units_out)) || !(b_host > 0) || !(b_hbm > 0)) return DAK_ERR_INVALID;
+    if (!(min_offload_bytes >= 0) || std::isinf(min_offload_bytes)) return DAK_ERR_INVALID;
+    double total = 0;
+    std::vector<int64_t> units(n), cnt(n);
+    for (int i = 0; i < n; ++i) {
+        if (!(ops[i].bytes >= 0) || !(ops[i].t_comp >= 0) || std::isinf(ops[i].bytes) || !(ops[i].tile_bytes > 0))
+            return DAK_ERR_INVALID;
+        total += ops[i].bytes;
+        units[i] = static_cast<int64_t>(std::ceil(ops[i].bytes / ops[i].tile_bytes - 1e-9));
+    }
+    if (min_offload_bytes > total * (1 + 1e-12)) return DAK_ERR_INVALID;
+    if (n == 0) {
+        if (model_time_out) *model_time_out = 0;
+        return DAK_OK;
+    }
+    std::vector<double> ratios(n);
+    dak_status st = plan_continuous(ops, n, b_host, b_hbm, std::min(min_offload_bytes, total), false, ratios.data(), nullptr);
+    if (st != DAK_OK) return st;
+    auto bytes_of = [&](int i, int64_t k) { return std::min(ops[i].bytes, static_cast<double>(k) * ops[i].tile_bytes); };
+    auto t_of = [&](int i, int64_t k) { return op_time(ops[i].bytes, ops[i].t_comp, bytes_of(i, k), b_host, b_hbm); };
+    double host = 0;
+    for (int i = 0; i < n; ++i) {
+        cnt[i] = std::min(units[i], static_cast<int64_t>(std::floor(ratios[i] * ops[i].bytes / ops[i].tile_bytes + 1e-9)));
+        host += bytes_of(i, cnt[i]);
+    }
+    const double D = std::min(min_offload_bytes, total);
+    while (host < D * (1 - 1e-12)) {
+        int best = -1;
+        long long best_dt = 0;
+        double best_r = 0;
+        for (int i = 0; i < n; ++i) {
+            if (cnt[i] >= units[i]) continue;
+            const long long dt = std::llround((t_of(i, cnt[i] + 1) - t_of(i, cnt[i])) * 1e12);
+            const double r = static_cast<double>(cnt[i] + 1) / static_cast<double>(units[i]);
+            if (best < 0 || dt < best_dt || (dt == best_dt && r < best_r)) {
+                best = i;
+                best_dt = dt;
+                best_r = r;
+            }
+        }
+        if (best < 0) break;
+        host += bytes_of(best, cnt[best] + 1) - bytes_of(best, cnt[best]);
+        ++cnt[best];
+    }
+    double t = 0;
+    for (int i = 0; i < n; ++i) {
+        host_units_out[i] = cnt[i];
+        t += t_of(i, cnt[i]);
+    }
+    if (model_time_out) *model_time_out = t;
+    return DAK_OK;
+}

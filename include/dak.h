@@ -363,6 +363,15 @@ typedef struct {
 dak_status dak_plan_ratios(const dak_op* ops, int n, double b_host, double b_hbm, double min_offload_bytes,
                            int mode, double* ratios_out, double* model_time_out);
 
+/* Whole-unit placement for any number of operations (where the exact tile DP of mode 2 is
+ * too large): ops[i].tile_bytes is operation i's placement unit (a 64-row tile row, one
+ * request's KV; > 0), and it has ceil(bytes / tile_bytes) of them. The ratios of mode 0 are
+ * floored to whole units; then units are added one at a time where the model time grows
+ * least (ties: the operation whose ratio stays lowest) until sum_i placed bytes >=
+ * min_offload_bytes. Outputs host_units_out[n] and the model time (may be NULL). */
+dak_status dak_plan_units(const dak_op* ops, int n, double b_host, double b_hbm, double min_offload_bytes,
+                          int64_t* host_units_out, double* model_time_out);
+
 /* ---------------------------------------------------------------------------------- *
  * Errors, device info, measurement helpers
  * ---------------------------------------------------------------------------------- */

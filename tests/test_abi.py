@@ -111,3 +111,45 @@ def test_planner_single_op_turning_points(dak):
     xt = op.turning_point_compute_bound(C, tc, bh)
     r, t = dak.dak_plan_ratios([(C, tc)], bh, bg, 0.5 * xt * C, mode=1)
     assert t == pytest.approx(tc) and r[0] == pytest.approx(0.5 * xt)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_plan_units_near_exhaustive_optimum(dak, seed):
+    """Whole-unit placement: meets the budget, never beats the exhaustive whole-tile optimum
+    and stays within one unit's host time per operation of it."""
+    bh, bg = 0.35e12, 6.7e12
+    ops = [(C, tc, t) for C, tc, t in _ops(200 + seed, 3, tiles=True)]
+    total = sum(o[0] for o in ops)
+    D = synth.uniform_f64(seed, 8, 1)[0] * 0.6 * total
+    units, t = dak.dak_plan_units(ops, bh, bg, D)
+    b = [min(o[0], u * o[2]) for u, o in zip(units, ops)]
+    assert sum(b) >= D * (1 - 1e-12)
+    assert op.objective([(C, tc) for C, tc, _ in ops], b, bh, bg) == pytest.approx(t, rel=1e-12)
+    ref, _ = op.exhaustive_tiles([(C, tc) for C, tc, _ in ops], [o[2] for o in ops], bh, bg, D)
+    assert t >= ref * (1 - 1e-12)
+    assert t <= ref + sum(o[2] for o in ops) / bh
+
+
+def test_plan_units_memory_bound_ops_stay_uniform(dak):
+    """All operations memory-bound and host-bound at the budget (one decode layer's shapes):
+    the model time is the host bytes over B_host, the budget is overshot by less than the
+    smallest unit, and operations with the same unit size end at the same ratio to within
+    one unit (the top-up goes to the cheapest units, lowest ratio first)."""
+    bh, bg = 211e9, 7.3e12
+    M = 1 << 20
+    ops = [(48 * M, 0.0, M // 2), (32 * M, 0.0, M // 2), (224 * M, 0.0, M // 2), (112 * M, 0.0, 7 * M // 4),
+           (256 * M, 0.0, 16 * M)]
+    total = sum(o[0] for o in ops)
+    units, t = dak.dak_plan_units(ops, bh, bg, 0.3 * total)
+    host = sum(min(o[0], u * o[2]) for u, o in zip(units, ops))
+    assert 0.3 * total <= host < 0.3 * total + M // 2
+    assert t == pytest.approx(host / bh, rel=1e-12)
+    small = [u / -(-o[0] // o[2]) for u, o in zip(units, ops) if o[2] == M // 2]
+    assert max(small) - min(small) <= 1.0 / 64 + 1e-12
+
+
+def test_plan_units_rejects_bad_arguments(dak):
+    with pytest.raises(dak.DakError):
+        dak.dak_plan_units([(1e9, 0.0, 0.0)], 1e11, 1e12, 0.0)  # no unit size
+    with pytest.raises(dak.DakError):
+        dak.dak_plan_units([(1e9, 0.0, 1e6)], 1e11, 1e12, 2e9)  # budget above the bytes

@@ -25,6 +25,16 @@
 
 namespace dak {
 
+// Chunking of a CTA's ring. kcb == kc: each ring stage holds its A chunk (kc columns) and the
+// matching B chunk. kcb < kc: the A ring holds kc-wide chunks only and B streams through its
+// own ring of wb slots of kcb columns, kc / kcb of them per A chunk. Chunking never changes
+// the sequence of K = 16 MMA steps, so it never changes a result.
+struct Chunks {
+    int kc, kcb;
+    int stages, stage_bytes;       // A ring (stage = A chunk [+ B chunk when kcb == kc])
+    int wb, b_ring_off, b_slot_bytes;
+};
+
 struct GemmParams {
     const uint8_t* a_host;  // tile rows 0 .. h-1 (device-visible address of the host mapping)
     const uint8_t* a_hbm;   // tile rows h .. T-1
@@ -32,9 +42,6 @@ struct GemmParams {
     void* C;                // [N][M]
     int M, K, K_pad, N, N_pad, T, h;
     int n_host_ctas, n_hbm_ctas, host_window, hbm_window;  // host/HBM counts are in clusters of S CTAs
-    int kc;           // chunk width along K (multiple of 64)
-    int stages;       // ring slots in shared memory
-    int stage_bytes;  // bytes per slot
     int c_fp32;
     long long tile_bytes;
     DevStatus* st;
@@ -43,10 +50,9 @@ struct GemmParams {
     int red_off;  // byte offset (from the aligned ring base) of the partial-sum area, S > 1
     int NC;       // CTAs per cluster sharing each tile row across 256-row blocks of B (1 = off)
     int glu;      // rows interleaved gate/up: C[n][row/2] = silu(gate) * up, C is [N][M/2]
-    // B chunk width. kcb == kc: each ring stage holds its A chunk and the matching B chunk.
-    // kcb < kc (wide B, N_pad > 128): the A ring holds kc-wide chunks only and B streams
-    // through its own ring of wb slots of kcb columns, kc / kcb of them per A chunk.
-    int kcb, wb, b_ring_off, b_slot_bytes;
+    // Ring layout per role: ch[0] for CTAs reading HBM tiles, ch[1] for CTAs reading host
+    // tiles (they differ only for wide B, where host tiles stream A in larger chunks)
+    Chunks ch[2];
 };
 
 // SwiGLU of one gate / up pair (the same expression as the decoder's standalone kernel)
@@ -55,6 +61,7 @@ __device__ __forceinline__ float swiglu_pair(float g, float u) { return g / (1.f
 // Tiles of this CTA: role, first tile, stride, count, and the chunk range [c_lo, c_hi) of
 // every tile row that this CTA (rank `rank` of its cluster) accumulates.
 struct TileIter {
+    Chunks c;  // this CTA's ring layout
     bool host;
     int first, stride, count;
     const uint8_t* base;
@@ -66,7 +73,8 @@ __device__ __forceinline__ TileIter tiles_of_cta(const GemmParams& p) {
     TileIter it;
     const int cl = p.S > 1 ? p.S : p.NC;  // CTAs per cluster
     const int b = blockIdx.x / cl;        // cluster index
-    const int nch = (p.K_pad + p.kc - 1) / p.kc;
+    it.c = p.ch[b < p.n_host_ctas ? 1 : 0];
+    const int nch = (p.K_pad + it.c.kc - 1) / it.c.kc;
     it.rank = cl > 1 ? static_cast<int>(cluster_ctarank()) : 0;
     it.c_lo = p.S > 1 ? it.rank * nch / p.S : 0;
     it.c_hi = p.S > 1 ? (it.rank + 1) * nch / p.S : nch;
@@ -127,10 +135,10 @@ __device__ __forceinline__ void drain_fills(uint64_t* full, int window, long lon
 enum BKind { kCoreB = 0, kUmmaB = 1 };
 
 __device__ __forceinline__ void issue_b(const GemmParams& p, const CUtensorMap* bmap, uint8_t* dst, int k0,
-                                        uint64_t* bar, int kind, int row0) {
+                                        uint64_t* bar, int kind, int row0, int kcb) {
     const int blk = kind == kUmmaB ? 64 : 256;
     const int rows = kind == kUmmaB ? p.N_pad : p.N;
-    const int nblk = p.kcb / blk;
+    const int nblk = kcb / blk;
     if (p.b3d) {
         tma_load_3d(dst, bmap, 0, row0, k0 / blk, bar);
     } else {
@@ -138,8 +146,8 @@ __device__ __forceinline__ void issue_b(const GemmParams& p, const CUtensorMap* 
     }
 }
 
-__device__ __forceinline__ uint32_t b_stage_bytes(const GemmParams& p, int kind) {
-    return static_cast<uint32_t>(p.kcb) * 2u * static_cast<uint32_t>(kind == kUmmaB ? p.N_pad : p.N);
+__device__ __forceinline__ uint32_t b_stage_bytes(const GemmParams& p, int kind, int kcb) {
+    return static_cast<uint32_t>(kcb) * 2u * static_cast<uint32_t>(kind == kUmmaB ? p.N_pad : p.N);
 }
 
 // Producer loops. `is_a` streams the tile rows of A (one bulk copy per stage), otherwise the
@@ -161,15 +169,15 @@ __device__ __forceinline__ void produce(const GemmParams& p, const TileIter& it,
                                      DAK_ERR_TIMEOUT, is_a ? W_PROD_EMPTY : W_BPROD_EMPTY)) {
                 goto done;
             }
-            const int k0 = c * p.kc;
-            uint8_t* dst = smem + static_cast<size_t>(s) * p.stage_bytes;
+            const int k0 = c * it.c.kc;
+            uint8_t* dst = smem + static_cast<size_t>(s) * it.c.stage_bytes;
             if (is_a) {
-                const uint32_t a_bytes = static_cast<uint32_t>(min(p.kc, p.K_pad - k0)) * 128u;
+                const uint32_t a_bytes = static_cast<uint32_t>(min(it.c.kc, p.K_pad - k0)) * 128u;
                 mbar_arrive_expect_tx(&full[s], a_bytes);
                 bulk_g2s(dst, src + static_cast<long long>(k0) * 128, a_bytes, &full[s], pol_a);
             } else {
-                mbar_arrive_expect_tx(&full[s], b_stage_bytes(p, kind));
-                issue_b(p, bmap, dst + p.kc * 128, k0, &full[s], kind, p.NC > 1 ? it.rank * p.N_pad : 0);
+                mbar_arrive_expect_tx(&full[s], b_stage_bytes(p, kind, it.c.kcb));
+                issue_b(p, bmap, dst + it.c.kc * 128, k0, &full[s], kind, p.NC > 1 ? it.rank * p.N_pad : 0, it.c.kcb);
             }
         }
     }
@@ -183,21 +191,21 @@ __device__ __forceinline__ void produce_b_ring(const GemmParams& p, const TileIt
                                                uint8_t* smem, uint64_t* b_full, uint64_t* b_empty,
                                                volatile int* abort) {
     grid_dep_wait();  // the hidden states may come from the previous kernel of the stream
-    const int WB = p.wb;
+    const int WB = it.c.wb;
     const int row0 = p.NC > 1 ? it.rank * p.N_pad : 0;
     long long ib = 0;
     for (int ti = 0; ti < it.count && !*abort; ++ti) {
         for (int c = it.c_lo; c < it.c_hi; ++c) {
-            const int kce = min(p.kc, p.K_pad - c * p.kc);
-            for (int sub = 0; sub * p.kcb < kce; ++sub, ++ib) {
+            const int kce = min(it.c.kc, p.K_pad - c * it.c.kc);
+            for (int sub = 0; sub * it.c.kcb < kce; ++sub, ++ib) {
                 const int sb = static_cast<int>(ib % WB);
                 if (ib >= WB && !mbar_wait(&b_empty[sb], static_cast<uint32_t>(((ib / WB) - 1) & 1), abort, p.st,
                                            DAK_ERR_TIMEOUT, W_BPROD_EMPTY)) {
                     goto done;
                 }
-                mbar_arrive_expect_tx(&b_full[sb], b_stage_bytes(p, kUmmaB));
-                issue_b(p, bmap, smem + p.b_ring_off + static_cast<size_t>(sb) * p.b_slot_bytes, c * p.kc + sub * p.kcb,
-                        &b_full[sb], kUmmaB, row0);
+                mbar_arrive_expect_tx(&b_full[sb], b_stage_bytes(p, kUmmaB, it.c.kcb));
+                issue_b(p, bmap, smem + it.c.b_ring_off + static_cast<size_t>(sb) * it.c.b_slot_bytes,
+                        c * it.c.kc + sub * it.c.kcb, &b_full[sb], kUmmaB, row0, it.c.kcb);
             }
         }
     }
@@ -229,9 +237,9 @@ __device__ __forceinline__ void forward_a(const GemmParams& p, const TileIter& i
                                        DAK_ERR_TIMEOUT, W_FWD_PEER);
             if (!__all_sync(0xffffffffu, ok)) goto done;
             if (r < p.NC) {
-                const int k0 = c * p.kc;
-                const uint32_t a_bytes = static_cast<uint32_t>(min(p.kc, p.K_pad - k0)) * 128u;
-                uint8_t* slot = smem + static_cast<size_t>(s) * p.stage_bytes;
+                const int k0 = c * it.c.kc;
+                const uint32_t a_bytes = static_cast<uint32_t>(min(it.c.kc, p.K_pad - k0)) * 128u;
+                uint8_t* slot = smem + static_cast<size_t>(s) * it.c.stage_bytes;
                 bulk_s2s_cluster(mapa_shared(smem_u32(slot), static_cast<uint32_t>(r)), slot, a_bytes,
                                  mapa_shared(smem_u32(&full[s]), static_cast<uint32_t>(r)));
                 bulk_commit_group();
@@ -259,8 +267,8 @@ __device__ __forceinline__ void arm_forwarded_a(const GemmParams& p, const TileI
                     goto done;
                 mbar_arrive_remote(mapa_shared(smem_u32(&peer_empty[s]), 0));
             }
-            const int k0 = c * p.kc;
-            mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(min(p.kc, p.K_pad - k0)) * 128u);
+            const int k0 = c * it.c.kc;
+            mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(min(it.c.kc, p.K_pad - k0)) * 128u);
         }
     }
 done:
@@ -285,7 +293,6 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const TileIter it = tiles_of_cta(p);
     const int W = it.window;
-    const int nch = (p.K_pad + p.kc - 1) / p.kc;
     uint8_t* smem = smem_raw;
 
     if (threadIdx.x == 0) {
@@ -321,10 +328,10 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
             if (!mbar_wait(&full[s], static_cast<uint32_t>((i / W) & 1), abort, p.st, DAK_ERR_TIMEOUT, W_CONS_FULL)) {
                 return;
             }
-            const int k0 = c * p.kc;
-            const int kgr = min(min(p.kc, p.K_pad - k0), p.K - k0) >> 3;  // real k-groups in this chunk
-            const uint8_t* st = smem + static_cast<size_t>(s) * p.stage_bytes;
-            const uint8_t* bst = st + p.kc * 128;
+            const int k0 = c * it.c.kc;
+            const int kgr = min(min(it.c.kc, p.K_pad - k0), p.K - k0) >> 3;  // real k-groups in this chunk
+            const uint8_t* st = smem + static_cast<size_t>(s) * it.c.stage_bytes;
+            const uint8_t* bst = st + it.c.kc * 128;
             for (int kg = kq; kg < kgr; kg += 4) {
                 const uint4 a = *reinterpret_cast<const uint4*>(st + kg * 1024 + w * 128 + r * 16);
                 const float a0 = bf_lo(a.x), a1 = bf_hi(a.x), a2 = bf_lo(a.y), a3 = bf_hi(a.y);
@@ -416,11 +423,10 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const TileIter it = tiles_of_cta(p);
     const int W = it.window;
-    const int nch = (p.K_pad + p.kc - 1) / p.kc;
     // 1024-byte aligned ring (128-byte swizzle atoms must start on 1024-byte boundaries)
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-    const int a_stage_bytes = p.kc * 128;
+    const int a_stage_bytes = it.c.kc * 128;
     const int bblk_bytes = p.N_pad * 128;  // one 64-column block of B
     uint32_t tmem_cols = 32;
     while (tmem_cols < static_cast<uint32_t>(2 * p.N_pad)) tmem_cols <<= 1;
@@ -429,14 +435,14 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     if (threadIdx.x == 0) {
         abort_flag = 0;
         const bool fwd = p.NC > 1 && it.rank == 0;
-        const bool b_ring = p.kcb < p.kc;
+        const bool b_ring = it.c.kcb < it.c.kc;
         for (int s = 0; s < W; ++s) {
             mbar_init(&full[s], b_ring ? 1 : 2);  // A producer (or A arming) [+ B producer]
             mbar_init(&empty[s], fwd ? 2 : 1);    // MMA commit (+ the forwarder on rank 0)
             if (fwd) mbar_init(&peer_empty[s], p.NC - 1);
         }
         if (b_ring) {
-            for (int s = 0; s < p.wb; ++s) {
+            for (int s = 0; s < it.c.wb; ++s) {
                 mbar_init(&b_full[s], 1);
                 mbar_init(&b_empty[s], 1);
             }
@@ -467,7 +473,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         if (lane == 0) {
             if (warp == 0 && p.NC > 1 && it.rank > 0) {
                 arm_forwarded_a(p, it, full, empty, peer_empty, abort);
-            } else if (warp == 6 && p.kcb < p.kc) {
+            } else if (warp == 6 && it.c.kcb < it.c.kc) {
                 produce_b_ring(p, it, &bmap, smem, b_full, b_empty, abort);
             } else {
                 produce(p, it, &bmap, smem, full, empty, abort, warp == 0, kUmmaB);
@@ -504,27 +510,27 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const int kce = min(p.kc, p.K_pad - c * p.kc);
-                const uint32_t a_base = smem_u32(smem + static_cast<size_t>(s) * p.stage_bytes);
+                const int kce = min(it.c.kc, p.K_pad - c * it.c.kc);
+                const uint32_t a_base = smem_u32(smem + static_cast<size_t>(s) * it.c.stage_bytes);
                 // A: no swizzle, K-major; 8x8 blocks of one k-group are 128 B apart along M,
                 // k-groups are 64 rows x 16 B = 1024 B apart along K (+2048 B per MMA).
                 // B: 128-byte swizzle, K-major; 8-row groups 1024 B apart, 64-column blocks
                 // N_pad x 128 B apart, +32 B per 16 columns inside a block.
-                for (int sub = 0; sub * p.kcb < kce && ok; ++sub) {
+                for (int sub = 0; sub * it.c.kcb < kce && ok; ++sub) {
                     uint32_t b_base = a_base + static_cast<uint32_t>(a_stage_bytes);
                     int sb = -1;
-                    if (p.kcb < p.kc) {  // wide B: this sub-chunk's B comes from B's own ring
-                        sb = static_cast<int>(ib % p.wb);
-                        if (!mbar_wait(&b_full[sb], static_cast<uint32_t>((ib / p.wb) & 1), abort, p.st,
+                    if (it.c.kcb < it.c.kc) {  // wide B: this sub-chunk's B comes from B's own ring
+                        sb = static_cast<int>(ib % it.c.wb);
+                        if (!mbar_wait(&b_full[sb], static_cast<uint32_t>((ib / it.c.wb) & 1), abort, p.st,
                                        DAK_ERR_TIMEOUT, W_MMA_FULL)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        b_base = smem_u32(smem + p.b_ring_off + static_cast<size_t>(sb) * p.b_slot_bytes);
+                        b_base = smem_u32(smem + it.c.b_ring_off + static_cast<size_t>(sb) * it.c.b_slot_bytes);
                     }
-                    const int k_sub = sub * p.kcb;
-                    const int kcs = min(p.kcb, kce - k_sub);
+                    const int k_sub = sub * it.c.kcb;
+                    const int kcs = min(it.c.kcb, kce - k_sub);
                     const uint64_t ad0 = smem_desc(a_base + static_cast<uint32_t>((k_sub >> 3) * 1024), 1024u, 128u, 0u);
                     const uint64_t bd0 = smem_desc(b_base, 16u, 1024u, 2u);
                     if (leader) {
@@ -547,7 +553,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
                     if (sb >= 0) {
                         ++ib;
                         last_bar = &b_empty[sb];
-                        last_par = static_cast<uint32_t>(((ib - 1) / p.wb) & 1);
+                        last_par = static_cast<uint32_t>(((ib - 1) / it.c.wb) & 1);
                     }
                 }
                 if (!ok) break;
@@ -862,15 +868,14 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
         kc = p.N_pad <= 32 ? 512 : (p.N_pad <= 64 ? 256 : (p.N_pad <= 128 ? 128 : 64));
     }
     if (kc % 64 != 0 || kc > 1024 || (!umma && kc % 256 != 0)) return DAK_ERR_INVALID;
-    // shared tile rows (NC > 1): A in 256-column chunks, B through its own ring of 64-column
-    // chunks, so that A copies and forwards stay large while B fills the rest (with one CTA
-    // per tile row the unified ring measured faster: it keeps more B in flight)
-    const bool b_ring = umma && NC > 1;
-    if (b_ring && !(t && t->chunk_k > 0)) kc = 256;
-    if (b_ring && kc % 64) return DAK_ERR_INVALID;
-    const int kcb = b_ring ? 64 : kc;
-    p.kc = kc;
-    p.kcb = kcb;
+    // Ring layouts. Shared tile rows (NC > 1): A in 256-column chunks and B through its own
+    // ring of 64-column chunks, so that A copies and forwards stay large while B fills the
+    // rest. One CTA per tile row with wide B (N_pad > 128): CTAs reading HBM keep the unified
+    // ring, which keeps more B in flight; CTAs reading host tiles take the split layout, whose
+    // 32 KiB A chunks keep more host bytes in flight (host reads are latency-bound).
+    const bool b_ring_all = umma && NC > 1;
+    const bool b_ring_host = umma && p.N_pad > 128 && !(t && t->chunk_k > 0);
+    if (b_ring_all && !(t && t->chunk_k > 0)) kc = 256;
     const int nch = (p.K_pad + kc - 1) / kc;
     S = std::min(S, nch);
     if (S == 1) per_sm = 1;
@@ -880,30 +885,42 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
     const int CL = S > 1 ? S : NC;  // CTAs per cluster
     const int red_bytes = S > 1 ? red_of(S) : 0;
     const int ring_budget = per_sm == 2 ? kSmemBudgetTwoPerSm : kSmemBudget;
-    int stage, stages, wb = 0, b_slot = 0;
-    if (b_ring) {
-        stage = (kc * 128 + 1023) & ~1023;
-        b_slot = (p.N_pad * kcb * 2 + 1023) & ~1023;
-        const int avail = ring_budget - red_bytes - 1024;
-        stages = std::min(4, std::max(2, avail / 2 / stage));  // about half for A
-        wb = std::min(8, (avail - stages * stage) / b_slot);
-        if (wb < 2) {
-            stages = 2;
-            wb = std::min(8, (avail - stages * stage) / b_slot);
+    auto layout = [&](int kc_, bool split, Chunks* L) -> bool {
+        L->kc = kc_;
+        L->kcb = split ? 64 : kc_;
+        if (split) {
+            L->stage_bytes = (kc_ * 128 + 1023) & ~1023;
+            L->b_slot_bytes = (p.N_pad * L->kcb * 2 + 1023) & ~1023;
+            const int avail = ring_budget - red_bytes - 1024;
+            L->stages = std::min(4, std::max(2, avail / 2 / L->stage_bytes));  // about half for A
+            L->wb = std::min(8, (avail - L->stages * L->stage_bytes) / L->b_slot_bytes);
+            if (L->wb < 2) {
+                L->stages = 2;
+                L->wb = std::min(8, (avail - L->stages * L->stage_bytes) / L->b_slot_bytes);
+            }
+            if (L->wb < 2) return false;
+        } else {
+            L->stage_bytes = stage_of(kc_);
+            L->stages = std::min(8, (ring_budget - red_bytes - (umma ? 1024 : 0)) / L->stage_bytes);
+            L->wb = 0;
+            L->b_slot_bytes = 0;
+            if (L->stages < 1 || (L->stages < 2 && !(t && t->chunk_k > 0))) return false;
         }
-        if (wb < 2) return DAK_ERR_INVALID;
-    } else {
-        stage = stage_of(kc);
-        stages = std::min(8, (ring_budget - red_bytes - (umma ? 1024 : 0)) / stage);
-        if (stages < 1 || (stages < 2 && !(t && t->chunk_k > 0))) return DAK_ERR_INVALID;
+        L->b_ring_off = L->stages * L->stage_bytes;
+        return true;
+    };
+    if (!layout(kc, b_ring_all, &p.ch[0])) return DAK_ERR_INVALID;
+    p.ch[1] = p.ch[0];
+    if (!b_ring_all && b_ring_host && S == 1 && p.h > 0) {
+        if (!layout(256, true, &p.ch[1])) p.ch[1] = p.ch[0];
     }
-    p.stages = stages;
-    p.stage_bytes = stage;
-    p.wb = wb;
-    p.b_slot_bytes = b_slot;
-    p.b_ring_off = stages * stage;
-    p.red_off = stages * stage + wb * b_slot;
-    const int smem = stages * stage + wb * b_slot + red_bytes + (umma ? 1024 : 0);
+    if (p.ch[0].kcb != p.ch[1].kcb) return DAK_ERR_INVALID;  // one B tensor map serves both
+    const int kcb = p.ch[0].kcb;
+    auto ring_bytes = [](const Chunks& L) { return L.stages * L.stage_bytes + L.wb * L.b_slot_bytes; };
+    const int rings = std::max(ring_bytes(p.ch[0]), ring_bytes(p.ch[1]));
+    p.red_off = rings;
+    const int smem = rings + red_bytes + (umma ? 1024 : 0);
+    const int max_stages = std::max(p.ch[0].stages, p.ch[1].stages);
 
     // schedule in cluster units
     dak_tuning tc{};
@@ -911,11 +928,11 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
     tc.host_ctas = std::max(1, (tc.host_ctas > 0 ? tc.host_ctas : kDefaultHostCtas) / CL);
     if (tc.hbm_ctas > 0) tc.hbm_ctas = std::max(1, tc.hbm_ctas / CL);
     Sched sc = schedule(p.h, p.T - p.h, std::max(1, (sms * per_sm) / CL), &tc, std::max(1, kDefaultHostCtas / CL),
-                        std::min(kDefaultHostWindow, stages), stages, stages);
+                        std::min(kDefaultHostWindow, p.ch[1].stages), p.ch[0].stages, max_stages);
     p.n_host_ctas = sc.n_host_ctas;
     p.n_hbm_ctas = sc.n_hbm_ctas;
-    p.host_window = sc.host_window;
-    p.hbm_window = sc.hbm_window;
+    p.host_window = std::min(sc.host_window, p.ch[1].stages);
+    p.hbm_window = std::min(sc.hbm_window, p.ch[0].stages);
     const int grid = (p.n_host_ctas + p.n_hbm_ctas) * CL;
     if (grid == 0) return DAK_OK;
     if (p.h > 0 && !p.a_host) return DAK_ERR_INVALID;

@@ -79,7 +79,7 @@ def test_integer_inputs_bit_exact(dak, N):
     assert np.array_equal(bits_of(C16), obf.round_f64_to_bf16(ref))
 
 
-@pytest.mark.parametrize("N", [1, 4, 16, 64])
+@pytest.mark.parametrize("N", [1, 4, 16, 64, 200, 256])
 def test_bit_identical_across_offload_ratio(dak, N):
     M, K = 640, 2048
     A, B = synth.gemm_inputs(M, K, N, seed=3)

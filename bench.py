@@ -660,6 +660,55 @@ def cpu_oracle_sample(lin, attn, frac_rows=1 / 32):
                               f"linear and {nreq} of {q.shape[0]} attention requests ({nbytes / 1e6:.0f} MB)", dt
 
 
+def cpu_oracle_sample_sliced(batch=32, frac=32):
+    """cpu_oracle_sample on the same sampled tile rows and requests, drawing only those
+    slices of the inputs (the generator is counter-based, so any slice regenerates alone)."""
+    import numpy as np
+    import synth
+    from oracle import attention as oa
+    from oracle import gemm as og
+    parts = []
+    for i, (name, (M, K)) in enumerate(synth.LINEARS_8B.items()):
+        s = 0 + i
+        rows = [synth.normal_bf16(s, 1, 64 * K, 0.0, synth.WEIGHT_STD, offset=t * 64 * K).reshape(64, K)
+                for t in range(0, M // 64, frac)]
+        B = synth.normal_bf16(s, 2, batch * K).reshape(batch, K)
+        parts.append((np.concatenate(rows), B))
+    c = synth.ATTN_DECODE
+    nreq = max(1, c["batch"] // frac)
+    ti = len(synth.LINEARS_8B)
+    q = synth.normal_bf16(ti, 11, nreq * c["h_q"] * c["head_dim"]).reshape(nreq, c["h_q"], c["head_dim"])
+    kv = [synth.attn_kv_request(b, c["h_kv"], c["head_dim"], c["context"], seed=0, tensor_index=ti)
+          for b in range(nreq)]
+    k = np.stack([a for a, _ in kv])
+    v = np.stack([b for _, b in kv])
+    t0 = time.perf_counter()
+    nbytes = 0
+    for A, B in parts:
+        og.gemm_ref(A, B)
+        nbytes += A.size * 2
+    oa.decode_attention_ref(q, k, v)
+    nbytes += 2 * k.size * 2
+    dt = time.perf_counter() - t0
+    return nbytes / dt / 1e9, dt
+
+
+def cpu_oracle_one_core(timeout_s=300):
+    """The same oracle sample in a child process limited to one BLAS / OpenMP thread (the
+    thread count is fixed when numpy loads, so it has to be a fresh process)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1")
+    code = ("import json, sys; sys.path.insert(0, %r); import bench; "
+            "g, dt = bench.cpu_oracle_sample_sliced(); print(json.dumps({'value': g, 'seconds': dt}))" % ROOT)
+    try:
+        out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                             timeout=timeout_s, check=True).stdout.strip().splitlines()[-1]
+        r = json.loads(out)
+        return {"value": r["value"], "unit": "GB/s", "cores": 1, "seconds": r["seconds"]}
+    except Exception as e:  # a failed reference measurement must not fail the benchmark
+        return {"unavailable": f"{type(e).__name__}"}
+
+
 def cpu_threads():
     try:
         import threadpoolctl
@@ -837,7 +886,8 @@ def main():
     cpu = None
     if rank == 0 and not args.no_cpu:
         gbps, sample, _ = cpu_oracle_sample(lin, attn)
-        cpu = {"value": gbps, "unit": "GB/s", "cores": cpu_threads(), "kind": "oracle", "sample": sample}
+        cpu = {"value": gbps, "unit": "GB/s", "cores": cpu_threads(), "kind": "oracle", "sample": sample,
+               "one_core": cpu_oracle_one_core()}
 
     n = world
     line = {

@@ -273,6 +273,26 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
         : "memory");
 }
 
+// Four MMAs into one accumulator, all accumulating, in one asm block. Descriptors are given
+// as their low words (which hold the start address) and a high word shared by the four.
+__device__ __forceinline__ void umma_bf16_x4(uint32_t d_tmem, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t a_hi, uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3,
+                                             uint32_t b_hi, uint32_t idesc) {
+    asm volatile(
+        "{\n .reg .pred p;\n .reg .b64 da, db;\n setp.ne.b32 p, %12, 0;\n"
+        " mov.b64 da, {%1, %5};\n mov.b64 db, {%6, %10};\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %11, p;\n"
+        " mov.b64 da, {%2, %5};\n mov.b64 db, {%7, %10};\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %11, p;\n"
+        " mov.b64 da, {%3, %5};\n mov.b64 db, {%8, %10};\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %11, p;\n"
+        " mov.b64 da, {%4, %5};\n mov.b64 db, {%9, %10};\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %11, p;\n}" ::"r"(d_tmem),
+        "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(a_hi), "r"(b0), "r"(b1), "r"(b2), "r"(b3), "r"(b_hi), "r"(idesc),
+        "r"(1u)
+        : "memory");
+}
+
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))

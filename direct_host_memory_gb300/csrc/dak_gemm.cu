@@ -8,8 +8,11 @@
 // a ring of shared-memory slots with single bulk asynchronous copies (the copy engine of
 // TMA) while other warps do the math (section 4.1, "Asynchronous TMA Access"). Host CTAs
 // keep at most `host_window` chunks in flight: the static congestion window of section
-// 4.3.1. Each tile row is read by exactly one CTA, which computes all N columns, so no
-// host byte crosses the link twice (the locality half of section 4.3.2's scheduling).
+// 4.3.1. Each byte of a tile row is read by exactly one CTA, which computes all N columns
+// for it, so no host byte crosses the link twice (the locality half of section 4.3.2's
+// scheduling). A tile row's K range may be cut into P pieces, each a unit of work of its
+// tier's CTAs, so that the units spread evenly over the SMs; the CTA that finishes a tile
+// row's last piece adds the fp32 partial tiles in piece order.
 //
 // Placement layout of a tile row (both tiers): 64 rows x K_pad columns stored k-group
 // major, [K_pad/8][64 rows][8 columns] bf16: every 8 x 8 block (8 rows x 16 bytes) is
@@ -19,6 +22,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "dak_device.cuh"
@@ -41,13 +45,14 @@ struct GemmParams {
     const __nv_bfloat16* B; // [N][K]
     void* C;                // [N][M]
     int M, K, K_pad, N, N_pad, T, h;
-    int n_host_ctas, n_hbm_ctas, host_window, hbm_window;  // host/HBM counts are in clusters of S CTAs
+    int n_host_ctas, n_hbm_ctas, host_window, hbm_window;  // host/HBM counts are in clusters of NC CTAs
     int c_fp32;
     long long tile_bytes;
     DevStatus* st;
     int b3d;      // B arrives in one 3-D tensor copy per stage (else several 2-D copies)
-    int S;        // CTAs per cluster splitting each tile row's K range (1 = no split)
-    int red_off;  // byte offset (from the aligned ring base) of the partial-sum area, S > 1
+    int P;        // pieces per tile row: its K range is cut into P parts, each a unit of work
+    float* part;  // P > 1: fp32 partial tiles [T][P][64 rows][N_pad]
+    int* cnt;     // P > 1: per tile row, pieces finished so far (back to 0 after the last)
     int NC;       // CTAs per cluster sharing each tile row across 256-row blocks of B (1 = off)
     int glu;      // rows interleaved gate/up: C[n][row/2] = silu(gate) * up, C is [N][M/2]
     // Ring layout per role: ch[0] for CTAs reading HBM tiles, ch[1] for CTAs reading host
@@ -58,44 +63,62 @@ struct GemmParams {
 // SwiGLU of one gate / up pair (the same expression as the decoder's standalone kernel)
 __device__ __forceinline__ float swiglu_pair(float g, float u) { return g / (1.f + expf(-g)) * u; }
 
-// Tiles of this CTA: role, first tile, stride, count, and the chunk range [c_lo, c_hi) of
-// every tile row that this CTA (rank `rank` of its cluster) accumulates.
+// Units of work of this CTA. A role's units are its tile rows times P pieces (unit u is piece
+// u % P of the role's tile row u / P); the CTA takes units first, first + stride, ... (count
+// of them), so that the pieces of one tile row go to different CTAs.
 struct TileIter {
     Chunks c;  // this CTA's ring layout
     bool host;
+    int tile0;  // first tile row of the role
     int first, stride, count;
     const uint8_t* base;
     int window;
-    int rank, c_lo, c_hi;
+    int rank;  // rank in the cluster of a wide B (0 otherwise)
 };
 
 __device__ __forceinline__ TileIter tiles_of_cta(const GemmParams& p) {
     TileIter it;
-    const int cl = p.S > 1 ? p.S : p.NC;  // CTAs per cluster
-    const int b = blockIdx.x / cl;        // cluster index
+    const int b = blockIdx.x / p.NC;  // cluster index
     it.c = p.ch[b < p.n_host_ctas ? 1 : 0];
-    const int nch = (p.K_pad + it.c.kc - 1) / it.c.kc;
-    it.rank = cl > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-    it.c_lo = p.S > 1 ? it.rank * nch / p.S : 0;
-    it.c_hi = p.S > 1 ? (it.rank + 1) * nch / p.S : nch;
+    it.rank = p.NC > 1 ? static_cast<int>(cluster_ctarank()) : 0;
     if (b < p.n_host_ctas) {
+        const int units = p.h * p.P;
         it.host = true;
+        it.tile0 = 0;
         it.first = b;
         it.stride = p.n_host_ctas;
-        it.count = (p.h > b) ? (p.h - b + p.n_host_ctas - 1) / p.n_host_ctas : 0;
+        it.count = (units > b) ? (units - b + p.n_host_ctas - 1) / p.n_host_ctas : 0;
         it.base = p.a_host;
         it.window = p.host_window;
     } else {
-        int j = b - p.n_host_ctas;
-        int nh = p.T - p.h;
+        const int j = b - p.n_host_ctas;
+        const int units = (p.T - p.h) * p.P;
         it.host = false;
-        it.first = p.h + j;
+        it.tile0 = p.h;
+        it.first = j;
         it.stride = p.n_hbm_ctas;
-        it.count = (nh > j) ? (nh - j + p.n_hbm_ctas - 1) / p.n_hbm_ctas : 0;
+        it.count = (units > j) ? (units - j + p.n_hbm_ctas - 1) / p.n_hbm_ctas : 0;
         it.base = p.a_hbm;
         it.window = p.hbm_window;
     }
     return it;
+}
+
+// The ui-th unit of a CTA: tile row t and its K range [k0, k1). A tile row's K range is cut
+// into P pieces at multiples of 64 columns, from the shape only.
+struct Piece {
+    int t, idx, k0, k1;
+};
+
+__device__ __forceinline__ Piece piece_of(const GemmParams& p, const TileIter& it, int ui) {
+    const int u = it.first + ui * it.stride;
+    Piece q;
+    q.t = it.tile0 + u / p.P;
+    q.idx = u % p.P;
+    const int steps = (p.K_pad + 63) >> 6;
+    q.k0 = (q.idx * steps / p.P) << 6;
+    q.k1 = min(((q.idx + 1) * steps / p.P) << 6, p.K_pad);
+    return q;
 }
 
 __device__ __forceinline__ const uint8_t* tile_src(const GemmParams& p, const TileIter& it, int t) {
@@ -106,7 +129,7 @@ __device__ __forceinline__ const uint8_t* tile_src(const GemmParams& p, const Ti
 // error location codes (upper 32 bits of the status info)
 enum : uint32_t {
     W_PROD_EMPTY = 1, W_CONS_FULL = 2, W_MMA_FULL = 3, W_MMA_ACC = 4, W_EPI_ACC = 5, W_DRAIN = 6, W_BPROD_EMPTY = 7,
-    W_RED_FULL = 8, W_RED_EMPTY = 9, W_FWD_FULL = 10, W_FWD_PEER = 11, W_ARM_EMPTY = 12
+    W_FWD_FULL = 10, W_FWD_PEER = 11, W_ARM_EMPTY = 12
 };
 
 // Wait (bounded, ignoring the abort flag) for the last fill of every ring slot, so that no
@@ -160,19 +183,18 @@ __device__ __forceinline__ void produce(const GemmParams& p, const TileIter& it,
     // the weights never depend on the previous kernel of the stream; the hidden states may
     if (!is_a) grid_dep_wait();
     long long i = 0;
-    for (int ti = 0; ti < it.count && !*abort; ++ti) {
-        const int t = it.first + ti * it.stride;
-        const uint8_t* src = tile_src(p, it, t);
-        for (int c = it.c_lo; c < it.c_hi; ++c, ++i) {
+    for (int ui = 0; ui < it.count && !*abort; ++ui) {
+        const Piece q = piece_of(p, it, ui);
+        const uint8_t* src = tile_src(p, it, q.t);
+        for (int k0 = q.k0; k0 < q.k1; k0 += it.c.kc, ++i) {
             const int s = static_cast<int>(i % W);
             if (i >= W && !mbar_wait(&empty[s], static_cast<uint32_t>(((i / W) - 1) & 1), abort, p.st,
                                      DAK_ERR_TIMEOUT, is_a ? W_PROD_EMPTY : W_BPROD_EMPTY)) {
                 goto done;
             }
-            const int k0 = c * it.c.kc;
             uint8_t* dst = smem + static_cast<size_t>(s) * it.c.stage_bytes;
             if (is_a) {
-                const uint32_t a_bytes = static_cast<uint32_t>(min(it.c.kc, p.K_pad - k0)) * 128u;
+                const uint32_t a_bytes = static_cast<uint32_t>(min(it.c.kc, q.k1 - k0)) * 128u;
                 mbar_arrive_expect_tx(&full[s], a_bytes);
                 bulk_g2s(dst, src + static_cast<long long>(k0) * 128, a_bytes, &full[s], pol_a);
             } else {
@@ -194,9 +216,10 @@ __device__ __forceinline__ void produce_b_ring(const GemmParams& p, const TileIt
     const int WB = it.c.wb;
     const int row0 = p.NC > 1 ? it.rank * p.N_pad : 0;
     long long ib = 0;
-    for (int ti = 0; ti < it.count && !*abort; ++ti) {
-        for (int c = it.c_lo; c < it.c_hi; ++c) {
-            const int kce = min(it.c.kc, p.K_pad - c * it.c.kc);
+    for (int ui = 0; ui < it.count && !*abort; ++ui) {
+        const Piece q = piece_of(p, it, ui);
+        for (int k0 = q.k0; k0 < q.k1; k0 += it.c.kc) {
+            const int kce = min(it.c.kc, q.k1 - k0);
             for (int sub = 0; sub * it.c.kcb < kce; ++sub, ++ib) {
                 const int sb = static_cast<int>(ib % WB);
                 if (ib >= WB && !mbar_wait(&b_empty[sb], static_cast<uint32_t>(((ib / WB) - 1) & 1), abort, p.st,
@@ -205,7 +228,7 @@ __device__ __forceinline__ void produce_b_ring(const GemmParams& p, const TileIt
                 }
                 mbar_arrive_expect_tx(&b_full[sb], b_stage_bytes(p, kUmmaB, it.c.kcb));
                 issue_b(p, bmap, smem + it.c.b_ring_off + static_cast<size_t>(sb) * it.c.b_slot_bytes,
-                        c * it.c.kc + sub * it.c.kcb, &b_full[sb], kUmmaB, row0, it.c.kcb);
+                        k0 + sub * it.c.kcb, &b_full[sb], kUmmaB, row0, it.c.kcb);
             }
         }
     }
@@ -228,8 +251,9 @@ __device__ __forceinline__ void forward_a(const GemmParams& p, const TileIter& i
     const int lane = threadIdx.x & 31;
     const int r = lane + 1;  // the rank this lane forwards to
     long long i = 0;
-    for (int ti = 0; ti < it.count; ++ti) {
-        for (int c = it.c_lo; c < it.c_hi; ++c, ++i) {
+    for (int ui = 0; ui < it.count; ++ui) {
+        const Piece q = piece_of(p, it, ui);
+        for (int k0 = q.k0; k0 < q.k1; k0 += it.c.kc, ++i) {
             const int s = static_cast<int>(i % W);
             bool ok = mbar_wait(&full[s], static_cast<uint32_t>((i / W) & 1), abort, p.st, DAK_ERR_TIMEOUT, W_FWD_FULL);
             if (ok && i >= W)
@@ -237,8 +261,7 @@ __device__ __forceinline__ void forward_a(const GemmParams& p, const TileIter& i
                                        DAK_ERR_TIMEOUT, W_FWD_PEER);
             if (!__all_sync(0xffffffffu, ok)) goto done;
             if (r < p.NC) {
-                const int k0 = c * it.c.kc;
-                const uint32_t a_bytes = static_cast<uint32_t>(min(it.c.kc, p.K_pad - k0)) * 128u;
+                const uint32_t a_bytes = static_cast<uint32_t>(min(it.c.kc, q.k1 - k0)) * 128u;
                 uint8_t* slot = smem + static_cast<size_t>(s) * it.c.stage_bytes;
                 bulk_s2s_cluster(mapa_shared(smem_u32(slot), static_cast<uint32_t>(r)), slot, a_bytes,
                                  mapa_shared(smem_u32(&full[s]), static_cast<uint32_t>(r)));
@@ -258,8 +281,9 @@ __device__ __forceinline__ void arm_forwarded_a(const GemmParams& p, const TileI
                                                 uint64_t* empty, uint64_t* peer_empty, volatile int* abort) {
     const int W = it.window;
     long long i = 0;
-    for (int ti = 0; ti < it.count && !*abort; ++ti) {
-        for (int c = it.c_lo; c < it.c_hi; ++c, ++i) {
+    for (int ui = 0; ui < it.count && !*abort; ++ui) {
+        const Piece q = piece_of(p, it, ui);
+        for (int k0 = q.k0; k0 < q.k1; k0 += it.c.kc, ++i) {
             const int s = static_cast<int>(i % W);
             if (i >= W) {
                 if (!mbar_wait(&empty[s], static_cast<uint32_t>(((i / W) - 1) & 1), abort, p.st, DAK_ERR_TIMEOUT,
@@ -267,8 +291,7 @@ __device__ __forceinline__ void arm_forwarded_a(const GemmParams& p, const TileI
                     goto done;
                 mbar_arrive_remote(mapa_shared(smem_u32(&peer_empty[s]), 0));
             }
-            const int k0 = c * it.c.kc;
-            mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(min(it.c.kc, p.K_pad - k0)) * 128u);
+            mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(min(it.c.kc, q.k1 - k0)) * 128u);
         }
     }
 done:
@@ -318,18 +341,18 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
     const int r = lane & 7;       // row within the group
     const int kq = lane >> 3;     // k-group phase 0..3
     long long i = 0;
-    for (int ti = 0; ti < it.count; ++ti) {
-        const int t = it.first + ti * it.stride;
+    for (int ui = 0; ui < it.count; ++ui) {
+        const Piece q = piece_of(p, it, ui);  // the CUDA-core path never splits a tile row (P = 1)
+        const int t = q.t;
         float acc[N];
 #pragma unroll
         for (int n = 0; n < N; ++n) acc[n] = 0.f;
-        for (int c = it.c_lo; c < it.c_hi; ++c, ++i) {
+        for (int k0 = q.k0; k0 < q.k1; k0 += it.c.kc, ++i) {
             const int s = static_cast<int>(i % W);
             if (!mbar_wait(&full[s], static_cast<uint32_t>((i / W) & 1), abort, p.st, DAK_ERR_TIMEOUT, W_CONS_FULL)) {
                 return;
             }
-            const int k0 = c * it.c.kc;
-            const int kgr = min(min(it.c.kc, p.K_pad - k0), p.K - k0) >> 3;  // real k-groups in this chunk
+            const int kgr = min(min(it.c.kc, q.k1 - k0), p.K - k0) >> 3;  // real k-groups in this chunk
             const uint8_t* st = smem + static_cast<size_t>(s) * it.c.stage_bytes;
             const uint8_t* bst = st + it.c.kc * 128;
             for (int kg = kq; kg < kgr; kg += 4) {
@@ -398,12 +421,94 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
 }
 
 // ======================================================================================
-// Tensor-core path, N in 8..256: tcgen05.mma (M = 64 rows of A, N = N_pad hidden-state
-// columns, K = 16 per instruction), fp32 accumulators in TMEM, double-buffered.
+// Tensor-core path, N >= 8: tcgen05.mma (M = 64 rows of A, N = N_pad <= 256 hidden-state
+// columns, K = 16 per instruction), fp32 accumulators in TMEM, double-buffered (one per
+// unit of work, so the epilogue of one unit overlaps the MMAs of the next).
 // Warps: 0 = A producer (bulk copies), 1 = TMEM allocator + MMA issuer,
-//        2..5 = epilogue (TMEM -> registers -> C), 6 = B producer (tensor-map copies).
+//        2..5 = epilogue (TMEM -> registers -> C, or -> partial tile and the piece count),
+//        6 = B producer (tensor-map copies), 7 = A forwarder of a wide-B cluster (NC > 1).
 // ======================================================================================
 constexpr int kUmmaThreads = 8 * 32;
+
+// The n MMAs (K = 16 each) of one sub-chunk. Step m reads A 2048 bytes (two k-groups of the
+// no-swizzle layout) further on and B 32 bytes further inside a 64-column block, with one
+// block (bblk16 descriptor units) per 64 columns. The first step of a piece starts the
+// accumulator; the rest go out four per asm block with 32-bit adds on the descriptors' low
+// words (the start-address field, which never carries into the high word here).
+__device__ __forceinline__ void issue_mmas(uint32_t d_tmem, uint64_t ad0, uint64_t bd0, uint32_t bblk16, int n,
+                                           uint32_t idesc, bool accumulate) {
+    const uint32_t a_lo = static_cast<uint32_t>(ad0), a_hi = static_cast<uint32_t>(ad0 >> 32);
+    const uint32_t b_lo = static_cast<uint32_t>(bd0), b_hi = static_cast<uint32_t>(bd0 >> 32);
+    auto a_at = [&](int m) { return a_lo + static_cast<uint32_t>(m) * 128u; };
+    auto b_at = [&](int m) { return b_lo + static_cast<uint32_t>(m >> 2) * bblk16 + static_cast<uint32_t>(m & 3) * 2u; };
+    int m = 0;
+    if (!accumulate && n > 0) {
+        umma_bf16(d_tmem, ad0, bd0, idesc, 0u);
+        m = 1;
+    }
+    for (; m + 4 <= n; m += 4) {
+        umma_bf16_x4(d_tmem, a_at(m), a_at(m + 1), a_at(m + 2), a_at(m + 3), a_hi, b_at(m), b_at(m + 1), b_at(m + 2),
+                     b_at(m + 3), b_hi, idesc);
+    }
+    for (; m < n; ++m) {
+        umma_bf16(d_tmem, (static_cast<uint64_t>(a_hi) << 32) | a_at(m), (static_cast<uint64_t>(b_hi) << 32) | b_at(m),
+                  idesc, 1u);
+    }
+}
+
+constexpr int kMaxPieces = 8;       // pieces per tile row
+constexpr int kMinPieceSteps = 16;  // 64-column steps of an automatically chosen piece
+
+// C[n][row] for the 8 hidden-state rows n_base .. n_base + 7 of one output row (n < N only),
+// fp32 or bf16. With a SwiGLU placement, rows 2j (gate) and 2j + 1 (up) are held by lanes l
+// and l ^ 1: the even lane writes C[n][j] = silu(gate) * up (C has M / 2 columns). Every lane
+// of the warp calls this (the pairing is a shuffle).
+__device__ __forceinline__ void store_c(const GemmParams& p, const float (&f)[8], int row, bool valid, int n_base) {
+    if (p.glu) {
+        float up[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) up[j] = __shfl_xor_sync(0xffffffffu, f[j], 1);
+        if (valid && !(row & 1)) {
+            const int half = p.M >> 1, col = row >> 1;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int n = n_base + j;
+                if (n < p.N) {
+                    const float a = swiglu_pair(f[j], up[j]);
+                    if (p.c_fp32) {
+                        reinterpret_cast<float*>(p.C)[static_cast<long long>(n) * half + col] = a;
+                    } else {
+                        reinterpret_cast<__nv_bfloat16*>(p.C)[static_cast<long long>(n) * half + col] =
+                            __float2bfloat16_rn(a);
+                    }
+                }
+            }
+        }
+    } else if (valid) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int n = n_base + j;
+            if (n < p.N) {
+                if (p.c_fp32) {
+                    reinterpret_cast<float*>(p.C)[static_cast<long long>(n) * p.M + row] = f[j];
+                } else {
+                    reinterpret_cast<__nv_bfloat16*>(p.C)[static_cast<long long>(n) * p.M + row] =
+                        __float2bfloat16_rn(f[j]);
+                }
+            }
+        }
+    }
+}
+
+// Atomic add at GPU scope with acquire and release semantics; returns the old value.
+__device__ __forceinline__ int atomic_add_acq_rel(int* addr, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+    return old;
+}
+
+// The 128 threads of the four epilogue warps meet (named barrier 1; barrier 0 is __syncthreads).
+__device__ __forceinline__ void epilogue_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 // TMEM lane holding output row `row` (0..63) of an M = 64 accumulator: rows 16q .. 16q+15
 // sit in lanes 32q .. 32q+15 of sub-partition q.
@@ -413,11 +518,11 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     gemm_umma_kernel(const GemmParams p, const __grid_constant__ CUtensorMap bmap) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ uint64_t full[8], empty[8], acc_full[2], acc_empty[2];
-    __shared__ uint64_t red_full, red_empty;  // cluster split: partials in / partial buffer free
     __shared__ uint64_t peer_empty[8];        // wide B, rank 0: every other rank has freed the slot
     __shared__ uint64_t b_full[8], b_empty[8];  // wide B: B's own ring
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
+    __shared__ int last_piece;  // split tile rows: this CTA finished the tile row's last piece
     volatile int* abort = &abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -451,10 +556,6 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_empty[b], 4);
         }
-        if (p.S > 1) {
-            mbar_init(&red_full, (p.S - 1) * 128);  // every epilogue thread of every partner, per tile
-            mbar_init(&red_empty, 128);             // every epilogue thread of the leader, per tile
-        }
         fence_mbar_init();
         prefetch_tmap(&bmap);
     }
@@ -465,7 +566,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (p.S > 1 || p.NC > 1) cluster_sync_all();  // partners' barriers exist before any remote access
+    if (p.NC > 1) cluster_sync_all();  // partners' barriers exist before any remote access
     grid_dep_launch();
     const uint32_t tmem = tmem_base_sh;
 
@@ -489,16 +590,17 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         long long i = 0, ib = 0;
         uint64_t* last_bar = nullptr;
         uint32_t last_par = 0;
-        for (int ti = 0; ti < it.count; ++ti) {
-            const int ab = ti & 1;
-            if (ti >= 2 && !mbar_wait(&acc_empty[ab], static_cast<uint32_t>(((ti >> 1) - 1) & 1), abort, p.st,
+        for (int ui = 0; ui < it.count; ++ui) {
+            const int ab = ui & 1;
+            if (ui >= 2 && !mbar_wait(&acc_empty[ab], static_cast<uint32_t>(((ui >> 1) - 1) & 1), abort, p.st,
                                       DAK_ERR_TIMEOUT, W_MMA_ACC)) {
                 break;
             }
             tc_fence_after();
             const uint32_t d_tmem = tmem + static_cast<uint32_t>(ab) * acc_stride;
+            const Piece q = piece_of(p, it, ui);
             bool ok = true;
-            for (int c = it.c_lo; c < it.c_hi; ++c, ++i) {
+            for (int k0 = q.k0; k0 < q.k1; k0 += it.c.kc, ++i) {
                 const int s = static_cast<int>(i % W);
                 // a forwarded A chunk is written by another CTA of the cluster
                 const bool got = p.NC > 1 ? mbar_wait_cluster(&full[s], static_cast<uint32_t>((i / W) & 1), abort,
@@ -510,7 +612,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const int kce = min(it.c.kc, p.K_pad - c * it.c.kc);
+                const int kce = min(it.c.kc, q.k1 - k0);
                 const uint32_t a_base = smem_u32(smem + static_cast<size_t>(s) * it.c.stage_bytes);
                 // A: no swizzle, K-major; 8x8 blocks of one k-group are 128 B apart along M,
                 // k-groups are 64 rows x 16 B = 1024 B apart along K (+2048 B per MMA).
@@ -534,19 +636,8 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
                     const uint64_t ad0 = smem_desc(a_base + static_cast<uint32_t>((k_sub >> 3) * 1024), 1024u, 128u, 0u);
                     const uint64_t bd0 = smem_desc(b_base, 16u, 1024u, 2u);
                     if (leader) {
-                        for (int kb = 0; kb < kcs; kb += 64) {
-                            const uint64_t bdb = bd0 + (static_cast<uint64_t>((kb >> 6) * bblk_bytes) >> 4);
-                            const uint64_t adb = ad0 + (static_cast<uint64_t>(kb >> 3) * 1024u >> 4);
-                            const int nk = min(4, (kcs - kb) >> 4);
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                if (j < nk) {
-                                    umma_bf16(d_tmem, adb + static_cast<uint64_t>(j * 128),
-                                              bdb + static_cast<uint64_t>(j * 2), idesc,
-                                              (c > it.c_lo || k_sub > 0 || kb > 0 || j > 0) ? 1u : 0u);
-                                }
-                            }
-                        }
+                        issue_mmas(d_tmem, ad0, bd0, static_cast<uint32_t>(bblk_bytes >> 4), kcs >> 4, idesc,
+                                   k0 > q.k0 || k_sub > 0);
                         if (sb >= 0) umma_commit(&b_empty[sb]);
                     }
                     __syncwarp();
@@ -566,7 +657,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
             if (leader) umma_commit(&acc_full[ab]);
             __syncwarp();
             last_bar = &acc_full[ab];
-            last_par = static_cast<uint32_t>((ti >> 1) & 1);
+            last_par = static_cast<uint32_t>((ui >> 1) & 1);
         }
         if (last_bar) {  // every issued MMA has finished before TMEM is released
             volatile int dummy = 0;
@@ -574,55 +665,89 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         }
         __syncwarp();
     } else {
-        // epilogue warps 2..5 -> TMEM sub-partitions 2, 3, 0, 1. With a cluster split the
-        // partners send their fp32 partial tiles into the leader's shared memory; the leader
-        // adds them to its own in rank order (a fixed order, independent of the placement).
-        const int q = warp & 3;
-        const int row_in_tile = umma_m64_row_of_lane(q, lane);
-        const bool leader = p.S > 1 ? it.rank == 0 : true;  // wide B: every rank writes its own rows
+        // epilogue warps 2..5 -> TMEM sub-partitions 2, 3, 0, 1 (lanes 0..15 of sub-partition q
+        // hold rows 16q .. 16q + 15). A split tile row (P > 1): the CTA of every piece stores
+        // its fp32 partial tile in the workspace and counts the piece in; the CTA that counts
+        // the last one adds the P partials in piece order (a fixed order, whichever CTA ran
+        // which piece and whatever the placement) and writes C. No CTA waits for another.
+        const int qp = warp & 3;
+        const int row_in_tile = umma_m64_row_of_lane(qp, lane);
         const int n_off = p.NC > 1 ? it.rank * p.N_pad : 0;  // first hidden-state row of this CTA's block
-        grid_dep_wait();  // C may be read by the previous kernel of the stream
-        float* red = reinterpret_cast<float*>(smem + p.red_off);  // [S-1][64 rows][N_pad] on the leader
-        for (int ti = 0; ti < it.count; ++ti) {
-            const int ab = ti & 1;
-            if (!mbar_wait(&acc_full[ab], static_cast<uint32_t>((ti >> 1) & 1), abort, p.st, DAK_ERR_TIMEOUT,
+        const int tile_floats = kTileM * p.N_pad;
+        grid_dep_wait();  // C and the split workspace may still be in use by the previous kernel of the stream
+        for (int ui = 0; ui < it.count; ++ui) {
+            const int ab = ui & 1;
+            if (!mbar_wait(&acc_full[ab], static_cast<uint32_t>((ui >> 1) & 1), abort, p.st, DAK_ERR_TIMEOUT,
                            W_EPI_ACC)) {
                 break;
             }
             tc_fence_after();
-            const int t = it.first + ti * it.stride;
-            const int row = t * kTileM + row_in_tile;
+            const Piece pc = piece_of(p, it, ui);
+            const int row = pc.t * kTileM + row_in_tile;
             const bool valid = row_in_tile >= 0 && row < p.M;
-            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(ab) * acc_stride;
-            if (!leader) {
-                // wait until the leader has consumed this CTA's previous partial
-                if (ti > 0 && !mbar_wait_cluster(&red_empty, static_cast<uint32_t>((ti - 1) & 1), abort, p.st,
-                                                 DAK_ERR_TIMEOUT, W_RED_EMPTY)) {
-                    break;
-                }
-                const int r_own = row_in_tile >= 0 ? row_in_tile : 0;
-                const uint32_t dst =
-                    mapa_shared(smem_u32(red + static_cast<size_t>((it.rank - 1) * kTileM + r_own) * p.N_pad), 0);
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(qp * 32) << 16) + static_cast<uint32_t>(ab) * acc_stride;
+            if (p.P > 1) {
+                float* mine = p.part + (static_cast<long long>(pc.t) * p.P + pc.idx) * tile_floats;
                 for (int n0 = 0; n0 < p.N_pad; n0 += 8) {
                     uint32_t v[8];
                     tmem_ld8(taddr + static_cast<uint32_t>(n0), v);
                     tmem_wait_ld();
                     if (row_in_tile >= 0) {
-                        st_cluster_v4(dst + n0 * 4, __uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]),
-                                      __uint_as_float(v[3]));
-                        st_cluster_v4(dst + n0 * 4 + 16, __uint_as_float(v[4]), __uint_as_float(v[5]),
-                                      __uint_as_float(v[6]), __uint_as_float(v[7]));
+                        float4* d = reinterpret_cast<float4*>(mine + row_in_tile * p.N_pad + n0);
+                        d[0] = make_float4(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]),
+                                           __uint_as_float(v[3]));
+                        d[1] = make_float4(__uint_as_float(v[4]), __uint_as_float(v[5]), __uint_as_float(v[6]),
+                                           __uint_as_float(v[7]));
                     }
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&acc_empty[ab]);
-                mbar_arrive_remote(mapa_shared(smem_u32(&red_full), 0));
+                if (lane == 0) mbar_arrive(&acc_empty[ab]);  // the accumulator is free again
+                // One thread counts the piece in, with release semantics for the 128 threads'
+                // stores (ordered before it by the barrier) and acquire semantics for the other
+                // pieces' partials, which the last piece's CTA reads next.
+                epilogue_bar_sync();
+                if (warp == 2 && lane == 0) {
+                    const int done = atomic_add_acq_rel(p.cnt + pc.t, 1) + 1;
+                    last_piece = done == p.P;
+                    if (done == p.P) p.cnt[pc.t] = 0;  // ready for the next launch
+                }
+                epilogue_bar_sync();
+                if (!last_piece) continue;
+                // The P partials, added in piece order. All 128 threads share the work: thread e
+                // takes row e % 64 and the 8-column blocks e / 64, e / 64 + 2, ...; lanes e and
+                // e ^ 1 hold rows 2j and 2j + 1 (the gate / up pair of a SwiGLU placement).
+                const int e = threadIdx.x - 64;
+                const int rr = e & 63;
+                const int rrow = pc.t * kTileM + rr;
+                const float* src0 = p.part + static_cast<long long>(pc.t) * p.P * tile_floats + rr * p.N_pad;
+                for (int blk = e >> 6; blk * 8 < p.N_pad; blk += 2) {
+                    const float* src = src0 + blk * 8;
+                    float f[8];
+                    for (int r0 = 0; r0 < p.P; r0 += 4) {  // four partials in flight at a time
+                        float4 x[8];
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            if (r0 + r < p.P) {
+                                x[2 * r] = __ldcg(reinterpret_cast<const float4*>(src + (r0 + r) * tile_floats));
+                                x[2 * r + 1] = __ldcg(reinterpret_cast<const float4*>(src + (r0 + r) * tile_floats + 4));
+                            }
+                        }
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            if (r0 + r == 0) {
+                                f[0] = x[0].x; f[1] = x[0].y; f[2] = x[0].z; f[3] = x[0].w;
+                                f[4] = x[1].x; f[5] = x[1].y; f[6] = x[1].z; f[7] = x[1].w;
+                            } else if (r0 + r < p.P) {
+                                f[0] += x[2 * r].x; f[1] += x[2 * r].y; f[2] += x[2 * r].z; f[3] += x[2 * r].w;
+                                f[4] += x[2 * r + 1].x; f[5] += x[2 * r + 1].y; f[6] += x[2 * r + 1].z;
+                                f[7] += x[2 * r + 1].w;
+                            }
+                        }
+                    }
+                    store_c(p, f, rrow, rrow < p.M, n_off + blk * 8);
+                }
                 continue;
-            }
-            if (p.S > 1 && !mbar_wait_cluster(&red_full, static_cast<uint32_t>(ti & 1), abort, p.st, DAK_ERR_TIMEOUT,
-                                              W_RED_FULL)) {
-                break;
             }
             for (int n0 = 0; n0 < p.N_pad; n0 += 8) {
                 uint32_t v[8];
@@ -631,61 +756,17 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
                 float f[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(v[j]);
-                if (valid) {
-                    for (int r = 1; r < p.S; ++r) {
-                        const float4* pr = reinterpret_cast<const float4*>(
-                            red + static_cast<size_t>((r - 1) * kTileM + row_in_tile) * p.N_pad + n0);
-                        const float4 x0 = pr[0], x1 = pr[1];
-                        f[0] += x0.x; f[1] += x0.y; f[2] += x0.z; f[3] += x0.w;
-                        f[4] += x1.x; f[5] += x1.y; f[6] += x1.z; f[7] += x1.w;
-                    }
-                }
-                if (p.glu) {
-                    // rows 2j (gate) and 2j + 1 (up) sit in neighbouring lanes of this sub-partition
-                    float up[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) up[j] = __shfl_xor_sync(0xffffffffu, f[j], 1);
-                    if (valid && !(row_in_tile & 1)) {
-                        const int half = p.M >> 1, col = row >> 1;
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const int n = n_off + n0 + j;
-                            if (n < p.N) {
-                                const float a = swiglu_pair(f[j], up[j]);
-                                if (p.c_fp32) {
-                                    reinterpret_cast<float*>(p.C)[static_cast<long long>(n) * half + col] = a;
-                                } else {
-                                    reinterpret_cast<__nv_bfloat16*>(p.C)[static_cast<long long>(n) * half + col] =
-                                        __float2bfloat16_rn(a);
-                                }
-                            }
-                        }
-                    }
-                } else if (valid) {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int n = n_off + n0 + j;
-                        if (n < p.N) {
-                            if (p.c_fp32) {
-                                reinterpret_cast<float*>(p.C)[static_cast<long long>(n) * p.M + row] = f[j];
-                            } else {
-                                reinterpret_cast<__nv_bfloat16*>(p.C)[static_cast<long long>(n) * p.M + row] =
-                                    __float2bfloat16_rn(f[j]);
-                            }
-                        }
-                    }
-                }
+                store_c(p, f, row, valid, n_off + n0);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[ab]);
-            for (int r = 1; r < p.S; ++r) mbar_arrive_remote(mapa_shared(smem_u32(&red_empty), static_cast<uint32_t>(r)));
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (p.S > 1 || p.NC > 1) cluster_sync_all();  // no CTA leaves while a partner may still touch its shared memory
+    if (p.NC > 1) cluster_sync_all();  // no CTA leaves while a partner may still touch its shared memory
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, tmem_cols);
@@ -780,6 +861,74 @@ static cudaError_t launch_ex(Kernel k, int grid, int threads, int smem, int clus
     return cudaLaunchKernelEx(&cfg, k, p, bmap);
 }
 
+// Workspace of split tile rows: fp32 partial tiles and one counter per tile row, in device
+// memory that the module owns (no allocation at launch time, so launches can be captured in
+// CUDA graphs). Launches on one stream use it in turn (the partials and counters are touched
+// only after the previous kernel of the stream has finished); launches that split tile rows
+// must not run concurrently on different streams of one device.
+constexpr long long kSplitFloats = 8ll << 20;  // 32 MiB
+constexpr int kSplitTiles = 1 << 16;
+static __device__ float g_split_part[kSplitFloats];
+static __device__ int g_split_cnt[kSplitTiles];
+
+static bool split_workspace(float** part, int** cnt) {
+    static std::atomic<float*> parts[64];
+    static std::atomic<int*> cnts[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    float* pp = parts[dev].load();
+    int* cp = cnts[dev].load();
+    if (!pp || !cp) {
+        void* a = nullptr;
+        void* b = nullptr;
+        if (cudaGetSymbolAddress(&a, g_split_part) != cudaSuccess || cudaGetSymbolAddress(&b, g_split_cnt) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        pp = static_cast<float*>(a);
+        cp = static_cast<int*>(b);
+        parts[dev].store(pp);
+        cnts[dev].store(cp);
+    }
+    *part = pp;
+    *cnt = cp;
+    return true;
+}
+
+// Pieces per tile row: the split of each tile row's K range into P parts (at multiples of
+// 64 columns), chosen from the shape and the SM count only, never from the placement, so
+// that results are bit-identical across offload ratios. Automatic: the P in 1..8 that
+// minimises what the busiest CTA streams, ceil(T P / slots) / P tile rows, if it saves at
+// least 3% over a smaller P. Pieces keep >= 1024 columns: a piece costs its CTA about a
+// microsecond of epilogue (partial tile out, count, and for the last piece the sum), which
+// shorter pieces cannot hide. The workspace must hold the partials.
+// tuning.split_k > 0 fixes P (1 = no split).
+static int split_pieces(int T, int K_pad, int N_pad, int slots, const dak_tuning* t) {
+    const int steps = (K_pad + 63) / 64;
+    auto fits = [&](int P) {
+        return P <= steps && T <= kSplitTiles &&
+               static_cast<long long>(T) * P * kTileM * N_pad <= kSplitFloats;
+    };
+    if (t && t->split_k > 0) {
+        int P = std::min(kMaxPieces, t->split_k);
+        while (P > 1 && !fits(P)) --P;
+        return P;
+    }
+    auto cost = [&](int P) { return static_cast<double>((static_cast<long long>(T) * P + slots - 1) / slots) / P; };
+    int best = 1;
+    for (int P = 2; P <= kMaxPieces; ++P) {
+        if (!fits(P) || steps / P < kMinPieceSteps) break;
+        if (cost(P) < 0.97 * cost(best)) best = P;
+    }
+    return best;
+}
+
+void reset_split_counters() {
+    float* part = nullptr;
+    int* cnt = nullptr;
+    if (split_workspace(&part, &cnt)) cudaMemset(cnt, 0, sizeof(int) * kSplitTiles);
+}
+
 // One launch over up to kMaxWideN hidden-state rows: one CTA per tile row up to 256 rows
 // (the widest tcgen05 tile used here), a cluster of ceil(N / 256) CTAs per tile row beyond.
 static dak_status launch_gemm_block(const dak_placement* A, const void* host_src, const void* B, void* C, int N,
@@ -810,7 +959,7 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
     p.c_fp32 = c_fp32 ? 1 : 0;
     p.tile_bytes = A->tile_bytes;
     p.glu = A->glu;
-    p.S = 1;
+    p.P = 1;
     p.st = status_ptr();
     if (!p.st) return DAK_ERR_CUDA;
 
@@ -821,44 +970,19 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
     const int NC = p.NC;
     auto stage_of = [&](int k) { return (k * 128 + k * 2 * rows_b + 1023) & ~1023; };
 
-    // Cluster split of each tile row's K range, chosen from the shape only (never from the
-    // placement, so that results are bit-identical across offload ratios): when there are
-    // fewer tile rows than SMs, S CTAs share a tile row and two CTAs run on each SM, which
-    // multiplies the copy streams that keep HBM busy.
-    auto red_of = [&](int s_) { return (s_ - 1) * kTileM * p.N_pad * 4; };
-    // two stages of at least 128 columns beside the partial-sum area
-    auto fits = [&](int s_, int budget_) { return 2 * stage_of(128) + red_of(s_) + 1024 <= budget_; };
-    // CTAs of one cluster wait on each other, so they must never wait for TMEM: a split is
-    // used only while two CTAs' accumulators (2 x 2 x N_pad columns) fit in one SM's TMEM.
-    const bool can_split = umma && p.N_pad <= 128 && !(t && t->split_k == 1);
-    int S = 1, per_sm = 1;
-    if (can_split && (p.T < sms || (t && t->split_k > 1))) {
-        const bool user = t && t->split_k > 1;
-        // automatic: enough CTAs for two per SM, but each CTA still streams >= ~448 KiB of its
-        // tile row (shorter slices are dominated by per-launch and pipeline-fill costs)
-        const int by_bytes = static_cast<int>(p.tile_bytes / (448 * 1024));
-        const int want = user ? std::min(8, t->split_k)
-                              : std::max(1, std::min(8, std::min((2 * sms) / p.T, by_bytes)));
-        if (fits(want, kSmemBudgetTwoPerSm)) {
-            S = want;
-            per_sm = want > 1 ? 2 : 1;
-        } else {
-            S = user ? want : std::max(1, std::min(8, sms / p.T));
-            while (S > 1 && red_of(S) + 2 * stage_of(64) + 1024 > kSmemBudget) --S;
-        }
-    }
-    if (umma && t && (t->ctas_per_sm == 1 || t->ctas_per_sm == 2)) per_sm = t->ctas_per_sm;
+    int per_sm = 1;
+    if (umma && NC == 1 && t && (t->ctas_per_sm == 1 || t->ctas_per_sm == 2)) per_sm = t->ctas_per_sm;
     const int budget = per_sm == 2 ? kSmemBudgetTwoPerSm : kSmemBudget;
     int kc;
     if (t && t->chunk_k > 0) {
         kc = t->chunk_k;
     } else if (!umma) {
         kc = 512;
-    } else if (S > 1 || per_sm == 2) {
-        // the widest chunk that leaves two stages beside the partial-sum area
+    } else if (per_sm == 2) {
+        // the widest chunk that leaves two stages
         kc = 64;
         for (int cand : {512, 384, 256, 192, 128}) {
-            if (2 * stage_of(cand) + red_of(S) + 1024 <= budget) {
+            if (2 * stage_of(cand) + 1024 <= budget) {
                 kc = cand;
                 break;
             }
@@ -876,22 +1000,16 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
     const bool b_ring_all = umma && NC > 1;
     const bool b_ring_host = umma && p.N_pad > 128 && !(t && t->chunk_k > 0);
     if (b_ring_all && !(t && t->chunk_k > 0)) kc = 256;
-    const int nch = (p.K_pad + kc - 1) / kc;
-    S = std::min(S, nch);
-    if (S == 1) per_sm = 1;
-    if (umma && t && (t->ctas_per_sm == 1 || t->ctas_per_sm == 2)) per_sm = t->ctas_per_sm;
-    if (NC > 1) per_sm = 1;  // each CTA holds 2 x 256 TMEM columns, the whole TMEM of an SM
-    p.S = S;
-    const int CL = S > 1 ? S : NC;  // CTAs per cluster
-    const int red_bytes = S > 1 ? red_of(S) : 0;
-    const int ring_budget = per_sm == 2 ? kSmemBudgetTwoPerSm : kSmemBudget;
+    // (NC > 1: each CTA holds 2 x 256 TMEM columns, the whole TMEM of an SM: one CTA per SM)
+    const int CL = NC;  // CTAs per cluster
+    const int ring_budget = budget;
     auto layout = [&](int kc_, bool split, Chunks* L) -> bool {
         L->kc = kc_;
         L->kcb = split ? 64 : kc_;
         if (split) {
             L->stage_bytes = (kc_ * 128 + 1023) & ~1023;
             L->b_slot_bytes = (p.N_pad * L->kcb * 2 + 1023) & ~1023;
-            const int avail = ring_budget - red_bytes - 1024;
+            const int avail = ring_budget - 1024;
             L->stages = std::min(4, std::max(2, avail / 2 / L->stage_bytes));  // about half for A
             L->wb = std::min(8, (avail - L->stages * L->stage_bytes) / L->b_slot_bytes);
             if (L->wb < 2) {
@@ -901,7 +1019,7 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
             if (L->wb < 2) return false;
         } else {
             L->stage_bytes = stage_of(kc_);
-            L->stages = std::min(8, (ring_budget - red_bytes - (umma ? 1024 : 0)) / L->stage_bytes);
+            L->stages = std::min(8, (ring_budget - (umma ? 1024 : 0)) / L->stage_bytes);
             L->wb = 0;
             L->b_slot_bytes = 0;
             if (L->stages < 1 || (L->stages < 2 && !(t && t->chunk_k > 0))) return false;
@@ -911,24 +1029,30 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
     };
     if (!layout(kc, b_ring_all, &p.ch[0])) return DAK_ERR_INVALID;
     p.ch[1] = p.ch[0];
-    if (!b_ring_all && b_ring_host && S == 1 && p.h > 0) {
+    if (!b_ring_all && b_ring_host && p.h > 0) {
         if (!layout(256, true, &p.ch[1])) p.ch[1] = p.ch[0];
     }
     if (p.ch[0].kcb != p.ch[1].kcb) return DAK_ERR_INVALID;  // one B tensor map serves both
     const int kcb = p.ch[0].kcb;
     auto ring_bytes = [](const Chunks& L) { return L.stages * L.stage_bytes + L.wb * L.b_slot_bytes; };
     const int rings = std::max(ring_bytes(p.ch[0]), ring_bytes(p.ch[1]));
-    p.red_off = rings;
-    const int smem = rings + red_bytes + (umma ? 1024 : 0);
+    const int smem = rings + (umma ? 1024 : 0);
     const int max_stages = std::max(p.ch[0].stages, p.ch[1].stages);
 
-    // schedule in cluster units
+    // pieces per tile row (tensor-core path, one CTA per tile row's columns)
+    if (umma && NC == 1) {
+        p.P = split_pieces(p.T, p.K_pad, p.N_pad, sms * per_sm, t);
+        if (p.P > 1 && !split_workspace(&p.part, &p.cnt)) return DAK_ERR_CUDA;
+    }
+
+    // schedule in cluster units; a role's units are its tile rows x P pieces
     dak_tuning tc{};
     if (t) tc = *t;
     tc.host_ctas = std::max(1, (tc.host_ctas > 0 ? tc.host_ctas : kDefaultHostCtas) / CL);
     if (tc.hbm_ctas > 0) tc.hbm_ctas = std::max(1, tc.hbm_ctas / CL);
-    Sched sc = schedule(p.h, p.T - p.h, std::max(1, (sms * per_sm) / CL), &tc, std::max(1, kDefaultHostCtas / CL),
-                        std::min(kDefaultHostWindow, p.ch[1].stages), p.ch[0].stages, max_stages);
+    Sched sc = schedule(p.h * p.P, (p.T - p.h) * p.P, std::max(1, (sms * per_sm) / CL), &tc,
+                        std::max(1, kDefaultHostCtas / CL), std::min(kDefaultHostWindow, p.ch[1].stages),
+                        p.ch[0].stages, max_stages);
     p.n_host_ctas = sc.n_host_ctas;
     p.n_hbm_ctas = sc.n_hbm_ctas;
     p.host_window = std::min(sc.host_window, p.ch[1].stages);

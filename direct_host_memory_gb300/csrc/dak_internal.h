@@ -41,6 +41,8 @@ struct DevStatus {
 
 // Device address of the status block of the current device (set up once per device).
 DevStatus* status_ptr();
+// Zero the per-tile-row counters of split GEMM tile rows (after a kernel gave up midway).
+void reset_split_counters();
 
 struct Sched {
     int n_host_ctas;  // CTAs [0, n_host_ctas) read the host tier

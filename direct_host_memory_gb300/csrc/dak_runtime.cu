@@ -440,6 +440,7 @@ extern "C" dak_status dak_last_error(void* stream, uint64_t* info) {
     if (h.code) {
         const DevStatus zero{};
         cudaMemcpy(st, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+        reset_split_counters();  // a GEMM that gave up may have counted only some pieces
     }
     if (info) *info = h.info;
     return static_cast<dak_status>(h.code);

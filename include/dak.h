@@ -56,9 +56,13 @@ typedef struct dak_placement dak_placement;
  *   n_split   : attention context splits per (request, kv head); fixed per call and
  *               independent of the placement, so results do not depend on the offload ratio.
  *   hbm_ctas  : cap on CTAs reading HBM (0 = every remaining SM).
- *   split_k   : GEMM CTAs per tile row (a thread-block cluster that splits the K range and
- *               reduces in fixed rank order); 0 = chosen from the shape, 1 = no split.
- *               Like chunk_k it changes the summation order, never with the offload ratio.
+ *   split_k   : GEMM pieces per tile row (1..8, tensor-core path): the tile row's K range is
+ *               cut at multiples of 64 columns into this many units of work that any CTA of
+ *               the tile row's tier may take; the CTA that finishes a tile row's last piece
+ *               adds the fp32 partials in piece order. 0 = chosen from the shape and the SM
+ *               count, 1 = no split. Like chunk_k it changes the summation order, never with
+ *               the offload ratio. Split launches share one device workspace: launches that
+ *               split tile rows must not run concurrently on different streams.
  *   pdl       : 1 = programmatic dependent launch: the kernel may start while the previous
  *               kernel of the stream is still running; it streams the weights / KV cache at
  *               once and waits for that kernel only before reading B / Q and writing C / O.
@@ -156,12 +160,14 @@ dak_status dak_placement_info(const dak_placement* p, int64_t* host_bytes, int64
  *       4.3.2's read amplification without multicast); larger N in launches of 1024 rows
  *       (tuning->column_blocks = 1: launches of 256 rows, each re-reading the host tiles).
  * One persistent launch: `host_ctas` CTAs stream the host tile rows and the other CTAs
- * the HBM tile rows; every CTA reads from exactly one tier and writes disjoint rows of
- * C. When the matrix has fewer tile rows than SMs, a cluster of CTAs shares each tile row,
- * each accumulating a fixed part of K, and the cluster's leader adds the partial tiles in
- * rank order through distributed shared memory. Every output row is accumulated in fp32
- * in an order fixed by the shape alone, so the result does not depend on n_host_tiles.
- * N < 8 runs on CUDA cores; N >= 8 on the tcgen05 tensor cores. */
+ * the HBM tile rows; every CTA reads from exactly one tier. When the tile rows do not
+ * spread evenly over the SMs, each tile row's K range is cut into pieces (tuning split_k)
+ * that the CTAs of its tier share; partial tiles go through a device workspace and the
+ * CTA finishing a tile row's last piece adds them in piece order. Every output row is
+ * accumulated in fp32 in an order fixed by the shape and the SM count alone, so the result
+ * does not depend on n_host_tiles. N < 8 runs on CUDA cores; N >= 8 on the tcgen05 tensor
+ * cores. Launches that split tile rows share the workspace: do not run them concurrently
+ * on different streams of one device. */
 dak_status dak_gemm(const dak_placement* A, const void* B, void* C, int N, int c_fp32, const dak_tuning* tuning,
                     void* stream);
 

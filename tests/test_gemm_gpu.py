@@ -107,9 +107,10 @@ def test_bit_identical_across_tuning(dak, N):
 
 @pytest.mark.parametrize("N", [8, 32, 64])
 @pytest.mark.parametrize("S", [1, 2, 3, 4, 8])
-def test_cluster_split_k(dak, N, S):
-    """Each tile row's K range split over S CTAs of a cluster, partials reduced by the
-    leader in rank order: matches the oracle and is identical for every offload ratio."""
+def test_split_pieces(dak, N, S):
+    """Each tile row's K range cut into S pieces that any CTA may take; the CTA finishing a
+    tile row's last piece adds the partials in piece order: matches the oracle and is
+    identical for every offload ratio."""
     M, K = 384, 3072  # 6 tile rows
     A, B = synth.gemm_inputs(M, K, N, seed=S * 100 + N)
     ref = og.gemm_ref(A, B)
@@ -118,6 +119,55 @@ def test_cluster_split_k(dak, N, S):
     assert og.rel_err(to_np(base), ref) <= FP32_OUT_TOL
     for h in (1, 3, 6):
         assert np.array_equal(bits_of(_run(dak, A, B, h, tuning=tun)), bits_of(base)), h
+
+
+@pytest.mark.parametrize("K", [1000, 1040, 4096 + 16])
+def test_split_pieces_ragged_k(dak, K):
+    """Pieces end at multiples of 64 columns except the last, which ends at K rounded up to 16;
+    few CTAs (hbm_ctas, host_ctas) so that one CTA takes several pieces of one tile row."""
+    M, N = 200, 24
+    A, B = synth.gemm_inputs(M, K, N, seed=K)
+    ref = og.gemm_ref(A, B)
+    for S in (2, 5, 8):
+        for tun in (dict(split_k=S), dict(split_k=S, hbm_ctas=3, host_ctas=2)):
+            C = _run(dak, A, B, 1, tuning=tun)
+            assert og.rel_err(to_np(C), ref) <= FP32_OUT_TOL, tun
+
+
+def test_split_pieces_graph_replay(dak):
+    """The per-tile-row piece counters return to zero after every launch: a CUDA graph of three
+    split GEMMs (two sharing tile-row indices) replayed many times gives the same bits."""
+    import torch
+    A1, B = synth.gemm_inputs(640, 2048, 16, seed=41)
+    A2, _ = synth.gemm_inputs(320, 640, 16, seed=42)
+    p1, p2 = dak.dak_place_matrix(A1, 2), dak.dak_place_matrix(A2, 0)
+    Bt = to_dev(B)
+    C1 = torch.empty(16, 640, device="cuda", dtype=torch.float32)
+    C2 = torch.empty(16, 320, device="cuda", dtype=torch.float32)
+    C3 = torch.empty(16, 640, device="cuda", dtype=torch.float32)
+
+    def step():
+        dak.dak_gemm(p1, Bt, C1, c_fp32=True, tuning=dict(split_k=3, pdl=1))
+        dak.dak_gemm(p2, C1.to(torch.bfloat16), C2, c_fp32=True, tuning=dict(split_k=5, pdl=1))
+        dak.dak_gemm(p1, Bt, C3, c_fp32=True, tuning=dict(split_k=7, pdl=1))
+
+    step()
+    torch.cuda.synchronize()
+    ref = [bits_of(x) for x in (C1, C2, C3)]
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            step()
+    for _ in range(25):
+        g.replay()
+    torch.cuda.synchronize()
+    assert dak.dak_last_error()[0] == 0
+    for r, x in zip(ref, (C1, C2, C3)):
+        assert np.array_equal(bits_of(x), r)
+    assert og.rel_err(to_np(C1), og.gemm_ref(A1, B)) <= FP32_OUT_TOL
+    for pl in (p1, p2):
+        pl.free()
 
 
 def test_split_k_integer_exact(dak):

@@ -5,8 +5,9 @@
 // congestion control and wave alignment ablations).
 //
 // Every candidate is timed with CUDA events over `reps` launches on a private stream after
-// one warm-up launch. The same routine measures the two ablations: congestion control off
-// (every SM may read the host tier, window 8) and wave alignment off.
+// one warm-up launch: host CTAs x window x chunk width, then (GEMM) the pieces per tile row
+// on top of the best of those. The same routine measures the two ablations: congestion
+// control off (every SM may read the host tier, window 8) and wave alignment off.
 #include <algorithm>
 #include <vector>
 
@@ -80,6 +81,24 @@ dak_status tune(Fn fn, bool has_host, bool gemm, int reps, const dak_tuning* bas
                     out->best_us = us;
                     out->best = t;
                 }
+            }
+        }
+    }
+    if (gemm && !(b.split_k > 0)) {
+        // then the pieces per tile row, on top of the best host CTAs / window / chunk
+        const dak_tuning top = out->best;
+        for (int P : {1, 2, 3, 4, 6, 7}) {
+            dak_tuning t = top;
+            t.split_k = P;
+            const double us = time_launches(tm, fn, t, reps);
+            if (us < 0) {
+                cudaGetLastError();
+                continue;
+            }
+            ++out->candidates;
+            if (us < out->best_us) {
+                out->best_us = us;
+                out->best = t;
             }
         }
     }

@@ -235,10 +235,11 @@ typedef struct {
 /* Time dak_gemm(A, B, C, N, c_fp32) with `reps` launches per candidate (after one warm-up
  * launch) on a private stream, over host_ctas in {4, 8, 12, 16, 24, 32} x window in
  * {2, 3, 4, 6, 8} (when A has host tiles) x chunk_k in {library default, 256, 512}, each
- * applied on top of *base (NULL = defaults); candidates the launcher rejects are skipped.
- * Synchronous; overwrites C. The chosen knobs move work between CTAs only, except
- * chunk_k, which changes the summation order of every output the same way at any
- * offload ratio. */
+ * applied on top of *base (NULL = defaults), and then, unless base fixes split_k, over
+ * split_k in {1, 2, 3, 4, 6, 7} on top of the best of those; candidates the launcher
+ * rejects are skipped. Synchronous; overwrites C. The chosen knobs move work between CTAs
+ * only, except chunk_k and split_k, which change the summation order of every output the
+ * same way at any offload ratio. */
 dak_status dak_tune_gemm(const dak_placement* A, const void* B, void* C, int N, int c_fp32, int reps,
                          const dak_tuning* base, dak_tune_result* out);
 

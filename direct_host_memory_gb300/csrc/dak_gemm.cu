@@ -826,7 +826,7 @@ static bool make_b_map(CUtensorMap* map, const void* B, int K, int N, int N_pad,
 
 constexpr int kSmemBudget = 216 * 1024;           // one CTA per SM
 constexpr int kSmemBudgetTwoPerSm = 108 * 1024;  // two CTAs per SM
-constexpr int kDefaultHostCtas = 32;
+constexpr int kDefaultHostCtas = 48;
 constexpr int kMaxBlockN = 256;          // hidden-state rows of one CTA's tile
 constexpr int kMaxWideN = 4 * kMaxBlockN;  // rows of one launch: a cluster of up to 4 CTAs shares A
 constexpr int kDefaultHostWindow = 4;

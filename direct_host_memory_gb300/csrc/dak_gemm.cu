@@ -826,7 +826,12 @@ static bool make_b_map(CUtensorMap* map, const void* B, int K, int N, int N_pad,
 
 constexpr int kSmemBudget = 216 * 1024;           // one CTA per SM
 constexpr int kSmemBudgetTwoPerSm = 108 * 1024;  // two CTAs per SM
+// Default cap on CTAs reading host tiles (the congestion cap of section 4.3.1). One CTA per
+// tile row: 48, measured best for the decode step (more host bytes in flight at once). Wide
+// B (clusters sharing tile rows): 32 CTAs, i.e. 32 / NC clusters, since there the HBM side
+// needs its SMs for the N_pad = 256 tensor work.
 constexpr int kDefaultHostCtas = 48;
+constexpr int kDefaultHostCtasWide = 32;
 constexpr int kMaxBlockN = 256;          // hidden-state rows of one CTA's tile
 constexpr int kMaxWideN = 4 * kMaxBlockN;  // rows of one launch: a cluster of up to 4 CTAs shares A
 constexpr int kDefaultHostWindow = 4;
@@ -1048,11 +1053,12 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
     // schedule in cluster units; a role's units are its tile rows x P pieces
     dak_tuning tc{};
     if (t) tc = *t;
-    tc.host_ctas = std::max(1, (tc.host_ctas > 0 ? tc.host_ctas : kDefaultHostCtas) / CL);
+    const int host_cap = NC > 1 ? kDefaultHostCtasWide : kDefaultHostCtas;
+    tc.host_ctas = std::max(1, (tc.host_ctas > 0 ? tc.host_ctas : host_cap) / CL);
     if (tc.hbm_ctas > 0) tc.hbm_ctas = std::max(1, tc.hbm_ctas / CL);
     Sched sc = schedule(p.h * p.P, (p.T - p.h) * p.P, std::max(1, (sms * per_sm) / CL), &tc,
-                        std::max(1, kDefaultHostCtas / CL), std::min(kDefaultHostWindow, p.ch[1].stages),
-                        p.ch[0].stages, max_stages);
+                        std::max(1, host_cap / CL), std::min(kDefaultHostWindow, p.ch[1].stages), p.ch[0].stages,
+                        max_stages);
     p.n_host_ctas = sc.n_host_ctas;
     p.n_hbm_ctas = sc.n_hbm_ctas;
     p.host_window = std::min(sc.host_window, p.ch[1].stages);

@@ -1044,8 +1044,10 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
     const int smem = rings + (umma ? 1024 : 0);
     const int max_stages = std::max(p.ch[0].stages, p.ch[1].stages);
 
-    // pieces per tile row (tensor-core path, one CTA per tile row's columns)
-    if (umma && NC == 1) {
+    // pieces per tile row (tensor-core path, one CTA per tile row's columns; automatic only
+    // while the tile rows are memory-bound, N_pad <= 128: at N_pad = 256 the tensor work of a
+    // tile row is what the split would spread, and the partial tiles cost more than it saves)
+    if (umma && NC == 1 && (p.N_pad <= 128 || (t && t->split_k > 0))) {
         p.P = split_pieces(p.T, p.K_pad, p.N_pad, sms * per_sm, t);
         if (p.P > 1 && !split_workspace(&p.part, &p.cnt)) return DAK_ERR_CUDA;
     }

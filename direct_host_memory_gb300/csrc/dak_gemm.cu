@@ -457,7 +457,7 @@ __device__ __forceinline__ void issue_mmas(uint32_t d_tmem, uint64_t ad0, uint64
 }
 
 constexpr int kMaxPieces = 8;       // pieces per tile row
-constexpr int kMinPieceSteps = 16;  // 64-column steps of an automatically chosen piece
+constexpr int kMinPieceSteps = 8;   // 64-column steps of an automatically chosen piece
 
 // C[n][row] for the 8 hidden-state rows n_base .. n_base + 7 of one output row (n < N only),
 // fp32 or bf16. With a SwiGLU placement, rows 2j (gate) and 2j + 1 (up) are held by lanes l
@@ -903,12 +903,16 @@ static bool split_workspace(float** part, int** cnt) {
 // Pieces per tile row: the split of each tile row's K range into P parts (at multiples of
 // 64 columns), chosen from the shape and the SM count only, never from the placement, so
 // that results are bit-identical across offload ratios. Automatic: the P in 1..8 that
-// minimises what the busiest CTA streams, ceil(T P / slots) / P tile rows, if it saves at
-// least 3% over a smaller P. Pieces keep >= 1024 columns: a piece costs its CTA about a
-// microsecond of epilogue (partial tile out, count, and for the last piece the sum), which
-// shorter pieces cannot hide. The workspace must hold the partials.
+// minimises the busiest CTA's time, ceil(T P / slots) waves of (1 / P of a tile row's bytes
+// plus the fixed cost of a piece), if it saves at least 3% over a smaller P. The fixed cost,
+// about 1.5 us of a CTA streaming at about 62 GB/s (measured on this GPU: the partial tile,
+// the count, the last piece's sum, and a ragged last chunk), is kPieceCostBytes; an unsplit
+// tile row pays half of it (its epilogue stores C only). Pieces keep at least 512 columns
+// and the workspace must hold the partials.
 // tuning.split_k > 0 fixes P (1 = no split).
-static int split_pieces(int T, int K_pad, int N_pad, int slots, const dak_tuning* t) {
+constexpr double kPieceCostBytes = 1.5e-6 * 62.5e9;
+
+static int split_pieces(int T, int K_pad, int N_pad, int slots, long long tile_bytes, const dak_tuning* t) {
     const int steps = (K_pad + 63) / 64;
     auto fits = [&](int P) {
         return P <= steps && T <= kSplitTiles &&
@@ -919,7 +923,11 @@ static int split_pieces(int T, int K_pad, int N_pad, int slots, const dak_tuning
         while (P > 1 && !fits(P)) --P;
         return P;
     }
-    auto cost = [&](int P) { return static_cast<double>((static_cast<long long>(T) * P + slots - 1) / slots) / P; };
+    const double c = kPieceCostBytes / static_cast<double>(tile_bytes);  // in tile rows
+    auto cost = [&](int P) {
+        const long long waves = (static_cast<long long>(T) * P + slots - 1) / slots;
+        return static_cast<double>(waves) * (1.0 / P + (P > 1 ? c : 0.5 * c));  // unsplit: the C store only
+    };
     int best = 1;
     for (int P = 2; P <= kMaxPieces; ++P) {
         if (!fits(P) || steps / P < kMinPieceSteps) break;
@@ -1048,7 +1056,7 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
     // while the tile rows are memory-bound, N_pad <= 128: at N_pad = 256 the tensor work of a
     // tile row is what the split would spread, and the partial tiles cost more than it saves)
     if (umma && NC == 1 && (p.N_pad <= 128 || (t && t->split_k > 0))) {
-        p.P = split_pieces(p.T, p.K_pad, p.N_pad, sms * per_sm, t);
+        p.P = split_pieces(p.T, p.K_pad, p.N_pad, sms * per_sm, p.tile_bytes, t);
         if (p.P > 1 && !split_workspace(&p.part, &p.cnt)) return DAK_ERR_CUDA;
     }
 

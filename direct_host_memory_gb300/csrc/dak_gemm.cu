@@ -902,17 +902,21 @@ static bool split_workspace(float** part, int** cnt) {
 
 // Pieces per tile row: the split of each tile row's K range into P parts (at multiples of
 // 64 columns), chosen from the shape and the SM count only, never from the placement, so
-// that results are bit-identical across offload ratios. Automatic: the P in 1..8 that
-// minimises the busiest CTA's time, ceil(T P / slots) waves of (1 / P of a tile row's bytes
-// plus the fixed cost of a piece), if it saves at least 3% over a smaller P. The fixed cost,
-// about 1.5 us of a CTA streaming at about 62 GB/s (measured on this GPU: the partial tile,
-// the count, the last piece's sum, and a ragged last chunk), is kPieceCostBytes; an unsplit
-// tile row pays half of it (its epilogue stores C only). Pieces keep at least 512 columns
-// and the workspace must hold the partials.
+// that results are bit-identical across offload ratios. Automatic, in two steps:
+//  1. the all-HBM cost of each P in 1..8: the busiest CTA's time, ceil(T P / slots) waves of
+//     (1 / P of a tile row's bytes plus the fixed cost of a piece). The fixed cost is
+//     max(1, N_pad / 16) us of a CTA streaming at about 62 GB/s, fitted to decode steps on
+//     this GPU: the partial tile (64 x N_pad fp32), the count, the last piece's sum, and a
+//     ragged last chunk. An unsplit tile row pays half of it (its epilogue stores C only).
+//  2. among the P within 3% of the lowest cost, the smallest whose pieces give a host part
+//     of a tenth of the tile rows at least as many units as the host CTA cap (a small host
+//     part spread over more CTAs keeps more host bytes in flight), else the cheapest.
+// Pieces keep at least 512 columns and the workspace must hold the partials.
 // tuning.split_k > 0 fixes P (1 = no split).
-constexpr double kPieceCostBytes = 1.5e-6 * 62.5e9;
+constexpr double kCtaStreamBytesPerUs = 62.5e3;
 
-static int split_pieces(int T, int K_pad, int N_pad, int slots, long long tile_bytes, const dak_tuning* t) {
+static int split_pieces(int T, int K_pad, int N_pad, int slots, long long tile_bytes, int host_cap,
+                        const dak_tuning* t) {
     const int steps = (K_pad + 63) / 64;
     auto fits = [&](int P) {
         return P <= steps && T <= kSplitTiles &&
@@ -923,17 +927,22 @@ static int split_pieces(int T, int K_pad, int N_pad, int slots, long long tile_b
         while (P > 1 && !fits(P)) --P;
         return P;
     }
-    const double c = kPieceCostBytes / static_cast<double>(tile_bytes);  // in tile rows
-    auto cost = [&](int P) {
+    const double c = std::max(1.0, N_pad / 16.0) * kCtaStreamBytesPerUs / static_cast<double>(tile_bytes);
+    double cost[kMaxPieces + 1] = {};
+    int top = 1;
+    for (int P = 1; P <= kMaxPieces; ++P) {
+        if (P > 1 && (!fits(P) || steps / P < kMinPieceSteps)) break;
         const long long waves = (static_cast<long long>(T) * P + slots - 1) / slots;
-        return static_cast<double>(waves) * (1.0 / P + (P > 1 ? c : 0.5 * c));  // unsplit: the C store only
-    };
-    int best = 1;
-    for (int P = 2; P <= kMaxPieces; ++P) {
-        if (!fits(P) || steps / P < kMinPieceSteps) break;
-        if (cost(P) < 0.97 * cost(best)) best = P;
+        cost[P] = static_cast<double>(waves) * (1.0 / P + (P > 1 ? c : 0.5 * c));
+        top = P;
     }
-    return best;
+    int cheapest = 1;
+    for (int P = 2; P <= top; ++P)
+        if (cost[P] < cost[cheapest]) cheapest = P;
+    const int h_small = (T + 9) / 10;
+    for (int P = 1; P <= top; ++P)
+        if (cost[P] <= 1.03 * cost[cheapest] && h_small * P >= host_cap) return P;
+    return cheapest;
 }
 
 void reset_split_counters() {
@@ -1056,7 +1065,7 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
     // while the tile rows are memory-bound, N_pad <= 128: at N_pad = 256 the tensor work of a
     // tile row is what the split would spread, and the partial tiles cost more than it saves)
     if (umma && NC == 1 && (p.N_pad <= 128 || (t && t->split_k > 0))) {
-        p.P = split_pieces(p.T, p.K_pad, p.N_pad, sms * per_sm, p.tile_bytes, t);
+        p.P = split_pieces(p.T, p.K_pad, p.N_pad, sms * per_sm, p.tile_bytes, kDefaultHostCtas, t);
         if (p.P > 1 && !split_workspace(&p.part, &p.cnt)) return DAK_ERR_CUDA;
     }
 

@@ -165,7 +165,7 @@ dak_status dak_placement_info(const dak_placement* p, int64_t* host_bytes, int64
  * that the CTAs of its tier share; partial tiles go through a device workspace and the
  * CTA finishing a tile row's last piece adds them in piece order. Every output row is
  * accumulated in fp32 in an order fixed by the shape and the SM count alone, so the result
- * does not depend on n_host_tiles. N < 8 runs on CUDA cores; N >= 8 on the tcgen05 tensor
+ * does not depend on n_host_tiles. N = 1 runs on CUDA cores; N >= 2 on the tcgen05 tensor
  * cores. Launches that split tile rows share the workspace: do not run them concurrently
  * on different streams of one device. */
 dak_status dak_gemm(const dak_placement* A, const void* B, void* C, int N, int c_fp32, const dak_tuning* tuning,

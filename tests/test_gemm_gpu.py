@@ -99,7 +99,7 @@ def test_bit_identical_across_tuning(dak, N):
     for tun in [dict(host_ctas=1), dict(host_ctas=3, window=1), dict(window=2, hbm_window=2), dict(hbm_ctas=3)]:
         assert np.array_equal(bits_of(_run(dak, A, B, 4, tuning=tun)), base), tun
     ref = og.gemm_ref(A, B)
-    chunks = [dict(chunk_k=256), dict(chunk_k=512)] if N < 8 else \
+    chunks = [dict(chunk_k=256), dict(chunk_k=512)] if N == 1 else \
         [dict(chunk_k=64), dict(chunk_k=128, split_k=1), dict(chunk_k=256, split_k=2)]
     for tun in chunks:
         assert og.rel_err(to_np(_run(dak, A, B, 4, tuning=tun)), ref) <= FP32_OUT_TOL, tun
@@ -119,6 +119,29 @@ def test_split_pieces(dak, N, S):
     assert og.rel_err(to_np(base), ref) <= FP32_OUT_TOL
     for h in (1, 3, 6):
         assert np.array_equal(bits_of(_run(dak, A, B, h, tuning=tun)), bits_of(base)), h
+
+
+@pytest.mark.parametrize("N", [2, 3, 5, 7])
+def test_small_n_on_tensor_cores(dak, N):
+    """N = 2..7 runs on the tensor cores with B padded to 8 rows (zero-filled by the tensor
+    map): matches the oracle, writes only the N real rows of C, and keeps its bits across
+    offload ratios; ragged M and K."""
+    import torch
+    M, K = 328, 1000
+    A, B = synth.gemm_inputs(M, K, N, seed=60 + N)
+    ref = og.gemm_ref(A, B)
+    base = _run(dak, A, B, 0)
+    assert base.shape == (N, M)
+    assert og.rel_err(to_np(base), ref) <= FP32_OUT_TOL
+    for h in (1, 3, 6):
+        assert np.array_equal(bits_of(_run(dak, A, B, h)), bits_of(base)), h
+    C = torch.full((N + 1, M), 7.0, device="cuda")  # one guard row past the N rows of C
+    p = dak.dak_place_matrix(A, 2)
+    dak.dak_gemm(p, to_dev(B), C[:N], c_fp32=True)
+    assert dak.dak_last_error()[0] == 0
+    assert torch.all(C[N] == 7.0)
+    assert og.rel_err(to_np(C[:N]), ref) <= FP32_OUT_TOL
+    p.free()
 
 
 @pytest.mark.parametrize("K", [1000, 1040, 4096 + 16])

@@ -51,6 +51,7 @@ struct GemmParams {
     DevStatus* st;
     int b3d;      // B arrives in one 3-D tensor copy per stage (else several 2-D copies)
     int P;        // pieces per tile row: its K range is cut into P parts, each a unit of work
+    int pstep;    // piece boundaries fall on multiples of this many columns (a B block: 64, 256)
     float* part;  // P > 1: fp32 partial tiles [T][P][64 rows][N_pad]
     int* cnt;     // P > 1: per tile row, pieces finished so far (back to 0 after the last)
     int NC;       // CTAs per cluster sharing each tile row across 256-row blocks of B (1 = off)
@@ -105,7 +106,8 @@ __device__ __forceinline__ TileIter tiles_of_cta(const GemmParams& p) {
 }
 
 // The ui-th unit of a CTA: tile row t and its K range [k0, k1). A tile row's K range is cut
-// into P pieces at multiples of 64 columns, from the shape only.
+// into P pieces at multiples of pstep columns (one block of the B layout, so that every chunk
+// starts on a block), from the shape only.
 struct Piece {
     int t, idx, k0, k1;
 };
@@ -115,9 +117,9 @@ __device__ __forceinline__ Piece piece_of(const GemmParams& p, const TileIter& i
     Piece q;
     q.t = it.tile0 + u / p.P;
     q.idx = u % p.P;
-    const int steps = (p.K_pad + 63) >> 6;
-    q.k0 = (q.idx * steps / p.P) << 6;
-    q.k1 = min(((q.idx + 1) * steps / p.P) << 6, p.K_pad);
+    const int steps = (p.K_pad + p.pstep - 1) / p.pstep;
+    q.k0 = (q.idx * steps / p.P) * p.pstep;
+    q.k1 = min(((q.idx + 1) * steps / p.P) * p.pstep, p.K_pad);
     return q;
 }
 
@@ -129,7 +131,7 @@ __device__ __forceinline__ const uint8_t* tile_src(const GemmParams& p, const Ti
 // error location codes (upper 32 bits of the status info)
 enum : uint32_t {
     W_PROD_EMPTY = 1, W_CONS_FULL = 2, W_MMA_FULL = 3, W_MMA_ACC = 4, W_EPI_ACC = 5, W_DRAIN = 6, W_BPROD_EMPTY = 7,
-    W_FWD_FULL = 10, W_FWD_PEER = 11, W_ARM_EMPTY = 12
+    W_FWD_FULL = 10, W_FWD_PEER = 11, W_ARM_EMPTY = 12, W_FIN_DONE = 13, W_FIN_FREED = 14
 };
 
 // Wait (bounded, ignoring the abort flag) for the last fill of every ring slot, so that no
@@ -300,16 +302,64 @@ done:
 
 // ======================================================================================
 // CUDA-core path, N = 1 (a GEMV): warp-level FMA, fp32 accumulation, shuffle reduction.
-// Warps: 0 = A producer, 1 = B producer, 2..9 = consumers (consumer w owns rows 8w .. 8w+7).
+// Warps: 0 = A producer, 1 = B producer, 2..9 = consumers (consumer w owns rows 8w .. 8w+7),
+// 10 = finisher of split tile rows. With P > 1 the consumers store each piece's partial rows
+// and move on; the finisher counts the piece in (one acquire-release atomic per piece) and,
+// for a tile row's last piece, adds the P partials in piece order and writes C, so the
+// count's round trip never stalls the FMA stream.
 // ======================================================================================
 constexpr int kCoreConsumers = 8;
-constexpr int kCoreThreads = 32 * (2 + kCoreConsumers);
+constexpr int kCoreThreads = 32 * (3 + kCoreConsumers);
+constexpr int kCoreDone = 4;  // units a finisher may lag behind the consumers
+
+// GPU-scope atomic add with acquire and release semantics; returns the old value.
+__device__ __forceinline__ int atomic_add_acq_rel(int* addr, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+    return old;
+}
+
+// C[n][row] for n < N of one output row (fp32 or bf16). With a SwiGLU placement, rows 2j
+// (gate) and 2j + 1 (up) are held by lanes l and l ^ 1; the even lane writes C[n][j] =
+// silu(gate) * up (C has M / 2 columns). Every lane of the warp calls this.
+template <int N>
+__device__ __forceinline__ void store_row(const GemmParams& p, const float (&acc)[N], int row, bool write) {
+    if (p.glu) {
+        float up[N];
+#pragma unroll
+        for (int n = 0; n < N; ++n) up[n] = __shfl_xor_sync(0xffffffffu, acc[n], 1);
+        if (write && row < p.M && !(row & 1)) {
+            const int half = p.M >> 1, col = row >> 1;
+#pragma unroll
+            for (int n = 0; n < N; ++n) {
+                const float a = swiglu_pair(acc[n], up[n]);
+                if (p.c_fp32) {
+                    reinterpret_cast<float*>(p.C)[static_cast<long long>(n) * half + col] = a;
+                } else {
+                    reinterpret_cast<__nv_bfloat16*>(p.C)[static_cast<long long>(n) * half + col] =
+                        __float2bfloat16_rn(a);
+                }
+            }
+        }
+    } else if (write && row < p.M) {
+#pragma unroll
+        for (int n = 0; n < N; ++n) {
+            if (p.c_fp32) {
+                reinterpret_cast<float*>(p.C)[static_cast<long long>(n) * p.M + row] = acc[n];
+            } else {
+                reinterpret_cast<__nv_bfloat16*>(p.C)[static_cast<long long>(n) * p.M + row] =
+                    __float2bfloat16_rn(acc[n]);
+            }
+        }
+    }
+}
 
 template <int N>
 __global__ void __launch_bounds__(kCoreThreads, 1)
     gemm_core_kernel(const GemmParams p, const __grid_constant__ CUtensorMap bmap) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     __shared__ uint64_t full[8], empty[8];
+    __shared__ uint64_t done[kCoreDone], freed[kCoreDone];  // split: partial rows stored / finisher done
     __shared__ int abort_flag;
     volatile int* abort = &abort_flag;
 
@@ -324,6 +374,10 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
             mbar_init(&full[s], 2);  // A producer + B producer
             mbar_init(&empty[s], kCoreConsumers);
         }
+        for (int j = 0; j < kCoreDone; ++j) {
+            mbar_init(&done[j], kCoreConsumers);
+            mbar_init(&freed[j], 1);
+        }
         fence_mbar_init();
         prefetch_tmap(&bmap);
     }
@@ -334,6 +388,45 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
         if (lane == 0) produce(p, it, &bmap, smem, full, empty, abort, warp == 0, kCoreB);
         return;
     }
+    const int tile_floats = kTileM * p.N_pad;  // one partial tile in the split workspace
+    if (warp == 2 + kCoreConsumers) {
+        if (p.P == 1) return;
+        // finisher: lane l sums rows l and l + 32 of a tile row whose last piece this CTA ran
+        grid_dep_wait();  // the split workspace may still be in use by the previous kernel
+        for (int ui = 0; ui < it.count; ++ui) {
+            const int j = ui % kCoreDone;
+            if (!mbar_wait(&done[j], static_cast<uint32_t>((ui / kCoreDone) & 1), abort, p.st, DAK_ERR_TIMEOUT,
+                           W_FIN_DONE)) {
+                return;
+            }
+            const Piece pc = piece_of(p, it, ui);
+            int last = 0;
+            if (lane == 0) {
+                __threadfence();
+                last = atomic_add_acq_rel(p.cnt + pc.t, 1) + 1 == p.P;
+                if (last) p.cnt[pc.t] = 0;  // ready for the next launch
+            }
+            last = __shfl_sync(0xffffffffu, last, 0);
+            __syncwarp();
+            if (last) {
+                const float* src = p.part + static_cast<long long>(pc.t) * p.P * tile_floats;
+                for (int h = 0; h < 2; ++h) {
+                    const int rr = lane + 32 * h;
+                    float acc[N];
+#pragma unroll
+                    for (int n = 0; n < N; ++n) {
+                        float v = __ldcg(src + rr * p.N_pad + n);
+                        for (int r = 1; r < p.P; ++r) v += __ldcg(src + static_cast<long long>(r) * tile_floats + rr * p.N_pad + n);
+                        acc[n] = v;
+                    }
+                    store_row<N>(p, acc, pc.t * kTileM + rr, true);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&freed[j]);
+        }
+        return;
+    }
 
     // consumers (C may be read by the previous kernel of the stream: wait before writing it)
     grid_dep_wait();
@@ -342,7 +435,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
     const int kq = lane >> 3;     // k-group phase 0..3
     long long i = 0;
     for (int ui = 0; ui < it.count; ++ui) {
-        const Piece q = piece_of(p, it, ui);  // the CUDA-core path never splits a tile row (P = 1)
+        const Piece q = piece_of(p, it, ui);
         const int t = q.t;
         float acc[N];
 #pragma unroll
@@ -388,35 +481,23 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
             acc[n] = v;
         }
         const int row = t * kTileM + w * 8 + r;
-        if (p.glu) {
-            // rows 2j (gate) and 2j + 1 (up) are lanes r and r ^ 1 of this group
-            float up[N];
-#pragma unroll
-            for (int n = 0; n < N; ++n) up[n] = __shfl_xor_sync(0xffffffffu, acc[n], 1);
-            if (kq == 0 && row < p.M && !(row & 1)) {
-                const int half = p.M >> 1, col = row >> 1;
-#pragma unroll
-                for (int n = 0; n < N; ++n) {
-                    const float a = swiglu_pair(acc[n], up[n]);
-                    if (p.c_fp32) {
-                        reinterpret_cast<float*>(p.C)[static_cast<long long>(n) * half + col] = a;
-                    } else {
-                        reinterpret_cast<__nv_bfloat16*>(p.C)[static_cast<long long>(n) * half + col] =
-                            __float2bfloat16_rn(a);
-                    }
-                }
-            }
-        } else if (kq == 0 && row < p.M) {
-#pragma unroll
-            for (int n = 0; n < N; ++n) {
-                if (p.c_fp32) {
-                    reinterpret_cast<float*>(p.C)[static_cast<long long>(n) * p.M + row] = acc[n];
-                } else {
-                    reinterpret_cast<__nv_bfloat16*>(p.C)[static_cast<long long>(n) * p.M + row] =
-                        __float2bfloat16_rn(acc[n]);
-                }
-            }
+        if (p.P == 1) {
+            store_row<N>(p, acc, row, kq == 0);
+            continue;
         }
+        // split tile row: this unit's partial rows to the workspace, then tell the finisher
+        if (kq == 0) {
+            float* mine = p.part + (static_cast<long long>(t) * p.P + q.idx) * tile_floats + (w * 8 + r) * p.N_pad;
+#pragma unroll
+            for (int n = 0; n < N; ++n) mine[n] = acc[n];
+        }
+        __syncwarp();
+        const int j = ui % kCoreDone;
+        if (ui >= kCoreDone && !mbar_wait(&freed[j], static_cast<uint32_t>(((ui / kCoreDone) - 1) & 1), abort, p.st,
+                                          DAK_ERR_TIMEOUT, W_FIN_FREED)) {
+            return;
+        }
+        if (lane == 0) mbar_arrive(&done[j]);
     }
 }
 
@@ -498,13 +579,6 @@ __device__ __forceinline__ void store_c(const GemmParams& p, const float (&f)[8]
             }
         }
     }
-}
-
-// Atomic add at GPU scope with acquire and release semantics; returns the old value.
-__device__ __forceinline__ int atomic_add_acq_rel(int* addr, int v) {
-    int old;
-    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
-    return old;
 }
 
 // The 128 threads of the four epilogue warps meet (named barrier 1; barrier 0 is __syncthreads).
@@ -904,10 +978,12 @@ static bool split_workspace(float** part, int** cnt) {
 // 64 columns), chosen from the shape and the SM count only, never from the placement, so
 // that results are bit-identical across offload ratios. Automatic, in two steps:
 //  1. the all-HBM cost of each P in 1..8: the busiest CTA's time, ceil(T P / slots) waves of
-//     (1 / P of a tile row's bytes plus the fixed cost of a piece). The fixed cost is
-//     max(1, N_pad / 16) us of a CTA streaming at about 62 GB/s, fitted to decode steps on
-//     this GPU: the partial tile (64 x N_pad fp32), the count, the last piece's sum, and a
-//     ragged last chunk. An unsplit tile row pays half of it (its epilogue stores C only).
+//     (1 / P of a tile row's bytes plus the fixed cost of a piece). The fixed cost, piece_us
+//     of a CTA streaming at about 62 GB/s, is fitted to decode steps on this GPU: on the
+//     tensor cores max(1, N_pad / 16) us (the partial tile of 64 x N_pad fp32, the count,
+//     the last piece's sum, a ragged last chunk), on the CUDA cores 2 us (there the
+//     consumers that run the FMAs also store the partial rows). An unsplit tile row pays
+//     half of it (its epilogue stores C only).
 //  2. among the P within 3% of the lowest cost, the smallest whose pieces give a host part
 //     of a tenth of the tile rows at least as many units as the host CTA cap (a small host
 //     part spread over more CTAs keeps more host bytes in flight), else the cheapest.
@@ -915,11 +991,11 @@ static bool split_workspace(float** part, int** cnt) {
 // tuning.split_k > 0 fixes P (1 = no split).
 constexpr double kCtaStreamBytesPerUs = 62.5e3;
 
-static int split_pieces(int T, int K_pad, int N_pad, int slots, long long tile_bytes, int host_cap,
-                        const dak_tuning* t) {
+static int split_pieces(int T, int K_pad, int N_pad, int slots, long long tile_bytes, int host_cap, int pstep,
+                        double piece_us, const dak_tuning* t) {
     const int steps = (K_pad + 63) / 64;
     auto fits = [&](int P) {
-        return P <= steps && T <= kSplitTiles &&
+        return P <= (K_pad + pstep - 1) / pstep && T <= kSplitTiles &&
                static_cast<long long>(T) * P * kTileM * N_pad <= kSplitFloats;
     };
     if (t && t->split_k > 0) {
@@ -927,7 +1003,7 @@ static int split_pieces(int T, int K_pad, int N_pad, int slots, long long tile_b
         while (P > 1 && !fits(P)) --P;
         return P;
     }
-    const double c = std::max(1.0, N_pad / 16.0) * kCtaStreamBytesPerUs / static_cast<double>(tile_bytes);
+    const double c = piece_us * kCtaStreamBytesPerUs / static_cast<double>(tile_bytes);  // in tile rows
     double cost[kMaxPieces + 1] = {};
     int top = 1;
     for (int P = 1; P <= kMaxPieces; ++P) {
@@ -982,6 +1058,7 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
     p.tile_bytes = A->tile_bytes;
     p.glu = A->glu;
     p.P = 1;
+    p.pstep = N >= 2 ? 64 : 256;  // the B block of the tensor-core / CUDA-core layout
     p.st = status_ptr();
     if (!p.st) return DAK_ERR_CUDA;
 
@@ -1061,11 +1138,12 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
     const int smem = rings + (umma ? 1024 : 0);
     const int max_stages = std::max(p.ch[0].stages, p.ch[1].stages);
 
-    // pieces per tile row (tensor-core path, one CTA per tile row's columns; automatic only
-    // while the tile rows are memory-bound, N_pad <= 128: at N_pad = 256 the tensor work of a
-    // tile row is what the split would spread, and the partial tiles cost more than it saves)
-    if (umma && NC == 1 && (p.N_pad <= 128 || (t && t->split_k > 0))) {
-        p.P = split_pieces(p.T, p.K_pad, p.N_pad, sms * per_sm, p.tile_bytes, kDefaultHostCtas, t);
+    // pieces per tile row (one CTA per tile row's columns; automatic only while the tile
+    // rows are memory-bound, N_pad <= 128: at N_pad = 256 the tensor work of a tile row is
+    // what the split would spread, and the partial tiles cost more than it saves)
+    if (NC == 1 && (p.N_pad <= 128 || (t && t->split_k > 0))) {
+        const double piece_us = umma ? std::max(1.0, p.N_pad / 16.0) : 2.0;
+        p.P = split_pieces(p.T, p.K_pad, p.N_pad, sms * per_sm, p.tile_bytes, kDefaultHostCtas, p.pstep, piece_us, t);
         if (p.P > 1 && !split_workspace(&p.part, &p.cnt)) return DAK_ERR_CUDA;
     }
 

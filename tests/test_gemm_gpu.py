@@ -105,7 +105,7 @@ def test_bit_identical_across_tuning(dak, N):
         assert og.rel_err(to_np(_run(dak, A, B, 4, tuning=tun)), ref) <= FP32_OUT_TOL, tun
 
 
-@pytest.mark.parametrize("N", [8, 32, 64])
+@pytest.mark.parametrize("N", [1, 8, 32, 64])
 @pytest.mark.parametrize("S", [1, 2, 3, 4, 8])
 def test_split_pieces(dak, N, S):
     """Each tile row's K range cut into S pieces that any CTA may take; the CTA finishing a
@@ -144,11 +144,13 @@ def test_small_n_on_tensor_cores(dak, N):
     p.free()
 
 
+@pytest.mark.parametrize("N", [1, 24])
 @pytest.mark.parametrize("K", [1000, 1040, 4096 + 16])
-def test_split_pieces_ragged_k(dak, K):
+def test_split_pieces_ragged_k(dak, K, N):
     """Pieces end at multiples of 64 columns except the last, which ends at K rounded up to 16;
-    few CTAs (hbm_ctas, host_ctas) so that one CTA takes several pieces of one tile row."""
-    M, N = 200, 24
+    few CTAs (hbm_ctas, host_ctas) so that one CTA takes several pieces of one tile row (on
+    the CUDA-core path, more units per CTA than the finisher's lag of four)."""
+    M = 200
     A, B = synth.gemm_inputs(M, K, N, seed=K)
     ref = og.gemm_ref(A, B)
     for S in (2, 5, 8):
@@ -342,10 +344,12 @@ def test_glu_placement_fused_swiglu(dak, N):
         p = dak.dak_place_matrix_glu(A, h)
         C = dak.dak_gemm(p, to_dev(B), c_fp32=True)
         C16 = dak.dak_gemm(p, to_dev(B), c_fp32=False)
+        C3 = dak.dak_gemm(p, to_dev(B), c_fp32=True, tuning=dict(split_k=3))  # summed by the last piece
         assert dak.dak_last_error()[0] == 0
         assert tuple(C.shape) == (N, f)
         assert og.rel_err(to_np(C), ref) <= FP32_OUT_TOL, h
         assert og.rel_err(to_np(C16), ref) <= REL_TOL, h
+        assert og.rel_err(to_np(C3), ref) <= FP32_OUT_TOL, h
         outs.append(bits_of(C))
         p.free()
     for o in outs[1:]:

@@ -489,6 +489,45 @@ def run_large_n(dak, lin, b_host, b_hbm, dev, x=0.25):
             "status": dak.dak_last_error()[0]}
 
 
+# ------------------------------------------------------------------------------ hidden-state rows
+
+def run_linears_n(dak, lin, b_host, b_hbm, dev, xs=(0.0, 0.25), ns=(1, 8, 32, 64)):
+    """The four 8B linears (QKV, O, gate+up, down: 436 MB, more than L2) as one graph of four
+    dak_gemm launches, at each offload ratio in xs and each hidden-state row count N in ns
+    (the batch sizes of the survey's linear configuration): time per pass, effective GB/s
+    and the fraction of the tier roofline."""
+    import torch
+    import synth
+    rows = []
+    for x in xs:
+        pls = {n: dak.dak_place_matrix(A, dak.host_tiles_for_ratio(x, A.shape[0])) for n, (A, _) in lin.items()}
+        C_bytes = sum(p.host_bytes + p.hbm_bytes for p in pls.values())
+        H = sum(p.host_bytes for p in pls.values())
+        for N in ns:
+            Bs = {n: torch.from_numpy(synth.normal_bf16(11, i, N * A.shape[1]).view("int16")).view(torch.bfloat16)
+                  .to(dev).view(N, A.shape[1]) for i, (n, (A, _)) in enumerate(lin.items())}
+            Cs = {n: torch.empty((N, A.shape[0]), dtype=torch.bfloat16, device=dev) for n, (A, _) in lin.items()}
+
+            def one_pass():
+                for n, p in pls.items():
+                    dak.dak_gemm(p, Bs[n], Cs[n], tuning=dict(pdl=1))
+            one_pass()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                with torch.cuda.graph(g, stream=s):
+                    one_pass()
+            t = time_steps(g.replay, 20, 3)
+            roof = tier_roofline(C_bytes, H / C_bytes, b_host, b_hbm)
+            rows.append({"N": N, "x": x, "us": t * 1e6, "gbps": C_bytes / t / 1e9, "frac": (C_bytes / t) / roof})
+            del g
+        for p in pls.values():
+            p.free()
+    return {"ops": "8B QKV, O, gate+up, down (one graph of four launches)", "rows": rows,
+            "status": dak.dak_last_error()[0]}
+
+
 # ------------------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -882,6 +921,7 @@ def main():
         pc_sampler.stop()
         planner_check["clocks"] = pc_sampler.summary(tw0, tw1)  # tensor-bound timings follow the SM clock
     large_n = None if args.no_planner_check else run_large_n(dak, lin, b_host, b_hbm, dev)
+    per_n = None if args.no_sweep else run_linears_n(dak, lin, b_host, b_hbm, dev)
 
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -920,6 +960,8 @@ def main():
         line["planner_check"] = planner_check
     if large_n:
         line["large_n"] = large_n
+    if per_n:
+        line["per_n"] = per_n
     if cpu:
         line["cpu_baseline"] = cpu
     st.free()

@@ -1086,9 +1086,20 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
                 break;
             }
         }
+    } else if (p.N_pad <= 128) {
+        // the widest chunk (up to 512 columns, 64 KiB of A) of which two stages fit: per-chunk
+        // costs dominate a CTA's stream, so two wide stages beat three narrow ones (measured:
+        // N = 64 at 384 columns 15% faster than at 256, N = 128 at 256 columns 25% faster
+        // than at 128)
+        kc = 64;
+        for (int cand : {512, 448, 384, 320, 256, 192, 128}) {
+            if (2 * stage_of(cand) + 1024 <= budget) {
+                kc = cand;
+                break;
+            }
+        }
     } else {
-        // 64 KiB A copies where two such stages fit, 32 KiB otherwise
-        kc = p.N_pad <= 32 ? 512 : (p.N_pad <= 64 ? 256 : (p.N_pad <= 128 ? 128 : 64));
+        kc = 64;
     }
     if (kc % 64 != 0 || kc > 1024 || (!umma && kc % 256 != 0)) return DAK_ERR_INVALID;
     // Ring layouts. Shared tile rows (NC > 1): A in 256-column chunks and B through its own

@@ -1086,11 +1086,11 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
                 break;
             }
         }
-    } else if (p.N_pad <= 128) {
+    } else {
         // the widest chunk (up to 512 columns, 64 KiB of A) of which two stages fit: per-chunk
-        // costs dominate a CTA's stream, so two wide stages beat three narrow ones (measured:
-        // N = 64 at 384 columns 15% faster than at 256, N = 128 at 256 columns 25% faster
-        // than at 128)
+        // costs dominate a CTA's stream, so two wide stages beat three narrow ones (measured
+        // at x = 0: N = 64 at 384 columns 15% faster than at 256, N = 128 at 256 columns 25%
+        // faster than at 128, N = 256 at 128 columns 30% faster than at 64)
         kc = 64;
         for (int cand : {512, 448, 384, 320, 256, 192, 128}) {
             if (2 * stage_of(cand) + 1024 <= budget) {
@@ -1098,17 +1098,16 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
                 break;
             }
         }
-    } else {
-        kc = 64;
     }
     if (kc % 64 != 0 || kc > 1024 || (!umma && kc % 256 != 0)) return DAK_ERR_INVALID;
     // Ring layouts. Shared tile rows (NC > 1): A in 256-column chunks and B through its own
     // ring of 64-column chunks, so that A copies and forwards stay large while B fills the
-    // rest. One CTA per tile row with wide B (N_pad > 128): CTAs reading HBM keep the unified
-    // ring, which keeps more B in flight; CTAs reading host tiles take the split layout, whose
-    // 32 KiB A chunks keep more host bytes in flight (host reads are latency-bound).
+    // rest. One CTA per tile row: the unified ring for both tiers, except that with wide B
+    // (N_pad > 128) and 64-column chunks (only where two wider stages do not fit) CTAs
+    // reading host tiles take the split layout, whose 32 KiB A chunks keep more host bytes
+    // in flight (host reads are latency-bound).
     const bool b_ring_all = umma && NC > 1;
-    const bool b_ring_host = umma && p.N_pad > 128 && !(t && t->chunk_k > 0);
+    const bool b_ring_host = umma && p.N_pad > 128 && kc == 64 && !(t && t->chunk_k > 0);
     if (b_ring_all && !(t && t->chunk_k > 0)) kc = 256;
     // (NC > 1: each CTA holds 2 x 256 TMEM columns, the whole TMEM of an SM: one CTA per SM)
     const int CL = NC;  // CTAs per cluster

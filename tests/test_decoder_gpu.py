@@ -84,6 +84,8 @@ def _run(dak, dec, x0, pos, mode=0, graph=False):
 @pytest.mark.parametrize("cfg,B,L,pos", [
     (SMALL64, 5, 200, [0, 63, 64, 130, 199]),
     (SMALL128, 3, 300, [299, 0, 128]),
+    (SMALL64, 1, 200, [130]),        # batch 1: the linears run on the CUDA-core GEMV path
+    (SMALL128, 2, 300, [5, 299]),    # batch 2: tensor cores with B padded to 8 rows
 ])
 @pytest.mark.parametrize("frac", [0.0, 0.3, 1.0])
 def test_decoder_small_parity(dak, cfg, B, L, pos, frac):

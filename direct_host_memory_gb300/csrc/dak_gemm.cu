@@ -1161,7 +1161,11 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
     dak_tuning tc{};
     if (t) tc = *t;
     const int host_cap = NC > 1 ? kDefaultHostCtasWide : kDefaultHostCtas;
-    tc.host_ctas = std::max(1, (tc.host_ctas > 0 ? tc.host_ctas : host_cap) / CL);
+    int hc = tc.host_ctas > 0 ? tc.host_ctas : host_cap;
+    if (!(tc.host_ctas > 0) && CL == 1 && p.h * p.P > hc && 3 * p.h * p.P <= 4 * hc) {
+        hc = p.h * p.P;  // up to a third over the cap: one wave of host units rather than two
+    }
+    tc.host_ctas = std::max(1, hc / CL);
     if (tc.hbm_ctas > 0) tc.hbm_ctas = std::max(1, tc.hbm_ctas / CL);
     Sched sc = schedule(p.h * p.P, (p.T - p.h) * p.P, std::max(1, (sms * per_sm) / CL), &tc,
                         std::max(1, host_cap / CL), std::min(kDefaultHostWindow, p.ch[1].stages), p.ch[0].stages,

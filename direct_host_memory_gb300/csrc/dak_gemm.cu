@@ -357,7 +357,7 @@ __device__ __forceinline__ void store_row(const GemmParams& p, const float (&acc
 template <int N>
 __global__ void __launch_bounds__(kCoreThreads, 1)
     gemm_core_kernel(const GemmParams p, const __grid_constant__ CUtensorMap bmap) {
-    extern __shared__ __align__(128) uint8_t smem_raw[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];  // one declaration for both GEMM kernels
     __shared__ uint64_t full[8], empty[8];
     __shared__ uint64_t done[kCoreDone], freed[kCoreDone];  // split: partial rows stored / finisher done
     __shared__ int abort_flag;

@@ -207,7 +207,7 @@ static dak_status place_matrix(const void* A_src, int src_on_device, int64_t M, 
     if (!out) return DAK_ERR_INVALID;
     *out = nullptr;
     if (M < 0 || K <= 0 || lda < K || (M > 0 && !A_src)) return DAK_ERR_INVALID;
-    if (glu && (M % (2 * kTileM))) return DAK_ERR_INVALID;  // whole tiles of 32 gate + 32 up rows
+    if (glu && (M % kTileM)) return DAK_ERR_INVALID;  // whole tiles of 32 gate + 32 up rows
     if (tile_m != kTileM) return DAK_ERR_UNSUPPORTED;
     if ((K % 8) || (lda % 8) || (reinterpret_cast<uintptr_t>(A_src) & 15)) return DAK_ERR_ALIGN;
     if (K > (1 << 24) || M > (1ll << 31)) return DAK_ERR_INVALID;

@@ -49,6 +49,40 @@ def test_gemm_random(dak, case):
     assert og.rel_err(to_np(C), og.gemm_ref(A, B)) <= FP32_OUT_TOL, (M, K, N, h, tun)
 
 
+@pytest.mark.parametrize("case", range(24))
+def test_gemm_random_pieces(dak, case):
+    """Random shapes with an explicit piece count, few CTAs (so that a CTA takes several
+    pieces, also of one tile row) and, half of the time, the gate/up interleaved placement:
+    matches the oracle, and the fp32 result does not depend on the placement."""
+    from oracle import decoder as od
+    u = synth.uniform_f64(903, case, 8)
+    glu = u[0] < 0.5
+    M = 64 * (1 + int(u[1] * 14)) if glu else 1 + int(u[1] * 900)  # glu: f a multiple of 32
+    K = 8 * (1 + int(u[2] * 600))
+    N = _pick(u[3], [1, 2, 5, 8, 16, 40, 64, 128])
+    T = math.ceil(M / 64)
+    P = _pick(u[4], [2, 3, 4, 5, 7, 8])
+    tun = dict(split_k=P)
+    if u[5] < 0.5:
+        tun["hbm_ctas"] = 1 + int(u[6] * 6)
+        tun["host_ctas"] = 1 + int(u[7] * 3)
+    A, B = synth.gemm_inputs(M, K, N, seed=3000 + case)
+    ref = og.gemm_ref(A, B)
+    if glu:
+        ref = od.swiglu(ref, M // 2)
+    outs = []
+    for h in sorted({0, T // 3, T}):
+        p = dak.dak_place_matrix_glu(A, h) if glu else dak.dak_place_matrix(A, h)
+        C = dak.dak_gemm(p, to_dev(B), c_fp32=True, tuning=tun)
+        st, info = dak.dak_last_error()
+        p.free()
+        assert st == 0, (M, K, N, h, tun, glu, hex(info))
+        assert og.rel_err(to_np(C), ref) <= FP32_OUT_TOL, (M, K, N, h, tun, glu)
+        outs.append(to_np(C))
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0]), (M, K, N, tun, glu)
+
+
 @pytest.mark.parametrize("case", range(16))
 def test_attn_random(dak, case):
     import torch

@@ -29,7 +29,7 @@ EXPORTS = [
     "dak_gemm_staged", "dak_attn_staged", "dak_attn_noalloc", "dak_selftest_wait",
     "dak_decoder_create", "dak_decoder_batch", "dak_decoder_step", "dak_decoder_capture",
     "dak_decoder_replay", "dak_decoder_launches", "dak_decoder_free", "dak_tune_gemm", "dak_tune_attn",
-    "dak_place_matrix_glu", "dak_plan_units",
+    "dak_place_matrix_glu", "dak_plan_units", "dak_gemm_workspace_bytes", "dak_gemm_ws",
 ]
 
 # size of the fixed device array dak_attn_noalloc uses (DAK_NOALLOC_SCRATCH_BYTES in dak.h)
@@ -87,6 +87,8 @@ def _load():
         "dak_placement_info": (i32, [vp, P(i64), P(i64), P(i64), P(i64)]),
         "dak_gemm": (i32, [vp, vp, vp, i32, i32, P(dak_tuning), vp]),
         "dak_gemm_staged": (i32, [vp, vp, vp, vp, i32, i32, P(dak_tuning), vp]),
+        "dak_gemm_workspace_bytes": (sz, [vp, i32]),
+        "dak_gemm_ws": (i32, [vp, vp, vp, i32, i32, P(dak_tuning), vp, sz, vp]),
         "dak_attn_workspace_bytes": (sz, [i32, i32, i32, i32]),
         "dak_attn": (i32, [vp, vp, vp, i32, ctypes.c_float, vp, vp, sz, P(dak_tuning), vp]),
         "dak_attn_staged": (i32, [vp, vp, vp, vp, i32, ctypes.c_float, vp, vp, sz, P(dak_tuning), vp]),
@@ -255,8 +257,10 @@ def _check_bf16_cuda(t, name):
         raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
 
 
-def dak_gemm(A: Placement, B, C=None, c_fp32: bool = False, tuning=None, stream=None):
-    """C [N][M] = B [N][K] . A^T over the tiered placement A (returns C)."""
+def dak_gemm(A: Placement, B, C=None, c_fp32: bool = False, tuning=None, stream=None, workspace=None):
+    """C [N][M] = B [N][K] . A^T over the tiered placement A (returns C). workspace: an optional
+    split workspace of the caller's (a zeroed device tensor of dak_gemm_workspace_bytes(A, N)
+    bytes or more), for launches that may overlap others on different streams."""
     import torch
     _check_bf16_cuda(B, "B")
     N = int(B.shape[0])
@@ -265,9 +269,19 @@ def dak_gemm(A: Placement, B, C=None, c_fp32: bool = False, tuning=None, stream=
     if C is None:
         cols = A.meta["M"] // 2 if A.meta.get("glu") else A.meta["M"]
         C = torch.empty((N, cols), dtype=torch.float32 if c_fp32 else torch.bfloat16, device=B.device)
-    _check(lib.dak_gemm(A.handle, _ptr(B), _ptr(C), N, int(bool(c_fp32)), _tuning(tuning), _stream_ptr(stream)),
-           "dak_gemm")
+    if workspace is None:
+        _check(lib.dak_gemm(A.handle, _ptr(B), _ptr(C), N, int(bool(c_fp32)), _tuning(tuning), _stream_ptr(stream)),
+               "dak_gemm")
+    else:
+        nbytes = workspace.numel() * workspace.element_size()
+        _check(lib.dak_gemm_ws(A.handle, _ptr(B), _ptr(C), N, int(bool(c_fp32)), _tuning(tuning), _ptr(workspace),
+                               ctypes.c_size_t(nbytes), _stream_ptr(stream)), "dak_gemm_ws")
     return C
+
+
+def dak_gemm_workspace_bytes(A: Placement, N: int) -> int:
+    """Bytes of a caller's split workspace for dak_gemm over A with N hidden-state rows."""
+    return int(lib.dak_gemm_workspace_bytes(A.handle, int(N)))
 
 
 def dak_gemm_staged(A: Placement, staging, B, C=None, c_fp32: bool = False, tuning=None, stream=None):

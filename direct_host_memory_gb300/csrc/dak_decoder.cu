@@ -52,6 +52,8 @@ struct dak_decoder {
     double* inv_freq;      // [D/2] theta^(-2i/D)
     float* ws;             // attention split workspace
     size_t ws_bytes;
+    void* gemm_ws;         // the GEMMs' split workspace (this decoder's own, zeroed)
+    size_t gemm_ws_bytes;
     // prefetch baseline
     uint8_t* staging[2];
     size_t staging_bytes;
@@ -66,6 +68,7 @@ namespace dak {
 namespace {
 
 constexpr int kNormThreads = 256;
+constexpr size_t kGemmWsCounterBytes = 256 * 1024;  // the counter region of a GEMM split workspace
 constexpr int kNormMaxVec = 16;  // float4 per thread: d <= 16384
 
 struct NormArgs {
@@ -285,7 +288,7 @@ size_t staging_offset(const dak_decoder_layer& L, int upto) {
 
 void release(dak_decoder* d) {
     void* bufs[] = {d->x, d->h, d->qkv, d->q, d->att, d->ao, d->gu, d->act, d->dn, d->seq_lens, d->rope_cs,
-                    d->inv_freq, d->ws, d->staging[0], d->staging[1]};
+                    d->inv_freq, d->ws, d->gemm_ws, d->staging[0], d->staging[1]};
     for (void* p : bufs)
         if (p) cudaFree(p);
     if (d->exec) cudaGraphExecDestroy(d->exec);
@@ -347,6 +350,10 @@ dak_status enqueue_step(dak_decoder* d, const void* x_in, const int* positions, 
     ta.pdl = pdl ? 2 : 0;  // the previous kernel appends the newest token
     const int nl = c.n_layers;
     const int Lcap = nl > 0 ? d->layers[0].kv->L : 1;
+    // the GEMMs' piece counters start every step at zero, even after a kernel that gave up
+    if (d->gemm_ws &&
+        cudaMemsetAsync(d->gemm_ws, 0, std::min<size_t>(d->gemm_ws_bytes, kGemmWsCounterBytes), s) != cudaSuccess)
+        return DAK_ERR_CUDA;
 
     NormArgs na{};
     na.x = d->x;
@@ -397,7 +404,8 @@ dak_status enqueue_step(dak_decoder* d, const void* x_in, const int* positions, 
             return stg ? static_cast<const void*>(stg + staging_offset(L, i)) : p->host_dev;
         };
         const int Hq = c.n_heads, Hkv = c.n_kv_heads, D = c.head_dim, B = d->B;
-        if ((r = launch_gemm(L.qkv, src(0), d->h, d->qkv, B, 1, &tg[0], s)) != DAK_OK) return r;
+        if ((r = launch_gemm(L.qkv, src(0), d->h, d->qkv, B, 1, &tg[0], s, d->gemm_ws, d->gemm_ws_bytes)) != DAK_OK)
+            return r;
         RopeArgs ra{};
         ra.qkv = d->qkv;
         ra.cs = d->rope_cs;
@@ -418,7 +426,8 @@ dak_status enqueue_step(dak_decoder* d, const void* x_in, const int* positions, 
             return r;
         if ((r = launch_attn(d->q, L.kv, src(4), d->seq_lens, Hq, 0.f, d->att, d->ws, d->ws_bytes, &ta, s)) != DAK_OK)
             return r;
-        if ((r = launch_gemm(L.o, src(1), d->att, d->ao, B, 1, &tg[1], s)) != DAK_OK) return r;
+        if ((r = launch_gemm(L.o, src(1), d->att, d->ao, B, 1, &tg[1], s, d->gemm_ws, d->gemm_ws_bytes)) != DAK_OK)
+            return r;
         NormArgs nb{};
         nb.x = d->x;
         nb.delta = d->ao;
@@ -429,16 +438,21 @@ dak_status enqueue_step(dak_decoder* d, const void* x_in, const int* positions, 
         if ((r = norm(d, nb, 0, pdl, s)) != DAK_OK) return r;
         if (L.gate_up->glu) {
             // gate/up interleaved placement: the GEMM's epilogue writes silu(gate) * up itself
-            if ((r = launch_gemm(L.gate_up, src(2), d->h, d->act, B, 0, &tg[2], s)) != DAK_OK) return r;
+            if ((r = launch_gemm(L.gate_up, src(2), d->h, d->act, B, 0, &tg[2], s, d->gemm_ws, d->gemm_ws_bytes)) !=
+                DAK_OK)
+                return r;
         } else {
-            if ((r = launch_gemm(L.gate_up, src(2), d->h, d->gu, B, 1, &tg[2], s)) != DAK_OK) return r;
+            if ((r = launch_gemm(L.gate_up, src(2), d->h, d->gu, B, 1, &tg[2], s, d->gemm_ws, d->gemm_ws_bytes)) !=
+                DAK_OK)
+                return r;
             const long long n4 = static_cast<long long>(B) * c.ffn / 4;
             const int sg = static_cast<int>(std::min<long long>((n4 + 255) / 256, 4ll * device_sm_count()));
             if ((r = cuda_status(launch(swiglu_kernel, dim3(static_cast<unsigned>(std::max(sg, 1))), 256, pdl, s,
                                         static_cast<const float*>(d->gu), d->act, B, c.ffn))) != DAK_OK)
                 return r;
         }
-        if ((r = launch_gemm(L.down, src(3), d->act, d->dn, B, 1, &tg[3], s)) != DAK_OK) return r;
+        if ((r = launch_gemm(L.down, src(3), d->act, d->dn, B, 1, &tg[3], s, d->gemm_ws, d->gemm_ws_bytes)) != DAK_OK)
+            return r;
         if (mode == 2 && cudaEventRecord(d->ev_consumed[l & 1], s) != cudaSuccess) return DAK_ERR_CUDA;
         NormArgs nc{};
         nc.x = d->x;
@@ -529,6 +543,15 @@ extern "C" dak_status dak_decoder_create(const dak_decoder_config* cfg, const da
     chk(dalloc(&dd->inv_freq, static_cast<size_t>(D / 2)));
     dd->ws_bytes = dak_attn_workspace_bytes(B, c.n_heads, c.head_dim, dd->n_split);
     if (dd->ws_bytes) chk(cudaMalloc(reinterpret_cast<void**>(&dd->ws), dd->ws_bytes));
+    // a split workspace of its own, so that decoders on different streams never share one
+    dd->gemm_ws_bytes = 0;
+    for (int l = 0; l < c.n_layers; ++l)
+        for (const dak_placement* g : {layers[l].qkv, layers[l].o, layers[l].gate_up, layers[l].down})
+            dd->gemm_ws_bytes = std::max(dd->gemm_ws_bytes, gemm_workspace_bytes(g, B));
+    if (dd->gemm_ws_bytes) {
+        chk(cudaMalloc(&dd->gemm_ws, dd->gemm_ws_bytes));
+        if (e == cudaSuccess) chk(cudaMemset(dd->gemm_ws, 0, dd->gemm_ws_bytes));
+    }
     if (e == cudaSuccess) {
         std::vector<double> inv(D / 2);
         for (int64_t i = 0; i < D / 2; ++i)

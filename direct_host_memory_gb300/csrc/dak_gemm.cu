@@ -992,11 +992,11 @@ static bool split_workspace(float** part, int** cnt) {
 constexpr double kCtaStreamBytesPerUs = 62.5e3;
 
 static int split_pieces(int T, int K_pad, int N_pad, int slots, long long tile_bytes, int host_cap, int pstep,
-                        double piece_us, const dak_tuning* t) {
+                        double piece_us, long long max_tiles, long long max_floats, const dak_tuning* t) {
     const int steps = (K_pad + 63) / 64;
     auto fits = [&](int P) {
-        return P <= (K_pad + pstep - 1) / pstep && T <= kSplitTiles &&
-               static_cast<long long>(T) * P * kTileM * N_pad <= kSplitFloats;
+        return P <= (K_pad + pstep - 1) / pstep && T <= max_tiles &&
+               static_cast<long long>(T) * P * kTileM * N_pad <= max_floats;
     };
     if (t && t->split_k > 0) {
         int P = std::min(kMaxPieces, t->split_k);
@@ -1021,6 +1021,18 @@ static int split_pieces(int T, int K_pad, int N_pad, int slots, long long tile_b
     return cheapest;
 }
 
+// A caller's workspace: the per-tile-row counters of every launch that uses it (a fixed
+// region, indexed by tile row, so that launches over different matrices can share it), then
+// the partial tiles.
+constexpr long long kCallerCounterBytes = static_cast<long long>(kSplitTiles) * 4;
+
+size_t gemm_workspace_bytes(const dak_placement* A, int N) {
+    if (!A || A->kind != 0 || N < 1) return 0;
+    if (N > kMaxBlockN || A->T > kSplitTiles) return 0;  // never split
+    const long long n_pad = (N + 7) & ~7;
+    return static_cast<size_t>(kCallerCounterBytes + static_cast<long long>(A->T) * kMaxPieces * kTileM * n_pad * 4);
+}
+
 void reset_split_counters() {
     float* part = nullptr;
     int* cnt = nullptr;
@@ -1030,7 +1042,7 @@ void reset_split_counters() {
 // One launch over up to kMaxWideN hidden-state rows: one CTA per tile row up to 256 rows
 // (the widest tcgen05 tile used here), a cluster of ceil(N / 256) CTAs per tile row beyond.
 static dak_status launch_gemm_block(const dak_placement* A, const void* host_src, const void* B, void* C, int N,
-                                    int c_fp32, const dak_tuning* t, cudaStream_t stream) {
+                                    int c_fp32, const dak_tuning* t, void* ws, size_t ws_bytes, cudaStream_t stream) {
     if (!A || A->kind != 0) return DAK_ERR_INVALID;
     if (N < 1 || N > kMaxWideN) return DAK_ERR_INVALID;
     if (A->M == 0 || A->T == 0) return DAK_OK;  // nothing to compute; C may be empty
@@ -1153,8 +1165,21 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
     // what the split would spread, and the partial tiles cost more than it saves)
     if (NC == 1 && (p.N_pad <= 128 || (t && t->split_k > 0))) {
         const double piece_us = umma ? std::max(1.0, p.N_pad / 16.0) : 2.0;
-        p.P = split_pieces(p.T, p.K_pad, p.N_pad, sms * per_sm, p.tile_bytes, kDefaultHostCtas, p.pstep, piece_us, t);
-        if (p.P > 1 && !split_workspace(&p.part, &p.cnt)) return DAK_ERR_CUDA;
+        // the caller's workspace (counters, then partial tiles) or the module's own
+        const long long cnt_bytes = ws ? kCallerCounterBytes : 0;
+        const long long max_tiles = kSplitTiles;
+        const long long max_floats =
+            ws ? std::max(0ll, (static_cast<long long>(ws_bytes) - cnt_bytes) / 4) : kSplitFloats;
+        p.P = split_pieces(p.T, p.K_pad, p.N_pad, sms * per_sm, p.tile_bytes, kDefaultHostCtas, p.pstep, piece_us,
+                           max_tiles, max_floats, t);
+        if (p.P > 1) {
+            if (ws) {
+                p.cnt = static_cast<int*>(ws);
+                p.part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + cnt_bytes);
+            } else if (!split_workspace(&p.part, &p.cnt)) {
+                return DAK_ERR_CUDA;
+            }
+        }
     }
 
     // schedule in cluster units; a role's units are its tile rows x P pieces
@@ -1200,17 +1225,19 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
 // again. Clusters stop at 4 CTAs: forwarding every A chunk to 7 peers measured slower than
 // two launches of 1024 rows.
 dak_status launch_gemm(const dak_placement* A, const void* host_src, const void* B, void* C, int N, int c_fp32,
-                       const dak_tuning* t, cudaStream_t stream) {
+                       const dak_tuning* t, cudaStream_t stream, void* ws, size_t ws_bytes) {
     if (!A || A->kind != 0) return DAK_ERR_INVALID;
+    if (ws && (reinterpret_cast<uintptr_t>(ws) & 255)) return DAK_ERR_ALIGN;
     const int block = (t && t->column_blocks == 1) ? kMaxBlockN : kMaxWideN;
-    if (N <= block) return launch_gemm_block(A, host_src, B, C, N, c_fp32, t, stream);
+    if (N <= block) return launch_gemm_block(A, host_src, B, C, N, c_fp32, t, ws, ws_bytes, stream);
     if (!B || !C) return DAK_ERR_INVALID;
     const size_t b_row = static_cast<size_t>(A->K) * 2;
     const size_t c_row = static_cast<size_t>(A->glu ? A->M / 2 : A->M) * (c_fp32 ? 4 : 2);
     for (int n0 = 0; n0 < N; n0 += block) {
         const int nb = std::min(block, N - n0);
         const dak_status r = launch_gemm_block(A, host_src, static_cast<const uint8_t*>(B) + n0 * b_row,
-                                               static_cast<uint8_t*>(C) + n0 * c_row, nb, c_fp32, t, stream);
+                                               static_cast<uint8_t*>(C) + n0 * c_row, nb, c_fp32, t, ws, ws_bytes,
+                                               stream);
         if (r != DAK_OK) return r;
     }
     return DAK_OK;
@@ -1222,6 +1249,16 @@ extern "C" dak_status dak_gemm(const dak_placement* A, const void* B, void* C, i
                                const dak_tuning* tuning, void* stream) {
     if (!A) return DAK_ERR_INVALID;
     return dak::launch_gemm(A, A->host_dev, B, C, N, c_fp32, tuning, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t dak_gemm_workspace_bytes(const dak_placement* A, int N) { return dak::gemm_workspace_bytes(A, N); }
+
+extern "C" dak_status dak_gemm_ws(const dak_placement* A, const void* B, void* C, int N, int c_fp32,
+                                  const dak_tuning* tuning, void* workspace, size_t ws_bytes, void* stream) {
+    if (!A || !workspace) return DAK_ERR_INVALID;
+    if (static_cast<long long>(ws_bytes) < dak::kCallerCounterBytes) return DAK_ERR_INVALID;
+    return dak::launch_gemm(A, A->host_dev, B, C, N, c_fp32, tuning, static_cast<cudaStream_t>(stream), workspace,
+                            ws_bytes);
 }
 
 extern "C" dak_status dak_gemm_staged(const dak_placement* A, const void* staging, const void* B, void* C, int N,

@@ -61,8 +61,10 @@ int device_sm_count();
 dak_status cuda_status(cudaError_t e);
 
 // kernel launchers (defined in dak_gemm.cu / dak_attn.cu)
+// ws / ws_bytes: the caller's split workspace (dak_gemm_ws), or null for the module's own
 dak_status launch_gemm(const dak_placement* A, const void* host_src, const void* B, void* C, int N, int c_fp32,
-                       const dak_tuning* t, cudaStream_t s);
+                       const dak_tuning* t, cudaStream_t s, void* ws = nullptr, size_t ws_bytes = 0);
+size_t gemm_workspace_bytes(const dak_placement* A, int N);
 dak_status launch_attn(const void* Q, const dak_placement* KV, const void* host_src, const int* seq_lens, int H_q,
                        float scale, void* O, void* ws, size_t ws_bytes, const dak_tuning* t, cudaStream_t s);
 

@@ -171,6 +171,21 @@ dak_status dak_placement_info(const dak_placement* p, int64_t* host_bytes, int64
 dak_status dak_gemm(const dak_placement* A, const void* B, void* C, int N, int c_fp32, const dak_tuning* tuning,
                     void* stream);
 
+/* dak_gemm with a split workspace of the caller's (device memory, 256-byte aligned, zeroed
+ * once before its first use; dak_gemm_workspace_bytes(A, N) bytes hold every piece count a
+ * launch over A with N rows may choose, 256 KiB is the least accepted). dak_gemm keeps
+ * the partial tiles of split tile rows in one workspace per device, so that split
+ * launches on different streams must not overlap; launches with workspaces of their own
+ * may. The workspace starts with 256 KiB of per-tile-row piece counters (indexed by tile
+ * row, shared by every matrix that uses the workspace) that every completed launch leaves
+ * at zero; after dak_last_error reported an error, zero those 256 KiB again. The partial
+ * tiles follow. A smaller workspace than a launch's pieces need makes it use fewer pieces;
+ * otherwise as dak_gemm. DAK_ERR_INVALID: workspace NULL or smaller than 256 KiB;
+ * DAK_ERR_ALIGN: not 256-byte aligned. */
+size_t dak_gemm_workspace_bytes(const dak_placement* A, int N);
+dak_status dak_gemm_ws(const dak_placement* A, const void* B, void* C, int N, int c_fp32, const dak_tuning* tuning,
+                       void* workspace, size_t ws_bytes, void* stream);
+
 /* Workspace bytes dak_attn needs for B requests, H_q query heads, head dim D and
  * n_split context splits (0 when n_split == 1). */
 size_t dak_attn_workspace_bytes(int B, int H_q, int D, int n_split);

@@ -159,6 +159,48 @@ def test_split_pieces_ragged_k(dak, K, N):
             assert og.rel_err(to_np(C), ref) <= FP32_OUT_TOL, tun
 
 
+def test_gemm_caller_workspace(dak):
+    """dak_gemm_ws: the split workspace of the caller's gives the same bits as the library's own;
+    launches on two streams with workspaces of their own may overlap; a workspace that is too
+    small or misaligned is refused."""
+    import torch
+    A1, B1 = synth.gemm_inputs(4096, 4096, 16, seed=71)
+    A2, B2 = synth.gemm_inputs(6144, 1024, 16, seed=72)
+    p1, p2 = dak.dak_place_matrix(A1, 5), dak.dak_place_matrix(A2, 0)
+    b1, b2 = to_dev(B1), to_dev(B2)
+    base1 = dak.dak_gemm(p1, b1, c_fp32=True, tuning=dict(split_k=3))
+    base2 = dak.dak_gemm(p2, b2, c_fp32=True, tuning=dict(split_k=5))
+    n1, n2 = dak.dak_gemm_workspace_bytes(p1, 16), dak.dak_gemm_workspace_bytes(p2, 16)
+    assert n1 >= 256 * 1024 + 64 * 8 * 64 * 16 * 4 and n2 > 0
+    w1 = torch.zeros(n1 // 4 + 64, dtype=torch.float32, device="cuda")
+    w2 = torch.zeros(n2 // 4 + 64, dtype=torch.float32, device="cuda")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = []
+    for _ in range(4):
+        with torch.cuda.stream(s1):
+            c1 = dak.dak_gemm(p1, b1, c_fp32=True, tuning=dict(split_k=3), workspace=w1, stream=s1)
+        with torch.cuda.stream(s2):
+            c2 = dak.dak_gemm(p2, b2, c_fp32=True, tuning=dict(split_k=5), workspace=w2, stream=s2)
+        outs.append((c1, c2))
+    torch.cuda.synchronize()
+    assert dak.dak_last_error()[0] == 0
+    for c1, c2 in outs:
+        assert np.array_equal(bits_of(c1), bits_of(base1))
+        assert np.array_equal(bits_of(c2), bits_of(base2))
+    assert og.rel_err(to_np(base1), og.gemm_ref(A1, B1)) <= FP32_OUT_TOL
+    # one workspace for both matrices, in turn on one stream: the counters are shared by tile row
+    for _ in range(3):
+        c1 = dak.dak_gemm(p1, b1, c_fp32=True, tuning=dict(split_k=3), workspace=w1)
+        c2 = dak.dak_gemm(p2, b2, c_fp32=True, tuning=dict(split_k=5), workspace=w1)
+    assert np.array_equal(bits_of(c1), bits_of(base1)) and np.array_equal(bits_of(c2), bits_of(base2))
+    with pytest.raises(dak.DakError):
+        dak.dak_gemm(p1, b1, c_fp32=True, workspace=torch.zeros(1024, device="cuda"))
+    with pytest.raises(dak.DakError):
+        dak.dak_gemm(p1, b1, c_fp32=True, workspace=w1[1:])  # 4-byte offset: not 256-byte aligned
+    for pl in (p1, p2):
+        pl.free()
+
+
 def test_split_pieces_graph_replay(dak):
     """The per-tile-row piece counters return to zero after every launch: a CUDA graph of three
     split GEMMs (two sharing tile-row indices) replayed many times gives the same bits."""

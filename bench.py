@@ -49,6 +49,8 @@ def _args():
                     help="further x_global values for the decode step (comma list, empty = none)")
     ap.add_argument("--no-planner-check", action="store_true",
                     help="skip the compute-bound / greedy-vs-uniform planner measurement")
+    ap.add_argument("--decode-batch", type=int, default=None,
+                    help="--profile decode: batch of the step (default: the model configuration's)")
     ap.add_argument("--plain-launch", action="store_true",
                     help="--profile decode: eager steps with ordinary launches (no graph, no programmatic launch)")
     ap.add_argument("--profile", default=None, choices=["attn", "qkv", "o", "gate_up", "down", "decode"],
@@ -335,7 +337,50 @@ def run_decode(dak, args, b_host, b_hbm, dev, sync_all, local):
         del dec
         torch.cuda.empty_cache()
     res["per_x"] = sweep
+    if not args.no_sweep:
+        res["batch1"] = run_decode_batch1(dak, args, cfg, b_host, b_hbm, dev, sync_all, peak_flops)
     return res
+
+
+def run_decode_batch1(dak, args, cfg, b_host, b_hbm, dev, sync_all, peak_flops):
+    """The same decode step at batch 1 (every linear a GEMV on CUDA cores), all in HBM and at
+    the target x_global, against both prefetch baselines."""
+    import torch
+    import synth
+    cfg = dict(cfg, batch=1)
+    L = cfg["context"]
+    x_in = torch.from_numpy(synth.decoder_x0(cfg, 1).view("int16")).view(torch.bfloat16).to(dev)
+    pos = torch.full((1,), L - 1, dtype=torch.int32, device=dev)
+    out = torch.empty_like(x_in)
+    recs = []
+    for xg in (0.0, args.decode_x):
+        units, tmodel = decode_plan(dak, cfg, b_host, b_hbm, xg, peak_flops)
+        dec = build_decoder(dak, cfg, units)
+        C = sum(L_[k].host_bytes + L_[k].hbm_bytes for L_ in dec.layers for k in dak.DECODER_OPS)
+        H = dec.host_bytes()
+        roof = tier_roofline(C, H / C, b_host, b_hbm)
+        rec = {"x_global": xg, "x_effective": H / C, "bytes_per_step": C}
+        modes = [(dak.MODE_DIRECT, "dak")]
+        if xg > 0:
+            modes += [(dak.MODE_PREFETCH_SERIAL, "prefetch_serial"), (dak.MODE_PREFETCH_OVERLAP, "prefetch_overlap")]
+        for mode, name in modes:
+            dec.capture(x_in, pos, out, mode)
+            t = time_steps(dec.replay, max(4, args.decode_steps // 2), 2, sync_all)
+            rec[name + "_tok_s"] = 1 / t
+            if mode == dak.MODE_DIRECT:
+                rec["ms_per_step"] = t * 1e3
+                rec["frac"] = (C / t) / roof
+                rec["eff_gbps"] = C / t / 1e9
+        if xg > 0:
+            rec["vs_prefetch_best"] = rec["dak_tok_s"] / max(rec["prefetch_serial_tok_s"],
+                                                             rec["prefetch_overlap_tok_s"])
+        rec["planner_model_ms"] = tmodel * 1e3
+        rec["status"] = dak.dak_last_error()[0]
+        recs.append(rec)
+        dec.free()
+        del dec
+        torch.cuda.empty_cache()
+    return recs
 
 
 # ------------------------------------------------------------------------------ planner check
@@ -937,7 +982,7 @@ def main():
         "config": step_config(args, world),
         "ms_per_step_p10_p50_p90": [pct(0.1), pct(0.5), pct(0.9)],
         "step": {"x_effective": x_eff, "bytes_per_step": C, "host_bytes_per_step": st.host_bytes,
-                 "kernels": "dak_gemm x4 (tcgen05 for N >= 8) + dak_attn (+ split combine)"},
+                 "kernels": "dak_gemm x4 (tcgen05 for N >= 2) + dak_attn (+ split combine)"},
         "decode_tok_s": n * args.batch / (t_step * LAYERS_8B),
         "tier_roofline_gbps": tier_roofline(C, x_eff, b_host, b_hbm) / 1e9,
         "tier_roofline_frac": (C / t_step) / tier_roofline(C, x_eff, b_host, b_hbm),
@@ -1008,6 +1053,8 @@ def run_profile(args):
     if args.profile == "decode":
         # the 8B-shaped decode step at x_global = --x (planner ratios), one graph replay per step
         cfg = dict(synth.DECODER_8B)
+        if args.decode_batch:
+            cfg["batch"] = args.decode_batch
         b_host, b_hbm, _ = measure_tiers(dak) if args.x > 0 else (211e9, 7.3e12, None)
         pk, _ = peaks()
         units, _ = decode_plan(dak, cfg, b_host, b_hbm, args.x, pk.get("bf16_tflops_sustained", 1700.0) * 1e12)

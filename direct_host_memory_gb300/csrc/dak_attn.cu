@@ -482,6 +482,12 @@ dak_status launch_attn(const void* Q, const dak_placement* KV, const void* host_
     const int host_units_i = static_cast<int>(std::min<long long>(p.host_units, 1 << 30));
     const int hbm_units_i = static_cast<int>(std::min<long long>(p.hbm_units, 1 << 30));
     int W_ring = (t && t->hbm_window > 0) ? std::min(t->hbm_window, kAttnMaxStages) : kAttnStages;
+    if (!(t && t->hbm_window > 0) && p.host_units + p.hbm_units <= device_sm_count()) {
+        // one CTA per SM holds every unit: a ring as deep as a unit's chunks (up to the
+        // maximum) puts all of them in flight at once (1 request x 16 splits of 4K context:
+        // 11.5 -> 10.8 us)
+        W_ring = std::max(W_ring, std::min(p.split_len / kChunkTok, kAttnMaxStages));
+    }
     if (t && t->window > 0) W_ring = std::max(W_ring, std::min(t->window, kAttnMaxStages));
     const int per_sm = KV->D == 128 ? attn_ctas_per_sm<128>(W_ring, G) : attn_ctas_per_sm<64>(W_ring, G);
     Sched sc2 = schedule(host_units_i, hbm_units_i, device_sm_count() * per_sm, t, kAttnDefaultHostCtas,

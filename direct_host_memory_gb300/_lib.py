@@ -29,7 +29,7 @@ EXPORTS = [
     "dak_gemm_staged", "dak_attn_staged", "dak_attn_noalloc", "dak_selftest_wait",
     "dak_decoder_create", "dak_decoder_batch", "dak_decoder_step", "dak_decoder_capture",
     "dak_decoder_replay", "dak_decoder_launches", "dak_decoder_free", "dak_tune_gemm", "dak_tune_attn",
-    "dak_place_matrix_glu", "dak_plan_units", "dak_gemm_workspace_bytes", "dak_gemm_ws",
+    "dak_place_matrix_glu", "dak_plan_units", "dak_gemm_workspace_bytes", "dak_gemm_ws", "dak_gemm_plan",
 ]
 
 # size of the fixed device array dak_attn_noalloc uses (DAK_NOALLOC_SCRATCH_BYTES in dak.h)
@@ -56,6 +56,12 @@ class dak_op(ctypes.Structure):
 class dak_tune_result(ctypes.Structure):
     _fields_ = [("best", dak_tuning), ("best_us", ctypes.c_double), ("default_us", ctypes.c_double),
                 ("cc_off_us", ctypes.c_double), ("no_align_us", ctypes.c_double), ("candidates", ctypes.c_int)]
+
+
+class dak_gemm_plan_info(ctypes.Structure):
+    _fields_ = [(f, ctypes.c_int) for f in (
+        "tensor_cores", "launches", "cluster", "n_pad", "pieces", "piece_step", "chunk_k", "host_chunk_k",
+        "hbm_stages", "host_stages", "host_ctas", "hbm_ctas", "host_window", "hbm_window", "smem_bytes")]
 
 
 class dak_decoder_config(ctypes.Structure):
@@ -89,6 +95,7 @@ def _load():
         "dak_gemm_staged": (i32, [vp, vp, vp, vp, i32, i32, P(dak_tuning), vp]),
         "dak_gemm_workspace_bytes": (sz, [vp, i32]),
         "dak_gemm_ws": (i32, [vp, vp, vp, i32, i32, P(dak_tuning), vp, sz, vp]),
+        "dak_gemm_plan": (i32, [i64, i64, i32, i32, i32, P(dak_tuning), sz, P(dak_gemm_plan_info)]),
         "dak_attn_workspace_bytes": (sz, [i32, i32, i32, i32]),
         "dak_attn": (i32, [vp, vp, vp, i32, ctypes.c_float, vp, vp, sz, P(dak_tuning), vp]),
         "dak_attn_staged": (i32, [vp, vp, vp, vp, i32, ctypes.c_float, vp, vp, sz, P(dak_tuning), vp]),
@@ -282,6 +289,19 @@ def dak_gemm(A: Placement, B, C=None, c_fp32: bool = False, tuning=None, stream=
 def dak_gemm_workspace_bytes(A: Placement, N: int) -> int:
     """Bytes of a caller's split workspace for dak_gemm over A with N hidden-state rows."""
     return int(lib.dak_gemm_workspace_bytes(A.handle, int(N)))
+
+
+def dak_gemm_plan(M: int, K: int, n_host_tiles: int, N: int, sm_count: int = None, tuning=None,
+                  ws_bytes: int = 0) -> dict:
+    """The launch dak_gemm would make for an M x K matrix with n_host_tiles tile rows on the
+    host and N hidden-state rows (pieces, rings, CTAs of each role), from host arithmetic
+    alone; sm_count None = this process's GPU."""
+    if sm_count is None:
+        sm_count = dak_sm_count()
+    out = dak_gemm_plan_info()
+    _check(lib.dak_gemm_plan(int(M), int(K), int(n_host_tiles), int(N), int(sm_count), _tuning(tuning),
+                             ctypes.c_size_t(int(ws_bytes)), ctypes.byref(out)), "dak_gemm_plan")
+    return {f: int(getattr(out, f)) for f, _ in dak_gemm_plan_info._fields_}
 
 
 def dak_gemm_staged(A: Placement, staging, B, C=None, c_fp32: bool = False, tuning=None, stream=None):

@@ -1039,46 +1039,32 @@ void reset_split_counters() {
     if (split_workspace(&part, &cnt)) cudaMemset(cnt, 0, sizeof(int) * kSplitTiles);
 }
 
-// One launch over up to kMaxWideN hidden-state rows: one CTA per tile row up to 256 rows
-// (the widest tcgen05 tile used here), a cluster of ceil(N / 256) CTAs per tile row beyond.
-static dak_status launch_gemm_block(const dak_placement* A, const void* host_src, const void* B, void* C, int N,
-                                    int c_fp32, const dak_tuning* t, void* ws, size_t ws_bytes, cudaStream_t stream) {
-    if (!A || A->kind != 0) return DAK_ERR_INVALID;
-    if (N < 1 || N > kMaxWideN) return DAK_ERR_INVALID;
-    if (A->M == 0 || A->T == 0) return DAK_OK;  // nothing to compute; C may be empty
-    if (!B || !C) return DAK_ERR_INVALID;
-    if ((reinterpret_cast<uintptr_t>(B) & 15) || (reinterpret_cast<uintptr_t>(C) & 15)) return DAK_ERR_ALIGN;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return DAK_ERR_CUDA;
-    if (dev != A->device) return DAK_ERR_INVALID;
+// Everything one launch decides from the shape, the SM count and the tuning: the rings'
+// layout, the pieces per tile row and the CTAs of each role. Host arithmetic only (no CUDA
+// call), so that dak_gemm_plan can report it without a GPU.
+struct BlockPlan {
+    bool umma;
+    int NC, N_pad, P, pstep, kcb, smem, grid;
+    Chunks ch[2];  // [0] HBM-side CTAs, [1] host-side CTAs
+    int n_host_ctas, n_hbm_ctas, host_window, hbm_window;
+};
 
-    GemmParams p{};
-    p.a_host = static_cast<const uint8_t*>(host_src);
-    p.a_hbm = static_cast<const uint8_t*>(A->hbm_ptr);
-    p.B = static_cast<const __nv_bfloat16*>(B);
-    p.C = C;
-    p.M = static_cast<int>(A->M);
-    p.K = static_cast<int>(A->K);
-    p.K_pad = static_cast<int>(A->K_pad);
-    p.N = N;
+// T tile rows (h of them on the host) of K_pad columns; N hidden-state rows (at most one
+// launch's worth); caller_ws: the partial tiles go to a caller's workspace of ws_bytes.
+static dak_status plan_block(int T, int h, int K_pad, long long tile_bytes, int N, int sms, const dak_tuning* t,
+                             bool caller_ws, size_t ws_bytes, BlockPlan* bp) {
+    if (N < 1 || N > kMaxWideN || sms < 1) return DAK_ERR_INVALID;
+    BlockPlan& q = *bp;
+    q = BlockPlan{};
     // wide B: NC CTAs of a cluster share each tile row, CTA r computing rows [256 r, 256 r + 256)
-    p.NC = N > kMaxBlockN ? (N + kMaxBlockN - 1) / kMaxBlockN : 1;
-    p.N_pad = N > kMaxBlockN ? kMaxBlockN : (N + 7) & ~7;
-    p.T = A->T;
-    p.h = A->h;
-    p.c_fp32 = c_fp32 ? 1 : 0;
-    p.tile_bytes = A->tile_bytes;
-    p.glu = A->glu;
-    p.P = 1;
-    p.pstep = N >= 2 ? 64 : 256;  // the B block of the tensor-core / CUDA-core layout
-    p.st = status_ptr();
-    if (!p.st) return DAK_ERR_CUDA;
-
-    const bool umma = N >= 2;  // N = 2..7 padded to 8 columns: measured 1.2-2.7x faster than FMA
-    const int kind = umma ? kUmmaB : kCoreB;
-    const int sms = device_sm_count();
-    const int rows_b = umma ? p.N_pad : N;
-    const int NC = p.NC;
+    q.NC = N > kMaxBlockN ? (N + kMaxBlockN - 1) / kMaxBlockN : 1;
+    q.N_pad = N > kMaxBlockN ? kMaxBlockN : (N + 7) & ~7;
+    q.P = 1;
+    q.pstep = N >= 2 ? 64 : 256;  // the B block of the tensor-core / CUDA-core layout
+    q.umma = N >= 2;  // N = 2..7 padded to 8 columns: measured 1.2-2.7x faster than FMA
+    const bool umma = q.umma;
+    const int rows_b = umma ? q.N_pad : N;
+    const int NC = q.NC;
     auto stage_of = [&](int k) { return (k * 128 + k * 2 * rows_b + 1023) & ~1023; };
 
     int per_sm = 1;
@@ -1119,18 +1105,17 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
     // reading host tiles take the split layout, whose 32 KiB A chunks keep more host bytes
     // in flight (host reads are latency-bound).
     const bool b_ring_all = umma && NC > 1;
-    const bool b_ring_host = umma && p.N_pad > 128 && kc == 64 && !(t && t->chunk_k > 0);
+    const bool b_ring_host = umma && q.N_pad > 128 && kc == 64 && !(t && t->chunk_k > 0);
     if (b_ring_all && !(t && t->chunk_k > 0)) kc = 256;
     // (NC > 1: each CTA holds 2 x 256 TMEM columns, the whole TMEM of an SM: one CTA per SM)
     const int CL = NC;  // CTAs per cluster
-    const int ring_budget = budget;
     auto layout = [&](int kc_, bool split, Chunks* L) -> bool {
         L->kc = kc_;
         L->kcb = split ? 64 : kc_;
         if (split) {
             L->stage_bytes = (kc_ * 128 + 1023) & ~1023;
-            L->b_slot_bytes = (p.N_pad * L->kcb * 2 + 1023) & ~1023;
-            const int avail = ring_budget - 1024;
+            L->b_slot_bytes = (q.N_pad * L->kcb * 2 + 1023) & ~1023;
+            const int avail = budget - 1024;
             L->stages = std::min(4, std::max(2, avail / 2 / L->stage_bytes));  // about half for A
             L->wb = std::min(8, (avail - L->stages * L->stage_bytes) / L->b_slot_bytes);
             if (L->wb < 2) {
@@ -1140,7 +1125,7 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
             if (L->wb < 2) return false;
         } else {
             L->stage_bytes = stage_of(kc_);
-            L->stages = std::min(8, (ring_budget - (umma ? 1024 : 0)) / L->stage_bytes);
+            L->stages = std::min(8, (budget - (umma ? 1024 : 0)) / L->stage_bytes);
             L->wb = 0;
             L->b_slot_bytes = 0;
             if (L->stages < 1 || (L->stages < 2 && !(t && t->chunk_k > 0))) return false;
@@ -1148,38 +1133,29 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
         L->b_ring_off = L->stages * L->stage_bytes;
         return true;
     };
-    if (!layout(kc, b_ring_all, &p.ch[0])) return DAK_ERR_INVALID;
-    p.ch[1] = p.ch[0];
-    if (!b_ring_all && b_ring_host && p.h > 0) {
-        if (!layout(256, true, &p.ch[1])) p.ch[1] = p.ch[0];
+    if (!layout(kc, b_ring_all, &q.ch[0])) return DAK_ERR_INVALID;
+    q.ch[1] = q.ch[0];
+    if (!b_ring_all && b_ring_host && h > 0) {
+        if (!layout(256, true, &q.ch[1])) q.ch[1] = q.ch[0];
     }
-    if (p.ch[0].kcb != p.ch[1].kcb) return DAK_ERR_INVALID;  // one B tensor map serves both
-    const int kcb = p.ch[0].kcb;
+    if (q.ch[0].kcb != q.ch[1].kcb) return DAK_ERR_INVALID;  // one B tensor map serves both
+    q.kcb = q.ch[0].kcb;
     auto ring_bytes = [](const Chunks& L) { return L.stages * L.stage_bytes + L.wb * L.b_slot_bytes; };
-    const int rings = std::max(ring_bytes(p.ch[0]), ring_bytes(p.ch[1]));
-    const int smem = rings + (umma ? 1024 : 0);
-    const int max_stages = std::max(p.ch[0].stages, p.ch[1].stages);
+    const int rings = std::max(ring_bytes(q.ch[0]), ring_bytes(q.ch[1]));
+    q.smem = rings + (umma ? 1024 : 0);
+    const int max_stages = std::max(q.ch[0].stages, q.ch[1].stages);
 
     // pieces per tile row (one CTA per tile row's columns; automatic only while the tile
     // rows are memory-bound, N_pad <= 128: at N_pad = 256 the tensor work of a tile row is
     // what the split would spread, and the partial tiles cost more than it saves)
-    if (NC == 1 && (p.N_pad <= 128 || (t && t->split_k > 0))) {
-        const double piece_us = umma ? std::max(1.0, p.N_pad / 16.0) : 2.0;
+    if (NC == 1 && (q.N_pad <= 128 || (t && t->split_k > 0))) {
+        const double piece_us = umma ? std::max(1.0, q.N_pad / 16.0) : 2.0;
         // the caller's workspace (counters, then partial tiles) or the module's own
-        const long long cnt_bytes = ws ? kCallerCounterBytes : 0;
-        const long long max_tiles = kSplitTiles;
+        const long long cnt_bytes = caller_ws ? kCallerCounterBytes : 0;
         const long long max_floats =
-            ws ? std::max(0ll, (static_cast<long long>(ws_bytes) - cnt_bytes) / 4) : kSplitFloats;
-        p.P = split_pieces(p.T, p.K_pad, p.N_pad, sms * per_sm, p.tile_bytes, kDefaultHostCtas, p.pstep, piece_us,
-                           max_tiles, max_floats, t);
-        if (p.P > 1) {
-            if (ws) {
-                p.cnt = static_cast<int*>(ws);
-                p.part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + cnt_bytes);
-            } else if (!split_workspace(&p.part, &p.cnt)) {
-                return DAK_ERR_CUDA;
-            }
-        }
+            caller_ws ? std::max(0ll, (static_cast<long long>(ws_bytes) - cnt_bytes) / 4) : kSplitFloats;
+        q.P = split_pieces(T, K_pad, q.N_pad, sms * per_sm, tile_bytes, kDefaultHostCtas, q.pstep, piece_us,
+                           kSplitTiles, max_floats, t);
     }
 
     // schedule in cluster units; a role's units are its tile rows x P pieces
@@ -1187,33 +1163,88 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
     if (t) tc = *t;
     const int host_cap = NC > 1 ? kDefaultHostCtasWide : kDefaultHostCtas;
     int hc = tc.host_ctas > 0 ? tc.host_ctas : host_cap;
-    if (!(tc.host_ctas > 0) && CL == 1 && p.h * p.P > hc && 3 * p.h * p.P <= 4 * hc) {
-        hc = p.h * p.P;  // up to a third over the cap: one wave of host units rather than two
+    if (!(tc.host_ctas > 0) && CL == 1 && h * q.P > hc && 3 * h * q.P <= 4 * hc) {
+        hc = h * q.P;  // up to a third over the cap: one wave of host units rather than two
     }
     tc.host_ctas = std::max(1, hc / CL);
     if (tc.hbm_ctas > 0) tc.hbm_ctas = std::max(1, tc.hbm_ctas / CL);
-    Sched sc = schedule(p.h * p.P, (p.T - p.h) * p.P, std::max(1, (sms * per_sm) / CL), &tc,
-                        std::max(1, host_cap / CL), std::min(kDefaultHostWindow, p.ch[1].stages), p.ch[0].stages,
-                        max_stages);
-    p.n_host_ctas = sc.n_host_ctas;
-    p.n_hbm_ctas = sc.n_hbm_ctas;
-    p.host_window = std::min(sc.host_window, p.ch[1].stages);
-    p.hbm_window = std::min(sc.hbm_window, p.ch[0].stages);
-    const int grid = (p.n_host_ctas + p.n_hbm_ctas) * CL;
-    if (grid == 0) return DAK_OK;
+    const Sched sc = schedule(h * q.P, (T - h) * q.P, std::max(1, (sms * per_sm) / CL), &tc,
+                              std::max(1, host_cap / CL), std::min(kDefaultHostWindow, q.ch[1].stages),
+                              q.ch[0].stages, max_stages);
+    q.n_host_ctas = sc.n_host_ctas;
+    q.n_hbm_ctas = sc.n_hbm_ctas;
+    q.host_window = std::min(sc.host_window, q.ch[1].stages);
+    q.hbm_window = std::min(sc.hbm_window, q.ch[0].stages);
+    q.grid = (q.n_host_ctas + q.n_hbm_ctas) * CL;
+    return DAK_OK;
+}
+
+// One launch over up to kMaxWideN hidden-state rows: one CTA per tile row up to 256 rows
+// (the widest tcgen05 tile used here), a cluster of ceil(N / 256) CTAs per tile row beyond.
+static dak_status launch_gemm_block(const dak_placement* A, const void* host_src, const void* B, void* C, int N,
+                                    int c_fp32, const dak_tuning* t, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    if (!A || A->kind != 0) return DAK_ERR_INVALID;
+    if (N < 1 || N > kMaxWideN) return DAK_ERR_INVALID;
+    if (A->M == 0 || A->T == 0) return DAK_OK;  // nothing to compute; C may be empty
+    if (!B || !C) return DAK_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(B) & 15) || (reinterpret_cast<uintptr_t>(C) & 15)) return DAK_ERR_ALIGN;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DAK_ERR_CUDA;
+    if (dev != A->device) return DAK_ERR_INVALID;
+
+    BlockPlan bp;
+    const dak_status r = plan_block(A->T, A->h, static_cast<int>(A->K_pad), A->tile_bytes, N, device_sm_count(), t,
+                                    ws != nullptr, ws_bytes, &bp);
+    if (r != DAK_OK) return r;
+    if (bp.grid == 0) return DAK_OK;
+
+    GemmParams p{};
+    p.a_host = static_cast<const uint8_t*>(host_src);
+    p.a_hbm = static_cast<const uint8_t*>(A->hbm_ptr);
+    p.B = static_cast<const __nv_bfloat16*>(B);
+    p.C = C;
+    p.M = static_cast<int>(A->M);
+    p.K = static_cast<int>(A->K);
+    p.K_pad = static_cast<int>(A->K_pad);
+    p.N = N;
+    p.NC = bp.NC;
+    p.N_pad = bp.N_pad;
+    p.T = A->T;
+    p.h = A->h;
+    p.c_fp32 = c_fp32 ? 1 : 0;
+    p.tile_bytes = A->tile_bytes;
+    p.glu = A->glu;
+    p.P = bp.P;
+    p.pstep = bp.pstep;
+    p.ch[0] = bp.ch[0];
+    p.ch[1] = bp.ch[1];
+    p.n_host_ctas = bp.n_host_ctas;
+    p.n_hbm_ctas = bp.n_hbm_ctas;
+    p.host_window = bp.host_window;
+    p.hbm_window = bp.hbm_window;
+    p.st = status_ptr();
+    if (!p.st) return DAK_ERR_CUDA;
     if (p.h > 0 && !p.a_host) return DAK_ERR_INVALID;
+    if (p.P > 1) {
+        if (ws) {
+            p.cnt = static_cast<int*>(ws);
+            p.part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kCallerCounterBytes);
+        } else if (!split_workspace(&p.part, &p.cnt)) {
+            return DAK_ERR_CUDA;
+        }
+    }
 
     alignas(64) CUtensorMap bmap;
     int b3d = 0;
-    if (!make_b_map(&bmap, B, p.K, N, p.N_pad, kcb, kind, &b3d)) return DAK_ERR_CUDA;
+    if (!make_b_map(&bmap, B, p.K, N, p.N_pad, bp.kcb, bp.umma ? kUmmaB : kCoreB, &b3d)) return DAK_ERR_CUDA;
     p.b3d = b3d;
 
     const bool pdl = t && t->pdl > 0;
     cudaError_t e;
-    if (umma) {
-        e = launch_ex(gemm_umma_kernel, grid, kUmmaThreads, smem, CL, pdl, stream, p, bmap);
+    if (bp.umma) {
+        e = launch_ex(gemm_umma_kernel, bp.grid, kUmmaThreads, bp.smem, bp.NC, pdl, stream, p, bmap);
     } else {
-        e = launch_ex(gemm_core_kernel<1>, grid, kCoreThreads, smem, 1, pdl, stream, p, bmap);
+        e = launch_ex(gemm_core_kernel<1>, bp.grid, kCoreThreads, bp.smem, 1, pdl, stream, p, bmap);
     }
     return cuda_status(e);
 }
@@ -1252,6 +1283,39 @@ extern "C" dak_status dak_gemm(const dak_placement* A, const void* B, void* C, i
 }
 
 extern "C" size_t dak_gemm_workspace_bytes(const dak_placement* A, int N) { return dak::gemm_workspace_bytes(A, N); }
+
+extern "C" dak_status dak_gemm_plan(int64_t M, int64_t K, int n_host_tiles, int N, int sm_count,
+                                    const dak_tuning* tuning, size_t ws_bytes, dak_gemm_plan_info* out) {
+    if (!out) return DAK_ERR_INVALID;
+    *out = dak_gemm_plan_info{};
+    if (M < 1 || K < 8 || (K % 8) || K > (1 << 24) || M > (1ll << 31) || N < 1 || sm_count < 1) return DAK_ERR_INVALID;
+    if (ws_bytes > 0 && static_cast<long long>(ws_bytes) < dak::kCallerCounterBytes) return DAK_ERR_INVALID;
+    const int T = static_cast<int>((M + dak::kTileM - 1) / dak::kTileM);
+    if (n_host_tiles < 0 || n_host_tiles > T) return DAK_ERR_INVALID;
+    const int K_pad = static_cast<int>((K + 15) / 16 * 16);
+    const long long tile_bytes = static_cast<long long>(dak::kTileM) * K_pad * 2;
+    const int block = (tuning && tuning->column_blocks == 1) ? dak::kMaxBlockN : dak::kMaxWideN;
+    dak::BlockPlan bp;
+    const dak_status r = dak::plan_block(T, n_host_tiles, K_pad, tile_bytes, std::min(N, block), sm_count, tuning,
+                                         ws_bytes > 0, ws_bytes, &bp);
+    if (r != DAK_OK) return r;
+    out->tensor_cores = bp.umma ? 1 : 0;
+    out->launches = (N + block - 1) / block;
+    out->cluster = bp.NC;
+    out->n_pad = bp.N_pad;
+    out->pieces = bp.P;
+    out->piece_step = bp.pstep;
+    out->chunk_k = bp.ch[0].kc;
+    out->host_chunk_k = bp.ch[1].kc;
+    out->hbm_stages = bp.ch[0].stages;
+    out->host_stages = bp.ch[1].stages;
+    out->host_ctas = bp.n_host_ctas * bp.NC;
+    out->hbm_ctas = bp.n_hbm_ctas * bp.NC;
+    out->host_window = bp.host_window;
+    out->hbm_window = bp.hbm_window;
+    out->smem_bytes = bp.smem;
+    return DAK_OK;
+}
 
 extern "C" dak_status dak_gemm_ws(const dak_placement* A, const void* B, void* C, int N, int c_fp32,
                                   const dak_tuning* tuning, void* workspace, size_t ws_bytes, void* stream) {

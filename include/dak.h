@@ -186,6 +186,33 @@ size_t dak_gemm_workspace_bytes(const dak_placement* A, int N);
 dak_status dak_gemm_ws(const dak_placement* A, const void* B, void* C, int N, int c_fp32, const dak_tuning* tuning,
                        void* workspace, size_t ws_bytes, void* stream);
 
+/* The launch dak_gemm (ws_bytes == 0) or dak_gemm_ws (a workspace of ws_bytes) would make
+ * for an M x K matrix with n_host_tiles of its 64-row tile rows on the host, N hidden-state
+ * rows and the tuning, on a GPU of sm_count SMs. Host arithmetic only: it needs no GPU and
+ * launches nothing. With more rows than one launch takes, the fields describe the first
+ * launch. DAK_ERR_INVALID: M < 1, K not a positive multiple of 8, n_host_tiles outside
+ * [0, ceil(M / 64)], N < 1, sm_count < 1, a non-zero ws_bytes below 256 KiB, or a tuning
+ * that leaves no valid ring (e.g. chunk_k not a multiple of 64). */
+typedef struct {
+    int tensor_cores;  /* 1: tcgen05 (N >= 2); 0: CUDA-core FMA (N == 1) */
+    int launches;      /* launches (column blocks of hidden-state rows) of the call */
+    int cluster;       /* CTAs per cluster that share each tile row (N > 256) */
+    int n_pad;         /* hidden-state rows of one CTA's tile, padded */
+    int pieces;        /* pieces each tile row's K range is cut into */
+    int piece_step;    /* the pieces are cut at multiples of this many columns */
+    int chunk_k;       /* columns of A per ring stage, CTAs reading HBM */
+    int host_chunk_k;  /* the same for CTAs reading the host tier */
+    int hbm_stages;    /* ring stages, CTAs reading HBM */
+    int host_stages;   /* ring stages, CTAs reading the host tier */
+    int host_ctas;     /* CTAs that stream the host tile rows */
+    int hbm_ctas;      /* CTAs that stream the HBM tile rows */
+    int host_window;   /* stages in flight per host CTA (congestion window) */
+    int hbm_window;    /* stages in flight per HBM CTA */
+    int smem_bytes;    /* dynamic shared memory per CTA */
+} dak_gemm_plan_info;
+dak_status dak_gemm_plan(int64_t M, int64_t K, int n_host_tiles, int N, int sm_count, const dak_tuning* tuning,
+                         size_t ws_bytes, dak_gemm_plan_info* out);
+
 /* Workspace bytes dak_attn needs for B requests, H_q query heads, head dim D and
  * n_split context splits (0 when n_split == 1). */
 size_t dak_attn_workspace_bytes(int B, int H_q, int D, int n_split);

@@ -288,10 +288,11 @@ def test_empty_and_errors(dak):
 
 @pytest.mark.slow
 @pytest.mark.parametrize("name", list(synth.LINEARS_8B))
-@pytest.mark.parametrize("N", [1, 8, 64])
+@pytest.mark.parametrize("N", [1, 8, 16, 32, 64])
 def test_8b_linears_full_size_sampled(dak, name, N):
-    """Full-size 8B-shaped linear at x = 0.25, in the bench's launch configuration; 96
-    sampled output rows (all N columns) against the oracle computed row by row."""
+    """Full-size 8B-shaped linear at x = 0.25 (N = 32: the bench's launch configuration;
+    16: the decode step's batch); 96 sampled output rows (all N columns) against the
+    oracle computed row by row."""
     M, K = synth.LINEARS_8B[name]
     A, B = synth.gemm_inputs(M, K, N, seed=0, tensor_index=list(synth.LINEARS_8B).index(name))
     h = opl.n_host_tiles(0.25, M, 64)

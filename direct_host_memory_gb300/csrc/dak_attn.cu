@@ -347,9 +347,12 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnParams 
 
 // Merge the context splits of every (request, query head) row in split order:
 //   o = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s,  M = max_s m_s.
+// Two forms; the order of every sum depends on the split count alone.
+//
+// A few splits: one warp per row walks the splits in order (lanes over the columns).
 template <int D>
-__global__ void attn_combine_kernel(const float* __restrict__ ws, __nv_bfloat16* __restrict__ O, int rows,
-                                    int n_split) {
+__global__ void attn_combine_warp_kernel(const float* __restrict__ ws, __nv_bfloat16* __restrict__ O, int rows,
+                                         int n_split) {
     grid_dep_launch();
     grid_dep_wait();  // the partials come from the attention kernel just before
     const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -376,19 +379,88 @@ __global__ void attn_combine_kernel(const float* __restrict__ ws, __nv_bfloat16*
     }
 }
 
+// Many splits: one CTA per row. The threads take the splits side by side (the maxima,
+// then the factors and the denominator, then column pairs of o_s in groups of splits), so
+// that every phase is one round trip to L2 whatever the split count; the groups' partial
+// sums are added in group order. (One request over a 4K context: the attention with 16
+// splits 10.7 -> 8.4 us, with 32 splits 13.7 -> 7.1 us; at 2 and 4 splits the warp form
+// is 0.5 us faster.)
+constexpr int kCombineThreads = 256;
+constexpr int kCombineWarpMaxSplits = 4;
+constexpr int kMaxSplits = 1024;
+
+template <int D>
+__global__ void __launch_bounds__(kCombineThreads) attn_combine_cta_kernel(const float* __restrict__ ws,
+                                                                           __nv_bfloat16* __restrict__ O,
+                                                                           int n_split) {
+    constexpr int CG = D / 2;                   // float2 column pairs of a row
+    constexpr int SG = kCombineThreads / CG;    // groups of splits
+    constexpr int NW = kCombineThreads / 32;
+    __shared__ float fs[kMaxSplits];
+    __shared__ float red[SG][D];
+    __shared__ float wred[2][NW];
+    grid_dep_launch();
+    grid_dep_wait();  // the partials come from the attention kernel just before
+    const int row = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float* base = ws + static_cast<long long>(row) * n_split * (D + 2);
+    float M = -INFINITY;
+    for (int s = tid; s < n_split; s += kCombineThreads) M = fmaxf(M, base[s * (D + 2) + D]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if (lane == 0) wred[0][warp] = M;
+    __syncthreads();
+    M = wred[0][0];
+#pragma unroll
+    for (int w = 1; w < NW; ++w) M = fmaxf(M, wred[0][w]);
+    const float mb = M == -INFINITY ? 0.f : M;
+    float l = 0.f;
+    for (int s = tid; s < n_split; s += kCombineThreads) {
+        const float f = exp2f(base[s * (D + 2) + D] - mb);
+        fs[s] = f;
+        l += f * base[s * (D + 2) + D + 1];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    if (lane == 0) wred[1][warp] = l;
+    __syncthreads();
+    float lsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) lsum += wred[1][w];
+    const int c = tid % CG, g = tid / CG;
+    float ax = 0.f, ay = 0.f;
+#pragma unroll 8
+    for (int s = g; s < n_split; s += SG) {
+        const float2 v = *reinterpret_cast<const float2*>(base + s * (D + 2) + 2 * c);
+        ax += fs[s] * v.x;
+        ay += fs[s] * v.y;
+    }
+    red[g][2 * c] = ax;
+    red[g][2 * c + 1] = ay;
+    __syncthreads();
+    for (int d = tid; d < D; d += kCombineThreads) {
+        float acc = 0.f;
+#pragma unroll
+        for (int gg = 0; gg < SG; ++gg) acc += red[gg][d];
+        O[static_cast<long long>(row) * D + d] = __float2bfloat16_rn(lsum > 0.f ? acc / lsum : 0.f);
+    }
+}
+
 constexpr int kAttnDefaultHostCtas = 32;
 constexpr int kAttnDefaultHostWindow = 4;
 constexpr int kAttnStages = 3;     // default ring depth: two CTAs fit on an SM
 constexpr int kAttnMaxStages = 5;
 
-// Context splits: split only until the units fill about 80% of the CTA slots (two CTAs
-// per SM). With every CTA streaming at the same rate, more splits add no token-waves of
-// parallelism, only partial results to merge (measured: 32 requests x 8 kv heads over 8K
-// context ran 1.3% faster unsplit than with 4 splits).
+// Context splits: double the split count while the units fill less than about 80% of the
+// CTA slots (two CTAs per SM) and a split keeps at least 128 tokens. With every CTA
+// streaming at the same rate, more splits add no token-waves of parallelism, only partial
+// results to merge (measured: 32 requests x 8 kv heads over 8K context ran 1.3% faster
+// unsplit than with 4 splits; one request over 4K context ran 7.1 us with 32 splits of 128
+// tokens, 8.4 with 16 of 256, 9.0 with 64).
 static int default_split(int B, int Hkv, int L) {
     const long long slots = 2ll * device_sm_count();
     int n = 1;
-    while (static_cast<long long>(B) * Hkv * n * 5 < slots * 4 && n * 2 * 256 <= L && n < 64) n *= 2;
+    while (static_cast<long long>(B) * Hkv * n * 5 < slots * 4 && n * 2 * 128 <= L && n < 64) n *= 2;
     return n;
 }
 
@@ -437,8 +509,12 @@ static cudaError_t launch_attn_d(const AttnParams& p, int grid, int W, bool pdl,
     e = launch_maybe_pdl(attn_kernel<D>, grid, kAttnThreads, smem, pdl, s, p);
     if (e != cudaSuccess || p.n_split == 1) return e;
     const int rows = p.B * p.Hq;
-    return launch_maybe_pdl(attn_combine_kernel<D>, (rows + 7) / 8, 256, 0, pdl, s,
-                            static_cast<const float*>(p.ws), p.O, rows, p.n_split);
+    if (p.n_split <= kCombineWarpMaxSplits) {
+        return launch_maybe_pdl(attn_combine_warp_kernel<D>, (rows + 7) / 8, 256, 0, pdl, s,
+                                static_cast<const float*>(p.ws), p.O, rows, p.n_split);
+    }
+    return launch_maybe_pdl(attn_combine_cta_kernel<D>, rows, kCombineThreads, 0, pdl, s,
+                            static_cast<const float*>(p.ws), p.O, p.n_split);
 }
 
 dak_status launch_attn(const void* Q, const dak_placement* KV, const void* host_src, const int* seq_lens, int H_q,
@@ -452,9 +528,10 @@ dak_status launch_attn(const void* Q, const dak_placement* KV, const void* host_
     if (cudaGetDevice(&dev) != cudaSuccess) return DAK_ERR_CUDA;
     if (dev != KV->device) return DAK_ERR_INVALID;
     const int n_split = (t && t->n_split > 0) ? t->n_split : default_split(KV->B, KV->H_kv, KV->L);
-    if (n_split > 1024) return DAK_ERR_INVALID;
+    if (n_split > kMaxSplits) return DAK_ERR_INVALID;
     const size_t need = dak_attn_workspace_bytes(KV->B, H_q, KV->D, n_split);
     if (need > 0 && (!ws || ws_bytes < need)) return DAK_ERR_INVALID;
+    if (need > 0 && (reinterpret_cast<uintptr_t>(ws) & 7)) return DAK_ERR_ALIGN;  // the combine reads float2
     if (KV->h_r > 0 && !host_src) return DAK_ERR_INVALID;
 
     AttnParams p{};

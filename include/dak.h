@@ -224,9 +224,9 @@ size_t dak_attn_workspace_bytes(int B, int H_q, int D, int n_split);
  *   seq_lens : int32 [B] (device) with 1 <= L_b <= L, or NULL for all L.
  *   scale    : softmax scale; <= 0 means 1/sqrt(D).
  *   O        : bf16 [B][H_q][D] (device).
- *   workspace: device scratch of dak_attn_workspace_bytes(B, H_q, D, n_split) bytes
- *              (NULL allowed when that is 0), caller-owned; its contents on entry do
- *              not matter.
+ *   workspace: device scratch of dak_attn_workspace_bytes(B, H_q, D, n_split) bytes,
+ *              8-byte aligned (DAK_ERR_ALIGN otherwise; NULL allowed when that size is
+ *              0), caller-owned; its contents on entry do not matter.
  * Requires H_q a multiple of H_kv with H_q / H_kv <= 16. */
 dak_status dak_attn(const void* Q, const dak_placement* KV, const int* seq_lens, int H_q, float scale, void* O,
                     void* workspace, size_t ws_bytes, const dak_tuning* tuning, void* stream);

@@ -47,6 +47,34 @@ def test_context_lengths_and_splits(dak, L, n_split):
     assert og.rel_err(to_np(_run(dak, q, k, v, 1, n_split=n_split)), ref) <= REL_TOL
 
 
+@pytest.mark.parametrize("D,L,n_split", [(128, 4096, 16), (128, 4096, 32), (128, 1000, 64), (64, 2000, 300),
+                                         (128, 700, 1024)])
+def test_many_splits_one_request(dak, D, L, n_split):
+    """One request: the context cut into many splits (some empty when the splits outnumber
+    the 64-token chunks), merged by the combine's split groups."""
+    q, k, v = synth.attn_inputs(1, 32, 8, D, L, seed=n_split)
+    ref = oa.decode_attention_ref(q, k, v)
+    assert og.rel_err(to_np(_run(dak, q, k, v, 0, n_split=n_split)), ref) <= REL_TOL
+    assert og.rel_err(to_np(_run(dak, q, k, v, 1, n_split=n_split)), ref) <= REL_TOL
+
+
+def test_workspace_alignment(dak):
+    import torch
+    q, k, v = synth.attn_inputs(2, 8, 2, 128, 300, seed=5)
+    p = dak.dak_place_kv(k, v, 1)
+    Q = to_dev(q)
+    need = dak.dak_attn_workspace_bytes(2, 8, 128, 4)
+    buf = torch.zeros(need + 64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(dak.DakError) as e:
+        dak.dak_attn(Q, p, workspace=buf[4:4 + need], tuning=dict(n_split=4))
+    assert e.value.status == 2  # DAK_ERR_ALIGN: the merge reads the partials as float2
+    O8 = dak.dak_attn(Q, p, workspace=buf[8:8 + need], tuning=dict(n_split=4))
+    O0 = dak.dak_attn(Q, p, tuning=dict(n_split=4))
+    assert dak.dak_last_error()[0] == 0
+    assert torch.equal(O8, O0)
+    p.free()
+
+
 @pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 4), (16, 4), (32, 4), (64, 4), (16, 1)])
 def test_group_sizes(dak, hq, hkv):
     q, k, v = synth.attn_inputs(2, hq, hkv, 128, 200, seed=hq)

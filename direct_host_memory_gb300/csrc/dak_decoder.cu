@@ -54,6 +54,11 @@ struct dak_decoder {
     size_t ws_bytes;
     void* gemm_ws;         // the GEMMs' split workspace (this decoder's own, zeroed)
     size_t gemm_ws_bytes;
+    // RMSNorms folded into the GEMMs (batch <= 128): the O and down projections add their
+    // product to x and write h = bf16(x * g) and per-tile-row sums of x^2; gate+up and the
+    // next QKV scale their accumulators by 1 / rms
+    bool fuse_norm;
+    float* ss[2];          // [T_d][B] sums of x^2 per 64 hidden units: [0] after O, [1] after down
     // prefetch baseline
     uint8_t* staging[2];
     size_t staging_bytes;
@@ -70,6 +75,7 @@ namespace {
 constexpr int kNormThreads = 256;
 constexpr size_t kGemmWsCounterBytes = 256 * 1024;  // the counter region of a GEMM split workspace
 constexpr int kNormMaxVec = 16;  // float4 per thread: d <= 16384
+constexpr int kFuseNormMaxBatch = 128;  // the GEMMs' fused norm takes up to this many rows
 
 struct NormArgs {
     float* x;                     // [B][d] residual, updated in place
@@ -288,7 +294,7 @@ size_t staging_offset(const dak_decoder_layer& L, int upto) {
 
 void release(dak_decoder* d) {
     void* bufs[] = {d->x, d->h, d->qkv, d->q, d->att, d->ao, d->gu, d->act, d->dn, d->seq_lens, d->rope_cs,
-                    d->inv_freq, d->ws, d->gemm_ws, d->staging[0], d->staging[1]};
+                    d->inv_freq, d->ws, d->gemm_ws, d->staging[0], d->staging[1], d->ss[0], d->ss[1]};
     for (void* p : bufs)
         if (p) cudaFree(p);
     if (d->exec) cudaGraphExecDestroy(d->exec);
@@ -404,7 +410,25 @@ dak_status enqueue_step(dak_decoder* d, const void* x_in, const int* positions, 
             return stg ? static_cast<const void*>(stg + staging_offset(L, i)) : p->host_dev;
         };
         const int Hq = c.n_heads, Hkv = c.n_kv_heads, D = c.head_dim, B = d->B;
-        if ((r = launch_gemm(L.qkv, src(0), d->h, d->qkv, B, 1, &tg[0], s, d->gemm_ws, d->gemm_ws_bytes)) != DAK_OK)
+        // fused norm: the sums of squares the producing projection left, and its tile rows
+        auto consumer = [&](int i) {
+            GemmFuse fz;
+            fz.ss_in = d->ss[i];
+            fz.ss_tiles = (c.hidden + kTileM - 1) / kTileM;
+            fz.inv_d = 1.f / static_cast<float>(c.hidden);
+            fz.eps = c.rms_eps;
+            return fz;
+        };
+        auto producer = [&](int i, const void* g) {
+            GemmFuse fz;
+            fz.res_x = d->x;
+            fz.res_g = g;
+            fz.ss_out = d->ss[i];
+            return fz;
+        };
+        const GemmFuse fz_qkv = consumer(1);
+        if ((r = launch_gemm(L.qkv, src(0), d->h, d->qkv, B, 1, &tg[0], s, d->gemm_ws, d->gemm_ws_bytes,
+                             d->fuse_norm && l > 0 ? &fz_qkv : nullptr)) != DAK_OK)
             return r;
         RopeArgs ra{};
         ra.qkv = d->qkv;
@@ -426,24 +450,34 @@ dak_status enqueue_step(dak_decoder* d, const void* x_in, const int* positions, 
             return r;
         if ((r = launch_attn(d->q, L.kv, src(4), d->seq_lens, Hq, 0.f, d->att, d->ws, d->ws_bytes, &ta, s)) != DAK_OK)
             return r;
-        if ((r = launch_gemm(L.o, src(1), d->att, d->ao, B, 1, &tg[1], s, d->gemm_ws, d->gemm_ws_bytes)) != DAK_OK)
-            return r;
-        NormArgs nb{};
-        nb.x = d->x;
-        nb.delta = d->ao;
-        nb.g = static_cast<const __nv_bfloat16*>(L.mlp_norm);
-        nb.h = d->h;
-        nb.d = c.hidden;
-        nb.eps = c.rms_eps;
-        if ((r = norm(d, nb, 0, pdl, s)) != DAK_OK) return r;
-        if (L.gate_up->glu) {
-            // gate/up interleaved placement: the GEMM's epilogue writes silu(gate) * up itself
-            if ((r = launch_gemm(L.gate_up, src(2), d->h, d->act, B, 0, &tg[2], s, d->gemm_ws, d->gemm_ws_bytes)) !=
+        if (d->fuse_norm) {
+            // x += attention projection, h = bf16(x * g_mlp), sums of x^2 for gate+up
+            const GemmFuse fz = producer(0, L.mlp_norm);
+            if ((r = launch_gemm(L.o, src(1), d->att, d->h, B, 0, &tg[1], s, d->gemm_ws, d->gemm_ws_bytes, &fz)) !=
                 DAK_OK)
                 return r;
         } else {
-            if ((r = launch_gemm(L.gate_up, src(2), d->h, d->gu, B, 1, &tg[2], s, d->gemm_ws, d->gemm_ws_bytes)) !=
-                DAK_OK)
+            if ((r = launch_gemm(L.o, src(1), d->att, d->ao, B, 1, &tg[1], s, d->gemm_ws, d->gemm_ws_bytes)) != DAK_OK)
+                return r;
+            NormArgs nb{};
+            nb.x = d->x;
+            nb.delta = d->ao;
+            nb.g = static_cast<const __nv_bfloat16*>(L.mlp_norm);
+            nb.h = d->h;
+            nb.d = c.hidden;
+            nb.eps = c.rms_eps;
+            if ((r = norm(d, nb, 0, pdl, s)) != DAK_OK) return r;
+        }
+        const GemmFuse fz_gu = consumer(0);
+        const GemmFuse* fgu = d->fuse_norm ? &fz_gu : nullptr;
+        if (L.gate_up->glu) {
+            // gate/up interleaved placement: the GEMM's epilogue writes silu(gate) * up itself
+            if ((r = launch_gemm(L.gate_up, src(2), d->h, d->act, B, 0, &tg[2], s, d->gemm_ws, d->gemm_ws_bytes,
+                                 fgu)) != DAK_OK)
+                return r;
+        } else {
+            if ((r = launch_gemm(L.gate_up, src(2), d->h, d->gu, B, 1, &tg[2], s, d->gemm_ws, d->gemm_ws_bytes,
+                                 fgu)) != DAK_OK)
                 return r;
             const long long n4 = static_cast<long long>(B) * c.ffn / 4;
             const int sg = static_cast<int>(std::min<long long>((n4 + 255) / 256, 4ll * device_sm_count()));
@@ -451,13 +485,22 @@ dak_status enqueue_step(dak_decoder* d, const void* x_in, const int* positions, 
                                         static_cast<const float*>(d->gu), d->act, B, c.ffn))) != DAK_OK)
                 return r;
         }
+        const bool last = l + 1 == nl;
+        if (d->fuse_norm && !last) {
+            // x += down projection, h = bf16(x * g_attn of the next layer), sums for its QKV
+            const GemmFuse fz = producer(1, d->layers[l + 1].attn_norm);
+            if ((r = launch_gemm(L.down, src(3), d->act, d->h, B, 0, &tg[3], s, d->gemm_ws, d->gemm_ws_bytes, &fz)) !=
+                DAK_OK)
+                return r;
+            if (mode == 2 && cudaEventRecord(d->ev_consumed[l & 1], s) != cudaSuccess) return DAK_ERR_CUDA;
+            continue;
+        }
         if ((r = launch_gemm(L.down, src(3), d->act, d->dn, B, 1, &tg[3], s, d->gemm_ws, d->gemm_ws_bytes)) != DAK_OK)
             return r;
         if (mode == 2 && cudaEventRecord(d->ev_consumed[l & 1], s) != cudaSuccess) return DAK_ERR_CUDA;
         NormArgs nc{};
         nc.x = d->x;
         nc.delta = d->dn;
-        const bool last = l + 1 == nl;
         nc.g = static_cast<const __nv_bfloat16*>(last ? d->final_norm : d->layers[l + 1].attn_norm);
         nc.h = last ? static_cast<__nv_bfloat16*>(out) : d->h;
         nc.d = c.hidden;
@@ -552,6 +595,11 @@ extern "C" dak_status dak_decoder_create(const dak_decoder_config* cfg, const da
         chk(cudaMalloc(&dd->gemm_ws, dd->gemm_ws_bytes));
         if (e == cudaSuccess) chk(cudaMemset(dd->gemm_ws, 0, dd->gemm_ws_bytes));
     }
+    dd->fuse_norm = B <= kFuseNormMaxBatch;
+    if (dd->fuse_norm) {
+        const size_t ss_bytes = static_cast<size_t>((d + kTileM - 1) / kTileM) * B * sizeof(float);
+        for (int i = 0; i < 2; ++i) chk(cudaMalloc(reinterpret_cast<void**>(&dd->ss[i]), ss_bytes));
+    }
     if (e == cudaSuccess) {
         std::vector<double> inv(D / 2);
         for (int64_t i = 0; i < D / 2; ++i)
@@ -637,7 +685,10 @@ extern "C" int dak_decoder_launches(const dak_decoder* dec, int mode) {
     (void)mode;
     if (!dec) return 0;
     int n = 1;
-    for (const auto& L : dec->layers) n += 8 + (dec->n_split > 1 ? 1 : 0) + (L.gate_up->glu ? 0 : 1);
+    // per layer: QKV, RoPE + append, attention (+ split merge), O, gate+up (+ SwiGLU), down and
+    // two RMSNorms, of which a fused decoder keeps only the step's last
+    for (const auto& L : dec->layers) n += 6 + (dec->n_split > 1 ? 1 : 0) + (L.gate_up->glu ? 0 : 1) + (dec->fuse_norm ? 0 : 2);
+    if (dec->fuse_norm && !dec->layers.empty()) n += 1;
     return n;
 }
 

@@ -59,7 +59,24 @@ struct GemmParams {
     // Ring layout per role: ch[0] for CTAs reading HBM tiles, ch[1] for CTAs reading host
     // tiles (they differ only for wide B, where host tiles stream A in larger chunks)
     Chunks ch[2];
+    // A decode step's RMSNorm folded into the GEMMs around it (see GemmFuse; null = off)
+    float* res_x;
+    const __nv_bfloat16* res_g;
+    float* ss_out;
+    const float* ss_in;
+    int ss_tiles;
+    float ss_inv_d, ss_eps;
 };
+
+// Fused RMSNorm (the decode step's norms folded into the GEMMs around them):
+//  - a producer GEMM (res_x set) does not output its product: it adds it to the fp32 residual
+//    stream, x[n][row] += acc, stores h[n][row] = bf16(x[n][row] * g[row]) as C (bf16), and
+//    for every tile row t the sums of x^2 over the tile's 64 rows, ss_out[t][n];
+//  - a consumer GEMM (ss_in set) multiplies hidden-state row n's accumulators by
+//    r_n = 1 / sqrt(sum_t ss_in[t][n] / d + eps) before storing them (before SwiGLU).
+// So consumer(h) = RMSNorm(x) * g . A^T with the 1 / rms factor applied after the product.
+constexpr int kFuseMaxN = 128;  // hidden-state rows of a fused launch (one CTA per tile row)
+constexpr int kFusePreloadN = 16;  // up to this many rows, the producer preloads x into registers
 
 // SwiGLU of one gate / up pair (the same expression as the decoder's standalone kernel)
 __device__ __forceinline__ float swiglu_pair(float g, float u) { return g / (1.f + expf(-g)) * u; }
@@ -323,7 +340,13 @@ __device__ __forceinline__ int atomic_add_acq_rel(int* addr, int v) {
 // (gate) and 2j + 1 (up) are held by lanes l and l ^ 1; the even lane writes C[n][j] =
 // silu(gate) * up (C has M / 2 columns). Every lane of the warp calls this.
 template <int N>
-__device__ __forceinline__ void store_row(const GemmParams& p, const float (&acc)[N], int row, bool write) {
+__device__ __forceinline__ void store_row(const GemmParams& p, float (&acc)[N], int row, bool write,
+                                          const float (&rsc)[N], float (&sq)[N], const float (&xpre)[N], float gpre) {
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+        if (p.ss_in) acc[n] *= rsc[n];
+        sq[n] = 0.f;
+    }
     if (p.glu) {
         float up[N];
 #pragma unroll
@@ -341,6 +364,18 @@ __device__ __forceinline__ void store_row(const GemmParams& p, const float (&acc
                 }
             }
         }
+    } else if (p.res_x) {
+        if (write && row < p.M) {
+            const float g = gpre;  // preloaded with x: xpre[n] = x[n][row], gpre = g[row]
+#pragma unroll
+            for (int n = 0; n < N; ++n) {
+                const long long i = static_cast<long long>(n) * p.M + row;
+                const float xn = xpre[n] + acc[n];
+                p.res_x[i] = xn;
+                reinterpret_cast<__nv_bfloat16*>(p.C)[i] = __float2bfloat16_rn(xn * g);
+                sq[n] = xn * xn;
+            }
+        }
     } else if (write && row < p.M) {
 #pragma unroll
         for (int n = 0; n < N; ++n) {
@@ -354,12 +389,47 @@ __device__ __forceinline__ void store_row(const GemmParams& p, const float (&acc
     }
 }
 
+// Fused norm, producer: x[n][row] (n < N) and g[row] of one output row, loaded ahead of the
+// row's accumulators (x is written only by the epilogue that finishes the row's tile row).
+template <int N>
+__device__ __forceinline__ void preload_residual(const GemmParams& p, int row, float (&xpre)[N], float& gpre) {
+    const bool ok = p.res_x && row < p.M;
+#pragma unroll
+    for (int n = 0; n < N; ++n) xpre[n] = ok ? p.res_x[static_cast<long long>(n) * p.M + row] : 0.f;
+    gpre = ok ? __bfloat162float(p.res_g[row]) : 0.f;
+}
+
+// Butterfly sum over the 32 lanes of a warp (every lane gets the total, in a fixed order).
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// r_n of a consumer GEMM computed by one warp: lane l sums tile rows l, l + 32, ... in order,
+// then the butterfly (the GEMV path's order; the tensor-core path has its own, fixed too).
+template <int N>
+__device__ __forceinline__ void warp_row_scales(const GemmParams& p, int lane, float (&rsc)[N]) {
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+        float v = 0.f;
+        if (p.ss_in) {
+            for (int t = lane; t < p.ss_tiles; t += 32) v += p.ss_in[static_cast<long long>(t) * p.N + n];
+        }
+        rsc[n] = rsqrtf(warp_sum(v) * p.ss_inv_d + p.ss_eps);
+    }
+}
+
+// The 256 threads of the eight FMA warps meet (named barrier 2).
+__device__ __forceinline__ void consumer_bar_sync() { asm volatile("bar.sync 2, 256;" ::: "memory"); }
+
 template <int N>
 __global__ void __launch_bounds__(kCoreThreads, 1)
     gemm_core_kernel(const GemmParams p, const __grid_constant__ CUtensorMap bmap) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];  // one declaration for both GEMM kernels
     __shared__ uint64_t full[8], empty[8];
     __shared__ uint64_t done[kCoreDone], freed[kCoreDone];  // split: partial rows stored / finisher done
+    __shared__ float ssw[kCoreConsumers][N];                // fused norm: each consumer warp's 8 rows
     __shared__ int abort_flag;
     volatile int* abort = &abort_flag;
 
@@ -393,6 +463,8 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
         if (p.P == 1) return;
         // finisher: lane l sums rows l and l + 32 of a tile row whose last piece this CTA ran
         grid_dep_wait();  // the split workspace may still be in use by the previous kernel
+        float rsc[N];
+        warp_row_scales<N>(p, lane, rsc);
         for (int ui = 0; ui < it.count; ++ui) {
             const int j = ui % kCoreDone;
             if (!mbar_wait(&done[j], static_cast<uint32_t>((ui / kCoreDone) & 1), abort, p.st, DAK_ERR_TIMEOUT,
@@ -400,6 +472,9 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
                 return;
             }
             const Piece pc = piece_of(p, it, ui);
+            float xp[2][N], gp[2];
+            preload_residual<N>(p, pc.t * kTileM + lane, xp[0], gp[0]);
+            preload_residual<N>(p, pc.t * kTileM + lane + 32, xp[1], gp[1]);
             int last = 0;
             if (lane == 0) {
                 __threadfence();
@@ -410,16 +485,28 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
             __syncwarp();
             if (last) {
                 const float* src = p.part + static_cast<long long>(pc.t) * p.P * tile_floats;
+                float ssl[N];
+#pragma unroll
+                for (int n = 0; n < N; ++n) ssl[n] = 0.f;
                 for (int h = 0; h < 2; ++h) {
                     const int rr = lane + 32 * h;
-                    float acc[N];
+                    float acc[N], sq[N];
 #pragma unroll
                     for (int n = 0; n < N; ++n) {
                         float v = __ldcg(src + rr * p.N_pad + n);
                         for (int r = 1; r < p.P; ++r) v += __ldcg(src + static_cast<long long>(r) * tile_floats + rr * p.N_pad + n);
                         acc[n] = v;
                     }
-                    store_row<N>(p, acc, pc.t * kTileM + rr, true);
+                    store_row<N>(p, acc, pc.t * kTileM + rr, true, rsc, sq, h ? xp[1] : xp[0], h ? gp[1] : gp[0]);
+#pragma unroll
+                    for (int n = 0; n < N; ++n) ssl[n] += sq[n];
+                }
+                if (p.res_x) {
+#pragma unroll
+                    for (int n = 0; n < N; ++n) {
+                        const float tot = warp_sum(ssl[n]);
+                        if (lane == 0) p.ss_out[static_cast<long long>(pc.t) * p.N + n] = tot;
+                    }
                 }
             }
             __syncwarp();
@@ -430,20 +517,28 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
 
     // consumers (C may be read by the previous kernel of the stream: wait before writing it)
     grid_dep_wait();
+    float rsc[N];
+    warp_row_scales<N>(p, lane, rsc);
     const int w = warp - 2;       // row group 0..7
     const int r = lane & 7;       // row within the group
     const int kq = lane >> 3;     // k-group phase 0..3
     long long i = 0;
+    // after a wait that ran out, a fused launch's consumers skip the work but keep meeting
+    // their named barrier, so that no warp is left waiting for one that gave up
+    bool failed = false;
     for (int ui = 0; ui < it.count; ++ui) {
         const Piece q = piece_of(p, it, ui);
         const int t = q.t;
-        float acc[N];
+        float acc[N], xp[N], gp = 0.f;
+        if (p.P == 1) preload_residual<N>(p, t * kTileM + w * 8 + r, xp, gp);
 #pragma unroll
         for (int n = 0; n < N; ++n) acc[n] = 0.f;
-        for (int k0 = q.k0; k0 < q.k1; k0 += it.c.kc, ++i) {
+        for (int k0 = q.k0; k0 < q.k1 && !failed; k0 += it.c.kc, ++i) {
             const int s = static_cast<int>(i % W);
             if (!mbar_wait(&full[s], static_cast<uint32_t>((i / W) & 1), abort, p.st, DAK_ERR_TIMEOUT, W_CONS_FULL)) {
-                return;
+                if (!(p.res_x && p.P == 1)) return;
+                failed = true;
+                break;
             }
             const int kgr = min(min(it.c.kc, q.k1 - k0), p.K - k0) >> 3;  // real k-groups in this chunk
             const uint8_t* st = smem + static_cast<size_t>(s) * it.c.stage_bytes;
@@ -482,7 +577,24 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
         }
         const int row = t * kTileM + w * 8 + r;
         if (p.P == 1) {
-            store_row<N>(p, acc, row, kq == 0);
+            float sq[N];
+            store_row<N>(p, acc, row, kq == 0 && !failed, rsc, sq, xp, gp);
+            if (p.res_x) {
+                // the tile row's sums of x^2: each warp's 8 rows, then the 8 warps in order
+#pragma unroll
+                for (int n = 0; n < N; ++n) {
+                    const float v = warp_sum(sq[n]);
+                    if (lane == 0) ssw[w][n] = v;
+                }
+                consumer_bar_sync();
+                if (w == 0 && lane < N) {
+                    float tot = 0.f;
+#pragma unroll
+                    for (int ww = 0; ww < kCoreConsumers; ++ww) tot += ssw[ww][lane];
+                    p.ss_out[static_cast<long long>(t) * p.N + lane] = tot;
+                }
+                consumer_bar_sync();  // ssw is rewritten by the next tile row
+            }
             continue;
         }
         // split tile row: this unit's partial rows to the workspace, then tell the finisher
@@ -544,7 +656,14 @@ constexpr int kMinPieceSteps = 8;   // 64-column steps of an automatically chose
 // fp32 or bf16. With a SwiGLU placement, rows 2j (gate) and 2j + 1 (up) are held by lanes l
 // and l ^ 1: the even lane writes C[n][j] = silu(gate) * up (C has M / 2 columns). Every lane
 // of the warp calls this (the pairing is a shuffle).
-__device__ __forceinline__ void store_c(const GemmParams& p, const float (&f)[8], int row, bool valid, int n_base) {
+__device__ __forceinline__ void store_c(const GemmParams& p, float (&f)[8], int row, bool valid, int n_base,
+                                        const float* rsc, float (&sq)[8], const float* xpre = nullptr,
+                                        float gpre = 0.f) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        if (rsc && n_base + j < p.N) f[j] *= rsc[n_base + j];
+        sq[j] = 0.f;
+    }
     if (p.glu) {
         float up[8];
 #pragma unroll
@@ -562,6 +681,22 @@ __device__ __forceinline__ void store_c(const GemmParams& p, const float (&f)[8]
                         reinterpret_cast<__nv_bfloat16*>(p.C)[static_cast<long long>(n) * half + col] =
                             __float2bfloat16_rn(a);
                     }
+                }
+            }
+        }
+    } else if (p.res_x) {
+        if (valid) {
+            // x and g come preloaded (xpre: this block's 8 values) or are read here
+            const float g = xpre ? gpre : __bfloat162float(p.res_g[row]);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int n = n_base + j;
+                if (n < p.N) {
+                    const long long i = static_cast<long long>(n) * p.M + row;
+                    const float xn = (xpre ? xpre[j] : p.res_x[i]) + f[j];
+                    p.res_x[i] = xn;
+                    reinterpret_cast<__nv_bfloat16*>(p.C)[i] = __float2bfloat16_rn(xn * g);
+                    sq[j] = xn * xn;
                 }
             }
         }
@@ -588,6 +723,19 @@ __device__ __forceinline__ void epilogue_bar_sync() { asm volatile("bar.sync 1, 
 // sit in lanes 32q .. 32q+15 of sub-partition q.
 __device__ __forceinline__ int umma_m64_row_of_lane(int q, int lane) { return lane < 16 ? q * 16 + lane : -1; }
 
+// Fused norm, producer: the tile row's sums of x^2 per hidden-state row from the warps'
+// partial sums (slots in order), written by thread e = n. Every epilogue thread calls this.
+__device__ __forceinline__ void fuse_tile_sums(const GemmParams& p, const float (*ssw)[kFuseMaxN], int t, int e,
+                                               int slots) {
+    epilogue_bar_sync();  // every warp's sums are in
+    if (e < p.N) {
+        float v = 0.f;
+        for (int k = 0; k < slots; ++k) v += ssw[k][e];
+        p.ss_out[static_cast<long long>(t) * p.N + e] = v;
+    }
+    epilogue_bar_sync();  // the slots are rewritten by the next tile row
+}
+
 __global__ void __launch_bounds__(kUmmaThreads, 1)
     gemm_umma_kernel(const GemmParams p, const __grid_constant__ CUtensorMap bmap) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -597,6 +745,9 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
     __shared__ int last_piece;  // split tile rows: this CTA finished the tile row's last piece
+    __shared__ float fuse_ssw[4][kFuseMaxN];  // fused norm, producer: each warp's partial sums of x^2
+    __shared__ float fuse_red[kFuseMaxN];     // fused norm, consumer: groups' partial sums
+    __shared__ float fuse_r[kFuseMaxN];       // fused norm, consumer: r_n
     volatile int* abort = &abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -744,17 +895,63 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         // its fp32 partial tile in the workspace and counts the piece in; the CTA that counts
         // the last one adds the P partials in piece order (a fixed order, whichever CTA ran
         // which piece and whatever the placement) and writes C. No CTA waits for another.
+        // After a wait that ran out, a warp skips the work but keeps meeting the epilogue's
+        // named barriers, so that no warp is left waiting for one that gave up.
         const int qp = warp & 3;
         const int row_in_tile = umma_m64_row_of_lane(qp, lane);
         const int n_off = p.NC > 1 ? it.rank * p.N_pad : 0;  // first hidden-state row of this CTA's block
         const int tile_floats = kTileM * p.N_pad;
+        const int e = threadIdx.x - 64;  // 0..127
         grid_dep_wait();  // C and the split workspace may still be in use by the previous kernel of the stream
+        const float* rsc = nullptr;
+        if (p.ss_in) {
+            // r_n of the consumed normalisation: thread e sums tile rows gi, gi + G, ... of one
+            // n in order (G groups), then the groups in order (host-checked N <= kFuseMaxN)
+            const int G = max(1, 128 / p.N);
+            if (e < G * p.N) {
+                const int n = e % p.N, gi = e / p.N;
+                float v = 0.f;
+                for (int t = gi; t < p.ss_tiles; t += G) v += p.ss_in[static_cast<long long>(t) * p.N + n];
+                fuse_red[gi * p.N + n] = v;
+            }
+            epilogue_bar_sync();
+            if (e < p.N) {
+                float v = 0.f;
+                for (int gi = 0; gi < G; ++gi) v += fuse_red[gi * p.N + e];
+                fuse_r[e] = rsqrtf(v * p.ss_inv_d + p.ss_eps);
+            }
+            epilogue_bar_sync();
+            rsc = fuse_r;
+        }
+        bool failed = false;
+        // fused norm, producer, up to 16 hidden-state rows: the residual values this thread
+        // adds to and the gain, loaded before the accumulator is ready (a round trip to L2
+        // off the tile row's tail); x is written only by the epilogue that finishes a tile row
+        const bool xpre_on = p.res_x && p.N_pad <= kFusePreloadN;
+        float xpre[kFusePreloadN];
+        float gpre = 0.f;
         for (int ui = 0; ui < it.count; ++ui) {
             const int ab = ui & 1;
-            if (!mbar_wait(&acc_full[ab], static_cast<uint32_t>((ui >> 1) & 1), abort, p.st, DAK_ERR_TIMEOUT,
-                           W_EPI_ACC)) {
-                break;
+            if (xpre_on) {
+                const int t = piece_of(p, it, ui).t;
+                // the split path's thread e holds row e % 64 and the 8 columns from 8 (e / 64);
+                // the one-piece path holds row_in_tile and every column
+                const int xrow = t * kTileM + (p.P > 1 ? (e & 63) : row_in_tile);
+                const int xn0 = p.P > 1 ? 8 * (e >> 6) : 0;
+                const bool ok = (p.P > 1 || row_in_tile >= 0) && xrow < p.M;
+#pragma unroll
+                for (int j = 0; j < kFusePreloadN; ++j) {
+                    const int n = xn0 + j;
+                    xpre[j] = (ok && j < (p.P > 1 ? 8 : p.N_pad) && n < p.N) ? p.res_x[static_cast<long long>(n) * p.M + xrow]
+                                                                            : 0.f;
+                }
+                gpre = ok ? __bfloat162float(p.res_g[xrow]) : 0.f;
             }
+            if (!failed && !mbar_wait(&acc_full[ab], static_cast<uint32_t>((ui >> 1) & 1), abort, p.st,
+                                      DAK_ERR_TIMEOUT, W_EPI_ACC)) {
+                failed = true;
+            }
+            if (failed && p.P == 1 && !p.res_x) break;  // no barrier to keep meeting
             tc_fence_after();
             const Piece pc = piece_of(p, it, ui);
             const int row = pc.t * kTileM + row_in_tile;
@@ -762,7 +959,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
             const uint32_t taddr = tmem + (static_cast<uint32_t>(qp * 32) << 16) + static_cast<uint32_t>(ab) * acc_stride;
             if (p.P > 1) {
                 float* mine = p.part + (static_cast<long long>(pc.t) * p.P + pc.idx) * tile_floats;
-                for (int n0 = 0; n0 < p.N_pad; n0 += 8) {
+                for (int n0 = 0; n0 < p.N_pad && !failed; n0 += 8) {
                     uint32_t v[8];
                     tmem_ld8(taddr + static_cast<uint32_t>(n0), v);
                     tmem_wait_ld();
@@ -776,22 +973,24 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&acc_empty[ab]);  // the accumulator is free again
+                if (lane == 0 && !failed) mbar_arrive(&acc_empty[ab]);  // the accumulator is free again
                 // One thread counts the piece in, with release semantics for the 128 threads'
                 // stores (ordered before it by the barrier) and acquire semantics for the other
                 // pieces' partials, which the last piece's CTA reads next.
                 epilogue_bar_sync();
                 if (warp == 2 && lane == 0) {
-                    const int done = atomic_add_acq_rel(p.cnt + pc.t, 1) + 1;
-                    last_piece = done == p.P;
-                    if (done == p.P) p.cnt[pc.t] = 0;  // ready for the next launch
+                    last_piece = 0;
+                    if (!failed) {
+                        const int done = atomic_add_acq_rel(p.cnt + pc.t, 1) + 1;
+                        last_piece = done == p.P;
+                        if (done == p.P) p.cnt[pc.t] = 0;  // ready for the next launch
+                    }
                 }
                 epilogue_bar_sync();
                 if (!last_piece) continue;
                 // The P partials, added in piece order. All 128 threads share the work: thread e
                 // takes row e % 64 and the 8-column blocks e / 64, e / 64 + 2, ...; lanes e and
                 // e ^ 1 hold rows 2j and 2j + 1 (the gate / up pair of a SwiGLU placement).
-                const int e = threadIdx.x - 64;
                 const int rr = e & 63;
                 const int rrow = pc.t * kTileM + rr;
                 const float* src0 = p.part + static_cast<long long>(pc.t) * p.P * tile_floats + rr * p.N_pad;
@@ -819,22 +1018,49 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
                             }
                         }
                     }
-                    store_c(p, f, rrow, rrow < p.M, n_off + blk * 8);
+                    float sq[8];
+                    store_c(p, f, rrow, rrow < p.M, n_off + blk * 8, rsc, sq, xpre_on ? xpre : nullptr, gpre);
+                    if (p.res_x) {
+                        // rows 32 w2 .. 32 w2 + 31 of this block: one sum per column
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float v = warp_sum(sq[j]);
+                            if (lane == 0) fuse_ssw[(e >> 5) & 1][blk * 8 + j] = v;
+                        }
+                    }
                 }
+                if (p.res_x) fuse_tile_sums(p, fuse_ssw, pc.t, e, 2);
                 continue;
             }
             for (int n0 = 0; n0 < p.N_pad; n0 += 8) {
-                uint32_t v[8];
-                tmem_ld8(taddr + static_cast<uint32_t>(n0), v);
-                tmem_wait_ld();
                 float f[8];
+                if (!failed) {
+                    uint32_t v[8];
+                    tmem_ld8(taddr + static_cast<uint32_t>(n0), v);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(v[j]);
-                store_c(p, f, row, valid, n_off + n0);
+                    for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(v[j]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) f[j] = 0.f;
+                }
+                float sq[8], xb[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) xb[j] = n0 == 0 ? xpre[j] : xpre[8 + j];  // registers, not a stack copy
+                store_c(p, f, row, valid && !failed, n_off + n0, rsc, sq, xpre_on ? xb : nullptr, gpre);
+                if (p.res_x) {
+                    // rows 16 qp .. 16 qp + 15 (lanes 0..15): one sum per column
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float v = warp_sum(sq[j]);
+                        if (lane == 0) fuse_ssw[qp][n0 + j] = v;
+                    }
+                }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[ab]);
+            if (lane == 0 && !failed) mbar_arrive(&acc_empty[ab]);
+            if (p.res_x) fuse_tile_sums(p, fuse_ssw, pc.t, e, 4);
         }
     }
 
@@ -1182,7 +1408,8 @@ static dak_status plan_block(int T, int h, int K_pad, long long tile_bytes, int 
 // One launch over up to kMaxWideN hidden-state rows: one CTA per tile row up to 256 rows
 // (the widest tcgen05 tile used here), a cluster of ceil(N / 256) CTAs per tile row beyond.
 static dak_status launch_gemm_block(const dak_placement* A, const void* host_src, const void* B, void* C, int N,
-                                    int c_fp32, const dak_tuning* t, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                                    int c_fp32, const dak_tuning* t, void* ws, size_t ws_bytes, cudaStream_t stream,
+                                    const GemmFuse* fuse) {
     if (!A || A->kind != 0) return DAK_ERR_INVALID;
     if (N < 1 || N > kMaxWideN) return DAK_ERR_INVALID;
     if (A->M == 0 || A->T == 0) return DAK_OK;  // nothing to compute; C may be empty
@@ -1225,6 +1452,22 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
     p.st = status_ptr();
     if (!p.st) return DAK_ERR_CUDA;
     if (p.h > 0 && !p.a_host) return DAK_ERR_INVALID;
+    if (fuse && (fuse->res_x || fuse->ss_in)) {
+        if (N > kFuseMaxN || bp.NC != 1) return DAK_ERR_UNSUPPORTED;
+        if (fuse->res_x) {
+            if (p.glu || c_fp32 || !fuse->res_g || !fuse->ss_out) return DAK_ERR_INVALID;
+            p.res_x = fuse->res_x;
+            p.res_g = static_cast<const __nv_bfloat16*>(fuse->res_g);
+            p.ss_out = fuse->ss_out;
+        }
+        if (fuse->ss_in) {
+            if (fuse->ss_tiles < 1) return DAK_ERR_INVALID;
+            p.ss_in = fuse->ss_in;
+            p.ss_tiles = fuse->ss_tiles;
+            p.ss_inv_d = fuse->inv_d;
+            p.ss_eps = fuse->eps;
+        }
+    }
     if (p.P > 1) {
         if (ws) {
             p.cnt = static_cast<int*>(ws);
@@ -1256,11 +1499,12 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
 // again. Clusters stop at 4 CTAs: forwarding every A chunk to 7 peers measured slower than
 // two launches of 1024 rows.
 dak_status launch_gemm(const dak_placement* A, const void* host_src, const void* B, void* C, int N, int c_fp32,
-                       const dak_tuning* t, cudaStream_t stream, void* ws, size_t ws_bytes) {
+                       const dak_tuning* t, cudaStream_t stream, void* ws, size_t ws_bytes, const GemmFuse* fuse) {
     if (!A || A->kind != 0) return DAK_ERR_INVALID;
     if (ws && (reinterpret_cast<uintptr_t>(ws) & 255)) return DAK_ERR_ALIGN;
     const int block = (t && t->column_blocks == 1) ? kMaxBlockN : kMaxWideN;
-    if (N <= block) return launch_gemm_block(A, host_src, B, C, N, c_fp32, t, ws, ws_bytes, stream);
+    if (N <= block) return launch_gemm_block(A, host_src, B, C, N, c_fp32, t, ws, ws_bytes, stream, fuse);
+    if (fuse && (fuse->res_x || fuse->ss_in)) return DAK_ERR_UNSUPPORTED;
     if (!B || !C) return DAK_ERR_INVALID;
     const size_t b_row = static_cast<size_t>(A->K) * 2;
     const size_t c_row = static_cast<size_t>(A->glu ? A->M / 2 : A->M) * (c_fp32 ? 4 : 2);
@@ -1268,7 +1512,7 @@ dak_status launch_gemm(const dak_placement* A, const void* host_src, const void*
         const int nb = std::min(block, N - n0);
         const dak_status r = launch_gemm_block(A, host_src, static_cast<const uint8_t*>(B) + n0 * b_row,
                                                static_cast<uint8_t*>(C) + n0 * c_row, nb, c_fp32, t, ws, ws_bytes,
-                                               stream);
+                                               stream, nullptr);
         if (r != DAK_OK) return r;
     }
     return DAK_OK;

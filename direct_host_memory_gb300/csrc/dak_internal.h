@@ -62,8 +62,23 @@ dak_status cuda_status(cudaError_t e);
 
 // kernel launchers (defined in dak_gemm.cu / dak_attn.cu)
 // ws / ws_bytes: the caller's split workspace (dak_gemm_ws), or null for the module's own
+// A decode step's RMSNorm folded into the GEMMs around it (all members null = off).
+// Producer (res_x): the launch adds its product to the fp32 residual x [N][M] in place and
+// writes C = bf16(x * g) (bf16 [N][M]) and ss_out [T][N], the sums of x^2 over each tile
+// row's 64 rows. Consumer (ss_in): the accumulators of hidden-state row n are multiplied by
+// 1 / sqrt(sum_t ss_in[t][n] * inv_d + eps) (t < ss_tiles) before they are stored. N <= 128.
+struct GemmFuse {
+    float* res_x = nullptr;
+    const void* res_g = nullptr;  // bf16 [M]
+    float* ss_out = nullptr;
+    const float* ss_in = nullptr;
+    int ss_tiles = 0;
+    float inv_d = 0.f, eps = 0.f;
+};
+
 dak_status launch_gemm(const dak_placement* A, const void* host_src, const void* B, void* C, int N, int c_fp32,
-                       const dak_tuning* t, cudaStream_t s, void* ws = nullptr, size_t ws_bytes = 0);
+                       const dak_tuning* t, cudaStream_t s, void* ws = nullptr, size_t ws_bytes = 0,
+                       const GemmFuse* fuse = nullptr);
 size_t gemm_workspace_bytes(const dak_placement* A, int N);
 dak_status launch_attn(const void* Q, const dak_placement* KV, const void* host_src, const int* seq_lens, int H_q,
                        float scale, void* O, void* ws, size_t ws_bytes, const dak_tuning* t, cudaStream_t s);

@@ -81,6 +81,21 @@ def _run(dak, dec, x0, pos, mode=0, graph=False):
     return out
 
 
+def test_decoder_large_batch_separate_norms(dak):
+    """More requests than the GEMMs' folded RMSNorm takes (128): the step keeps its separate
+    RMSNorm kernels, with the same results against the oracle."""
+    cfg, B, L = SMALL64, 130, 80
+    pos = [(7 * b) % L for b in range(B)]
+    layers, caches, fnorm, x0 = _inputs(cfg, B, L, seed=21)
+    ref, _ = od.decode_step(_ocfg(cfg), x0, layers, caches, np.array(pos), fnorm)
+    dec = _build(dak, cfg, layers, caches, fnorm, _host_units(cfg, B, 0.3))
+    combine = 1 if dak.dak_attn_default_split(dec.layers[0]["kv"]) > 1 else 0
+    assert dec.launches() == 1 + cfg["n_layers"] * (8 + combine)
+    out = _run(dak, dec, x0, pos)
+    assert og.rel_err(to_np(out), ref) <= REL_TOL
+    dec.free()
+
+
 @pytest.mark.parametrize("cfg,B,L,pos", [
     (SMALL64, 5, 200, [0, 63, 64, 130, 199]),
     (SMALL128, 3, 300, [299, 0, 128]),
@@ -126,7 +141,9 @@ def test_decoder_fused_swiglu_matches_separate_kernel(dak):
         dec = _build(dak, cfg, layers, caches, fnorm, _host_units(cfg, B, 0.3), glu=glu)
         outs.append(bits_of(_run(dak, dec, x0, pos)))
         combine = 1 if dak.dak_attn_default_split(dec.layers[0]["kv"]) > 1 else 0
-        assert dec.launches() == 1 + cfg["n_layers"] * (8 + combine + (0 if glu else 1))
+        # the first RMSNorm, per layer QKV, RoPE + append, attention (+ merge), O, gate+up
+        # (+ SwiGLU), down; the mid-layer norms are folded into the GEMMs, the last one stays
+        assert dec.launches() == 1 + cfg["n_layers"] * (6 + combine + (0 if glu else 1)) + 1
         dec.free()
     assert np.array_equal(outs[0], outs[1])
 
@@ -195,12 +212,15 @@ def test_decoder_errors(dak):
 
 
 @pytest.mark.slow
-def test_decoder_8b_width_two_layers(dak):
-    """Two layers at the 8B shape (hidden 4096, GQA 32/8, FFN 14336), 16 requests with
-    contexts up to 4096, every operation offloaded about 30% as the planner does at
-    x_global = 0.3, in the launch configuration the benchmark times."""
-    cfg = dict(synth.DECODER_8B, n_layers=2)
-    B, L = cfg["batch"], cfg["context"]
+@pytest.mark.parametrize("B", [16, 1])
+def test_decoder_8b_width_two_layers(dak, B):
+    """Two layers at the 8B shape (hidden 4096, GQA 32/8, FFN 14336), 16 requests (or one)
+    with contexts up to 4096, every operation offloaded about 30% as the planner does at
+    x_global = 0.3, in the launch configuration the benchmark times. At this width the O and
+    down projections split their tile rows into pieces, so the folded RMSNorms run in the
+    epilogues that add the pieces (tensor cores at 16 requests, the GEMV's finisher at one)."""
+    cfg = dict(synth.DECODER_8B, n_layers=2, batch=B)
+    L = cfg["context"]
     pos = np.array([L - 1 - 97 * b for b in range(B)])
     layers, caches, fnorm, x0 = _inputs(cfg, B, L, seed=0)
     dec = _build(dak, cfg, layers, caches, fnorm, _host_units(cfg, B, 0.3))

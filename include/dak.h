@@ -355,9 +355,14 @@ int dak_decoder_batch(const dak_decoder* dec);
  *     x += attention(q; cache positions 0..pos) Wo^T; h = rmsnorm(x) g_mlp;
  *     x += (silu(gate) * up) Wdown^T          with [gate|up] = h Wgu^T,
  * then out = rmsnorm(x) g_final. The weight products are dak_gemm and the attention is
- * dak_attn over the tiered placements; RMSNorm, RoPE + KV append and SwiGLU are small
- * kernels of this library. The residual stream x is fp32; h, q, the attention output and
- * silu(gate) * up are bf16; projections accumulate in fp32.
+ * dak_attn over the tiered placements; RoPE + KV append, SwiGLU (for a placement made
+ * without the gate/up interleave) and the first and last RMSNorm are small kernels of this
+ * library. With B <= 128 the mid-layer RMSNorms are folded into the GEMMs around them: the
+ * O and down projections add their product to x and store h = bf16(x * g) with per-64-row
+ * sums of x^2, and gate+up and the next QKV multiply their fp32 accumulators by
+ * 1 / sqrt(mean(x^2) + eps) (so h carries the gain but not the 1/rms factor). The residual
+ * stream x is fp32; h, q, the attention output and silu(gate) * up are bf16; projections
+ * accumulate in fp32.
  *   x_in     : bf16 [B][d] (device), the hidden states entering layer 0.
  *   positions: int32 [B] (device), the position of each request's new token, 0 <= pos < L
  *              (a position outside the cache is skipped and reported as DAK_ERR_BOUNDS by

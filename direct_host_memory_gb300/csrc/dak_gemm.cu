@@ -340,11 +340,12 @@ __device__ __forceinline__ int atomic_add_acq_rel(int* addr, int v) {
 // (gate) and 2j + 1 (up) are held by lanes l and l ^ 1; the even lane writes C[n][j] =
 // silu(gate) * up (C has M / 2 columns). Every lane of the warp calls this.
 template <int N>
-__device__ __forceinline__ void store_row(const GemmParams& p, float (&acc)[N], int row, bool write,
-                                          const float (&rsc)[N], float (&sq)[N], const float (&xpre)[N], float gpre) {
+__device__ __forceinline__ void store_row(const GemmParams& p, float (&acc)[N], int row, bool write, bool fx,
+                                          bool fr, const float (&rsc)[N], float (&sq)[N], const float (&xpre)[N],
+                                          float gpre) {
 #pragma unroll
     for (int n = 0; n < N; ++n) {
-        if (p.ss_in) acc[n] *= rsc[n];
+        if (fr) acc[n] *= rsc[n];
         sq[n] = 0.f;
     }
     if (p.glu) {
@@ -364,7 +365,7 @@ __device__ __forceinline__ void store_row(const GemmParams& p, float (&acc)[N], 
                 }
             }
         }
-    } else if (p.res_x) {
+    } else if (fx) {
         if (write && row < p.M) {
             const float g = gpre;  // preloaded with x: xpre[n] = x[n][row], gpre = g[row]
 #pragma unroll
@@ -392,8 +393,9 @@ __device__ __forceinline__ void store_row(const GemmParams& p, float (&acc)[N], 
 // Fused norm, producer: x[n][row] (n < N) and g[row] of one output row, loaded ahead of the
 // row's accumulators (x is written only by the epilogue that finishes the row's tile row).
 template <int N>
-__device__ __forceinline__ void preload_residual(const GemmParams& p, int row, float (&xpre)[N], float& gpre) {
-    const bool ok = p.res_x && row < p.M;
+__device__ __forceinline__ void preload_residual(const GemmParams& p, bool fx, int row, float (&xpre)[N],
+                                                 float& gpre) {
+    const bool ok = fx && row < p.M;
 #pragma unroll
     for (int n = 0; n < N; ++n) xpre[n] = ok ? p.res_x[static_cast<long long>(n) * p.M + row] : 0.f;
     gpre = ok ? __bfloat162float(p.res_g[row]) : 0.f;
@@ -409,11 +411,11 @@ __device__ __forceinline__ float warp_sum(float v) {
 // r_n of a consumer GEMM computed by one warp: lane l sums tile rows l, l + 32, ... in order,
 // then the butterfly (the GEMV path's order; the tensor-core path has its own, fixed too).
 template <int N>
-__device__ __forceinline__ void warp_row_scales(const GemmParams& p, int lane, float (&rsc)[N]) {
+__device__ __forceinline__ void warp_row_scales(const GemmParams& p, bool fr, int lane, float (&rsc)[N]) {
 #pragma unroll
     for (int n = 0; n < N; ++n) {
         float v = 0.f;
-        if (p.ss_in) {
+        if (fr) {
             for (int t = lane; t < p.ss_tiles; t += 32) v += p.ss_in[static_cast<long long>(t) * p.N + n];
         }
         rsc[n] = rsqrtf(warp_sum(v) * p.ss_inv_d + p.ss_eps);
@@ -423,9 +425,12 @@ __device__ __forceinline__ void warp_row_scales(const GemmParams& p, int lane, f
 // The 256 threads of the eight FMA warps meet (named barrier 2).
 __device__ __forceinline__ void consumer_bar_sync() { asm volatile("bar.sync 2, 256;" ::: "memory"); }
 
-template <int N>
+template <int N, bool F>
 __global__ void __launch_bounds__(kCoreThreads, 1)
     gemm_core_kernel(const GemmParams p, const __grid_constant__ CUtensorMap bmap) {
+    // the folded norm's code exists only in the F = true instantiation
+    const bool fx = F && p.res_x != nullptr;
+    const bool fr = F && p.ss_in != nullptr;
     extern __shared__ __align__(1024) uint8_t smem_raw[];  // one declaration for both GEMM kernels
     __shared__ uint64_t full[8], empty[8];
     __shared__ uint64_t done[kCoreDone], freed[kCoreDone];  // split: partial rows stored / finisher done
@@ -464,7 +469,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
         // finisher: lane l sums rows l and l + 32 of a tile row whose last piece this CTA ran
         grid_dep_wait();  // the split workspace may still be in use by the previous kernel
         float rsc[N];
-        warp_row_scales<N>(p, lane, rsc);
+        warp_row_scales<N>(p, fr, lane, rsc);
         for (int ui = 0; ui < it.count; ++ui) {
             const int j = ui % kCoreDone;
             if (!mbar_wait(&done[j], static_cast<uint32_t>((ui / kCoreDone) & 1), abort, p.st, DAK_ERR_TIMEOUT,
@@ -473,8 +478,8 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
             }
             const Piece pc = piece_of(p, it, ui);
             float xp[2][N], gp[2];
-            preload_residual<N>(p, pc.t * kTileM + lane, xp[0], gp[0]);
-            preload_residual<N>(p, pc.t * kTileM + lane + 32, xp[1], gp[1]);
+            preload_residual<N>(p, fx, pc.t * kTileM + lane, xp[0], gp[0]);
+            preload_residual<N>(p, fx, pc.t * kTileM + lane + 32, xp[1], gp[1]);
             int last = 0;
             if (lane == 0) {
                 __threadfence();
@@ -497,11 +502,12 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
                         for (int r = 1; r < p.P; ++r) v += __ldcg(src + static_cast<long long>(r) * tile_floats + rr * p.N_pad + n);
                         acc[n] = v;
                     }
-                    store_row<N>(p, acc, pc.t * kTileM + rr, true, rsc, sq, h ? xp[1] : xp[0], h ? gp[1] : gp[0]);
+                    store_row<N>(p, acc, pc.t * kTileM + rr, true, fx, fr, rsc, sq, h ? xp[1] : xp[0],
+                                 h ? gp[1] : gp[0]);
 #pragma unroll
                     for (int n = 0; n < N; ++n) ssl[n] += sq[n];
                 }
-                if (p.res_x) {
+                if (fx) {
 #pragma unroll
                     for (int n = 0; n < N; ++n) {
                         const float tot = warp_sum(ssl[n]);
@@ -518,7 +524,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
     // consumers (C may be read by the previous kernel of the stream: wait before writing it)
     grid_dep_wait();
     float rsc[N];
-    warp_row_scales<N>(p, lane, rsc);
+    warp_row_scales<N>(p, fr, lane, rsc);
     const int w = warp - 2;       // row group 0..7
     const int r = lane & 7;       // row within the group
     const int kq = lane >> 3;     // k-group phase 0..3
@@ -530,13 +536,13 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
         const Piece q = piece_of(p, it, ui);
         const int t = q.t;
         float acc[N], xp[N], gp = 0.f;
-        if (p.P == 1) preload_residual<N>(p, t * kTileM + w * 8 + r, xp, gp);
+        if (p.P == 1) preload_residual<N>(p, fx, t * kTileM + w * 8 + r, xp, gp);
 #pragma unroll
         for (int n = 0; n < N; ++n) acc[n] = 0.f;
         for (int k0 = q.k0; k0 < q.k1 && !failed; k0 += it.c.kc, ++i) {
             const int s = static_cast<int>(i % W);
             if (!mbar_wait(&full[s], static_cast<uint32_t>((i / W) & 1), abort, p.st, DAK_ERR_TIMEOUT, W_CONS_FULL)) {
-                if (!(p.res_x && p.P == 1)) return;
+                if (!(fx && p.P == 1)) return;
                 failed = true;
                 break;
             }
@@ -578,8 +584,8 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
         const int row = t * kTileM + w * 8 + r;
         if (p.P == 1) {
             float sq[N];
-            store_row<N>(p, acc, row, kq == 0 && !failed, rsc, sq, xp, gp);
-            if (p.res_x) {
+            store_row<N>(p, acc, row, kq == 0 && !failed, fx, fr, rsc, sq, xp, gp);
+            if (fx) {
                 // the tile row's sums of x^2: each warp's 8 rows, then the 8 warps in order
 #pragma unroll
                 for (int n = 0; n < N; ++n) {
@@ -657,11 +663,11 @@ constexpr int kMinPieceSteps = 8;   // 64-column steps of an automatically chose
 // and l ^ 1: the even lane writes C[n][j] = silu(gate) * up (C has M / 2 columns). Every lane
 // of the warp calls this (the pairing is a shuffle).
 __device__ __forceinline__ void store_c(const GemmParams& p, float (&f)[8], int row, bool valid, int n_base,
-                                        const float* rsc, float (&sq)[8], const float* xpre = nullptr,
-                                        float gpre = 0.f) {
+                                        bool fx, bool fr, const float* rsc, float (&sq)[8],
+                                        const float* xpre = nullptr, float gpre = 0.f) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        if (rsc && n_base + j < p.N) f[j] *= rsc[n_base + j];
+        if (fr && n_base + j < p.N) f[j] *= rsc[n_base + j];
         sq[j] = 0.f;
     }
     if (p.glu) {
@@ -684,7 +690,7 @@ __device__ __forceinline__ void store_c(const GemmParams& p, float (&f)[8], int 
                 }
             }
         }
-    } else if (p.res_x) {
+    } else if (fx) {
         if (valid) {
             // x and g come preloaded (xpre: this block's 8 values) or are read here
             const float g = xpre ? gpre : __bfloat162float(p.res_g[row]);
@@ -736,8 +742,12 @@ __device__ __forceinline__ void fuse_tile_sums(const GemmParams& p, const float 
     epilogue_bar_sync();  // the slots are rewritten by the next tile row
 }
 
+template <bool F>
 __global__ void __launch_bounds__(kUmmaThreads, 1)
     gemm_umma_kernel(const GemmParams p, const __grid_constant__ CUtensorMap bmap) {
+    // the folded norm's code exists only in the F = true instantiation
+    const bool fx = F && p.res_x != nullptr;
+    const bool fr = F && p.ss_in != nullptr;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ uint64_t full[8], empty[8], acc_full[2], acc_empty[2];
     __shared__ uint64_t peer_empty[8];        // wide B, rank 0: every other rank has freed the slot
@@ -904,7 +914,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         const int e = threadIdx.x - 64;  // 0..127
         grid_dep_wait();  // C and the split workspace may still be in use by the previous kernel of the stream
         const float* rsc = nullptr;
-        if (p.ss_in) {
+        if (fr) {
             // r_n of the consumed normalisation: thread e sums tile rows gi, gi + G, ... of one
             // n in order (G groups), then the groups in order (host-checked N <= kFuseMaxN)
             const int G = max(1, 128 / p.N);
@@ -927,7 +937,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         // fused norm, producer, up to 16 hidden-state rows: the residual values this thread
         // adds to and the gain, loaded before the accumulator is ready (a round trip to L2
         // off the tile row's tail); x is written only by the epilogue that finishes a tile row
-        const bool xpre_on = p.res_x && p.N_pad <= kFusePreloadN;
+        const bool xpre_on = fx && p.N_pad <= kFusePreloadN;
         float xpre[kFusePreloadN];
         float gpre = 0.f;
         for (int ui = 0; ui < it.count; ++ui) {
@@ -939,11 +949,12 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
                 const int xrow = t * kTileM + (p.P > 1 ? (e & 63) : row_in_tile);
                 const int xn0 = p.P > 1 ? 8 * (e >> 6) : 0;
                 const bool ok = (p.P > 1 || row_in_tile >= 0) && xrow < p.M;
+                const int xcols = p.P > 1 ? 8 : p.N_pad;
 #pragma unroll
                 for (int j = 0; j < kFusePreloadN; ++j) {
                     const int n = xn0 + j;
-                    xpre[j] = (ok && j < (p.P > 1 ? 8 : p.N_pad) && n < p.N) ? p.res_x[static_cast<long long>(n) * p.M + xrow]
-                                                                            : 0.f;
+                    const bool use = ok && j < xcols && n < p.N;
+                    xpre[j] = use ? p.res_x[static_cast<long long>(n) * p.M + xrow] : 0.f;
                 }
                 gpre = ok ? __bfloat162float(p.res_g[xrow]) : 0.f;
             }
@@ -951,7 +962,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
                                       DAK_ERR_TIMEOUT, W_EPI_ACC)) {
                 failed = true;
             }
-            if (failed && p.P == 1 && !p.res_x) break;  // no barrier to keep meeting
+            if (failed && p.P == 1 && !fx) break;  // no barrier to keep meeting
             tc_fence_after();
             const Piece pc = piece_of(p, it, ui);
             const int row = pc.t * kTileM + row_in_tile;
@@ -1019,8 +1030,9 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
                         }
                     }
                     float sq[8];
-                    store_c(p, f, rrow, rrow < p.M, n_off + blk * 8, rsc, sq, xpre_on ? xpre : nullptr, gpre);
-                    if (p.res_x) {
+                    store_c(p, f, rrow, rrow < p.M, n_off + blk * 8, fx, fr, rsc, sq, xpre_on ? xpre : nullptr,
+                            gpre);
+                    if (fx) {
                         // rows 32 w2 .. 32 w2 + 31 of this block: one sum per column
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
@@ -1029,7 +1041,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
                         }
                     }
                 }
-                if (p.res_x) fuse_tile_sums(p, fuse_ssw, pc.t, e, 2);
+                if (fx) fuse_tile_sums(p, fuse_ssw, pc.t, e, 2);
                 continue;
             }
             for (int n0 = 0; n0 < p.N_pad; n0 += 8) {
@@ -1047,8 +1059,8 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
                 float sq[8], xb[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) xb[j] = n0 == 0 ? xpre[j] : xpre[8 + j];  // registers, not a stack copy
-                store_c(p, f, row, valid && !failed, n_off + n0, rsc, sq, xpre_on ? xb : nullptr, gpre);
-                if (p.res_x) {
+                store_c(p, f, row, valid && !failed, n_off + n0, fx, fr, rsc, sq, xpre_on ? xb : nullptr, gpre);
+                if (fx) {
                     // rows 16 qp .. 16 qp + 15 (lanes 0..15): one sum per column
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
@@ -1060,7 +1072,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0 && !failed) mbar_arrive(&acc_empty[ab]);
-            if (p.res_x) fuse_tile_sums(p, fuse_ssw, pc.t, e, 4);
+            if (fx) fuse_tile_sums(p, fuse_ssw, pc.t, e, 4);
         }
     }
 
@@ -1483,11 +1495,14 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
     p.b3d = b3d;
 
     const bool pdl = t && t->pdl > 0;
+    const bool fused = p.res_x || p.ss_in;
     cudaError_t e;
     if (bp.umma) {
-        e = launch_ex(gemm_umma_kernel, bp.grid, kUmmaThreads, bp.smem, bp.NC, pdl, stream, p, bmap);
+        e = fused ? launch_ex(gemm_umma_kernel<true>, bp.grid, kUmmaThreads, bp.smem, bp.NC, pdl, stream, p, bmap)
+                  : launch_ex(gemm_umma_kernel<false>, bp.grid, kUmmaThreads, bp.smem, bp.NC, pdl, stream, p, bmap);
     } else {
-        e = launch_ex(gemm_core_kernel<1>, bp.grid, kCoreThreads, bp.smem, 1, pdl, stream, p, bmap);
+        e = fused ? launch_ex(gemm_core_kernel<1, true>, bp.grid, kCoreThreads, bp.smem, 1, pdl, stream, p, bmap)
+                  : launch_ex(gemm_core_kernel<1, false>, bp.grid, kCoreThreads, bp.smem, 1, pdl, stream, p, bmap);
     }
     return cuda_status(e);
 }

@@ -338,7 +338,9 @@ __device__ __forceinline__ int atomic_add_acq_rel(int* addr, int v) {
 
 // C[n][row] for n < N of one output row (fp32 or bf16). With a SwiGLU placement, rows 2j
 // (gate) and 2j + 1 (up) are held by lanes l and l ^ 1; the even lane writes C[n][j] =
-// silu(gate) * up (C has M / 2 columns). Every lane of the warp calls this.
+// silu(gate) * up (C has M / 2 columns). Every lane of the warp calls this. Folded norm:
+// fr scales acc[n] by rsc[n] first; fx adds acc to the residual (xpre / gpre: x[n][row] and
+// g[row], preloaded) and writes C = bf16(x * g), returning x^2 in sq (0 elsewhere).
 template <int N>
 __device__ __forceinline__ void store_row(const GemmParams& p, float (&acc)[N], int row, bool write, bool fx,
                                           bool fr, const float (&rsc)[N], float (&sq)[N], const float (&xpre)[N],
@@ -662,6 +664,8 @@ constexpr int kMinPieceSteps = 8;   // 64-column steps of an automatically chose
 // fp32 or bf16. With a SwiGLU placement, rows 2j (gate) and 2j + 1 (up) are held by lanes l
 // and l ^ 1: the even lane writes C[n][j] = silu(gate) * up (C has M / 2 columns). Every lane
 // of the warp calls this (the pairing is a shuffle).
+// Folded norm: fr scales f[j] by rsc[n_base + j] first; fx adds f to the residual (x read
+// here or preloaded in xpre / gpre) and writes C = bf16(x * g), returning x^2 in sq.
 __device__ __forceinline__ void store_c(const GemmParams& p, float (&f)[8], int row, bool valid, int n_base,
                                         bool fx, bool fr, const float* rsc, float (&sq)[8],
                                         const float* xpre = nullptr, float gpre = 0.f) {

@@ -723,25 +723,45 @@ def peaks():
 
 # ------------------------------------------------------------------------------ CPU oracle
 
-def cpu_oracle_sample(lin, attn, frac_rows=1 / 32):
+def cpu_oracle_sample(lin, attn, frac_rows=1 / 32, offset=0):
     """Time the CPU oracle (as it stands) on a bounded sample of one step: every 32nd tile
-    row of each linear and one request in 32 of the attention. Returns (GB/s, sample, s)."""
+    row of each linear (from tile row `offset` mod 32) and one request in 32 of the
+    attention (the offset-th). Returns (GB/s, sample, s)."""
     import numpy as np
     from oracle import attention as oa
     from oracle import gemm as og
+    f = int(1 / frac_rows)
     t0 = time.perf_counter()
     nbytes = 0
     for A, B in lin.values():
-        rows = np.concatenate([np.arange(t * 64, t * 64 + 64) for t in range(0, A.shape[0] // 64, int(1 / frac_rows))])
+        rows = np.concatenate([np.arange(t * 64, t * 64 + 64) for t in range(offset % f, A.shape[0] // 64, f)])
         og.gemm_ref(A[rows], B)
         nbytes += rows.size * A.shape[1] * 2
     q, k, v = attn
     nreq = max(1, int(q.shape[0] * frac_rows))
-    oa.decode_attention_ref(q[:nreq], k[:nreq], v[:nreq])
-    nbytes += 2 * k[:nreq].size * 2
+    r0 = (offset * nreq) % q.shape[0]
+    oa.decode_attention_ref(q[r0:r0 + nreq], k[r0:r0 + nreq], v[r0:r0 + nreq])
+    nbytes += 2 * k[r0:r0 + nreq].size * 2
     dt = time.perf_counter() - t0
     return nbytes / dt / 1e9, f"1/{int(1 / frac_rows)} of the step: one 64-row tile in {int(1 / frac_rows)} of each " \
                               f"linear and {nreq} of {q.shape[0]} attention requests ({nbytes / 1e6:.0f} MB)", dt
+
+
+def cpu_oracle_timed(lin, attn, target_s=10.0):
+    """The oracle over successive 1/32 slices of the step (offsets 0, 1, 2, ..., every 32 a
+    whole step) until about target_s seconds have passed. Returns (GB/s, sample)."""
+    t0 = time.perf_counter()
+    nbytes, n = 0.0, 0
+    while True:
+        g, _, dt = cpu_oracle_sample(lin, attn, offset=n)
+        nbytes += g * dt * 1e9
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= target_s:
+            break
+    return nbytes / el / 1e9, (f"{n} slices of 1/32 of the step (every 32nd tile row of each linear from "
+                               f"offsets 0..{n - 1} mod 32, one attention request each; {nbytes / 1e9:.1f} GB, "
+                               f"{el:.1f} s)")
 
 
 def cpu_oracle_sample_sliced(batch=32, frac=32):
@@ -970,7 +990,7 @@ def main():
 
     cpu = None
     if rank == 0 and not args.no_cpu:
-        gbps, sample, _ = cpu_oracle_sample(lin, attn)
+        gbps, sample = cpu_oracle_timed(lin, attn)
         cpu = {"value": gbps, "unit": "GB/s", "cores": cpu_threads(), "kind": "oracle", "sample": sample,
                "one_core": cpu_oracle_one_core()}
 

@@ -834,11 +834,11 @@ def run_reference(args, rank, world):
         return
     w_bytes, kv_bytes = workload_bytes(args.batch)
     lin, attn = gen_inputs(args.batch)
-    for _ in range(args.warmup):
-        cpu_oracle_sample(lin, attn)
+    for i in range(args.warmup):
+        cpu_oracle_sample(lin, attn, offset=i)
     vals, dts = [], []
-    for _ in range(args.steps):
-        gbps, sample, dt = cpu_oracle_sample(lin, attn)
+    for i in range(args.steps):  # successive 1/32 slices of the step
+        gbps, sample, dt = cpu_oracle_sample(lin, attn, offset=args.warmup + i)
         vals.append(gbps)
         dts.append(dt)
     v = statistics.median(vals)

@@ -36,6 +36,23 @@ def test_every_declared_symbol_is_exported(dak):
     assert set(names) == set(dak.EXPORTS)
 
 
+@pytest.mark.parametrize("lang,std", [("c", "-std=c99"), ("c++", "-std=c++11")])
+def test_header_compiles_standalone(lang, std, tmp_path):
+    """include/dak.h is plain C: it compiles on its own as C99 (pedantic) and as C++."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    src = tmp_path / ("t.c" if lang == "c" else "t.cpp")
+    src.write_text('#include "dak.h"\nint main(void) { dak_gemm_plan_info i; dak_tuning t; (void)i; (void)t;'
+                   ' return 0; }\n')
+    inc = os.path.join(ROOT, "include")
+    r = subprocess.run([cc, std, "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only", "-I", inc, str(src)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
 def test_status_strings(dak):
     assert dak.lib.dak_status_string(0) == b"ok"
     assert dak.lib.dak_status_string(6) == b"kernel wait timed out"

@@ -15,7 +15,10 @@
 //                                                            Wgu is placed gate/up interleaved;
 //                                                            else gu (fp32) + swiglu here]
 //   dak_gemm  Wdown . act -> x +=
-// and a final rmsnorm writes the output. With programmatic dependent launch every kernel
+// and a final rmsnorm writes the output. With B <= kFuseNormMaxBatch every rmsnorm but the
+// step's first and last is folded into the GEMMs around it (GemmFuse): the O and down
+// projections add their product to x themselves and write h = bf16(x * g) and per-tile sums
+// of x^2; gate+up and the next layer's QKV scale their accumulators by 1 / rms. With programmatic dependent launch every kernel
 // starts while its predecessors drain. Before its own griddepcontrol.wait a kernel reads
 // only what no kernel of the step writes (weights, KV entries older than the new token,
 // the sequence lengths and the RoPE table) and writes nothing to global memory; after

@@ -81,6 +81,20 @@ def _run(dak, dec, x0, pos, mode=0, graph=False):
     return out
 
 
+@pytest.mark.parametrize("B", [24, 100])
+def test_decoder_folded_norms_wide_batch(dak, B):
+    """Batches above 16 rows (the folded norm reads the residual in its store instead of
+    preloading it) and up to the 128-row limit, against the oracle."""
+    cfg, L = SMALL128, 96
+    pos = [(11 * b + 3) % L for b in range(B)]
+    layers, caches, fnorm, x0 = _inputs(cfg, B, L, seed=22)
+    ref, _ = od.decode_step(_ocfg(cfg), x0, layers, caches, np.array(pos), fnorm)
+    dec = _build(dak, cfg, layers, caches, fnorm, _host_units(cfg, B, 0.3))
+    out = _run(dak, dec, x0, pos)
+    assert og.rel_err(to_np(out), ref) <= REL_TOL
+    dec.free()
+
+
 def test_decoder_large_batch_separate_norms(dak):
     """More requests than the GEMMs' folded RMSNorm takes (128): the step keeps its separate
     RMSNorm kernels, with the same results against the oracle."""

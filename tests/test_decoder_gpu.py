@@ -95,6 +95,21 @@ def test_decoder_folded_norms_wide_batch(dak, B):
     dec.free()
 
 
+@pytest.mark.parametrize("B", [5, 24])
+def test_decoder_folded_norms_split_tile_rows(dak, B):
+    """Every projection with its tile rows cut into pieces (split_k = 3): the folded norm
+    runs in the epilogue that adds the pieces, with and without the residual preload."""
+    cfg, L = SMALL128, 96
+    pos = [(13 * b + 5) % L for b in range(B)]
+    layers, caches, fnorm, x0 = _inputs(cfg, B, L, seed=23)
+    ref, _ = od.decode_step(_ocfg(cfg), x0, layers, caches, np.array(pos), fnorm)
+    tun = {k: {"split_k": 3} for k in ("qkv", "o", "gate_up", "down")}
+    dec = _build(dak, cfg, layers, caches, fnorm, _host_units(cfg, B, 0.3), op_tuning=tun)
+    out = _run(dak, dec, x0, pos)
+    assert og.rel_err(to_np(out), ref) <= REL_TOL
+    dec.free()
+
+
 def test_decoder_large_batch_separate_norms(dak):
     """More requests than the GEMMs' folded RMSNorm takes (128): the step keeps its separate
     RMSNorm kernels, with the same results against the oracle."""

@@ -539,8 +539,8 @@ def run_large_n(dak, lin, b_host, b_hbm, dev, x=0.25):
 def run_linears_n(dak, lin, b_host, b_hbm, dev, xs=(0.0, 0.25), ns=(1, 8, 32, 64)):
     """The four 8B linears (QKV, O, gate+up, down: 436 MB, more than L2) as one graph of four
     dak_gemm launches, at each offload ratio in xs and each hidden-state row count N in ns
-    (the batch sizes of the survey's linear configuration): time per pass, effective GB/s
-    and the fraction of the tier roofline."""
+    (decode batch sizes from one request to 64): time per pass, effective GB/s and the
+    fraction of the tier roofline."""
     import torch
     import synth
     rows = []

@@ -95,15 +95,16 @@ def test_decoder_folded_norms_wide_batch(dak, B):
     dec.free()
 
 
-@pytest.mark.parametrize("B", [5, 24])
-def test_decoder_folded_norms_split_tile_rows(dak, B):
+@pytest.mark.parametrize("B,knobs", [(5, {"split_k": 3}), (24, {"split_k": 3}), (16, {"ctas_per_sm": 2})])
+def test_decoder_folded_norms_split_tile_rows(dak, B, knobs):
     """Every projection with its tile rows cut into pieces (split_k = 3): the folded norm
-    runs in the epilogue that adds the pieces, with and without the residual preload."""
+    runs in the epilogue that adds the pieces, with and without the residual preload; and
+    rings sized for two CTAs per SM."""
     cfg, L = SMALL128, 96
     pos = [(13 * b + 5) % L for b in range(B)]
     layers, caches, fnorm, x0 = _inputs(cfg, B, L, seed=23)
     ref, _ = od.decode_step(_ocfg(cfg), x0, layers, caches, np.array(pos), fnorm)
-    tun = {k: {"split_k": 3} for k in ("qkv", "o", "gate_up", "down")}
+    tun = {k: dict(knobs) for k in ("qkv", "o", "gate_up", "down")}
     dec = _build(dak, cfg, layers, caches, fnorm, _host_units(cfg, B, 0.3), op_tuning=tun)
     out = _run(dak, dec, x0, pos)
     assert og.rel_err(to_np(out), ref) <= REL_TOL

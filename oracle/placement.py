@@ -15,7 +15,7 @@
   output tiles n_tile columns wide, each host tile row is read once per column tile:
   traffic = host_bytes * ceil(N / n_tile).
 
-Parity pins (tests/test_oracle_placement.py): Table 1's five rows (98 MiB host matrix,
+Parity pins (tests/test_oracle_planner.py, placement section): Table 1's five rows (98 MiB host matrix,
 n_tile = 256), Fig. 10's and Fig. 14's global ratios from footprint and H = 96 GB, and
 the tile-count edge cases (x = 0, x = 1, ragged last tile).
 """

@@ -22,7 +22,10 @@ The oracle solves it by plain enumeration, not by the paper's greedy phases:
 * ``exhaustive_tiles``: every vector of whole tile counts (b_i = min(k_i * tile_i, C_i)),
   for the tile-granular variant; tiny cases only.
 
-Parity pins (tests/test_oracle_planner.py): the single-operation turning points
+Parity pins (tests/test_oracle_planner.py): hand-worked values of EB(x) for a
+memory-bound and a compute-bound operation; a hand-worked two-operation whole-tile case
+whose optimum puts an operation (one with a ragged last tile) wholly on the host; the
+single-operation turning points
 x* = B_h/(B_h+B_g) (memory-bound) and x* = B_h/B_i with B_i = C_i/T_comp,i
 (compute-bound) from [DAK] section 4.2.1 / Fig. 6; the worked GH200 value
 x* = 0.9/(4.0+0.9) ~ 18.4% from [DAK-explainer]; the optimal objective values that
@@ -108,7 +111,7 @@ def exhaustive_tiles(ops, tile_bytes, b_host, b_gpu, D):
     ops: list of (C_i, T_comp_i); tile_bytes[i]: granularity of op i; b_i(k) = min(k tile, C)."""
     grids = []
     for (C, _), t in zip(ops, tile_bytes):
-        nt = -(-int(round(C)) // int(t)) if C > 0 else 0
+        nt = math.ceil(C / t) if C > 0 else 0  # the last tile may be ragged: b = C there
         grids.append([min(k * t, C) for k in range(nt + 1)])
     best, best_b = INF, None
     for combo in itertools.product(*grids):

@@ -1,7 +1,8 @@
 """Helpers for the GPU tests: bf16 bit arrays <-> torch tensors, tolerances."""
 import numpy as np
 
-# BASELINE-level tolerance for bf16 inputs with fp32 accumulation: max |gpu - ref| / max |ref|
+# rel-err bound for bf16 inputs with fp32 accumulation, max |gpu - ref| / max |ref| against the
+# fp64 oracle: the 2e-2 the direct-access kernels are held to for bf16 outputs
 REL_TOL = 2e-2
 # the kernels accumulate in fp32; against the fp64 oracle the error is far below REL_TOL
 FP32_OUT_TOL = 1e-5

@@ -156,3 +156,43 @@ def test_tier_roofline_limits():
     xb = 1e11 / (1e11 + 7e12)
     assert opl.tier_roofline(C, xb, 1e11, 7e12) == pytest.approx(7.1e12)
     assert opl.tier_roofline(C, 0.5, 1e11, 7e12) == pytest.approx(2e11)
+
+
+# ------------------------------ effective bandwidth and whole-tile search, hand values ------
+
+def test_effective_bandwidth_memory_bound_hand_values():
+    """EB(x) of a memory-bound op ([DAK] section 4.2.1, Fig. 6) at C = 1 GB, B_h = 100 GB/s,
+    B_g = 400 GB/s, worked by hand: all in HBM 400; at x* = 0.2 the two transfers take
+    2 ms each, EB = 500 = B_h + B_g; at x = 0.5 the host half takes 5 ms, EB = 200; all on
+    the host 100."""
+    C, bh, bg = 1e9, 100e9, 400e9
+    for x, eb in ((0.0, 400e9), (0.2, 500e9), (0.5, 200e9), (1.0, 100e9), (0.1, 1e9 / 2.25e-3)):
+        assert op.effective_bandwidth(C, 0.0, x, bh, bg) == pytest.approx(eb, rel=1e-12), x
+
+
+def test_effective_bandwidth_compute_bound_hand_values():
+    """A compute-bound op (T_comp = 4 ms > C / B_g = 2.5 ms): EB stays at C / T_comp = 250 GB/s
+    until the host part takes 4 ms (x = 0.4), then falls as C / (x C / B_h): 1/6 TB/s at 0.6."""
+    C, tc, bh, bg = 1e9, 4e-3, 100e9, 400e9
+    for x, eb in ((0.0, 250e9), (0.25, 250e9), (0.4, 250e9), (0.6, 1e9 / 6e-3), (1.0, 100e9)):
+        assert op.effective_bandwidth(C, tc, x, bh, bg) == pytest.approx(eb, rel=1e-12), x
+
+
+def test_exhaustive_tiles_hand_case_fully_offloaded_op():
+    """Two ops, three whole tiles (unit bandwidths B_h = B_g = 1). Op 0: C = 2.5 in tiles of 1
+    (grid 0, 1, 2, 2.5: the last tile ragged), no compute; op 1: C = 1 in one tile,
+    T_comp = 0.9. Worked by hand over every grid point:
+      D = 2:   (1, 1) -> max(1.5, 1) + max(0.9, 0, 1) = 2.5   (best; op 1 at b = C)
+               (2, 0) -> 2 + 1 = 3, (2, 1) -> 3, (2.5, 0) -> 3.5, (2.5, 1) -> 3.5
+      D = 3.5: only (2.5, 1) -> 2.5 + 1 = 3.5                   (both ops at b = C)
+    A search that dropped the last grid point of an op, or put op 0's last point at 3,
+    would miss these optima."""
+    ops = [(2.5, 0.0), (1.0, 0.9)]
+    obj, b = op.exhaustive_tiles(ops, [1.0, 1.0], 1.0, 1.0, 2.0)
+    assert obj == pytest.approx(2.5, abs=1e-12)
+    assert b == [1.0, 1.0]
+    obj, b = op.exhaustive_tiles(ops, [1.0, 1.0], 1.0, 1.0, 3.5)
+    assert obj == pytest.approx(3.5, abs=1e-12)
+    assert b == [2.5, 1.0]
+    obj, b = op.exhaustive_tiles(ops, [1.0, 1.0], 1.0, 1.0, 4.0)  # more than both ops hold
+    assert obj == math.inf and b is None

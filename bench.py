@@ -41,8 +41,10 @@ def _args():
     ap.add_argument("--batch", type=int, default=32)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--decode", default="8b", choices=["8b", "70b", "none"],
-                    help="also time a full decode step of this model (planner ratios at --decode-x)")
+    ap.add_argument("--decode", default="8b,70b",
+                    help="also time full decode steps of these models (comma list of 8b, 70b; none = off): the "
+                         "8B step with the launch tuner, the x_global sweep and the one-request step, the 70B step "
+                         "at --decode-x and all in HBM")
     ap.add_argument("--decode-x", type=float, default=0.3, help="x_global of the decode step's HBM cap")
     ap.add_argument("--decode-steps", type=int, default=20)
     ap.add_argument("--decode-sweep", default="0.1,0.2,0.5",
@@ -232,18 +234,19 @@ def tune_decoder_ops(dak, cfg, dec, dev):
     return res, table
 
 
-def run_decode(dak, args, b_host, b_hbm, dev, sync_all, local):
-    """Full decode step: planner-chosen per-op ratios at x_global, one CUDA graph per mode."""
+def run_decode(dak, args, b_host, b_hbm, dev, sync_all, local, model="8b", full=True):
+    """Full decode step: planner-chosen per-op ratios at x_global, one CUDA graph per mode.
+    full: also the launch tuner, the x_global sweep and the one-request step."""
     import torch
     import synth
-    cfg = dict(synth.DECODER_8B if args.decode == "8b" else synth.DECODER_70B)
+    cfg = dict(synth.DECODER_8B if model == "8b" else synth.DECODER_70B)
     pk, _ = peaks()
     peak_flops = pk.get("bf16_tflops_sustained", 1700.0) * 1e12
     B, d, L = cfg["batch"], cfg["hidden"], cfg["context"]
     x_in = torch.from_numpy(synth.decoder_x0(cfg, B).view("int16")).view(torch.bfloat16).to(dev)
     pos = torch.full((B,), L - 1, dtype=torch.int32, device=dev)  # context L: L - 1 cached + the new token
     out = torch.empty_like(x_in)
-    res = {"workload": f"{cfg['n_layers']}-layer {args.decode.upper()}-shaped decode step (hidden {d}, GQA "
+    res = {"workload": f"{cfg['n_layers']}-layer {model.upper()}-shaped decode step (hidden {d}, GQA "
                        f"{cfg['n_heads']}/{cfg['n_kv_heads']}, head dim {cfg['head_dim']}, FFN {cfg['ffn']}, "
                        f"RMSNorm, RoPE, SwiGLU), random-init bf16, batch {B}, context {L}",
            "batch": B, "context": L, "x_global_target": args.decode_x}
@@ -273,7 +276,7 @@ def run_decode(dak, args, b_host, b_hbm, dev, sync_all, local):
                "planner_model_ms": tmodel * 1e3, "host_units_per_layer": units[0] if units else {},
                "build_s": build_s,
                "launches_per_step": dec.launches(), "clocks": sampler.summary(tw0, tw1)}
-        if xg > 0:
+        if xg > 0 and full:
             # launch tuner per operation type on layer 0's placements, then the step with its choices
             tuned, table = tune_decoder_ops(dak, cfg, dec, dev)
             rec["tuner"] = tuned
@@ -283,6 +286,7 @@ def run_decode(dak, args, b_host, b_hbm, dev, sync_all, local):
             rec["tuned_tok_s"] = B / tt
             rec["tuned_frac"] = (C / tt) / roof
             dec_t.free(placements=False)
+        if xg > 0:
             for mode, name in ((dak.MODE_PREFETCH_SERIAL, "prefetch_serial"), (dak.MODE_PREFETCH_OVERLAP,
                                                                                  "prefetch_overlap")):
                 dec.capture(x_in, pos, out, mode)
@@ -314,7 +318,7 @@ def run_decode(dak, args, b_host, b_hbm, dev, sync_all, local):
             res.update(rec)
     # per-x sweep of the step with both prefetch baselines (planner ratios at each x_global)
     sweep = []
-    for xs in [float(v) for v in args.decode_sweep.split(",") if v.strip()]:
+    for xs in [float(v) for v in args.decode_sweep.split(",") if v.strip() and full]:
         units, tmodel = decode_plan(dak, cfg, b_host, b_hbm, xs, peak_flops)
         dec = build_decoder(dak, cfg, units)
         C = sum(L_[k].host_bytes + L_[k].hbm_bytes for L_ in dec.layers for k in dak.DECODER_OPS)
@@ -336,8 +340,9 @@ def run_decode(dak, args, b_host, b_hbm, dev, sync_all, local):
         dec.free()
         del dec
         torch.cuda.empty_cache()
-    res["per_x"] = sweep
-    if not args.no_sweep:
+    if full:
+        res["per_x"] = sweep
+    if full and not args.no_sweep:
         res["batch1"] = run_decode_batch1(dak, args, cfg, b_host, b_hbm, dev, sync_all, peak_flops)
     return res
 
@@ -571,6 +576,116 @@ def run_linears_n(dak, lin, b_host, b_hbm, dev, xs=(0.0, 0.25), ns=(1, 8, 32, 64
             p.free()
     return {"ops": "8B QKV, O, gate+up, down (one graph of four launches)", "rows": rows,
             "status": dak.dak_last_error()[0]}
+
+
+# ------------------------------------------------------------------------------ per operation, per x
+
+def _capture(fn):
+    """A CUDA graph of fn's launches (captured on a side stream)."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            fn()
+    return g
+
+
+def run_per_op_x(dak, lin, attn, b_host, b_hbm, dev, ns=(1, 8, 32, 64)):
+    """Each operation of the step alone, against its tier roofline at every offload ratio:
+    the four 8B linears at x = 0, 0.05, ..., 0.5 for N in ns, the 32-request attention at
+    x in {0, 0.125, 0.25, 0.5}, and the 1024x1024 GEMV at x = 0.25. Two timings per point:
+    `single`, one launch after a write of twice the L2 size (cold L2, launch latency
+    included; CUDA events around the launch), and `chain`, a CUDA graph of launches with
+    programmatic launch over enough copies of the placement that they stream more than
+    twice the L2 size (the rate of the operation repeated back to back, as in a model's
+    layers). Bytes are the operation's weights (or KV cache)."""
+    import math
+    import torch
+    import synth
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    xs = [round(0.05 * i, 2) for i in range(11)]
+
+    def single(fn, reps=5):
+        ts = []
+        for _ in range(reps):
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) / 1e3)
+        return statistics.median(ts)
+
+    def point(C_bytes, H, t1, tc):
+        roof = tier_roofline(C_bytes, H / C_bytes, b_host, b_hbm)
+        return {"x_effective": H / C_bytes, "single_us": t1 * 1e6, "chain_us": tc * 1e6,
+                "single_gbps": C_bytes / t1 / 1e9, "chain_gbps": C_bytes / tc / 1e9, "roofline_gbps": roof / 1e9,
+                "single_frac": (C_bytes / t1) / roof, "chain_frac": (C_bytes / tc) / roof}
+
+    res = {"linears": [], "l2_bytes": l2}
+    pdl = dict(pdl=1)
+    for i, (name, (A, _)) in enumerate(lin.items()):
+        M, K = A.shape
+        Ad = torch.from_numpy(A.view("int16")).view(torch.bfloat16).to(dev)
+        copies = max(2, math.ceil(2 * l2 / (M * K * 2)))
+        Bs = {N: torch.from_numpy(synth.normal_bf16(13, i, N * K).view("int16")).view(torch.bfloat16).to(dev)
+              .view(N, K) for N in ns}
+        Cs = {N: torch.empty((N, M), dtype=torch.bfloat16, device=dev) for N in ns}
+        rows = []
+        for x in xs:
+            pls = [dak.dak_place_matrix(Ad, dak.host_tiles_for_ratio(x, M)) for _ in range(copies)]
+            C_bytes, H = pls[0].host_bytes + pls[0].hbm_bytes, pls[0].host_bytes
+            for N in ns:
+                t1 = single(lambda: dak.dak_gemm(pls[0], Bs[N], Cs[N]))
+                g = _capture(lambda: [dak.dak_gemm(p, Bs[N], Cs[N], tuning=pdl) for p in pls])
+                tc = time_steps(g.replay, 10, 3) / copies
+                del g
+                rows.append(dict(x=x, N=N, **point(C_bytes, H, t1, tc)))
+            for p in pls:
+                p.free()
+        del Ad
+        res["linears"].append({"op": f"{name} {M}x{K}", "copies_in_chain": copies, "rows": rows})
+        torch.cuda.empty_cache()
+    # the attention (1 GiB of KV: launches back to back already stream more than twice the L2)
+    q, k, v = attn
+    Q = torch.from_numpy(q.view("int16")).view(torch.bfloat16).to(dev)
+    O = torch.empty_like(Q)
+    arows = []
+    for x in (0.0, 0.125, 0.25, 0.5):
+        p = dak.dak_place_kv(k, v, dak.host_requests_for_ratio(x, k.shape[0]))
+        ns_ = dak.dak_attn_default_split(p)
+        ws = torch.empty(max(1, dak.dak_attn_workspace_bytes(q.shape[0], q.shape[1], q.shape[2], ns_) // 4),
+                         dtype=torch.float32, device=dev)
+        t1 = single(lambda: dak.dak_attn(Q, p, O=O, workspace=ws, tuning=dict(n_split=ns_)))
+        tc = time_steps(lambda: dak.dak_attn(Q, p, O=O, workspace=ws, tuning=dict(pdl=1, n_split=ns_)), 10, 3)
+        C_bytes, H = p.host_bytes + p.hbm_bytes, p.host_bytes
+        arows.append(dict(x=x, n_split=ns_, **point(C_bytes, H, t1, tc)))
+        p.free()
+    res["attention"] = {"op": "GQA decode attention, 32 requests, 32/8 heads, D 128, context 8192",
+                        "rows": arows}
+    # the single decode GEMV (2 MiB: the chain cycles over enough copies to leave L2)
+    A1, B1 = synth.gemm_inputs(1024, 1024, 1, seed=0)
+    A1d = torch.from_numpy(A1.view("int16")).view(torch.bfloat16).to(dev)
+    B1d = torch.from_numpy(B1.view("int16")).view(torch.bfloat16).to(dev)
+    C1 = torch.empty((1, 1024), dtype=torch.bfloat16, device=dev)
+    copies = math.ceil(2 * l2 / (1024 * 1024 * 2))
+    pls = [dak.dak_place_matrix(A1d, dak.host_tiles_for_ratio(0.25, 1024)) for _ in range(copies)]
+    t1 = single(lambda: dak.dak_gemm(pls[0], B1d, C1))
+    g = _capture(lambda: [dak.dak_gemm(p, B1d, C1, tuning=pdl) for p in pls])
+    tc = time_steps(g.replay, 10, 3) / copies
+    del g
+    res["gemv"] = dict(op="GEMV 1024x1024, N = 1, x = 0.25 (4 of 16 tile rows on the host)", copies_in_chain=copies,
+                       **point(pls[0].host_bytes + pls[0].hbm_bytes, pls[0].host_bytes, t1, tc))
+    for p in pls:
+        p.free()
+    res["status"] = dak.dak_last_error()[0]
+    torch.cuda.empty_cache()
+    return res
 
 
 # ------------------------------------------------------------------------------ clocks
@@ -975,7 +1090,9 @@ def main():
     achieved = att_bytes / (att_ms / 1e3)
     traffic = read_ncu_traffic()
 
-    decode = run_decode(dak, args, b_host, b_hbm, dev, sync_all, local) if args.decode != "none" else None
+    models = [m.strip() for m in args.decode.split(",") if m.strip() in ("8b", "70b")]
+    decode = {m: run_decode(dak, args, b_host, b_hbm, dev, sync_all, local, model=m, full=(m == "8b"))
+              for m in models}
     planner_check = None
     if not args.no_planner_check:
         pc_sampler = ClockSampler(local)
@@ -987,6 +1104,7 @@ def main():
         planner_check["clocks"] = pc_sampler.summary(tw0, tw1)  # tensor-bound timings follow the SM clock
     large_n = None if args.no_planner_check else run_large_n(dak, lin, b_host, b_hbm, dev)
     per_n = None if args.no_sweep else run_linears_n(dak, lin, b_host, b_hbm, dev)
+    per_op = None if args.no_sweep else run_per_op_x(dak, lin, attn, b_host, b_hbm, dev)
 
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -1019,8 +1137,12 @@ def main():
         "clocks": clocks,
         "status": [status[0], status2[0], status3[0]],
     }
-    if decode:
-        line["decode_step"] = decode
+    if "8b" in decode:
+        line["decode_step"] = decode["8b"]
+    if "70b" in decode:
+        line["decode_step_70b"] = decode["70b"]
+    if per_op:
+        line["per_op_x"] = per_op
     if planner_check:
         line["planner_check"] = planner_check
     if large_n:

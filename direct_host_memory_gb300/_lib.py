@@ -30,7 +30,11 @@ EXPORTS = [
     "dak_decoder_create", "dak_decoder_batch", "dak_decoder_step", "dak_decoder_capture",
     "dak_decoder_replay", "dak_decoder_launches", "dak_decoder_free", "dak_tune_gemm", "dak_tune_attn",
     "dak_place_matrix_glu", "dak_plan_units", "dak_gemm_workspace_bytes", "dak_gemm_ws", "dak_gemm_plan",
+    "dak_attn_f32", "dak_inject_fault", "dak_fault_pending", "dak_alloc_counts",
 ]
+
+# host-side fault injection kinds (DAK_FAULT_* in dak.h)
+FAULT_HOST_ALLOC, FAULT_DEVICE_ALLOC, FAULT_TENSOR_MAP = 1, 2, 3
 
 # size of the fixed device array dak_attn_noalloc uses (DAK_NOALLOC_SCRATCH_BYTES in dak.h)
 NOALLOC_SCRATCH_BYTES = 4 << 20
@@ -99,6 +103,7 @@ def _load():
         "dak_attn_workspace_bytes": (sz, [i32, i32, i32, i32]),
         "dak_attn": (i32, [vp, vp, vp, i32, ctypes.c_float, vp, vp, sz, P(dak_tuning), vp]),
         "dak_attn_staged": (i32, [vp, vp, vp, vp, i32, ctypes.c_float, vp, vp, sz, P(dak_tuning), vp]),
+        "dak_attn_f32": (i32, [vp, vp, vp, i32, ctypes.c_float, vp, vp, sz, P(dak_tuning), vp]),
         "dak_attn_default_split": (i32, [vp]),
         "dak_plan_ratios": (i32, [P(dak_op), i32, dbl, dbl, dbl, i32, P(dbl), P(dbl)]),
         "dak_plan_units": (i32, [P(dak_op), i32, dbl, dbl, dbl, P(i64), P(dbl)]),
@@ -109,6 +114,9 @@ def _load():
         "dak_prefetch": (i32, [vp, vp, vp]),
         "dak_attn_noalloc": (i32, [vp, vp, vp, i32, ctypes.c_float, vp, P(dak_tuning), vp]),
         "dak_selftest_wait": (i32, [vp]),
+        "dak_inject_fault": (i32, [i32, i32, i32]),
+        "dak_fault_pending": (i32, [i32]),
+        "dak_alloc_counts": (i32, [P(i64), P(i64)]),
         "dak_decoder_create": (i32, [P(dak_decoder_config), P(dak_decoder_layer), vp, P(vp)]),
         "dak_decoder_batch": (i32, [vp]),
         "dak_decoder_step": (i32, [vp, vp, vp, vp, i32, vp]),
@@ -352,6 +360,20 @@ def dak_attn(Q, KV: Placement, seq_lens=None, scale: float = 0.0, O=None, worksp
     return O
 
 
+def dak_attn_f32(Q, KV: Placement, seq_lens=None, scale: float = 0.0, O=None, workspace=None, tuning=None,
+                 stream=None):
+    """dak_attn with an fp32 output o [B][Hq][D] (the parity mode; returns O)."""
+    import torch
+    if O is None:
+        O = torch.empty(tuple(Q.shape), dtype=torch.float32, device=Q.device)
+    if not (O.dtype == torch.float32 and O.is_cuda and O.is_contiguous() and tuple(O.shape) == tuple(Q.shape)):
+        raise ValueError("O must be a contiguous fp32 CUDA tensor shaped like Q")
+    Hq, O, workspace, ws_len, tun = _attn_common(Q, KV, O, workspace, tuning)
+    _check(lib.dak_attn_f32(_ptr(Q), KV.handle, _ptr(seq_lens), Hq, float(scale), _ptr(O), _ptr(workspace), ws_len,
+                            _tuning(tun), _stream_ptr(stream)), "dak_attn_f32")
+    return O
+
+
 def dak_attn_staged(Q, KV: Placement, staging, seq_lens=None, scale: float = 0.0, O=None, workspace=None,
                     tuning=None, stream=None):
     Hq, O, workspace, ws_len, tun = _attn_common(Q, KV, O, workspace, tuning)
@@ -430,6 +452,23 @@ def dak_last_error(stream=None):
 def dak_selftest_wait(stream=None):
     """Launch the bounded-wait self-test kernel (its wait must time out after ~2 s)."""
     _check(lib.dak_selftest_wait(_stream_ptr(stream)), "dak_selftest_wait")
+
+
+def dak_inject_fault(kind: int, count: int = 1, skip: int = 0):
+    """Make the library's next `count` calls of this kind (FAULT_*) fail after `skip` more
+    succeed (count -1: every call; count 0 clears). Host side only."""
+    _check(lib.dak_inject_fault(int(kind), int(skip), int(count)), "dak_inject_fault")
+
+
+def dak_fault_pending(kind: int) -> int:
+    return int(lib.dak_fault_pending(int(kind)))
+
+
+def dak_alloc_counts():
+    """(pinned host buffers, device buffers) the library holds right now."""
+    h, d = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib.dak_alloc_counts(ctypes.byref(h), ctypes.byref(d)), "dak_alloc_counts")
+    return int(h.value), int(d.value)
 
 
 def dak_sm_count() -> int:

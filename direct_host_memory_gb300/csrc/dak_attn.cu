@@ -13,7 +13,11 @@
 // so they run on warp-level m16n8k16 MMAs rather than the tcgen05 pipeline:
 //   S  = Q_g (16 x D, rows >= G zero) . K^T (D x 16 tokens)
 //   O += P   (16 x 16 tokens)         . V   (16 tokens x D)
-// with online softmax in fp32 (base-2 exponentials, the scale folded with log2 e).
+// with online softmax in fp32 (base-2 exponentials, the scale folded with log2 e). The
+// MMA takes bf16 operands, so the fp32 probabilities P enter the second product as two
+// bf16 parts, P_hi = bf16(P) and P_lo = bf16(P - P_hi), multiplied into the same fp32
+// accumulators: P_hi + P_lo equals P to about 2^-17 relative, so the product is not
+// limited by bf16 rounding of P (the denominator sums the fp32 P).
 // Partial results of the splits are merged by a log-sum-exp combine in fixed order.
 //
 // KV placement layout: per tier [requests][H_kv] slabs; a slab is ceil(L/64) chunks of 64
@@ -31,7 +35,8 @@ struct AttnParams {
     const __nv_bfloat16* Q;  // [B][Hq][D]
     const uint8_t* kv[2];    // [0] host tier (device-visible), [1] HBM tier
     const int* seq_lens;
-    __nv_bfloat16* O;        // [B][Hq][D]
+    void* O;                 // [B][Hq][D], bf16 or (o_fp32) fp32
+    int o_fp32;
     float* ws;               // [B][Hq][n_split][D + 2] partials: m (log2 domain), l, o[D]
     int B, Hq, Hkv, G, L, h_r, n_split, split_len;
     int wait_newest;         // stream the chunk holding token L_b - 1 only after the previous kernel
@@ -96,6 +101,22 @@ __device__ __forceinline__ Unit decode_unit(const AttnParams& p, long long u, in
 }
 
 enum : uint32_t { A_PROD_EMPTY = 11, A_CONS_FULL = 12, A_DRAIN = 13 };
+
+// One output element, bf16 (round to nearest even) or fp32.
+__device__ __forceinline__ void store_out(void* O, int o_fp32, long long i, float v) {
+    if (o_fp32) {
+        static_cast<float*>(O)[i] = v;
+    } else {
+        static_cast<__nv_bfloat16*>(O)[i] = __float2bfloat16_rn(v);
+    }
+}
+
+// Two fp32 values as the bf16 pairs hi = bf16(v) and lo = bf16(v - hi) (round to nearest even).
+__device__ __forceinline__ void split_bf16(float v0, float v1, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat16 h0 = __float2bfloat16_rn(v0), h1 = __float2bfloat16_rn(v1);
+    hi = static_cast<uint32_t>(__bfloat16_as_ushort(h0)) | (static_cast<uint32_t>(__bfloat16_as_ushort(h1)) << 16);
+    lo = pack_bf16(v0 - __bfloat162float(h0), v1 - __bfloat162float(h1));
+}
 
 __device__ __forceinline__ void named_bar_consumers() {
     asm volatile("bar.sync 1, %0;" ::"n"(32 * kAttnConsumers) : "memory");
@@ -260,11 +281,13 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnParams 
                     o[nb][2] *= corr_b;
                     o[nb][3] *= corr_b;
                 }
-                // P as the A operand (16 rows x 16 tokens)
-                const uint32_t pa0 = pack_bf16(pr[0][0], pr[0][1]);
-                const uint32_t pa1 = pack_bf16(pr[0][2], pr[0][3]);
-                const uint32_t pa2 = pack_bf16(pr[1][0], pr[1][1]);
-                const uint32_t pa3 = pack_bf16(pr[1][2], pr[1][3]);
+                // P as the A operand (16 rows x 16 tokens), in two bf16 parts: hi = bf16(P) and
+                // lo = bf16(P - hi), both multiplied into the same accumulators
+                uint32_t pa0, pa1, pa2, pa3, pl0, pl1, pl2, pl3;
+                split_bf16(pr[0][0], pr[0][1], pa0, pl0);
+                split_bf16(pr[0][2], pr[0][3], pa1, pl1);
+                split_bf16(pr[1][0], pr[1][1], pa2, pl2);
+                split_bf16(pr[1][2], pr[1][3], pa3, pl3);
                 // ---- O += P V
                 {
                     const int tok = 16 * w + (mi & 1) * 8 + rr;
@@ -276,6 +299,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnParams 
                         ldsm_x4_t(addr, b0, b1, b2, b3);
                         mma_bf16_16816(o[2 * db], pa0, pa1, pa2, pa3, b0, b1);
                         mma_bf16_16816(o[2 * db + 1], pa0, pa1, pa2, pa3, b2, b3);
+                        mma_bf16_16816(o[2 * db], pl0, pl1, pl2, pl3, b0, b1);
+                        mma_bf16_16816(o[2 * db + 1], pl0, pl1, pl2, pl3, b2, b3);
                     }
                 }
             }
@@ -331,7 +356,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnParams 
             }
             const long long orow = static_cast<long long>(x.b) * p.Hq + static_cast<long long>(x.g) * p.G + r;
             if (p.n_split == 1) {
-                p.O[orow * D + d] = __float2bfloat16_rn(lsum > 0.f ? acc / lsum : 0.f);
+                store_out(p.O, p.o_fp32, orow * D + d, lsum > 0.f ? acc / lsum : 0.f);
             } else {
                 float* wr = p.ws + (orow * p.n_split + x.s) * (D + 2);
                 wr[d] = acc;
@@ -351,7 +376,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnParams 
 //
 // A few splits: one warp per row walks the splits in order (lanes over the columns).
 template <int D>
-__global__ void attn_combine_warp_kernel(const float* __restrict__ ws, __nv_bfloat16* __restrict__ O, int rows,
+__global__ void attn_combine_warp_kernel(const float* __restrict__ ws, void* __restrict__ O, int o_fp32, int rows,
                                          int n_split) {
     grid_dep_launch();
     grid_dep_wait();  // the partials come from the attention kernel just before
@@ -375,7 +400,7 @@ __global__ void attn_combine_warp_kernel(const float* __restrict__ ws, __nv_bflo
     }
 #pragma unroll
     for (int j = 0; j < D / 32; ++j) {
-        O[static_cast<long long>(row) * D + lane + 32 * j] = __float2bfloat16_rn(lsum > 0.f ? acc[j] / lsum : 0.f);
+        store_out(O, o_fp32, static_cast<long long>(row) * D + lane + 32 * j, lsum > 0.f ? acc[j] / lsum : 0.f);
     }
 }
 
@@ -391,7 +416,7 @@ constexpr int kMaxSplits = 1024;
 
 template <int D>
 __global__ void __launch_bounds__(kCombineThreads) attn_combine_cta_kernel(const float* __restrict__ ws,
-                                                                           __nv_bfloat16* __restrict__ O,
+                                                                           void* __restrict__ O, int o_fp32,
                                                                            int n_split) {
     constexpr int CG = D / 2;                   // float2 column pairs of a row
     constexpr int SG = kCombineThreads / CG;    // groups of splits
@@ -442,7 +467,7 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_cta_kernel(const
         float acc = 0.f;
 #pragma unroll
         for (int gg = 0; gg < SG; ++gg) acc += red[gg][d];
-        O[static_cast<long long>(row) * D + d] = __float2bfloat16_rn(lsum > 0.f ? acc / lsum : 0.f);
+        store_out(O, o_fp32, static_cast<long long>(row) * D + d, lsum > 0.f ? acc / lsum : 0.f);
     }
 }
 
@@ -511,14 +536,15 @@ static cudaError_t launch_attn_d(const AttnParams& p, int grid, int W, bool pdl,
     const int rows = p.B * p.Hq;
     if (p.n_split <= kCombineWarpMaxSplits) {
         return launch_maybe_pdl(attn_combine_warp_kernel<D>, (rows + 7) / 8, 256, 0, pdl, s,
-                                static_cast<const float*>(p.ws), p.O, rows, p.n_split);
+                                static_cast<const float*>(p.ws), p.O, p.o_fp32, rows, p.n_split);
     }
     return launch_maybe_pdl(attn_combine_cta_kernel<D>, rows, kCombineThreads, 0, pdl, s,
-                            static_cast<const float*>(p.ws), p.O, p.n_split);
+                            static_cast<const float*>(p.ws), p.O, p.o_fp32, p.n_split);
 }
 
 dak_status launch_attn(const void* Q, const dak_placement* KV, const void* host_src, const int* seq_lens, int H_q,
-                       float scale, void* O, void* ws, size_t ws_bytes, const dak_tuning* t, cudaStream_t stream) {
+                       float scale, void* O, void* ws, size_t ws_bytes, const dak_tuning* t, cudaStream_t stream,
+                       int o_fp32) {
     if (!KV || KV->kind != 1 || !Q || !O) return DAK_ERR_INVALID;
     if (H_q <= 0 || H_q % KV->H_kv) return DAK_ERR_INVALID;
     const int G = H_q / KV->H_kv;
@@ -539,7 +565,8 @@ dak_status launch_attn(const void* Q, const dak_placement* KV, const void* host_
     p.kv[0] = static_cast<const uint8_t*>(host_src);
     p.kv[1] = static_cast<const uint8_t*>(KV->hbm_ptr);
     p.seq_lens = seq_lens;
-    p.O = static_cast<__nv_bfloat16*>(O);
+    p.O = O;
+    p.o_fp32 = o_fp32 ? 1 : 0;
     p.ws = static_cast<float*>(ws);
     p.B = KV->B;
     p.Hq = H_q;
@@ -599,6 +626,14 @@ extern "C" dak_status dak_attn(const void* Q, const dak_placement* KV, const int
     if (!KV) return DAK_ERR_INVALID;
     return dak::launch_attn(Q, KV, KV->host_dev, seq_lens, H_q, scale, O, workspace, ws_bytes, tuning,
                             static_cast<cudaStream_t>(stream));
+}
+
+extern "C" dak_status dak_attn_f32(const void* Q, const dak_placement* KV, const int* seq_lens, int H_q,
+                                   float scale, void* O, void* workspace, size_t ws_bytes, const dak_tuning* tuning,
+                                   void* stream) {
+    if (!KV) return DAK_ERR_INVALID;
+    return dak::launch_attn(Q, KV, KV->host_dev, seq_lens, H_q, scale, O, workspace, ws_bytes, tuning,
+                            static_cast<cudaStream_t>(stream), 1);
 }
 
 extern "C" dak_status dak_attn_staged(const void* Q, const dak_placement* KV, const void* staging,

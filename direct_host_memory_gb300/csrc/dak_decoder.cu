@@ -271,7 +271,7 @@ cudaError_t launch(Kernel k, dim3 grid, int threads, bool pdl, cudaStream_t s, A
 
 template <typename T>
 cudaError_t dalloc(T** p, size_t count) {
-    return cudaMalloc(reinterpret_cast<void**>(p), std::max<size_t>(count, 1) * sizeof(T));
+    return dev_alloc(reinterpret_cast<void**>(p), std::max<size_t>(count, 1) * sizeof(T));
 }
 
 bool matrix_is(const dak_placement* p, int64_t M, int64_t K) {
@@ -298,8 +298,7 @@ size_t staging_offset(const dak_decoder_layer& L, int upto) {
 void release(dak_decoder* d) {
     void* bufs[] = {d->x, d->h, d->qkv, d->q, d->att, d->ao, d->gu, d->act, d->dn, d->seq_lens, d->rope_cs,
                     d->inv_freq, d->ws, d->gemm_ws, d->staging[0], d->staging[1], d->ss[0], d->ss[1]};
-    for (void* p : bufs)
-        if (p) cudaFree(p);
+    for (void* p : bufs) dev_free(p);
     if (d->exec) cudaGraphExecDestroy(d->exec);
     for (int i = 0; i < 2; ++i) {
         if (d->ev_copied[i]) cudaEventDestroy(d->ev_copied[i]);
@@ -318,8 +317,12 @@ dak_status ensure_staging(dak_decoder* d) {
     d->staging_bytes = need;
     if (need == 0) return DAK_OK;
     for (int i = 0; i < 2; ++i) {
-        if (cudaMalloc(reinterpret_cast<void**>(&d->staging[i]), need) != cudaSuccess) {
+        if (dev_alloc(reinterpret_cast<void**>(&d->staging[i]), need) != cudaSuccess) {
             cudaGetLastError();
+            for (int j = 0; j < 2; ++j) {  // all or nothing: a later call tries both again
+                dev_free(d->staging[j]);
+                d->staging[j] = nullptr;
+            }
             return DAK_ERR_DEVICE_ALLOC;
         }
     }
@@ -588,20 +591,20 @@ extern "C" dak_status dak_decoder_create(const dak_decoder_config* cfg, const da
     chk(dalloc(&dd->rope_cs, Bs * D / 2));
     chk(dalloc(&dd->inv_freq, static_cast<size_t>(D / 2)));
     dd->ws_bytes = dak_attn_workspace_bytes(B, c.n_heads, c.head_dim, dd->n_split);
-    if (dd->ws_bytes) chk(cudaMalloc(reinterpret_cast<void**>(&dd->ws), dd->ws_bytes));
+    if (dd->ws_bytes) chk(dev_alloc(reinterpret_cast<void**>(&dd->ws), dd->ws_bytes));
     // a split workspace of its own, so that decoders on different streams never share one
     dd->gemm_ws_bytes = 0;
     for (int l = 0; l < c.n_layers; ++l)
         for (const dak_placement* g : {layers[l].qkv, layers[l].o, layers[l].gate_up, layers[l].down})
             dd->gemm_ws_bytes = std::max(dd->gemm_ws_bytes, gemm_workspace_bytes(g, B));
     if (dd->gemm_ws_bytes) {
-        chk(cudaMalloc(&dd->gemm_ws, dd->gemm_ws_bytes));
+        chk(dev_alloc(&dd->gemm_ws, dd->gemm_ws_bytes));
         if (e == cudaSuccess) chk(cudaMemset(dd->gemm_ws, 0, dd->gemm_ws_bytes));
     }
     dd->fuse_norm = B <= kFuseNormMaxBatch;
     if (dd->fuse_norm) {
         const size_t ss_bytes = static_cast<size_t>((d + kTileM - 1) / kTileM) * B * sizeof(float);
-        for (int i = 0; i < 2; ++i) chk(cudaMalloc(reinterpret_cast<void**>(&dd->ss[i]), ss_bytes));
+        for (int i = 0; i < 2; ++i) chk(dev_alloc(reinterpret_cast<void**>(&dd->ss[i]), ss_bytes));
     }
     if (e == cudaSuccess) {
         std::vector<double> inv(D / 2);

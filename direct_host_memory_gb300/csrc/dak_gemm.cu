@@ -1114,7 +1114,7 @@ static EncodeTiledFn encode_fn() {
 // element of B); otherwise 2-D boxes. Sets *b3d accordingly.
 static bool make_b_map(CUtensorMap* map, const void* B, int K, int N, int N_pad, int kc, int kind, int* b3d) {
     EncodeTiledFn enc = encode_fn();
-    if (!enc) return false;
+    if (!enc || fault_due(DAK_FAULT_TENSOR_MAP)) return false;
     const int blk = kind == kUmmaB ? 64 : 256;
     const int rows = kind == kUmmaB ? N_pad : N;
     const CUtensorMapSwizzle swz = kind == kUmmaB ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
@@ -1192,27 +1192,30 @@ constexpr int kSplitTiles = 1 << 16;
 static __device__ float g_split_part[kSplitFloats];
 static __device__ int g_split_cnt[kSplitTiles];
 
+// The arrays' device addresses on the current device, looked up once per device and context
+// (after cudaDeviceReset they live at new addresses of a new context).
 static bool split_workspace(float** part, int** cnt) {
-    static std::atomic<float*> parts[64];
-    static std::atomic<int*> cnts[64];
+    static float* parts[64];
+    static int* cnts[64];
+    static unsigned long long ctx[64];
+    static std::mutex mu;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
-    float* pp = parts[dev].load();
-    int* cp = cnts[dev].load();
-    if (!pp || !cp) {
+    std::lock_guard<std::mutex> lock(mu);
+    const unsigned long long id = current_context_id();
+    if (!parts[dev] || !cnts[dev] || ctx[dev] != id) {
         void* a = nullptr;
         void* b = nullptr;
         if (cudaGetSymbolAddress(&a, g_split_part) != cudaSuccess || cudaGetSymbolAddress(&b, g_split_cnt) != cudaSuccess) {
             cudaGetLastError();
             return false;
         }
-        pp = static_cast<float*>(a);
-        cp = static_cast<int*>(b);
-        parts[dev].store(pp);
-        cnts[dev].store(cp);
+        parts[dev] = static_cast<float*>(a);
+        cnts[dev] = static_cast<int*>(b);
+        ctx[dev] = current_context_id();
     }
-    *part = pp;
-    *cnt = cp;
+    *part = parts[dev];
+    *cnt = cnts[dev];
     return true;
 }
 

@@ -60,6 +60,21 @@ Sched schedule(int host_units, int hbm_units, int sm_slots, const dak_tuning* t,
 int device_sm_count();
 dak_status cuda_status(cudaError_t e);
 
+// Identifier of the current CUDA context, unique for the process's lifetime (0 if none): a
+// device address looked up with cudaGetSymbolAddress is kept together with it, so that the
+// address is looked up again after the context was destroyed and made anew.
+unsigned long long current_context_id();
+
+// The library's allocations go through these wrappers, which count the live allocations
+// (dak_alloc_counts) and take the host-side fault injection of dak_inject_fault: an injected
+// failure returns cudaErrorMemoryAllocation without calling CUDA.
+cudaError_t host_alloc_mapped(void** p, size_t bytes);  // cudaHostAlloc(Mapped | Portable)
+void host_free(void* p);
+cudaError_t dev_alloc(void** p, size_t bytes);
+void dev_free(void* p);
+// True when an injected failure of this kind (DAK_FAULT_*) is due now (consumes it).
+bool fault_due(int kind);
+
 // kernel launchers (defined in dak_gemm.cu / dak_attn.cu)
 // ws / ws_bytes: the caller's split workspace (dak_gemm_ws), or null for the module's own
 // A decode step's RMSNorm folded into the GEMMs around it (all members null = off).
@@ -80,7 +95,9 @@ dak_status launch_gemm(const dak_placement* A, const void* host_src, const void*
                        const dak_tuning* t, cudaStream_t s, void* ws = nullptr, size_t ws_bytes = 0,
                        const GemmFuse* fuse = nullptr);
 size_t gemm_workspace_bytes(const dak_placement* A, int N);
+// o_fp32: O is fp32 [B][H_q][D] (dak_attn_f32) instead of bf16
 dak_status launch_attn(const void* Q, const dak_placement* KV, const void* host_src, const int* seq_lens, int H_q,
-                       float scale, void* O, void* ws, size_t ws_bytes, const dak_tuning* t, cudaStream_t s);
+                       float scale, void* O, void* ws, size_t ws_bytes, const dak_tuning* t, cudaStream_t s,
+                       int o_fp32 = 0);
 
 }  // namespace dak

@@ -24,14 +24,18 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratch
 
 // Device address of the array on the current device. In host code the array's name is
 // only a host-side handle, so the address is looked up once per device (with that device
-// current) and kept.
+// current) and kept, together with the identifier of the context it belongs to: after a
+// cudaDeviceReset the context (and with it the array) is made anew at a new address, so a
+// changed identifier means looking it up again.
 void* noalloc_scratch_address() {
     static void* addr[64] = {nullptr};
+    static unsigned long long ctx[64] = {0};
     static std::mutex mu;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
+    const unsigned long long id = dak::current_context_id();
+    if (!addr[dev] || ctx[dev] != id) {
         void* p = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess) {
@@ -39,6 +43,7 @@ void* noalloc_scratch_address() {
             return nullptr;
         }
         addr[dev] = p;
+        ctx[dev] = dak::current_context_id();  // the lookup may have created the context
     }
     return addr[dev];
 }

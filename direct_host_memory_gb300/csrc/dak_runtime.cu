@@ -9,7 +9,9 @@
 #include <chrono>
 #include <cmath>
 #include <cstring>
+#include <cstdlib>
 #include <mutex>
+#include <string>
 #include <vector>
 
 #include "dak_device.cuh"
@@ -18,21 +20,138 @@ namespace dak {
 
 __device__ DevStatus g_status_block = {0, 0, 0ull};
 
+unsigned long long current_context_id() {
+    using GetCurrentFn = CUresult (*)(CUcontext*);
+    using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrentFn get_current = nullptr;
+    static GetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* a = nullptr;
+        void* b = nullptr;
+        cudaDriverEntryPointQueryResult qa, qb;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) == cudaSuccess &&
+            qa == cudaDriverEntryPointSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) == cudaSuccess &&
+            qb == cudaDriverEntryPointSuccess) {
+            get_current = reinterpret_cast<GetCurrentFn>(a);
+            get_id = reinterpret_cast<GetIdFn>(b);
+        }
+        cudaGetLastError();
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
 DevStatus* status_ptr() {
     static DevStatus* cache[64] = {nullptr};
+    static unsigned long long ctx[64] = {0};
     static std::mutex mu;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
     std::lock_guard<std::mutex> lock(mu);
-    if (!cache[dev]) {
+    const unsigned long long id = current_context_id();
+    if (!cache[dev] || ctx[dev] != id) {
         void* ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_status_block) != cudaSuccess) {
             cudaGetLastError();
             return nullptr;
         }
         cache[dev] = static_cast<DevStatus*>(ptr);
+        ctx[dev] = current_context_id();  // the lookup may have created the context
     }
     return cache[dev];
+}
+
+// ------------------------------------------------------------------------------------
+// allocations: live counts and host-side fault injection
+// ------------------------------------------------------------------------------------
+static std::atomic<long long> g_live_host{0}, g_live_dev{0};
+constexpr int kFaultKinds = 4;  // DAK_FAULT_HOST_ALLOC .. DAK_FAULT_TENSOR_MAP are 1..3
+static std::mutex g_fault_mu;
+static int g_fault_skip[kFaultKinds], g_fault_count[kFaultKinds];
+
+// DAK_FAULT_INJECT="host_alloc=SKIP:COUNT,device_alloc=COUNT,tensor_map=..." (SKIP defaults
+// to 0, COUNT -1 = every call), read once, at the library's first allocation or fault query.
+static void load_fault_env() {
+    static std::once_flag once;
+    std::call_once(once, [] {
+        const char* env = std::getenv("DAK_FAULT_INJECT");
+        if (!env) return;
+        static const char* names[kFaultKinds] = {"", "host_alloc", "device_alloc", "tensor_map"};
+        std::string spec(env);
+        size_t pos = 0;
+        std::lock_guard<std::mutex> lock(g_fault_mu);
+        while (pos < spec.size()) {
+            size_t end = spec.find(',', pos);
+            if (end == std::string::npos) end = spec.size();
+            const std::string item = spec.substr(pos, end - pos);
+            pos = end + 1;
+            const size_t eq = item.find('=');
+            if (eq == std::string::npos) continue;
+            const std::string name = item.substr(0, eq), val = item.substr(eq + 1);
+            for (int k = 1; k < kFaultKinds; ++k) {
+                if (name != names[k]) continue;
+                const size_t colon = val.find(':');
+                const int skip = colon == std::string::npos ? 0 : std::atoi(val.substr(0, colon).c_str());
+                const int count = std::atoi(colon == std::string::npos ? val.c_str() : val.substr(colon + 1).c_str());
+                g_fault_skip[k] = std::max(0, skip);
+                g_fault_count[k] = count;
+            }
+        }
+    });
+}
+
+bool fault_due(int kind) {
+    if (kind < 1 || kind >= kFaultKinds) return false;
+    load_fault_env();
+    std::lock_guard<std::mutex> lock(g_fault_mu);
+    if (g_fault_count[kind] == 0) return false;
+    if (g_fault_skip[kind] > 0) {
+        --g_fault_skip[kind];
+        return false;
+    }
+    if (g_fault_count[kind] > 0) --g_fault_count[kind];
+    return true;
+}
+
+cudaError_t host_alloc_mapped(void** p, size_t bytes) {
+    *p = nullptr;
+    if (fault_due(DAK_FAULT_HOST_ALLOC)) return cudaErrorMemoryAllocation;
+    const cudaError_t e = cudaHostAlloc(p, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+    if (e == cudaSuccess) {
+        ++g_live_host;
+    } else {
+        *p = nullptr;
+    }
+    return e;
+}
+
+void host_free(void* p) {
+    if (!p) return;
+    cudaFreeHost(p);
+    --g_live_host;
+}
+
+cudaError_t dev_alloc(void** p, size_t bytes) {
+    *p = nullptr;
+    if (fault_due(DAK_FAULT_DEVICE_ALLOC)) return cudaErrorMemoryAllocation;
+    const cudaError_t e = cudaMalloc(p, bytes);
+    if (e == cudaSuccess) {
+        ++g_live_dev;
+    } else {
+        *p = nullptr;
+    }
+    return e;
+}
+
+void dev_free(void* p) {
+    if (!p) return;
+    cudaFree(p);
+    --g_live_dev;
 }
 
 dak_status cuda_status(cudaError_t e) {
@@ -148,15 +267,14 @@ __global__ void pack_kv_kernel(const uint4* __restrict__ src, long long n_heads,
 
 static void free_parts(dak_placement* p) {
     if (!p) return;
-    if (p->host_ptr) cudaFreeHost(p->host_ptr);
-    if (p->hbm_ptr) cudaFree(p->hbm_ptr);
+    host_free(p->host_ptr);
+    dev_free(p->hbm_ptr);
     p->host_ptr = p->host_dev = p->hbm_ptr = nullptr;
 }
 
 static dak_status alloc_tiers(dak_placement* p) {
     if (p->host_bytes > 0) {
-        if (cudaHostAlloc(&p->host_ptr, static_cast<size_t>(p->host_bytes),
-                          cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess) {
+        if (host_alloc_mapped(&p->host_ptr, static_cast<size_t>(p->host_bytes)) != cudaSuccess) {
             cudaGetLastError();
             p->host_ptr = nullptr;
             return DAK_ERR_HOST_ALLOC;
@@ -167,7 +285,7 @@ static dak_status alloc_tiers(dak_placement* p) {
         }
     }
     if (p->hbm_bytes > 0) {
-        if (cudaMalloc(&p->hbm_ptr, static_cast<size_t>(p->hbm_bytes)) != cudaSuccess) {
+        if (dev_alloc(&p->hbm_ptr, static_cast<size_t>(p->hbm_bytes)) != cudaSuccess) {
             cudaGetLastError();
             p->hbm_ptr = nullptr;
             return DAK_ERR_DEVICE_ALLOC;
@@ -245,7 +363,7 @@ static dak_status place_matrix(const void* A_src, int src_on_device, int64_t M, 
     void* tmp = nullptr;
     cudaError_t e = cudaSuccess;
     if (!src_on_device && M > 0) {
-        e = cudaMalloc(&tmp, static_cast<size_t>(batch_tiles) * kTileM * lda * 2);
+        e = dev_alloc(&tmp, static_cast<size_t>(batch_tiles) * kTileM * lda * 2);
         if (e != cudaSuccess) {
             cudaGetLastError();
             free_parts(p);
@@ -301,7 +419,7 @@ static dak_status place_matrix(const void* A_src, int src_on_device, int64_t M, 
         }
         if (e == cudaSuccess) e = cudaDeviceSynchronize();
     }
-    if (tmp) cudaFree(tmp);
+    dev_free(tmp);
     if (e != cudaSuccess) {
         cudaGetLastError();
         free_parts(p);
@@ -366,7 +484,7 @@ extern "C" dak_status dak_place_kv(const void* K_src, const void* V_src, int src
     const int batch = std::max(1, static_cast<int>((256ll << 20) / src_req_bytes));
     void* tmp = nullptr;
     if (!src_on_device && e == cudaSuccess) {
-        e = cudaMalloc(&tmp, static_cast<size_t>(std::min(batch, B)) * src_req_bytes);
+        e = dev_alloc(&tmp, static_cast<size_t>(std::min(batch, B)) * src_req_bytes);
         if (e != cudaSuccess) {
             cudaGetLastError();
             free_parts(p);
@@ -402,7 +520,7 @@ extern "C" dak_status dak_place_kv(const void* K_src, const void* V_src, int src
             if (e == cudaSuccess) e = cudaDeviceSynchronize();
         }
     }
-    if (tmp) cudaFree(tmp);
+    dev_free(tmp);
     if (e != cudaSuccess) {
         cudaGetLastError();
         free_parts(p);
@@ -410,6 +528,28 @@ extern "C" dak_status dak_place_kv(const void* K_src, const void* V_src, int src
         return DAK_ERR_CUDA;
     }
     *out = p;
+    return DAK_OK;
+}
+
+extern "C" dak_status dak_inject_fault(int kind, int skip, int count) {
+    if (kind < 1 || kind >= kFaultKinds || skip < 0 || count < -1) return DAK_ERR_INVALID;
+    load_fault_env();
+    std::lock_guard<std::mutex> lock(g_fault_mu);
+    g_fault_skip[kind] = skip;
+    g_fault_count[kind] = count;
+    return DAK_OK;
+}
+
+extern "C" int dak_fault_pending(int kind) {
+    if (kind < 1 || kind >= kFaultKinds) return 0;
+    load_fault_env();
+    std::lock_guard<std::mutex> lock(g_fault_mu);
+    return g_fault_count[kind];
+}
+
+extern "C" dak_status dak_alloc_counts(int64_t* host_live, int64_t* device_live) {
+    if (host_live) *host_live = g_live_host.load();
+    if (device_live) *device_live = g_live_dev.load();
     return DAK_OK;
 }
 
@@ -598,14 +738,14 @@ struct ProbeBuffers {
     void* hbm = nullptr;
     long long host_bytes = 0, hbm_bytes = 0;
     ~ProbeBuffers() {
-        if (host) cudaFreeHost(host);
-        if (hbm) cudaFree(hbm);
+        host_free(host);
+        dev_free(hbm);
     }
 };
 
 static dak_status probe_alloc(ProbeBuffers& b, long long host_bytes, long long hbm_bytes) {
     if (host_bytes > 0) {
-        if (cudaHostAlloc(&b.host, host_bytes, cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess) {
+        if (host_alloc_mapped(&b.host, host_bytes) != cudaSuccess) {
             cudaGetLastError();
             b.host = nullptr;
             return DAK_ERR_HOST_ALLOC;
@@ -617,7 +757,7 @@ static dak_status probe_alloc(ProbeBuffers& b, long long host_bytes, long long h
         for (long long i = 0; i < n; ++i) w[i] = static_cast<uint32_t>(i * 2654435761ull);
     }
     if (hbm_bytes > 0) {
-        if (cudaMalloc(&b.hbm, hbm_bytes) != cudaSuccess) {
+        if (dev_alloc(&b.hbm, hbm_bytes) != cudaSuccess) {
             cudaGetLastError();
             b.hbm = nullptr;
             return DAK_ERR_DEVICE_ALLOC;
@@ -649,7 +789,8 @@ static dak_status probe_run(ProbeBuffers& b, int method, int host_ctas, int host
     if (grid <= 0) return DAK_ERR_INVALID;
     std::vector<unsigned long long> h_sums(grid), h_t0(grid), h_t1(grid);
     unsigned long long* d = nullptr;
-    if (cudaMalloc(&d, sizeof(unsigned long long) * 3 * grid) != cudaSuccess) return DAK_ERR_DEVICE_ALLOC;
+    if (dev_alloc(reinterpret_cast<void**>(&d), sizeof(unsigned long long) * 3 * grid) != cudaSuccess)
+        return DAK_ERR_DEVICE_ALLOC;
     a.sums = d;
     a.t_start = d + grid;
     a.t_end = d + 2 * grid;
@@ -660,7 +801,7 @@ static dak_status probe_run(ProbeBuffers& b, int method, int host_ctas, int host
         const uint8_t* tbuf = host_ctas > 0 ? a.buf[0] : a.buf[1];
         const long long tbytes = host_ctas > 0 ? a.bytes[0] : a.bytes[1];
         if (!enc || (host_ctas > 0 && hbm_ctas > 0) || chunk % 512 || chunk / 512 > 256) {
-            cudaFree(d);
+            dev_free(d);
             return DAK_ERR_UNSUPPORTED;
         }
         cuuint64_t dims[2] = {256, static_cast<cuuint64_t>(tbytes / 512)};
@@ -670,13 +811,13 @@ static dak_status probe_run(ProbeBuffers& b, int method, int host_ctas, int host
         if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint8_t*>(tbuf), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
-            cudaFree(d);
+            dev_free(d);
             return DAK_ERR_UNSUPPORTED;  // the tensor map does not encode over this memory
         }
     }
     const int smem = method == 1 ? 0 : std::max(a.window[0], a.window[1]) * chunk;
     if (smem > 220 * 1024) {
-        cudaFree(d);
+        dev_free(d);
         return DAK_ERR_INVALID;
     }
     cudaFuncSetAttribute(probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -687,7 +828,7 @@ static dak_status probe_run(ProbeBuffers& b, int method, int host_ctas, int host
         probe_kernel<<<grid, kProbeThreads, smem>>>(a, map);
         cudaError_t e = cudaDeviceSynchronize();
         if (e != cudaSuccess) {
-            cudaFree(d);
+            dev_free(d);
             return DAK_ERR_CUDA;
         }
         cudaMemcpy(h_sums.data(), a.sums, sizeof(unsigned long long) * grid, cudaMemcpyDeviceToHost);
@@ -710,7 +851,7 @@ static dak_status probe_run(ProbeBuffers& b, int method, int host_ctas, int host
             best[tier] = std::max(best[tier], gbps);
         }
     }
-    cudaFree(d);
+    dev_free(d);
     if (gbps_host) *gbps_host = best[0];
     if (gbps_hbm) *gbps_hbm = best[1];
     if (ok) *ok = data_ok;

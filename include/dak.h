@@ -231,6 +231,14 @@ size_t dak_attn_workspace_bytes(int B, int H_q, int D, int n_split);
 dak_status dak_attn(const void* Q, const dak_placement* KV, const int* seq_lens, int H_q, float scale, void* O,
                     void* workspace, size_t ws_bytes, const dak_tuning* tuning, void* stream);
 
+/* dak_attn with an fp32 output: O is fp32 [B][H_q][D] (device, 16-byte aligned), the same
+ * values as dak_attn before their final bf16 rounding. The parity mode of the attention, as
+ * c_fp32 is dak_gemm's: scores and probabilities are fp32, and the probabilities enter the
+ * P.V product as two bf16 parts (bf16(P) and bf16(P - bf16(P))), so nothing on the way is
+ * rounded to bf16 except the inputs. Arguments, workspace and errors as dak_attn. */
+dak_status dak_attn_f32(const void* Q, const dak_placement* KV, const int* seq_lens, int H_q, float scale, void* O,
+                        void* workspace, size_t ws_bytes, const dak_tuning* tuning, void* stream);
+
 /* The n_split dak_attn uses for a placement when tuning->n_split <= 0. */
 int dak_attn_default_split(const dak_placement* KV);
 
@@ -253,7 +261,8 @@ int dak_attn_default_split(const dak_placement* KV);
  *   dak_attn with a caller-provided workspace, or a smaller n_split, then.
  *   The first call on a device looks up the array's device address (cudaGetSymbolAddress,
  *   with that device current) and keeps it; make that first call before any stream
- *   capture. All calls share the array and it keeps the last call's contents (nothing in
+ *   capture. After cudaDeviceReset (a new context, with the array at a new address) the
+ *   next call looks it up again, so make that call outside a capture too. All calls share the array and it keeps the last call's contents (nothing in
  *   it has to start at zero): calls that overlap on the GPU race on it, so order them on
  *   one stream or with events. */
 dak_status dak_attn_noalloc(const void* Q, const dak_placement* KV, const int* seq_lens, int H_q, float scale,
@@ -453,6 +462,33 @@ dak_status dak_probe_read_bw(int tier, int64_t bytes, int method, int ctas, int 
 dak_status dak_probe_concurrent(int64_t host_bytes, int64_t hbm_bytes, int host_ctas, int host_window,
                                 int hbm_ctas, int hbm_window, int chunk_bytes, int iters, double* host_gbps,
                                 double* hbm_gbps);
+
+/* Host-side fault injection, for tests of the library's failure paths (the paper has no
+ * counterpart). The library's own allocations and its tensor-map encode check a per-kind
+ * switch first: after `skip` more calls of that kind succeed, the next `count` calls (-1 =
+ * every call until the switch is reset) fail as if CUDA had failed, without calling it:
+ *   DAK_FAULT_HOST_ALLOC   : the pinned, device-mapped host buffer of a placement or probe
+ *                            (the call returns DAK_ERR_HOST_ALLOC);
+ *   DAK_FAULT_DEVICE_ALLOC : the HBM part of a placement, its packing buffer, a decoder's
+ *                            activations and staging, a probe's buffers (DAK_ERR_DEVICE_ALLOC);
+ *   DAK_FAULT_TENSOR_MAP   : the hidden states' tensor map of dak_gemm (DAK_ERR_CUDA; nothing
+ *                            is launched and C is not written).
+ * A failed call frees whatever it had allocated and leaves its outputs unset. The switch is
+ * process-wide. It can also be set before the process starts with the environment variable
+ * DAK_FAULT_INJECT="host_alloc=SKIP:COUNT,device_alloc=COUNT,tensor_map=SKIP:COUNT" (SKIP
+ * optional), read at the first allocation or fault query; dak_inject_fault overrides it.
+ * DAK_ERR_INVALID for an unknown kind, skip < 0 or count < -1. Nothing touches a GPU. */
+#define DAK_FAULT_HOST_ALLOC 1
+#define DAK_FAULT_DEVICE_ALLOC 2
+#define DAK_FAULT_TENSOR_MAP 3
+dak_status dak_inject_fault(int kind, int skip, int count);
+
+/* Injected failures of this kind still to come (-1: every call), 0 for an unknown kind. */
+int dak_fault_pending(int kind);
+
+/* Allocations the library holds right now: pinned host buffers and device buffers (each
+ * placement holds at most one of each; a decoder holds its activations). For leak checks. */
+dak_status dak_alloc_counts(int64_t* host_live, int64_t* device_live);
 
 /* Self-test of the kernels' failure path: launches one CTA whose bounded wait on an
  * mbarrier that nothing arrives at runs out after about 2 s. The launch returns DAK_OK;

@@ -24,7 +24,7 @@ def dak():
 def _declared():
     src = open(os.path.join(ROOT, "include", "dak.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(dak_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(dak_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_every_declared_symbol_is_exported(dak):

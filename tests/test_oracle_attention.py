@@ -7,6 +7,7 @@ import pytest
 import synth
 from oracle import attention as oa
 from oracle import bf16 as obf
+from oracle import gemm as og
 
 pytestmark = pytest.mark.cpu
 
@@ -105,3 +106,20 @@ def test_one_row_helper_matches_full():
     o = oa.decode_attention_ref(q, k, v)
     for b, h in [(0, 0), (1, 7), (1, 3)]:
         assert np.allclose(oa.decode_attention_one(q, k, v, b, h), o[b, h], rtol=1e-14, atol=0)
+
+
+def test_fp32_tolerance_sees_a_dropped_or_doubled_token():
+    """The fp32-output parity mode's 1e-4 bound (of max |ref|) sees one token dropped or
+    counted twice at the full context of 8192, wherever it sits; the mistakes are planted in
+    the oracle's input, on the CPU."""
+    from gpu_util import ATTN_FP32_TOL
+    L = 8192
+    q, k, v = synth.attn_inputs(1, 4, 1, 128, L, seed=3)
+    ref = oa.decode_attention_ref(q, k, v)
+    for j in (0, 63, 64, 4095, L - 1):
+        keep = np.delete(np.arange(L), j)
+        dropped = oa.decode_attention_ref(q, k[:, :, keep], v[:, :, keep])
+        assert og.rel_err(dropped, ref) > 2 * ATTN_FP32_TOL, j
+        twice = np.concatenate([np.arange(L), [j]])
+        doubled = oa.decode_attention_ref(q, k[:, :, twice], v[:, :, twice])
+        assert og.rel_err(doubled, ref) > 2 * ATTN_FP32_TOL, j

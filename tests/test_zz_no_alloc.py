@@ -41,6 +41,8 @@ def test_noalloc_matches_dak_attn_on_two_calls(dak):
         dak.dak_attn_noalloc(qt, p, out, seq_lens=lens)
         st, info = dak.dak_last_error()
         assert st == 0, f"device status {st} info {info:#x}"
+        # the same kernels with the same split and merge order: only the workspace differs
+        assert torch.equal(out, ref)
         assert og.rel_err(to_np(out), to_np(ref)) <= REL_TOL
     p.free()
 
@@ -55,4 +57,12 @@ def test_noalloc_rejects_calls_beyond_its_array(dak):
     assert dak.dak_attn_workspace_bytes(64, 128, 128, 64) > dak.NOALLOC_SCRATCH_BYTES
     with pytest.raises(dak.DakError):
         dak.dak_attn_noalloc(q, p, out, tuning=dict(n_split=64))
+    # the library's own check, called through the C ABI past the Python wrapper's
+    import ctypes
+    t = dak.dak_tuning(n_split=64)
+    st = dak.lib.dak_attn_noalloc(ctypes.c_void_p(q.data_ptr()), p.handle, None, 128, ctypes.c_float(0.0),
+                                  ctypes.c_void_p(out.data_ptr()), ctypes.byref(t),
+                                  ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 1  # DAK_ERR_INVALID
+    assert dak.dak_last_error()[0] == 0  # nothing was launched
     p.free()

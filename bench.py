@@ -55,8 +55,9 @@ def _args():
                     help="--profile decode: batch of the step (default: the model configuration's)")
     ap.add_argument("--plain-launch", action="store_true",
                     help="--profile decode: eager steps with ordinary launches (no graph, no programmatic launch)")
-    ap.add_argument("--profile", default=None, choices=["attn", "qkv", "o", "gate_up", "down", "decode"],
-                    help="place one operation of the step at --x and launch it --steps times (for ncu)")
+    ap.add_argument("--profile", default=None, choices=["attn", "qkv", "o", "gate_up", "down", "decode", "chain"],
+                    help="place one operation of the step at --x and launch it --steps times (for ncu); chain: the "
+                         "four 8B linears as one grouped dak_gemm_chain launch")
     return ap.parse_args()
 
 
@@ -570,11 +571,21 @@ def run_linears_n(dak, lin, b_host, b_hbm, dev, xs=(0.0, 0.25), ns=(1, 8, 32, 64
                     one_pass()
             t = time_steps(g.replay, 20, 3)
             roof = tier_roofline(C_bytes, H / C_bytes, b_host, b_hbm)
-            rows.append({"N": N, "x": x, "us": t * 1e6, "gbps": C_bytes / t / 1e9, "frac": (C_bytes / t) / roof})
+            row = {"N": N, "x": x, "us": t * 1e6, "gbps": C_bytes / t / 1e9, "frac": (C_bytes / t) / roof}
             del g
+            if N >= 2:
+                # the same four GEMMs as one grouped launch (dak_gemm_chain, no dependencies)
+                ops = [dict(A=p, B=Bs[n], C=Cs[n]) for n, p in pls.items()]
+                ws = torch.zeros(dak.dak_gemm_chain_workspace_bytes(ops, N), dtype=torch.uint8, device=dev)
+                g = _capture(lambda: dak.dak_gemm_chain(ops, workspace=ws, tuning=dict(pdl=1)))
+                tc = time_steps(g.replay, 20, 3)
+                row.update(chain_us=tc * 1e6, chain_gbps=C_bytes / tc / 1e9, chain_frac=(C_bytes / tc) / roof)
+                del g, ws
+            rows.append(row)
         for p in pls.values():
             p.free()
-    return {"ops": "8B QKV, O, gate+up, down (one graph of four launches)", "rows": rows,
+    return {"ops": "8B QKV, O, gate+up, down: one graph of four dak_gemm launches (us, frac), and one grouped "
+                   "dak_gemm_chain launch of the four (chain_us, chain_frac; N >= 2)", "rows": rows,
             "status": dak.dak_last_error()[0]}
 
 
@@ -601,7 +612,8 @@ def run_per_op_x(dak, lin, attn, b_host, b_hbm, dev, ns=(1, 8, 32, 64)):
     included; CUDA events around the launch), and `chain`, a CUDA graph of launches with
     programmatic launch over enough copies of the placement that they stream more than
     twice the L2 size (the rate of the operation repeated back to back, as in a model's
-    layers). Bytes are the operation's weights (or KV cache)."""
+    layers); for the linears at N >= 2 also `grouped`, up to 8 of those copies in one
+    dak_gemm_chain launch. Bytes are the operation's weights (or KV cache)."""
     import math
     import torch
     import synth
@@ -645,7 +657,17 @@ def run_per_op_x(dak, lin, attn, b_host, b_hbm, dev, ns=(1, 8, 32, 64)):
                 g = _capture(lambda: [dak.dak_gemm(p, Bs[N], Cs[N], tuning=pdl) for p in pls])
                 tc = time_steps(g.replay, 10, 3) / copies
                 del g
-                rows.append(dict(x=x, N=N, **point(C_bytes, H, t1, tc)))
+                rec = dict(x=x, N=N, **point(C_bytes, H, t1, tc))
+                if N >= 2:
+                    # the copies as one grouped launch (dak_gemm_chain: up to 8 operations)
+                    ops = [dict(A=p, B=Bs[N], C=Cs[N]) for p in pls[:8]]
+                    ws = torch.zeros(dak.dak_gemm_chain_workspace_bytes(ops, N), dtype=torch.uint8, device=dev)
+                    g = _capture(lambda: dak.dak_gemm_chain(ops, workspace=ws, tuning=pdl))
+                    tg = time_steps(g.replay, 10, 3) / len(ops)
+                    del g, ws
+                    roof = tier_roofline(C_bytes, H / C_bytes, b_host, b_hbm)
+                    rec.update(grouped_us=tg * 1e6, grouped_frac=(C_bytes / tg) / roof)
+                rows.append(rec)
             for p in pls:
                 p.free()
         del Ad
@@ -1214,6 +1236,23 @@ def run_profile(args):
                           "tok_s": cfg["batch"] / t, "launches_per_step": dec.launches(), "status": st[0],
                           "host_units_per_layer": units[0]}))
         dec.free()
+        return
+    if args.profile == "chain":
+        pls, ops = [], []
+        for i, (name, (M, K)) in enumerate(synth.LINEARS_8B.items()):
+            A, B = synth.gemm_inputs(M, K, args.batch, seed=0, tensor_index=i)
+            pls.append(dak.dak_place_matrix(A, dak.host_tiles_for_ratio(args.x, M)))
+            ops.append(dict(A=pls[-1], B=torch.from_numpy(B.view("int16")).view(torch.bfloat16).to(dev)))
+        ws = torch.zeros(dak.dak_gemm_chain_workspace_bytes(ops, args.batch), dtype=torch.uint8, device=dev)
+        outs = [torch.empty((args.batch, p.meta["M"]), dtype=torch.bfloat16, device=dev) for p in pls]
+        for o, c in zip(ops, outs):
+            o["C"] = c
+        t = time_steps(lambda: dak.dak_gemm_chain(ops, workspace=ws), args.steps, args.warmup)
+        nbytes = sum(p.host_bytes + p.hbm_bytes for p in pls)
+        print(json.dumps({"profile": "chain", "x": args.x, "batch": args.batch, "us_per_launch": t * 1e6,
+                          "gbps": nbytes / t / 1e9, "status": dak.dak_last_error()[0]}))
+        for p in pls:
+            p.free()
         return
     if args.profile == "attn":
         c = synth.ATTN_DECODE

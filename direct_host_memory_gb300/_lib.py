@@ -30,7 +30,8 @@ EXPORTS = [
     "dak_decoder_create", "dak_decoder_batch", "dak_decoder_step", "dak_decoder_capture",
     "dak_decoder_replay", "dak_decoder_launches", "dak_decoder_free", "dak_tune_gemm", "dak_tune_attn",
     "dak_place_matrix_glu", "dak_plan_units", "dak_gemm_workspace_bytes", "dak_gemm_ws", "dak_gemm_plan",
-    "dak_attn_f32", "dak_inject_fault", "dak_fault_pending", "dak_alloc_counts",
+    "dak_attn_f32", "dak_inject_fault", "dak_fault_pending", "dak_alloc_counts", "dak_gemm_chain",
+    "dak_gemm_chain_workspace_bytes",
 ]
 
 # host-side fault injection kinds (DAK_FAULT_* in dak.h)
@@ -51,6 +52,11 @@ class dak_tuning(ctypes.Structure):
                 ("chunk_k", ctypes.c_int), ("n_split", ctypes.c_int), ("hbm_ctas", ctypes.c_int),
                 ("split_k", ctypes.c_int), ("pdl", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
                 ("no_wave_align", ctypes.c_int), ("column_blocks", ctypes.c_int)]
+
+
+class dak_gemm_op(ctypes.Structure):
+    _fields_ = [("A", ctypes.c_void_p), ("B", ctypes.c_void_p), ("C", ctypes.c_void_p), ("c_fp32", ctypes.c_int),
+                ("after_prev", ctypes.c_int)]
 
 
 class dak_op(ctypes.Structure):
@@ -100,6 +106,8 @@ def _load():
         "dak_gemm_workspace_bytes": (sz, [vp, i32]),
         "dak_gemm_ws": (i32, [vp, vp, vp, i32, i32, P(dak_tuning), vp, sz, vp]),
         "dak_gemm_plan": (i32, [i64, i64, i32, i32, i32, P(dak_tuning), sz, P(dak_gemm_plan_info)]),
+        "dak_gemm_chain_workspace_bytes": (sz, [P(dak_gemm_op), i32, i32, P(dak_tuning)]),
+        "dak_gemm_chain": (i32, [P(dak_gemm_op), i32, i32, P(dak_tuning), vp, sz, vp]),
         "dak_attn_workspace_bytes": (sz, [i32, i32, i32, i32]),
         "dak_attn": (i32, [vp, vp, vp, i32, ctypes.c_float, vp, vp, sz, P(dak_tuning), vp]),
         "dak_attn_staged": (i32, [vp, vp, vp, vp, i32, ctypes.c_float, vp, vp, sz, P(dak_tuning), vp]),
@@ -292,6 +300,53 @@ def dak_gemm(A: Placement, B, C=None, c_fp32: bool = False, tuning=None, stream=
         _check(lib.dak_gemm_ws(A.handle, _ptr(B), _ptr(C), N, int(bool(c_fp32)), _tuning(tuning), _ptr(workspace),
                                ctypes.c_size_t(nbytes), _stream_ptr(stream)), "dak_gemm_ws")
     return C
+
+
+def _chain_ops(ops):
+    arr = (dak_gemm_op * len(ops))()
+    for j, o in enumerate(ops):
+        arr[j].A = o["A"].handle
+        arr[j].B = o["B"].data_ptr() if o.get("B") is not None else None
+        arr[j].C = o["C"].data_ptr() if o.get("C") is not None else None
+        arr[j].c_fp32 = int(bool(o.get("c_fp32", False)))
+        arr[j].after_prev = int(bool(o.get("after_prev", False)))
+    return arr
+
+
+def dak_gemm_chain_workspace_bytes(ops, N: int, tuning=None) -> int:
+    """Bytes of the workspace dak_gemm_chain needs (ops: dicts with at least 'A')."""
+    return int(lib.dak_gemm_chain_workspace_bytes(_chain_ops(ops), len(ops), int(N), _tuning(tuning)))
+
+
+def dak_gemm_chain(ops, tuning=None, workspace=None, stream=None):
+    """Several GEMMs in one persistent launch. ops: list of dicts with 'A' (Placement), 'B'
+    (bf16 [N][K] CUDA tensor), optional 'C', 'c_fp32' and 'after_prev' (B comes from an
+    earlier operation of the chain). workspace: a zeroed CUDA tensor of
+    dak_gemm_chain_workspace_bytes bytes (allocated and zeroed here when None). Returns the
+    list of C tensors."""
+    import torch
+    if not ops:
+        raise ValueError("empty chain")
+    N = int(ops[0]["B"].shape[0])
+    ops = [dict(o) for o in ops]
+    for o in ops:
+        _check_bf16_cuda(o["B"], "B")
+        if int(o["B"].shape[0]) != N or int(o["B"].shape[1]) != o["A"].meta["K"]:
+            raise ValueError("every B must be [N][K] with the same N")
+        if o.get("C") is None:
+            cols = o["A"].meta["M"] // 2 if o["A"].meta.get("glu") else o["A"].meta["M"]
+            o["C"] = torch.empty((N, cols), dtype=torch.float32 if o.get("c_fp32") else torch.bfloat16,
+                                 device=o["B"].device)
+    if workspace is None:
+        nbytes = dak_gemm_chain_workspace_bytes(ops, N, tuning) if len(ops) <= 8 else 0
+        if nbytes == 0:  # a chain the library rejects: let it say why
+            _check(lib.dak_gemm_chain(_chain_ops(ops), len(ops), N, _tuning(tuning), None, 0, _stream_ptr(stream)),
+                   "dak_gemm_chain")
+        workspace = torch.zeros(nbytes, dtype=torch.uint8, device=ops[0]["B"].device)
+    _check(lib.dak_gemm_chain(_chain_ops(ops), len(ops), N, _tuning(tuning), _ptr(workspace),
+                              ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream_ptr(stream)),
+           "dak_gemm_chain")
+    return [o["C"] for o in ops]
 
 
 def dak_gemm_workspace_bytes(A: Placement, N: int) -> int:

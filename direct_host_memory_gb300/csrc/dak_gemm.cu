@@ -23,6 +23,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cstring>
 #include <mutex>
 
 #include "dak_device.cuh"
@@ -255,13 +256,16 @@ done:
     drain_fills(b_full, WB, ib, p.st);
 }
 
-// Shared tile rows across the 256-row blocks of a wide B (NC > 1). Rank 0 of the cluster
-// fetches every A chunk (host or HBM) once; its forwarder copies each arrived chunk from its
+// Shared tile rows across the 256-row blocks of a wide B (NC > 1). For host tile rows, rank 0
+// of the cluster fetches every A chunk once; its forwarder copies each arrived chunk from its
 // ring slot into the same slot of every other rank with shared-to-shared bulk copies, waits
 // until the copies have read the slot, and then releases it. The other ranks only arm their
 // full barrier with the chunk's byte count and, once their MMAs have finished with a slot,
 // tell rank 0 that it may be refilled. Each host byte therefore crosses the host link once
-// however many 256-row blocks B has (no multicast is involved).
+// however many 256-row blocks B has (no multicast is involved). HBM tile rows are not
+// forwarded: every rank streams its chunks itself, and since the ranks of a cluster read the
+// same tile row together, L2 serves the repeats (HBM reads stay at one per byte; forwarding
+// them to three peers made 4-CTA clusters 2.4x slower per tile row than 2-CTA ones).
 // Run by the whole forwarder warp of rank 0: lane r - 1 copies to rank r, so the copies to
 // the NC - 1 other ranks are issued in parallel.
 __device__ __forceinline__ void forward_a(const GemmParams& p, const TileIter& it, uint8_t* smem, uint64_t* full,
@@ -748,7 +752,8 @@ __device__ __forceinline__ void fuse_tile_sums(const GemmParams& p, const float 
 
 template <bool F>
 __global__ void __launch_bounds__(kUmmaThreads, 1)
-    gemm_umma_kernel(const GemmParams p, const __grid_constant__ CUtensorMap bmap) {
+    gemm_umma_kernel(const GemmParams p, const __grid_constant__ CUtensorMap bmap,
+                     const __grid_constant__ CUtensorMap bmap_host) {
     // the folded norm's code exists only in the F = true instantiation
     const bool fx = F && p.res_x != nullptr;
     const bool fr = F && p.ss_in != nullptr;
@@ -778,7 +783,10 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
-        const bool fwd = p.NC > 1 && it.rank == 0;
+        // host tiles in a cluster: rank 0 fetches and forwards (each host byte crosses the link
+        // once); HBM tiles: every rank fetches its chunks itself (the cluster's ranks read the same
+        // tile row together, so L2 serves the repeats)
+        const bool fwd = p.NC > 1 && it.rank == 0 && it.host;
         const bool b_ring = it.c.kcb < it.c.kc;
         for (int s = 0; s < W; ++s) {
             mbar_init(&full[s], b_ring ? 1 : 2);  // A producer (or A arming) [+ B producer]
@@ -797,6 +805,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         }
         fence_mbar_init();
         prefetch_tmap(&bmap);
+        prefetch_tmap(&bmap_host);
     }
     if (warp == 1) {
         tmem_alloc(&tmem_base_sh, tmem_cols);
@@ -811,16 +820,17 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
 
     if (warp == 0 || warp == 6) {
         if (lane == 0) {
-            if (warp == 0 && p.NC > 1 && it.rank > 0) {
+            if (warp == 0 && p.NC > 1 && it.rank > 0 && it.host) {
                 arm_forwarded_a(p, it, full, empty, peer_empty, abort);
             } else if (warp == 6 && it.c.kcb < it.c.kc) {
-                produce_b_ring(p, it, &bmap, smem, b_full, b_empty, abort);
+                // B of a split ring (a role whose B chunks are kcb wide: its own tensor map)
+                produce_b_ring(p, it, it.host ? &bmap_host : &bmap, smem, b_full, b_empty, abort);
             } else {
-                produce(p, it, &bmap, smem, full, empty, abort, warp == 0, kUmmaB);
+                produce(p, it, it.host ? &bmap_host : &bmap, smem, full, empty, abort, warp == 0, kUmmaB);
             }
         }
     } else if (warp == 7) {
-        if (p.NC > 1 && it.rank == 0) forward_a(p, it, smem, full, empty, peer_empty, abort);
+        if (p.NC > 1 && it.rank == 0 && it.host) forward_a(p, it, smem, full, empty, peer_empty, abort);
     } else if (warp == 1) {
         // The whole warp runs the loop (so that loop state and descriptors stay warp-uniform);
         // one elected lane issues the MMAs and commits.
@@ -1090,6 +1100,403 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
 }
 
 // ======================================================================================
+// Chains of GEMMs in one persistent launch (N = 2..128, tensor cores). Every CTA takes its
+// units of operation 0, then of operation 1, and so on, each operation dealt to its tiers'
+// CTAs exactly as a launch of its own would deal it. The A producer streams the weights of
+// the next operation as soon as ring slots free up, so the weight stream does not stop at
+// an operation boundary (the weights never depend on an earlier operation). An operation
+// marked after_prev reads its hidden states (B), and any fused-norm input, from the
+// previous operation's outputs: its B loads and its epilogue wait until every CTA of the
+// launch has counted the previous operation done (a device counter per operation; each
+// CTA counts itself in after its last store of that operation, with release semantics,
+// and only after it has itself seen the previous operation done, so the order is
+// transitive). The waits are bounded like every other wait of the library.
+// ======================================================================================
+struct ChainParams {
+    GemmParams op[kMaxChainOps];
+    int after_prev[kMaxChainOps];
+    int n_ops;
+    int n_ctas;  // CTAs of the launch: every one counts itself in after every operation
+    int* done;   // [n_ops] CTAs that finished operation j; the last CTA of the launch zeroes them
+    DevStatus* st;
+};
+
+struct ChainMaps {
+    CUtensorMap m[kMaxChainOps];  // B of each operation
+};
+static_assert(sizeof(ChainParams) + sizeof(ChainMaps) <= 4096, "chain parameters exceed the 4 KB kernel parameter space");
+
+enum : uint32_t { W_CHAIN_DEP = 20 };
+
+// Wait (bounded) until *addr >= target, with acquire semantics; then order this thread's later
+// asynchronous-proxy reads (bulk tensor copies) after the acquire.
+__device__ __forceinline__ bool wait_count(const int* addr, int target, volatile int* abort, DevStatus* st,
+                                           uint32_t where) {
+    const uint64_t t0 = globaltimer();
+    while (true) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+        if (v >= target) {
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            return true;
+        }
+        if (*abort) return false;
+        if (globaltimer() - t0 > kWaitLimitNs) {
+            *abort = 1;
+            report(st, DAK_ERR_TIMEOUT, (static_cast<unsigned long long>(where) << 32) | blockIdx.x);
+            return false;
+        }
+        __nanosleep(128);
+    }
+}
+
+// One CTA's units of an operation in a chain (its tier and unit range, as tiles_of_cta);
+// none for a CTA beyond the operation's own CTAs (a chain launches as many as its widest
+// operation uses).
+__device__ __forceinline__ TileIter chain_tiles(const GemmParams& p, int W) {
+    TileIter it = tiles_of_cta(p);
+    it.window = W;
+    if (static_cast<int>(blockIdx.x) >= p.n_host_ctas + p.n_hbm_ctas) it.count = 0;
+    return it;
+}
+
+// A or B producer of a chain: the chunks of every operation in order, ring index i running
+// on across operations. The B producer waits for an operation's inputs before its first copy.
+__device__ __forceinline__ void chain_produce(const ChainParams& cp, const ChainMaps& maps, uint8_t* smem,
+                                              uint64_t* full, uint64_t* empty, volatile int* abort, bool is_a,
+                                              int W) {
+    const uint64_t pol_a = policy_evict_first();
+    long long i = 0;
+    for (int j = 0; j < cp.n_ops && !*abort; ++j) {
+        const GemmParams& p = cp.op[j];
+        const TileIter it = chain_tiles(p, W);
+        if (!is_a) {
+            if (j == 0) {
+                grid_dep_wait();  // the first operation's hidden states may come from the previous kernel
+            } else if (cp.after_prev[j] && !wait_count(cp.done + (j - 1), cp.n_ctas, abort, cp.st, W_CHAIN_DEP)) {
+                break;
+            }
+        }
+        for (int ui = 0; ui < it.count && !*abort; ++ui) {
+            const Piece q = piece_of(p, it, ui);
+            const uint8_t* src = tile_src(p, it, q.t);
+            for (int k0 = q.k0; k0 < q.k1; k0 += it.c.kc, ++i) {
+                const int s = static_cast<int>(i % W);
+                if (i >= W && !mbar_wait(&empty[s], static_cast<uint32_t>(((i / W) - 1) & 1), abort, p.st,
+                                         DAK_ERR_TIMEOUT, is_a ? W_PROD_EMPTY : W_BPROD_EMPTY)) {
+                    goto done;
+                }
+                uint8_t* dst = smem + static_cast<size_t>(s) * it.c.stage_bytes;
+                if (is_a) {
+                    const uint32_t a_bytes = static_cast<uint32_t>(min(it.c.kc, q.k1 - k0)) * 128u;
+                    mbar_arrive_expect_tx(&full[s], a_bytes);
+                    bulk_g2s(dst, src + static_cast<long long>(k0) * 128, a_bytes, &full[s], pol_a);
+                } else {
+                    mbar_arrive_expect_tx(&full[s], b_stage_bytes(p, kUmmaB, it.c.kcb));
+                    issue_b(p, &maps.m[j], dst + it.c.kc * 128, k0, &full[s], kUmmaB, 0, it.c.kcb);
+                }
+            }
+        }
+    }
+done:
+    drain_fills(full, W, i, cp.st);
+}
+
+template <bool F>
+__global__ void __launch_bounds__(kUmmaThreads, 1)
+    gemm_chain_kernel(const __grid_constant__ ChainParams cp, const __grid_constant__ ChainMaps maps) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ uint64_t full[8], empty[8], acc_full[2], acc_empty[2];
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int abort_flag;
+    __shared__ int last_piece;
+    __shared__ float fuse_ssw[4][kFuseMaxN];
+    __shared__ float fuse_red[kFuseMaxN];
+    __shared__ float fuse_r[kFuseMaxN];
+    volatile int* abort = &abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int N_pad = cp.op[0].N_pad;      // the same for every operation of a chain
+    const int W = cp.op[0].ch[0].stages;  // one ring for every operation and tier
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    uint32_t tmem_cols = 32;
+    while (tmem_cols < static_cast<uint32_t>(2 * N_pad)) tmem_cols <<= 1;
+    const uint32_t acc_stride = tmem_cols >> 1;
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int s = 0; s < W; ++s) {
+            mbar_init(&full[s], 2);   // A producer + B producer
+            mbar_init(&empty[s], 1);  // MMA commit
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 4);
+        }
+        fence_mbar_init();
+        for (int j = 0; j < cp.n_ops; ++j) prefetch_tmap(&maps.m[j]);
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_base_sh, tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    grid_dep_launch();
+    const uint32_t tmem = tmem_base_sh;
+
+    if (warp == 0 || warp == 6) {
+        if (lane == 0) chain_produce(cp, maps, smem, full, empty, abort, warp == 0, W);
+    } else if (warp == 1) {
+        const uint32_t idesc = idesc_bf16_f32(64, static_cast<uint32_t>(N_pad));
+        const bool leader = elect_one();
+        const int a_stage_bytes = cp.op[0].ch[0].kc * 128;
+        const uint32_t bblk16 = static_cast<uint32_t>((N_pad * 128) >> 4);
+        long long i = 0;
+        int uu = 0;  // units of the whole chain so far (the accumulator alternates on it)
+        uint64_t* last_bar = nullptr;
+        uint32_t last_par = 0;
+        bool ok = true;
+        for (int j = 0; j < cp.n_ops && ok; ++j) {
+            const GemmParams& p = cp.op[j];
+            const TileIter it = chain_tiles(p, W);
+            for (int ui = 0; ui < it.count && ok; ++ui, ++uu) {
+                const int ab = uu & 1;
+                if (uu >= 2 && !mbar_wait(&acc_empty[ab], static_cast<uint32_t>(((uu >> 1) - 1) & 1), abort, p.st,
+                                          DAK_ERR_TIMEOUT, W_MMA_ACC)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + static_cast<uint32_t>(ab) * acc_stride;
+                const Piece q = piece_of(p, it, ui);
+                for (int k0 = q.k0; k0 < q.k1; k0 += it.c.kc, ++i) {
+                    const int s = static_cast<int>(i % W);
+                    if (!mbar_wait(&full[s], static_cast<uint32_t>((i / W) & 1), abort, p.st, DAK_ERR_TIMEOUT,
+                                   W_MMA_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int kce = min(it.c.kc, q.k1 - k0);
+                    const uint32_t a_base = smem_u32(smem + static_cast<size_t>(s) * it.c.stage_bytes);
+                    const uint64_t ad0 = smem_desc(a_base, 1024u, 128u, 0u);
+                    const uint64_t bd0 = smem_desc(a_base + static_cast<uint32_t>(a_stage_bytes), 16u, 1024u, 2u);
+                    if (leader) {
+                        issue_mmas(d_tmem, ad0, bd0, bblk16, kce >> 4, idesc, k0 > q.k0);
+                        umma_commit(&empty[s]);
+                    }
+                    __syncwarp();
+                    last_bar = &empty[s];
+                    last_par = static_cast<uint32_t>((i / W) & 1);
+                }
+                if (!ok) break;
+                if (leader) umma_commit(&acc_full[ab]);
+                __syncwarp();
+                last_bar = &acc_full[ab];
+                last_par = static_cast<uint32_t>((uu >> 1) & 1);
+            }
+        }
+        if (last_bar) {  // every issued MMA has finished before TMEM is released
+            volatile int dummy = 0;
+            mbar_wait(last_bar, last_par, &dummy, cp.st, DAK_ERR_TIMEOUT, W_DRAIN);
+        }
+        __syncwarp();
+    } else if (warp >= 2 && warp <= 5) {
+        // epilogue warps 2..5 -> TMEM sub-partitions 2, 3, 0, 1 (as gemm_umma_kernel)
+        const int qp = warp & 3;
+        const int row_in_tile = umma_m64_row_of_lane(qp, lane);
+        const int tile_floats = kTileM * N_pad;
+        const int e = threadIdx.x - 64;  // 0..127
+        grid_dep_wait();  // C, the fused inputs and the workspace may be in use by the previous kernel
+        bool failed = false;
+        int uu = 0;
+        for (int j = 0; j < cp.n_ops; ++j) {
+            const GemmParams& p = cp.op[j];
+            const bool fx = F && p.res_x != nullptr;
+            const bool fr = F && p.ss_in != nullptr;
+            const TileIter it = chain_tiles(p, W);
+            if (j > 0 && cp.after_prev[j]) {
+                // the previous operation's outputs (this one's B, fused inputs, or a buffer it
+                // overwrites) are complete once every CTA has counted it in
+                if (e == 0 && !failed && !wait_count(cp.done + (j - 1), cp.n_ctas, abort, cp.st, W_CHAIN_DEP))
+                    failed = true;
+                epilogue_bar_sync();
+                failed = failed || *abort;
+            }
+            const float* rsc = nullptr;
+            if (fr) {
+                const int G = max(1, 128 / p.N);
+                if (e < G * p.N) {
+                    const int n = e % p.N, gi = e / p.N;
+                    float v = 0.f;
+                    for (int t = gi; t < p.ss_tiles; t += G) v += p.ss_in[static_cast<long long>(t) * p.N + n];
+                    fuse_red[gi * p.N + n] = v;
+                }
+                epilogue_bar_sync();
+                if (e < p.N) {
+                    float v = 0.f;
+                    for (int gi = 0; gi < G; ++gi) v += fuse_red[gi * p.N + e];
+                    fuse_r[e] = rsqrtf(v * p.ss_inv_d + p.ss_eps);
+                }
+                epilogue_bar_sync();
+                rsc = fuse_r;
+            }
+            const bool xpre_on = fx && N_pad <= kFusePreloadN;
+            float xpre[kFusePreloadN];
+            float gpre = 0.f;
+            for (int ui = 0; ui < it.count; ++ui, ++uu) {
+                const int ab = uu & 1;
+                if (xpre_on) {
+                    const int t = piece_of(p, it, ui).t;
+                    const int xrow = t * kTileM + (p.P > 1 ? (e & 63) : row_in_tile);
+                    const int xn0 = p.P > 1 ? 8 * (e >> 6) : 0;
+                    const bool ok = (p.P > 1 || row_in_tile >= 0) && xrow < p.M;
+                    const int xcols = p.P > 1 ? 8 : N_pad;
+#pragma unroll
+                    for (int jj = 0; jj < kFusePreloadN; ++jj) {
+                        const int n = xn0 + jj;
+                        const bool use = ok && jj < xcols && n < p.N;
+                        xpre[jj] = use ? p.res_x[static_cast<long long>(n) * p.M + xrow] : 0.f;
+                    }
+                    gpre = ok ? __bfloat162float(p.res_g[xrow]) : 0.f;
+                }
+                if (!failed && !mbar_wait(&acc_full[ab], static_cast<uint32_t>((uu >> 1) & 1), abort, p.st,
+                                          DAK_ERR_TIMEOUT, W_EPI_ACC)) {
+                    failed = true;
+                }
+                tc_fence_after();
+                const Piece pc = piece_of(p, it, ui);
+                const int row = pc.t * kTileM + row_in_tile;
+                const bool valid = row_in_tile >= 0 && row < p.M;
+                const uint32_t taddr =
+                    tmem + (static_cast<uint32_t>(qp * 32) << 16) + static_cast<uint32_t>(ab) * acc_stride;
+                if (p.P > 1) {
+                    float* mine = p.part + (static_cast<long long>(pc.t) * p.P + pc.idx) * tile_floats;
+                    for (int n0 = 0; n0 < N_pad && !failed; n0 += 8) {
+                        uint32_t v[8];
+                        tmem_ld8(taddr + static_cast<uint32_t>(n0), v);
+                        tmem_wait_ld();
+                        if (row_in_tile >= 0) {
+                            float4* d = reinterpret_cast<float4*>(mine + row_in_tile * N_pad + n0);
+                            d[0] = make_float4(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]),
+                                               __uint_as_float(v[3]));
+                            d[1] = make_float4(__uint_as_float(v[4]), __uint_as_float(v[5]), __uint_as_float(v[6]),
+                                               __uint_as_float(v[7]));
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0 && !failed) mbar_arrive(&acc_empty[ab]);
+                    epilogue_bar_sync();
+                    if (warp == 2 && lane == 0) {
+                        last_piece = 0;
+                        if (!failed) {
+                            const int dn = atomic_add_acq_rel(p.cnt + pc.t, 1) + 1;
+                            last_piece = dn == p.P;
+                            if (dn == p.P) p.cnt[pc.t] = 0;  // ready for the next launch
+                        }
+                    }
+                    epilogue_bar_sync();
+                    if (!last_piece) continue;
+                    const int rr = e & 63;
+                    const int rrow = pc.t * kTileM + rr;
+                    const float* src0 = p.part + static_cast<long long>(pc.t) * p.P * tile_floats + rr * N_pad;
+                    for (int blk = e >> 6; blk * 8 < N_pad; blk += 2) {
+                        const float* src = src0 + blk * 8;
+                        float f[8];
+                        for (int r0 = 0; r0 < p.P; r0 += 4) {
+                            float4 x[8];
+#pragma unroll
+                            for (int r = 0; r < 4; ++r) {
+                                if (r0 + r < p.P) {
+                                    x[2 * r] = __ldcg(reinterpret_cast<const float4*>(src + (r0 + r) * tile_floats));
+                                    x[2 * r + 1] =
+                                        __ldcg(reinterpret_cast<const float4*>(src + (r0 + r) * tile_floats + 4));
+                                }
+                            }
+#pragma unroll
+                            for (int r = 0; r < 4; ++r) {
+                                if (r0 + r == 0) {
+                                    f[0] = x[0].x; f[1] = x[0].y; f[2] = x[0].z; f[3] = x[0].w;
+                                    f[4] = x[1].x; f[5] = x[1].y; f[6] = x[1].z; f[7] = x[1].w;
+                                } else if (r0 + r < p.P) {
+                                    f[0] += x[2 * r].x; f[1] += x[2 * r].y; f[2] += x[2 * r].z; f[3] += x[2 * r].w;
+                                    f[4] += x[2 * r + 1].x; f[5] += x[2 * r + 1].y; f[6] += x[2 * r + 1].z;
+                                    f[7] += x[2 * r + 1].w;
+                                }
+                            }
+                        }
+                        float sq[8];
+                        store_c(p, f, rrow, rrow < p.M, blk * 8, fx, fr, rsc, sq, xpre_on ? xpre : nullptr, gpre);
+                        if (fx) {
+#pragma unroll
+                            for (int jj = 0; jj < 8; ++jj) {
+                                const float v = warp_sum(sq[jj]);
+                                if (lane == 0) fuse_ssw[(e >> 5) & 1][blk * 8 + jj] = v;
+                            }
+                        }
+                    }
+                    if (fx) fuse_tile_sums(p, fuse_ssw, pc.t, e, 2);
+                    continue;
+                }
+                for (int n0 = 0; n0 < N_pad; n0 += 8) {
+                    float f[8];
+                    if (!failed) {
+                        uint32_t v[8];
+                        tmem_ld8(taddr + static_cast<uint32_t>(n0), v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj) f[jj] = __uint_as_float(v[jj]);
+                    } else {
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj) f[jj] = 0.f;
+                    }
+                    float sq[8], xb[8];
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) xb[jj] = n0 == 0 ? xpre[jj] : xpre[8 + jj];
+                    store_c(p, f, row, valid && !failed, n0, fx, fr, rsc, sq, xpre_on ? xb : nullptr, gpre);
+                    if (fx) {
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj) {
+                            const float v = warp_sum(sq[jj]);
+                            if (lane == 0) fuse_ssw[qp][n0 + jj] = v;
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0 && !failed) mbar_arrive(&acc_empty[ab]);
+                if (fx) fuse_tile_sums(p, fuse_ssw, pc.t, e, 4);
+            }
+            // this CTA is done with operation j: every epilogue thread's stores are ordered
+            // before the count by the barrier, and made visible at GPU scope (and to the
+            // bulk copies that read them) before it
+            epilogue_bar_sync();
+            if (e == 0 && !failed && !*abort) {
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                __threadfence();
+                const int before = atomic_add_acq_rel(cp.done + j, 1);
+                if (j == cp.n_ops - 1 && before == cp.n_ctas - 1) {
+                    // every CTA has finished every operation: ready for the next launch
+                    for (int jj = 0; jj < cp.n_ops; ++jj) cp.done[jj] = 0;
+                    __threadfence();
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, tmem_cols);
+    }
+}
+
+// ======================================================================================
 // host side
 // ======================================================================================
 using EncodeTiledFn = PFN_cuTensorMapEncodeTiled_v12000;
@@ -1153,9 +1560,9 @@ constexpr int kMaxWideN = 4 * kMaxBlockN;  // rows of one launch: a cluster of u
 constexpr int kDefaultHostWindow = 4;
 
 // Launch with the optional cluster dimension and programmatic-dependent-launch attribute.
-template <typename Kernel>
+template <typename Kernel, typename... Args>
 static cudaError_t launch_ex(Kernel k, int grid, int threads, int smem, int cluster, bool pdl, cudaStream_t s,
-                             const GemmParams& p, const CUtensorMap& bmap) {
+                             const Args&... args) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
@@ -1179,7 +1586,7 @@ static cudaError_t launch_ex(Kernel k, int grid, int threads, int smem, int clus
     }
     cfg.attrs = attr;
     cfg.numAttrs = static_cast<unsigned>(n);
-    return cudaLaunchKernelEx(&cfg, k, p, bmap);
+    return cudaLaunchKernelEx(&cfg, k, args...);
 }
 
 // Workspace of split tile rows: fp32 partial tiles and one counter per tile row, in device
@@ -1235,6 +1642,12 @@ static bool split_workspace(float** part, int** cnt) {
 // Pieces keep at least 512 columns and the workspace must hold the partials.
 // tuning.split_k > 0 fixes P (1 = no split).
 constexpr double kCtaStreamBytesPerUs = 62.5e3;
+// bf16 tensor rate of one SM issuing M = 64 tiles, FLOP per us (fitted: the 8B gate+up at 256
+// rows, 448 tile rows in three waves on 150 SMs, took 104 us all-HBM), and the host link's
+// read rate, bytes per us (the read-stream probe: 211 GB/s)
+constexpr double kSmTensorFlopsPerUs = 3.76e6;
+constexpr double kHostLinkBytesPerUs = 2.1e5;
+constexpr double kHostCtaBytesPerUs = 1.3e4;  // one CTA's host reads (the probe: 16 CTAs fill the link)
 
 static int split_pieces(int T, int K_pad, int N_pad, int slots, long long tile_bytes, int host_cap, int pstep,
                         double piece_us, long long max_tiles, long long max_floats, const dak_tuning* t) {
@@ -1289,7 +1702,7 @@ void reset_split_counters() {
 // call), so that dak_gemm_plan can report it without a GPU.
 struct BlockPlan {
     bool umma;
-    int NC, N_pad, P, pstep, kcb, smem, grid;
+    int NC, N_pad, P, pstep, kcb, kcb_host, smem, grid;  // kcb / kcb_host: B chunk width of each role's map
     Chunks ch[2];  // [0] HBM-side CTAs, [1] host-side CTAs
     int n_host_ctas, n_hbm_ctas, host_window, hbm_window;
 };
@@ -1346,12 +1759,15 @@ static dak_status plan_block(int T, int h, int K_pad, long long tile_bytes, int 
     // Ring layouts. Shared tile rows (NC > 1): A in 256-column chunks and B through its own
     // ring of 64-column chunks, so that A copies and forwards stay large while B fills the
     // rest. One CTA per tile row: the unified ring for both tiers, except that with wide B
-    // (N_pad > 128) and 64-column chunks (only where two wider stages do not fit) CTAs
-    // reading host tiles take the split layout, whose 32 KiB A chunks keep more host bytes
-    // in flight (host reads are latency-bound).
-    const bool b_ring_all = umma && NC > 1;
-    const bool b_ring_host = umma && q.N_pad > 128 && kc == 64 && !(t && t->chunk_k > 0);
-    if (b_ring_all && !(t && t->chunk_k > 0)) kc = 256;
+    // (N_pad > 128, where two unified stages hold only 128 columns of A) CTAs reading host
+    // tiles take the split layout: 32 KiB A chunks in three or four stages keep about three
+    // times the host bytes in flight, and host reads are latency-bound (a tensor-bound
+    // linear at N = 256 ran its host tile rows 1.3x slower than its HBM ones without it).
+    // That role's B chunks are 64 columns wide, so it gets a tensor map of its own.
+    // Clusters (NC > 1): host tile rows are forwarded by rank 0 (A-only slots, split layout);
+    // HBM tile rows are streamed by every rank and take the unified ring like N_pad = 256 alone.
+    const bool b_ring_all = false;
+    const bool b_ring_host = umma && (NC > 1 || (q.N_pad > 128 && kc <= 128 && !(t && t->chunk_k > 0)));
     // (NC > 1: each CTA holds 2 x 256 TMEM columns, the whole TMEM of an SM: one CTA per SM)
     const int CL = NC;  // CTAs per cluster
     auto layout = [&](int kc_, bool split, Chunks* L) -> bool {
@@ -1381,10 +1797,14 @@ static dak_status plan_block(int T, int h, int K_pad, long long tile_bytes, int 
     if (!layout(kc, b_ring_all, &q.ch[0])) return DAK_ERR_INVALID;
     q.ch[1] = q.ch[0];
     if (!b_ring_all && b_ring_host && h > 0) {
-        if (!layout(256, true, &q.ch[1])) q.ch[1] = q.ch[0];
+        const int kch = (NC > 1 && t && t->chunk_k > 0) ? std::max(64, t->chunk_k) : 256;
+        if (!layout(kch, true, &q.ch[1])) {
+            if (NC > 1) return DAK_ERR_INVALID;  // a forwarding cluster needs A-only slots
+            q.ch[1] = q.ch[0];
+        }
     }
-    if (q.ch[0].kcb != q.ch[1].kcb) return DAK_ERR_INVALID;  // one B tensor map serves both
     q.kcb = q.ch[0].kcb;
+    q.kcb_host = q.ch[1].kcb;
     auto ring_bytes = [](const Chunks& L) { return L.stages * L.stage_bytes + L.wb * L.b_slot_bytes; };
     const int rings = std::max(ring_bytes(q.ch[0]), ring_bytes(q.ch[1]));
     q.smem = rings + (umma ? 1024 : 0);
@@ -1410,6 +1830,40 @@ static dak_status plan_block(int T, int h, int K_pad, long long tile_bytes, int 
     int hc = tc.host_ctas > 0 ? tc.host_ctas : host_cap;
     if (!(tc.host_ctas > 0) && CL == 1 && h * q.P > hc && 3 * h * q.P <= 4 * hc) {
         hc = h * q.P;  // up to a third over the cap: one wave of host units rather than two
+    }
+    // A tile row at N_pad >= 256 is tensor work: its MMAs take longer than its bytes, and
+    // every host CTA is an SM taken from the HBM side's compute. There the host CTA count is
+    // chosen by the time model of section 4.1 (factor 3: the two roles' times balanced, each
+    // in whole waves): host time = max(waves x per-unit time of a host CTA, host bytes / link
+    // rate), HBM time = waves x per-unit compute time; the count minimising the larger is
+    // taken, or the largest count within 1% of it (more host CTAs keep the link busier), at
+    // most the congestion cap. A host CTA reads at most about
+    // 13 GB/s on this GPU, so a host tile row takes longer on its CTA than an HBM one, and the
+    // flat segment of Fig. 6 ends before x = B_host T_comp / C. Memory-bound tile rows keep
+    // the fixed cap above.
+    if (q.N_pad >= 256 && h > 0 && !(t && t->host_ctas > 0)) {
+        const double unit_bytes = static_cast<double>(tile_bytes) / q.P;
+        const double t_unit = std::max(2.0 * kTileM * q.N_pad * (static_cast<double>(K_pad) / q.P) / kSmTensorFlopsPerUs,
+                                       unit_bytes / kCtaStreamBytesPerUs);
+        const double t_host_unit = std::max(t_unit, unit_bytes / kHostCtaBytesPerUs);
+        const double t_link = static_cast<double>(h) * tile_bytes / kHostLinkBytesPerUs;
+        const int slots = std::max(1, (sms * per_sm) / CL);
+        const long long hu = static_cast<long long>(h) * q.P, gu = static_cast<long long>(T - h) * q.P;
+        // one SM of a host cluster reads the link (rank 0 forwards): the cap counts reading SMs
+        const int n_max = static_cast<int>(std::min<long long>(std::min<long long>(hu, kDefaultHostCtas),
+                                                               slots - (gu > 0 ? 1 : 0)));
+        auto model = [&](int n) {  // n counts cluster units, as schedule() does
+            const double th = std::max(static_cast<double>((hu + n - 1) / n) * t_host_unit, t_link);
+            const int m = slots - n;
+            const double tg = gu > 0 ? static_cast<double>((gu + m - 1) / m) * t_unit : 0.0;
+            return std::max(th, tg);
+        };
+        double best = 1e300;
+        for (int n = 1; n <= n_max; ++n) best = std::min(best, model(n));
+        int best_n = 1;
+        for (int n = 1; n <= n_max; ++n)
+            if (model(n) <= 1.01 * best) best_n = n;
+        hc = best_n * CL;
     }
     tc.host_ctas = std::max(1, hc / CL);
     if (tc.hbm_ctas > 0) tc.hbm_ctas = std::max(1, tc.hbm_ctas / CL);
@@ -1496,17 +1950,25 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
         }
     }
 
-    alignas(64) CUtensorMap bmap;
-    int b3d = 0;
+    alignas(64) CUtensorMap bmap, bmap_host;
+    int b3d = 0, b3d_host = 0;
     if (!make_b_map(&bmap, B, p.K, N, p.N_pad, bp.kcb, bp.umma ? kUmmaB : kCoreB, &b3d)) return DAK_ERR_CUDA;
+    if (bp.kcb_host != bp.kcb) {
+        if (!make_b_map(&bmap_host, B, p.K, N, p.N_pad, bp.kcb_host, kUmmaB, &b3d_host)) return DAK_ERR_CUDA;
+        if (b3d_host != b3d) return DAK_ERR_CUDA;  // both maps take 64-column blocks: the same box form
+    } else {
+        bmap_host = bmap;
+    }
     p.b3d = b3d;
 
     const bool pdl = t && t->pdl > 0;
     const bool fused = p.res_x || p.ss_in;
     cudaError_t e;
     if (bp.umma) {
-        e = fused ? launch_ex(gemm_umma_kernel<true>, bp.grid, kUmmaThreads, bp.smem, bp.NC, pdl, stream, p, bmap)
-                  : launch_ex(gemm_umma_kernel<false>, bp.grid, kUmmaThreads, bp.smem, bp.NC, pdl, stream, p, bmap);
+        e = fused ? launch_ex(gemm_umma_kernel<true>, bp.grid, kUmmaThreads, bp.smem, bp.NC, pdl, stream, p, bmap,
+                              bmap_host)
+                  : launch_ex(gemm_umma_kernel<false>, bp.grid, kUmmaThreads, bp.smem, bp.NC, pdl, stream, p, bmap,
+                              bmap_host);
     } else {
         e = fused ? launch_ex(gemm_core_kernel<1, true>, bp.grid, kCoreThreads, bp.smem, 1, pdl, stream, p, bmap)
                   : launch_ex(gemm_core_kernel<1, false>, bp.grid, kCoreThreads, bp.smem, 1, pdl, stream, p, bmap);
@@ -1538,6 +2000,147 @@ dak_status launch_gemm(const dak_placement* A, const void* host_src, const void*
         if (r != DAK_OK) return r;
     }
     return DAK_OK;
+}
+
+
+// ---------------------------------------------------------------------------------- chains
+// Workspace of a chain: the operations' done counters (256 bytes), then each operation's
+// per-tile-row piece counters (256-byte aligned), then each operation's partial tiles.
+constexpr long long kChainDoneBytes = 256;
+
+static long long align256(long long v) { return (v + 255) & ~255ll; }
+
+// Plans of the chain's operations (each as a launch of its own would plan it) and the
+// workspace they need; DAK_ERR_UNSUPPORTED for a chain the kernel does not take.
+static dak_status plan_chain(const ChainOp* ops, int n, int N, int sms, const dak_tuning* t, BlockPlan* bps,
+                             long long* cnt_off, long long* part_off, long long* need) {
+    if (n < 1 || n > kMaxChainOps) return DAK_ERR_INVALID;
+    if (N < 2 || N > kFuseMaxN) return DAK_ERR_UNSUPPORTED;  // tensor cores, one CTA per tile row
+    long long off = kChainDoneBytes;
+    for (int j = 0; j < n; ++j) {
+        const dak_placement* A = ops[j].A;
+        if (!A || A->kind != 0 || A->T == 0) return DAK_ERR_INVALID;
+        const dak_status r = plan_block(A->T, A->h, static_cast<int>(A->K_pad), A->tile_bytes, N, sms, t, false, 0,
+                                        &bps[j]);
+        if (r != DAK_OK) return r;
+        const BlockPlan& b = bps[j];
+        if (!b.umma || b.NC != 1 || b.kcb != b.ch[0].kc || b.ch[0].kc != b.ch[1].kc ||
+            b.ch[0].stages != b.ch[1].stages || b.ch[0].stage_bytes != b.ch[1].stage_bytes)
+            return DAK_ERR_UNSUPPORTED;
+        if (b.ch[0].kc != bps[0].ch[0].kc || b.ch[0].stages != bps[0].ch[0].stages || b.N_pad != bps[0].N_pad)
+            return DAK_ERR_UNSUPPORTED;
+        cnt_off[j] = off;
+        off = align256(off + static_cast<long long>(A->T) * 4);
+    }
+    for (int j = 0; j < n; ++j) {
+        part_off[j] = off;
+        if (bps[j].P > 1) off = align256(off + static_cast<long long>(ops[j].A->T) * bps[j].P * kTileM * bps[j].N_pad * 4);
+    }
+    *need = off;
+    return DAK_OK;
+}
+
+size_t gemm_chain_workspace_bytes(const ChainOp* ops, int n, int N, const dak_tuning* t) {
+    BlockPlan bps[kMaxChainOps];
+    long long co[kMaxChainOps], po[kMaxChainOps], need = 0;
+    if (plan_chain(ops, n, N, device_sm_count(), t, bps, co, po, &need) != DAK_OK) return 0;
+    return static_cast<size_t>(need);
+}
+
+dak_status launch_gemm_chain(const ChainOp* ops, int n, int N, const dak_tuning* t, void* ws, size_t ws_bytes,
+                             cudaStream_t stream) {
+    if (!ops || n < 1 || n > kMaxChainOps) return DAK_ERR_INVALID;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DAK_ERR_CUDA;
+    BlockPlan bps[kMaxChainOps];
+    long long cnt_off[kMaxChainOps], part_off[kMaxChainOps], need = 0;
+    const dak_status r = plan_chain(ops, n, N, device_sm_count(), t, bps, cnt_off, part_off, &need);
+    if (r != DAK_OK) return r;
+    if (!ws || static_cast<long long>(ws_bytes) < need) return DAK_ERR_INVALID;
+    if (reinterpret_cast<uintptr_t>(ws) & 255) return DAK_ERR_ALIGN;
+
+    ChainParams cp{};
+    alignas(64) ChainMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    cp.n_ops = n;
+    cp.st = status_ptr();
+    if (!cp.st) return DAK_ERR_CUDA;
+    cp.done = static_cast<int*>(ws);
+    int grid = 0, smem = 0;
+    bool fused = false;
+    for (int j = 0; j < n; ++j) {
+        const ChainOp& o = ops[j];
+        const dak_placement* A = o.A;
+        const BlockPlan& bp = bps[j];
+        if (A->device != dev) return DAK_ERR_INVALID;
+        if (!o.B || !o.C) return DAK_ERR_INVALID;
+        if ((reinterpret_cast<uintptr_t>(o.B) & 15) || (reinterpret_cast<uintptr_t>(o.C) & 15)) return DAK_ERR_ALIGN;
+        if (A->h > 0 && !o.host_src) return DAK_ERR_INVALID;
+        GemmParams& p = cp.op[j];
+        p.a_host = static_cast<const uint8_t*>(o.host_src);
+        p.a_hbm = static_cast<const uint8_t*>(A->hbm_ptr);
+        p.B = static_cast<const __nv_bfloat16*>(o.B);
+        p.C = o.C;
+        p.M = static_cast<int>(A->M);
+        p.K = static_cast<int>(A->K);
+        p.K_pad = static_cast<int>(A->K_pad);
+        p.N = N;
+        p.NC = 1;
+        p.N_pad = bp.N_pad;
+        p.T = A->T;
+        p.h = A->h;
+        p.c_fp32 = o.c_fp32 ? 1 : 0;
+        p.tile_bytes = A->tile_bytes;
+        p.glu = A->glu;
+        p.P = bp.P;
+        p.pstep = bp.pstep;
+        p.ch[0] = bp.ch[0];
+        p.ch[1] = bp.ch[1];
+        p.n_host_ctas = bp.n_host_ctas;
+        p.n_hbm_ctas = bp.n_hbm_ctas;
+        p.host_window = p.hbm_window = bp.ch[0].stages;  // one ring for every operation
+        p.st = cp.st;
+        p.cnt = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + cnt_off[j]);
+        p.part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + part_off[j]);
+        const GemmFuse& f = o.fuse;
+        if (f.res_x) {
+            if (p.glu || o.c_fp32 || !f.res_g || !f.ss_out) return DAK_ERR_INVALID;
+            p.res_x = f.res_x;
+            p.res_g = static_cast<const __nv_bfloat16*>(f.res_g);
+            p.ss_out = f.ss_out;
+            fused = true;
+        }
+        if (f.ss_in) {
+            if (f.ss_tiles < 1) return DAK_ERR_INVALID;
+            p.ss_in = f.ss_in;
+            p.ss_tiles = f.ss_tiles;
+            p.ss_inv_d = f.inv_d;
+            p.ss_eps = f.eps;
+            fused = true;
+        }
+        cp.after_prev[j] = (j > 0 && o.after_prev) ? 1 : 0;
+        int b3d = 0;
+        if (!make_b_map(&maps.m[j], o.B, p.K, N, p.N_pad, bp.kcb, kUmmaB, &b3d)) return DAK_ERR_CUDA;
+        p.b3d = b3d;
+        grid = std::max(grid, bp.grid);
+        smem = std::max(smem, bp.smem);
+    }
+    cp.n_ctas = grid;
+    if (grid == 0) return DAK_OK;
+    auto k = fused ? gemm_chain_kernel<true> : gemm_chain_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return cuda_status(e);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(kUmmaThreads));
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = (t && t->pdl > 0) ? 1 : 0;
+    return cuda_status(cudaLaunchKernelEx(&cfg, k, cp, maps));
 }
 
 }  // namespace dak
@@ -1596,4 +2199,27 @@ extern "C" dak_status dak_gemm_staged(const dak_placement* A, const void* stagin
     if (!A || (A->h > 0 && !staging)) return DAK_ERR_INVALID;
     if (reinterpret_cast<uintptr_t>(staging) & 15) return DAK_ERR_ALIGN;
     return dak::launch_gemm(A, staging, B, C, N, c_fp32, tuning, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t dak_gemm_chain_workspace_bytes(const dak_gemm_op* ops, int n_ops, int N, const dak_tuning* tuning) {
+    if (!ops || n_ops < 1 || n_ops > dak::kMaxChainOps) return 0;
+    dak::ChainOp co[dak::kMaxChainOps];
+    for (int j = 0; j < n_ops; ++j) co[j].A = ops[j].A;
+    return dak::gemm_chain_workspace_bytes(co, n_ops, N, tuning);
+}
+
+extern "C" dak_status dak_gemm_chain(const dak_gemm_op* ops, int n_ops, int N, const dak_tuning* tuning,
+                                     void* workspace, size_t ws_bytes, void* stream) {
+    if (!ops || n_ops < 1 || n_ops > dak::kMaxChainOps) return DAK_ERR_INVALID;
+    dak::ChainOp co[dak::kMaxChainOps];
+    for (int j = 0; j < n_ops; ++j) {
+        if (!ops[j].A) return DAK_ERR_INVALID;
+        co[j].A = ops[j].A;
+        co[j].host_src = ops[j].A->host_dev;
+        co[j].B = ops[j].B;
+        co[j].C = ops[j].C;
+        co[j].c_fp32 = ops[j].c_fp32;
+        co[j].after_prev = ops[j].after_prev;
+    }
+    return dak::launch_gemm_chain(co, n_ops, N, tuning, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
 }

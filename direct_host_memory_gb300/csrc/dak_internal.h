@@ -91,6 +91,26 @@ struct GemmFuse {
     float inv_d = 0.f, eps = 0.f;
 };
 
+// One operation of a chain of GEMMs run by one persistent launch (launch_gemm_chain):
+// host_src is the host tier's device-visible address (or a prefetch staging copy);
+// after_prev: B (and the fused inputs) come from earlier operations of the chain, so the
+// operation's loads of B and its epilogue wait until every CTA has finished the previous one.
+constexpr int kMaxChainOps = 8;
+struct ChainOp {
+    const dak_placement* A = nullptr;
+    const void* host_src = nullptr;
+    const void* B = nullptr;
+    void* C = nullptr;
+    int c_fp32 = 0;
+    int after_prev = 0;
+    GemmFuse fuse;
+};
+// ws: the chain's workspace (256-byte aligned, gemm_chain_workspace_bytes of it, zeroed before
+// its first use; every completed launch leaves its counters at zero again).
+dak_status launch_gemm_chain(const ChainOp* ops, int n, int N, const dak_tuning* t, void* ws, size_t ws_bytes,
+                             cudaStream_t s);
+size_t gemm_chain_workspace_bytes(const ChainOp* ops, int n, int N, const dak_tuning* t);
+
 dak_status launch_gemm(const dak_placement* A, const void* host_src, const void* B, void* C, int N, int c_fp32,
                        const dak_tuning* t, cudaStream_t s, void* ws = nullptr, size_t ws_bytes = 0,
                        const GemmFuse* fuse = nullptr);

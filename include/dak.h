@@ -213,6 +213,44 @@ typedef struct {
 dak_status dak_gemm_plan(int64_t M, int64_t K, int n_host_tiles, int N, int sm_count, const dak_tuning* tuning,
                          size_t ws_bytes, dak_gemm_plan_info* out);
 
+/* A chain of GEMMs C_j = A_j x B_j in one persistent launch, for 2 <= N <= 128 hidden-state
+ * rows (tensor-core path). The paper launches one kernel per nn.Linear (section 5); here the
+ * operations of a chain share one launch, so that each CTA's weight stream runs on from one
+ * operation to the next instead of draining and ramping up at every launch boundary (the
+ * weights never depend on an earlier operation, so a CTA streams the next operation's tiles
+ * while the previous one finishes).
+ *   ops[j].A, .B, .C, .c_fp32: as dak_gemm (B bf16 [N][K_j], C [N][M_j]; a placement made by
+ *       dak_place_matrix_glu gives silu(gate) * up).
+ *   ops[j].after_prev: 1 = operation j reads what earlier operations of the chain wrote (its B
+ *       is an earlier C, or its C overwrites an earlier operation's B): its loads of B and its
+ *       writes of C wait until every CTA of the launch has finished operations 0 .. j-1. 0 =
+ *       independent of them (a grouped launch). ops[0].after_prev is ignored: the first
+ *       operation is ordered after the previous work of the stream like any launch (with
+ *       tuning->pdl, as dak_gemm with pdl).
+ * Each operation is tiered, dealt to CTAs and (when its tile rows do not spread evenly) cut
+ * into pieces exactly as its own dak_gemm launch would be, so results are bit-identical to
+ * dak_gemm's with the same tuning, at every offload ratio. n_ops 1..8, one N for all.
+ * Workspace: device memory of dak_gemm_chain_workspace_bytes(ops, n_ops, N, tuning) bytes,
+ * 256-byte aligned, zeroed once before its first use: per-operation completion counters,
+ * piece counters and partial tiles. Every completed launch leaves its counters at zero; after
+ * dak_last_error reported an error, zero the workspace again. Launches with one workspace must
+ * not overlap. The operations' completion waits are bounded (DAK_ERR_TIMEOUT through
+ * dak_last_error), and every CTA of the launch must be able to run at once (the launch uses
+ * at most one CTA per SM).
+ * DAK_ERR_UNSUPPORTED: N outside 2..128, or operations whose launches would stream with
+ * different ring layouts. DAK_ERR_INVALID: n_ops outside 1..8, null pointers, workspace
+ * smaller than needed; DAK_ERR_ALIGN as dak_gemm or an unaligned workspace. */
+typedef struct {
+    const dak_placement* A;
+    const void* B;
+    void* C;
+    int c_fp32;
+    int after_prev;
+} dak_gemm_op;
+size_t dak_gemm_chain_workspace_bytes(const dak_gemm_op* ops, int n_ops, int N, const dak_tuning* tuning);
+dak_status dak_gemm_chain(const dak_gemm_op* ops, int n_ops, int N, const dak_tuning* tuning, void* workspace,
+                          size_t ws_bytes, void* stream);
+
 /* Workspace bytes dak_attn needs for B requests, H_q query heads, head dim D and
  * n_split context splits (0 when n_split == 1). */
 size_t dak_attn_workspace_bytes(int B, int H_q, int D, int n_split);

@@ -75,7 +75,10 @@ def test_caller_workspace_bounds_pieces():
 def test_wide_b_clusters_and_launches():
     M, K = LINEARS_8B["o"]
     p = plan(M, K, 8, 512)
-    assert (p["cluster"], p["n_pad"], p["launches"], p["pieces"], p["chunk_k"]) == (2, 256, 1, 1, 256)
+    # HBM tile rows: every rank streams them in the unified ring (128-column chunks at 256
+    # rows); host tile rows: rank 0 fetches 256-column A-only chunks and forwards them
+    assert (p["cluster"], p["n_pad"], p["launches"], p["pieces"], p["chunk_k"]) == (2, 256, 1, 1, 128)
+    assert p["host_chunk_k"] == 256
     assert p["host_ctas"] % 2 == 0 and p["hbm_ctas"] % 2 == 0
     assert plan(M, K, 8, 1024)["cluster"] == 4
     assert plan(M, K, 8, 1500)["launches"] == 2

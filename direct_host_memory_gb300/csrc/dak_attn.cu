@@ -14,10 +14,13 @@
 //   S  = Q_g (16 x D, rows >= G zero) . K^T (D x 16 tokens)
 //   O += P   (16 x 16 tokens)         . V   (16 tokens x D)
 // with online softmax in fp32 (base-2 exponentials, the scale folded with log2 e). The
-// MMA takes bf16 operands, so the fp32 probabilities P enter the second product as two
-// bf16 parts, P_hi = bf16(P) and P_lo = bf16(P - P_hi), multiplied into the same fp32
-// accumulators: P_hi + P_lo equals P to about 2^-17 relative, so the product is not
-// limited by bf16 rounding of P (the denominator sums the fp32 P).
+// MMA takes bf16 operands, so the fp32 probabilities P enter the second product as bf16.
+// With a bf16 output (dak_attn) that is one bf16(P): its rounding (2^-9 relative per
+// probability, averaging out over the tokens) stays below the output's own rounding. With
+// an fp32 output (dak_attn_f32, the parity mode) P enters as two bf16 parts, P_hi = bf16(P)
+// and P_lo = bf16(P - P_hi), multiplied into the same fp32 accumulators: P_hi + P_lo equals
+// P to about 2^-17 relative (the second set of P.V MMAs costs 4% on an all-HBM launch with
+// 8 query heads per kv head). The denominator always sums the fp32 P.
 // Partial results of the splits are merged by a log-sum-exp combine in fixed order.
 //
 // KV placement layout: per tier [requests][H_kv] slabs; a slab is ceil(L/64) chunks of 64
@@ -122,7 +125,7 @@ __device__ __forceinline__ void named_bar_consumers() {
     asm volatile("bar.sync 1, %0;" ::"n"(32 * kAttnConsumers) : "memory");
 }
 
-template <int D>
+template <int D, bool SPLIT_P>
 __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnParams p) {
     constexpr int KS = D / 16;                       // k-steps of the score MMA
     constexpr int NB = D / 8;                        // 8-wide column blocks of O
@@ -281,7 +284,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnParams 
                     o[nb][2] *= corr_b;
                     o[nb][3] *= corr_b;
                 }
-                // P as the A operand (16 rows x 16 tokens), in two bf16 parts: hi = bf16(P) and
+                // P as the A operand (16 rows x 16 tokens): hi = bf16(P), and with SPLIT_P also
                 // lo = bf16(P - hi), both multiplied into the same accumulators
                 uint32_t pa0, pa1, pa2, pa3, pl0, pl1, pl2, pl3;
                 split_bf16(pr[0][0], pr[0][1], pa0, pl0);
@@ -299,8 +302,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnParams 
                         ldsm_x4_t(addr, b0, b1, b2, b3);
                         mma_bf16_16816(o[2 * db], pa0, pa1, pa2, pa3, b0, b1);
                         mma_bf16_16816(o[2 * db + 1], pa0, pa1, pa2, pa3, b2, b3);
-                        mma_bf16_16816(o[2 * db], pl0, pl1, pl2, pl3, b0, b1);
-                        mma_bf16_16816(o[2 * db + 1], pl0, pl1, pl2, pl3, b2, b3);
+                        if (SPLIT_P) {
+                            mma_bf16_16816(o[2 * db], pl0, pl1, pl2, pl3, b0, b1);
+                            mma_bf16_16816(o[2 * db + 1], pl0, pl1, pl2, pl3, b2, b3);
+                        }
                     }
                 }
             }
@@ -500,8 +505,8 @@ template <int D>
 static int attn_ctas_per_sm(int W, int G) {
     int n = 0;
     const int smem = attn_smem_bytes<D>(W, G);
-    if (cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<D>, kAttnThreads, smem) != cudaSuccess) {
+    if (cudaFuncSetAttribute(attn_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<D, false>, kAttnThreads, smem) != cudaSuccess) {
         cudaGetLastError();
         return 1;
     }
@@ -529,9 +534,10 @@ static cudaError_t launch_maybe_pdl(Kernel k, int grid, int threads, int smem, b
 template <int D>
 static cudaError_t launch_attn_d(const AttnParams& p, int grid, int W, bool pdl, cudaStream_t s) {
     const int smem = attn_smem_bytes<D>(W, p.G);
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    auto k = p.o_fp32 ? attn_kernel<D, true> : attn_kernel<D, false>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    e = launch_maybe_pdl(attn_kernel<D>, grid, kAttnThreads, smem, pdl, s, p);
+    e = launch_maybe_pdl(k, grid, kAttnThreads, smem, pdl, s, p);
     if (e != cudaSuccess || p.n_split == 1) return e;
     const int rows = p.B * p.Hq;
     if (p.n_split <= kCombineWarpMaxSplits) {

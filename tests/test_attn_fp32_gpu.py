@@ -1,7 +1,7 @@
 """SplitK_FlashAttn in its fp32-output parity mode (dak_attn_f32) against the fp64 oracle,
 through the C ABI: a tolerance of 1e-4 of max |ref| that a dropped or doubled token would
 exceed, dominant keys placed at chunk and split boundaries (o = v_j in closed form), the
-per-element error report, and the bf16 output equal to the fp32 output rounded."""
+per-element error report, and the bf16 output of dak_attn from the same inputs."""
 import numpy as np
 import pytest
 
@@ -33,8 +33,8 @@ def _run32(dak, q, k, v, h_r, seq_lens=None, n_split=0):
     assert st == 0, f"device status {st} info {info:#x}"
     p.free()
     torch.cuda.synchronize()
-    # the bf16 output is the fp32 output rounded to nearest even
-    assert np.array_equal(bits_of(O16), obf.round_f32_to_bf16(O32.cpu().numpy()))
+    # each output is checked against the oracle by the caller: the bf16 one at the method's
+    # 2e-2, the fp32 one at 1e-4
     return to_np(O32), to_np(O16)
 
 

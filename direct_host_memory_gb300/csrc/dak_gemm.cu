@@ -95,9 +95,9 @@ struct TileIter {
     int rank;  // rank in the cluster of a wide B (0 otherwise)
 };
 
-__device__ __forceinline__ TileIter tiles_of_cta(const GemmParams& p) {
+__device__ __forceinline__ TileIter tiles_of_cta(const GemmParams& p, int cta = -1) {
     TileIter it;
-    const int b = blockIdx.x / p.NC;  // cluster index
+    const int b = (cta < 0 ? static_cast<int>(blockIdx.x) : cta) / p.NC;  // cluster index
     it.c = p.ch[b < p.n_host_ctas ? 1 : 0];
     it.rank = p.NC > 1 ? static_cast<int>(cluster_ctarank()) : 0;
     if (b < p.n_host_ctas) {
@@ -1115,6 +1115,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
 struct ChainParams {
     GemmParams op[kMaxChainOps];
     int after_prev[kMaxChainOps];
+    int rot[kMaxChainOps];  // operation j deals its units to CTAs from rot[j] on (round the launch)
     int n_ops;
     int n_ctas;  // CTAs of the launch: every one counts itself in after every operation
     int* done;   // [n_ops] CTAs that finished operation j; the last CTA of the launch zeroes them
@@ -1150,13 +1151,15 @@ __device__ __forceinline__ bool wait_count(const int* addr, int target, volatile
     }
 }
 
-// One CTA's units of an operation in a chain (its tier and unit range, as tiles_of_cta);
-// none for a CTA beyond the operation's own CTAs (a chain launches as many as its widest
-// operation uses).
-__device__ __forceinline__ TileIter chain_tiles(const GemmParams& p, int W) {
-    TileIter it = tiles_of_cta(p);
+// One CTA's units of operation j of a chain: the operation's own dealing (as tiles_of_cta)
+// over the launch's CTAs counted from rot[j], so that operations with fewer CTAs than the
+// launch do not all land on the same ones; none for a CTA beyond the operation's own CTAs.
+__device__ __forceinline__ TileIter chain_tiles(const ChainParams& cp, int j, int W) {
+    const GemmParams& p = cp.op[j];
+    const int cta = (static_cast<int>(blockIdx.x) + cp.n_ctas - cp.rot[j]) % cp.n_ctas;
+    TileIter it = tiles_of_cta(p, cta);
     it.window = W;
-    if (static_cast<int>(blockIdx.x) >= p.n_host_ctas + p.n_hbm_ctas) it.count = 0;
+    if (cta >= p.n_host_ctas + p.n_hbm_ctas) it.count = 0;
     return it;
 }
 
@@ -1169,7 +1172,7 @@ __device__ __forceinline__ void chain_produce(const ChainParams& cp, const Chain
     long long i = 0;
     for (int j = 0; j < cp.n_ops && !*abort; ++j) {
         const GemmParams& p = cp.op[j];
-        const TileIter it = chain_tiles(p, W);
+        const TileIter it = chain_tiles(cp, j, W);
         if (!is_a) {
             if (j == 0) {
                 grid_dep_wait();  // the first operation's hidden states may come from the previous kernel
@@ -1261,7 +1264,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         bool ok = true;
         for (int j = 0; j < cp.n_ops && ok; ++j) {
             const GemmParams& p = cp.op[j];
-            const TileIter it = chain_tiles(p, W);
+            const TileIter it = chain_tiles(cp, j, W);
             for (int ui = 0; ui < it.count && ok; ++ui, ++uu) {
                 const int ab = uu & 1;
                 if (uu >= 2 && !mbar_wait(&acc_empty[ab], static_cast<uint32_t>(((uu >> 1) - 1) & 1), abort, p.st,
@@ -1317,7 +1320,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
             const GemmParams& p = cp.op[j];
             const bool fx = F && p.res_x != nullptr;
             const bool fr = F && p.ss_in != nullptr;
-            const TileIter it = chain_tiles(p, W);
+            const TileIter it = chain_tiles(cp, j, W);
             if (j > 0 && cp.after_prev[j]) {
                 // the previous operation's outputs (this one's B, fused inputs, or a buffer it
                 // overwrites) are complete once every CTA has counted it in
@@ -2127,6 +2130,11 @@ dak_status launch_gemm_chain(const ChainOp* ops, int n, int N, const dak_tuning*
     }
     cp.n_ctas = grid;
     if (grid == 0) return DAK_OK;
+    // each operation starts dealing where the previous one's CTAs ended
+    for (int j = 0, r = 0; j < n; ++j) {
+        cp.rot[j] = r;
+        r = (r + cp.op[j].n_host_ctas + cp.op[j].n_hbm_ctas) % grid;
+    }
     auto k = fused ? gemm_chain_kernel<true> : gemm_chain_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return cuda_status(e);

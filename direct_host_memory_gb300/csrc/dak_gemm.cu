@@ -1650,7 +1650,7 @@ constexpr double kCtaStreamBytesPerUs = 62.5e3;
 // read rate, bytes per us (the read-stream probe: 211 GB/s)
 constexpr double kSmTensorFlopsPerUs = 3.76e6;
 constexpr double kHostLinkBytesPerUs = 2.1e5;
-constexpr double kHostCtaBytesPerUs = 1.3e4;  // one CTA's host reads (the probe: 16 CTAs fill the link)
+constexpr double kHostCtaBytesPerUs = 1.3e4;  // a host CTA through tensor-bound tile rows (fitted: 512 KiB in ~40 us)
 
 static int split_pieces(int T, int K_pad, int N_pad, int slots, long long tile_bytes, int host_cap, int pstep,
                         double piece_us, long long max_tiles, long long max_floats, const dak_tuning* t) {
@@ -1840,10 +1840,10 @@ static dak_status plan_block(int T, int h, int K_pad, long long tile_bytes, int 
     // in whole waves): host time = max(waves x per-unit time of a host CTA, host bytes / link
     // rate), HBM time = waves x per-unit compute time; the count minimising the larger is
     // taken, or the largest count within 1% of it (more host CTAs keep the link busier), at
-    // most the congestion cap. A host CTA reads at most about
-    // 13 GB/s on this GPU, so a host tile row takes longer on its CTA than an HBM one, and the
-    // flat segment of Fig. 6 ends before x = B_host T_comp / C. Memory-bound tile rows keep
-    // the fixed cap above.
+    // most the congestion cap. A host CTA of such a GEMM gets through a tile row more slowly
+    // than an HBM one (about 40 us per 512 KiB against 36 us of MMAs, measured at 256 rows),
+    // so the flat segment of Fig. 6 ends before x = B_host T_comp / C. Memory-bound tile rows
+    // keep the fixed cap above.
     if (q.N_pad >= 256 && h > 0 && !(t && t->host_ctas > 0)) {
         const double unit_bytes = static_cast<double>(tile_bytes) / q.P;
         const double t_unit = std::max(2.0 * kTileM * q.N_pad * (static_cast<double>(K_pad) / q.P) / kSmTensorFlopsPerUs,

@@ -71,7 +71,8 @@ class dak_tune_result(ctypes.Structure):
 class dak_gemm_plan_info(ctypes.Structure):
     _fields_ = [(f, ctypes.c_int) for f in (
         "tensor_cores", "launches", "cluster", "n_pad", "pieces", "piece_step", "chunk_k", "host_chunk_k",
-        "hbm_stages", "host_stages", "host_ctas", "hbm_ctas", "host_window", "hbm_window", "smem_bytes")]
+        "hbm_stages", "host_stages", "host_ctas", "hbm_ctas", "host_window", "hbm_window", "smem_bytes",
+        "tile_m")]
 
 
 class dak_decoder_config(ctypes.Structure):
@@ -105,7 +106,7 @@ def _load():
         "dak_gemm_staged": (i32, [vp, vp, vp, vp, i32, i32, P(dak_tuning), vp]),
         "dak_gemm_workspace_bytes": (sz, [vp, i32]),
         "dak_gemm_ws": (i32, [vp, vp, vp, i32, i32, P(dak_tuning), vp, sz, vp]),
-        "dak_gemm_plan": (i32, [i64, i64, i32, i32, i32, P(dak_tuning), sz, P(dak_gemm_plan_info)]),
+        "dak_gemm_plan": (i32, [i64, i64, i32, i32, i32, i32, P(dak_tuning), sz, P(dak_gemm_plan_info)]),
         "dak_gemm_chain_workspace_bytes": (sz, [P(dak_gemm_op), i32, i32, P(dak_tuning)]),
         "dak_gemm_chain": (i32, [P(dak_gemm_op), i32, i32, P(dak_tuning), vp, sz, vp]),
         "dak_attn_workspace_bytes": (sz, [i32, i32, i32, i32]),
@@ -355,14 +356,14 @@ def dak_gemm_workspace_bytes(A: Placement, N: int) -> int:
 
 
 def dak_gemm_plan(M: int, K: int, n_host_tiles: int, N: int, sm_count: int = None, tuning=None,
-                  ws_bytes: int = 0) -> dict:
-    """The launch dak_gemm would make for an M x K matrix with n_host_tiles tile rows on the
-    host and N hidden-state rows (pieces, rings, CTAs of each role), from host arithmetic
-    alone; sm_count None = this process's GPU."""
+                  ws_bytes: int = 0, tile_m: int = 64) -> dict:
+    """The launch dak_gemm would make for an M x K matrix placed in tiles of tile_m rows with
+    n_host_tiles of them on the host and N hidden-state rows (pieces, rings, CTAs of each
+    role), from host arithmetic alone; sm_count None = this process's GPU."""
     if sm_count is None:
         sm_count = dak_sm_count()
     out = dak_gemm_plan_info()
-    _check(lib.dak_gemm_plan(int(M), int(K), int(n_host_tiles), int(N), int(sm_count), _tuning(tuning),
+    _check(lib.dak_gemm_plan(int(M), int(K), int(tile_m), int(n_host_tiles), int(N), int(sm_count), _tuning(tuning),
                              ctypes.c_size_t(int(ws_bytes)), ctypes.byref(out)), "dak_gemm_plan")
     return {f: int(getattr(out, f)) for f, _ in dak_gemm_plan_info._fields_}
 

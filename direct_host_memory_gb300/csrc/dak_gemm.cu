@@ -14,10 +14,14 @@
 // tier's CTAs, so that the units spread evenly over the SMs; the CTA that finishes a tile
 // row's last piece adds the fp32 partial tiles in piece order.
 //
-// Placement layout of a tile row (both tiers): 64 rows x K_pad columns stored k-group
-// major, [K_pad/8][64 rows][8 columns] bf16: every 8 x 8 block (8 rows x 16 bytes) is
-// contiguous, every chunk of kc columns is one contiguous range, and that range is
-// already the no-swizzle K-major operand layout the tcgen05 tensor cores read.
+// Placement layout (both tiers): the tier's tile rows in blocks of two, tier-local tile
+// rows 2b and 2b + 1 stored together k-group major, [K_pad/8][128 rows][8 columns] bf16,
+// 2b tile rows into the tier; with an odd count the last tile row is a block of its own,
+// [K_pad/8][64][8]. Every 8 x 8 block (8 rows x 16 bytes) is contiguous, every chunk of kc
+// columns of a block is one contiguous range, and that range is already the no-swizzle
+// K-major operand layout the tcgen05 tensor cores read: a block of two is one M = 128
+// operand, so one MMA covers 128 rows (twice the rows per instruction and per byte of B of
+// an M = 64 tile row).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -38,6 +42,7 @@ struct Chunks {
     int kc, kcb;
     int stages, stage_bytes;       // A ring (stage = A chunk [+ B chunk when kcb == kc])
     int wb, b_ring_off, b_slot_bytes;
+    int a_cb;                      // bytes of A per column in a stage: 128 (one tile row) or 256 (two)
 };
 
 struct GemmParams {
@@ -46,6 +51,8 @@ struct GemmParams {
     const __nv_bfloat16* B; // [N][K]
     void* C;                // [N][M]
     int M, K, K_pad, N, N_pad, T, h;
+    int pairs;    // 1: the HBM tier's units are blocks of two tile rows (M = 128 MMAs, A through a tensor map)
+    int hb, gb;   // blocks of the host tier and of the HBM tier (tile rows, or pairs of them)
     int n_host_ctas, n_hbm_ctas, host_window, hbm_window;  // host/HBM counts are in clusters of NC CTAs
     int c_fp32;
     long long tile_bytes;
@@ -53,8 +60,8 @@ struct GemmParams {
     int b3d;      // B arrives in one 3-D tensor copy per stage (else several 2-D copies)
     int P;        // pieces per tile row: its K range is cut into P parts, each a unit of work
     int pstep;    // piece boundaries fall on multiples of this many columns (a B block: 64, 256)
-    float* part;  // P > 1: fp32 partial tiles [T][P][64 rows][N_pad]
-    int* cnt;     // P > 1: per tile row, pieces finished so far (back to 0 after the last)
+    float* part;  // P > 1: fp32 partials, per block [P][64 or 128 rows][N_pad] (host blocks first)
+    int* cnt;     // P > 1: per block, pieces finished so far (back to 0 after the last)
     int NC;       // CTAs per cluster sharing each tile row across 256-row blocks of B (1 = off)
     int glu;      // rows interleaved gate/up: C[n][row/2] = silu(gate) * up, C is [N][M/2]
     // Ring layout per role: ch[0] for CTAs reading HBM tiles, ch[1] for CTAs reading host
@@ -82,9 +89,13 @@ constexpr int kFusePreloadN = 16;  // up to this many rows, the producer preload
 // SwiGLU of one gate / up pair (the same expression as the decoder's standalone kernel)
 __device__ __forceinline__ float swiglu_pair(float g, float u) { return g / (1.f + expf(-g)) * u; }
 
-// Units of work of this CTA. A role's units are its tile rows times P pieces (unit u is piece
-// u % P of the role's tile row u / P); the CTA takes units first, first + stride, ... (count
-// of them), so that the pieces of one tile row go to different CTAs.
+// Blocks of a tier of n tile rows: one tile row each, or (pairs) n / 2 blocks of two and one of
+// one when n is odd.
+__host__ __device__ __forceinline__ int blocks_of(int n, int pairs) { return pairs ? (n + 1) / 2 : n; }
+
+// Units of work of this CTA. A role's units are its blocks times P pieces (unit u is piece
+// u % P of the role's block u / P); the CTA takes units first, first + stride, ... (count
+// of them), so that the pieces of one block go to different CTAs.
 struct TileIter {
     Chunks c;  // this CTA's ring layout
     bool host;
@@ -101,7 +112,7 @@ __device__ __forceinline__ TileIter tiles_of_cta(const GemmParams& p, int cta = 
     it.c = p.ch[b < p.n_host_ctas ? 1 : 0];
     it.rank = p.NC > 1 ? static_cast<int>(cluster_ctarank()) : 0;
     if (b < p.n_host_ctas) {
-        const int units = p.h * p.P;
+        const int units = p.hb * p.P;
         it.host = true;
         it.tile0 = 0;
         it.first = b;
@@ -111,7 +122,7 @@ __device__ __forceinline__ TileIter tiles_of_cta(const GemmParams& p, int cta = 
         it.window = p.host_window;
     } else {
         const int j = b - p.n_host_ctas;
-        const int units = (p.T - p.h) * p.P;
+        const int units = p.gb * p.P;
         it.host = false;
         it.tile0 = p.h;
         it.first = j;
@@ -123,28 +134,49 @@ __device__ __forceinline__ TileIter tiles_of_cta(const GemmParams& p, int cta = 
     return it;
 }
 
-// The ui-th unit of a CTA: tile row t and its K range [k0, k1). A tile row's K range is cut
-// into P pieces at multiples of pstep columns (one block of the B layout, so that every chunk
-// starts on a block), from the shape only.
+// The ui-th unit of a CTA: a block (its first tile row t, whether it holds two tile rows)
+// and its K range [k0, k1). A block's K range is cut into P pieces at multiples of pstep
+// columns (one block of the B layout, so that every chunk starts on one), from the shape only.
 struct Piece {
-    int t, idx, k0, k1;
+    int t;      // first tile row of the block (global)
+    int lb;     // block index within the tier
+    int blk;    // block index over both tiers (host blocks first): the piece counter's index
+    int m128;   // a pair block (M = 128: rows 0..63 tile row t, 64..127 tile row t + 1)
+    int pair;   // m128 and tile row t + 1 holds rows of A (a 128-row tile may end past M)
+    long long prow;  // first row of the block's partials in the split workspace (x P x N_pad floats)
+    int idx, k0, k1;
 };
 
 __device__ __forceinline__ Piece piece_of(const GemmParams& p, const TileIter& it, int ui) {
     const int u = it.first + ui * it.stride;
     Piece q;
-    q.t = it.tile0 + u / p.P;
+    q.lb = u / p.P;
     q.idx = u % p.P;
+    const int n_tier = it.host ? p.h : p.T - p.h;
+    q.m128 = p.pairs;
+    q.t = it.tile0 + (q.m128 ? 2 * q.lb : q.lb);
+    q.pair = (q.m128 && 2 * q.lb + 1 < n_tier && (q.t + 1) * kTileM < p.M) ? 1 : 0;
+    q.blk = (it.host ? 0 : p.hb) + q.lb;
+    q.prow = static_cast<long long>(q.blk) * (q.m128 ? 2 * kTileM : kTileM);
     const int steps = (p.K_pad + p.pstep - 1) / p.pstep;
     q.k0 = (q.idx * steps / p.P) * p.pstep;
     q.k1 = min(((q.idx + 1) * steps / p.P) * p.pstep, p.K_pad);
     return q;
 }
 
-__device__ __forceinline__ const uint8_t* tile_src(const GemmParams& p, const TileIter& it, int t) {
-    int local = it.host ? t : t - p.h;
-    return it.base + static_cast<long long>(local) * p.tile_bytes;
+// rows of a block's partials, and where piece r's partial block starts
+__device__ __forceinline__ int block_rows(const Piece& q) { return q.m128 ? 2 * kTileM : kTileM; }
+__device__ __forceinline__ float* piece_part(const GemmParams& p, const Piece& q, int r) {
+    return p.part + (q.prow * p.P + static_cast<long long>(r) * block_rows(q)) * p.N_pad;
 }
+
+// the block's bytes in its tier ([K_pad / 8][64 or 128 rows][8])
+__device__ __forceinline__ const uint8_t* block_src(const GemmParams& p, const TileIter& it, const Piece& q) {
+    return it.base + static_cast<long long>(q.m128 ? 2 * q.lb : q.lb) * p.tile_bytes;
+}
+
+// bytes of one column of a block's A, in the placement and in a stage
+__device__ __forceinline__ int col_bytes(const Piece& q) { return q.m128 ? 256 : 128; }
 
 // error location codes (upper 32 bits of the status info)
 enum : uint32_t {
@@ -193,11 +225,12 @@ __device__ __forceinline__ uint32_t b_stage_bytes(const GemmParams& p, int kind,
     return static_cast<uint32_t>(kcb) * 2u * static_cast<uint32_t>(kind == kUmmaB ? p.N_pad : p.N);
 }
 
-// Producer loops. `is_a` streams the tile rows of A (one bulk copy per stage), otherwise the
+// Producer loops. `is_a` streams the blocks of A (one bulk copy per stage), otherwise the
 // matching chunk of B. Both wait for the slot to be released and then arm the stage's full
-// barrier with their own byte count.
-__device__ __forceinline__ void produce(const GemmParams& p, const TileIter& it, const CUtensorMap* bmap, uint8_t* smem,
-                                        uint64_t* full, uint64_t* empty, volatile int* abort, bool is_a, int kind) {
+// barrier with their own byte count. A stage holds A (kc x a_cb bytes), then B.
+__device__ __forceinline__ void produce(const GemmParams& p, const TileIter& it, const CUtensorMap* bmap,
+                                        uint8_t* smem, uint64_t* full, uint64_t* empty, volatile int* abort, bool is_a,
+                                        int kind) {
     const int W = it.window;
     const uint64_t pol_a = policy_evict_first();
     // the weights never depend on the previous kernel of the stream; the hidden states may
@@ -205,7 +238,7 @@ __device__ __forceinline__ void produce(const GemmParams& p, const TileIter& it,
     long long i = 0;
     for (int ui = 0; ui < it.count && !*abort; ++ui) {
         const Piece q = piece_of(p, it, ui);
-        const uint8_t* src = tile_src(p, it, q.t);
+        const uint8_t* src = block_src(p, it, q);
         for (int k0 = q.k0; k0 < q.k1; k0 += it.c.kc, ++i) {
             const int s = static_cast<int>(i % W);
             if (i >= W && !mbar_wait(&empty[s], static_cast<uint32_t>(((i / W) - 1) & 1), abort, p.st,
@@ -213,13 +246,16 @@ __device__ __forceinline__ void produce(const GemmParams& p, const TileIter& it,
                 goto done;
             }
             uint8_t* dst = smem + static_cast<size_t>(s) * it.c.stage_bytes;
+            const int kce = min(it.c.kc, q.k1 - k0);
             if (is_a) {
-                const uint32_t a_bytes = static_cast<uint32_t>(min(it.c.kc, q.k1 - k0)) * 128u;
+                const int cb = col_bytes(q);
+                const uint32_t a_bytes = static_cast<uint32_t>(kce * cb);
                 mbar_arrive_expect_tx(&full[s], a_bytes);
-                bulk_g2s(dst, src + static_cast<long long>(k0) * 128, a_bytes, &full[s], pol_a);
+                bulk_g2s(dst, src + static_cast<long long>(k0) * cb, a_bytes, &full[s], pol_a);
             } else {
                 mbar_arrive_expect_tx(&full[s], b_stage_bytes(p, kind, it.c.kcb));
-                issue_b(p, bmap, dst + it.c.kc * 128, k0, &full[s], kind, p.NC > 1 ? it.rank * p.N_pad : 0, it.c.kcb);
+                issue_b(p, bmap, dst + it.c.kc * it.c.a_cb, k0, &full[s], kind, p.NC > 1 ? it.rank * p.N_pad : 0,
+                        it.c.kcb);
             }
         }
     }
@@ -284,7 +320,7 @@ __device__ __forceinline__ void forward_a(const GemmParams& p, const TileIter& i
                                        DAK_ERR_TIMEOUT, W_FWD_PEER);
             if (!__all_sync(0xffffffffu, ok)) goto done;
             if (r < p.NC) {
-                const uint32_t a_bytes = static_cast<uint32_t>(min(it.c.kc, q.k1 - k0)) * 128u;
+                const uint32_t a_bytes = static_cast<uint32_t>(min(it.c.kc, q.k1 - k0) * col_bytes(q));
                 uint8_t* slot = smem + static_cast<size_t>(s) * it.c.stage_bytes;
                 bulk_s2s_cluster(mapa_shared(smem_u32(slot), static_cast<uint32_t>(r)), slot, a_bytes,
                                  mapa_shared(smem_u32(&full[s]), static_cast<uint32_t>(r)));
@@ -314,7 +350,7 @@ __device__ __forceinline__ void arm_forwarded_a(const GemmParams& p, const TileI
                     goto done;
                 mbar_arrive_remote(mapa_shared(smem_u32(&peer_empty[s]), 0));
             }
-            mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(min(it.c.kc, q.k1 - k0)) * 128u);
+            mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(min(it.c.kc, q.k1 - k0) * col_bytes(q)));
         }
     }
 done:
@@ -324,8 +360,9 @@ done:
 // ======================================================================================
 // CUDA-core path, N = 1 (a GEMV): warp-level FMA, fp32 accumulation, shuffle reduction.
 // Warps: 0 = A producer, 1 = B producer, 2..9 = consumers (consumer w owns rows 8w .. 8w+7),
-// 10 = finisher of split tile rows. With P > 1 the consumers store each piece's partial rows
-// and move on; the finisher counts the piece in (one acquire-release atomic per piece) and,
+// 10 = finisher of split tile rows (blocks of one tile row: the piece counter's index and the
+// partials' position are the tile row's). With P > 1 the consumers store each piece's partial
+// rows and move on; the finisher counts the piece in (one acquire-release atomic per piece) and,
 // for a tile row's last piece, adds the P partials in piece order and writes C, so the
 // count's round trip never stalls the FMA stream.
 // ======================================================================================
@@ -469,10 +506,10 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
         if (lane == 0) produce(p, it, &bmap, smem, full, empty, abort, warp == 0, kCoreB);
         return;
     }
-    const int tile_floats = kTileM * p.N_pad;  // one partial tile in the split workspace
     if (warp == 2 + kCoreConsumers) {
         if (p.P == 1) return;
-        // finisher: lane l sums rows l and l + 32 of a tile row whose last piece this CTA ran
+        // finisher: lane l sums rows l, l + 32 (, l + 64, l + 96 for a block of two tile rows)
+        // of a block whose last piece this CTA ran
         grid_dep_wait();  // the split workspace may still be in use by the previous kernel
         float rsc[N];
         warp_row_scales<N>(p, fr, lane, rsc);
@@ -483,41 +520,43 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
                 return;
             }
             const Piece pc = piece_of(p, it, ui);
-            float xp[2][N], gp[2];
-            preload_residual<N>(p, fx, pc.t * kTileM + lane, xp[0], gp[0]);
-            preload_residual<N>(p, fx, pc.t * kTileM + lane + 32, xp[1], gp[1]);
+            const int nr = pc.pair ? 4 : 2;  // 32-row groups of the block
+            float xp[4][N], gp[4];
+            for (int g = 0; g < nr; ++g) preload_residual<N>(p, fx, pc.t * kTileM + lane + 32 * g, xp[g], gp[g]);
             int last = 0;
             if (lane == 0) {
                 __threadfence();
-                last = atomic_add_acq_rel(p.cnt + pc.t, 1) + 1 == p.P;
-                if (last) p.cnt[pc.t] = 0;  // ready for the next launch
+                last = atomic_add_acq_rel(p.cnt + pc.blk, 1) + 1 == p.P;
+                if (last) p.cnt[pc.blk] = 0;  // ready for the next launch
             }
             last = __shfl_sync(0xffffffffu, last, 0);
             __syncwarp();
             if (last) {
-                const float* src = p.part + static_cast<long long>(pc.t) * p.P * tile_floats;
-                float ssl[N];
+                const float* src = piece_part(p, pc, 0);
+                const long long blk_floats = static_cast<long long>(block_rows(pc)) * p.N_pad;
+                float ssl[2][N];
 #pragma unroll
-                for (int n = 0; n < N; ++n) ssl[n] = 0.f;
-                for (int h = 0; h < 2; ++h) {
-                    const int rr = lane + 32 * h;
+                for (int n = 0; n < N; ++n) ssl[0][n] = ssl[1][n] = 0.f;
+                for (int g = 0; g < nr; ++g) {
+                    const int rr = lane + 32 * g;
                     float acc[N], sq[N];
 #pragma unroll
                     for (int n = 0; n < N; ++n) {
                         float v = __ldcg(src + rr * p.N_pad + n);
-                        for (int r = 1; r < p.P; ++r) v += __ldcg(src + static_cast<long long>(r) * tile_floats + rr * p.N_pad + n);
+                        for (int r = 1; r < p.P; ++r) v += __ldcg(src + r * blk_floats + rr * p.N_pad + n);
                         acc[n] = v;
                     }
-                    store_row<N>(p, acc, pc.t * kTileM + rr, true, fx, fr, rsc, sq, h ? xp[1] : xp[0],
-                                 h ? gp[1] : gp[0]);
+                    store_row<N>(p, acc, pc.t * kTileM + rr, true, fx, fr, rsc, sq, xp[g], gp[g]);
 #pragma unroll
-                    for (int n = 0; n < N; ++n) ssl[n] += sq[n];
+                    for (int n = 0; n < N; ++n) ssl[g >> 1][n] += sq[n];
                 }
                 if (fx) {
+                    for (int h = 0; h < (pc.pair ? 2 : 1); ++h) {
 #pragma unroll
-                    for (int n = 0; n < N; ++n) {
-                        const float tot = warp_sum(ssl[n]);
-                        if (lane == 0) p.ss_out[static_cast<long long>(pc.t) * p.N + n] = tot;
+                        for (int n = 0; n < N; ++n) {
+                            const float tot = warp_sum(ssl[h][n]);
+                            if (lane == 0) p.ss_out[static_cast<long long>(pc.t + h) * p.N + n] = tot;
+                        }
                     }
                 }
             }
@@ -531,7 +570,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
     grid_dep_wait();
     float rsc[N];
     warp_row_scales<N>(p, fr, lane, rsc);
-    const int w = warp - 2;       // row group 0..7
+    const int w = warp - 2;       // row group 0..7 (of each tile row of the block)
     const int r = lane & 7;       // row within the group
     const int kq = lane >> 3;     // k-group phase 0..3
     long long i = 0;
@@ -541,10 +580,14 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
     for (int ui = 0; ui < it.count; ++ui) {
         const Piece q = piece_of(p, it, ui);
         const int t = q.t;
-        float acc[N], xp[N], gp = 0.f;
-        if (p.P == 1) preload_residual<N>(p, fx, t * kTileM + w * 8 + r, xp, gp);
+        const int halves = q.pair ? 2 : 1;          // tile rows of the block that hold rows of A
+        const int kg_bytes = q.m128 ? 2048 : 1024;  // one k-group of the block in the stage
+        float acc[2][N], xp[2][N], gp[2] = {0.f, 0.f};
+        if (p.P == 1) {
+            for (int h = 0; h < halves; ++h) preload_residual<N>(p, fx, (t + h) * kTileM + w * 8 + r, xp[h], gp[h]);
+        }
 #pragma unroll
-        for (int n = 0; n < N; ++n) acc[n] = 0.f;
+        for (int n = 0; n < N; ++n) acc[0][n] = acc[1][n] = 0.f;
         for (int k0 = q.k0; k0 < q.k1 && !failed; k0 += it.c.kc, ++i) {
             const int s = static_cast<int>(i % W);
             if (!mbar_wait(&full[s], static_cast<uint32_t>((i / W) & 1), abort, p.st, DAK_ERR_TIMEOUT, W_CONS_FULL)) {
@@ -554,26 +597,28 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
             }
             const int kgr = min(min(it.c.kc, q.k1 - k0), p.K - k0) >> 3;  // real k-groups in this chunk
             const uint8_t* st = smem + static_cast<size_t>(s) * it.c.stage_bytes;
-            const uint8_t* bst = st + it.c.kc * 128;
+            const uint8_t* bst = st + it.c.kc * it.c.a_cb;
             for (int kg = kq; kg < kgr; kg += 4) {
-                const uint4 a = *reinterpret_cast<const uint4*>(st + kg * 1024 + w * 128 + r * 16);
-                const float a0 = bf_lo(a.x), a1 = bf_hi(a.x), a2 = bf_lo(a.y), a3 = bf_hi(a.y);
-                const float a4 = bf_lo(a.z), a5 = bf_hi(a.z), a6 = bf_lo(a.w), a7 = bf_hi(a.w);
                 // B block of 256 columns holding this k-group: [N rows][512 bytes]
                 const uint8_t* bb = bst + (kg >> 5) * (N * 512) + (kg & 31) * 16;
+                for (int h = 0; h < halves; ++h) {
+                    const uint4 a = *reinterpret_cast<const uint4*>(st + kg * kg_bytes + h * 1024 + w * 128 + r * 16);
+                    const float a0 = bf_lo(a.x), a1 = bf_hi(a.x), a2 = bf_lo(a.y), a3 = bf_hi(a.y);
+                    const float a4 = bf_lo(a.z), a5 = bf_hi(a.z), a6 = bf_lo(a.w), a7 = bf_hi(a.w);
 #pragma unroll
-                for (int n = 0; n < N; ++n) {
-                    const uint4 b = *reinterpret_cast<const uint4*>(bb + n * 512);
-                    float v = acc[n];
-                    v = fmaf(a0, bf_lo(b.x), v);
-                    v = fmaf(a1, bf_hi(b.x), v);
-                    v = fmaf(a2, bf_lo(b.y), v);
-                    v = fmaf(a3, bf_hi(b.y), v);
-                    v = fmaf(a4, bf_lo(b.z), v);
-                    v = fmaf(a5, bf_hi(b.z), v);
-                    v = fmaf(a6, bf_lo(b.w), v);
-                    v = fmaf(a7, bf_hi(b.w), v);
-                    acc[n] = v;
+                    for (int n = 0; n < N; ++n) {
+                        const uint4 b = *reinterpret_cast<const uint4*>(bb + n * 512);
+                        float v = acc[h][n];
+                        v = fmaf(a0, bf_lo(b.x), v);
+                        v = fmaf(a1, bf_hi(b.x), v);
+                        v = fmaf(a2, bf_lo(b.y), v);
+                        v = fmaf(a3, bf_hi(b.y), v);
+                        v = fmaf(a4, bf_lo(b.z), v);
+                        v = fmaf(a5, bf_hi(b.z), v);
+                        v = fmaf(a6, bf_lo(b.w), v);
+                        v = fmaf(a7, bf_hi(b.w), v);
+                        acc[h][n] = v;
+                    }
                 }
             }
             __syncwarp();
@@ -581,39 +626,45 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
         }
         // reduce the four k phases: lanes r, r+8, r+16, r+24 hold the same row
 #pragma unroll
-        for (int n = 0; n < N; ++n) {
-            float v = acc[n];
-            v += __shfl_xor_sync(0xffffffffu, v, 8);
-            v += __shfl_xor_sync(0xffffffffu, v, 16);
-            acc[n] = v;
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int n = 0; n < N; ++n) {
+                float v = acc[h][n];
+                v += __shfl_xor_sync(0xffffffffu, v, 8);
+                v += __shfl_xor_sync(0xffffffffu, v, 16);
+                acc[h][n] = v;
+            }
         }
-        const int row = t * kTileM + w * 8 + r;
         if (p.P == 1) {
-            float sq[N];
-            store_row<N>(p, acc, row, kq == 0 && !failed, fx, fr, rsc, sq, xp, gp);
-            if (fx) {
-                // the tile row's sums of x^2: each warp's 8 rows, then the 8 warps in order
+            for (int h = 0; h < halves; ++h) {
+                float sq[N];
+                store_row<N>(p, acc[h], (t + h) * kTileM + w * 8 + r, kq == 0 && !failed, fx, fr, rsc, sq, xp[h], gp[h]);
+                if (fx) {
+                    // the tile row's sums of x^2: each warp's 8 rows, then the 8 warps in order
 #pragma unroll
-                for (int n = 0; n < N; ++n) {
-                    const float v = warp_sum(sq[n]);
-                    if (lane == 0) ssw[w][n] = v;
-                }
-                consumer_bar_sync();
-                if (w == 0 && lane < N) {
-                    float tot = 0.f;
+                    for (int n = 0; n < N; ++n) {
+                        const float v = warp_sum(sq[n]);
+                        if (lane == 0) ssw[w][n] = v;
+                    }
+                    consumer_bar_sync();
+                    if (w == 0 && lane < N) {
+                        float tot = 0.f;
 #pragma unroll
-                    for (int ww = 0; ww < kCoreConsumers; ++ww) tot += ssw[ww][lane];
-                    p.ss_out[static_cast<long long>(t) * p.N + lane] = tot;
+                        for (int ww = 0; ww < kCoreConsumers; ++ww) tot += ssw[ww][lane];
+                        p.ss_out[static_cast<long long>(t + h) * p.N + lane] = tot;
+                    }
+                    consumer_bar_sync();  // ssw is rewritten by the next tile row
                 }
-                consumer_bar_sync();  // ssw is rewritten by the next tile row
             }
             continue;
         }
-        // split tile row: this unit's partial rows to the workspace, then tell the finisher
+        // split block: this unit's partial rows to the workspace, then tell the finisher
         if (kq == 0) {
-            float* mine = p.part + (static_cast<long long>(t) * p.P + q.idx) * tile_floats + (w * 8 + r) * p.N_pad;
+            for (int h = 0; h < halves; ++h) {
+                float* mine = piece_part(p, q, q.idx) + (h * kTileM + w * 8 + r) * p.N_pad;
 #pragma unroll
-            for (int n = 0; n < N; ++n) mine[n] = acc[n];
+                for (int n = 0; n < N; ++n) mine[n] = acc[h][n];
+            }
         }
         __syncwarp();
         const int j = ui % kCoreDone;
@@ -626,25 +677,29 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
 }
 
 // ======================================================================================
-// Tensor-core path, N >= 2: tcgen05.mma (M = 64 rows of A, N = N_pad <= 256 hidden-state
-// columns, K = 16 per instruction), fp32 accumulators in TMEM, double-buffered (one per
-// unit of work, so the epilogue of one unit overlaps the MMAs of the next).
-// Warps: 0 = A producer (bulk copies), 1 = TMEM allocator + MMA issuer,
+// Tensor-core path, N >= 2: tcgen05.mma (M = 64 rows of A for a single-row block, 128 for a
+// pair block; N = N_pad <= 256 hidden-state columns; K = 16 per instruction), fp32
+// accumulators in TMEM, double-buffered (one per unit of work, so the epilogue of one unit
+// overlaps the MMAs of the next). Pair blocks (launches with `pairs`, HBM tier only) give
+// one MMA the work of two: at N_pad >= 128 a tile row is tensor-bound, and an M = 128
+// instruction takes about as long as an M = 64 one there.
+// Warps: 0 = A producer (bulk copies; tensor-map copies for pair blocks), 1 = TMEM allocator + MMA issuer,
 //        2..5 = epilogue (TMEM -> registers -> C, or -> partial tile and the piece count),
 //        6 = B producer (tensor-map copies), 7 = A forwarder of a wide-B cluster (NC > 1).
 // ======================================================================================
 constexpr int kUmmaThreads = 8 * 32;
 
-// The n MMAs (K = 16 each) of one sub-chunk. Step m reads A 2048 bytes (two k-groups of the
-// no-swizzle layout) further on and B 32 bytes further inside a 64-column block, with one
-// block (bblk16 descriptor units) per 64 columns. The first step of a piece starts the
+// The n MMAs (K = 16 each) of one sub-chunk. Step m reads A two k-groups of the no-swizzle
+// layout further on (a_step16 descriptor units: 2048 bytes for a 64-row operand, 4096 for a
+// 128-row one) and B 32 bytes further inside a 64-column block, with one block (bblk16
+// descriptor units) per 64 columns. The first step of a piece starts the
 // accumulator; the rest go out four per asm block with 32-bit adds on the descriptors' low
 // words (the start-address field, which never carries into the high word here).
 __device__ __forceinline__ void issue_mmas(uint32_t d_tmem, uint64_t ad0, uint64_t bd0, uint32_t bblk16, int n,
-                                           uint32_t idesc, bool accumulate) {
+                                           uint32_t idesc, bool accumulate, uint32_t a_step16) {
     const uint32_t a_lo = static_cast<uint32_t>(ad0), a_hi = static_cast<uint32_t>(ad0 >> 32);
     const uint32_t b_lo = static_cast<uint32_t>(bd0), b_hi = static_cast<uint32_t>(bd0 >> 32);
-    auto a_at = [&](int m) { return a_lo + static_cast<uint32_t>(m) * 128u; };
+    auto a_at = [&](int m) { return a_lo + static_cast<uint32_t>(m) * a_step16; };
     auto b_at = [&](int m) { return b_lo + static_cast<uint32_t>(m >> 2) * bblk16 + static_cast<uint32_t>(m & 3) * 2u; };
     int m = 0;
     if (!accumulate && n > 0) {
@@ -738,16 +793,194 @@ __device__ __forceinline__ void epilogue_bar_sync() { asm volatile("bar.sync 1, 
 __device__ __forceinline__ int umma_m64_row_of_lane(int q, int lane) { return lane < 16 ? q * 16 + lane : -1; }
 
 // Fused norm, producer: the tile row's sums of x^2 per hidden-state row from the warps'
-// partial sums (slots in order), written by thread e = n. Every epilogue thread calls this.
+// partial sums (slots slot0 .. slot0 + slots - 1 in order), written by thread e = n. Every
+// epilogue thread calls this.
 __device__ __forceinline__ void fuse_tile_sums(const GemmParams& p, const float (*ssw)[kFuseMaxN], int t, int e,
-                                               int slots) {
+                                               int slot0, int slots) {
     epilogue_bar_sync();  // every warp's sums are in
     if (e < p.N) {
         float v = 0.f;
-        for (int k = 0; k < slots; ++k) v += ssw[k][e];
+        for (int k = slot0; k < slot0 + slots; ++k) v += ssw[k][e];
         p.ss_out[static_cast<long long>(t) * p.N + e] = v;
     }
     epilogue_bar_sync();  // the slots are rewritten by the next tile row
+}
+
+// Fused norm, producer: the tile rows' sums of x^2 of a unit's block (a pair block: rows
+// 0..63 in slots 0, 1, rows 64..127 in slots 2, 3; a single-row block: slots 0 .. slots - 1).
+__device__ __forceinline__ void fuse_block_sums(const GemmParams& p, const float (*ssw)[kFuseMaxN], const Piece& pc,
+                                                int e, int single_slots) {
+    if (pc.m128) {
+        fuse_tile_sums(p, ssw, pc.t, e, 0, 2);
+        if (pc.pair) fuse_tile_sums(p, ssw, pc.t + 1, e, 2, 2);
+    } else {
+        fuse_tile_sums(p, ssw, pc.t, e, 0, single_slots);
+    }
+}
+
+// The output row (within its block) that TMEM lane `lane` of sub-partition qp holds: a pair
+// block (M = 128) has rows 32 qp .. 32 qp + 31, a single-row block (M = 64) rows 16 qp ..
+// 16 qp + 15 in lanes 0..15 (-1 elsewhere).
+__device__ __forceinline__ int block_row_of_lane(bool m128, int qp, int lane) {
+    return m128 ? qp * 32 + lane : umma_m64_row_of_lane(qp, lane);
+}
+
+// Whether row r of a block is an output row of this unit: rows 64..127 of a pair block only
+// when its second tile row is in the tier, and never past M.
+__device__ __forceinline__ bool block_row_ok(const GemmParams& p, const Piece& pc, int r) {
+    return r >= 0 && (r < kTileM || pc.pair) && pc.t * kTileM + r < p.M;
+}
+
+// Fused norm, producer, up to 16 hidden-state rows: the residual values an epilogue thread
+// adds to and the gain, loaded before the accumulator is ready (a round trip to L2 off the
+// unit's tail); x is written only by the epilogue that finishes a block. In the split path
+// thread e holds row e of a pair block (every column), or row e % 64 of a single-row block
+// and the 8 columns from 8 (e / 64); in the one-piece path the row of its TMEM lane (rib) and
+// every column.
+__device__ __forceinline__ void preload_x(const GemmParams& p, const Piece& pc, int e, int rib,
+                                          float (&xpre)[kFusePreloadN], float& gpre) {
+    const bool split = p.P > 1;
+    const int r = split ? (pc.m128 ? e : (e & 63)) : rib;
+    const int xrow = pc.t * kTileM + r;
+    const int xn0 = (split && !pc.m128) ? 8 * (e >> 6) : 0;
+    const int xcols = (split && !pc.m128) ? 8 : p.N_pad;
+    const bool ok = block_row_ok(p, pc, r);
+#pragma unroll
+    for (int j = 0; j < kFusePreloadN; ++j) {
+        const int n = xn0 + j;
+        const bool use = ok && j < xcols && n < p.N;
+        xpre[j] = use ? p.res_x[static_cast<long long>(n) * p.M + xrow] : 0.f;
+    }
+    gpre = ok ? __bfloat162float(p.res_g[xrow]) : 0.f;
+}
+
+// One unit's epilogue, run by the four epilogue warps (thread e = 0..127; warp `warp` reads
+// TMEM sub-partition warp & 3). A split block (P > 1): the CTA of every piece stores its fp32
+// partial block in the workspace and counts the piece in; the CTA that counts the last one
+// adds the P partials in piece order (a fixed order, whichever CTA ran which piece and
+// whatever the placement) and writes C. No CTA waits for another. After a wait that ran
+// out (`failed`), the threads skip the work but meet the epilogue's named barriers.
+__device__ __forceinline__ void epilogue_unit(const GemmParams& p, const Piece& pc, uint32_t taddr, bool failed,
+                                              uint64_t* acc_empty_ab, int warp, int lane, int e, int n_off, bool fx,
+                                              bool fr, const float* rsc, float (*fuse_ssw)[kFuseMaxN],
+                                              volatile int* last_piece, bool xpre_on,
+                                              const float (&xpre)[kFusePreloadN], float gpre) {
+    const int qp = warp & 3;
+    const int rib = block_row_of_lane(pc.m128, qp, lane);
+    const int row = pc.t * kTileM + rib;
+    const bool valid = block_row_ok(p, pc, rib);
+    const int blk_floats = block_rows(pc) * p.N_pad;  // one piece's partial block in the workspace
+    if (p.P > 1) {
+        float* mine = piece_part(p, pc, pc.idx);
+        for (int n0 = 0; n0 < p.N_pad && !failed; n0 += 8) {
+            uint32_t v[8];
+            tmem_ld8(taddr + static_cast<uint32_t>(n0), v);
+            tmem_wait_ld();
+            if (rib >= 0) {  // (rows past the tier or M too: the sum skips them)
+                float4* d = reinterpret_cast<float4*>(mine + rib * p.N_pad + n0);
+                d[0] = make_float4(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]),
+                                   __uint_as_float(v[3]));
+                d[1] = make_float4(__uint_as_float(v[4]), __uint_as_float(v[5]), __uint_as_float(v[6]),
+                                   __uint_as_float(v[7]));
+            }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0 && !failed) mbar_arrive(acc_empty_ab);  // the accumulator is free again
+        // One thread counts the piece in, with release semantics for the 128 threads' stores
+        // (ordered before it by the barrier) and acquire semantics for the other pieces'
+        // partials, which the last piece's CTA reads next.
+        epilogue_bar_sync();
+        if (warp == 2 && lane == 0) {
+            *last_piece = 0;
+            if (!failed) {
+                const int done = atomic_add_acq_rel(p.cnt + pc.blk, 1) + 1;
+                *last_piece = done == p.P;
+                if (done == p.P) p.cnt[pc.blk] = 0;  // ready for the next launch
+            }
+        }
+        epilogue_bar_sync();
+        if (!*last_piece) return;
+        // The P partials, added in piece order. All 128 threads share the work: thread e takes
+        // row e of a pair block (every 8-column block), or row e % 64 of a single-row block and
+        // the 8-column blocks e / 64, e / 64 + 2, ...; lanes e and e ^ 1 hold rows 2j and 2j + 1
+        // (the gate / up pair of a SwiGLU placement).
+        const int rr = pc.m128 ? e : (e & 63);
+        const int b0 = pc.m128 ? 0 : (e >> 6), bstep = pc.m128 ? 1 : 2;
+        const int rrow = pc.t * kTileM + rr;
+        const bool rok = block_row_ok(p, pc, rr);
+        const float* src0 = piece_part(p, pc, 0) + rr * p.N_pad;
+        for (int blk = b0; blk * 8 < p.N_pad; blk += bstep) {
+            const float* src = src0 + blk * 8;
+            float f[8];
+            for (int r0 = 0; r0 < p.P; r0 += 4) {  // four partials in flight at a time
+                float4 x[8];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    if (r0 + r < p.P) {
+                        x[2 * r] = __ldcg(reinterpret_cast<const float4*>(src + (r0 + r) * blk_floats));
+                        x[2 * r + 1] = __ldcg(reinterpret_cast<const float4*>(src + (r0 + r) * blk_floats + 4));
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    if (r0 + r == 0) {
+                        f[0] = x[0].x; f[1] = x[0].y; f[2] = x[0].z; f[3] = x[0].w;
+                        f[4] = x[1].x; f[5] = x[1].y; f[6] = x[1].z; f[7] = x[1].w;
+                    } else if (r0 + r < p.P) {
+                        f[0] += x[2 * r].x; f[1] += x[2 * r].y; f[2] += x[2 * r].z; f[3] += x[2 * r].w;
+                        f[4] += x[2 * r + 1].x; f[5] += x[2 * r + 1].y; f[6] += x[2 * r + 1].z;
+                        f[7] += x[2 * r + 1].w;
+                    }
+                }
+            }
+            float sq[8], xb[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) xb[j] = (pc.m128 && blk == 1) ? xpre[8 + j] : xpre[j];  // registers
+            store_c(p, f, rrow, rok, n_off + blk * 8, fx, fr, rsc, sq, xpre_on ? xb : nullptr, gpre);
+            if (fx) {
+                // rows 32 w2 .. 32 w2 + 31 of the thread's warp w2 = e / 32: one sum per column
+                // (a pair block: slot w2; a single-row block: slot w2 % 2, the column blocks of
+                // the two halves being different)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float v = warp_sum(sq[j]);
+                    if (lane == 0) fuse_ssw[pc.m128 ? (e >> 5) : ((e >> 5) & 1)][blk * 8 + j] = v;
+                }
+            }
+        }
+        if (fx) fuse_block_sums(p, fuse_ssw, pc, e, 2);
+        return;
+    }
+    for (int n0 = 0; n0 < p.N_pad; n0 += 8) {
+        float f[8];
+        if (!failed) {
+            uint32_t v[8];
+            tmem_ld8(taddr + static_cast<uint32_t>(n0), v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(v[j]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] = 0.f;
+        }
+        float sq[8], xb[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) xb[j] = n0 == 0 ? xpre[j] : xpre[8 + j];  // registers, not a stack copy
+        store_c(p, f, row, valid && !failed, n_off + n0, fx, fr, rsc, sq, xpre_on ? xb : nullptr, gpre);
+        if (fx) {
+            // the rows of this warp's sub-partition: one sum per column
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float v = warp_sum(sq[j]);
+                if (lane == 0) fuse_ssw[qp][n0 + j] = v;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0 && !failed) mbar_arrive(acc_empty_ab);
+    if (fx) fuse_block_sums(p, fuse_ssw, pc, e, 4);
 }
 
 template <bool F>
@@ -775,8 +1008,8 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     // 1024-byte aligned ring (128-byte swizzle atoms must start on 1024-byte boundaries)
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-    const int a_stage_bytes = it.c.kc * 128;
-    const int bblk_bytes = p.N_pad * 128;  // one 64-column block of B
+    const int a_stage_bytes = it.c.kc * it.c.a_cb;  // A of the stage (128 or 256 bytes per column)
+    const int bblk_bytes = p.N_pad * 128;     // one 64-column block of B
     uint32_t tmem_cols = 32;
     while (tmem_cols < static_cast<uint32_t>(2 * p.N_pad)) tmem_cols <<= 1;
     const uint32_t acc_stride = tmem_cols >> 1;  // column offset of the second accumulator
@@ -834,7 +1067,8 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     } else if (warp == 1) {
         // The whole warp runs the loop (so that loop state and descriptors stay warp-uniform);
         // one elected lane issues the MMAs and commits.
-        const uint32_t idesc = idesc_bf16_f32(64, static_cast<uint32_t>(p.N_pad));
+        const uint32_t idesc2 = idesc_bf16_f32(128, static_cast<uint32_t>(p.N_pad));  // a block of two
+        const uint32_t idesc1 = idesc_bf16_f32(64, static_cast<uint32_t>(p.N_pad));   // one tile row
         const bool leader = elect_one();
         long long i = 0, ib = 0;
         uint64_t* last_bar = nullptr;
@@ -848,6 +1082,8 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
             tc_fence_after();
             const uint32_t d_tmem = tmem + static_cast<uint32_t>(ab) * acc_stride;
             const Piece q = piece_of(p, it, ui);
+            const uint32_t idesc = q.m128 ? idesc2 : idesc1;
+            const uint32_t kg_bytes = q.m128 ? 2048u : 1024u;  // one k-group of the block's A
             bool ok = true;
             for (int k0 = q.k0; k0 < q.k1; k0 += it.c.kc, ++i) {
                 const int s = static_cast<int>(i % W);
@@ -864,9 +1100,9 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
                 const int kce = min(it.c.kc, q.k1 - k0);
                 const uint32_t a_base = smem_u32(smem + static_cast<size_t>(s) * it.c.stage_bytes);
                 // A: no swizzle, K-major; 8x8 blocks of one k-group are 128 B apart along M,
-                // k-groups are 64 rows x 16 B = 1024 B apart along K (+2048 B per MMA).
-                // B: 128-byte swizzle, K-major; 8-row groups 1024 B apart, 64-column blocks
-                // N_pad x 128 B apart, +32 B per 16 columns inside a block.
+                // k-groups are 128 (or 64) rows x 16 B = 2048 (1024) B apart along K, two per
+                // MMA. B: 128-byte swizzle, K-major; 8-row groups 1024 B apart, 64-column
+                // blocks N_pad x 128 B apart, +32 B per 16 columns inside a block.
                 for (int sub = 0; sub * it.c.kcb < kce && ok; ++sub) {
                     uint32_t b_base = a_base + static_cast<uint32_t>(a_stage_bytes);
                     int sb = -1;
@@ -882,11 +1118,12 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
                     }
                     const int k_sub = sub * it.c.kcb;
                     const int kcs = min(it.c.kcb, kce - k_sub);
-                    const uint64_t ad0 = smem_desc(a_base + static_cast<uint32_t>((k_sub >> 3) * 1024), 1024u, 128u, 0u);
+                    const uint64_t ad0 =
+                        smem_desc(a_base + static_cast<uint32_t>(k_sub >> 3) * kg_bytes, kg_bytes, 128u, 0u);
                     const uint64_t bd0 = smem_desc(b_base, 16u, 1024u, 2u);
                     if (leader) {
                         issue_mmas(d_tmem, ad0, bd0, static_cast<uint32_t>(bblk_bytes >> 4), kcs >> 4, idesc,
-                                   k0 > q.k0 || k_sub > 0);
+                                   k0 > q.k0 || k_sub > 0, (2u * kg_bytes) >> 4);
                         if (sb >= 0) umma_commit(&b_empty[sb]);
                     }
                     __syncwarp();
@@ -914,17 +1151,9 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         }
         __syncwarp();
     } else {
-        // epilogue warps 2..5 -> TMEM sub-partitions 2, 3, 0, 1 (lanes 0..15 of sub-partition q
-        // hold rows 16q .. 16q + 15). A split tile row (P > 1): the CTA of every piece stores
-        // its fp32 partial tile in the workspace and counts the piece in; the CTA that counts
-        // the last one adds the P partials in piece order (a fixed order, whichever CTA ran
-        // which piece and whatever the placement) and writes C. No CTA waits for another.
-        // After a wait that ran out, a warp skips the work but keeps meeting the epilogue's
-        // named barriers, so that no warp is left waiting for one that gave up.
+        // epilogue warps 2..5 -> TMEM sub-partitions 2, 3, 0, 1 (epilogue_unit has the row map)
         const int qp = warp & 3;
-        const int row_in_tile = umma_m64_row_of_lane(qp, lane);
         const int n_off = p.NC > 1 ? it.rank * p.N_pad : 0;  // first hidden-state row of this CTA's block
-        const int tile_floats = kTileM * p.N_pad;
         const int e = threadIdx.x - 64;  // 0..127
         grid_dep_wait();  // C and the split workspace may still be in use by the previous kernel of the stream
         const float* rsc = nullptr;
@@ -948,145 +1177,22 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
             rsc = fuse_r;
         }
         bool failed = false;
-        // fused norm, producer, up to 16 hidden-state rows: the residual values this thread
-        // adds to and the gain, loaded before the accumulator is ready (a round trip to L2
-        // off the tile row's tail); x is written only by the epilogue that finishes a tile row
         const bool xpre_on = fx && p.N_pad <= kFusePreloadN;
         float xpre[kFusePreloadN];
         float gpre = 0.f;
         for (int ui = 0; ui < it.count; ++ui) {
             const int ab = ui & 1;
-            if (xpre_on) {
-                const int t = piece_of(p, it, ui).t;
-                // the split path's thread e holds row e % 64 and the 8 columns from 8 (e / 64);
-                // the one-piece path holds row_in_tile and every column
-                const int xrow = t * kTileM + (p.P > 1 ? (e & 63) : row_in_tile);
-                const int xn0 = p.P > 1 ? 8 * (e >> 6) : 0;
-                const bool ok = (p.P > 1 || row_in_tile >= 0) && xrow < p.M;
-                const int xcols = p.P > 1 ? 8 : p.N_pad;
-#pragma unroll
-                for (int j = 0; j < kFusePreloadN; ++j) {
-                    const int n = xn0 + j;
-                    const bool use = ok && j < xcols && n < p.N;
-                    xpre[j] = use ? p.res_x[static_cast<long long>(n) * p.M + xrow] : 0.f;
-                }
-                gpre = ok ? __bfloat162float(p.res_g[xrow]) : 0.f;
-            }
+            const Piece pc = piece_of(p, it, ui);
+            if (xpre_on) preload_x(p, pc, e, block_row_of_lane(pc.m128, qp, lane), xpre, gpre);
             if (!failed && !mbar_wait(&acc_full[ab], static_cast<uint32_t>((ui >> 1) & 1), abort, p.st,
                                       DAK_ERR_TIMEOUT, W_EPI_ACC)) {
                 failed = true;
             }
             if (failed && p.P == 1 && !fx) break;  // no barrier to keep meeting
             tc_fence_after();
-            const Piece pc = piece_of(p, it, ui);
-            const int row = pc.t * kTileM + row_in_tile;
-            const bool valid = row_in_tile >= 0 && row < p.M;
             const uint32_t taddr = tmem + (static_cast<uint32_t>(qp * 32) << 16) + static_cast<uint32_t>(ab) * acc_stride;
-            if (p.P > 1) {
-                float* mine = p.part + (static_cast<long long>(pc.t) * p.P + pc.idx) * tile_floats;
-                for (int n0 = 0; n0 < p.N_pad && !failed; n0 += 8) {
-                    uint32_t v[8];
-                    tmem_ld8(taddr + static_cast<uint32_t>(n0), v);
-                    tmem_wait_ld();
-                    if (row_in_tile >= 0) {
-                        float4* d = reinterpret_cast<float4*>(mine + row_in_tile * p.N_pad + n0);
-                        d[0] = make_float4(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]),
-                                           __uint_as_float(v[3]));
-                        d[1] = make_float4(__uint_as_float(v[4]), __uint_as_float(v[5]), __uint_as_float(v[6]),
-                                           __uint_as_float(v[7]));
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0 && !failed) mbar_arrive(&acc_empty[ab]);  // the accumulator is free again
-                // One thread counts the piece in, with release semantics for the 128 threads'
-                // stores (ordered before it by the barrier) and acquire semantics for the other
-                // pieces' partials, which the last piece's CTA reads next.
-                epilogue_bar_sync();
-                if (warp == 2 && lane == 0) {
-                    last_piece = 0;
-                    if (!failed) {
-                        const int done = atomic_add_acq_rel(p.cnt + pc.t, 1) + 1;
-                        last_piece = done == p.P;
-                        if (done == p.P) p.cnt[pc.t] = 0;  // ready for the next launch
-                    }
-                }
-                epilogue_bar_sync();
-                if (!last_piece) continue;
-                // The P partials, added in piece order. All 128 threads share the work: thread e
-                // takes row e % 64 and the 8-column blocks e / 64, e / 64 + 2, ...; lanes e and
-                // e ^ 1 hold rows 2j and 2j + 1 (the gate / up pair of a SwiGLU placement).
-                const int rr = e & 63;
-                const int rrow = pc.t * kTileM + rr;
-                const float* src0 = p.part + static_cast<long long>(pc.t) * p.P * tile_floats + rr * p.N_pad;
-                for (int blk = e >> 6; blk * 8 < p.N_pad; blk += 2) {
-                    const float* src = src0 + blk * 8;
-                    float f[8];
-                    for (int r0 = 0; r0 < p.P; r0 += 4) {  // four partials in flight at a time
-                        float4 x[8];
-#pragma unroll
-                        for (int r = 0; r < 4; ++r) {
-                            if (r0 + r < p.P) {
-                                x[2 * r] = __ldcg(reinterpret_cast<const float4*>(src + (r0 + r) * tile_floats));
-                                x[2 * r + 1] = __ldcg(reinterpret_cast<const float4*>(src + (r0 + r) * tile_floats + 4));
-                            }
-                        }
-#pragma unroll
-                        for (int r = 0; r < 4; ++r) {
-                            if (r0 + r == 0) {
-                                f[0] = x[0].x; f[1] = x[0].y; f[2] = x[0].z; f[3] = x[0].w;
-                                f[4] = x[1].x; f[5] = x[1].y; f[6] = x[1].z; f[7] = x[1].w;
-                            } else if (r0 + r < p.P) {
-                                f[0] += x[2 * r].x; f[1] += x[2 * r].y; f[2] += x[2 * r].z; f[3] += x[2 * r].w;
-                                f[4] += x[2 * r + 1].x; f[5] += x[2 * r + 1].y; f[6] += x[2 * r + 1].z;
-                                f[7] += x[2 * r + 1].w;
-                            }
-                        }
-                    }
-                    float sq[8];
-                    store_c(p, f, rrow, rrow < p.M, n_off + blk * 8, fx, fr, rsc, sq, xpre_on ? xpre : nullptr,
-                            gpre);
-                    if (fx) {
-                        // rows 32 w2 .. 32 w2 + 31 of this block: one sum per column
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const float v = warp_sum(sq[j]);
-                            if (lane == 0) fuse_ssw[(e >> 5) & 1][blk * 8 + j] = v;
-                        }
-                    }
-                }
-                if (fx) fuse_tile_sums(p, fuse_ssw, pc.t, e, 2);
-                continue;
-            }
-            for (int n0 = 0; n0 < p.N_pad; n0 += 8) {
-                float f[8];
-                if (!failed) {
-                    uint32_t v[8];
-                    tmem_ld8(taddr + static_cast<uint32_t>(n0), v);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(v[j]);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) f[j] = 0.f;
-                }
-                float sq[8], xb[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) xb[j] = n0 == 0 ? xpre[j] : xpre[8 + j];  // registers, not a stack copy
-                store_c(p, f, row, valid && !failed, n_off + n0, fx, fr, rsc, sq, xpre_on ? xb : nullptr, gpre);
-                if (fx) {
-                    // rows 16 qp .. 16 qp + 15 (lanes 0..15): one sum per column
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float v = warp_sum(sq[j]);
-                        if (lane == 0) fuse_ssw[qp][n0 + j] = v;
-                    }
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0 && !failed) mbar_arrive(&acc_empty[ab]);
-            if (fx) fuse_tile_sums(p, fuse_ssw, pc.t, e, 4);
+            epilogue_unit(p, pc, taddr, failed, &acc_empty[ab], warp, lane, e, n_off, fx, fr, rsc, fuse_ssw,
+                                &last_piece, xpre_on, xpre, gpre);
         }
     }
 
@@ -1182,7 +1288,8 @@ __device__ __forceinline__ void chain_produce(const ChainParams& cp, const Chain
         }
         for (int ui = 0; ui < it.count && !*abort; ++ui) {
             const Piece q = piece_of(p, it, ui);
-            const uint8_t* src = tile_src(p, it, q.t);
+            const uint8_t* src = block_src(p, it, q);
+            const int cb = col_bytes(q);
             for (int k0 = q.k0; k0 < q.k1; k0 += it.c.kc, ++i) {
                 const int s = static_cast<int>(i % W);
                 if (i >= W && !mbar_wait(&empty[s], static_cast<uint32_t>(((i / W) - 1) & 1), abort, p.st,
@@ -1191,12 +1298,12 @@ __device__ __forceinline__ void chain_produce(const ChainParams& cp, const Chain
                 }
                 uint8_t* dst = smem + static_cast<size_t>(s) * it.c.stage_bytes;
                 if (is_a) {
-                    const uint32_t a_bytes = static_cast<uint32_t>(min(it.c.kc, q.k1 - k0)) * 128u;
+                    const uint32_t a_bytes = static_cast<uint32_t>(min(it.c.kc, q.k1 - k0) * cb);
                     mbar_arrive_expect_tx(&full[s], a_bytes);
-                    bulk_g2s(dst, src + static_cast<long long>(k0) * 128, a_bytes, &full[s], pol_a);
+                    bulk_g2s(dst, src + static_cast<long long>(k0) * cb, a_bytes, &full[s], pol_a);
                 } else {
                     mbar_arrive_expect_tx(&full[s], b_stage_bytes(p, kUmmaB, it.c.kcb));
-                    issue_b(p, &maps.m[j], dst + it.c.kc * 128, k0, &full[s], kUmmaB, 0, it.c.kcb);
+                    issue_b(p, &maps.m[j], dst + it.c.kc * it.c.a_cb, k0, &full[s], kUmmaB, 0, it.c.kcb);
                 }
             }
         }
@@ -1253,9 +1360,10 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     if (warp == 0 || warp == 6) {
         if (lane == 0) chain_produce(cp, maps, smem, full, empty, abort, warp == 0, W);
     } else if (warp == 1) {
-        const uint32_t idesc = idesc_bf16_f32(64, static_cast<uint32_t>(N_pad));
+        const uint32_t idesc2 = idesc_bf16_f32(128, static_cast<uint32_t>(N_pad));  // a block of two
+        const uint32_t idesc1 = idesc_bf16_f32(64, static_cast<uint32_t>(N_pad));   // one tile row
         const bool leader = elect_one();
-        const int a_stage_bytes = cp.op[0].ch[0].kc * 128;
+        const int a_stage_bytes = cp.op[0].ch[0].kc * cp.op[0].ch[0].a_cb;
         const uint32_t bblk16 = static_cast<uint32_t>((N_pad * 128) >> 4);
         long long i = 0;
         int uu = 0;  // units of the whole chain so far (the accumulator alternates on it)
@@ -1275,6 +1383,8 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + static_cast<uint32_t>(ab) * acc_stride;
                 const Piece q = piece_of(p, it, ui);
+                const uint32_t idesc = q.m128 ? idesc2 : idesc1;
+                const uint32_t kg_bytes = q.m128 ? 2048u : 1024u;
                 for (int k0 = q.k0; k0 < q.k1; k0 += it.c.kc, ++i) {
                     const int s = static_cast<int>(i % W);
                     if (!mbar_wait(&full[s], static_cast<uint32_t>((i / W) & 1), abort, p.st, DAK_ERR_TIMEOUT,
@@ -1285,10 +1395,10 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
                     tc_fence_after();
                     const int kce = min(it.c.kc, q.k1 - k0);
                     const uint32_t a_base = smem_u32(smem + static_cast<size_t>(s) * it.c.stage_bytes);
-                    const uint64_t ad0 = smem_desc(a_base, 1024u, 128u, 0u);
+                    const uint64_t ad0 = smem_desc(a_base, kg_bytes, 128u, 0u);
                     const uint64_t bd0 = smem_desc(a_base + static_cast<uint32_t>(a_stage_bytes), 16u, 1024u, 2u);
                     if (leader) {
-                        issue_mmas(d_tmem, ad0, bd0, bblk16, kce >> 4, idesc, k0 > q.k0);
+                        issue_mmas(d_tmem, ad0, bd0, bblk16, kce >> 4, idesc, k0 > q.k0, (2u * kg_bytes) >> 4);
                         umma_commit(&empty[s]);
                     }
                     __syncwarp();
@@ -1310,8 +1420,6 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     } else if (warp >= 2 && warp <= 5) {
         // epilogue warps 2..5 -> TMEM sub-partitions 2, 3, 0, 1 (as gemm_umma_kernel)
         const int qp = warp & 3;
-        const int row_in_tile = umma_m64_row_of_lane(qp, lane);
-        const int tile_floats = kTileM * N_pad;
         const int e = threadIdx.x - 64;  // 0..127
         grid_dep_wait();  // C, the fused inputs and the workspace may be in use by the previous kernel
         bool failed = false;
@@ -1352,127 +1460,17 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
             float gpre = 0.f;
             for (int ui = 0; ui < it.count; ++ui, ++uu) {
                 const int ab = uu & 1;
-                if (xpre_on) {
-                    const int t = piece_of(p, it, ui).t;
-                    const int xrow = t * kTileM + (p.P > 1 ? (e & 63) : row_in_tile);
-                    const int xn0 = p.P > 1 ? 8 * (e >> 6) : 0;
-                    const bool ok = (p.P > 1 || row_in_tile >= 0) && xrow < p.M;
-                    const int xcols = p.P > 1 ? 8 : N_pad;
-#pragma unroll
-                    for (int jj = 0; jj < kFusePreloadN; ++jj) {
-                        const int n = xn0 + jj;
-                        const bool use = ok && jj < xcols && n < p.N;
-                        xpre[jj] = use ? p.res_x[static_cast<long long>(n) * p.M + xrow] : 0.f;
-                    }
-                    gpre = ok ? __bfloat162float(p.res_g[xrow]) : 0.f;
-                }
+                const Piece pc = piece_of(p, it, ui);
+                if (xpre_on) preload_x(p, pc, e, block_row_of_lane(pc.m128, qp, lane), xpre, gpre);
                 if (!failed && !mbar_wait(&acc_full[ab], static_cast<uint32_t>((uu >> 1) & 1), abort, p.st,
                                           DAK_ERR_TIMEOUT, W_EPI_ACC)) {
                     failed = true;
                 }
                 tc_fence_after();
-                const Piece pc = piece_of(p, it, ui);
-                const int row = pc.t * kTileM + row_in_tile;
-                const bool valid = row_in_tile >= 0 && row < p.M;
                 const uint32_t taddr =
                     tmem + (static_cast<uint32_t>(qp * 32) << 16) + static_cast<uint32_t>(ab) * acc_stride;
-                if (p.P > 1) {
-                    float* mine = p.part + (static_cast<long long>(pc.t) * p.P + pc.idx) * tile_floats;
-                    for (int n0 = 0; n0 < N_pad && !failed; n0 += 8) {
-                        uint32_t v[8];
-                        tmem_ld8(taddr + static_cast<uint32_t>(n0), v);
-                        tmem_wait_ld();
-                        if (row_in_tile >= 0) {
-                            float4* d = reinterpret_cast<float4*>(mine + row_in_tile * N_pad + n0);
-                            d[0] = make_float4(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]),
-                                               __uint_as_float(v[3]));
-                            d[1] = make_float4(__uint_as_float(v[4]), __uint_as_float(v[5]), __uint_as_float(v[6]),
-                                               __uint_as_float(v[7]));
-                        }
-                    }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0 && !failed) mbar_arrive(&acc_empty[ab]);
-                    epilogue_bar_sync();
-                    if (warp == 2 && lane == 0) {
-                        last_piece = 0;
-                        if (!failed) {
-                            const int dn = atomic_add_acq_rel(p.cnt + pc.t, 1) + 1;
-                            last_piece = dn == p.P;
-                            if (dn == p.P) p.cnt[pc.t] = 0;  // ready for the next launch
-                        }
-                    }
-                    epilogue_bar_sync();
-                    if (!last_piece) continue;
-                    const int rr = e & 63;
-                    const int rrow = pc.t * kTileM + rr;
-                    const float* src0 = p.part + static_cast<long long>(pc.t) * p.P * tile_floats + rr * N_pad;
-                    for (int blk = e >> 6; blk * 8 < N_pad; blk += 2) {
-                        const float* src = src0 + blk * 8;
-                        float f[8];
-                        for (int r0 = 0; r0 < p.P; r0 += 4) {
-                            float4 x[8];
-#pragma unroll
-                            for (int r = 0; r < 4; ++r) {
-                                if (r0 + r < p.P) {
-                                    x[2 * r] = __ldcg(reinterpret_cast<const float4*>(src + (r0 + r) * tile_floats));
-                                    x[2 * r + 1] =
-                                        __ldcg(reinterpret_cast<const float4*>(src + (r0 + r) * tile_floats + 4));
-                                }
-                            }
-#pragma unroll
-                            for (int r = 0; r < 4; ++r) {
-                                if (r0 + r == 0) {
-                                    f[0] = x[0].x; f[1] = x[0].y; f[2] = x[0].z; f[3] = x[0].w;
-                                    f[4] = x[1].x; f[5] = x[1].y; f[6] = x[1].z; f[7] = x[1].w;
-                                } else if (r0 + r < p.P) {
-                                    f[0] += x[2 * r].x; f[1] += x[2 * r].y; f[2] += x[2 * r].z; f[3] += x[2 * r].w;
-                                    f[4] += x[2 * r + 1].x; f[5] += x[2 * r + 1].y; f[6] += x[2 * r + 1].z;
-                                    f[7] += x[2 * r + 1].w;
-                                }
-                            }
-                        }
-                        float sq[8];
-                        store_c(p, f, rrow, rrow < p.M, blk * 8, fx, fr, rsc, sq, xpre_on ? xpre : nullptr, gpre);
-                        if (fx) {
-#pragma unroll
-                            for (int jj = 0; jj < 8; ++jj) {
-                                const float v = warp_sum(sq[jj]);
-                                if (lane == 0) fuse_ssw[(e >> 5) & 1][blk * 8 + jj] = v;
-                            }
-                        }
-                    }
-                    if (fx) fuse_tile_sums(p, fuse_ssw, pc.t, e, 2);
-                    continue;
-                }
-                for (int n0 = 0; n0 < N_pad; n0 += 8) {
-                    float f[8];
-                    if (!failed) {
-                        uint32_t v[8];
-                        tmem_ld8(taddr + static_cast<uint32_t>(n0), v);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int jj = 0; jj < 8; ++jj) f[jj] = __uint_as_float(v[jj]);
-                    } else {
-#pragma unroll
-                        for (int jj = 0; jj < 8; ++jj) f[jj] = 0.f;
-                    }
-                    float sq[8], xb[8];
-#pragma unroll
-                    for (int jj = 0; jj < 8; ++jj) xb[jj] = n0 == 0 ? xpre[jj] : xpre[8 + jj];
-                    store_c(p, f, row, valid && !failed, n0, fx, fr, rsc, sq, xpre_on ? xb : nullptr, gpre);
-                    if (fx) {
-#pragma unroll
-                        for (int jj = 0; jj < 8; ++jj) {
-                            const float v = warp_sum(sq[jj]);
-                            if (lane == 0) fuse_ssw[qp][n0 + jj] = v;
-                        }
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0 && !failed) mbar_arrive(&acc_empty[ab]);
-                if (fx) fuse_tile_sums(p, fuse_ssw, pc.t, e, 4);
+                epilogue_unit(p, pc, taddr, failed, &acc_empty[ab], warp, lane, e, 0, fx, fr, rsc, fuse_ssw,
+                              &last_piece, xpre_on, xpre, gpre);
             }
             // this CTA is done with operation j: every epilogue thread's stores are ordered
             // before the count by the barrier, and made visible at GPU scope (and to the
@@ -1629,20 +1627,24 @@ static bool split_workspace(float** part, int** cnt) {
     return true;
 }
 
-// Pieces per tile row: the split of each tile row's K range into P parts (at multiples of
-// 64 columns), chosen from the shape and the SM count only, never from the placement, so
-// that results are bit-identical across offload ratios. Automatic, in two steps:
-//  1. the all-HBM cost of each P in 1..8: the busiest CTA's time, ceil(T P / slots) waves of
-//     (1 / P of a tile row's bytes plus the fixed cost of a piece). The fixed cost, piece_us
-//     of a CTA streaming at about 62 GB/s, is fitted to decode steps on this GPU: on the
-//     tensor cores max(1, N_pad / 16) us (the partial tile of 64 x N_pad fp32, the count,
-//     the last piece's sum, a ragged last chunk), on the CUDA cores 2 us (there the
-//     consumers that run the FMAs also store the partial rows). An unsplit tile row pays
-//     half of it (its epilogue stores C only).
+// Pieces per block: the split of each block's K range into P parts (at multiples of 64
+// columns), chosen from the shape and the SM count only, never from the placement, so that
+// results are bit-identical across offload ratios. Automatic, in two steps:
+//  1. the all-HBM cost of each P in 1..8: the busiest CTA's time, ceil(B P / slots) waves of
+//     (1 / P of a block's bytes plus the fixed cost of a piece), B = T blocks of one tile row
+//     or ceil(T / 2) pair blocks (rows = 2). The fixed cost, piece_us of a CTA streaming at
+//     about 62 GB/s, is fitted to decode steps on this GPU: on the tensor cores
+//     max(1, N_pad / 16) us (the partial tile of 64 x N_pad fp32, the count, the last
+//     piece's sum, a ragged last chunk), on the CUDA cores 2 us (there the consumers that
+//     run the FMAs also store the partial rows). An unsplit block pays half of it (its
+//     epilogue stores C only).
 //  2. among the P within 3% of the lowest cost, the smallest whose pieces give a host part
-//     of a tenth of the tile rows at least as many units as the host CTA cap (a small host
-//     part spread over more CTAs keeps more host bytes in flight), else the cheapest.
-// Pieces keep at least 512 columns and the workspace must hold the partials.
+//     of a tenth of the tile rows (single-row blocks: the host tier never pairs) at least as
+//     many units as the host CTA cap (a small host part spread over more CTAs keeps more
+//     host bytes in flight), else the cheapest.
+// Pieces keep at least 512 columns and the workspace must hold the partials: at most
+// T + 2 tile rows' worth (pairs: an odd tile row at the end of each tier is a block of 128
+// rows of which 64 are used).
 // tuning.split_k > 0 fixes P (1 = no split).
 constexpr double kCtaStreamBytesPerUs = 62.5e3;
 // bf16 tensor rate of one SM issuing M = 64 tiles, FLOP per us (fitted: the 8B gate+up at 256
@@ -1653,23 +1655,24 @@ constexpr double kHostLinkBytesPerUs = 2.1e5;
 constexpr double kHostCtaBytesPerUs = 1.3e4;  // a host CTA through tensor-bound tile rows (fitted: 512 KiB in ~40 us)
 
 static int split_pieces(int T, int K_pad, int N_pad, int slots, long long tile_bytes, int host_cap, int pstep,
-                        double piece_us, long long max_tiles, long long max_floats, const dak_tuning* t) {
+                        double piece_us, long long max_tiles, long long max_floats, const dak_tuning* t, int rows) {
     const int steps = (K_pad + 63) / 64;
     auto fits = [&](int P) {
         return P <= (K_pad + pstep - 1) / pstep && T <= max_tiles &&
-               static_cast<long long>(T) * P * kTileM * N_pad <= max_floats;
+               static_cast<long long>(T + 2) * P * kTileM * N_pad <= max_floats;
     };
     if (t && t->split_k > 0) {
         int P = std::min(kMaxPieces, t->split_k);
         while (P > 1 && !fits(P)) --P;
         return P;
     }
-    const double c = piece_us * kCtaStreamBytesPerUs / static_cast<double>(tile_bytes);  // in tile rows
+    const double c = piece_us * kCtaStreamBytesPerUs / (static_cast<double>(rows) * tile_bytes);  // in blocks
+    const long long nb = blocks_of(T, rows == 2);
     double cost[kMaxPieces + 1] = {};
     int top = 1;
     for (int P = 1; P <= kMaxPieces; ++P) {
         if (P > 1 && (!fits(P) || steps / P < kMinPieceSteps)) break;
-        const long long waves = (static_cast<long long>(T) * P + slots - 1) / slots;
+        const long long waves = (nb * P + slots - 1) / slots;
         cost[P] = static_cast<double>(waves) * (1.0 / P + (P > 1 ? c : 0.5 * c));
         top = P;
     }
@@ -1690,8 +1693,9 @@ constexpr long long kCallerCounterBytes = static_cast<long long>(kSplitTiles) * 
 size_t gemm_workspace_bytes(const dak_placement* A, int N) {
     if (!A || A->kind != 0 || N < 1) return 0;
     if (N > kMaxBlockN || A->T > kSplitTiles) return 0;  // never split
-    const long long n_pad = (N + 7) & ~7;
-    return static_cast<size_t>(kCallerCounterBytes + static_cast<long long>(A->T) * kMaxPieces * kTileM * n_pad * 4);
+    const long long n_pad = (N + 15) & ~15;
+    return static_cast<size_t>(kCallerCounterBytes +
+                               static_cast<long long>(A->T + 2) * kMaxPieces * kTileM * n_pad * 4);
 }
 
 void reset_split_counters() {
@@ -1705,28 +1709,37 @@ void reset_split_counters() {
 // call), so that dak_gemm_plan can report it without a GPU.
 struct BlockPlan {
     bool umma;
+    int pairs;  // HBM tier in pair blocks (M = 128)
     int NC, N_pad, P, pstep, kcb, kcb_host, smem, grid;  // kcb / kcb_host: B chunk width of each role's map
     Chunks ch[2];  // [0] HBM-side CTAs, [1] host-side CTAs
     int n_host_ctas, n_hbm_ctas, host_window, hbm_window;
 };
 
-// T tile rows (h of them on the host) of K_pad columns; N hidden-state rows (at most one
-// launch's worth); caller_ws: the partial tiles go to a caller's workspace of ws_bytes.
+// T tile rows of 64 (h of them on the host) of K_pad columns, tile_bytes each; N
+// hidden-state rows (at most one launch's worth); caller_ws: the partial tiles go to a
+// caller's workspace of ws_bytes; pairs: a placement of 128-row tiles (T and h even), whose
+// blocks of two tile rows are the units of work.
 static dak_status plan_block(int T, int h, int K_pad, long long tile_bytes, int N, int sms, const dak_tuning* t,
-                             bool caller_ws, size_t ws_bytes, BlockPlan* bp) {
+                             bool caller_ws, size_t ws_bytes, BlockPlan* bp, int pairs) {
     if (N < 1 || N > kMaxWideN || sms < 1) return DAK_ERR_INVALID;
     BlockPlan& q = *bp;
     q = BlockPlan{};
     // wide B: NC CTAs of a cluster share each tile row, CTA r computing rows [256 r, 256 r + 256)
     q.NC = N > kMaxBlockN ? (N + kMaxBlockN - 1) / kMaxBlockN : 1;
-    q.N_pad = N > kMaxBlockN ? kMaxBlockN : (N + 7) & ~7;
     q.P = 1;
     q.pstep = N >= 2 ? 64 : 256;  // the B block of the tensor-core / CUDA-core layout
     q.umma = N >= 2;  // N = 2..7 padded to 8 columns: measured 1.2-2.7x faster than FMA
     const bool umma = q.umma;
+    if (pairs && ((T | h) & 1)) return DAK_ERR_INVALID;
+    q.pairs = pairs ? 1 : 0;
+    // (pair blocks on the tensor cores: a multiple of 16, the N step of M = 128 MMAs)
+    q.N_pad = N > kMaxBlockN ? kMaxBlockN : ((q.pairs && umma) ? (N + 15) & ~15 : (N + 7) & ~7);
     const int rows_b = umma ? q.N_pad : N;
     const int NC = q.NC;
-    auto stage_of = [&](int k) { return (k * 128 + k * 2 * rows_b + 1023) & ~1023; };
+    const int cb_hbm = q.pairs ? 256 : 128;  // bytes of A per column in a stage (both roles)
+    // a stage: A (k x cb bytes: one tile row, or two), then B (k x 2 bytes per hidden-state row)
+    auto stage_cb = [&](int k, int cb) { return (k * cb + k * 2 * rows_b + 1023) & ~1023; };
+    auto stage_of = [&](int k) { return stage_cb(k, cb_hbm); };
 
     int per_sm = 1;
     if (umma && NC == 1 && t && (t->ctas_per_sm == 1 || t->ctas_per_sm == 2)) per_sm = t->ctas_per_sm;
@@ -1735,7 +1748,7 @@ static dak_status plan_block(int T, int h, int K_pad, long long tile_bytes, int 
     if (t && t->chunk_k > 0) {
         kc = t->chunk_k;
     } else if (!umma) {
-        kc = 512;
+        kc = q.pairs ? 256 : 512;  // 64 KiB of A per stage
     } else if (per_sm == 2) {
         // the widest chunk that leaves two stages
         kc = 64;
@@ -1773,11 +1786,12 @@ static dak_status plan_block(int T, int h, int K_pad, long long tile_bytes, int 
     const bool b_ring_host = umma && (NC > 1 || (q.N_pad > 128 && kc <= 128 && !(t && t->chunk_k > 0)));
     // (NC > 1: each CTA holds 2 x 256 TMEM columns, the whole TMEM of an SM: one CTA per SM)
     const int CL = NC;  // CTAs per cluster
-    auto layout = [&](int kc_, bool split, Chunks* L) -> bool {
+    auto layout = [&](int kc_, bool split, int cb, Chunks* L) -> bool {
         L->kc = kc_;
         L->kcb = split ? 64 : kc_;
+        L->a_cb = cb;
         if (split) {
-            L->stage_bytes = (kc_ * 128 + 1023) & ~1023;
+            L->stage_bytes = (kc_ * cb + 1023) & ~1023;
             L->b_slot_bytes = (q.N_pad * L->kcb * 2 + 1023) & ~1023;
             const int avail = budget - 1024;
             L->stages = std::min(4, std::max(2, avail / 2 / L->stage_bytes));  // about half for A
@@ -1788,7 +1802,7 @@ static dak_status plan_block(int T, int h, int K_pad, long long tile_bytes, int 
             }
             if (L->wb < 2) return false;
         } else {
-            L->stage_bytes = stage_of(kc_);
+            L->stage_bytes = stage_cb(kc_, cb);
             L->stages = std::min(8, (budget - (umma ? 1024 : 0)) / L->stage_bytes);
             L->wb = 0;
             L->b_slot_bytes = 0;
@@ -1797,13 +1811,16 @@ static dak_status plan_block(int T, int h, int K_pad, long long tile_bytes, int 
         L->b_ring_off = L->stages * L->stage_bytes;
         return true;
     };
-    if (!layout(kc, b_ring_all, &q.ch[0])) return DAK_ERR_INVALID;
+    if (!layout(kc, b_ring_all, cb_hbm, &q.ch[0])) return DAK_ERR_INVALID;
     q.ch[1] = q.ch[0];
     if (!b_ring_all && b_ring_host && h > 0) {
-        const int kch = (NC > 1 && t && t->chunk_k > 0) ? std::max(64, t->chunk_k) : 256;
-        if (!layout(kch, true, &q.ch[1])) {
-            if (NC > 1) return DAK_ERR_INVALID;  // a forwarding cluster needs A-only slots
-            q.ch[1] = q.ch[0];
+        // 32 KiB of A per chunk
+        const int kch = (NC > 1 && t && t->chunk_k > 0) ? std::max(64, t->chunk_k) : (q.pairs ? 128 : 256);
+        Chunks L;
+        if (layout(kch, true, cb_hbm, &L)) {
+            q.ch[1] = L;
+        } else if (NC > 1) {
+            return DAK_ERR_INVALID;  // a forwarding cluster needs A-only slots
         }
     }
     q.kcb = q.ch[0].kcb;
@@ -1812,10 +1829,11 @@ static dak_status plan_block(int T, int h, int K_pad, long long tile_bytes, int 
     const int rings = std::max(ring_bytes(q.ch[0]), ring_bytes(q.ch[1]));
     q.smem = rings + (umma ? 1024 : 0);
     const int max_stages = std::max(q.ch[0].stages, q.ch[1].stages);
+    const int hb = blocks_of(h, q.pairs), gb = blocks_of(T - h, q.pairs);  // blocks: units before the split
 
-    // pieces per tile row (one CTA per tile row's columns; automatic only while the tile
-    // rows are memory-bound, N_pad <= 128: at N_pad = 256 the tensor work of a tile row is
-    // what the split would spread, and the partial tiles cost more than it saves)
+    // pieces per block (one CTA per block's columns; automatic only while the tile rows are
+    // memory-bound, N_pad <= 128: at N_pad = 256 the tensor work of a tile row is what the
+    // split would spread, and the partial tiles cost more than it saves)
     if (NC == 1 && (q.N_pad <= 128 || (t && t->split_k > 0))) {
         const double piece_us = umma ? std::max(1.0, q.N_pad / 16.0) : 2.0;
         // the caller's workspace (counters, then partial tiles) or the module's own
@@ -1823,7 +1841,7 @@ static dak_status plan_block(int T, int h, int K_pad, long long tile_bytes, int 
         const long long max_floats =
             caller_ws ? std::max(0ll, (static_cast<long long>(ws_bytes) - cnt_bytes) / 4) : kSplitFloats;
         q.P = split_pieces(T, K_pad, q.N_pad, sms * per_sm, tile_bytes, kDefaultHostCtas, q.pstep, piece_us,
-                           kSplitTiles, max_floats, t);
+                           kSplitTiles, max_floats, t, q.pairs ? 2 : 1);
     }
 
     // schedule in cluster units; a role's units are its tile rows x P pieces
@@ -1831,8 +1849,8 @@ static dak_status plan_block(int T, int h, int K_pad, long long tile_bytes, int 
     if (t) tc = *t;
     const int host_cap = NC > 1 ? kDefaultHostCtasWide : kDefaultHostCtas;
     int hc = tc.host_ctas > 0 ? tc.host_ctas : host_cap;
-    if (!(tc.host_ctas > 0) && CL == 1 && h * q.P > hc && 3 * h * q.P <= 4 * hc) {
-        hc = h * q.P;  // up to a third over the cap: one wave of host units rather than two
+    if (!(tc.host_ctas > 0) && CL == 1 && hb * q.P > hc && 3 * hb * q.P <= 4 * hc) {
+        hc = hb * q.P;  // up to a third over the cap: one wave of host units rather than two
     }
     // A tile row at N_pad >= 256 is tensor work: its MMAs take longer than its bytes, and
     // every host CTA is an SM taken from the HBM side's compute. There the host CTA count is
@@ -1845,13 +1863,15 @@ static dak_status plan_block(int T, int h, int K_pad, long long tile_bytes, int 
     // so the flat segment of Fig. 6 ends before x = B_host T_comp / C. Memory-bound tile rows
     // keep the fixed cap above.
     if (q.N_pad >= 256 && h > 0 && !(t && t->host_ctas > 0)) {
-        const double unit_bytes = static_cast<double>(tile_bytes) / q.P;
-        const double t_unit = std::max(2.0 * kTileM * q.N_pad * (static_cast<double>(K_pad) / q.P) / kSmTensorFlopsPerUs,
-                                       unit_bytes / kCtaStreamBytesPerUs);
+        // a unit is a block's piece; the M = 128 MMAs of a pair block take about as long as one
+        // tile row's M = 64 ones at N >= 128 (measured)
+        const double unit_bytes = (q.pairs ? 2.0 : 1.0) * static_cast<double>(tile_bytes) / q.P;
+        const double t_mma = 2.0 * kTileM * q.N_pad * (static_cast<double>(K_pad) / q.P) / kSmTensorFlopsPerUs;
+        const double t_unit = std::max(t_mma, unit_bytes / kCtaStreamBytesPerUs);
         const double t_host_unit = std::max(t_unit, unit_bytes / kHostCtaBytesPerUs);
         const double t_link = static_cast<double>(h) * tile_bytes / kHostLinkBytesPerUs;
         const int slots = std::max(1, (sms * per_sm) / CL);
-        const long long hu = static_cast<long long>(h) * q.P, gu = static_cast<long long>(T - h) * q.P;
+        const long long hu = static_cast<long long>(hb) * q.P, gu = static_cast<long long>(gb) * q.P;
         // one SM of a host cluster reads the link (rank 0 forwards): the cap counts reading SMs
         const int n_max = static_cast<int>(std::min<long long>(std::min<long long>(hu, kDefaultHostCtas),
                                                                slots - (gu > 0 ? 1 : 0)));
@@ -1870,7 +1890,7 @@ static dak_status plan_block(int T, int h, int K_pad, long long tile_bytes, int 
     }
     tc.host_ctas = std::max(1, hc / CL);
     if (tc.hbm_ctas > 0) tc.hbm_ctas = std::max(1, tc.hbm_ctas / CL);
-    const Sched sc = schedule(h * q.P, (T - h) * q.P, std::max(1, (sms * per_sm) / CL), &tc,
+    const Sched sc = schedule(hb * q.P, gb * q.P, std::max(1, (sms * per_sm) / CL), &tc,
                               std::max(1, host_cap / CL), std::min(kDefaultHostWindow, q.ch[1].stages),
                               q.ch[0].stages, max_stages);
     q.n_host_ctas = sc.n_host_ctas;
@@ -1897,7 +1917,7 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
 
     BlockPlan bp;
     const dak_status r = plan_block(A->T, A->h, static_cast<int>(A->K_pad), A->tile_bytes, N, device_sm_count(), t,
-                                    ws != nullptr, ws_bytes, &bp);
+                                    ws != nullptr, ws_bytes, &bp, A->tile_m == 2 * kTileM);
     if (r != DAK_OK) return r;
     if (bp.grid == 0) return DAK_OK;
 
@@ -1914,6 +1934,9 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
     p.N_pad = bp.N_pad;
     p.T = A->T;
     p.h = A->h;
+    p.pairs = bp.pairs;
+    p.hb = blocks_of(p.h, p.pairs);
+    p.gb = blocks_of(p.T - p.h, p.pairs);
     p.c_fp32 = c_fp32 ? 1 : 0;
     p.tile_bytes = A->tile_bytes;
     p.glu = A->glu;
@@ -2024,9 +2047,10 @@ static dak_status plan_chain(const ChainOp* ops, int n, int N, int sms, const da
         const dak_placement* A = ops[j].A;
         if (!A || A->kind != 0 || A->T == 0) return DAK_ERR_INVALID;
         const dak_status r = plan_block(A->T, A->h, static_cast<int>(A->K_pad), A->tile_bytes, N, sms, t, false, 0,
-                                        &bps[j]);
+                                        &bps[j], A->tile_m == 2 * kTileM);
         if (r != DAK_OK) return r;
         const BlockPlan& b = bps[j];
+        if (b.pairs != bps[0].pairs) return DAK_ERR_UNSUPPORTED;  // one ring layout for every operation
         if (!b.umma || b.NC != 1 || b.kcb != b.ch[0].kc || b.ch[0].kc != b.ch[1].kc ||
             b.ch[0].stages != b.ch[1].stages || b.ch[0].stage_bytes != b.ch[1].stage_bytes)
             return DAK_ERR_UNSUPPORTED;
@@ -2037,7 +2061,7 @@ static dak_status plan_chain(const ChainOp* ops, int n, int N, int sms, const da
     }
     for (int j = 0; j < n; ++j) {
         part_off[j] = off;
-        if (bps[j].P > 1) off = align256(off + static_cast<long long>(ops[j].A->T) * bps[j].P * kTileM * bps[j].N_pad * 4);
+        if (bps[j].P > 1) off = align256(off + static_cast<long long>(ops[j].A->T + 2) * bps[j].P * kTileM * bps[j].N_pad * 4);
     }
     *need = off;
     return DAK_OK;
@@ -2092,6 +2116,9 @@ dak_status launch_gemm_chain(const ChainOp* ops, int n, int N, const dak_tuning*
         p.N_pad = bp.N_pad;
         p.T = A->T;
         p.h = A->h;
+        p.pairs = bp.pairs;
+        p.hb = blocks_of(p.h, p.pairs);
+        p.gb = blocks_of(p.T - p.h, p.pairs);
         p.c_fp32 = o.c_fp32 ? 1 : 0;
         p.tile_bytes = A->tile_bytes;
         p.glu = A->glu;
@@ -2161,20 +2188,23 @@ extern "C" dak_status dak_gemm(const dak_placement* A, const void* B, void* C, i
 
 extern "C" size_t dak_gemm_workspace_bytes(const dak_placement* A, int N) { return dak::gemm_workspace_bytes(A, N); }
 
-extern "C" dak_status dak_gemm_plan(int64_t M, int64_t K, int n_host_tiles, int N, int sm_count,
+extern "C" dak_status dak_gemm_plan(int64_t M, int64_t K, int tile_m, int n_host_tiles, int N, int sm_count,
                                     const dak_tuning* tuning, size_t ws_bytes, dak_gemm_plan_info* out) {
     if (!out) return DAK_ERR_INVALID;
     *out = dak_gemm_plan_info{};
     if (M < 1 || K < 8 || (K % 8) || K > (1 << 24) || M > (1ll << 31) || N < 1 || sm_count < 1) return DAK_ERR_INVALID;
+    if (tile_m != dak::kTileM && tile_m != 2 * dak::kTileM) return DAK_ERR_UNSUPPORTED;
     if (ws_bytes > 0 && static_cast<long long>(ws_bytes) < dak::kCallerCounterBytes) return DAK_ERR_INVALID;
-    const int T = static_cast<int>((M + dak::kTileM - 1) / dak::kTileM);
-    if (n_host_tiles < 0 || n_host_tiles > T) return DAK_ERR_INVALID;
+    const int tiles = static_cast<int>((M + tile_m - 1) / tile_m);
+    if (n_host_tiles < 0 || n_host_tiles > tiles) return DAK_ERR_INVALID;
+    const int per = tile_m / dak::kTileM;  // 64-row tile rows per tile
+    const int T = tiles * per;
     const int K_pad = static_cast<int>((K + 15) / 16 * 16);
     const long long tile_bytes = static_cast<long long>(dak::kTileM) * K_pad * 2;
     const int block = (tuning && tuning->column_blocks == 1) ? dak::kMaxBlockN : dak::kMaxWideN;
     dak::BlockPlan bp;
-    const dak_status r = dak::plan_block(T, n_host_tiles, K_pad, tile_bytes, std::min(N, block), sm_count, tuning,
-                                         ws_bytes > 0, ws_bytes, &bp);
+    const dak_status r = dak::plan_block(T, n_host_tiles * per, K_pad, tile_bytes, std::min(N, block), sm_count,
+                                         tuning, ws_bytes > 0, ws_bytes, &bp, per == 2);
     if (r != DAK_OK) return r;
     out->tensor_cores = bp.umma ? 1 : 0;
     out->launches = (N + block - 1) / block;
@@ -2191,6 +2221,7 @@ extern "C" dak_status dak_gemm_plan(int64_t M, int64_t K, int n_host_tiles, int 
     out->host_window = bp.host_window;
     out->hbm_window = bp.hbm_window;
     out->smem_bytes = bp.smem;
+    out->tile_m = bp.pairs ? 2 * dak::kTileM : dak::kTileM;
     return DAK_OK;
 }
 

@@ -221,12 +221,16 @@ Sched schedule(int host_units, int hbm_units, int sm_slots, const dak_tuning* t,
 // placement
 // ------------------------------------------------------------------------------------
 
-// Row-major A rows [rows][lda] (16-byte units of 8 bf16) -> tile rows stored
-// [K_pad/8][64][8]: unit (t, kg, r) at t*KG*64 + kg*64 + r. Rows past `rows` and
-// k-groups past K/8 are zero. With src_b set, packed row j comes from row j/2 of src
-// (j even) or of src_b (j odd): the gate/up interleave of a SwiGLU weight.
+// Row-major A rows [rows][lda] (16-byte units of 8 bf16) -> the tile rows of one tier,
+// tier-local tile rows l0, l0 + 1, ... (units / (KG * 64) of them). Tiles of 64 rows are
+// stored [K_pad/8][64][8]: unit (l, kg, r) at l*KG*64 + kg*64 + r. Tiles of 128 rows
+// (pairs) hold tile rows 2b and 2b + 1 of 64 as [K_pad/8][128][8]: unit (l, kg, r) at
+// (l - l%2)*KG*64 + kg*128 + (l%2)*64 + r. Rows past `rows` and k-groups past K/8 are zero.
+// With src_b set, packed row j comes from row j/2 of src (j even) or of src_b (j odd): the
+// gate/up interleave of a SwiGLU weight.
 __global__ void pack_matrix_kernel(const uint4* __restrict__ src, const uint4* __restrict__ src_b, long long lda16,
-                                   long long rows, int K16, int KG, uint4* __restrict__ dst, long long units) {
+                                   long long rows, int K16, int KG, uint4* __restrict__ tier, long long l0,
+                                   int pairs, long long units) {
     for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < units;
          idx += static_cast<long long>(gridDim.x) * blockDim.x) {
         const long long per_tile = static_cast<long long>(KG) * kTileM;
@@ -239,7 +243,10 @@ __global__ void pack_matrix_kernel(const uint4* __restrict__ src, const uint4* _
         if (row < rows && kg < K16) {
             v = src_b ? ((row & 1) ? src_b : src)[(row >> 1) * lda16 + kg] : src[row * lda16 + kg];
         }
-        dst[idx] = v;
+        const long long l = l0 + t;
+        const long long half = pairs ? (l & 1) : 0;
+        const int rows_kg = pairs ? 2 * kTileM : kTileM;  // rows of one k-group of the tile
+        tier[(l - half) * per_tile + static_cast<long long>(kg) * rows_kg + half * kTileM + r] = v;
     }
 }
 
@@ -326,11 +333,15 @@ static dak_status place_matrix(const void* A_src, int src_on_device, int64_t M, 
     *out = nullptr;
     if (M < 0 || K <= 0 || lda < K || (M > 0 && !A_src)) return DAK_ERR_INVALID;
     if (glu && (M % kTileM)) return DAK_ERR_INVALID;  // whole tiles of 32 gate + 32 up rows
-    if (tile_m != kTileM) return DAK_ERR_UNSUPPORTED;
+    if (tile_m != kTileM && tile_m != 2 * kTileM) return DAK_ERR_UNSUPPORTED;
     if ((K % 8) || (lda % 8) || (reinterpret_cast<uintptr_t>(A_src) & 15)) return DAK_ERR_ALIGN;
     if (K > (1 << 24) || M > (1ll << 31)) return DAK_ERR_INVALID;
-    const int T = static_cast<int>((M + kTileM - 1) / kTileM);
-    if (n_host_tiles < 0 || n_host_tiles > T) return DAK_ERR_INVALID;
+    // internally every tier is counted in tile rows of 64: a 128-row tile is two of them (the
+    // second all zero rows when the matrix ends in its first half)
+    const int per = tile_m / kTileM;
+    const int tiles = static_cast<int>((M + tile_m - 1) / tile_m);
+    if (n_host_tiles < 0 || n_host_tiles > tiles) return DAK_ERR_INVALID;
+    const int T = tiles * per;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return DAK_ERR_CUDA;
 
@@ -342,9 +353,9 @@ static dak_status place_matrix(const void* A_src, int src_on_device, int64_t M, 
     p->M = M;
     p->K = K;
     p->K_pad = (K + 15) / 16 * 16;
-    p->tile_m = kTileM;
+    p->tile_m = tile_m;
     p->T = T;
-    p->h = n_host_tiles;
+    p->h = n_host_tiles * per;
     p->tile_bytes = static_cast<int64_t>(kTileM) * p->K_pad * 2;
     p->host_bytes = p->tile_bytes * p->h;
     p->hbm_bytes = p->tile_bytes * (T - p->h);
@@ -375,7 +386,8 @@ static dak_status place_matrix(const void* A_src, int src_on_device, int64_t M, 
     for (int t0 = 0; t0 < T && e == cudaSuccess; t0 += batch_tiles) {
         const int nt = std::min(batch_tiles, T - t0);
         const long long row0 = static_cast<long long>(t0) * kTileM;
-        const long long rows = std::min<long long>(static_cast<long long>(nt) * kTileM, M - row0);
+        // (0 for a batch holding only the zero second half of the last 128-row tile)
+        const long long rows = std::max(0ll, std::min<long long>(static_cast<long long>(nt) * kTileM, M - row0));
         const uint8_t* a8 = static_cast<const uint8_t*>(A_src);
         const uint4* src;
         const uint4* src_b = nullptr;  // glu: the up rows (src: the gate rows)
@@ -407,14 +419,14 @@ static dak_status place_matrix(const void* A_src, int src_on_device, int64_t M, 
             if (hi <= lo) continue;
             uint8_t* base = static_cast<uint8_t*>(tier == 0 ? p->host_dev : p->hbm_ptr);
             const int first = tier == 0 ? 0 : p->h;  // first tile row stored in this tier
-            uint4* dst = reinterpret_cast<uint4*>(base + static_cast<long long>(lo - first) * p->tile_bytes);
             const long long units = static_cast<long long>(hi - lo) * KG * kTileM;
             const long long src_row0 = static_cast<long long>(lo - t0) * kTileM;
             const long long src_rows = std::max(0ll, rows - src_row0);
             // glu: packed row j of this part reads row j/2 of the gate or up block
             const long long off = glu ? (src_row0 / 2) * lda16 : src_row0 * lda16;
             pack_matrix_kernel<<<pack_grid(units), 256>>>(src + off, src_b ? src_b + off : nullptr, lda16, src_rows,
-                                                          K16, KG, dst, units);
+                                                          K16, KG, reinterpret_cast<uint4*>(base), lo - first,
+                                                          per == 2 ? 1 : 0, units);
             e = cudaGetLastError();
         }
         if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -565,8 +577,9 @@ extern "C" dak_status dak_placement_info(const dak_placement* p, int64_t* host_b
     if (!p) return DAK_ERR_INVALID;
     if (host_bytes) *host_bytes = p->host_bytes;
     if (hbm_bytes) *hbm_bytes = p->hbm_bytes;
-    if (units) *units = p->kind == 0 ? p->T : p->B;
-    if (host_units) *host_units = p->kind == 0 ? p->h : p->h_r;
+    const int per = (p->kind == 0 && p->tile_m > kTileM) ? p->tile_m / kTileM : 1;  // tiles, not 64-row rows
+    if (units) *units = p->kind == 0 ? p->T / per : p->B;
+    if (host_units) *host_units = p->kind == 0 ? p->h / per : p->h_r;
     return DAK_OK;
 }
 

@@ -110,12 +110,17 @@ typedef struct {
  * the remaining ceil(M/tile_m) - n_host_tiles rows to HBM.
  *   A_src        : source data; host memory if src_on_device == 0, else device memory.
  *                  Read once; the caller keeps ownership.
- *   tile_m       : 64 (the only tile height implemented).
- *   n_host_tiles : 0 .. ceil(M/64); the caller turns a ratio x into tiles (the library's
+ *   tile_m       : 64 or 128 (else DAK_ERR_UNSUPPORTED). A tile is the unit of placement and
+ *                  of work: 64-row tiles run M = 64 tcgen05 MMAs and spread finer over the
+ *                  SMs (decode-sized N); 128-row tiles run M = 128 MMAs, about 1.7x the
+ *                  tensor throughput per SM, for tensor-bound N (measured on the 8B
+ *                  gate+up: 1.3x faster at N = 256, 1.75x at N = 512, all in HBM).
+ *   n_host_tiles : 0 .. ceil(M/tile_m); the caller turns a ratio x into tiles (the library's
  *                  own reading is ceil(x * T)).
  * Requirements: K % 8 == 0, lda % 8 == 0, A_src 16-byte aligned (else DAK_ERR_ALIGN).
- * Internally each tier stores its tile rows in a k-group-major layout (8 x 8 core
- * blocks) that the kernels copy into shared memory with single bulk copies.
+ * Internally each tier stores its tiles in a k-group-major layout ([K/8][tile_m][8]: 8 x 8
+ * core blocks) that the kernels copy into shared memory with single bulk copies; a
+ * 128-row tile that ends past M holds zero rows there.
  * On success *out holds a new placement (free with dak_free). Synchronous. */
 dak_status dak_place_matrix(const void* A_src, int src_on_device, int64_t M, int64_t K, int64_t lda,
                             int tile_m, int n_host_tiles, dak_placement** out);
@@ -141,8 +146,8 @@ dak_status dak_place_kv(const void* K_src, const void* V_src, int src_on_device,
 /* Release a placement (host and HBM parts). NULL is accepted. */
 dak_status dak_free(dak_placement* p);
 
-/* Sizes of a placement: bytes in host memory and in HBM, number of units (tile rows or
- * requests) and how many are on the host. Any output pointer may be NULL. */
+/* Sizes of a placement: bytes in host memory and in HBM, number of units (tiles of tile_m
+ * rows, or requests) and how many are on the host. Any output pointer may be NULL. */
 dak_status dak_placement_info(const dak_placement* p, int64_t* host_bytes, int64_t* hbm_bytes, int64_t* units,
                               int64_t* host_units);
 
@@ -187,12 +192,14 @@ dak_status dak_gemm_ws(const dak_placement* A, const void* B, void* C, int N, in
                        void* workspace, size_t ws_bytes, void* stream);
 
 /* The launch dak_gemm (ws_bytes == 0) or dak_gemm_ws (a workspace of ws_bytes) would make
- * for an M x K matrix with n_host_tiles of its 64-row tile rows on the host, N hidden-state
- * rows and the tuning, on a GPU of sm_count SMs. Host arithmetic only: it needs no GPU and
- * launches nothing. With more rows than one launch takes, the fields describe the first
- * launch. DAK_ERR_INVALID: M < 1, K not a positive multiple of 8, n_host_tiles outside
- * [0, ceil(M / 64)], N < 1, sm_count < 1, a non-zero ws_bytes below 256 KiB, or a tuning
- * that leaves no valid ring (e.g. chunk_k not a multiple of 64). */
+ * for an M x K matrix placed in tiles of tile_m rows (64 or 128) with n_host_tiles of them
+ * on the host, N hidden-state rows and the tuning, on a GPU of sm_count SMs. Host
+ * arithmetic only: it needs no GPU and launches nothing. With more rows than one launch
+ * takes, the fields describe the first launch. DAK_ERR_INVALID: M < 1, K not a positive
+ * multiple of 8, n_host_tiles outside [0, ceil(M / tile_m)], N < 1, sm_count < 1, a non-zero
+ * ws_bytes below 256 KiB, or a tuning that leaves no valid ring (e.g. chunk_k not a multiple
+ * of 64); DAK_ERR_UNSUPPORTED: another tile_m. Pieces count along the K range of one tile
+ * (tile_m rows). */
 typedef struct {
     int tensor_cores;  /* 1: tcgen05 (N >= 2); 0: CUDA-core FMA (N == 1) */
     int launches;      /* launches (column blocks of hidden-state rows) of the call */
@@ -209,9 +216,10 @@ typedef struct {
     int host_window;   /* stages in flight per host CTA (congestion window) */
     int hbm_window;    /* stages in flight per HBM CTA */
     int smem_bytes;    /* dynamic shared memory per CTA */
+    int tile_m;        /* tile height of the placement: 64, or 128 (M = 128 MMAs) */
 } dak_gemm_plan_info;
-dak_status dak_gemm_plan(int64_t M, int64_t K, int n_host_tiles, int N, int sm_count, const dak_tuning* tuning,
-                         size_t ws_bytes, dak_gemm_plan_info* out);
+dak_status dak_gemm_plan(int64_t M, int64_t K, int tile_m, int n_host_tiles, int N, int sm_count,
+                         const dak_tuning* tuning, size_t ws_bytes, dak_gemm_plan_info* out);
 
 /* A chain of GEMMs C_j = A_j x B_j in one persistent launch, for 2 <= N <= 128 hidden-state
  * rows (tensor-core path). The paper launches one kernel per nn.Linear (section 5); here the

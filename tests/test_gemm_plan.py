@@ -66,9 +66,10 @@ def test_caller_workspace_bounds_pieces():
     M, K = LINEARS_8B["down"]
     full = plan(M, K, 0, 16)
     assert full["pieces"] == 7
-    assert plan(M, K, 0, 16, ws_bytes=(256 << 10) + 64 * 64 * 16 * 4 * 7)["pieces"] == 7
+    # the partials of 7 pieces: room for T + 2 = 66 tile rows of 64 x 16 fp32 each
+    assert plan(M, K, 0, 16, ws_bytes=(256 << 10) + 66 * 64 * 16 * 4 * 7)["pieces"] == 7
     # room for fewer partial tiles than 7 pieces of 64 tile rows need: fewer pieces
-    small = plan(M, K, 0, 16, ws_bytes=(256 << 10) + 64 * 64 * 16 * 4 * 3)
+    small = plan(M, K, 0, 16, ws_bytes=(256 << 10) + 66 * 64 * 16 * 4 * 3)
     assert 1 <= small["pieces"] <= 3
 
 
@@ -106,10 +107,12 @@ def _waves(units, ctas):
     return -(-units // ctas)
 
 
-def _check_invariants(M, K, h, N, sms, tuning=None):
-    p = plan(M, K, h, N, sms=sms, tuning=tuning)
-    T = -(-M // 64)
+def _check_invariants(M, K, h, N, sms, tuning=None, tile_m=64):
+    p = plan(M, K, h, N, sms=sms, tuning=tuning, tile_m=tile_m)
+    assert p["tile_m"] == tile_m
+    T = -(-M // tile_m)
     P, cl = p["pieces"], p["cluster"]
+    # a unit is a piece of one tile (64 or 128 rows)
     hu, mu = h * P, (T - h) * P
     assert (p["host_ctas"] > 0) == (hu > 0)
     assert (p["hbm_ctas"] > 0) == (mu > 0)
@@ -133,20 +136,23 @@ def test_invariants_random_shapes():
         M = rng.choice([64, 100, 1000, 4096, 6144, 14336, 28672]) * rng.choice([1, 1, 2])
         K = 8 * rng.randint(1, 4096)
         N = rng.choice([1, 2, 5, 8, 16, 24, 32, 48, 64, 96, 128, 200, 256, 300, 512, 1024])
-        T = -(-M // 64)
+        tile_m = rng.choice([64, 64, 128])
+        T = -(-M // tile_m)
         h = rng.randint(0, T)
         sms = rng.choice([132, 148, 152, 160])
         tun = rng.choice([None, {"no_wave_align": 1}, {"host_ctas": 16}, {"split_k": rng.randint(1, 8)}])
-        _check_invariants(M, K, h, N, sms, tun)
+        _check_invariants(M, K, h, N, sms, tun, tile_m)
 
 
-@pytest.mark.parametrize("N", [1, 8, 16, 32, 64, 128])
-def test_pieces_do_not_depend_on_placement(N):
+@pytest.mark.parametrize("tile_m", [64, 128])
+@pytest.mark.parametrize("N", [1, 8, 16, 32, 64, 128, 256])
+def test_pieces_do_not_depend_on_placement(N, tile_m):
     # the pieces, and so the order of every tile row's fp32 sum, come from the shape and the
     # SM count alone: the result is bit-identical at every offload ratio
     for (M, K) in itertools.chain(LINEARS_8B.values(), [(1000, 1032), (64, 8), (640, 20000)]):
-        T = -(-M // 64)
-        ps = {plan(M, K, h, N)["pieces"] for h in sorted({0, 1, T // 3, T // 2, T - 1, T})}
+        T = -(-M // tile_m)
+        ps = {(plan(M, K, h, N, tile_m=tile_m)["pieces"], plan(M, K, h, N, tile_m=tile_m)["n_pad"])
+              for h in sorted({0, 1, T // 3, T // 2, T - 1, T})}
         assert len(ps) == 1, (M, K, N, ps)
 
 

@@ -29,7 +29,7 @@ EXPORTS = [
     "dak_gemm_staged", "dak_attn_staged", "dak_attn_noalloc", "dak_selftest_wait",
     "dak_decoder_create", "dak_decoder_batch", "dak_decoder_step", "dak_decoder_capture",
     "dak_decoder_replay", "dak_decoder_launches", "dak_decoder_free", "dak_tune_gemm", "dak_tune_attn",
-    "dak_place_matrix_glu", "dak_plan_units", "dak_gemm_workspace_bytes", "dak_gemm_ws", "dak_gemm_plan",
+    "dak_place_matrix_glu", "dak_plan_units", "dak_gemm_workspace_bytes", "dak_gemm_ws", "dak_gemm_plan", "dak_gemm_launch_plan",
     "dak_attn_f32", "dak_inject_fault", "dak_fault_pending", "dak_alloc_counts", "dak_gemm_chain",
     "dak_gemm_chain_workspace_bytes",
 ]
@@ -51,7 +51,7 @@ class dak_tuning(ctypes.Structure):
     _fields_ = [("host_ctas", ctypes.c_int), ("window", ctypes.c_int), ("hbm_window", ctypes.c_int),
                 ("chunk_k", ctypes.c_int), ("n_split", ctypes.c_int), ("hbm_ctas", ctypes.c_int),
                 ("split_k", ctypes.c_int), ("pdl", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
-                ("no_wave_align", ctypes.c_int), ("column_blocks", ctypes.c_int)]
+                ("no_wave_align", ctypes.c_int), ("column_blocks", ctypes.c_int), ("cluster_slots", ctypes.c_int)]
 
 
 class dak_gemm_op(ctypes.Structure):
@@ -72,7 +72,7 @@ class dak_gemm_plan_info(ctypes.Structure):
     _fields_ = [(f, ctypes.c_int) for f in (
         "tensor_cores", "launches", "cluster", "n_pad", "pieces", "piece_step", "chunk_k", "host_chunk_k",
         "hbm_stages", "host_stages", "host_ctas", "hbm_ctas", "host_window", "hbm_window", "smem_bytes",
-        "tile_m")]
+        "tile_m", "cluster_slots")]
 
 
 class dak_decoder_config(ctypes.Structure):
@@ -107,6 +107,7 @@ def _load():
         "dak_gemm_workspace_bytes": (sz, [vp, i32]),
         "dak_gemm_ws": (i32, [vp, vp, vp, i32, i32, P(dak_tuning), vp, sz, vp]),
         "dak_gemm_plan": (i32, [i64, i64, i32, i32, i32, i32, P(dak_tuning), sz, P(dak_gemm_plan_info)]),
+        "dak_gemm_launch_plan": (i32, [vp, i32, P(dak_tuning), sz, P(dak_gemm_plan_info)]),
         "dak_gemm_chain_workspace_bytes": (sz, [P(dak_gemm_op), i32, i32, P(dak_tuning)]),
         "dak_gemm_chain": (i32, [P(dak_gemm_op), i32, i32, P(dak_tuning), vp, sz, vp]),
         "dak_attn_workspace_bytes": (sz, [i32, i32, i32, i32]),
@@ -365,6 +366,14 @@ def dak_gemm_plan(M: int, K: int, n_host_tiles: int, N: int, sm_count: int = Non
     out = dak_gemm_plan_info()
     _check(lib.dak_gemm_plan(int(M), int(K), int(tile_m), int(n_host_tiles), int(N), int(sm_count), _tuning(tuning),
                              ctypes.c_size_t(int(ws_bytes)), ctypes.byref(out)), "dak_gemm_plan")
+    return {f: int(getattr(out, f)) for f, _ in dak_gemm_plan_info._fields_}
+
+
+def dak_gemm_launch_plan(A: Placement, N: int, tuning=None, ws_bytes: int = 0) -> dict:
+    """The plan dak_gemm would use for placement A and N rows on this process's GPU."""
+    out = dak_gemm_plan_info()
+    _check(lib.dak_gemm_launch_plan(A.handle, int(N), _tuning(tuning), ctypes.c_size_t(int(ws_bytes)),
+                                    ctypes.byref(out)), "dak_gemm_launch_plan")
     return {f: int(getattr(out, f)) for f, _ in dak_gemm_plan_info._fields_}
 
 

@@ -29,6 +29,7 @@
 #include <atomic>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "dak_device.cuh"
 
@@ -1590,6 +1591,53 @@ static cudaError_t launch_ex(Kernel k, int grid, int threads, int smem, int clus
     return cudaLaunchKernelEx(&cfg, k, args...);
 }
 
+// Clusters of `cluster` CTAs of kernel k (threads, smem) that the device holds at once: a
+// cluster's CTAs share a GPC, so clusters of 4 leave the SMs of a GPC beyond a multiple of 4
+// idle and fewer than sms / 4 fit. A persistent grid sized for more clusters than fit runs
+// the extra ones after the others, a whole tail. Cached per device and shape; 0 when the
+// query fails (the caller then assumes sms / cluster).
+template <typename Kernel>
+static int max_active_clusters(Kernel k, int threads, int smem, int cluster) {
+    struct Key {
+        int dev, threads, smem, cluster;
+        const void* fn;
+    };
+    static std::mutex mu;
+    static std::vector<std::pair<Key, int>> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const Key key{dev, threads, smem, cluster, reinterpret_cast<const void*>(k)};
+    std::lock_guard<std::mutex> lock(mu);
+    for (const auto& e : cache) {
+        const Key& c = e.first;
+        if (c.dev == key.dev && c.threads == key.threads && c.smem == key.smem && c.cluster == key.cluster &&
+            c.fn == key.fn)
+            return e.second;
+    }
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(cluster * 64));
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+    }
+    cache.push_back({key, n});
+    return n;
+}
+
 // Workspace of split tile rows: fp32 partial tiles and one counter per tile row, in device
 // memory that the module owns (no allocation at launch time, so launches can be captured in
 // CUDA graphs). Launches on one stream use it in turn (the partials and counters are touched
@@ -1653,6 +1701,12 @@ constexpr double kCtaStreamBytesPerUs = 62.5e3;
 constexpr double kSmTensorFlopsPerUs = 3.76e6;
 constexpr double kHostLinkBytesPerUs = 2.1e5;
 constexpr double kHostCtaBytesPerUs = 1.3e4;  // a host CTA through tensor-bound tile rows (fitted: 512 KiB in ~40 us)
+// The same two rates for 128-row tiles (M = 128 MMAs), fitted to the 8B gate+up at N = 1024
+// in 128-row tiles: 224 tiles in 7 waves of 32 clusters took 234 us all-HBM (33 us per
+// M = 128 x N = 256 x K = 4096 unit), and at x = 0.25 a host cluster took ~96 us per 1 MiB
+// tile while the link was not yet full.
+constexpr double kSmTensorFlopsPerUs128 = 8.1e6;
+constexpr double kHostCtaBytesPerUs128 = 1.09e4;
 
 static int split_pieces(int T, int K_pad, int N_pad, int slots, long long tile_bytes, int host_cap, int pstep,
                         double piece_us, long long max_tiles, long long max_floats, const dak_tuning* t, int rows) {
@@ -1709,7 +1763,8 @@ void reset_split_counters() {
 // call), so that dak_gemm_plan can report it without a GPU.
 struct BlockPlan {
     bool umma;
-    int pairs;  // HBM tier in pair blocks (M = 128)
+    int pairs;  // 128-row tiles: pair blocks (M = 128)
+    int cl_slots;  // clusters (of NC CTAs) the schedule assumes the device holds at once
     int NC, N_pad, P, pstep, kcb, kcb_host, smem, grid;  // kcb / kcb_host: B chunk width of each role's map
     Chunks ch[2];  // [0] HBM-side CTAs, [1] host-side CTAs
     int n_host_ctas, n_hbm_ctas, host_window, hbm_window;
@@ -1720,7 +1775,7 @@ struct BlockPlan {
 // caller's workspace of ws_bytes; pairs: a placement of 128-row tiles (T and h even), whose
 // blocks of two tile rows are the units of work.
 static dak_status plan_block(int T, int h, int K_pad, long long tile_bytes, int N, int sms, const dak_tuning* t,
-                             bool caller_ws, size_t ws_bytes, BlockPlan* bp, int pairs) {
+                             bool caller_ws, size_t ws_bytes, BlockPlan* bp, int pairs, int cluster_slots = 0) {
     if (N < 1 || N > kMaxWideN || sms < 1) return DAK_ERR_INVALID;
     BlockPlan& q = *bp;
     q = BlockPlan{};
@@ -1844,7 +1899,11 @@ static dak_status plan_block(int T, int h, int K_pad, long long tile_bytes, int 
                            kSplitTiles, max_floats, t, q.pairs ? 2 : 1);
     }
 
-    // schedule in cluster units; a role's units are its tile rows x P pieces
+    // schedule in cluster units; a role's units are its tile rows x P pieces; cluster_slots
+    // (when known): the clusters the device holds at once
+    const int cs = (t && t->cluster_slots > 0) ? t->cluster_slots : cluster_slots;
+    const int cl_slots = std::max(1, (CL > 1 && cs > 0) ? std::min(cs, (sms * per_sm) / CL) : (sms * per_sm) / CL);
+    q.cl_slots = cl_slots;
     dak_tuning tc{};
     if (t) tc = *t;
     const int host_cap = NC > 1 ? kDefaultHostCtasWide : kDefaultHostCtas;
@@ -1863,14 +1922,15 @@ static dak_status plan_block(int T, int h, int K_pad, long long tile_bytes, int 
     // so the flat segment of Fig. 6 ends before x = B_host T_comp / C. Memory-bound tile rows
     // keep the fixed cap above.
     if (q.N_pad >= 256 && h > 0 && !(t && t->host_ctas > 0)) {
-        // a unit is a block's piece; the M = 128 MMAs of a pair block take about as long as one
-        // tile row's M = 64 ones at N >= 128 (measured)
+        // a unit is a block's piece: one 64-row tile row (M = 64 MMAs) or a 128-row tile
+        // (M = 128 MMAs, about twice the rate per SM)
         const double unit_bytes = (q.pairs ? 2.0 : 1.0) * static_cast<double>(tile_bytes) / q.P;
-        const double t_mma = 2.0 * kTileM * q.N_pad * (static_cast<double>(K_pad) / q.P) / kSmTensorFlopsPerUs;
+        const double t_mma = (q.pairs ? 2.0 : 1.0) * 2.0 * kTileM * q.N_pad * (static_cast<double>(K_pad) / q.P) /
+                             (q.pairs ? kSmTensorFlopsPerUs128 : kSmTensorFlopsPerUs);
         const double t_unit = std::max(t_mma, unit_bytes / kCtaStreamBytesPerUs);
-        const double t_host_unit = std::max(t_unit, unit_bytes / kHostCtaBytesPerUs);
+        const double t_host_unit = std::max(t_unit, unit_bytes / (q.pairs ? kHostCtaBytesPerUs128 : kHostCtaBytesPerUs));
         const double t_link = static_cast<double>(h) * tile_bytes / kHostLinkBytesPerUs;
-        const int slots = std::max(1, (sms * per_sm) / CL);
+        const int slots = cl_slots;
         const long long hu = static_cast<long long>(hb) * q.P, gu = static_cast<long long>(gb) * q.P;
         // one SM of a host cluster reads the link (rank 0 forwards): the cap counts reading SMs
         const int n_max = static_cast<int>(std::min<long long>(std::min<long long>(hu, kDefaultHostCtas),
@@ -1890,7 +1950,7 @@ static dak_status plan_block(int T, int h, int K_pad, long long tile_bytes, int 
     }
     tc.host_ctas = std::max(1, hc / CL);
     if (tc.hbm_ctas > 0) tc.hbm_ctas = std::max(1, tc.hbm_ctas / CL);
-    const Sched sc = schedule(hb * q.P, gb * q.P, std::max(1, (sms * per_sm) / CL), &tc,
+    const Sched sc = schedule(hb * q.P, gb * q.P, cl_slots, &tc,
                               std::max(1, host_cap / CL), std::min(kDefaultHostWindow, q.ch[1].stages),
                               q.ch[0].stages, max_stages);
     q.n_host_ctas = sc.n_host_ctas;
@@ -1899,6 +1959,23 @@ static dak_status plan_block(int T, int h, int K_pad, long long tile_bytes, int 
     q.hbm_window = std::min(sc.hbm_window, q.ch[0].stages);
     q.grid = (q.n_host_ctas + q.n_hbm_ctas) * CL;
     return DAK_OK;
+}
+
+// The plan of one launch over placement A on the current device: plan_block, with the
+// persistent grid of a cluster launch sized to the clusters that fit at once (unless the
+// tuning fixes cluster_slots).
+static dak_status plan_launch(const dak_placement* A, int N, const dak_tuning* t, bool caller_ws, size_t ws_bytes,
+                              BlockPlan* bp) {
+    const int sms = device_sm_count();
+    const int pairs = A->tile_m == 2 * kTileM;
+    dak_status r = plan_block(A->T, A->h, static_cast<int>(A->K_pad), A->tile_bytes, N, sms, t, caller_ws, ws_bytes,
+                              bp, pairs);
+    if (r != DAK_OK || bp->NC == 1 || (t && t->cluster_slots > 0)) return r;
+    const int fit = max_active_clusters(gemm_umma_kernel<false>, kUmmaThreads, bp->smem, bp->NC);
+    if (fit > 0 && fit < sms / bp->NC)
+        r = plan_block(A->T, A->h, static_cast<int>(A->K_pad), A->tile_bytes, N, sms, t, caller_ws, ws_bytes, bp,
+                       pairs, fit);
+    return r;
 }
 
 // One launch over up to kMaxWideN hidden-state rows: one CTA per tile row up to 256 rows
@@ -1916,8 +1993,7 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
     if (dev != A->device) return DAK_ERR_INVALID;
 
     BlockPlan bp;
-    const dak_status r = plan_block(A->T, A->h, static_cast<int>(A->K_pad), A->tile_bytes, N, device_sm_count(), t,
-                                    ws != nullptr, ws_bytes, &bp, A->tile_m == 2 * kTileM);
+    const dak_status r = plan_launch(A, N, t, ws != nullptr, ws_bytes, &bp);
     if (r != DAK_OK) return r;
     if (bp.grid == 0) return DAK_OK;
 
@@ -2188,6 +2264,26 @@ extern "C" dak_status dak_gemm(const dak_placement* A, const void* B, void* C, i
 
 extern "C" size_t dak_gemm_workspace_bytes(const dak_placement* A, int N) { return dak::gemm_workspace_bytes(A, N); }
 
+static void fill_plan_info(const dak::BlockPlan& bp, int N, int block, dak_gemm_plan_info* out) {
+    out->tensor_cores = bp.umma ? 1 : 0;
+    out->launches = (N + block - 1) / block;
+    out->cluster = bp.NC;
+    out->n_pad = bp.N_pad;
+    out->pieces = bp.P;
+    out->piece_step = bp.pstep;
+    out->chunk_k = bp.ch[0].kc;
+    out->host_chunk_k = bp.ch[1].kc;
+    out->hbm_stages = bp.ch[0].stages;
+    out->host_stages = bp.ch[1].stages;
+    out->host_ctas = bp.n_host_ctas * bp.NC;
+    out->hbm_ctas = bp.n_hbm_ctas * bp.NC;
+    out->host_window = bp.host_window;
+    out->hbm_window = bp.hbm_window;
+    out->smem_bytes = bp.smem;
+    out->tile_m = bp.pairs ? 2 * dak::kTileM : dak::kTileM;
+    out->cluster_slots = bp.cl_slots;
+}
+
 extern "C" dak_status dak_gemm_plan(int64_t M, int64_t K, int tile_m, int n_host_tiles, int N, int sm_count,
                                     const dak_tuning* tuning, size_t ws_bytes, dak_gemm_plan_info* out) {
     if (!out) return DAK_ERR_INVALID;
@@ -2206,22 +2302,23 @@ extern "C" dak_status dak_gemm_plan(int64_t M, int64_t K, int tile_m, int n_host
     const dak_status r = dak::plan_block(T, n_host_tiles * per, K_pad, tile_bytes, std::min(N, block), sm_count,
                                          tuning, ws_bytes > 0, ws_bytes, &bp, per == 2);
     if (r != DAK_OK) return r;
-    out->tensor_cores = bp.umma ? 1 : 0;
-    out->launches = (N + block - 1) / block;
-    out->cluster = bp.NC;
-    out->n_pad = bp.N_pad;
-    out->pieces = bp.P;
-    out->piece_step = bp.pstep;
-    out->chunk_k = bp.ch[0].kc;
-    out->host_chunk_k = bp.ch[1].kc;
-    out->hbm_stages = bp.ch[0].stages;
-    out->host_stages = bp.ch[1].stages;
-    out->host_ctas = bp.n_host_ctas * bp.NC;
-    out->hbm_ctas = bp.n_hbm_ctas * bp.NC;
-    out->host_window = bp.host_window;
-    out->hbm_window = bp.hbm_window;
-    out->smem_bytes = bp.smem;
-    out->tile_m = bp.pairs ? 2 * dak::kTileM : dak::kTileM;
+    fill_plan_info(bp, N, block, out);
+    return DAK_OK;
+}
+
+extern "C" dak_status dak_gemm_launch_plan(const dak_placement* A, int N, const dak_tuning* tuning, size_t ws_bytes,
+                                           dak_gemm_plan_info* out) {
+    if (!A || !out || A->kind != 0 || N < 1) return DAK_ERR_INVALID;
+    *out = dak_gemm_plan_info{};
+    if (ws_bytes > 0 && static_cast<long long>(ws_bytes) < dak::kCallerCounterBytes) return DAK_ERR_INVALID;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DAK_ERR_CUDA;
+    if (dev != A->device) return DAK_ERR_INVALID;
+    const int block = (tuning && tuning->column_blocks == 1) ? dak::kMaxBlockN : dak::kMaxWideN;
+    dak::BlockPlan bp;
+    const dak_status r = dak::plan_launch(A, std::min(N, block), tuning, ws_bytes > 0, ws_bytes, &bp);
+    if (r != DAK_OK) return r;
+    fill_plan_info(bp, N, block, out);
     return DAK_OK;
 }
 

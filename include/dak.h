@@ -85,6 +85,10 @@ typedef struct dak_placement dak_placement;
  *               host tiles again (host-link bytes = host bytes x ceil(N/256)). Like chunk_k
  *               it may change the summation order of the last, partial block (never with
  *               the offload ratio).
+ *   cluster_slots: dak_gemm with N > 256: clusters the schedule assumes the GPU holds at
+ *               once. 0 = asked of the device at launch (a cluster's CTAs share a GPC, so
+ *               fewer clusters of 4 fit than SMs / 4; a persistent grid sized past that runs
+ *               its extra clusters as a tail); dak_gemm_plan assumes sm_count / cluster.
  */
 typedef struct {
     int host_ctas;
@@ -98,6 +102,7 @@ typedef struct {
     int ctas_per_sm;
     int no_wave_align;
     int column_blocks;
+    int cluster_slots;
 } dak_tuning;
 
 /* ---------------------------------------------------------------------------------- *
@@ -217,9 +222,18 @@ typedef struct {
     int hbm_window;    /* stages in flight per HBM CTA */
     int smem_bytes;    /* dynamic shared memory per CTA */
     int tile_m;        /* tile height of the placement: 64, or 128 (M = 128 MMAs) */
+    int cluster_slots; /* clusters (or CTAs, cluster == 1) the schedule counts as held at once */
 } dak_gemm_plan_info;
 dak_status dak_gemm_plan(int64_t M, int64_t K, int tile_m, int n_host_tiles, int N, int sm_count,
                          const dak_tuning* tuning, size_t ws_bytes, dak_gemm_plan_info* out);
+
+/* The plan dak_gemm (ws_bytes == 0) or dak_gemm_ws would use for placement A and N
+ * hidden-state rows on the current device: dak_gemm_plan's arithmetic with the device's SM
+ * count and, for cluster launches, the clusters the device holds at once. Launches
+ * nothing. DAK_ERR_INVALID: A not a matrix placement of this device, N < 1, ws_bytes below
+ * 256 KiB but non-zero. */
+dak_status dak_gemm_launch_plan(const dak_placement* A, int N, const dak_tuning* tuning, size_t ws_bytes,
+                                dak_gemm_plan_info* out);
 
 /* A chain of GEMMs C_j = A_j x B_j in one persistent launch, for 2 <= N <= 128 hidden-state
  * rows (tensor-core path). The paper launches one kernel per nn.Linear (section 5); here the

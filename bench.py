@@ -401,9 +401,10 @@ def _time_fn(fn, reps=20, warmup=3):
 def run_planner_check(dak, lin, attn, b_host, b_hbm, dev, x_global=0.1):
     """The planner outside the all-memory-bound regime ([DAK] section 4.2, Fig. 6 and 11):
     (1) t(x) of the 8B gate+up linear at N = 256 against the model max(T_c, (1-x)C/B_hbm,
-    xC/B_host) with T_c its measured all-HBM time; (2) one step of the four linears at
-    N = 256 plus the 32-request attention, placed by the greedy planner and uniformly at
-    the same x_global, both timed."""
+    xC/B_host) with T_c its measured all-HBM time, in 128-row tiles (and 64-row ones); (2)
+    one step of the four linears at N = 256 (each in the tile height that runs it faster all
+    in HBM) plus the 32-request attention, placed by the greedy planner and uniformly at the
+    same x_global, both timed."""
     import math
     import numpy as np
     import torch
@@ -418,25 +419,34 @@ def run_planner_check(dak, lin, attn, b_host, b_hbm, dev, x_global=0.1):
         Cs[name] = torch.empty((N, A.shape[0]), dtype=torch.bfloat16, device=dev)
     gt = dict(pdl=1)
 
-    # (1) flat segment of a tensor-bound operation
+    # (1) flat segment of a tensor-bound operation, in 128-row tiles (M = 128 MMAs, the
+    # placement for tensor-bound N) and, for comparison, in 64-row tiles
     A = lin["gate_up"][0]
     M, K = A.shape
     C = M * K * 2
-    curve = []
-    t0 = None
-    for x in (0.0, 0.02, 0.04, 0.06, 0.08, 0.12, 0.2):
-        p = dak.dak_place_matrix(A, dak.host_tiles_for_ratio(x, M))
-        t = _time_fn(lambda: dak.dak_gemm(p, Bs["gate_up"], Cs["gate_up"], tuning=gt))
-        xe = p.host_bytes / C
-        if t0 is None:
-            t0 = t
-        curve.append({"x": xe, "us": t * 1e6,
-                      "model_us": 1e6 * max(t0, (1 - xe) * C / b_hbm, xe * C / b_host)})
-        p.free()
+
+    def curve_of(tile_m):
+        curve, t0 = [], None
+        for x in (0.0, 0.02, 0.04, 0.06, 0.08, 0.12, 0.2):
+            p = dak.dak_place_matrix(A, dak.host_tiles_for_ratio(x, M, tile_m), tile_m=tile_m)
+            t = _time_fn(lambda: dak.dak_gemm(p, Bs["gate_up"], Cs["gate_up"], tuning=gt))
+            xe = p.host_bytes / C
+            if t0 is None:
+                t0 = t
+            model = max(t0, (1 - xe) * C / b_hbm, xe * C / b_host)
+            curve.append({"x": xe, "us": t * 1e6, "model_us": 1e6 * model, "vs_model": t / model})
+            p.free()
+        return curve, t0
+
+    curve, t0 = curve_of(128)
+    res["gate_up_tile_m"] = 128
     res["gate_up_curve"] = curve
     res["gate_up_t_comp_us"] = t0 * 1e6
     res["gate_up_memory_us"] = C / b_hbm * 1e6
     res["gate_up_flat_until_x"] = t0 * b_host / C
+    curve64, t064 = curve_of(64)
+    res["gate_up_curve_tile64"] = curve64
+    res["gate_up_t_comp_us_tile64"] = t064 * 1e6
 
     # (2) greedy vs uniform on a mixed step
     q, k, v = attn
@@ -450,6 +460,7 @@ def run_planner_check(dak, lin, attn, b_host, b_hbm, dev, x_global=0.1):
     P = pk.get("bf16_tflops_sustained", 1700.0) * 1e12
     ops, units = [], []
     pl0 = {}
+    tile_ms = {}
     for name in names:
         if name == "attn":
             pl0[name] = dak.dak_place_kv(k, v, 0)
@@ -462,13 +473,25 @@ def run_planner_check(dak, lin, attn, b_host, b_hbm, dev, x_global=0.1):
             ops.append((nb, t if t > 1.15 * nb / b_hbm else flops / P, kv_req))
             units.append(k.shape[0])
         else:
+            # each linear in the tile height that runs it faster all in HBM (128-row tiles
+            # when it is tensor-bound with many tiles, else 64)
             A = lin[name][0]
-            pl0[name] = dak.dak_place_matrix(A, 0)
+            best = None
+            for tm in (64, 128):
+                pt = dak.dak_place_matrix(A, 0, tile_m=tm)
+                t = _time_fn(lambda: dak.dak_gemm(pt, Bs[name], Cs[name], tuning=gt))
+                if best is None or t < best[1]:
+                    if best is not None:
+                        best[2].free()
+                    best = (tm, t, pt)
+                else:
+                    pt.free()
+            tm, t, pl0[name] = best
+            tile_ms[name] = tm
             nb = A.shape[0] * A.shape[1] * 2
-            t = _time_fn(lambda: dak.dak_gemm(pl0[name], Bs[name], Cs[name], tuning=gt))
             flops = 2.0 * A.shape[0] * A.shape[1] * N
-            ops.append((nb, t if t > 1.15 * nb / b_hbm else flops / P, 64 * A.shape[1] * 2))
-            units.append(-(-A.shape[0] // 64))
+            ops.append((nb, t if t > 1.15 * nb / b_hbm else flops / P, tm * A.shape[1] * 2))
+            units.append(-(-A.shape[0] // tm))
         res.setdefault("t_comp_us", {})[name] = ops[-1][1] * 1e6
     for p in pl0.values():
         p.free()
@@ -488,7 +511,8 @@ def run_planner_check(dak, lin, attn, b_host, b_hbm, dev, x_global=0.1):
     for pname, counts in plans.items():
         pl = {}
         for name, h in zip(names, counts):
-            pl[name] = dak.dak_place_kv(k, v, h) if name == "attn" else dak.dak_place_matrix(lin[name][0], h)
+            pl[name] = dak.dak_place_kv(k, v, h) if name == "attn" else \
+                dak.dak_place_matrix(lin[name][0], h, tile_m=tile_ms[name])
 
         def step():
             for name in lin:
@@ -502,6 +526,7 @@ def run_planner_check(dak, lin, attn, b_host, b_hbm, dev, x_global=0.1):
         for p in pl.values():
             p.free()
     res["greedy_vs_uniform"] = res["uniform"]["ms"] / res["greedy"]["ms"]
+    res["tile_m"] = tile_ms
     res["status"] = dak.dak_last_error()[0]
     torch.cuda.empty_cache()
     return res
@@ -509,18 +534,20 @@ def run_planner_check(dak, lin, attn, b_host, b_hbm, dev, x_global=0.1):
 
 # ------------------------------------------------------------------------------ large N
 
-def run_large_n(dak, lin, b_host, b_hbm, dev, x=0.25):
-    """dak_gemm beyond one CTA's 256 hidden-state rows: the 8B gate+up linear at x, N in
-    {256, 512, 1024, 2048}, both ways: shared tile rows (the default: a cluster of
-    ceil(N/256) CTAs, at most 4, rank 0 forwarding every A chunk through distributed shared
-    memory, host bytes read once per launch of up to 1024 rows) and column blocks of 256
-    rows (host bytes read once per block, as [DAK] Table 1 counts traffic without
-    multicast), against both traffic models."""
+def run_large_n(dak, lin, b_host, b_hbm, dev, x=0.25, tile_m=128):
+    """dak_gemm beyond one CTA's 256 hidden-state rows: the 8B gate+up linear at x in tiles
+    of tile_m rows, N in {256, 512, 1024, 2048}, both ways: shared tiles (the default: a
+    cluster of ceil(N/256) CTAs, at most 4, rank 0 forwarding every A chunk through
+    distributed shared memory, host bytes read once per launch of up to 1024 rows) and
+    column blocks of 256 rows (host bytes read once per block, as [DAK] Table 1 counts traffic
+    without multicast), against both traffic models. t_comp_us: the same launch all in HBM;
+    frac_single_read: the single-read host-link bound over the shared-tile time."""
     import torch
     import synth
     A = lin["gate_up"][0]
     M, K = A.shape
-    p = dak.dak_place_matrix(A, dak.host_tiles_for_ratio(x, M))
+    p = dak.dak_place_matrix(A, dak.host_tiles_for_ratio(x, M, tile_m), tile_m=tile_m)
+    p0 = dak.dak_place_matrix(A, 0, tile_m=tile_m)
     rows = []
     for N in (256, 512, 1024, 2048):
         B = torch.from_numpy(synth.normal_bf16(7, 2, N * K).view("int16")).view(torch.bfloat16).to(dev).view(N, K)
@@ -529,14 +556,19 @@ def run_large_n(dak, lin, b_host, b_hbm, dev, x=0.25):
         launches = -(-N // 1024)
         rec = {"N": N,
                "model_per_256_rows_us": 1e6 * blocks * max(p.host_bytes / b_host, p.hbm_bytes / b_hbm),
-               "model_single_read_us": 1e6 * launches * max(p.host_bytes / b_host, p.hbm_bytes / b_hbm)}
+               "model_single_read_us": 1e6 * launches * max(p.host_bytes / b_host, p.hbm_bytes / b_hbm),
+               "t_comp_us": 1e6 * time_steps(lambda: dak.dak_gemm(p0, B, C, tuning=dict(pdl=1)), 5, 1),
+               "plan": {k: v for k, v in dak.dak_gemm_launch_plan(p, N, tuning=dict(pdl=1)).items()
+                        if k in ("cluster", "cluster_slots", "host_ctas", "hbm_ctas")}}
         for cols, key in ((1, "column_blocks"), (0, "shared_tiles")):
             t = time_steps(lambda: dak.dak_gemm(p, B, C, tuning=dict(pdl=1, column_blocks=cols)), 5, 1)
             link = p.host_bytes * (blocks if cols else launches)
             rec[key] = {"us": t * 1e6, "host_link_bytes": link, "host_link_gbps": link / t / 1e9}
+        rec["frac_single_read"] = rec["model_single_read_us"] / rec["shared_tiles"]["us"]
         rows.append(rec)
     p.free()
-    return {"op": "gate_up 28672x4096", "x": x, "host_bytes": p.host_bytes, "rows": rows,
+    p0.free()
+    return {"op": "gate_up 28672x4096", "x": x, "tile_m": tile_m, "host_bytes": p.host_bytes, "rows": rows,
             "status": dak.dak_last_error()[0]}
 
 

@@ -55,6 +55,8 @@ def _args():
                     help="--profile decode: batch of the step (default: the model configuration's)")
     ap.add_argument("--plain-launch", action="store_true",
                     help="--profile decode: eager steps with ordinary launches (no graph, no programmatic launch)")
+    ap.add_argument("--tile-m", type=int, default=64, choices=[64, 128],
+                    help="--profile of one linear: tile height of its placement")
     ap.add_argument("--profile", default=None, choices=["attn", "qkv", "o", "gate_up", "down", "decode", "chain"],
                     help="place one operation of the step at --x and launch it --steps times (for ncu); chain: the "
                          "four 8B linears as one grouped dak_gemm_chain launch")
@@ -1298,14 +1300,15 @@ def run_profile(args):
     else:
         M, K = synth.LINEARS_8B[args.profile]
         A, B = synth.gemm_inputs(M, K, args.batch, seed=0, tensor_index=list(synth.LINEARS_8B).index(args.profile))
-        p = dak.dak_place_matrix(A, dak.host_tiles_for_ratio(args.x, M))
+        p = dak.dak_place_matrix(A, dak.host_tiles_for_ratio(args.x, M, args.tile_m), tile_m=args.tile_m)
         Bt = torch.from_numpy(B.view("int16")).view(torch.bfloat16).to(dev)
         C = torch.empty((args.batch, M), dtype=torch.bfloat16, device=dev)
         fn = lambda: dak.dak_gemm(p, Bt, C)  # noqa: E731
         nbytes = A.nbytes
     t = time_steps(fn, args.steps, args.warmup)
     st = dak.dak_last_error()
-    print(json.dumps({"profile": args.profile, "x": args.x, "batch": args.batch, "us_per_launch": t * 1e6,
+    print(json.dumps({"profile": args.profile, "x": args.x, "batch": args.batch, "tile_m": args.tile_m,
+                      "us_per_launch": t * 1e6,
                       "gbps": nbytes / t / 1e9, "host_bytes": p.host_bytes, "status": st[0],
                       "source_hash": kernel_source_hash()}))
     p.free()

@@ -148,13 +148,16 @@ struct Piece {
     int idx, k0, k1;
 };
 
+// PM: the tile height fixed at compile time (0: 64 rows, 1: 128) in a kernel instantiated
+// per height, or -1: the launch's p.pairs
+template <int PM = -1>
 __device__ __forceinline__ Piece piece_of(const GemmParams& p, const TileIter& it, int ui) {
     const int u = it.first + ui * it.stride;
     Piece q;
     q.lb = u / p.P;
     q.idx = u % p.P;
     const int n_tier = it.host ? p.h : p.T - p.h;
-    q.m128 = p.pairs;
+    q.m128 = PM < 0 ? p.pairs : PM;
     q.t = it.tile0 + (q.m128 ? 2 * q.lb : q.lb);
     q.pair = (q.m128 && 2 * q.lb + 1 < n_tier && (q.t + 1) * kTileM < p.M) ? 1 : 0;
     q.blk = (it.host ? 0 : p.hb) + q.lb;
@@ -469,7 +472,9 @@ __device__ __forceinline__ void warp_row_scales(const GemmParams& p, bool fr, in
 // The 256 threads of the eight FMA warps meet (named barrier 2).
 __device__ __forceinline__ void consumer_bar_sync() { asm volatile("bar.sync 2, 256;" ::: "memory"); }
 
-template <int N, bool F>
+// PAIRS: the placement's tiles are 128 rows (blocks of two tile rows); a separate
+// instantiation, so that the 64-row path keeps its single-row inner loop.
+template <int N, bool F, bool PAIRS>
 __global__ void __launch_bounds__(kCoreThreads, 1)
     gemm_core_kernel(const GemmParams p, const __grid_constant__ CUtensorMap bmap) {
     // the folded norm's code exists only in the F = true instantiation
@@ -520,7 +525,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
                            W_FIN_DONE)) {
                 return;
             }
-            const Piece pc = piece_of(p, it, ui);
+            const Piece pc = piece_of<PAIRS ? 1 : 0>(p, it, ui);
             const int nr = pc.pair ? 4 : 2;  // 32-row groups of the block
             float xp[4][N], gp[4];
             for (int g = 0; g < nr; ++g) preload_residual<N>(p, fx, pc.t * kTileM + lane + 32 * g, xp[g], gp[g]);
@@ -579,16 +584,23 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
     // their named barrier, so that no warp is left waiting for one that gave up
     bool failed = false;
     for (int ui = 0; ui < it.count; ++ui) {
-        const Piece q = piece_of(p, it, ui);
+        const Piece q = piece_of<PAIRS ? 1 : 0>(p, it, ui);
         const int t = q.t;
-        const int halves = q.pair ? 2 : 1;          // tile rows of the block that hold rows of A
-        const int kg_bytes = q.m128 ? 2048 : 1024;  // one k-group of the block in the stage
-        float acc[2][N], xp[2][N], gp[2] = {0.f, 0.f};
+        constexpr int kH = PAIRS ? 2 : 1;
+        const int halves = (PAIRS && q.pair) ? 2 : 1;    // tile rows of the block that hold rows of A
+        constexpr int kg_bytes = PAIRS ? 2048 : 1024;  // one k-group of the block in the stage
+        float acc[kH][N], xp[kH][N], gp[kH];
+#pragma unroll
+        for (int h = 0; h < kH; ++h) gp[h] = 0.f;
         if (p.P == 1) {
-            for (int h = 0; h < halves; ++h) preload_residual<N>(p, fx, (t + h) * kTileM + w * 8 + r, xp[h], gp[h]);
+#pragma unroll
+            for (int h = 0; h < kH; ++h)
+                if (h < halves) preload_residual<N>(p, fx, (t + h) * kTileM + w * 8 + r, xp[h], gp[h]);
         }
 #pragma unroll
-        for (int n = 0; n < N; ++n) acc[0][n] = acc[1][n] = 0.f;
+        for (int h = 0; h < kH; ++h)
+#pragma unroll
+            for (int n = 0; n < N; ++n) acc[h][n] = 0.f;
         for (int k0 = q.k0; k0 < q.k1 && !failed; k0 += it.c.kc, ++i) {
             const int s = static_cast<int>(i % W);
             if (!mbar_wait(&full[s], static_cast<uint32_t>((i / W) & 1), abort, p.st, DAK_ERR_TIMEOUT, W_CONS_FULL)) {
@@ -602,7 +614,9 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
             for (int kg = kq; kg < kgr; kg += 4) {
                 // B block of 256 columns holding this k-group: [N rows][512 bytes]
                 const uint8_t* bb = bst + (kg >> 5) * (N * 512) + (kg & 31) * 16;
-                for (int h = 0; h < halves; ++h) {
+#pragma unroll
+                for (int h = 0; h < kH; ++h) {
+                    if (h >= halves) break;
                     const uint4 a = *reinterpret_cast<const uint4*>(st + kg * kg_bytes + h * 1024 + w * 128 + r * 16);
                     const float a0 = bf_lo(a.x), a1 = bf_hi(a.x), a2 = bf_lo(a.y), a3 = bf_hi(a.y);
                     const float a4 = bf_lo(a.z), a5 = bf_hi(a.z), a6 = bf_lo(a.w), a7 = bf_hi(a.w);
@@ -627,7 +641,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
         }
         // reduce the four k phases: lanes r, r+8, r+16, r+24 hold the same row
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < kH; ++h) {
 #pragma unroll
             for (int n = 0; n < N; ++n) {
                 float v = acc[h][n];
@@ -637,7 +651,9 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
             }
         }
         if (p.P == 1) {
-            for (int h = 0; h < halves; ++h) {
+#pragma unroll
+            for (int h = 0; h < kH; ++h) {
+                if (h >= halves) break;
                 float sq[N];
                 store_row<N>(p, acc[h], (t + h) * kTileM + w * 8 + r, kq == 0 && !failed, fx, fr, rsc, sq, xp[h], gp[h]);
                 if (fx) {
@@ -661,7 +677,9 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
         }
         // split block: this unit's partial rows to the workspace, then tell the finisher
         if (kq == 0) {
-            for (int h = 0; h < halves; ++h) {
+#pragma unroll
+            for (int h = 0; h < kH; ++h) {
+                if (h >= halves) break;
                 float* mine = piece_part(p, q, q.idx) + (h * kTileM + w * 8 + r) * p.N_pad;
 #pragma unroll
                 for (int n = 0; n < N; ++n) mine[n] = acc[h][n];
@@ -984,7 +1002,8 @@ __device__ __forceinline__ void epilogue_unit(const GemmParams& p, const Piece& 
     if (fx) fuse_block_sums(p, fuse_ssw, pc, e, 4);
 }
 
-template <bool F>
+// PAIRS: the placement's tiles are 128 rows (an instantiation per height)
+template <bool F, bool PAIRS>
 __global__ void __launch_bounds__(kUmmaThreads, 1)
     gemm_umma_kernel(const GemmParams p, const __grid_constant__ CUtensorMap bmap,
                      const __grid_constant__ CUtensorMap bmap_host) {
@@ -1082,7 +1101,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
             }
             tc_fence_after();
             const uint32_t d_tmem = tmem + static_cast<uint32_t>(ab) * acc_stride;
-            const Piece q = piece_of(p, it, ui);
+            const Piece q = piece_of<PAIRS ? 1 : 0>(p, it, ui);
             const uint32_t idesc = q.m128 ? idesc2 : idesc1;
             const uint32_t kg_bytes = q.m128 ? 2048u : 1024u;  // one k-group of the block's A
             bool ok = true;
@@ -1183,7 +1202,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         float gpre = 0.f;
         for (int ui = 0; ui < it.count; ++ui) {
             const int ab = ui & 1;
-            const Piece pc = piece_of(p, it, ui);
+            const Piece pc = piece_of<PAIRS ? 1 : 0>(p, it, ui);
             if (xpre_on) preload_x(p, pc, e, block_row_of_lane(pc.m128, qp, lane), xpre, gpre);
             if (!failed && !mbar_wait(&acc_full[ab], static_cast<uint32_t>((ui >> 1) & 1), abort, p.st,
                                       DAK_ERR_TIMEOUT, W_EPI_ACC)) {
@@ -1971,7 +1990,8 @@ static dak_status plan_launch(const dak_placement* A, int N, const dak_tuning* t
     dak_status r = plan_block(A->T, A->h, static_cast<int>(A->K_pad), A->tile_bytes, N, sms, t, caller_ws, ws_bytes,
                               bp, pairs);
     if (r != DAK_OK || bp->NC == 1 || (t && t->cluster_slots > 0)) return r;
-    const int fit = max_active_clusters(gemm_umma_kernel<false>, kUmmaThreads, bp->smem, bp->NC);
+    const int fit = max_active_clusters(pairs ? gemm_umma_kernel<false, true> : gemm_umma_kernel<false, false>,
+                                        kUmmaThreads, bp->smem, bp->NC);
     if (fit > 0 && fit < sms / bp->NC)
         r = plan_block(A->T, A->h, static_cast<int>(A->K_pad), A->tile_bytes, N, sms, t, caller_ws, ws_bytes, bp,
                        pairs, fit);
@@ -2067,13 +2087,13 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
     const bool fused = p.res_x || p.ss_in;
     cudaError_t e;
     if (bp.umma) {
-        e = fused ? launch_ex(gemm_umma_kernel<true>, bp.grid, kUmmaThreads, bp.smem, bp.NC, pdl, stream, p, bmap,
-                              bmap_host)
-                  : launch_ex(gemm_umma_kernel<false>, bp.grid, kUmmaThreads, bp.smem, bp.NC, pdl, stream, p, bmap,
-                              bmap_host);
+        auto k = bp.pairs ? (fused ? gemm_umma_kernel<true, true> : gemm_umma_kernel<false, true>)
+                          : (fused ? gemm_umma_kernel<true, false> : gemm_umma_kernel<false, false>);
+        e = launch_ex(k, bp.grid, kUmmaThreads, bp.smem, bp.NC, pdl, stream, p, bmap, bmap_host);
     } else {
-        e = fused ? launch_ex(gemm_core_kernel<1, true>, bp.grid, kCoreThreads, bp.smem, 1, pdl, stream, p, bmap)
-                  : launch_ex(gemm_core_kernel<1, false>, bp.grid, kCoreThreads, bp.smem, 1, pdl, stream, p, bmap);
+        auto k = bp.pairs ? (fused ? gemm_core_kernel<1, true, true> : gemm_core_kernel<1, false, true>)
+                          : (fused ? gemm_core_kernel<1, true, false> : gemm_core_kernel<1, false, false>);
+        e = launch_ex(k, bp.grid, kCoreThreads, bp.smem, 1, pdl, stream, p, bmap);
     }
     return cuda_status(e);
 }

@@ -478,7 +478,12 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_cta_kernel(const
 
 constexpr int kAttnDefaultHostCtas = 32;
 constexpr int kAttnDefaultHostWindow = 4;
-constexpr int kAttnStages = 3;     // default ring depth: two CTAs fit on an SM
+// Default ring depth: 2 stages (64 KiB in flight per CTA; three CTAs fit on an SM). Measured
+// all in HBM, graphs of back-to-back launches: 32 requests x 8 kv heads over 8K context (4
+// MiB units) 0.89-0.91 of B_hbm with 3 stages, 0.97 with 2 (more copies in flight only queue
+// in the memory system); 16 x 8 over 4K in two splits 0.82-0.83 either way; with host
+// requests the link bounds both alike.
+constexpr int kAttnStages = 2;
 constexpr int kAttnMaxStages = 5;
 
 // Context splits: double the split count while the units fill less than about 80% of the

@@ -167,3 +167,18 @@ def test_errors():
         plan(4096, 4096, 0, 16, ws_bytes=1000)
     with pytest.raises(dak.DakError):
         plan(4096, 4096, 0, 16, tuning={"chunk_k": 100})
+
+
+def test_cluster_slots_bound_the_schedule():
+    # a cluster launch schedules at most cluster_slots clusters (the count the GPU holds at
+    # once; the plan API's default is sm_count / cluster)
+    M, K = LINEARS_8B["gate_up"]
+    for tile_m, h in ((64, 112), (128, 56)):
+        for cs in (0, 36, 20, 7):
+            p = plan(M, K, h, 1024, tile_m=tile_m, tuning={"cluster_slots": cs} if cs else None)
+            assert p["cluster"] == 4
+            assert p["cluster_slots"] == (cs or SMS // 4)
+            assert (p["host_ctas"] + p["hbm_ctas"]) // 4 <= p["cluster_slots"]
+            assert p["host_ctas"] > 0 and p["hbm_ctas"] > 0
+    # one CTA per tile: cluster_slots counts CTAs and is not capped
+    assert plan(4096, 4096, 0, 16)["cluster_slots"] == SMS

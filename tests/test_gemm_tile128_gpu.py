@@ -186,3 +186,26 @@ def test_gate_up_full_size_sampled(dak, N):
     check_errors(got, ref, FP32_OUT_TOL, f"gate_up tile128 N={N} sampled")
     p.free()
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("tile_m", [64, 128])
+def test_cluster_slots_keep_results(dak, tile_m):
+    """Cluster launches (N > 256) size their persistent grid to the clusters the GPU holds at
+    once; the launch plan reports the count it uses, and scheduling for fewer clusters moves
+    work between CTAs without changing a bit of the result."""
+    M, K, N = 640, 1024, 600
+    A, B = synth.gemm_inputs(M, K, N, seed=11)
+    p = dak.dak_place_matrix(A, 2, tile_m=tile_m)
+    lp = dak.dak_gemm_launch_plan(p, N)
+    assert lp["cluster"] == 3 and lp["tile_m"] == tile_m
+    assert 1 <= lp["cluster_slots"] <= dak.dak_sm_count() // 3
+    assert (lp["host_ctas"] + lp["hbm_ctas"]) // 3 <= lp["cluster_slots"]
+    Bd = to_dev(B)
+    base = bits_of(dak.dak_gemm(p, Bd, c_fp32=True))
+    for cs in (2, 5, lp["cluster_slots"]):
+        tun = dict(cluster_slots=cs)
+        assert dak.dak_gemm_launch_plan(p, N, tuning=tun)["cluster_slots"] == cs
+        assert np.array_equal(bits_of(dak.dak_gemm(p, Bd, c_fp32=True, tuning=tun)), base), cs
+    assert dak.dak_last_error()[0] == 0
+    assert og.rel_err(to_np(dak.dak_gemm(p, Bd, c_fp32=True)), og.gemm_ref(A, B)) <= FP32_OUT_TOL
+    p.free()

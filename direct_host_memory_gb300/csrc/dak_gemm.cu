@@ -52,7 +52,7 @@ struct GemmParams {
     const __nv_bfloat16* B; // [N][K]
     void* C;                // [N][M]
     int M, K, K_pad, N, N_pad, T, h;
-    int pairs;    // 1: the HBM tier's units are blocks of two tile rows (M = 128 MMAs, A through a tensor map)
+    int pairs;    // 1: a placement of 128-row tiles: every unit is a block of two tile rows (M = 128 MMAs)
     int hb, gb;   // blocks of the host tier and of the HBM tier (tile rows, or pairs of them)
     int n_host_ctas, n_hbm_ctas, host_window, hbm_window;  // host/HBM counts are in clusters of NC CTAs
     int c_fp32;
@@ -699,10 +699,10 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
 // Tensor-core path, N >= 2: tcgen05.mma (M = 64 rows of A for a single-row block, 128 for a
 // pair block; N = N_pad <= 256 hidden-state columns; K = 16 per instruction), fp32
 // accumulators in TMEM, double-buffered (one per unit of work, so the epilogue of one unit
-// overlaps the MMAs of the next). Pair blocks (launches with `pairs`, HBM tier only) give
-// one MMA the work of two: at N_pad >= 128 a tile row is tensor-bound, and an M = 128
-// instruction takes about as long as an M = 64 one there.
-// Warps: 0 = A producer (bulk copies; tensor-map copies for pair blocks), 1 = TMEM allocator + MMA issuer,
+// overlaps the MMAs of the next). Pair blocks (placements of 128-row tiles) give one MMA
+// the work of two: at N_pad >= 128 a tile row is tensor-bound, and an M = 128 instruction
+// keeps the tensor pipe only about 1.25x as long as an M = 64 one.
+// Warps: 0 = A producer (bulk copies), 1 = TMEM allocator + MMA issuer,
 //        2..5 = epilogue (TMEM -> registers -> C, or -> partial tile and the piece count),
 //        6 = B producer (tensor-map copies), 7 = A forwarder of a wide-B cluster (NC > 1).
 // ======================================================================================
@@ -1706,12 +1706,10 @@ static bool split_workspace(float** part, int** cnt) {
 //     run the FMAs also store the partial rows). An unsplit block pays half of it (its
 //     epilogue stores C only).
 //  2. among the P within 3% of the lowest cost, the smallest whose pieces give a host part
-//     of a tenth of the tile rows (single-row blocks: the host tier never pairs) at least as
-//     many units as the host CTA cap (a small host part spread over more CTAs keeps more
-//     host bytes in flight), else the cheapest.
-// Pieces keep at least 512 columns and the workspace must hold the partials: at most
-// T + 2 tile rows' worth (pairs: an odd tile row at the end of each tier is a block of 128
-// rows of which 64 are used).
+//     of a tenth of the blocks at least as many units as the host CTA cap (a small host
+//     part spread over more CTAs keeps more host bytes in flight), else the cheapest.
+// Pieces keep at least 512 columns and the workspace must hold the partials (T tile rows'
+// worth; the bound used, T + 2, leaves room to spare).
 // tuning.split_k > 0 fixes P (1 = no split).
 constexpr double kCtaStreamBytesPerUs = 62.5e3;
 // bf16 tensor rate of one SM issuing M = 64 tiles, FLOP per us (fitted: the 8B gate+up at 256
@@ -1752,7 +1750,7 @@ static int split_pieces(int T, int K_pad, int N_pad, int slots, long long tile_b
     int cheapest = 1;
     for (int P = 2; P <= top; ++P)
         if (cost[P] < cost[cheapest]) cheapest = P;
-    const int h_small = (T + 9) / 10;
+    const int h_small = blocks_of((T + 9) / 10, rows == 2);
     for (int P = 1; P <= top; ++P)
         if (cost[P] <= 1.03 * cost[cheapest] && h_small * P >= host_cap) return P;
     return cheapest;

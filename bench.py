@@ -104,9 +104,14 @@ class Step:
         self.n_split = dak.dak_attn_default_split(self.kv)
         ws = dak.dak_attn_workspace_bytes(q.shape[0], q.shape[1], q.shape[2], self.n_split)
         self.ws = torch.empty(max(1, ws // 4), dtype=torch.float32, device=dev)
-        # programmatic launch: no op of the step writes the weights or KV cache another op streams
-        self.tun = dict(n_split=self.n_split, pdl=1)
-        self.gtun = dict(pdl=1)
+        # programmatic launch: no op of the step writes the weights or KV cache another op streams;
+        # the direct-access launches join host-link handoff sequence 1 (begun here, on the
+        # stream every run() uses; eager launches keep the count in step from run to run)
+        self.tun = dict(n_split=self.n_split, pdl=1, link=1)
+        self.gtun = dict(pdl=1, link=1)
+        self.stun = dict(n_split=self.n_split, pdl=1)  # the prefetch baselines' staged launches
+        self.sgtun = dict(pdl=1)
+        dak.dak_link_begin(1)
         self.host_bytes = sum(p.host_bytes for p in self.pl.values()) + self.kv.host_bytes
         self.total_bytes = sum(p.host_bytes + p.hbm_bytes for p in self.pl.values()) + \
             self.kv.host_bytes + self.kv.hbm_bytes
@@ -134,8 +139,8 @@ class Step:
             d.dak_prefetch(p, self.stage[name])
         d.dak_prefetch(self.kv, self.stage_kv)
         for name, p in self.pl.items():
-            d.dak_gemm_staged(p, self.stage[name], self.B[name], self.C[name], tuning=self.gtun)
-        d.dak_attn_staged(self.Q, self.kv, self.stage_kv, O=self.O, workspace=self.ws, tuning=self.tun)
+            d.dak_gemm_staged(p, self.stage[name], self.B[name], self.C[name], tuning=self.sgtun)
+        d.dak_attn_staged(self.Q, self.kv, self.stage_kv, O=self.O, workspace=self.ws, tuning=self.stun)
 
     def run_prefetch_overlap(self, copy_stream, events):
         """FlexGen-style: copies of the host parts run on a side stream in op order and each
@@ -153,9 +158,9 @@ class Step:
             events[len(names)].record(copy_stream)
         for i, name in enumerate(names):
             cur.wait_event(events[i])
-            d.dak_gemm_staged(self.pl[name], self.stage[name], self.B[name], self.C[name], tuning=self.gtun)
+            d.dak_gemm_staged(self.pl[name], self.stage[name], self.B[name], self.C[name], tuning=self.sgtun)
         cur.wait_event(events[len(names)])
-        d.dak_attn_staged(self.Q, self.kv, self.stage_kv, O=self.O, workspace=self.ws, tuning=self.tun)
+        d.dak_attn_staged(self.Q, self.kv, self.stage_kv, O=self.O, workspace=self.ws, tuning=self.stun)
 
     def free(self):
         for p in self.pl.values():
@@ -290,6 +295,12 @@ def run_decode(dak, args, b_host, b_hbm, dev, sync_all, local, model="8b", full=
             rec["tuned_frac"] = (C / tt) / roof
             dec_t.free(placements=False)
         if xg > 0:
+            # ablation: the same step without the host-link handoff between its kernels
+            dec_n = dak.Decoder(cfg, dec.layers, dec.final_norm, link_handoff=False)
+            dec_n.capture(x_in, pos, out, dak.MODE_DIRECT)
+            tn = time_steps(dec_n.replay, max(5, args.decode_steps // 2), 2, sync_all)
+            rec["no_link_handoff_tok_s"] = B / tn
+            dec_n.free(placements=False)
             for mode, name in ((dak.MODE_PREFETCH_SERIAL, "prefetch_serial"), (dak.MODE_PREFETCH_OVERLAP,
                                                                                  "prefetch_overlap")):
                 dec.capture(x_in, pos, out, mode)
@@ -644,10 +655,11 @@ def run_per_op_x(dak, lin, attn, b_host, b_hbm, dev, ns=(1, 8, 32, 64)):
     x in {0, 0.125, 0.25, 0.5}, and the 1024x1024 GEMV at x = 0.25. Two timings per point:
     `single`, one launch after a write of twice the L2 size (cold L2, launch latency
     included; CUDA events around the launch), and `chain`, a CUDA graph of launches with
-    programmatic launch over enough copies of the placement that they stream more than
-    twice the L2 size (the rate of the operation repeated back to back, as in a model's
-    layers); for the linears at N >= 2 also `grouped`, up to 8 of those copies in one
-    dak_gemm_chain launch. Bytes are the operation's weights (or KV cache)."""
+    programmatic launch and the host-link handoff (dak_link_begin) over enough copies of
+    the placement that they stream more than twice the L2 size (the rate of the operation
+    repeated back to back, as in a model's layers); for the linears at N >= 2 also
+    `grouped`, up to 8 of those copies in one dak_gemm_chain launch. Bytes are the
+    operation's weights (or KV cache)."""
     import math
     import torch
     import synth
@@ -675,6 +687,12 @@ def run_per_op_x(dak, lin, attn, b_host, b_hbm, dev, ns=(1, 8, 32, 64)):
 
     res = {"linears": [], "l2_bytes": l2}
     pdl = dict(pdl=1)
+    linked = dict(pdl=1, link=2)
+
+    def seq(launches):
+        dak.dak_link_begin(2)
+        for f in launches:
+            f()
     for i, (name, (A, _)) in enumerate(lin.items()):
         M, K = A.shape
         Ad = torch.from_numpy(A.view("int16")).view(torch.bfloat16).to(dev)
@@ -688,7 +706,7 @@ def run_per_op_x(dak, lin, attn, b_host, b_hbm, dev, ns=(1, 8, 32, 64)):
             C_bytes, H = pls[0].host_bytes + pls[0].hbm_bytes, pls[0].host_bytes
             for N in ns:
                 t1 = single(lambda: dak.dak_gemm(pls[0], Bs[N], Cs[N]))
-                g = _capture(lambda: [dak.dak_gemm(p, Bs[N], Cs[N], tuning=pdl) for p in pls])
+                g = _capture(lambda: seq([lambda p=p: dak.dak_gemm(p, Bs[N], Cs[N], tuning=linked) for p in pls]))
                 tc = time_steps(g.replay, 10, 3) / copies
                 del g
                 rec = dict(x=x, N=N, **point(C_bytes, H, t1, tc))
@@ -718,7 +736,9 @@ def run_per_op_x(dak, lin, attn, b_host, b_hbm, dev, ns=(1, 8, 32, 64)):
         ws = torch.empty(max(1, dak.dak_attn_workspace_bytes(q.shape[0], q.shape[1], q.shape[2], ns_) // 4),
                          dtype=torch.float32, device=dev)
         t1 = single(lambda: dak.dak_attn(Q, p, O=O, workspace=ws, tuning=dict(n_split=ns_)))
-        tc = time_steps(lambda: dak.dak_attn(Q, p, O=O, workspace=ws, tuning=dict(pdl=1, n_split=ns_)), 10, 3)
+        dak.dak_link_begin(3)  # eager launches back to back, each joining the sequence
+        tc = time_steps(lambda: dak.dak_attn(Q, p, O=O, workspace=ws, tuning=dict(pdl=1, n_split=ns_, link=3)),
+                        10, 3)
         C_bytes, H = p.host_bytes + p.hbm_bytes, p.host_bytes
         arows.append(dict(x=x, n_split=ns_, **point(C_bytes, H, t1, tc)))
         p.free()
@@ -732,7 +752,7 @@ def run_per_op_x(dak, lin, attn, b_host, b_hbm, dev, ns=(1, 8, 32, 64)):
     copies = math.ceil(2 * l2 / (1024 * 1024 * 2))
     pls = [dak.dak_place_matrix(A1d, dak.host_tiles_for_ratio(0.25, 1024)) for _ in range(copies)]
     t1 = single(lambda: dak.dak_gemm(pls[0], B1d, C1))
-    g = _capture(lambda: [dak.dak_gemm(p, B1d, C1, tuning=pdl) for p in pls])
+    g = _capture(lambda: seq([lambda p=p: dak.dak_gemm(p, B1d, C1, tuning=linked) for p in pls]))
     tc = time_steps(g.replay, 10, 3) / copies
     del g
     res["gemv"] = dict(op="GEMV 1024x1024, N = 1, x = 0.25 (4 of 16 tile rows on the host)", copies_in_chain=copies,

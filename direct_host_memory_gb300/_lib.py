@@ -31,7 +31,7 @@ EXPORTS = [
     "dak_decoder_replay", "dak_decoder_launches", "dak_decoder_free", "dak_tune_gemm", "dak_tune_attn",
     "dak_place_matrix_glu", "dak_plan_units", "dak_gemm_workspace_bytes", "dak_gemm_ws", "dak_gemm_plan", "dak_gemm_launch_plan",
     "dak_attn_f32", "dak_inject_fault", "dak_fault_pending", "dak_alloc_counts", "dak_gemm_chain",
-    "dak_gemm_chain_workspace_bytes",
+    "dak_gemm_chain_workspace_bytes", "dak_link_begin",
 ]
 
 # host-side fault injection kinds (DAK_FAULT_* in dak.h)
@@ -51,7 +51,8 @@ class dak_tuning(ctypes.Structure):
     _fields_ = [("host_ctas", ctypes.c_int), ("window", ctypes.c_int), ("hbm_window", ctypes.c_int),
                 ("chunk_k", ctypes.c_int), ("n_split", ctypes.c_int), ("hbm_ctas", ctypes.c_int),
                 ("split_k", ctypes.c_int), ("pdl", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
-                ("no_wave_align", ctypes.c_int), ("column_blocks", ctypes.c_int), ("cluster_slots", ctypes.c_int)]
+                ("no_wave_align", ctypes.c_int), ("column_blocks", ctypes.c_int), ("cluster_slots", ctypes.c_int),
+                ("link", ctypes.c_int)]
 
 
 class dak_gemm_op(ctypes.Structure):
@@ -79,7 +80,7 @@ class dak_decoder_config(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int), ("hidden", ctypes.c_int), ("n_heads", ctypes.c_int),
                 ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("ffn", ctypes.c_int),
                 ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float), ("plain_launch", ctypes.c_int),
-                ("op_tuning", dak_tuning * 5)]
+                ("op_tuning", dak_tuning * 5), ("no_link_handoff", ctypes.c_int)]
 
 
 class dak_decoder_layer(ctypes.Structure):
@@ -122,6 +123,7 @@ def _load():
         "dak_probe_read_bw": (i32, [i32, i64, i32, i32, i32, i32, i32, P(dbl), P(i32)]),
         "dak_probe_concurrent": (i32, [i64, i64, i32, i32, i32, i32, i32, i32, P(dbl), P(dbl)]),
         "dak_prefetch": (i32, [vp, vp, vp]),
+        "dak_link_begin": (i32, [i32, vp]),
         "dak_attn_noalloc": (i32, [vp, vp, vp, i32, ctypes.c_float, vp, P(dak_tuning), vp]),
         "dak_selftest_wait": (i32, [vp]),
         "dak_inject_fault": (i32, [i32, i32, i32]),
@@ -471,6 +473,14 @@ def dak_attn_noalloc(Q, KV: Placement, O, seq_lens=None, scale: float = 0.0, tun
     return O
 
 
+def dak_link_begin(slot: int, stream=None):
+    """Start host-link handoff sequence `slot` (1..8) on `stream`: later dak_gemm / dak_attn
+    calls with tuning link=slot stream their host tiles / requests only once the sequence's
+    earlier launches have issued all of their host loads (paces the loads; results are
+    unchanged)."""
+    _check(lib.dak_link_begin(int(slot), _stream_ptr(stream)), "dak_link_begin")
+
+
 def dak_prefetch(p: Placement, staging, stream=None):
     _check(lib.dak_prefetch(p.handle, _ptr(staging), _stream_ptr(stream)), "dak_prefetch")
 
@@ -569,14 +579,15 @@ class Decoder:
     the decoder keeps references to them (and frees the placements in .free())."""
 
     def __init__(self, cfg: dict, layers, final_norm, n_split: int = 0, plain_launch: bool = False,
-                 op_tuning=None):
+                 op_tuning=None, link_handoff: bool = True):
         """op_tuning: optional dict mapping 'qkv', 'o', 'gate_up', 'down', 'attn' to dak_tuning
-        fields (dicts); n_split sets the attention's context splits (0 = library default)."""
+        fields (dicts); n_split sets the attention's context splits (0 = library default);
+        link_handoff=False turns off the host-link handoff between the step's kernels."""
         c = dak_decoder_config(n_layers=len(layers), hidden=int(cfg["hidden"]), n_heads=int(cfg["n_heads"]),
                                n_kv_heads=int(cfg["n_kv_heads"]), head_dim=int(cfg["head_dim"]),
                                ffn=int(cfg["ffn"]), rms_eps=float(cfg.get("rms_eps", 1e-5)),
                                rope_theta=float(cfg.get("rope_theta", 500000.0)),
-                               plain_launch=int(bool(plain_launch)))
+                               plain_launch=int(bool(plain_launch)), no_link_handoff=int(not link_handoff))
         for i, name in enumerate(("qkv", "o", "gate_up", "down", "attn")):
             for k, v in dict((op_tuning or {}).get(name, {})).items():
                 setattr(c.op_tuning[i], k, int(v))

@@ -48,6 +48,9 @@ struct AttnParams {
     int n_host_ctas, n_hbm_ctas, host_window, hbm_window;
     long long host_units, hbm_units;
     DevStatus* st;
+    // host-link handoff of a decode step (link_wait / link_signal; null = off)
+    unsigned* link;
+    unsigned link_after;
 };
 
 constexpr int kChunkTok = 64;
@@ -155,6 +158,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnParams 
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
+            const bool link = ur.tier == 0 && p.link;
+            if (link) link_wait(p.link, p.link_after);
             long long i = 0;
             bool waited = false;
             for (long long u = ur.begin; u < ur.end && !*abort; ++u) {
@@ -175,6 +180,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnParams 
                 }
             }
         producer_done:
+            if (link) link_signal(p.link);
             volatile int dummy = 0;
             for (int s = 0; s < W && s < i; ++s) {
                 const long long last = ((i - 1 - s) / W) * W + s;
@@ -553,9 +559,10 @@ static cudaError_t launch_attn_d(const AttnParams& p, int grid, int W, bool pdl,
                             static_cast<const float*>(p.ws), p.O, p.o_fp32, p.n_split);
 }
 
-dak_status launch_attn(const void* Q, const dak_placement* KV, const void* host_src, const int* seq_lens, int H_q,
-                       float scale, void* O, void* ws, size_t ws_bytes, const dak_tuning* t, cudaStream_t stream,
-                       int o_fp32) {
+static dak_status launch_attn_link(const void* Q, const dak_placement* KV, const void* host_src, const int* seq_lens,
+                                   int H_q, float scale, void* O, void* ws, size_t ws_bytes, const dak_tuning* t,
+                                   cudaStream_t stream, int o_fp32, const LinkHandoff* link) {
+    if (link && link->signals) *link->signals = 0;
     if (!KV || KV->kind != 1 || !Q || !O) return DAK_ERR_INVALID;
     if (H_q <= 0 || H_q % KV->H_kv) return DAK_ERR_INVALID;
     const int G = H_q / KV->H_kv;
@@ -616,8 +623,30 @@ dak_status launch_attn(const void* Q, const dak_placement* KV, const void* host_
     const int W = std::max(p.host_window, p.hbm_window);
     const bool pdl = t && t->pdl > 0;
     p.wait_newest = t && t->pdl == 2;
+    if (link && link->ctr) {
+        p.link = link->ctr;
+        p.link_after = link->after;
+    }
     cudaError_t e = KV->D == 128 ? launch_attn_d<128>(p, grid, W, pdl, stream) : launch_attn_d<64>(p, grid, W, pdl, stream);
+    if (e == cudaSuccess && link && link->signals && p.link) *link->signals = p.n_host_ctas;
     return cuda_status(e);
+}
+
+dak_status launch_attn(const void* Q, const dak_placement* KV, const void* host_src, const int* seq_lens, int H_q,
+                       float scale, void* O, void* ws, size_t ws_bytes, const dak_tuning* t, cudaStream_t stream,
+                       int o_fp32, const LinkHandoff* link) {
+    // a public launch that joins a handoff sequence (dak_link_begin, tuning link)
+    LinkHandoff own;
+    int own_signals = 0;
+    const bool joined = !link && link_join(t, &own);
+    if (joined) {
+        own.signals = &own_signals;
+        link = &own;
+    }
+    const dak_status r =
+        launch_attn_link(Q, KV, host_src, seq_lens, H_q, scale, O, ws, ws_bytes, t, stream, o_fp32, link);
+    if (joined && r == DAK_OK) link_commit(t, own_signals);
+    return r;
 }
 
 }  // namespace dak

@@ -62,6 +62,9 @@ struct dak_decoder {
     // next QKV scale their accumulators by 1 / rms
     bool fuse_norm;
     float* ss[2];          // [T_d][B] sums of x^2 per 64 hidden units: [0] after O, [1] after down
+    // host-link handoff (direct access under programmatic launch): host-tier producers of
+    // the step's kernels that have issued their last load
+    unsigned* link;
     // prefetch baseline
     uint8_t* staging[2];
     size_t staging_bytes;
@@ -297,7 +300,7 @@ size_t staging_offset(const dak_decoder_layer& L, int upto) {
 
 void release(dak_decoder* d) {
     void* bufs[] = {d->x, d->h, d->qkv, d->q, d->att, d->ao, d->gu, d->act, d->dn, d->seq_lens, d->rope_cs,
-                    d->inv_freq, d->ws, d->gemm_ws, d->staging[0], d->staging[1], d->ss[0], d->ss[1]};
+                    d->inv_freq, d->ws, d->gemm_ws, d->staging[0], d->staging[1], d->ss[0], d->ss[1], d->link};
     for (void* p : bufs) dev_free(p);
     if (d->exec) cudaGraphExecDestroy(d->exec);
     for (int i = 0; i < 2; ++i) {
@@ -356,16 +359,39 @@ dak_status enqueue_step(dak_decoder* d, const void* x_in, const int* positions, 
     for (int i = 0; i < 4; ++i) {
         tg[i] = c.op_tuning[i];
         tg[i].pdl = pdl ? 1 : 0;
+        tg[i].link = 0;  // the step runs its own handoff
     }
     dak_tuning ta = c.op_tuning[4];
     ta.n_split = d->n_split;
     ta.pdl = pdl ? 2 : 0;  // the previous kernel appends the newest token
+    ta.link = 0;
     const int nl = c.n_layers;
     const int Lcap = nl > 0 ? d->layers[0].kv->L : 1;
     // the GEMMs' piece counters start every step at zero, even after a kernel that gave up
     if (d->gemm_ws &&
         cudaMemsetAsync(d->gemm_ws, 0, std::min<size_t>(d->gemm_ws_bytes, kGemmWsCounterBytes), s) != cudaSuccess)
         return DAK_ERR_CUDA;
+    // Host-link handoff: each kernel's host tiles / requests start streaming once the
+    // earlier kernels' host loads have all been issued (see link_wait). Every kernel of the
+    // previous step has finished before the step's first one starts, so the count restarts
+    // at zero here.
+    const bool handoff = mode == 0 && pdl && c.no_link_handoff == 0;
+    unsigned link_after = 0;
+    int link_signals = 0;
+    LinkHandoff lk;
+    if (handoff) {
+        if (cudaMemsetAsync(d->link, 0, sizeof(unsigned), s) != cudaSuccess) return DAK_ERR_CUDA;
+        lk.ctr = d->link;
+        lk.signals = &link_signals;
+    }
+    // the handoff of the next host-streaming launch, after the previous one's signals
+    auto next_link = [&]() -> const LinkHandoff* {
+        if (!handoff) return nullptr;
+        link_after += static_cast<unsigned>(link_signals);
+        link_signals = 0;
+        lk.after = link_after;
+        return &lk;
+    };
 
     NormArgs na{};
     na.x = d->x;
@@ -434,7 +460,7 @@ dak_status enqueue_step(dak_decoder* d, const void* x_in, const int* positions, 
         };
         const GemmFuse fz_qkv = consumer(1);
         if ((r = launch_gemm(L.qkv, src(0), d->h, d->qkv, B, 1, &tg[0], s, d->gemm_ws, d->gemm_ws_bytes,
-                             d->fuse_norm && l > 0 ? &fz_qkv : nullptr)) != DAK_OK)
+                             d->fuse_norm && l > 0 ? &fz_qkv : nullptr, next_link())) != DAK_OK)
             return r;
         RopeArgs ra{};
         ra.qkv = d->qkv;
@@ -454,16 +480,18 @@ dak_status enqueue_step(dak_decoder* d, const void* x_in, const int* positions, 
         if ((r = cuda_status(launch(rope_append_kernel, dim3(static_cast<unsigned>(B), static_cast<unsigned>(Hq + 2 * Hkv)),
                                     D / 2, pdl, s, ra))) != DAK_OK)
             return r;
-        if ((r = launch_attn(d->q, L.kv, src(4), d->seq_lens, Hq, 0.f, d->att, d->ws, d->ws_bytes, &ta, s)) != DAK_OK)
+        if ((r = launch_attn(d->q, L.kv, src(4), d->seq_lens, Hq, 0.f, d->att, d->ws, d->ws_bytes, &ta, s, 0,
+                             next_link())) != DAK_OK)
             return r;
         if (d->fuse_norm) {
             // x += attention projection, h = bf16(x * g_mlp), sums of x^2 for gate+up
             const GemmFuse fz = producer(0, L.mlp_norm);
-            if ((r = launch_gemm(L.o, src(1), d->att, d->h, B, 0, &tg[1], s, d->gemm_ws, d->gemm_ws_bytes, &fz)) !=
-                DAK_OK)
+            if ((r = launch_gemm(L.o, src(1), d->att, d->h, B, 0, &tg[1], s, d->gemm_ws, d->gemm_ws_bytes, &fz,
+                                 next_link())) != DAK_OK)
                 return r;
         } else {
-            if ((r = launch_gemm(L.o, src(1), d->att, d->ao, B, 1, &tg[1], s, d->gemm_ws, d->gemm_ws_bytes)) != DAK_OK)
+            if ((r = launch_gemm(L.o, src(1), d->att, d->ao, B, 1, &tg[1], s, d->gemm_ws, d->gemm_ws_bytes, nullptr,
+                                 next_link())) != DAK_OK)
                 return r;
             NormArgs nb{};
             nb.x = d->x;
@@ -479,11 +507,11 @@ dak_status enqueue_step(dak_decoder* d, const void* x_in, const int* positions, 
         if (L.gate_up->glu) {
             // gate/up interleaved placement: the GEMM's epilogue writes silu(gate) * up itself
             if ((r = launch_gemm(L.gate_up, src(2), d->h, d->act, B, 0, &tg[2], s, d->gemm_ws, d->gemm_ws_bytes,
-                                 fgu)) != DAK_OK)
+                                 fgu, next_link())) != DAK_OK)
                 return r;
         } else {
             if ((r = launch_gemm(L.gate_up, src(2), d->h, d->gu, B, 1, &tg[2], s, d->gemm_ws, d->gemm_ws_bytes,
-                                 fgu)) != DAK_OK)
+                                 fgu, next_link())) != DAK_OK)
                 return r;
             const long long n4 = static_cast<long long>(B) * c.ffn / 4;
             const int sg = static_cast<int>(std::min<long long>((n4 + 255) / 256, 4ll * device_sm_count()));
@@ -495,13 +523,14 @@ dak_status enqueue_step(dak_decoder* d, const void* x_in, const int* positions, 
         if (d->fuse_norm && !last) {
             // x += down projection, h = bf16(x * g_attn of the next layer), sums for its QKV
             const GemmFuse fz = producer(1, d->layers[l + 1].attn_norm);
-            if ((r = launch_gemm(L.down, src(3), d->act, d->h, B, 0, &tg[3], s, d->gemm_ws, d->gemm_ws_bytes, &fz)) !=
-                DAK_OK)
+            if ((r = launch_gemm(L.down, src(3), d->act, d->h, B, 0, &tg[3], s, d->gemm_ws, d->gemm_ws_bytes, &fz,
+                                 next_link())) != DAK_OK)
                 return r;
             if (mode == 2 && cudaEventRecord(d->ev_consumed[l & 1], s) != cudaSuccess) return DAK_ERR_CUDA;
             continue;
         }
-        if ((r = launch_gemm(L.down, src(3), d->act, d->dn, B, 1, &tg[3], s, d->gemm_ws, d->gemm_ws_bytes)) != DAK_OK)
+        if ((r = launch_gemm(L.down, src(3), d->act, d->dn, B, 1, &tg[3], s, d->gemm_ws, d->gemm_ws_bytes, nullptr,
+                             next_link())) != DAK_OK)
             return r;
         if (mode == 2 && cudaEventRecord(d->ev_consumed[l & 1], s) != cudaSuccess) return DAK_ERR_CUDA;
         NormArgs nc{};
@@ -590,6 +619,7 @@ extern "C" dak_status dak_decoder_create(const dak_decoder_config* cfg, const da
     chk(dalloc(&dd->seq_lens, Bs));
     chk(dalloc(&dd->rope_cs, Bs * D / 2));
     chk(dalloc(&dd->inv_freq, static_cast<size_t>(D / 2)));
+    chk(dalloc(&dd->link, 1));
     dd->ws_bytes = dak_attn_workspace_bytes(B, c.n_heads, c.head_dim, dd->n_split);
     if (dd->ws_bytes) chk(dev_alloc(reinterpret_cast<void**>(&dd->ws), dd->ws_bytes));
     // a split workspace of its own, so that decoders on different streams never share one

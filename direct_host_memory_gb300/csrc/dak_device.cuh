@@ -89,6 +89,32 @@ __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ------------------------------------------------------------------------------------
+// host-link handoff between the kernels of a decode step (LinkHandoff): a kernel's
+// host-tier producer issues its first load only once the host-tier producers of the
+// step's earlier kernels have issued all of theirs (a count in global memory), and adds
+// itself to the count after its own last load. Under programmatic launch the next kernel's
+// host CTAs otherwise fill their rings early, while the previous kernel still streams,
+// and the link then idles through the dependency at the boundary; held back until the
+// previous kernel's last host loads are in flight, the next loads queue right behind them
+// and arrive while the boundary resolves. Only the pace changes: the wait is bounded and
+// then the producer goes ahead, and no data is read through the count.
+// ------------------------------------------------------------------------------------
+constexpr uint64_t kLinkWaitNs = 500000ull;  // 0.5 ms
+__device__ __forceinline__ void link_wait(const unsigned* ctr, unsigned after) {
+    if (!ctr || after == 0) return;
+    const uint64_t t0 = globaltimer();
+    while (true) {
+        unsigned v;
+        asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+        if (v >= after || globaltimer() - t0 > kLinkWaitNs) return;
+        __nanosleep(64);
+    }
+}
+__device__ __forceinline__ void link_signal(unsigned* ctr) {
+    if (ctr) asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
+}
+
+// ------------------------------------------------------------------------------------
 // thread-block clusters: distributed shared memory, remote arrives, cluster barriers
 // ------------------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_ctarank() {

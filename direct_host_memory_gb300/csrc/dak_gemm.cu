@@ -75,6 +75,9 @@ struct GemmParams {
     const float* ss_in;
     int ss_tiles;
     float ss_inv_d, ss_eps;
+    // host-link handoff of a decode step (link_wait / link_signal; null = off)
+    unsigned* link;
+    unsigned link_after;
 };
 
 // Fused RMSNorm (the decode step's norms folded into the GEMMs around them):
@@ -239,6 +242,8 @@ __device__ __forceinline__ void produce(const GemmParams& p, const TileIter& it,
     const uint64_t pol_a = policy_evict_first();
     // the weights never depend on the previous kernel of the stream; the hidden states may
     if (!is_a) grid_dep_wait();
+    const bool link = is_a && it.host && p.link;
+    if (link) link_wait(p.link, p.link_after);
     long long i = 0;
     for (int ui = 0; ui < it.count && !*abort; ++ui) {
         const Piece q = piece_of(p, it, ui);
@@ -264,6 +269,7 @@ __device__ __forceinline__ void produce(const GemmParams& p, const TileIter& it,
         }
     }
 done:
+    if (link) link_signal(p.link);
     drain_fills(full, W, i, p.st);
 }
 
@@ -2000,7 +2006,7 @@ static dak_status plan_launch(const dak_placement* A, int N, const dak_tuning* t
 // (the widest tcgen05 tile used here), a cluster of ceil(N / 256) CTAs per tile row beyond.
 static dak_status launch_gemm_block(const dak_placement* A, const void* host_src, const void* B, void* C, int N,
                                     int c_fp32, const dak_tuning* t, void* ws, size_t ws_bytes, cudaStream_t stream,
-                                    const GemmFuse* fuse) {
+                                    const GemmFuse* fuse, const LinkHandoff* link) {
     if (!A || A->kind != 0) return DAK_ERR_INVALID;
     if (N < 1 || N > kMaxWideN) return DAK_ERR_INVALID;
     if (A->M == 0 || A->T == 0) return DAK_OK;  // nothing to compute; C may be empty
@@ -2045,6 +2051,11 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
     p.st = status_ptr();
     if (!p.st) return DAK_ERR_CUDA;
     if (p.h > 0 && !p.a_host) return DAK_ERR_INVALID;
+    if (link && link->ctr) {
+        // one signal per host cluster: its rank 0 runs the A producer (the others are fed)
+        p.link = link->ctr;
+        p.link_after = link->after;
+    }
     if (fuse && (fuse->res_x || fuse->ss_in)) {
         if (N > kFuseMaxN || bp.NC != 1) return DAK_ERR_UNSUPPORTED;
         if (fuse->res_x) {
@@ -2093,6 +2104,7 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
                           : (fused ? gemm_core_kernel<1, true, false> : gemm_core_kernel<1, false, false>);
         e = launch_ex(k, bp.grid, kCoreThreads, bp.smem, 1, pdl, stream, p, bmap);
     }
+    if (e == cudaSuccess && link && link->signals && p.link) *link->signals = p.n_host_ctas;
     return cuda_status(e);
 }
 
@@ -2102,12 +2114,14 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
 // once per block; with column_blocks, blocks of 256 rows that each read the host tiles
 // again. Clusters stop at 4 CTAs: forwarding every A chunk to 7 peers measured slower than
 // two launches of 1024 rows.
-dak_status launch_gemm(const dak_placement* A, const void* host_src, const void* B, void* C, int N, int c_fp32,
-                       const dak_tuning* t, cudaStream_t stream, void* ws, size_t ws_bytes, const GemmFuse* fuse) {
+static dak_status launch_gemm_blocks(const dak_placement* A, const void* host_src, const void* B, void* C, int N,
+                                     int c_fp32, const dak_tuning* t, cudaStream_t stream, void* ws, size_t ws_bytes,
+                                     const GemmFuse* fuse, const LinkHandoff* link) {
+    if (link && link->signals) *link->signals = 0;
     if (!A || A->kind != 0) return DAK_ERR_INVALID;
     if (ws && (reinterpret_cast<uintptr_t>(ws) & 255)) return DAK_ERR_ALIGN;
     const int block = (t && t->column_blocks == 1) ? kMaxBlockN : kMaxWideN;
-    if (N <= block) return launch_gemm_block(A, host_src, B, C, N, c_fp32, t, ws, ws_bytes, stream, fuse);
+    if (N <= block) return launch_gemm_block(A, host_src, B, C, N, c_fp32, t, ws, ws_bytes, stream, fuse, link);
     if (fuse && (fuse->res_x || fuse->ss_in)) return DAK_ERR_UNSUPPORTED;
     if (!B || !C) return DAK_ERR_INVALID;
     const size_t b_row = static_cast<size_t>(A->K) * 2;
@@ -2116,10 +2130,26 @@ dak_status launch_gemm(const dak_placement* A, const void* host_src, const void*
         const int nb = std::min(block, N - n0);
         const dak_status r = launch_gemm_block(A, host_src, static_cast<const uint8_t*>(B) + n0 * b_row,
                                                static_cast<uint8_t*>(C) + n0 * c_row, nb, c_fp32, t, ws, ws_bytes,
-                                               stream, nullptr);
+                                               stream, nullptr, nullptr);
         if (r != DAK_OK) return r;
     }
     return DAK_OK;
+}
+
+dak_status launch_gemm(const dak_placement* A, const void* host_src, const void* B, void* C, int N, int c_fp32,
+                       const dak_tuning* t, cudaStream_t stream, void* ws, size_t ws_bytes, const GemmFuse* fuse,
+                       const LinkHandoff* link) {
+    // a public launch that joins a handoff sequence (dak_link_begin, tuning link)
+    LinkHandoff own;
+    int own_signals = 0;
+    const bool joined = !link && link_join(t, &own);
+    if (joined) {
+        own.signals = &own_signals;
+        link = &own;
+    }
+    const dak_status r = launch_gemm_blocks(A, host_src, B, C, N, c_fp32, t, stream, ws, ws_bytes, fuse, link);
+    if (joined && r == DAK_OK) link_commit(t, own_signals);
+    return r;
 }
 
 

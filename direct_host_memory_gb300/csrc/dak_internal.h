@@ -91,6 +91,22 @@ struct GemmFuse {
     float inv_d = 0.f, eps = 0.f;
 };
 
+// Host-link handoff of a sequence of launches on one stream, e.g. a decode step's kernels
+// (link_wait / link_signal): ctr counts the host-tier producers of the sequence's launches
+// that have issued their last load (zeroed when the sequence starts); this launch's host
+// producers start once it reaches `after`. The launcher stores in *signals how many
+// producers of this launch add to the count (0 for a launch without host tiles).
+struct LinkHandoff {
+    unsigned* ctr = nullptr;
+    unsigned after = 0;
+    int* signals = nullptr;
+};
+// Sequences of the public calls (dak_link_begin; a launch joins sequence t->link): the
+// handoff a joining launch takes (false: the launch joins none), and the signals it adds.
+constexpr int kLinkSlots = 8;
+bool link_join(const dak_tuning* t, LinkHandoff* lk);
+void link_commit(const dak_tuning* t, int signals);
+
 // One operation of a chain of GEMMs run by one persistent launch (launch_gemm_chain):
 // host_src is the host tier's device-visible address (or a prefetch staging copy);
 // after_prev: B (and the fused inputs) come from earlier operations of the chain, so the
@@ -113,11 +129,11 @@ size_t gemm_chain_workspace_bytes(const ChainOp* ops, int n, int N, const dak_tu
 
 dak_status launch_gemm(const dak_placement* A, const void* host_src, const void* B, void* C, int N, int c_fp32,
                        const dak_tuning* t, cudaStream_t s, void* ws = nullptr, size_t ws_bytes = 0,
-                       const GemmFuse* fuse = nullptr);
+                       const GemmFuse* fuse = nullptr, const LinkHandoff* link = nullptr);
 size_t gemm_workspace_bytes(const dak_placement* A, int N);
 // o_fp32: O is fp32 [B][H_q][D] (dak_attn_f32) instead of bf16
 dak_status launch_attn(const void* Q, const dak_placement* KV, const void* host_src, const int* seq_lens, int H_q,
                        float scale, void* O, void* ws, size_t ws_bytes, const dak_tuning* t, cudaStream_t s,
-                       int o_fp32 = 0);
+                       int o_fp32 = 0, const LinkHandoff* link = nullptr);
 
 }  // namespace dak

@@ -67,6 +67,71 @@ DevStatus* status_ptr() {
 }
 
 // ------------------------------------------------------------------------------------
+// host-link handoff sequences of the public calls (dak_link_begin, dak_tuning.link): a
+// device count per slot, and per device and slot the signals of the sequence's launches so
+// far (the `after` of its next launch)
+// ------------------------------------------------------------------------------------
+__device__ unsigned g_link_count[kLinkSlots];
+static std::mutex g_link_mu;
+static unsigned g_link_after[64][kLinkSlots];
+
+static unsigned* link_counts() {
+    static unsigned* cache[64] = {nullptr};
+    static unsigned long long ctx[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    const unsigned long long id = current_context_id();
+    if (!cache[dev] || ctx[dev] != id) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_link_count) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        cache[dev] = static_cast<unsigned*>(ptr);
+        ctx[dev] = current_context_id();
+    }
+    return cache[dev];
+}
+
+bool link_join(const dak_tuning* t, LinkHandoff* lk) {
+    if (!t || t->link < 1 || t->link > kLinkSlots) return false;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    std::lock_guard<std::mutex> lock(g_link_mu);
+    unsigned* c = link_counts();
+    if (!c) return false;
+    lk->ctr = c + (t->link - 1);
+    lk->after = g_link_after[dev][t->link - 1];
+    return true;
+}
+
+void link_commit(const dak_tuning* t, int signals) {
+    int dev = 0;
+    if (!t || t->link < 1 || t->link > kLinkSlots || signals <= 0) return;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return;
+    std::lock_guard<std::mutex> lock(g_link_mu);
+    g_link_after[dev][t->link - 1] += static_cast<unsigned>(signals);
+}
+
+}  // namespace dak
+
+extern "C" dak_status dak_link_begin(int slot, void* stream) {
+    using namespace dak;
+    if (slot < 1 || slot > kLinkSlots) return DAK_ERR_INVALID;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DAK_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_link_mu);
+    unsigned* c = link_counts();
+    if (!c) return DAK_ERR_CUDA;
+    const cudaError_t e = cudaMemsetAsync(c + (slot - 1), 0, sizeof(unsigned), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_status(e);
+    g_link_after[dev][slot - 1] = 0;
+    return DAK_OK;
+}
+
+namespace dak {
+
+// ------------------------------------------------------------------------------------
 // allocations: live counts and host-side fault injection
 // ------------------------------------------------------------------------------------
 static std::atomic<long long> g_live_host{0}, g_live_dev{0};

@@ -53,6 +53,7 @@ dak_status tune(Fn fn, bool has_host, bool gemm, int reps, const dak_tuning* bas
     }
     dak_tuning b{};
     if (base) b = *base;
+    b.link = 0;  // timed launches join no handoff sequence
     *out = dak_tune_result{};
     out->default_us = time_launches(tm, fn, b, reps);
     if (out->default_us < 0) {

@@ -89,6 +89,9 @@ typedef struct dak_placement dak_placement;
  *               once. 0 = asked of the device at launch (a cluster's CTAs share a GPC, so
  *               fewer clusters of 4 fit than SMs / 4; a persistent grid sized past that runs
  *               its extra clusters as a tail); dak_gemm_plan assumes sm_count / cluster.
+ *   link      : dak_gemm / dak_attn: 1..8 = join host-link handoff sequence `link`, started
+ *               by dak_link_begin on the same stream (see there); 0 = none. The tuner
+ *               ignores it.
  */
 typedef struct {
     int host_ctas;
@@ -103,6 +106,7 @@ typedef struct {
     int no_wave_align;
     int column_blocks;
     int cluster_slots;
+    int link;
 } dak_tuning;
 
 /* ---------------------------------------------------------------------------------- *
@@ -330,6 +334,27 @@ dak_status dak_attn_noalloc(const void* Q, const dak_placement* KV, const int* s
                             void* O, const dak_tuning* tuning, void* stream);
 
 /* ---------------------------------------------------------------------------------- *
+ * Host-link handoff across launches (section 4.3.1, "Congestion Control Strategy": the
+ * host requests in flight are paced; here across the operations of a step)
+ * ---------------------------------------------------------------------------------- */
+
+/* Start host-link handoff sequence `slot` (1..8) of the current device on `stream`: a
+ * stream-ordered write zeroes the slot's device count, and the library's host-side count of
+ * the sequence's launches restarts. Every later dak_gemm / dak_gemm_ws / dak_attn /
+ * dak_attn_f32 / dak_attn_noalloc call with tuning->link = slot then joins the sequence in
+ * call order: the CTAs that stream its host tiles or requests issue their first load only
+ * once the host CTAs of the sequence's earlier launches have issued all of theirs, and count
+ * themselves in when their own last load is issued. Under programmatic launch (tuning->pdl)
+ * a launch's host CTAs otherwise fill their rings while the previous launch still streams
+ * its host part, and the host link then idles through the boundary between the two; held
+ * back, their loads queue right behind the previous launch's last ones. The wait is bounded
+ * (0.5 ms, after which the CTA goes ahead) and only paces the loads: results never change.
+ * Meant for the launches of one stream, issued (or captured into one CUDA graph) in order
+ * after this call; a sequence belongs to one stream at a time. DAK_ERR_INVALID: slot out of
+ * range. */
+dak_status dak_link_begin(int slot, void* stream);
+
+/* ---------------------------------------------------------------------------------- *
  * Launch tuner (section 4.3.1, "Congestion Control Strategy": the host-SM cap and the
  * in-flight window are profiled per operation before launch; section 6.2, Fig. 12)
  * ---------------------------------------------------------------------------------- */
@@ -373,7 +398,12 @@ dak_status dak_tune_attn(const void* Q, const dak_placement* KV, const int* seq_
  *               1 = ordinary stream-ordered launches.
  *   op_tuning : launch tuning of the operations qkv, o, gate_up, down (dak_gemm) and the
  *               attention (dak_attn; its n_split defaults to dak_attn_default_split of
- *               layer 0's cache), as in dak_tuning; the pdl field is set by the decoder. */
+ *               layer 0's cache), as in dak_tuning; the pdl field is set by the decoder.
+ *   no_link_handoff: 0 = with programmatic launch in direct-access mode, the host tiles /
+ *               requests of each operation start streaming only once the step's earlier
+ *               operations have issued all their host loads, so that the host link keeps
+ *               busy through the dependency at each boundary (a bounded, pacing-only wait:
+ *               results are the same either way); 1 = off. */
 typedef struct {
     int n_layers;
     int hidden;
@@ -385,6 +415,7 @@ typedef struct {
     float rope_theta;
     int plain_launch;
     dak_tuning op_tuning[5];
+    int no_link_handoff;
 } dak_decoder_config;
 
 /* One layer's operands, all placed by the caller beforehand (dak_place_matrix with the

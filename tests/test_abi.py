@@ -58,6 +58,12 @@ def test_status_strings(dak):
     assert dak.lib.dak_status_string(6) == b"kernel wait timed out"
 
 
+def test_link_begin_rejects_bad_slots(dak):
+    """Handoff sequences are slots 1..8; any other slot is refused before any CUDA call."""
+    for slot in (0, -1, 9, 1 << 20):
+        assert dak.lib.dak_link_begin(slot, None) == 1  # DAK_ERR_INVALID
+
+
 def test_planner_rejects_bad_arguments(dak):
     with pytest.raises(dak.DakError):
         dak.dak_plan_ratios([(1e9, 0.0)], 1e11, 1e12, 2e9)  # budget above the total

@@ -143,22 +143,51 @@ def test_decoder_small_parity(dak, cfg, B, L, pos, frac):
 
 
 def test_decoder_bit_identical_across_placement_modes_and_launches(dak):
-    """Offload ratio, prefetch baselines, CUDA graph and plain launches change where bytes
-    come from and when kernels start, never the result."""
+    """Offload ratio, prefetch baselines, CUDA graph, plain launches and the host-link handoff
+    change where bytes come from and when kernels start, never the result."""
     cfg, B, L, pos = SMALL64, 5, 200, [0, 63, 64, 130, 199]
     layers, caches, fnorm, x0 = _inputs(cfg, B, L, seed=12)
     base = None
     mixed = [_host_units(cfg, B, f) for f in (0.1, 0.5, 0.9)]
     for units in (_host_units(cfg, B, 0.0), mixed, _host_units(cfg, B, 1.0)):
-        for plain in (False, True):
-            dec = _build(dak, cfg, layers, caches, fnorm, units, plain_launch=plain)
+        for plain, handoff in ((False, True), (False, False), (True, True)):
+            dec = _build(dak, cfg, layers, caches, fnorm, units, plain_launch=plain, link_handoff=handoff)
             for mode in (0, 1, 2):
                 for graph in (False, True):
                     b = bits_of(_run(dak, dec, x0, pos, mode, graph))
                     if base is None:
                         base = b
-                    assert np.array_equal(b, base), (units, plain, mode, graph)
+                    assert np.array_equal(b, base), (units, plain, handoff, mode, graph)
             dec.free()
+
+
+@pytest.mark.slow
+def test_decoder_link_handoff_8b_width(dak):
+    """The host-link handoff at 8B widths (QKV 6144, O 4096, gate+up 28672, down 14336 rows /
+    columns; 16 requests, a third of every operation on the host): each kernel's host tiles
+    start after the previous kernels' host loads are issued; the results are those of the
+    step without it, bit for bit, in one step and over consecutive graph replays."""
+    import torch
+    cfg = dict(synth.DECODER_8B, n_layers=2)
+    B, L = 16, 320
+    layers = [synth.decoder_layer(cfg, l, 21) for l in range(2)]
+    caches = [synth.decoder_kv(cfg, l, B, L, 21) for l in range(2)]
+    fnorm, x0 = synth.decoder_final_norm(cfg, 21), synth.decoder_x0(cfg, B, 21)
+    units = _host_units(cfg, B, 0.3)
+    pos = [L - 1 - 7 * i for i in range(B)]
+    outs = []
+    for handoff in (True, False):
+        dec = _build(dak, cfg, layers, caches, fnorm, units, link_handoff=handoff)
+        x, p = _dev(x0), _pos(pos)
+        out = torch.empty_like(x)
+        dec.capture(x, p, out, 0)
+        for _ in range(3):
+            dec.replay()
+        torch.cuda.synchronize()
+        assert dak.dak_last_error()[0] == 0
+        outs.append(bits_of(out))
+        dec.free()
+    assert np.array_equal(outs[0], outs[1])
 
 
 def test_decoder_fused_swiglu_matches_separate_kernel(dak):

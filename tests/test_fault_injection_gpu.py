@@ -97,7 +97,7 @@ def test_decoder_allocation_failures(dak):
     L = dak.place_decoder_layer(w, kv, dict(qkv=1, o=1, gate_up=1, down=1, kv=1))
     fn = to_dev(synth.decoder_final_norm(cfg, 3))
     counts0 = dak.dak_alloc_counts()
-    for skip in range(16):
+    for skip in range(24):
         dak.dak_inject_fault(dak.FAULT_DEVICE_ALLOC, count=1, skip=skip)
         try:
             dec = dak.Decoder(cfg, [L], fn)

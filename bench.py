@@ -417,7 +417,8 @@ def run_planner_check(dak, lin, attn, b_host, b_hbm, dev, x_global=0.1):
     xC/B_host) with T_c its measured all-HBM time, in 128-row tiles (and 64-row ones); (2)
     one step of the four linears at N = 256 (each in the tile height that runs it faster all
     in HBM) plus the 32-request attention, placed by the greedy planner and uniformly at the
-    same x_global, both timed."""
+    same x_global, both timed. Launches run back to back with programmatic launch in one
+    host-link handoff sequence."""
     import math
     import numpy as np
     import torch
@@ -430,7 +431,9 @@ def run_planner_check(dak, lin, attn, b_host, b_hbm, dev, x_global=0.1):
         Bs[name] = torch.from_numpy(synth.normal_bf16(0 + i, 2, N * K).view("int16")).view(torch.bfloat16) \
             .to(dev).view(N, K)
         Cs[name] = torch.empty((N, A.shape[0]), dtype=torch.bfloat16, device=dev)
-    gt = dict(pdl=1)
+    # back-to-back launches with programmatic launch, joined in one host-link handoff sequence
+    gt = dict(pdl=1, link=5)
+    dak.dak_link_begin(5)
 
     # (1) flat segment of a tensor-bound operation, in 128-row tiles (M = 128 MMAs, the
     # placement for tensor-bound N) and, for comparison, in 64-row tiles
@@ -481,7 +484,7 @@ def run_planner_check(dak, lin, attn, b_host, b_hbm, dev, x_global=0.1):
             ws = torch.empty(max(1, dak.dak_attn_workspace_bytes(q.shape[0], q.shape[1], q.shape[2],
                                                                dak.dak_attn_default_split(pl0[name])) // 4),
                              dtype=torch.float32, device=dev)
-            t = _time_fn(lambda: dak.dak_attn(Q, pl0["attn"], O=O, workspace=ws, tuning=dict(pdl=1)))
+            t = _time_fn(lambda: dak.dak_attn(Q, pl0["attn"], O=O, workspace=ws, tuning=dict(pdl=1, link=5)))
             flops = 4.0 * q.shape[0] * q.shape[1] * k.shape[2] * k.shape[3]
             ops.append((nb, t if t > 1.15 * nb / b_hbm else flops / P, kv_req))
             units.append(k.shape[0])
@@ -530,7 +533,7 @@ def run_planner_check(dak, lin, attn, b_host, b_hbm, dev, x_global=0.1):
         def step():
             for name in lin:
                 dak.dak_gemm(pl[name], Bs[name], Cs[name], tuning=gt)
-            dak.dak_attn(Q, pl["attn"], O=O, workspace=ws, tuning=dict(pdl=1))
+            dak.dak_attn(Q, pl["attn"], O=O, workspace=ws, tuning=dict(pdl=1, link=5))
 
         t = _time_fn(step, 10, 2)
         host = sum(pl[n].host_bytes for n in names)
@@ -554,7 +557,8 @@ def run_large_n(dak, lin, b_host, b_hbm, dev, x=0.25, tile_m=128):
     distributed shared memory, host bytes read once per launch of up to 1024 rows) and
     column blocks of 256 rows (host bytes read once per block, as [DAK] Table 1 counts traffic
     without multicast), against both traffic models. t_comp_us: the same launch all in HBM;
-    frac_single_read: the single-read host-link bound over the shared-tile time."""
+    frac_single_read: the single-read host-link bound over the shared-tile time. Launches run
+    back to back with programmatic launch in one host-link handoff sequence."""
     import torch
     import synth
     A = lin["gate_up"][0]
@@ -574,7 +578,8 @@ def run_large_n(dak, lin, b_host, b_hbm, dev, x=0.25, tile_m=128):
                "plan": {k: v for k, v in dak.dak_gemm_launch_plan(p, N, tuning=dict(pdl=1)).items()
                         if k in ("cluster", "cluster_slots", "host_ctas", "hbm_ctas")}}
         for cols, key in ((1, "column_blocks"), (0, "shared_tiles")):
-            t = time_steps(lambda: dak.dak_gemm(p, B, C, tuning=dict(pdl=1, column_blocks=cols)), 5, 1)
+            dak.dak_link_begin(6)  # back-to-back launches in one host-link handoff sequence
+            t = time_steps(lambda: dak.dak_gemm(p, B, C, tuning=dict(pdl=1, column_blocks=cols, link=6)), 5, 1)
             link = p.host_bytes * (blocks if cols else launches)
             rec[key] = {"us": t * 1e6, "host_link_bytes": link, "host_link_gbps": link / t / 1e9}
         rec["frac_single_read"] = rec["model_single_read_us"] / rec["shared_tiles"]["us"]

@@ -270,6 +270,7 @@ def run_decode(dak, args, b_host, b_hbm, dev, sync_all, local, model="8b", full=
             dec.replay()
         torch.cuda.synchronize()
         st0 = dak.dak_last_error()[0]
+        dak.dak_link_timeouts()  # count the handoff waits of the timed steps only
         sampler = ClockSampler(local)
         sampler.start()
         time.sleep(0.2)
@@ -279,11 +280,13 @@ def run_decode(dak, args, b_host, b_hbm, dev, sync_all, local, model="8b", full=
         time.sleep(0.2)
         sampler.stop()
         roof = tier_roofline(C, H / C, b_host, b_hbm)
+        timeouts = dak.dak_link_timeouts()
         rec = {"x_effective": H / C, "bytes_per_step": C, "host_bytes_per_step": H, "ms_per_step": t * 1e3,
                "tok_s": B / t, "eff_gbps": C / t / 1e9, "roofline_gbps": roof / 1e9, "frac": (C / t) / roof,
                "planner_model_ms": tmodel * 1e3, "host_units_per_layer": units[0] if units else {},
                "build_s": build_s,
-               "launches_per_step": dec.launches(), "clocks": sampler.summary(tw0, tw1)}
+               "launches_per_step": dec.launches(), "clocks": sampler.summary(tw0, tw1),
+               "link_timeouts": timeouts}
         if xg > 0 and full:
             # launch tuner per operation type on layer 0's placements, then the step with its choices
             tuned, table = tune_decoder_ops(dak, cfg, dec, dev)

@@ -31,7 +31,7 @@ EXPORTS = [
     "dak_decoder_replay", "dak_decoder_launches", "dak_decoder_free", "dak_tune_gemm", "dak_tune_attn",
     "dak_place_matrix_glu", "dak_plan_units", "dak_gemm_workspace_bytes", "dak_gemm_ws", "dak_gemm_plan", "dak_gemm_launch_plan",
     "dak_attn_f32", "dak_inject_fault", "dak_fault_pending", "dak_alloc_counts", "dak_gemm_chain",
-    "dak_gemm_chain_workspace_bytes", "dak_link_begin",
+    "dak_gemm_chain_workspace_bytes", "dak_link_begin", "dak_link_timeouts", "dak_selftest_link",
 ]
 
 # host-side fault injection kinds (DAK_FAULT_* in dak.h)
@@ -124,6 +124,8 @@ def _load():
         "dak_probe_concurrent": (i32, [i64, i64, i32, i32, i32, i32, i32, i32, P(dbl), P(dbl)]),
         "dak_prefetch": (i32, [vp, vp, vp]),
         "dak_link_begin": (i32, [i32, vp]),
+        "dak_link_timeouts": (i32, [vp, P(ctypes.c_uint32)]),
+        "dak_selftest_link": (i32, [vp]),
         "dak_attn_noalloc": (i32, [vp, vp, vp, i32, ctypes.c_float, vp, P(dak_tuning), vp]),
         "dak_selftest_wait": (i32, [vp]),
         "dak_inject_fault": (i32, [i32, i32, i32]),
@@ -479,6 +481,19 @@ def dak_link_begin(slot: int, stream=None):
     earlier launches have issued all of their host loads (paces the loads; results are
     unchanged)."""
     _check(lib.dak_link_begin(int(slot), _stream_ptr(stream)), "dak_link_begin")
+
+
+def dak_link_timeouts(stream=None) -> int:
+    """Handoff waits that gave up at their bound since the last call (0 when every launch of
+    every sequence found its predecessors in time); the count restarts at zero."""
+    c = ctypes.c_uint32()
+    _check(lib.dak_link_timeouts(_stream_ptr(stream), ctypes.byref(c)), "dak_link_timeouts")
+    return int(c.value)
+
+
+def dak_selftest_link(stream=None):
+    """One pacing wait that must give up (see dak_link_timeouts)."""
+    _check(lib.dak_selftest_link(_stream_ptr(stream)), "dak_selftest_link")
 
 
 def dak_prefetch(p: Placement, staging, stream=None):

@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnParams 
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
             const bool link = ur.tier == 0 && p.link;
-            if (link) link_wait(p.link, p.link_after);
+            if (link) link_wait(p.link, p.link_after, p.st);
             long long i = 0;
             bool waited = false;
             for (long long u = ur.begin; u < ur.end && !*abort; ++u) {

@@ -97,16 +97,21 @@ __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.w
 // and the link then idles through the dependency at the boundary; held back until the
 // previous kernel's last host loads are in flight, the next loads queue right behind them
 // and arrive while the boundary resolves. Only the pace changes: the wait is bounded and
-// then the producer goes ahead, and no data is read through the count.
+// then the producer goes ahead (counted in the status block's link_timeouts, not an
+// error), and no data is read through the count.
 // ------------------------------------------------------------------------------------
 constexpr uint64_t kLinkWaitNs = 500000ull;  // 0.5 ms
-__device__ __forceinline__ void link_wait(const unsigned* ctr, unsigned after) {
+__device__ __forceinline__ void link_wait(const unsigned* ctr, unsigned after, DevStatus* st) {
     if (!ctr || after == 0) return;
     const uint64_t t0 = globaltimer();
     while (true) {
         unsigned v;
         asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
-        if (v >= after || globaltimer() - t0 > kLinkWaitNs) return;
+        if (v >= after) return;
+        if (globaltimer() - t0 > kLinkWaitNs) {
+            if (st) atomicAdd(&st->link_timeouts, 1u);
+            return;
+        }
         __nanosleep(64);
     }
 }

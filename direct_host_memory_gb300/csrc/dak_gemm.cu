@@ -243,7 +243,7 @@ __device__ __forceinline__ void produce(const GemmParams& p, const TileIter& it,
     // the weights never depend on the previous kernel of the stream; the hidden states may
     if (!is_a) grid_dep_wait();
     const bool link = is_a && it.host && p.link;
-    if (link) link_wait(p.link, p.link_after);
+    if (link) link_wait(p.link, p.link_after, p.st);
     long long i = 0;
     for (int ui = 0; ui < it.count && !*abort; ++ui) {
         const Piece q = piece_of(p, it, ui);

@@ -35,7 +35,7 @@ constexpr int kTileM = 64;
 // Device status block: first failure code and where it happened.
 struct DevStatus {
     int code;
-    int pad;
+    unsigned link_timeouts;  // host-link handoff waits that gave up (dak_link_timeouts)
     unsigned long long info;
 };
 

@@ -995,6 +995,41 @@ extern "C" dak_status dak_selftest_wait(void* stream) {
     return cuda_status(cudaGetLastError());
 }
 
+// One thread waits for a handoff count that nothing raises: the pacing wait gives up after
+// its bound, counts itself in link_timeouts and the kernel returns normally.
+__global__ void selftest_link_kernel(const unsigned* never, DevStatus* st) { link_wait(never, 1u, st); }
+
+extern "C" dak_status dak_selftest_link(void* stream) {
+    DevStatus* st = status_ptr();
+    if (!st) return DAK_ERR_CUDA;
+    void* zero = nullptr;  // a count that stays at zero
+    if (dev_alloc(&zero, sizeof(unsigned)) != cudaSuccess) return DAK_ERR_DEVICE_ALLOC;
+    cudaError_t e = cudaMemsetAsync(zero, 0, sizeof(unsigned), static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) {
+        selftest_link_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<const unsigned*>(zero), st);
+        e = cudaGetLastError();
+    }
+    const cudaError_t s = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    dev_free(zero);
+    return cuda_status(e != cudaSuccess ? e : s);
+}
+
+extern "C" dak_status dak_link_timeouts(void* stream, uint32_t* count) {
+    if (!count) return DAK_ERR_INVALID;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return DAK_ERR_CUDA;
+    DevStatus* st = status_ptr();
+    if (!st) return DAK_ERR_CUDA;
+    unsigned v = 0;
+    if (cudaMemcpy(&v, &st->link_timeouts, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return DAK_ERR_CUDA;
+    if (v) {
+        const unsigned z = 0;
+        if (cudaMemcpy(&st->link_timeouts, &z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return DAK_ERR_CUDA;
+    }
+    *count = v;
+    return DAK_OK;
+}
+
 extern "C" dak_status dak_prefetch(const dak_placement* p, void* staging, void* stream) {
     if (!p) return DAK_ERR_INVALID;
     if (p->host_bytes == 0) return DAK_OK;

@@ -354,6 +354,14 @@ dak_status dak_attn_noalloc(const void* Q, const dak_placement* KV, const int* s
  * range. */
 dak_status dak_link_begin(int slot, void* stream);
 
+/* Handoff waits (of any launch, sequence or decode step) that gave up at their bound since
+ * the last call: *count, after the work on `stream` has finished; the count restarts at
+ * zero. A wait that gives up is no error (the CTA streams anyway and results are the
+ * same), only a sign that a sequence's launches were not all ordered on one stream or
+ * that an earlier launch stopped early. dak_last_error zeroes it too when it reports an
+ * error. DAK_ERR_INVALID: count NULL. */
+dak_status dak_link_timeouts(void* stream, uint32_t* count);
+
 /* ---------------------------------------------------------------------------------- *
  * Launch tuner (section 4.3.1, "Congestion Control Strategy": the host-SM cap and the
  * in-flight window are profiled per operation before launch; section 6.2, Fig. 12)
@@ -587,6 +595,12 @@ dak_status dak_alloc_counts(int64_t* host_live, int64_t* device_live);
  * a following dak_last_error() must report DAK_ERR_TIMEOUT (info 0x5E1F in the upper 32
  * bits) and the CUDA context stays usable. The paper has no counterpart. */
 dak_status dak_selftest_wait(void* stream);
+
+/* Self-test of the handoff's pacing wait: one thread waits for a handoff count that stays
+ * at zero; after 0.5 ms it gives up and goes on. Returns when the launch has finished;
+ * dak_link_timeouts then reports 1 and dak_last_error DAK_OK (giving up is not an error).
+ * The paper has no counterpart. */
+dak_status dak_selftest_link(void* stream);
 
 /* Prefetch baseline (section 2.2-2.3, Fig. 2-3): copy a placement's host-resident part into
  * a caller-provided HBM staging buffer (cudaMemcpyAsync on `stream`), so that a following

@@ -181,10 +181,12 @@ def test_decoder_link_handoff_8b_width(dak):
         x, p = _dev(x0), _pos(pos)
         out = torch.empty_like(x)
         dec.capture(x, p, out, 0)
+        dak.dak_link_timeouts()
         for _ in range(3):
             dec.replay()
         torch.cuda.synchronize()
         assert dak.dak_last_error()[0] == 0
+        assert dak.dak_link_timeouts() == 0  # every kernel found its predecessors in time
         outs.append(bits_of(out))
         dec.free()
     assert np.array_equal(outs[0], outs[1])

@@ -31,3 +31,13 @@ def test_bounded_wait_times_out_and_context_survives(dak):
     assert dak.dak_last_error()[0] == 0
     assert og.rel_err(to_np(C), og.gemm_ref(A, B)) <= FP32_OUT_TOL
     p.free()
+
+
+def test_handoff_wait_gives_up_without_error(dak):
+    """The host-link handoff's wait only paces loads: one that nothing releases gives up
+    after its bound, is counted, and raises no error."""
+    dak.dak_link_timeouts()  # start from zero
+    dak.dak_selftest_link()
+    assert dak.dak_link_timeouts() == 1
+    assert dak.dak_link_timeouts() == 0  # read clears it
+    assert dak.dak_last_error()[0] == 0

@@ -44,6 +44,7 @@ def _run(dak, ops, tuning, begin=None):
 @pytest.mark.parametrize("N,tile_m", [(1, 64), (16, 64), (128, 64), (64, 128), (300, 64)])
 def test_gemm_sequence_same_bits(dak, N, tile_m):
     import torch
+    dak.dak_link_timeouts()  # start from zero
     for frac in (0.0, 0.3, 1.0):
         ops = _ops(dak, N, frac, tile_m, seed=N)
         base = [bits_of(c) for c in _run(dak, ops, dict(pdl=1))]
@@ -76,6 +77,7 @@ def test_gemm_sequence_same_bits(dak, N, tile_m):
         for C, b, (_, _, A, B) in zip(outs, base, ops):
             assert np.array_equal(bits_of(C), b), frac
             assert og.rel_err(to_np(C), og.gemm_ref(A, B)) <= FP32_OUT_TOL
+        assert dak.dak_link_timeouts() == 0  # every launch found its predecessors in time
         for p, _, _, _ in ops:
             p.free()
 
@@ -102,11 +104,13 @@ def test_attention_and_gemms_in_one_sequence(dak):
         return [bits_of(c0), bits_of(O), bits_of(c1)]
 
     base = seq(0)
+    dak.dak_link_timeouts()
     for _ in range(2):
         got = seq(2)
         assert dak.dak_last_error()[0] == 0
         for g, b in zip(got, base):
             assert np.array_equal(g, b)
+    assert dak.dak_link_timeouts() == 0
     kv.free()
     for p, _, _, _ in ops:
         p.free()

@@ -559,7 +559,7 @@ static cudaError_t launch_attn_d(const AttnParams& p, int grid, int W, bool pdl,
                             static_cast<const float*>(p.ws), p.O, p.o_fp32, p.n_split);
 }
 
-static dak_status launch_attn_link(const void* Q, const dak_placement* KV, const void* host_src, const int* seq_lens,
+static dak_status launch_attn_kernels(const void* Q, const dak_placement* KV, const void* host_src, const int* seq_lens,
                                    int H_q, float scale, void* O, void* ws, size_t ws_bytes, const dak_tuning* t,
                                    cudaStream_t stream, int o_fp32, const LinkHandoff* link) {
     if (link && link->signals) *link->signals = 0;
@@ -644,7 +644,7 @@ dak_status launch_attn(const void* Q, const dak_placement* KV, const void* host_
         link = &own;
     }
     const dak_status r =
-        launch_attn_link(Q, KV, host_src, seq_lens, H_q, scale, O, ws, ws_bytes, t, stream, o_fp32, link);
+        launch_attn_kernels(Q, KV, host_src, seq_lens, H_q, scale, O, ws, ws_bytes, t, stream, o_fp32, link);
     if (joined && r == DAK_OK) link_commit(t, own_signals);
     return r;
 }

@@ -24,7 +24,11 @@
 // the sequence lengths and the RoPE table) and writes nothing to global memory; after
 // the wait its predecessor, and so every earlier kernel, has finished. The step's first
 // kernel writes the sequence lengths and the RoPE table and does not signal its
-// dependents, so nothing of the step starts before those are complete.
+// dependents, so nothing of the step starts before those are complete. In direct-access
+// mode the step's kernels also hand the host link on from one to the next (LinkHandoff):
+// a kernel's host tiles or requests start streaming once the earlier kernels have issued
+// all of their host loads, instead of filling their rings while the previous kernel still
+// streams and then idling through the boundary.
 #include <algorithm>
 #include <cmath>
 #include <cstring>

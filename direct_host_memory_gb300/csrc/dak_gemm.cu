@@ -2114,7 +2114,7 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
 // once per block; with column_blocks, blocks of 256 rows that each read the host tiles
 // again. Clusters stop at 4 CTAs: forwarding every A chunk to 7 peers measured slower than
 // two launches of 1024 rows.
-static dak_status launch_gemm_blocks(const dak_placement* A, const void* host_src, const void* B, void* C, int N,
+static dak_status launch_gemm_column_blocks(const dak_placement* A, const void* host_src, const void* B, void* C, int N,
                                      int c_fp32, const dak_tuning* t, cudaStream_t stream, void* ws, size_t ws_bytes,
                                      const GemmFuse* fuse, const LinkHandoff* link) {
     if (link && link->signals) *link->signals = 0;
@@ -2147,7 +2147,7 @@ dak_status launch_gemm(const dak_placement* A, const void* host_src, const void*
         own.signals = &own_signals;
         link = &own;
     }
-    const dak_status r = launch_gemm_blocks(A, host_src, B, C, N, c_fp32, t, stream, ws, ws_bytes, fuse, link);
+    const dak_status r = launch_gemm_column_blocks(A, host_src, B, C, N, c_fp32, t, stream, ws, ws_bytes, fuse, link);
     if (joined && r == DAK_OK) link_commit(t, own_signals);
     return r;
 }

@@ -559,9 +559,9 @@ static cudaError_t launch_attn_d(const AttnParams& p, int grid, int W, bool pdl,
                             static_cast<const float*>(p.ws), p.O, p.o_fp32, p.n_split);
 }
 
-static dak_status launch_attn_kernels(const void* Q, const dak_placement* KV, const void* host_src, const int* seq_lens,
-                                   int H_q, float scale, void* O, void* ws, size_t ws_bytes, const dak_tuning* t,
-                                   cudaStream_t stream, int o_fp32, const LinkHandoff* link) {
+static dak_status launch_attn_kernels(const void* Q, const dak_placement* KV, const void* host_src,
+                                      const int* seq_lens, int H_q, float scale, void* O, void* ws, size_t ws_bytes,
+                                      const dak_tuning* t, cudaStream_t stream, int o_fp32, const LinkHandoff* link) {
     if (link && link->signals) *link->signals = 0;
     if (!KV || KV->kind != 1 || !Q || !O) return DAK_ERR_INVALID;
     if (H_q <= 0 || H_q % KV->H_kv) return DAK_ERR_INVALID;

@@ -2114,9 +2114,9 @@ static dak_status launch_gemm_block(const dak_placement* A, const void* host_src
 // once per block; with column_blocks, blocks of 256 rows that each read the host tiles
 // again. Clusters stop at 4 CTAs: forwarding every A chunk to 7 peers measured slower than
 // two launches of 1024 rows.
-static dak_status launch_gemm_column_blocks(const dak_placement* A, const void* host_src, const void* B, void* C, int N,
-                                     int c_fp32, const dak_tuning* t, cudaStream_t stream, void* ws, size_t ws_bytes,
-                                     const GemmFuse* fuse, const LinkHandoff* link) {
+static dak_status launch_gemm_column_blocks(const dak_placement* A, const void* host_src, const void* B, void* C,
+                                            int N, int c_fp32, const dak_tuning* t, cudaStream_t stream, void* ws,
+                                            size_t ws_bytes, const GemmFuse* fuse, const LinkHandoff* link) {
     if (link && link->signals) *link->signals = 0;
     if (!A || A->kind != 0) return DAK_ERR_INVALID;
     if (ws && (reinterpret_cast<uintptr_t>(ws) & 255)) return DAK_ERR_ALIGN;

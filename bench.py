@@ -597,9 +597,9 @@ def run_large_n(dak, lin, b_host, b_hbm, dev, x=0.25, tile_m=128):
 
 def run_linears_n(dak, lin, b_host, b_hbm, dev, xs=(0.0, 0.25), ns=(1, 8, 32, 64)):
     """The four 8B linears (QKV, O, gate+up, down: 436 MB, more than L2) as one graph of four
-    dak_gemm launches, at each offload ratio in xs and each hidden-state row count N in ns
-    (decode batch sizes from one request to 64): time per pass, effective GB/s and the
-    fraction of the tier roofline."""
+    dak_gemm launches (programmatic launch, one host-link handoff sequence), at each offload
+    ratio in xs and each hidden-state row count N in ns (decode batch sizes from one request
+    to 64): time per pass, effective GB/s and the fraction of the tier roofline."""
     import torch
     import synth
     rows = []
@@ -613,8 +613,10 @@ def run_linears_n(dak, lin, b_host, b_hbm, dev, xs=(0.0, 0.25), ns=(1, 8, 32, 64
             Cs = {n: torch.empty((N, A.shape[0]), dtype=torch.bfloat16, device=dev) for n, (A, _) in lin.items()}
 
             def one_pass():
+                if H:  # (all in HBM there is nothing to hand on)
+                    dak.dak_link_begin(7)
                 for n, p in pls.items():
-                    dak.dak_gemm(p, Bs[n], Cs[n], tuning=dict(pdl=1))
+                    dak.dak_gemm(p, Bs[n], Cs[n], tuning=dict(pdl=1, link=7 if H else 0))
             one_pass()
             torch.cuda.synchronize()
             g = torch.cuda.CUDAGraph()
@@ -697,8 +699,9 @@ def run_per_op_x(dak, lin, attn, b_host, b_hbm, dev, ns=(1, 8, 32, 64)):
     pdl = dict(pdl=1)
     linked = dict(pdl=1, link=2)
 
-    def seq(launches):
-        dak.dak_link_begin(2)
+    def seq(launches, begin=True):
+        if begin:  # (all in HBM there is nothing to hand on)
+            dak.dak_link_begin(2)
         for f in launches:
             f()
     for i, (name, (A, _)) in enumerate(lin.items()):
@@ -714,7 +717,8 @@ def run_per_op_x(dak, lin, attn, b_host, b_hbm, dev, ns=(1, 8, 32, 64)):
             C_bytes, H = pls[0].host_bytes + pls[0].hbm_bytes, pls[0].host_bytes
             for N in ns:
                 t1 = single(lambda: dak.dak_gemm(pls[0], Bs[N], Cs[N]))
-                g = _capture(lambda: seq([lambda p=p: dak.dak_gemm(p, Bs[N], Cs[N], tuning=linked) for p in pls]))
+                tun = linked if H else pdl
+                g = _capture(lambda: seq([lambda p=p: dak.dak_gemm(p, Bs[N], Cs[N], tuning=tun) for p in pls], H > 0))
                 tc = time_steps(g.replay, 10, 3) / copies
                 del g
                 rec = dict(x=x, N=N, **point(C_bytes, H, t1, tc))

@@ -75,6 +75,9 @@ __device__ unsigned g_link_count[kLinkSlots];
 static std::mutex g_link_mu;
 static unsigned g_link_after[64][kLinkSlots];
 
+// The device counts of the current device (called with g_link_mu held). A new context (after
+// cudaDeviceReset) starts with the module's counts at zero, so the host-side counts of its
+// sequences restart too.
 static unsigned* link_counts() {
     static unsigned* cache[64] = {nullptr};
     static unsigned long long ctx[64] = {0};
@@ -89,6 +92,7 @@ static unsigned* link_counts() {
         }
         cache[dev] = static_cast<unsigned*>(ptr);
         ctx[dev] = current_context_id();
+        for (int k = 0; k < kLinkSlots; ++k) g_link_after[dev][k] = 0;
     }
     return cache[dev];
 }

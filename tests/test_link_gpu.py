@@ -132,3 +132,55 @@ def test_join_without_begin_and_tuner_ignore_link(dak):
     assert r["best"].get("link", 0) == 0
     for p, _, _, _ in ops:
         p.free()
+
+
+def test_random_sequences(dak):
+    """Random sequences of GEMM launches (N from 1 to 300, 64- and 128-row tiles, any number of
+    host tile rows) and attention launches (any number of host requests), joined in one
+    sequence, eager and captured: the same bits as without the handoff, and no wait gives up."""
+    import torch
+    rng = np.random.default_rng(2024)
+    dak.dak_link_timeouts()
+    for case in range(8):
+        launches = []
+        for j in range(int(rng.integers(3, 7))):
+            if rng.random() < 0.7:
+                tm = int(rng.choice([64, 128]))
+                M, K = int(rng.integers(1, 1500)), int(rng.choice([64, 520, 1024, 4096]))
+                N = int(rng.choice([1, 2, 16, 64, 200, 300]))
+                A, B = synth.gemm_inputs(M, K, N, seed=1000 * case + j)
+                T = -(-M // tm)
+                p = dak.dak_place_matrix(A, int(rng.integers(0, T + 1)), tile_m=tm)
+                launches.append(("gemm", p, to_dev(B)))
+            else:
+                Bq, Hkv, G, L = int(rng.integers(1, 20)), int(rng.choice([1, 2, 8])), int(rng.choice([1, 4])), \
+                    int(rng.integers(1, 900))
+                q, k, v = synth.attn_inputs(Bq, Hkv * G, Hkv, 128, L, seed=1000 * case + j)
+                kv = dak.dak_place_kv(k, v, int(rng.integers(0, Bq + 1)))
+                Qd = torch.from_numpy(q.view("int16")).view(torch.bfloat16).cuda()
+                ns = dak.dak_attn_default_split(kv)
+                ws = torch.empty(max(1, dak.dak_attn_workspace_bytes(Bq, Hkv * G, 128, ns) // 4),
+                                 dtype=torch.float32, device="cuda")
+                launches.append(("attn", kv, Qd, ws, ns))
+
+        def run(link):
+            outs = []
+            if link:
+                dak.dak_link_begin(5)
+            for ln in launches:
+                t = dict(pdl=1, link=link)
+                if ln[0] == "gemm":
+                    outs.append(dak.dak_gemm(ln[1], ln[2], c_fp32=True, tuning=t))
+                else:
+                    outs.append(dak.dak_attn(ln[2], ln[1], workspace=ln[3], tuning=dict(t, n_split=ln[4])))
+            return outs
+
+        base = [bits_of(o) for o in run(0)]
+        for link in (5, 5):
+            got = run(link)
+            assert dak.dak_last_error()[0] == 0
+            for g, b in zip(got, base):
+                assert np.array_equal(bits_of(g), b), case
+        assert dak.dak_link_timeouts() == 0, case
+        for ln in launches:
+            ln[1].free()

@@ -47,7 +47,7 @@ def _args():
                          "at --decode-x and all in HBM")
     ap.add_argument("--decode-x", type=float, default=0.3, help="x_global of the decode step's HBM cap")
     ap.add_argument("--decode-steps", type=int, default=20)
-    ap.add_argument("--decode-sweep", default="0.1,0.2,0.5",
+    ap.add_argument("--decode-sweep", default="0.03,0.05,0.1,0.2,0.5",
                     help="further x_global values for the decode step (comma list, empty = none)")
     ap.add_argument("--no-planner-check", action="store_true",
                     help="skip the compute-bound / greedy-vs-uniform planner measurement")
@@ -174,7 +174,8 @@ def decode_ops(cfg, peak_flops):
     """The planner's view of one decode step, one entry per operation type (every layer is
     alike, so each type gets one ratio for all layers): the four weight products and the
     attention over the KV cache, with their bytes and compute time over all layers at
-    peak_flops, and their placement unit (a 64-row tile row or one request's KV)."""
+    peak_flops, and their placement unit (a 64-row tile row, or one (request, kv head) slab
+    of the KV cache: dak_place_kv_heads)."""
     import synth
     sh = synth.decoder_shapes(cfg)
     nl, B, L, D = cfg["n_layers"], cfg["batch"], cfg["context"], cfg["head_dim"]
@@ -184,13 +185,13 @@ def decode_ops(cfg, peak_flops):
         M, K = sh[k]
         ops.append((nl * M * K * 2, nl * 2.0 * M * K * B / peak_flops, 64 * K * 2))
         meta.append((k, -(-M // 64)))
-    ops.append((nl * B * kv_req, nl * 4.0 * B * cfg["n_heads"] * L * D / peak_flops, kv_req))
-    meta.append(("kv", B))
+    ops.append((nl * B * kv_req, nl * 4.0 * B * cfg["n_heads"] * L * D / peak_flops, kv_req // cfg["n_kv_heads"]))
+    meta.append(("kv_heads", B * cfg["n_kv_heads"]))
     return ops, meta
 
 
 def decode_plan(dak, cfg, b_host, b_hbm, x_global, peak_flops):
-    """Host units per operation type (tile rows or requests, the same in every layer) for an
+    """Host units per operation type (tile rows or KV slabs, the same in every layer) for an
     HBM cap of (1 - x_global) of all bytes, from the library's whole-unit planner
     (dak_plan_units: the greedy ratios floored to whole units and topped up where the model
     time grows least). x_global = 0: no offload."""

@@ -32,6 +32,7 @@ EXPORTS = [
     "dak_place_matrix_glu", "dak_plan_units", "dak_gemm_workspace_bytes", "dak_gemm_ws", "dak_gemm_plan", "dak_gemm_launch_plan",
     "dak_attn_f32", "dak_inject_fault", "dak_fault_pending", "dak_alloc_counts", "dak_gemm_chain",
     "dak_gemm_chain_workspace_bytes", "dak_link_begin", "dak_link_timeouts", "dak_selftest_link",
+    "dak_place_kv_heads",
 ]
 
 # host-side fault injection kinds (DAK_FAULT_* in dak.h)
@@ -100,6 +101,7 @@ def _load():
         "dak_status_string": (ctypes.c_char_p, [i32]),
         "dak_place_matrix": (i32, [vp, i32, i64, i64, i64, i32, i32, P(vp)]),
         "dak_place_kv": (i32, [vp, vp, i32, i32, i32, i32, i32, i32, P(vp)]),
+        "dak_place_kv_heads": (i32, [vp, vp, i32, i32, i32, i32, i32, i32, P(vp)]),
         "dak_place_matrix_glu": (i32, [vp, i32, i64, i64, i64, i32, i32, P(vp)]),
         "dak_free": (i32, [vp]),
         "dak_placement_info": (i32, [vp, P(i64), P(i64), P(i64), P(i64)]),
@@ -236,6 +238,11 @@ def host_requests_for_ratio(x: float, batch: int) -> int:
     return max(0, min(int(batch), math.ceil(float(x) * int(batch) - 1e-12)))
 
 
+def host_heads_for_ratio(x: float, batch: int, h_kv: int) -> int:
+    """(request, kv head) slabs whose KV goes to the host for offload ratio x: ceil(x * B * H_kv)."""
+    return host_requests_for_ratio(x, int(batch) * int(h_kv))
+
+
 def dak_place_matrix(A, n_host_tiles: int, tile_m: int = 64) -> Placement:
     """Place weights A [M][K] (bf16: torch tensor on host or device, or numpy uint16 bits)."""
     if A.ndim != 2:
@@ -267,6 +274,18 @@ def dak_place_kv(K, V, n_host_requests: int) -> Placement:
     out = ctypes.c_void_p()
     _check(lib.dak_place_kv(_ptr(K), _ptr(V), _on_device(K), B, Hkv, L, D, int(n_host_requests),
                             ctypes.byref(out)), "dak_place_kv")
+    return Placement(out, "kv", B=B, H_kv=Hkv, L=L, D=D)
+
+
+def dak_place_kv_heads(K, V, n_host_heads: int) -> Placement:
+    """dak_place_kv by (request, kv head) slab: the first n_host_heads slabs in request-major
+    order (request b, head g is slab b * H_kv + g) go to the host."""
+    if K.shape != V.shape or K.ndim != 4:
+        raise ValueError("K and V must both be [B][H_kv][L][D]")
+    B, Hkv, L, D = (int(s) for s in K.shape)
+    out = ctypes.c_void_p()
+    _check(lib.dak_place_kv_heads(_ptr(K), _ptr(V), _on_device(K), B, Hkv, L, D, int(n_host_heads),
+                                  ctypes.byref(out)), "dak_place_kv_heads")
     return Placement(out, "kv", B=B, H_kv=Hkv, L=L, D=D)
 
 
@@ -674,7 +693,8 @@ class Decoder:
 def place_decoder_layer(weights: dict, kv, host_units: dict, device=None, glu: bool = True) -> dict:
     """Place one layer: weights maps 'qkv', 'o', 'gate_up', 'down' to [out][in] bf16 sources
     (numpy bits or torch) and 'attn_norm', 'mlp_norm' to [d] gains; kv = (K, V) sources
-    [B][H_kv][L][D]; host_units maps each of DECODER_OPS to its host tile rows / requests.
+    [B][H_kv][L][D]; host_units maps 'qkv', 'o', 'gate_up', 'down' to their host tile rows
+    and either 'kv' to host requests or 'kv_heads' to host (request, kv head) slabs.
     glu places gate_up interleaved so that the SwiGLU runs in the GEMM's epilogue."""
     import torch
     dev = device or torch.device("cuda")
@@ -684,7 +704,10 @@ def place_decoder_layer(weights: dict, kv, host_units: dict, device=None, glu: b
             L[k] = dak_place_matrix_glu(weights[k], int(host_units[k]))
         else:
             L[k] = dak_place_matrix(weights[k], int(host_units[k]))
-    L["kv"] = dak_place_kv(kv[0], kv[1], int(host_units["kv"]))
+    if "kv_heads" in host_units:
+        L["kv"] = dak_place_kv_heads(kv[0], kv[1], int(host_units["kv_heads"]))
+    else:
+        L["kv"] = dak_place_kv(kv[0], kv[1], int(host_units["kv"]))
     for k in ("attn_norm", "mlp_norm"):
         g = weights[k]
         if isinstance(g, np.ndarray):

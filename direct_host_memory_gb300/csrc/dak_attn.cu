@@ -41,7 +41,7 @@ struct AttnParams {
     void* O;                 // [B][Hq][D], bf16 or (o_fp32) fp32
     int o_fp32;
     float* ws;               // [B][Hq][n_split][D + 2] partials: m (log2 domain), l, o[D]
-    int B, Hq, Hkv, G, L, h_r, n_split, split_len;
+    int B, Hq, Hkv, G, L, h_s, n_split, split_len;  // h_s: host slabs (request-major)
     int wait_newest;         // stream the chunk holding token L_b - 1 only after the previous kernel
     float scale_log2;
     long long head_bytes;    // bytes of one (request, kv head) slab
@@ -100,9 +100,8 @@ __device__ __forceinline__ Unit decode_unit(const AttnParams& p, long long u, in
     x.Lb = Lb;
     x.t0 = x.s * p.split_len;
     x.t1 = min(Lb, x.t0 + p.split_len);
-    const int lb = tier == 0 ? x.b : x.b - p.h_r;
-    const long long head = static_cast<long long>(lb) * p.Hkv + x.g;
-    x.base = p.kv[tier] + head * p.head_bytes;
+    const long long slab = static_cast<long long>(x.b) * p.Hkv + x.g;  // its index in the tier
+    x.base = p.kv[tier] + (tier == 0 ? slab : slab - p.h_s) * p.head_bytes;
     return x;
 }
 
@@ -576,7 +575,7 @@ static dak_status launch_attn_kernels(const void* Q, const dak_placement* KV, co
     const size_t need = dak_attn_workspace_bytes(KV->B, H_q, KV->D, n_split);
     if (need > 0 && (!ws || ws_bytes < need)) return DAK_ERR_INVALID;
     if (need > 0 && (reinterpret_cast<uintptr_t>(ws) & 7)) return DAK_ERR_ALIGN;  // the combine reads float2
-    if (KV->h_r > 0 && !host_src) return DAK_ERR_INVALID;
+    if (KV->h_s > 0 && !host_src) return DAK_ERR_INVALID;
 
     AttnParams p{};
     p.Q = static_cast<const __nv_bfloat16*>(Q);
@@ -591,7 +590,7 @@ static dak_status launch_attn_kernels(const void* Q, const dak_placement* KV, co
     p.Hkv = KV->H_kv;
     p.G = G;
     p.L = KV->L;
-    p.h_r = KV->h_r;
+    p.h_s = KV->h_s;
     p.n_split = n_split;
     p.split_len = ((KV->L + n_split - 1) / n_split + kChunkTok - 1) / kChunkTok * kChunkTok;
     const float sc = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(KV->D));
@@ -599,8 +598,8 @@ static dak_status launch_attn_kernels(const void* Q, const dak_placement* KV, co
     p.head_bytes = KV->head_bytes;
     p.st = status_ptr();
     if (!p.st) return DAK_ERR_CUDA;
-    p.host_units = static_cast<long long>(KV->h_r) * KV->H_kv * n_split;
-    p.hbm_units = static_cast<long long>(KV->B - KV->h_r) * KV->H_kv * n_split;
+    p.host_units = static_cast<long long>(KV->h_s) * n_split;
+    p.hbm_units = (static_cast<long long>(KV->B) * KV->H_kv - KV->h_s) * n_split;
     const int host_units_i = static_cast<int>(std::min<long long>(p.host_units, 1 << 30));
     const int hbm_units_i = static_cast<int>(std::min<long long>(p.hbm_units, 1 << 30));
     int W_ring = (t && t->hbm_window > 0) ? std::min(t->hbm_window, kAttnMaxStages) : kAttnStages;
@@ -679,7 +678,7 @@ extern "C" dak_status dak_attn_f32(const void* Q, const dak_placement* KV, const
 extern "C" dak_status dak_attn_staged(const void* Q, const dak_placement* KV, const void* staging,
                                       const int* seq_lens, int H_q, float scale, void* O, void* workspace,
                                       size_t ws_bytes, const dak_tuning* tuning, void* stream) {
-    if (!KV || (KV->h_r > 0 && !staging)) return DAK_ERR_INVALID;
+    if (!KV || (KV->h_s > 0 && !staging)) return DAK_ERR_INVALID;
     if (reinterpret_cast<uintptr_t>(staging) & 15) return DAK_ERR_ALIGN;
     return dak::launch_attn(Q, KV, staging, seq_lens, H_q, scale, O, workspace, ws_bytes, tuning,
                             static_cast<cudaStream_t>(stream));

@@ -190,7 +190,7 @@ struct RopeArgs {
     uint8_t* kv_host_copy;     // a staged copy of the host tier to update too, or null
     uint8_t* kv_hbm;
     long long head_bytes;
-    int Hq, Hkv, D, L, h_r;
+    int Hq, Hkv, D, L, h_s;  // h_s: (request, kv head) slabs on the host, request-major
     DevStatus* st;
 };
 
@@ -229,13 +229,13 @@ __global__ void __launch_bounds__(64) rope_append_kernel(const RopeArgs a) {
         const uint4 piece = reinterpret_cast<const uint4*>(row)[i];
         const long long off = static_cast<long long>(pos >> 6) * (2ll * 64 * a.D * 2) + (is_v ? 64ll * a.D * 2 : 0ll) +
                               static_cast<long long>(pos & 63) * a.D * 2 + ((i ^ (pos & 7)) << 4);
-        if (b < a.h_r) {
-            const long long slab = (static_cast<long long>(b) * a.Hkv + g) * a.head_bytes;
-            *reinterpret_cast<uint4*>(a.kv_host + slab + off) = piece;
-            if (a.kv_host_copy) *reinterpret_cast<uint4*>(a.kv_host_copy + slab + off) = piece;
+        const long long slab = static_cast<long long>(b) * a.Hkv + g;
+        if (slab < a.h_s) {
+            const long long at = slab * a.head_bytes + off;
+            *reinterpret_cast<uint4*>(a.kv_host + at) = piece;
+            if (a.kv_host_copy) *reinterpret_cast<uint4*>(a.kv_host_copy + at) = piece;
         } else {
-            const long long slab = (static_cast<long long>(b - a.h_r) * a.Hkv + g) * a.head_bytes;
-            *reinterpret_cast<uint4*>(a.kv_hbm + slab + off) = piece;
+            *reinterpret_cast<uint4*>(a.kv_hbm + (slab - a.h_s) * a.head_bytes + off) = piece;
         }
     }
 }
@@ -479,7 +479,7 @@ dak_status enqueue_step(dak_decoder* d, const void* x_in, const int* positions, 
         ra.Hkv = Hkv;
         ra.D = D;
         ra.L = L.kv->L;
-        ra.h_r = L.kv->h_r;
+        ra.h_s = L.kv->h_s;
         ra.st = st;
         if ((r = cuda_status(launch(rope_append_kernel, dim3(static_cast<unsigned>(B), static_cast<unsigned>(Hq + 2 * Hkv)),
                                     D / 2, pdl, s, ra))) != DAK_OK)

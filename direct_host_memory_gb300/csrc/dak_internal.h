@@ -24,7 +24,7 @@ struct dak_placement {
     int64_t tile_bytes;
     // kv
     int B, H_kv, L, D;
-    int h_r;                // requests on the host
+    int h_s;                // (request, kv head) slabs on the host: the first h_s in request-major order
     int64_t head_bytes;     // one (request, kv head) slab: ceil(L/64) chunks of [K 64 x D][V 64 x D] bf16
 };
 

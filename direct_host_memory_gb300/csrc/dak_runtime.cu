@@ -525,14 +525,16 @@ extern "C" dak_status dak_place_matrix_glu(const void* A_src, int src_on_device,
     return place_matrix(A_src, src_on_device, 2 * f, K, lda, tile_m, n_host_tiles, true, out);
 }
 
-extern "C" dak_status dak_place_kv(const void* K_src, const void* V_src, int src_on_device, int B, int H_kv, int L,
-                                   int D, int n_host_requests, dak_placement** out) {
+extern "C" dak_status dak_place_kv_heads(const void* K_src, const void* V_src, int src_on_device, int B, int H_kv,
+                                         int L, int D, int n_host_heads, dak_placement** out) {
     if (!out) return DAK_ERR_INVALID;
     *out = nullptr;
     if (B <= 0 || H_kv <= 0 || L <= 0 || !K_src || !V_src) return DAK_ERR_INVALID;
+    if (static_cast<long long>(B) * H_kv > (1ll << 30)) return DAK_ERR_INVALID;
     if (D != 64 && D != 128) return DAK_ERR_UNSUPPORTED;
     if ((reinterpret_cast<uintptr_t>(K_src) & 15) || (reinterpret_cast<uintptr_t>(V_src) & 15)) return DAK_ERR_ALIGN;
-    if (n_host_requests < 0 || n_host_requests > B) return DAK_ERR_INVALID;
+    const int S = B * H_kv;  // (request, kv head) slabs, request-major
+    if (n_host_heads < 0 || n_host_heads > S) return DAK_ERR_INVALID;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return DAK_ERR_CUDA;
 
@@ -544,13 +546,12 @@ extern "C" dak_status dak_place_kv(const void* K_src, const void* V_src, int src
     p->H_kv = H_kv;
     p->L = L;
     p->D = D;
-    p->h_r = n_host_requests;
+    p->h_s = n_host_heads;
     const int64_t n_chunks = (L + 63) / 64;
     p->head_bytes = n_chunks * 2 * 64 * D * 2;  // one (request, kv head) slab: K and V chunks
-    const int64_t req_bytes = p->head_bytes * H_kv;
-    const int64_t src_req_bytes = static_cast<int64_t>(L) * D * 2 * H_kv;  // K (or V) of one request in the source
-    p->host_bytes = req_bytes * p->h_r;
-    p->hbm_bytes = req_bytes * (B - p->h_r);
+    const int64_t src_slab_bytes = static_cast<int64_t>(L) * D * 2;  // K (or V) of one slab in the source
+    p->host_bytes = p->head_bytes * p->h_s;
+    p->hbm_bytes = p->head_bytes * (S - p->h_s);
     dak_status st = alloc_tiers(p);
     if (st != DAK_OK) {
         free_parts(p);
@@ -562,10 +563,10 @@ extern "C" dak_status dak_place_kv(const void* K_src, const void* V_src, int src
     if (p->host_bytes) std::memset(p->host_ptr, 0, static_cast<size_t>(p->host_bytes));
     if (p->hbm_bytes) e = cudaMemset(p->hbm_ptr, 0, static_cast<size_t>(p->hbm_bytes));
     const int D16 = D / 8;
-    const int batch = std::max(1, static_cast<int>((256ll << 20) / src_req_bytes));
+    const int batch = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(S, (256ll << 20) / src_slab_bytes)));
     void* tmp = nullptr;
     if (!src_on_device && e == cudaSuccess) {
-        e = dev_alloc(&tmp, static_cast<size_t>(std::min(batch, B)) * src_req_bytes);
+        e = dev_alloc(&tmp, static_cast<size_t>(batch) * src_slab_bytes);
         if (e != cudaSuccess) {
             cudaGetLastError();
             free_parts(p);
@@ -575,25 +576,25 @@ extern "C" dak_status dak_place_kv(const void* K_src, const void* V_src, int src
     }
     for (int kv = 0; kv < 2 && e == cudaSuccess; ++kv) {
         const uint8_t* srcb = static_cast<const uint8_t*>(kv == 0 ? K_src : V_src);
-        int nb = 0;
-        for (int b0 = 0; b0 < B && e == cudaSuccess; b0 += nb) {
-            // keep a batch within one tier
-            nb = std::min(batch, B - b0);
-            if (b0 < p->h_r) nb = std::min(nb, p->h_r - b0);
+        int ns = 0;
+        for (int s0 = 0; s0 < S && e == cudaSuccess; s0 += ns) {
+            // a batch of slabs (the source holds each slab contiguously), kept within one tier
+            ns = std::min(batch, S - s0);
+            if (s0 < p->h_s) ns = std::min(ns, p->h_s - s0);
             const uint4* src;
             if (src_on_device) {
-                src = reinterpret_cast<const uint4*>(srcb + static_cast<long long>(b0) * src_req_bytes);
+                src = reinterpret_cast<const uint4*>(srcb + static_cast<long long>(s0) * src_slab_bytes);
             } else {
-                e = cudaMemcpy(tmp, srcb + static_cast<long long>(b0) * src_req_bytes,
-                               static_cast<size_t>(nb) * src_req_bytes, cudaMemcpyHostToDevice);
+                e = cudaMemcpy(tmp, srcb + static_cast<long long>(s0) * src_slab_bytes,
+                               static_cast<size_t>(ns) * src_slab_bytes, cudaMemcpyHostToDevice);
                 src = reinterpret_cast<const uint4*>(tmp);
             }
             if (e != cudaSuccess) break;
-            const bool host = b0 < p->h_r;
-            const int lb = host ? b0 : b0 - p->h_r;
+            const bool host = s0 < p->h_s;
+            const int ls = host ? s0 : s0 - p->h_s;
             uint8_t* tier = static_cast<uint8_t*>(host ? p->host_dev : p->hbm_ptr);
-            uint8_t* dstb = tier + static_cast<long long>(lb) * req_bytes;
-            const long long n_heads = static_cast<long long>(nb) * H_kv;
+            uint8_t* dstb = tier + static_cast<long long>(ls) * p->head_bytes;
+            const long long n_heads = ns;
             const long long units = n_heads * L * D16;
             pack_kv_kernel<<<pack_grid(units), 256>>>(src, n_heads, L, D16, kv, p->head_bytes / 16,
                                                       reinterpret_cast<uint4*>(dstb));
@@ -610,6 +611,14 @@ extern "C" dak_status dak_place_kv(const void* K_src, const void* V_src, int src
     }
     *out = p;
     return DAK_OK;
+}
+
+extern "C" dak_status dak_place_kv(const void* K_src, const void* V_src, int src_on_device, int B, int H_kv, int L,
+                                   int D, int n_host_requests, dak_placement** out) {
+    // whole requests: their H_kv slabs each (an out-of-range count stays out of range)
+    const bool ok = B > 0 && H_kv > 0 && static_cast<long long>(B) * H_kv <= (1ll << 30) && n_host_requests >= 0 &&
+                    n_host_requests <= B;
+    return dak_place_kv_heads(K_src, V_src, src_on_device, B, H_kv, L, D, ok ? n_host_requests * H_kv : -1, out);
 }
 
 extern "C" dak_status dak_inject_fault(int kind, int skip, int count) {
@@ -647,8 +656,8 @@ extern "C" dak_status dak_placement_info(const dak_placement* p, int64_t* host_b
     if (host_bytes) *host_bytes = p->host_bytes;
     if (hbm_bytes) *hbm_bytes = p->hbm_bytes;
     const int per = (p->kind == 0 && p->tile_m > kTileM) ? p->tile_m / kTileM : 1;  // tiles, not 64-row rows
-    if (units) *units = p->kind == 0 ? p->T / per : p->B;
-    if (host_units) *host_units = p->kind == 0 ? p->h / per : p->h_r;
+    if (units) *units = p->kind == 0 ? p->T / per : static_cast<int64_t>(p->B) * p->H_kv;
+    if (host_units) *host_units = p->kind == 0 ? p->h / per : p->h_s;
     return DAK_OK;
 }
 

@@ -132,5 +132,5 @@ extern "C" dak_status dak_tune_attn(const void* Q, const dak_placement* KV, cons
     auto fn = [&](const dak_tuning* t, cudaStream_t s) {
         return dak::launch_attn(Q, KV, KV->host_dev, seq_lens, H_q, 0.f, O, workspace, ws_bytes, t, s);
     };
-    return tune(fn, KV->h_r > 0, false, reps, base, out);
+    return tune(fn, KV->h_s > 0, false, reps, base, out);
 }

@@ -152,11 +152,22 @@ dak_status dak_place_matrix_glu(const void* A_src, int src_on_device, int64_t f,
 dak_status dak_place_kv(const void* K_src, const void* V_src, int src_on_device, int B, int H_kv, int L, int D,
                         int n_host_requests, dak_placement** out);
 
+/* dak_place_kv at the granularity of one (request, kv head) slab: the first n_host_heads
+ * slabs in request-major order (request b, head g is slab b * H_kv + g) go to the host and
+ * the rest to HBM, 0 <= n_host_heads <= B * H_kv (dak_place_kv places n_host_requests *
+ * H_kv). Every (request, kv head) still attends within one tier, so the attention computes
+ * the same result bit for bit whatever the split; a request may now have heads in both
+ * tiers. A finer unit lets a planner give the cache a ratio close to its turning point
+ * when the host budget is small (one request of 16 is 6% of the cache, one slab 0.8%). */
+dak_status dak_place_kv_heads(const void* K_src, const void* V_src, int src_on_device, int B, int H_kv, int L,
+                              int D, int n_host_heads, dak_placement** out);
+
 /* Release a placement (host and HBM parts). NULL is accepted. */
 dak_status dak_free(dak_placement* p);
 
 /* Sizes of a placement: bytes in host memory and in HBM, number of units (tiles of tile_m
- * rows, or requests) and how many are on the host. Any output pointer may be NULL. */
+ * rows, or (request, kv head) slabs of a KV cache) and how many are on the host. Any
+ * output pointer may be NULL. */
 dak_status dak_placement_info(const dak_placement* p, int64_t* host_bytes, int64_t* hbm_bytes, int64_t* units,
                               int64_t* host_units);
 

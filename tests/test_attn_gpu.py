@@ -149,3 +149,46 @@ def test_decode_gqa_full_size_sampled(dak):
     got = np.stack([O[b, h] for b, h in sorted(picks)])
     ref = np.stack([oa.decode_attention_one(q, k, v, b, h) for b, h in sorted(picks)])
     assert og.rel_err(got, ref) <= REL_TOL
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_head_granular_placement(dak, D):
+    """dak_place_kv_heads: the first h (request, kv head) slabs on the host, so a request may
+    have heads in both tiers. Every slab attends within its tier: the output is the same bit
+    for bit for every h (device and host sources, eager and staged), matches the oracle, and
+    the placement reports slabs."""
+    import torch
+    B, Hq, Hkv, L = 5, 8, 2, 300
+    q, k, v = synth.attn_inputs(B, Hq, Hkv, D, L, seed=31 + D)
+    ref = oa.decode_attention_ref(q, k, v)
+    qt = to_dev(q)
+    base = None
+    slab = -(-L // 64) * 2 * 64 * D * 2
+    for h in range(B * Hkv + 1):
+        src = (to_dev(k), to_dev(v)) if h % 2 else (k, v)
+        p = dak.dak_place_kv_heads(src[0], src[1], h)
+        info = dak.dak_placement_info(p)
+        assert (info["units"], info["host_units"], info["host_bytes"]) == (B * Hkv, h, h * slab)
+        O = dak.dak_attn(qt, p, tuning=dict(n_split=2))
+        assert dak.dak_last_error()[0] == 0
+        if base is None:
+            base = bits_of(O)
+            assert og.rel_err(to_np(O), ref) <= REL_TOL
+        assert np.array_equal(bits_of(O), base), h
+        if h in (3, 7):
+            staging = torch.empty(max(16, p.host_bytes), dtype=torch.uint8, device="cuda")
+            dak.dak_prefetch(p, staging)
+            staged = dak.dak_attn_staged(qt, p, staging, tuning=dict(n_split=2))
+            assert dak.dak_last_error()[0] == 0
+            assert np.array_equal(bits_of(staged), base), h
+        p.free()
+    # whole requests through either entry point: the same placement
+    a = dak.dak_place_kv(k, v, 2)
+    b = dak.dak_place_kv_heads(k, v, 2 * Hkv)
+    assert dak.dak_placement_info(a) == dak.dak_placement_info(b)
+    a.free()
+    b.free()
+    with pytest.raises(dak.DakError):
+        dak.dak_place_kv_heads(k, v, B * Hkv + 1)
+    with pytest.raises(dak.DakError):
+        dak.dak_place_kv_heads(k, v, -1)

@@ -27,15 +27,16 @@ def test_decode_ops_bytes_and_units():
     cfg = dict(synth.DECODER_8B)
     ops, meta = bench.decode_ops(cfg, peak_flops=1.7e15)
     names = [k for k, _ in meta]
-    assert names == ["qkv", "o", "gate_up", "down", "kv"]
+    assert names == ["qkv", "o", "gate_up", "down", "kv_heads"]
     nl, B, L = cfg["n_layers"], cfg["batch"], cfg["context"]
     d, f, D = cfg["hidden"], cfg["ffn"], cfg["head_dim"]
     qkv_rows = (cfg["n_heads"] + 2 * cfg["n_kv_heads"]) * D
     want = {"qkv": qkv_rows * d, "o": d * cfg["n_heads"] * D, "gate_up": 2 * f * d, "down": d * f}
     for (C, tc, tile), (k, units) in zip(ops, meta):
-        if k == "kv":
-            per_req = 2 * cfg["n_kv_heads"] * L * D * 2
-            assert C == nl * B * per_req and tile == per_req and units == B
+        if k == "kv_heads":
+            per_slab = 2 * L * D * 2  # K and V of one (request, kv head)
+            Hkv = cfg["n_kv_heads"]
+            assert C == nl * B * Hkv * per_slab and tile == per_slab and units == B * Hkv
         else:
             assert C == nl * want[k] * 2
             M = want[k] // (d if k != "down" else f)

@@ -192,6 +192,35 @@ def test_decoder_link_handoff_8b_width(dak):
     assert np.array_equal(outs[0], outs[1])
 
 
+def test_decoder_kv_head_granular_placement(dak):
+    """KV caches placed by (request, kv head) slab, with a request split between the tiers
+    (its first kv head on the host, its second in HBM): three consecutive steps append each
+    new key and value into the right tier and match the oracle, and equal the all-HBM
+    decoder bit for bit, in every mode."""
+    cfg, B, L = SMALL64, 3, 150
+    layers, caches, fnorm, _ = _inputs(cfg, B, L, seed=17)
+    units = dict(_host_units(cfg, B, 0.3))
+    del units["kv"]
+    outs = {}
+    for name, kvh in (("split", 3), ("hbm", 0)):
+        u = dict(units, kv_heads=kvh) if name == "split" else dict(_host_units(cfg, B, 0.0))
+        ocfg = _ocfg(cfg)
+        dec = _build(dak, cfg, layers, caches, fnorm, u)
+        ocaches = caches
+        pos = np.array([5, 70, 130])
+        res = []
+        for t in range(3):
+            x = synth.normal_bf16(17, 600 + t, B * cfg["hidden"]).reshape(B, cfg["hidden"])
+            ref, ocaches = od.decode_step(ocfg, x, layers, ocaches, pos + t, fnorm)
+            out = _run(dak, dec, x, pos + t, graph=(t == 2))
+            assert og.rel_err(to_np(out), ref) <= REL_TOL, (name, t)
+            res.append(bits_of(out))
+        outs[name] = res
+        dec.free()
+    for a, b in zip(outs["split"], outs["hbm"]):
+        assert np.array_equal(a, b)
+
+
 def test_decoder_fused_swiglu_matches_separate_kernel(dak):
     """SwiGLU in the gate/up GEMM's epilogue (interleaved placement) against the separate
     SwiGLU kernel: same expression on the same fp32 accumulators, identical outputs."""

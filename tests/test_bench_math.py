@@ -45,3 +45,19 @@ def test_decode_ops_bytes_and_units():
             assert tc == pytest.approx(nl * 2.0 * want[k] * B / 1.7e15)
     # one step of the 8B shape: 22.5 GB of weights and KV
     assert sum(o[0] for o in ops) == pytest.approx(22.55e9, rel=2e-3)
+
+
+def test_ratio_to_units_matches_the_oracle():
+    """The package's caller-side rounding of a ratio to host units (tile rows, requests,
+    (request, kv head) slabs) is the oracle's ceil(x * units)."""
+    import __graft_entry__
+    __graft_entry__.build()
+    import direct_host_memory_gb300 as dak
+    from oracle import placement as opl
+    for x in (0.0, 0.01, 0.03, 0.05, 0.1, 0.125, 0.25, 1 / 3, 0.5, 0.99, 1.0):
+        for M in (64, 1000, 6144, 28672):
+            assert dak.host_tiles_for_ratio(x, M) == opl.n_host_tiles(x, M, 64)
+            assert dak.host_tiles_for_ratio(x, M, 128) == opl.n_host_tiles(x, M, 128)
+        for B, Hkv in ((1, 8), (16, 8), (32, 8), (5, 2)):
+            assert dak.host_requests_for_ratio(x, B) == opl.n_host_requests(x, B)
+            assert dak.host_heads_for_ratio(x, B, Hkv) == opl.n_host_requests(x, B * Hkv)

@@ -32,7 +32,7 @@ EXPORTS = [
     "dak_place_matrix_glu", "dak_plan_units", "dak_gemm_workspace_bytes", "dak_gemm_ws", "dak_gemm_plan", "dak_gemm_launch_plan",
     "dak_attn_f32", "dak_inject_fault", "dak_fault_pending", "dak_alloc_counts", "dak_gemm_chain",
     "dak_gemm_chain_workspace_bytes", "dak_link_begin", "dak_link_timeouts", "dak_selftest_link",
-    "dak_place_kv_heads",
+    "dak_place_kv_heads", "dak_kv_append",
 ]
 
 # host-side fault injection kinds (DAK_FAULT_* in dak.h)
@@ -102,6 +102,7 @@ def _load():
         "dak_place_matrix": (i32, [vp, i32, i64, i64, i64, i32, i32, P(vp)]),
         "dak_place_kv": (i32, [vp, vp, i32, i32, i32, i32, i32, i32, P(vp)]),
         "dak_place_kv_heads": (i32, [vp, vp, i32, i32, i32, i32, i32, i32, P(vp)]),
+        "dak_kv_append": (i32, [vp, vp, vp, vp, vp]),
         "dak_place_matrix_glu": (i32, [vp, i32, i64, i64, i64, i32, i32, P(vp)]),
         "dak_free": (i32, [vp]),
         "dak_placement_info": (i32, [vp, P(i64), P(i64), P(i64), P(i64)]),
@@ -287,6 +288,21 @@ def dak_place_kv_heads(K, V, n_host_heads: int) -> Placement:
     _check(lib.dak_place_kv_heads(_ptr(K), _ptr(V), _on_device(K), B, Hkv, L, D, int(n_host_heads),
                                   ctypes.byref(out)), "dak_place_kv_heads")
     return Placement(out, "kv", B=B, H_kv=Hkv, L=L, D=D)
+
+
+def dak_kv_append(KV: Placement, k_new, v_new, positions, stream=None):
+    """Write one new token per (request, kv head) into a placed cache: k_new and v_new bf16
+    CUDA [B][H_kv][D], positions int32 CUDA [B] (the row each request's token goes to)."""
+    import torch
+    _check_bf16_cuda(k_new, "k_new")
+    _check_bf16_cuda(v_new, "v_new")
+    shape = (KV.meta["B"], KV.meta["H_kv"], KV.meta["D"])
+    if tuple(k_new.shape) != shape or tuple(v_new.shape) != shape:
+        raise ValueError(f"k_new / v_new must be {list(shape)}")
+    if positions.dtype != torch.int32 or not positions.is_cuda or positions.numel() != shape[0]:
+        raise ValueError("positions must be int32 CUDA [B]")
+    _check(lib.dak_kv_append(KV.handle, _ptr(k_new), _ptr(v_new), _ptr(positions), _stream_ptr(stream)),
+           "dak_kv_append")
 
 
 def dak_free(p: Placement):

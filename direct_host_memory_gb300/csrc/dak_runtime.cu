@@ -1043,6 +1043,48 @@ extern "C" dak_status dak_link_timeouts(void* stream, uint32_t* count) {
     return DAK_OK;
 }
 
+// Append one token's key and value per (request, kv head) to a placed cache: block (b, g)
+// writes k_new[b][g] and v_new[b][g] into the slab of (b, g), in whichever tier holds it, at
+// row positions[b] of its chunk layout (16-byte piece c of token j stored at c ^ (j mod 8)).
+// A position outside [0, L) is skipped and reported (DAK_ERR_BOUNDS, info = request).
+__global__ void kv_append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+                                 const int* __restrict__ positions, uint8_t* host, uint8_t* hbm, long long head_bytes,
+                                 int H_kv, int D16, int L, int h_s, DevStatus* st) {
+    const int b = blockIdx.x, g = blockIdx.y;
+    const int pos = positions[b];
+    if (pos < 0 || pos >= L) {
+        if (g == 0 && threadIdx.x == 0) report(st, DAK_ERR_BOUNDS, 0xA9900000ull | static_cast<unsigned>(b));
+        return;
+    }
+    const long long slab = static_cast<long long>(b) * H_kv + g;
+    uint4* base = reinterpret_cast<uint4*>(slab < h_s ? host + slab * head_bytes : hbm + (slab - h_s) * head_bytes);
+    const long long row = static_cast<long long>(pos >> 6) * (2 * 64 * D16) + static_cast<long long>(pos & 63) * D16;
+    for (int t = threadIdx.x; t < 2 * D16; t += blockDim.x) {
+        const bool is_v = t >= D16;
+        const int c = is_v ? t - D16 : t;
+        const uint4 piece = (is_v ? v_new : k_new)[slab * D16 + c];
+        base[row + (is_v ? 64 * D16 : 0) + (c ^ (pos & 7))] = piece;
+    }
+}
+
+extern "C" dak_status dak_kv_append(const dak_placement* KV, const void* k_new, const void* v_new,
+                                    const int* positions, void* stream) {
+    if (!KV || KV->kind != 1 || !k_new || !v_new || !positions) return DAK_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(k_new) & 15) || (reinterpret_cast<uintptr_t>(v_new) & 15)) return DAK_ERR_ALIGN;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DAK_ERR_CUDA;
+    if (dev != KV->device) return DAK_ERR_INVALID;
+    DevStatus* st = status_ptr();
+    if (!st) return DAK_ERR_CUDA;
+    const int D16 = KV->D / 8;
+    kv_append_kernel<<<dim3(static_cast<unsigned>(KV->B), static_cast<unsigned>(KV->H_kv)), 2 * D16, 0,
+                       static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), positions,
+        static_cast<uint8_t*>(KV->host_dev), static_cast<uint8_t*>(KV->hbm_ptr), KV->head_bytes, KV->H_kv, D16,
+        KV->L, KV->h_s, st);
+    return cuda_status(cudaGetLastError());
+}
+
 extern "C" dak_status dak_prefetch(const dak_placement* p, void* staging, void* stream) {
     if (!p) return DAK_ERR_INVALID;
     if (p->host_bytes == 0) return DAK_OK;

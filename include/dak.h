@@ -162,6 +162,16 @@ dak_status dak_place_kv(const void* K_src, const void* V_src, int src_on_device,
 dak_status dak_place_kv_heads(const void* K_src, const void* V_src, int src_on_device, int B, int H_kv, int L,
                               int D, int n_host_heads, dak_placement** out);
 
+/* Append one new token to a placed KV cache (the static cache's per-step update, [DAK]
+ * section 5): for every request b and kv head g, k_new[b][g][:] and v_new[b][g][:] (bf16
+ * [B][H_kv][D], device, 16-byte aligned) are written at position positions[b] (int32 [B],
+ * device) of that (request, kv head)'s slab, in whichever tier holds it. Stream-ordered;
+ * a following dak_attn sees the token when positions[b] < its seq_lens[b] (launched with
+ * tuning->pdl 2, or without programmatic launch). A position outside [0, L) is skipped and
+ * reported by dak_last_error as DAK_ERR_BOUNDS. */
+dak_status dak_kv_append(const dak_placement* KV, const void* k_new, const void* v_new, const int* positions,
+                         void* stream);
+
 /* Release a placement (host and HBM parts). NULL is accepted. */
 dak_status dak_free(dak_placement* p);
 

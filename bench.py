@@ -92,15 +92,26 @@ class Step:
         self.dak = dak
         self.x = x
         self.pl, self.B, self.C = {}, {}, {}
+        q, k, v = attn
+        # the step's inputs (every B, then Q) and outputs (every C, then O) are views of one
+        # device buffer each, so that the end-to-end step moves them in one copy each way
+        n_in = sum(B.size for _, B in lin.values()) + q.size
+        n_out = sum(B.shape[0] * A.shape[0] for A, B in lin.values()) + q.size
+        self.inbuf = torch.empty(n_in, dtype=torch.bfloat16, device=dev)
+        self.outbuf = torch.empty(n_out, dtype=torch.bfloat16, device=dev)
+        oi = oo = 0
         for name, (A, B) in lin.items():
             M = A.shape[0]
             self.pl[name] = dak.dak_place_matrix(A, dak.host_tiles_for_ratio(x, M))
-            self.B[name] = torch.from_numpy(B.view("int16")).view(torch.bfloat16).to(dev)
-            self.C[name] = torch.empty((B.shape[0], M), dtype=torch.bfloat16, device=dev)
-        q, k, v = attn
+            self.B[name] = self.inbuf[oi:oi + B.size].view(B.shape)
+            self.B[name].copy_(torch.from_numpy(B.view("int16")).view(torch.bfloat16))
+            self.C[name] = self.outbuf[oo:oo + B.shape[0] * M].view(B.shape[0], M)
+            oi += B.size
+            oo += B.shape[0] * M
         self.kv = dak.dak_place_kv(k, v, dak.host_requests_for_ratio(x, k.shape[0]))
-        self.Q = torch.from_numpy(q.view("int16")).view(torch.bfloat16).to(dev)
-        self.O = torch.empty_like(self.Q)
+        self.Q = self.inbuf[oi:].view(q.shape)
+        self.Q.copy_(torch.from_numpy(q.view("int16")).view(torch.bfloat16))
+        self.O = self.outbuf[oo:].view(q.shape)
         self.n_split = dak.dak_attn_default_split(self.kv)
         ws = dak.dak_attn_workspace_bytes(q.shape[0], q.shape[1], q.shape[2], self.n_split)
         self.ws = torch.empty(max(1, ws // 4), dtype=torch.float32, device=dev)
@@ -1127,21 +1138,16 @@ def main():
 
     # end to end through the public API with host buffers: hidden states / queries copied in
     # from pinned memory and outputs copied back every step
-    hostB = {n: b.cpu().pin_memory() for n, b in st.B.items()}
-    hostQ = st.Q.cpu().pin_memory()
-    hostC = {n: torch.empty(c.shape, dtype=c.dtype).pin_memory() for n, c in st.C.items()}
-    hostO = torch.empty(st.O.shape, dtype=st.O.dtype).pin_memory()
-    h2d = sum(b.numel() * 2 for b in hostB.values()) + hostQ.numel() * 2
-    d2h = sum(c.numel() * 2 for c in hostC.values()) + hostO.numel() * 2
+    # (every B and Q in one pinned buffer and one copy in; every C and O in one copy out)
+    host_in = st.inbuf.cpu().pin_memory()
+    host_out = torch.empty(st.outbuf.shape, dtype=st.outbuf.dtype).pin_memory()
+    h2d = host_in.numel() * 2
+    d2h = host_out.numel() * 2
 
     def e2e_step():
-        for n in st.B:
-            st.B[n].copy_(hostB[n], non_blocking=True)
-        st.Q.copy_(hostQ, non_blocking=True)
+        st.inbuf.copy_(host_in, non_blocking=True)
         st.run()
-        for n in st.C:
-            hostC[n].copy_(st.C[n], non_blocking=True)
-        hostO.copy_(st.O, non_blocking=True)
+        host_out.copy_(st.outbuf, non_blocking=True)
 
     e2e_value, t_e2e = aggregate_replicas(time_steps(e2e_step, max(10, args.steps // 3), 3, sync_all), C, dist)
 

@@ -640,19 +640,19 @@ def run_linears_n(dak, lin, b_host, b_hbm, dev, xs=(0.0, 0.25), ns=(1, 8, 32, 64
             roof = tier_roofline(C_bytes, H / C_bytes, b_host, b_hbm)
             row = {"N": N, "x": x, "us": t * 1e6, "gbps": C_bytes / t / 1e9, "frac": (C_bytes / t) / roof}
             del g
-            if N >= 2:
-                # the same four GEMMs as one grouped launch (dak_gemm_chain, no dependencies)
-                ops = [dict(A=p, B=Bs[n], C=Cs[n]) for n, p in pls.items()]
-                ws = torch.zeros(dak.dak_gemm_chain_workspace_bytes(ops, N), dtype=torch.uint8, device=dev)
-                g = _capture(lambda: dak.dak_gemm_chain(ops, workspace=ws, tuning=dict(pdl=1)))
-                tc = time_steps(g.replay, 20, 3)
-                row.update(chain_us=tc * 1e6, chain_gbps=C_bytes / tc / 1e9, chain_frac=(C_bytes / tc) / roof)
-                del g, ws
+            # the same four GEMMs as one grouped launch (dak_gemm_chain, no dependencies;
+            # tensor cores at every N, B padded to 8 rows at N = 1)
+            ops = [dict(A=p, B=Bs[n], C=Cs[n]) for n, p in pls.items()]
+            ws = torch.zeros(dak.dak_gemm_chain_workspace_bytes(ops, N), dtype=torch.uint8, device=dev)
+            g = _capture(lambda: dak.dak_gemm_chain(ops, workspace=ws, tuning=dict(pdl=1)))
+            tc = time_steps(g.replay, 20, 3)
+            row.update(chain_us=tc * 1e6, chain_gbps=C_bytes / tc / 1e9, chain_frac=(C_bytes / tc) / roof)
+            del g, ws
             rows.append(row)
         for p in pls.values():
             p.free()
     return {"ops": "8B QKV, O, gate+up, down: one graph of four dak_gemm launches (us, frac), and one grouped "
-                   "dak_gemm_chain launch of the four (chain_us, chain_frac; N >= 2)", "rows": rows,
+                   "dak_gemm_chain launch of the four (chain_us, chain_frac)", "rows": rows,
             "status": dak.dak_last_error()[0]}
 
 
@@ -679,7 +679,7 @@ def run_per_op_x(dak, lin, attn, b_host, b_hbm, dev, ns=(1, 8, 32, 64)):
     included; CUDA events around the launch), and `chain`, a CUDA graph of launches with
     programmatic launch and the host-link handoff (dak_link_begin) over enough copies of
     the placement that they stream more than twice the L2 size (the rate of the operation
-    repeated back to back, as in a model's layers); for the linears at N >= 2 also
+    repeated back to back, as in a model's layers); for the linears also
     `grouped`, up to 8 of those copies in one dak_gemm_chain launch. Bytes are the
     operation's weights (or KV cache)."""
     import math
@@ -734,15 +734,14 @@ def run_per_op_x(dak, lin, attn, b_host, b_hbm, dev, ns=(1, 8, 32, 64)):
                 tc = time_steps(g.replay, 10, 3) / copies
                 del g
                 rec = dict(x=x, N=N, **point(C_bytes, H, t1, tc))
-                if N >= 2:
-                    # the copies as one grouped launch (dak_gemm_chain: up to 8 operations)
-                    ops = [dict(A=p, B=Bs[N], C=Cs[N]) for p in pls[:8]]
-                    ws = torch.zeros(dak.dak_gemm_chain_workspace_bytes(ops, N), dtype=torch.uint8, device=dev)
-                    g = _capture(lambda: dak.dak_gemm_chain(ops, workspace=ws, tuning=pdl))
-                    tg = time_steps(g.replay, 10, 3) / len(ops)
-                    del g, ws
-                    roof = tier_roofline(C_bytes, H / C_bytes, b_host, b_hbm)
-                    rec.update(grouped_us=tg * 1e6, grouped_frac=(C_bytes / tg) / roof)
+                # the copies as one grouped launch (dak_gemm_chain: up to 8 operations)
+                ops = [dict(A=p, B=Bs[N], C=Cs[N]) for p in pls[:8]]
+                ws = torch.zeros(dak.dak_gemm_chain_workspace_bytes(ops, N), dtype=torch.uint8, device=dev)
+                g = _capture(lambda: dak.dak_gemm_chain(ops, workspace=ws, tuning=pdl))
+                tg = time_steps(g.replay, 10, 3) / len(ops)
+                del g, ws
+                roof = tier_roofline(C_bytes, H / C_bytes, b_host, b_hbm)
+                rec.update(grouped_us=tg * 1e6, grouped_frac=(C_bytes / tg) / roof)
                 rows.append(rec)
             for p in pls:
                 p.free()

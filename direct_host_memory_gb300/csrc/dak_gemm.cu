@@ -1797,16 +1797,18 @@ struct BlockPlan {
 // hidden-state rows (at most one launch's worth); caller_ws: the partial tiles go to a
 // caller's workspace of ws_bytes; pairs: a placement of 128-row tiles (T and h even), whose
 // blocks of two tile rows are the units of work.
+// tensor_cores: plan the tcgen05 kernel at N = 1 too (a chain has no CUDA-core path)
 static dak_status plan_block(int T, int h, int K_pad, long long tile_bytes, int N, int sms, const dak_tuning* t,
-                             bool caller_ws, size_t ws_bytes, BlockPlan* bp, int pairs, int cluster_slots = 0) {
+                             bool caller_ws, size_t ws_bytes, BlockPlan* bp, int pairs, int cluster_slots = 0,
+                             bool tensor_cores = false) {
     if (N < 1 || N > kMaxWideN || sms < 1) return DAK_ERR_INVALID;
     BlockPlan& q = *bp;
     q = BlockPlan{};
     // wide B: NC CTAs of a cluster share each tile row, CTA r computing rows [256 r, 256 r + 256)
     q.NC = N > kMaxBlockN ? (N + kMaxBlockN - 1) / kMaxBlockN : 1;
     q.P = 1;
-    q.pstep = N >= 2 ? 64 : 256;  // the B block of the tensor-core / CUDA-core layout
-    q.umma = N >= 2;  // N = 2..7 padded to 8 columns: measured 1.2-2.7x faster than FMA
+    q.umma = N >= 2 || tensor_cores;  // N = 2..7 padded to 8 columns: measured 1.2-2.7x faster than FMA
+    q.pstep = q.umma ? 64 : 256;      // the B block of the tensor-core / CUDA-core layout
     const bool umma = q.umma;
     if (pairs && ((T | h) & 1)) return DAK_ERR_INVALID;
     q.pairs = pairs ? 1 : 0;
@@ -2165,13 +2167,13 @@ static long long align256(long long v) { return (v + 255) & ~255ll; }
 static dak_status plan_chain(const ChainOp* ops, int n, int N, int sms, const dak_tuning* t, BlockPlan* bps,
                              long long* cnt_off, long long* part_off, long long* need) {
     if (n < 1 || n > kMaxChainOps) return DAK_ERR_INVALID;
-    if (N < 2 || N > kFuseMaxN) return DAK_ERR_UNSUPPORTED;  // tensor cores, one CTA per tile row
+    if (N < 1 || N > kFuseMaxN) return DAK_ERR_UNSUPPORTED;  // tensor cores, one CTA per tile row
     long long off = kChainDoneBytes;
     for (int j = 0; j < n; ++j) {
         const dak_placement* A = ops[j].A;
         if (!A || A->kind != 0 || A->T == 0) return DAK_ERR_INVALID;
         const dak_status r = plan_block(A->T, A->h, static_cast<int>(A->K_pad), A->tile_bytes, N, sms, t, false, 0,
-                                        &bps[j], A->tile_m == 2 * kTileM);
+                                        &bps[j], A->tile_m == 2 * kTileM, 0, true);
         if (r != DAK_OK) return r;
         const BlockPlan& b = bps[j];
         if (b.pairs != bps[0].pairs) return DAK_ERR_UNSUPPORTED;  // one ring layout for every operation

@@ -260,8 +260,8 @@ dak_status dak_gemm_plan(int64_t M, int64_t K, int tile_m, int n_host_tiles, int
 dak_status dak_gemm_launch_plan(const dak_placement* A, int N, const dak_tuning* tuning, size_t ws_bytes,
                                 dak_gemm_plan_info* out);
 
-/* A chain of GEMMs C_j = A_j x B_j in one persistent launch, for 2 <= N <= 128 hidden-state
- * rows (tensor-core path). The paper launches one kernel per nn.Linear (section 5); here the
+/* A chain of GEMMs C_j = A_j x B_j in one persistent launch, for 1 <= N <= 128 hidden-state
+ * rows (tensor-core path; at N = 1, B padded to 8 rows as dak_gemm pads N = 2..7). The paper launches one kernel per nn.Linear (section 5); here the
  * operations of a chain share one launch, so that each CTA's weight stream runs on from one
  * operation to the next instead of draining and ramping up at every launch boundary (the
  * weights never depend on an earlier operation, so a CTA streams the next operation's tiles
@@ -276,7 +276,9 @@ dak_status dak_gemm_launch_plan(const dak_placement* A, int N, const dak_tuning*
  *       tuning->pdl, as dak_gemm with pdl).
  * Each operation is tiered, dealt to CTAs and (when its tile rows do not spread evenly) cut
  * into pieces exactly as its own dak_gemm launch would be, so results are bit-identical to
- * dak_gemm's with the same tuning, at every offload ratio. n_ops 1..8, one N for all.
+ * dak_gemm's with the same tuning, at every offload ratio (at N = 1, where dak_gemm runs on
+ * the CUDA cores, they are the same product summed in another order: equal to dak_gemm to
+ * fp32 rounding, and bit-identical across offload ratios). n_ops 1..8, one N for all.
  * Workspace: device memory of dak_gemm_chain_workspace_bytes(ops, n_ops, N, tuning) bytes,
  * 256-byte aligned, zeroed once before its first use: per-operation completion counters,
  * piece counters and partial tiles. Every completed launch leaves its counters at zero; after
@@ -284,7 +286,7 @@ dak_status dak_gemm_launch_plan(const dak_placement* A, int N, const dak_tuning*
  * not overlap. The operations' completion waits are bounded (DAK_ERR_TIMEOUT through
  * dak_last_error), and every CTA of the launch must be able to run at once (the launch uses
  * at most one CTA per SM).
- * DAK_ERR_UNSUPPORTED: N outside 2..128, or operations whose launches would stream with
+ * DAK_ERR_UNSUPPORTED: N outside 1..128, or operations whose launches would stream with
  * different ring layouts. DAK_ERR_INVALID: n_ops outside 1..8, null pointers, workspace
  * smaller than needed; DAK_ERR_ALIGN as dak_gemm or an unaligned workspace. */
 typedef struct {

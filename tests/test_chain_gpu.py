@@ -51,7 +51,33 @@ def test_independent_chain_equals_separate_launches(dak, N):
             p.free()
 
 
-@pytest.mark.parametrize("N", [4, 16, 64])
+def test_one_row_chain(dak):
+    """N = 1: the chain runs the tensor cores with B padded to 8 rows, where dak_gemm runs the
+    CUDA cores. The same bits at every offload ratio, the oracle's values, and dak_gemm's to
+    fp32 rounding (the same products summed in another order)."""
+    mats = [synth.gemm_inputs(M, K, 1, seed=140 + i)[0] for i, (M, K) in enumerate(SHAPES)]
+    Bs = [synth.normal_bf16(150 + i, 2, K).reshape(1, K) for i, (M, K) in enumerate(SHAPES)]
+    base = None
+    for frac in (0.0, 0.3, 1.0):
+        pls = [dak.dak_place_matrix(A, int(np.ceil(frac * -(-A.shape[0] // 64)))) for A in mats]
+        ops = [dict(A=p, B=to_dev(B), c_fp32=True) for p, B in zip(pls, Bs)]
+        got = [bits_of(c) for c in dak.dak_gemm_chain(ops, tuning=dict(pdl=1))]
+        st, info = dak.dak_last_error()
+        assert st == 0, f"device status {st} info {info:#x}"
+        if base is None:
+            base = got
+        for g, b in zip(got, base):
+            assert np.array_equal(g, b), frac
+        sep = _separate(dak, ops)
+        for g, s, A, B in zip(got, sep, mats, Bs):
+            ref = og.gemm_ref(A, B)
+            assert og.rel_err(g.view(np.float32), ref) <= FP32_OUT_TOL
+            assert og.rel_err(g.view(np.float32), to_np(s)) <= FP32_OUT_TOL
+        for p in pls:
+            p.free()
+
+
+@pytest.mark.parametrize("N", [1, 4, 16, 64])
 def test_dependent_chain(dak, N):
     """C1 = A1 . B, C2 = A2 . C1, C3 = A3 . C2, C4 = A4 . C3 (bf16 between the operations),
     one launch with after_prev, against the four launches one after the other."""
@@ -64,19 +90,27 @@ def test_dependent_chain(dak, N):
     ops = [dict(A=pls[0], B=B0, C=Cs[0])] + [dict(A=pls[i], B=Cs[i - 1], C=Cs[i], after_prev=True)
                                            for i in range(1, 4)]
     ws = torch.zeros(dak.dak_gemm_chain_workspace_bytes(ops, N), dtype=torch.uint8, device="cuda")
-    seq = []
+    seq, seq_t = [], []
     x = B0
     for p in pls:
         x = dak.dak_gemm(p, x)
         seq.append(bits_of(x))
+        seq_t.append(x)
+    first = None
     for rep in range(3):  # the counters are back at zero after every launch
         for c in Cs:
             c.fill_(float("nan"))
         dak.dak_gemm_chain(ops, workspace=ws, tuning=dict(pdl=rep % 2))
         st, info = dak.dak_last_error()
         assert st == 0, f"device status {st} info {info:#x}"
-        for c, s in zip(Cs, seq):
-            assert np.array_equal(bits_of(c), s), rep
+        got = [bits_of(c) for c in Cs]
+        first = first or got
+        for c, g, f, s, st_ in zip(Cs, got, first, seq, seq_t):
+            assert np.array_equal(g, f), rep
+            if N > 1:
+                assert np.array_equal(g, s), rep
+            else:  # dak_gemm on the CUDA cores: the same products in another order
+                assert og.rel_err(to_np(c), to_np(st_)) <= REL_TOL, rep
     assert int(ws[:256].view(torch.int32).abs().sum()) == 0
     ref = og.gemm_ref(mats[1], bits_of(Cs[0]))
     assert og.rel_err(to_np(Cs[1]), ref) <= REL_TOL
@@ -139,8 +173,8 @@ def test_chain_errors(dak):
         with pytest.raises(dak.DakError) as e:
             dak.dak_gemm_chain(one, workspace=small)
         assert e.value.status == 1
-    with pytest.raises(dak.DakError) as e:  # N = 1 runs on the CUDA cores, not in a chain
-        dak.dak_gemm_chain([dict(A=p, B=Bt[:1].contiguous())])
+    with pytest.raises(dak.DakError) as e:  # one CTA per tile row holds at most 128 rows
+        dak.dak_gemm_chain([dict(A=p, B=torch.zeros((129, 512), dtype=torch.bfloat16, device="cuda"))])
     assert e.value.status == 7
     with pytest.raises(dak.DakError) as e:
         dak.dak_gemm_chain([dict(A=p, B=Bt)] * 9)

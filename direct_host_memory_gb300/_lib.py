@@ -53,7 +53,7 @@ class dak_tuning(ctypes.Structure):
                 ("chunk_k", ctypes.c_int), ("n_split", ctypes.c_int), ("hbm_ctas", ctypes.c_int),
                 ("split_k", ctypes.c_int), ("pdl", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
                 ("no_wave_align", ctypes.c_int), ("column_blocks", ctypes.c_int), ("cluster_slots", ctypes.c_int),
-                ("link", ctypes.c_int)]
+                ("link", ctypes.c_int), ("chain_rr", ctypes.c_int)]
 
 
 class dak_gemm_op(ctypes.Structure):

@@ -92,6 +92,12 @@ typedef struct dak_placement dak_placement;
  *   link      : dak_gemm / dak_attn: 1..8 = join host-link handoff sequence `link`, started
  *               by dak_link_begin on the same stream (see there); 0 = none. The tuner
  *               ignores it.
+ *   chain_rr  : dak_gemm_chain only. 0 (default) = a chain with no tile row on the host and
+ *               no after_prev deals its units (tile rows or pieces) by size: longest first
+ *               to the CTA with the least work so far, so that operations of different
+ *               shapes even out over the launch. 1 = every operation deals its units round
+ *               the launch as its own launch would (always so for other chains). Which CTA
+ *               computes a unit never changes a result.
  */
 typedef struct {
     int host_ctas;
@@ -107,6 +113,7 @@ typedef struct {
     int column_blocks;
     int cluster_slots;
     int link;
+    int chain_rr;
 } dak_tuning;
 
 /* ---------------------------------------------------------------------------------- *

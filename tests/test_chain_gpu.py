@@ -51,6 +51,58 @@ def test_independent_chain_equals_separate_launches(dak, N):
             p.free()
 
 
+@pytest.mark.parametrize("N", [1, 8, 32, 64])
+def test_size_dealing_same_bits(dak, N):
+    """An independent chain all in HBM deals its units by size over the CTAs (chain_rr = 0);
+    every unit is computed once and lands where the per-operation dealing (chain_rr = 1)
+    and the separate launches put it (N >= 2; at N = 1 dak_gemm runs the CUDA cores): the
+    same bits, eagerly (a new chain, then the same one again) and replayed from a CUDA
+    graph."""
+    import torch
+    lin = [synth.gemm_inputs(M, K, N, seed=170 + i, tensor_index=i) for i, (M, K) in
+           enumerate(list(synth.LINEARS_8B.values()) + [(1000, 520)])]
+    pls = [dak.dak_place_matrix(A, 0) for A, _ in lin]
+    Bs = [to_dev(B) for _, B in lin]
+
+    def ops(cs=None):
+        return [dict(A=p, B=B, c_fp32=(i % 2 == 1), C=None if cs is None else cs[i])
+                for i, (p, B) in enumerate(zip(pls, Bs))]
+
+    def nan_outs():
+        return [torch.full((N, A.shape[0]), float("nan"), device="cuda",
+                           dtype=torch.float32 if i % 2 == 1 else torch.bfloat16) for i, (A, _) in enumerate(lin)]
+
+    if N > 1:
+        sep = [bits_of(c) for c in _separate(dak, ops())]
+    else:
+        sep = [bits_of(c) for c in dak.dak_gemm_chain(ops(), tuning=dict(pdl=1, chain_rr=1))]
+    for rr in (0, 1, 0):
+        outs = nan_outs()
+        dak.dak_gemm_chain(ops(outs), tuning=dict(pdl=1, chain_rr=rr))
+        st, info = dak.dak_last_error()
+        assert st == 0, f"device status {st} info {info:#x}"
+        for c, r in zip(outs, sep):
+            assert np.array_equal(bits_of(c), r), rr
+    outs = nan_outs()
+    o = ops(outs)
+    ws = torch.zeros(dak.dak_gemm_chain_workspace_bytes(o, N), dtype=torch.uint8, device="cuda")
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        dak.dak_gemm_chain(o, workspace=ws, tuning=dict(pdl=1))
+        with torch.cuda.graph(g, stream=s):
+            dak.dak_gemm_chain(o, workspace=ws, tuning=dict(pdl=1))
+    for c in outs:
+        c.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert dak.dak_last_error()[0] == 0
+    for c, r, (A, B) in zip(outs, sep, lin):
+        assert np.array_equal(bits_of(c), r)
+    for p in pls:
+        p.free()
+
+
 def test_one_row_chain(dak):
     """N = 1: the chain runs the tensor cores with B padded to 8 rows, where dak_gemm runs the
     CUDA cores. The same bits at every offload ratio, the oracle's values, and dak_gemm's to

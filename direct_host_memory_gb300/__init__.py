@@ -10,7 +10,7 @@ from ._lib import (  # noqa: F401
     MODE_PREFETCH_OVERLAP, MODE_PREFETCH_SERIAL, NOALLOC_SCRATCH_BYTES, TUNING_FIELDS, DakError,
     Decoder, Placement, dak_alloc_counts, dak_attn, dak_attn_default_split, dak_attn_f32,
     dak_attn_noalloc, dak_attn_staged, dak_attn_workspace_bytes, dak_fault_pending, dak_free, dak_gemm,
-    dak_gemm_chain, dak_gemm_chain_workspace_bytes, dak_gemm_launch_plan, dak_gemm_op, dak_gemm_plan,
+    dak_gemm_chain, dak_gemm_chain_plan, dak_gemm_chain_workspace_bytes, dak_gemm_launch_plan, dak_gemm_op, dak_gemm_plan,
     dak_gemm_staged, dak_gemm_workspace_bytes, dak_inject_fault, dak_kv_append, dak_last_error,
     dak_link_begin, dak_link_timeouts, dak_op, dak_place_kv, dak_place_kv_heads, dak_place_matrix,
     dak_place_matrix_glu, dak_placement_info, dak_plan_ratios, dak_plan_units, dak_prefetch,

@@ -32,7 +32,7 @@ EXPORTS = [
     "dak_place_matrix_glu", "dak_plan_units", "dak_gemm_workspace_bytes", "dak_gemm_ws", "dak_gemm_plan", "dak_gemm_launch_plan",
     "dak_attn_f32", "dak_inject_fault", "dak_fault_pending", "dak_alloc_counts", "dak_gemm_chain",
     "dak_gemm_chain_workspace_bytes", "dak_link_begin", "dak_link_timeouts", "dak_selftest_link",
-    "dak_place_kv_heads", "dak_kv_append",
+    "dak_place_kv_heads", "dak_kv_append", "dak_gemm_chain_plan",
 ]
 
 # host-side fault injection kinds (DAK_FAULT_* in dak.h)
@@ -68,6 +68,10 @@ class dak_op(ctypes.Structure):
 class dak_tune_result(ctypes.Structure):
     _fields_ = [("best", dak_tuning), ("best_us", ctypes.c_double), ("default_us", ctypes.c_double),
                 ("cc_off_us", ctypes.c_double), ("no_align_us", ctypes.c_double), ("candidates", ctypes.c_int)]
+
+
+class dak_gemm_chain_plan_info(ctypes.Structure):
+    _fields_ = [(f, ctypes.c_int) for f in ("grid", "units", "by_size", "busiest_per_op", "busiest_by_size")]
 
 
 class dak_gemm_plan_info(ctypes.Structure):
@@ -114,6 +118,8 @@ def _load():
         "dak_gemm_launch_plan": (i32, [vp, i32, P(dak_tuning), sz, P(dak_gemm_plan_info)]),
         "dak_gemm_chain_workspace_bytes": (sz, [P(dak_gemm_op), i32, i32, P(dak_tuning)]),
         "dak_gemm_chain": (i32, [P(dak_gemm_op), i32, i32, P(dak_tuning), vp, sz, vp]),
+        "dak_gemm_chain_plan": (i32, [P(i64), P(i64), P(i32), P(i32), P(i32), i32, i32, i32, P(dak_tuning),
+                                      P(dak_gemm_chain_plan_info)]),
         "dak_attn_workspace_bytes": (sz, [i32, i32, i32, i32]),
         "dak_attn": (i32, [vp, vp, vp, i32, ctypes.c_float, vp, vp, sz, P(dak_tuning), vp]),
         "dak_attn_staged": (i32, [vp, vp, vp, vp, i32, ctypes.c_float, vp, vp, sz, P(dak_tuning), vp]),
@@ -388,6 +394,25 @@ def dak_gemm_chain(ops, tuning=None, workspace=None, stream=None):
                               ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream_ptr(stream)),
            "dak_gemm_chain")
     return [o["C"] for o in ops]
+
+
+def dak_gemm_chain_plan(shapes, N: int, n_host_tiles=None, tile_m=None, after_prev=None, sm_count: int = None,
+                        tuning=None) -> dict:
+    """How dak_gemm_chain would deal a chain's units over its CTAs, from host arithmetic alone:
+    shapes [(M, K), ...], per operation n_host_tiles, tile_m (64 or 128) and after_prev;
+    sm_count None = this process's GPU."""
+    n = len(shapes)
+    if sm_count is None:
+        sm_count = dak_sm_count()
+
+    def arr(t, vals):
+        return (t * n)(*[int(v) for v in vals])
+    out = dak_gemm_chain_plan_info()
+    _check(lib.dak_gemm_chain_plan(arr(ctypes.c_int64, [m for m, _ in shapes]), arr(ctypes.c_int64, [k for _, k in shapes]),
+                                   arr(ctypes.c_int, tile_m or [64] * n), arr(ctypes.c_int, n_host_tiles or [0] * n),
+                                   arr(ctypes.c_int, after_prev or [0] * n), n, int(N), int(sm_count), _tuning(tuning),
+                                   ctypes.byref(out)), "dak_gemm_chain_plan")
+    return {f: int(getattr(out, f)) for f, _ in dak_gemm_chain_plan_info._fields_}
 
 
 def dak_gemm_workspace_bytes(A: Placement, N: int) -> int:

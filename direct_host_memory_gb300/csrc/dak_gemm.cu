@@ -2248,8 +2248,11 @@ constexpr long long kUnitFixedBytes = 32 * 1024;
 // N = 1-16, where it leaves 2%. Returns false (cl->n = 0) otherwise. The choice and the
 // list are functions of the shapes and the plan only; the last ones are kept for the next
 // launch.
-static bool deal_by_size(const ChainParams& cp, ChainList* cl) {
+// busiest: where given, the busiest CTA's work over the mean in thousandths, dealt per
+// operation ([0]) and by size ([1]).
+static bool deal_by_size(const ChainParams& cp, ChainList* cl, int* busiest = nullptr) {
     cl->n = 0;
+    if (busiest) busiest[0] = busiest[1] = 0;
     const int C = cp.n_ctas;
     if (C < 1 || C > kChainListCtas) return false;
     std::vector<int> key{C, cp.n_ops};
@@ -2258,15 +2261,17 @@ static bool deal_by_size(const ChainParams& cp, ChainList* cl) {
         const GemmParams& p = cp.op[j];
         if (p.h != 0 || cp.after_prev[j] || p.NC != 1 || p.n_hbm_ctas < 1) return false;
         total += p.gb * p.P;
-        key.insert(key.end(), {p.T, p.gb, p.P, p.K_pad, p.pstep, p.pairs, p.ch[0].kc});
+        key.insert(key.end(), {p.T, p.gb, p.P, p.K_pad, p.pstep, p.pairs, p.n_host_ctas, p.n_hbm_ctas, cp.rot[j]});
     }
     if (total < 1 || total > kChainListMax) return false;
     static std::mutex mu;
     static std::vector<int> last_key;
     static ChainList last;
+    static int last_busiest[2];
     std::lock_guard<std::mutex> lock(mu);
     if (key == last_key) {
         *cl = last;
+        if (busiest) busiest[0] = last_busiest[0], busiest[1] = last_busiest[1];
         return cl->n > 0;
     }
     struct Unit {
@@ -2294,6 +2299,8 @@ static bool deal_by_size(const ChainParams& cp, ChainList* cl) {
         load[(p.n_host_ctas + u % p.n_hbm_ctas + cp.rot[x.e >> 13]) % C] += x.cost;
     }
     const long long rr_max = *std::max_element(load.begin(), load.end());
+    long long sum = 0;
+    for (long long v : load) sum += v;
     std::fill(load.begin(), load.end(), 0);
     std::stable_sort(units.begin(), units.end(), [](const Unit& a, const Unit& b) { return a.cost > b.cost; });
     std::vector<std::vector<uint16_t>> per(static_cast<size_t>(C));
@@ -2311,10 +2318,48 @@ static bool deal_by_size(const ChainParams& cp, ChainList* cl) {
         for (uint16_t v : per[c]) cl->e[at++] = v;
     }
     cl->start[C] = static_cast<uint16_t>(at);
-    cl->n = *std::max_element(load.begin(), load.end()) * 100 <= rr_max * 97 ? at : 0;
+    const long long size_max = *std::max_element(load.begin(), load.end());
+    cl->n = size_max * 100 <= rr_max * 97 ? at : 0;
     last_key = key;
     last = *cl;
+    last_busiest[0] = static_cast<int>(rr_max * 1000 * C / sum);
+    last_busiest[1] = static_cast<int>(size_max * 1000 * C / sum);
+    if (busiest) busiest[0] = last_busiest[0], busiest[1] = last_busiest[1];
     return cl->n > 0;
+}
+
+// The fields of a chain's parameters that its schedule and dealing read, from its plans.
+static void chain_schedule(const ChainOp* ops, int n, const BlockPlan* bps, ChainParams* cp) {
+    int grid = 0;
+    for (int j = 0; j < n; ++j) {
+        const dak_placement* A = ops[j].A;
+        const BlockPlan& bp = bps[j];
+        GemmParams& p = cp->op[j];
+        p.K_pad = static_cast<int>(A->K_pad);
+        p.NC = 1;
+        p.N_pad = bp.N_pad;
+        p.T = A->T;
+        p.h = A->h;
+        p.pairs = bp.pairs;
+        p.hb = blocks_of(p.h, p.pairs);
+        p.gb = blocks_of(p.T - p.h, p.pairs);
+        p.P = bp.P;
+        p.pstep = bp.pstep;
+        p.ch[0] = bp.ch[0];
+        p.ch[1] = bp.ch[1];
+        p.n_host_ctas = bp.n_host_ctas;
+        p.n_hbm_ctas = bp.n_hbm_ctas;
+        p.host_window = p.hbm_window = bp.ch[0].stages;  // one ring for every operation
+        cp->after_prev[j] = (j > 0 && ops[j].after_prev) ? 1 : 0;
+        grid = std::max(grid, bp.grid);
+    }
+    cp->n_ops = n;
+    cp->n_ctas = grid;
+    // each operation starts dealing where the previous one's CTAs ended
+    for (int j = 0, r = 0; j < n; ++j) {
+        cp->rot[j] = r;
+        r = grid > 0 ? (r + cp->op[j].n_host_ctas + cp->op[j].n_hbm_ctas) % grid : 0;
+    }
 }
 
 size_t gemm_chain_workspace_bytes(const ChainOp* ops, int n, int N, const dak_tuning* t) {
@@ -2339,11 +2384,11 @@ dak_status launch_gemm_chain(const ChainOp* ops, int n, int N, const dak_tuning*
     ChainParams cp{};
     alignas(64) ChainMaps maps;
     std::memset(&maps, 0, sizeof(maps));
-    cp.n_ops = n;
+    chain_schedule(ops, n, bps, &cp);
     cp.st = status_ptr();
     if (!cp.st) return DAK_ERR_CUDA;
     cp.done = static_cast<int*>(ws);
-    int grid = 0, smem = 0;
+    int smem = 0;
     bool fused = false;
     for (int j = 0; j < n; ++j) {
         const ChainOp& o = ops[j];
@@ -2360,25 +2405,10 @@ dak_status launch_gemm_chain(const ChainOp* ops, int n, int N, const dak_tuning*
         p.C = o.C;
         p.M = static_cast<int>(A->M);
         p.K = static_cast<int>(A->K);
-        p.K_pad = static_cast<int>(A->K_pad);
         p.N = N;
-        p.NC = 1;
-        p.N_pad = bp.N_pad;
-        p.T = A->T;
-        p.h = A->h;
-        p.pairs = bp.pairs;
-        p.hb = blocks_of(p.h, p.pairs);
-        p.gb = blocks_of(p.T - p.h, p.pairs);
         p.c_fp32 = o.c_fp32 ? 1 : 0;
         p.tile_bytes = A->tile_bytes;
         p.glu = A->glu;
-        p.P = bp.P;
-        p.pstep = bp.pstep;
-        p.ch[0] = bp.ch[0];
-        p.ch[1] = bp.ch[1];
-        p.n_host_ctas = bp.n_host_ctas;
-        p.n_hbm_ctas = bp.n_hbm_ctas;
-        p.host_window = p.hbm_window = bp.ch[0].stages;  // one ring for every operation
         p.st = cp.st;
         p.cnt = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + cnt_off[j]);
         p.part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + part_off[j]);
@@ -2398,20 +2428,13 @@ dak_status launch_gemm_chain(const ChainOp* ops, int n, int N, const dak_tuning*
             p.ss_eps = f.eps;
             fused = true;
         }
-        cp.after_prev[j] = (j > 0 && o.after_prev) ? 1 : 0;
         int b3d = 0;
         if (!make_b_map(&maps.m[j], o.B, p.K, N, p.N_pad, bp.kcb, kUmmaB, &b3d)) return DAK_ERR_CUDA;
         p.b3d = b3d;
-        grid = std::max(grid, bp.grid);
         smem = std::max(smem, bp.smem);
     }
-    cp.n_ctas = grid;
+    const int grid = cp.n_ctas;
     if (grid == 0) return DAK_OK;
-    // each operation starts dealing where the previous one's CTAs ended
-    for (int j = 0, r = 0; j < n; ++j) {
-        cp.rot[j] = r;
-        r = (r + cp.op[j].n_host_ctas + cp.op[j].n_hbm_ctas) % grid;
-    }
     static thread_local ChainList cl;
     if (!(t && t->chain_rr > 0)) deal_by_size(cp, &cl);
     else cl.n = 0;
@@ -2480,6 +2503,51 @@ extern "C" dak_status dak_gemm_plan(int64_t M, int64_t K, int tile_m, int n_host
                                          tuning, ws_bytes > 0, ws_bytes, &bp, per == 2);
     if (r != DAK_OK) return r;
     fill_plan_info(bp, N, block, out);
+    return DAK_OK;
+}
+
+extern "C" dak_status dak_gemm_chain_plan(const int64_t* M, const int64_t* K, const int* tile_m,
+                                          const int* n_host_tiles, const int* after_prev, int n_ops, int N,
+                                          int sm_count, const dak_tuning* tuning, dak_gemm_chain_plan_info* out) {
+    if (!out) return DAK_ERR_INVALID;
+    *out = dak_gemm_chain_plan_info{};
+    if (!M || !K || !tile_m || !n_host_tiles || n_ops < 1 || n_ops > dak::kMaxChainOps || sm_count < 1)
+        return DAK_ERR_INVALID;
+    dak_placement shapes[dak::kMaxChainOps];
+    dak::ChainOp ops[dak::kMaxChainOps];
+    for (int j = 0; j < n_ops; ++j) {
+        if (M[j] < 1 || K[j] < 8 || (K[j] % 8) || K[j] > (1 << 24) || M[j] > (1ll << 31)) return DAK_ERR_INVALID;
+        if (tile_m[j] != dak::kTileM && tile_m[j] != 2 * dak::kTileM) return DAK_ERR_UNSUPPORTED;
+        const int tiles = static_cast<int>((M[j] + tile_m[j] - 1) / tile_m[j]);
+        if (n_host_tiles[j] < 0 || n_host_tiles[j] > tiles) return DAK_ERR_INVALID;
+        const int per = tile_m[j] / dak::kTileM;
+        dak_placement& A = shapes[j];
+        A = dak_placement{};
+        A.kind = 0;
+        A.M = M[j];
+        A.K = K[j];
+        A.K_pad = (K[j] + 15) / 16 * 16;
+        A.tile_m = tile_m[j];
+        A.T = tiles * per;
+        A.h = n_host_tiles[j] * per;
+        A.tile_bytes = static_cast<int64_t>(dak::kTileM) * A.K_pad * 2;
+        ops[j].A = &A;
+        ops[j].after_prev = after_prev ? after_prev[j] : 0;
+    }
+    dak::BlockPlan bps[dak::kMaxChainOps];
+    long long cnt_off[dak::kMaxChainOps], part_off[dak::kMaxChainOps], need = 0;
+    const dak_status r = dak::plan_chain(ops, n_ops, N, sm_count, tuning, bps, cnt_off, part_off, &need);
+    if (r != DAK_OK) return r;
+    dak::ChainParams cp{};
+    dak::chain_schedule(ops, n_ops, bps, &cp);
+    static thread_local dak::ChainList cl;
+    int busiest[2] = {0, 0};
+    const bool by_size = dak::deal_by_size(cp, &cl, busiest);
+    out->grid = cp.n_ctas;
+    for (int j = 0; j < n_ops; ++j) out->units += (cp.op[j].hb + cp.op[j].gb) * cp.op[j].P;
+    out->by_size = (by_size && !(tuning && tuning->chain_rr > 0)) ? 1 : 0;
+    out->busiest_per_op = busiest[0];
+    out->busiest_by_size = busiest[1];
     return DAK_OK;
 }
 

@@ -268,7 +268,8 @@ dak_status dak_gemm_launch_plan(const dak_placement* A, int N, const dak_tuning*
                                 dak_gemm_plan_info* out);
 
 /* A chain of GEMMs C_j = A_j x B_j in one persistent launch, for 1 <= N <= 128 hidden-state
- * rows (tensor-core path; at N = 1, B padded to 8 rows as dak_gemm pads N = 2..7). The paper launches one kernel per nn.Linear (section 5); here the
+ * rows (tensor-core path; at N = 1, B padded to 8 rows as dak_gemm pads N = 2..7). The
+ * paper launches one kernel per nn.Linear (section 5); here the
  * operations of a chain share one launch, so that each CTA's weight stream runs on from one
  * operation to the next instead of draining and ramping up at every launch boundary (the
  * weights never depend on an earlier operation, so a CTA streams the next operation's tiles
@@ -306,6 +307,24 @@ typedef struct {
 size_t dak_gemm_chain_workspace_bytes(const dak_gemm_op* ops, int n_ops, int N, const dak_tuning* tuning);
 dak_status dak_gemm_chain(const dak_gemm_op* ops, int n_ops, int N, const dak_tuning* tuning, void* workspace,
                           size_t ws_bytes, void* stream);
+
+/* How dak_gemm_chain would deal the units of a chain (its tile rows, or their pieces) over
+ * its CTAs, from host arithmetic alone (no GPU): n_ops (1..8) matrices M[j] x K[j] in tiles
+ * of tile_m[j] rows, n_host_tiles[j] of them on the host, after_prev[j] as in dak_gemm_op,
+ * N (1..128) hidden-state rows, a GPU of sm_count SMs. A unit's work counts its bytes plus
+ * 32 KiB for its fixed cost. Errors as dak_gemm_plan for each operation and as
+ * dak_gemm_chain for the chain. */
+typedef struct {
+    int grid;            /* CTAs of the launch */
+    int units;           /* units of all operations */
+    int by_size;         /* 1: dealt by size (see tuning chain_rr), 0: per operation */
+    int busiest_per_op;  /* the busiest CTA's work over the mean x 1000, dealt per operation */
+    int busiest_by_size; /* the same dealt by size; both 0 where the size dealing does not apply
+                          * (host tile rows, after_prev, more than 4096 units or 256 CTAs) */
+} dak_gemm_chain_plan_info;
+dak_status dak_gemm_chain_plan(const int64_t* M, const int64_t* K, const int* tile_m, const int* n_host_tiles,
+                               const int* after_prev, int n_ops, int N, int sm_count, const dak_tuning* tuning,
+                               dak_gemm_chain_plan_info* out);
 
 /* Workspace bytes dak_attn needs for B requests, H_q query heads, head dim D and
  * n_split context splits (0 when n_split == 1). */

@@ -182,3 +182,102 @@ def test_cluster_slots_bound_the_schedule():
             assert p["host_ctas"] > 0 and p["hbm_ctas"] > 0
     # one CTA per tile: cluster_slots counts CTAs and is not capped
     assert plan(4096, 4096, 0, 16)["cluster_slots"] == SMS
+
+
+# ------------------------------------------------------------------ chains: dealing by size
+
+FIXED_BYTES = 32 * 1024  # a unit's fixed cost in the dealing's work measure
+
+
+def _chain_units(shapes, N, tile_ms):
+    """Each operation's units (work, operation, unit) and its CTAs, re-derived from
+    dak_gemm_plan's pieces, piece step and CTA counts (tensor cores at every N of a chain)."""
+    units, ctas = [], []
+    for j, ((M, K), tm) in enumerate(zip(shapes, tile_ms)):
+        p = plan(M, K, 0, max(N, 2), tile_m=tm)
+        blocks = -(-M // tm)
+        P, step = p["pieces"], p["piece_step"]
+        K_pad = -(-K // 16) * 16
+        steps = -(-K_pad // step)
+        for u in range(blocks * P):
+            i = u % P
+            k0 = (i * steps // P) * step
+            k1 = min(((i + 1) * steps // P) * step, K_pad)
+            units.append(((k1 - k0) * 128 * (tm // 64) + FIXED_BYTES, j, u))
+        ctas.append((p["host_ctas"], p["hbm_ctas"]))
+    return units, ctas
+
+
+def _deal(units, ctas):
+    """The busiest CTA's work over the mean (x 1000, floored) dealt per operation (unit u of
+    operation j on CTA host_ctas + u mod hbm_ctas, counted from where the previous operation's
+    CTAs ended) and dealt by size (longest first to the least loaded, ties to the lower CTA)."""
+    grid = max(h + g for h, g in ctas)
+    rot, r = [], 0
+    for h, g in ctas:
+        rot.append(r)
+        r = (r + h + g) % grid
+    per_op = [0] * grid
+    for w, j, u in units:
+        per_op[(ctas[j][0] + u % ctas[j][1] + rot[j]) % grid] += w
+    by_size = [0] * grid
+    for w, j, u in sorted(units, key=lambda x: -x[0]):
+        c = min(range(grid), key=lambda i: (by_size[i], i))
+        by_size[c] += w
+    total = sum(per_op)
+    return grid, max(per_op) * 1000 * grid // total, max(by_size) * 1000 * grid // total, max(by_size), max(per_op)
+
+
+@pytest.mark.parametrize("N", [2, 8, 16, 32, 64, 128])
+def test_chain_dealing_8b_linears(N):
+    shapes = list(LINEARS_8B.values())
+    got = dak.dak_gemm_chain_plan(shapes, N, sm_count=SMS)
+    units, ctas = _chain_units(shapes, N, [64] * 4)
+    grid, per_op, by_size, smax, rmax = _deal(units, ctas)
+    assert got == {"grid": grid, "units": len(units), "by_size": int(smax * 100 <= rmax * 97),
+                   "busiest_per_op": per_op, "busiest_by_size": by_size}
+    # the pieces of a tile row at N >= 32 are few and uneven in size (896 KiB down rows beside
+    # 512 and 256 KiB ones): dealt per operation the busiest CTA carries 13% over the mean
+    assert got["by_size"] == (N >= 32)
+    if N >= 32:
+        assert (got["busiest_per_op"], got["busiest_by_size"]) == (1126, 1041)
+    assert dak.dak_gemm_chain_plan(shapes, N, sm_count=SMS, tuning=dict(chain_rr=1))["by_size"] == 0
+
+
+def test_chain_dealing_one_row_is_eight():
+    shapes = list(LINEARS_8B.values())
+    assert dak.dak_gemm_chain_plan(shapes, 1, sm_count=SMS) == dak.dak_gemm_chain_plan(shapes, 8, sm_count=SMS)
+
+
+def test_chain_dealing_random_shapes():
+    rng = random.Random(7)
+    for case in range(12):
+        n = rng.randint(1, 8)
+        tms = [rng.choice([64, 128])] * n  # one ring layout (tile height) per chain
+        shapes = [(rng.randint(1, 9000), 8 * rng.randint(1, 2048)) for _ in range(n)]
+        N = rng.choice([2, 8, 24, 40, 64, 96])
+        try:
+            got = dak.dak_gemm_chain_plan(shapes, N, tile_m=tms, sm_count=SMS)
+        except dak.DakError as e:
+            assert e.status == 7  # operations whose launches stream with different rings
+            continue
+        units, ctas = _chain_units(shapes, N, tms)
+        assert got["units"] == len(units), case
+        if len(units) > 4096:
+            assert got["by_size"] == 0 and got["busiest_per_op"] == 0, case
+            continue
+        grid, per_op, by_size, smax, rmax = _deal(units, ctas)
+        assert got == {"grid": grid, "units": len(units), "by_size": int(smax * 100 <= rmax * 97),
+                       "busiest_per_op": per_op, "busiest_by_size": by_size}, case
+
+
+def test_chain_dealing_applies_only_all_hbm_and_independent():
+    shapes = list(LINEARS_8B.values())
+    for kw in (dict(n_host_tiles=[1, 0, 0, 0]), dict(after_prev=[0, 1, 0, 0])):
+        got = dak.dak_gemm_chain_plan(shapes, 32, sm_count=SMS, **kw)
+        assert (got["by_size"], got["busiest_per_op"], got["busiest_by_size"]) == (0, 0, 0), kw
+        assert got["units"] == 800
+    with pytest.raises(dak.DakError):
+        dak.dak_gemm_chain_plan(shapes, 129, sm_count=SMS)
+    with pytest.raises(dak.DakError):
+        dak.dak_gemm_chain_plan([(64, 12)], 8, sm_count=SMS)  # K not a multiple of 8

@@ -647,12 +647,15 @@ def run_linears_n(dak, lin, b_host, b_hbm, dev, xs=(0.0, 0.25), ns=(1, 8, 32, 64
             g = _capture(lambda: dak.dak_gemm_chain(ops, workspace=ws, tuning=dict(pdl=1)))
             tc = time_steps(g.replay, 20, 3)
             row.update(chain_us=tc * 1e6, chain_gbps=C_bytes / tc / 1e9, chain_frac=(C_bytes / tc) / roof)
+            cplan = dak.dak_gemm_chain_plan([A.shape for A, _ in lin.values()], N, n_host_tiles=[
+                dak.host_tiles_for_ratio(x, A.shape[0]) for A, _ in lin.values()])
+            row["chain_dealing"] = "by size" if cplan["by_size"] else "per operation"
             del g, ws
             rows.append(row)
         for p in pls.values():
             p.free()
     return {"ops": "8B QKV, O, gate+up, down: one graph of four dak_gemm launches (us, frac), and one grouped "
-                   "dak_gemm_chain launch of the four (chain_us, chain_frac)", "rows": rows,
+                   "dak_gemm_chain launch of the four (chain_us, chain_frac; chain_dealing: how its units were dealt to its CTAs)", "rows": rows,
             "status": dak.dak_last_error()[0]}
 
 

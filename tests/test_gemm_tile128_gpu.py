@@ -168,6 +168,39 @@ def test_chain_of_128_row_placements(dak, N):
         p.free()
 
 
+@pytest.mark.parametrize("N", [1, 128])
+def test_chain_of_128_row_8b_linears_dealt_by_size(dak, N):
+    """The four 8B-shaped linears in 128-row tiles, all in HBM, as one chain: at N = 128 the
+    chain deals its pair blocks by size (the busiest CTA 20% over the mean dealt per
+    operation), at N = 1 per operation; either way the same bits as the other dealing and
+    (N = 128) as the separate launches."""
+    import torch
+    shapes = list(synth.LINEARS_8B.values())
+    plan = dak.dak_gemm_chain_plan(shapes, N, tile_m=[128] * 4)
+    assert plan["by_size"] == (1 if N == 128 else 0)  # on a 152-SM GB300
+    lin = [synth.gemm_inputs(M, K, N, seed=190 + i, tensor_index=i) for i, (M, K) in enumerate(shapes)]
+    pls = [dak.dak_place_matrix(A, 0, tile_m=128) for A, _ in lin]
+    Bs = [to_dev(B) for _, B in lin]
+    ops = [dict(A=p, B=B, c_fp32=True) for p, B in zip(pls, Bs)]
+    outs = {}
+    for rr in (0, 1):
+        Cs = [torch.full((N, A.shape[0]), float("nan"), device="cuda") for A, _ in lin]
+        dak.dak_gemm_chain([dict(o, C=C) for o, C in zip(ops, Cs)], tuning=dict(pdl=1, chain_rr=rr))
+        st, info = dak.dak_last_error()
+        assert st == 0, f"device status {st} info {info:#x}"
+        outs[rr] = [bits_of(C) for C in Cs]
+    for a, b in zip(outs[0], outs[1]):
+        assert np.array_equal(a, b)
+    if N > 1:
+        for o, a in zip(ops, outs[0]):
+            assert np.array_equal(bits_of(dak.dak_gemm(o["A"], o["B"], c_fp32=True)), a)
+    rows = np.arange(0, shapes[3][0], 257)
+    ref = og.gemm_ref(lin[3][0][rows], lin[3][1])
+    assert og.rel_err(outs[0][3].view(np.float32)[:, rows], ref) <= FP32_OUT_TOL
+    for p in pls:
+        p.free()
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("N", [128, 256, 512])
 def test_gate_up_full_size_sampled(dak, N):
